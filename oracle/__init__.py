@@ -1,0 +1,172 @@
+"""CPU oracle for the W8A8 FP8 block-scaled linear layer (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports it, and it imports nothing from the product.
+
+The arithmetic lives in ``sgq_oracle.c`` (plain C, fp64 GEMM); this module
+builds it with gcc on first use and wraps it with numpy arrays:
+
+* ``e4m3_encode`` / ``e4m3_decode`` / ``ue8m0_ceil`` -- the bit-level codec.
+* ``quant_token_group`` -- per-token-group quantisation ("Sgl project Sglang
+  GEMM Interface", Quantization Routines: sgl_per_token_group_quant_8bit).
+* ``quant_weight_block`` -- one scale per [blk_n, blk_k] weight tile, stored
+  [n_blocks, k_blocks] (vLLM scaled_mm page, XPUFp8BlockScaledMMKernel).
+* ``gemm`` -- D = mm(As*Aq, (Ws*Wq)^T) in fp64 (vLLM scaled_mm page,
+  AiterInt8ScaledMMLinearKernel.apply_weights docstring) plus the bound
+  sum_k |a_deq||w_deq| used by the error criterion.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+EPS = 1e-10          # reading: the pages name eps without a value
+FP8_MAX = 448.0      # OCP E4M3FN largest finite value
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sgq_oracle.c")
+_LIB = os.path.join(_HERE, "libsgq_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP if available). Returns the .so path."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-std=c11", _SRC,
+            "-o", _LIB + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        ci = ctypes.c_int
+        cf = ctypes.c_float
+        lib.sgqo_e4m3_encode.argtypes = [cf]
+        lib.sgqo_e4m3_encode.restype = ctypes.c_uint8
+        lib.sgqo_e4m3_encode_array.argtypes = [P, i64, P]
+        lib.sgqo_e4m3_encode_array.restype = None
+        lib.sgqo_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.sgqo_e4m3_decode.restype = ctypes.c_double
+        lib.sgqo_ue8m0_ceil.argtypes = [cf]
+        lib.sgqo_ue8m0_ceil.restype = cf
+        lib.sgqo_group_scale.argtypes = [cf, cf, ci]
+        lib.sgqo_group_scale.restype = cf
+        lib.sgqo_quant_token_group.argtypes = [P, i64, i64, ci, ci, cf, P, P]
+        lib.sgqo_quant_token_group.restype = None
+        lib.sgqo_quant_weight_block.argtypes = [P, i64, i64, ci, ci, ci, cf, P, P]
+        lib.sgqo_quant_weight_block.restype = None
+        lib.sgqo_gemm.argtypes = [P, P, P, P, i64, i64, i64, ci, ci, ci, P, P]
+        lib.sgqo_gemm.restype = None
+        lib.sgqo_num_threads.argtypes = []
+        lib.sgqo_num_threads.restype = ci
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().sgqo_num_threads())
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """fp32 values -> E4M3 codes (uint8), elementwise, by the bit-level encoder."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().sgqo_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e4m3_decode(c) -> np.ndarray:
+    """E4M3 codes -> fp64 values."""
+    lib = _load()
+    c = np.asarray(c, dtype=np.uint8)
+    table = np.array([lib.sgqo_e4m3_decode(i) for i in range(256)], dtype=np.float64)
+    return table[c]
+
+
+def ue8m0_ceil(s) -> np.ndarray:
+    lib = _load()
+    s = np.asarray(s, dtype=np.float32)
+    return np.array([lib.sgqo_ue8m0_ceil(float(x)) for x in s.reshape(-1)],
+                    dtype=np.float32).reshape(s.shape)
+
+
+def group_scale(amax: float, ue8m0: bool, eps: float = EPS) -> np.float32:
+    return np.float32(_load().sgqo_group_scale(float(amax), float(eps), int(ue8m0)))
+
+
+def _as_bf16_bits(x) -> np.ndarray:
+    """Accept a torch bf16 tensor or a uint16 array of bf16 bits."""
+    if hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16":
+        import torch
+        return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    a = np.asarray(x)
+    if a.dtype != np.uint16:
+        raise TypeError("expected bf16 bits as uint16 or a torch.bfloat16 tensor")
+    return np.ascontiguousarray(a)
+
+
+def quant_token_group(x, group: int, ue8m0: bool, eps: float = EPS):
+    """x: bf16 [M, K] -> (codes uint8 [M, K], scales fp32 [M, K/group])."""
+    xb = _as_bf16_bits(x)
+    M, K = xb.shape
+    if K % group:
+        raise ValueError("K must be a multiple of group")
+    xq = np.empty((M, K), dtype=np.uint8)
+    xs = np.empty((M, K // group), dtype=np.float32)
+    _load().sgqo_quant_token_group(_ptr(xb), M, K, group, int(ue8m0), eps, _ptr(xq), _ptr(xs))
+    return xq, xs
+
+
+def quant_weight_block(w, blk_n: int, blk_k: int, ue8m0: bool, eps: float = EPS):
+    """w: bf16 [N, K] -> (codes uint8 [N, K], scales fp32 [ceil(N/blk_n), K/blk_k])."""
+    wb = _as_bf16_bits(w)
+    N, K = wb.shape
+    if K % blk_k:
+        raise ValueError("K must be a multiple of blk_k")
+    wq = np.empty((N, K), dtype=np.uint8)
+    ws = np.empty(((N + blk_n - 1) // blk_n, K // blk_k), dtype=np.float32)
+    _load().sgqo_quant_weight_block(_ptr(wb), N, K, blk_n, blk_k, int(ue8m0), eps,
+                                    _ptr(wq), _ptr(ws))
+    return wq, ws
+
+
+def gemm(aq, a_s, wq, ws, blk_n: int, blk_k: int, a_group: int | None = None,
+         with_bound: bool = True):
+    """fp64 D [M, N] (and bound [M, N]) of the block-scaled product."""
+    aq = np.ascontiguousarray(aq, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    a_s = np.ascontiguousarray(a_s, dtype=np.float32)
+    ws = np.ascontiguousarray(ws, dtype=np.float32)
+    M, K = aq.shape
+    N = wq.shape[0]
+    if a_group is None:
+        a_group = K // a_s.shape[1]
+    d = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64) if with_bound else None
+    _load().sgqo_gemm(_ptr(aq), _ptr(a_s), _ptr(wq), _ptr(ws), M, N, K, a_group,
+                      blk_n, blk_k, _ptr(d), _ptr(b) if b is not None else None)
+    return (d, b) if with_bound else d

@@ -1,0 +1,241 @@
+/*
+ * sgq_oracle.c -- plain, slow CPU oracle for the W8A8 FP8 block-scaled linear
+ * layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file.  Only the tests, the smoke check and the CPU-baseline leg
+ * of the benchmark use it.  It shares no code, header, table or constant
+ * generator with the CUDA library; the two are compared against each other.
+ *
+ * What it computes, and where the pages define it:
+ *
+ *  - Per-token-group quantisation: "Sgl project Sglang GEMM Interface",
+ *    Description / Quantization Routines (sgl_per_token_group_quant_8bit:
+ *    group size, epsilon, clipping range, UE8M0 scale format) and its
+ *    Signature section (input, output_q, output_s, group_size, eps, fp8_min,
+ *    fp8_max, scale_ue8m0).  The UE8M0 rounding of activation scales is the
+ *    "UE8M0 activation rounding" of sglang PR #42604 "[SM90] Use native
+ *    block32 DeepGEMM for DeepSeek-V4.1", Modifications.
+ *  - Weight block quantisation into [blk_n, blk_k] tiles with one scale per
+ *    tile, stored [n_blocks, k_blocks]: the same PR, Motivation ([32,32] vs
+ *    [128,128] blocks), and the vLLM "scaled_mm" API page,
+ *    XPUFp8BlockScaledMMKernel.process_weights_after_loading ("[n_blocks,
+ *    k_blocks] (one value per block tile)").
+ *  - The GEMM: the vLLM "scaled_mm" API page,
+ *    AiterInt8ScaledMMLinearKernel.apply_weights docstring: the output is
+ *    mm(scale_a * a, scale_b * b) with numpy-style broadcasting of the scales,
+ *    here with B given as [N, K] (the "_nt" form fp8_gemm_nt((Aq, As), (Wq,
+ *    Ws), D, recipe) of the PR's Modifications).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - E4M3 is the OCP "E4M3FN" format: bias 7, no infinities, 0x7F/0xFF NaN,
+ *    largest finite 448, subnormals k * 2^-9.  fp8_max = 448, fp8_min = -448.
+ *  - eps = 1e-10 (fp32); scale = max(amax, eps) / 448 as a correctly rounded
+ *    fp32 division; UE8M0 rounds that scale up to the next power of two.
+ *  - codes = E4M3 round-to-nearest-even of clamp(x / scale, -448, 448), with
+ *    x / scale a correctly rounded fp32 division; the sign of zero results is
+ *    kept (-0 encodes as 0x80).
+ *  - The GEMM is evaluated in fp64 on the dequantised operands.
+ *
+ * Build: gcc -O2 -fPIC -shared -ffp-contract=off [-fopenmp] (no fast-math:
+ * the quantiser relies on IEEE fp32 division).
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_FP8_MAX 448.0f
+
+static uint32_t orc_bits(float f) { uint32_t u; memcpy(&u, &f, sizeof u); return u; }
+static float orc_float(uint32_t u) { float f; memcpy(&f, &u, sizeof f); return f; }
+
+int sgqo_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits. */
+float sgqo_bf16_to_f32(uint16_t h) { return orc_float((uint32_t)h << 16); }
+
+/*
+ * E4M3 encoder working only on the integer bits of the fp32 input.
+ * Round-to-nearest-even at the E4M3 quantum of the input's binade, saturating
+ * to +-448.  NaN inputs give 0x7F with the input's sign (outside the
+ * contract; the quantiser never produces them from finite inputs).
+ */
+uint8_t sgqo_e4m3_encode(float v) {
+    uint32_t u = orc_bits(v);
+    uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    uint32_t mag = u & 0x7FFFFFFFu;
+    if (mag > 0x7F800000u) return (uint8_t)(sign | 0x7Fu);      /* NaN */
+    if (mag >= orc_bits(ORC_FP8_MAX)) return (uint8_t)(sign | 0x7Eu); /* >= 448, inf */
+    int e_field = (int)(mag >> 23);
+    if (e_field == 0) return sign;   /* fp32 zero/subnormal: far below 2^-10 */
+    /* value = sig * 2^(e - 23), sig in [2^23, 2^24) */
+    uint32_t sig = (mag & 0x7FFFFFu) | 0x800000u;
+    int e = e_field - 127;
+    /* E4M3 quantum: 2^(e-3) in the normal range (e >= -6), else 2^-9. */
+    int q_exp = (e >= -6) ? (e - 3) : -9;
+    int shift = q_exp - (e - 23);      /* >= 20 */
+    uint32_t n;
+    if (shift >= 32) {
+        n = 0;                         /* below half of the smallest subnormal */
+    } else {
+        n = sig >> shift;
+        uint32_t rem = sig & ((1u << shift) - 1u);
+        uint32_t half = 1u << (shift - 1);
+        if (rem > half || (rem == half && (n & 1u))) n += 1u;
+    }
+    /* value = n * 2^q_exp */
+    if (n == 0) return sign;
+    uint32_t code;
+    if (q_exp == -9 && n < 8) {
+        code = n;                                   /* subnormal: n * 2^-9 */
+    } else if (n < 16) {
+        code = ((uint32_t)(q_exp + 10) << 3) | (n - 8u);   /* (8+m) * 2^(E-10) */
+    } else {                                        /* rounded up into next binade */
+        code = ((uint32_t)(q_exp + 11) << 3);
+    }
+    if (code > 0x7Eu) code = 0x7Eu;                 /* saturate (cannot trigger below 448) */
+    return (uint8_t)(sign | code);
+}
+
+void sgqo_e4m3_encode_array(const float* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = sgqo_e4m3_encode(v[i]);
+}
+
+/* E4M3 decoder straight from the bit fields. */
+double sgqo_e4m3_decode(uint8_t c) {
+    int s = (c >> 7) & 1;
+    int E = (c >> 3) & 0xF;
+    int m = c & 7;
+    double v;
+    if (E == 0xF && m == 7) return s ? -NAN : NAN;
+    if (E == 0) v = ldexp((double)m, -9);
+    else v = ldexp((double)(8 + m), E - 10);
+    return s ? -v : v;
+}
+
+/* Smallest power of two >= s, for positive normal s, by bits. */
+float sgqo_ue8m0_ceil(float s) {
+    uint32_t u = orc_bits(s);
+    if (u & 0x7FFFFFu) u = (u & 0xFF800000u) + 0x800000u;
+    return orc_float(u);
+}
+
+/* scale = max(amax, eps) / 448 (fp32, correctly rounded), optionally
+ * rounded up to a power of two. */
+float sgqo_group_scale(float amax, float eps, int ue8m0) {
+    float a = amax > eps ? amax : eps;
+    volatile float s = a / ORC_FP8_MAX;   /* volatile: keep it one fp32 division */
+    float r = s;
+    if (ue8m0) r = sgqo_ue8m0_ceil(r);
+    return r;
+}
+
+/* One element: E4M3(clamp(x / s, -448, 448)). */
+static uint8_t orc_quant_one(float x, float s) {
+    volatile float q = x / s;
+    float t = q;
+    if (t > ORC_FP8_MAX) t = ORC_FP8_MAX;
+    if (t < -ORC_FP8_MAX) t = -ORC_FP8_MAX;
+    return sgqo_e4m3_encode(t);
+}
+
+/*
+ * Per-token-group quantisation.  x: bf16 bits [M, K] row-major.
+ * xq: E4M3 codes [M, K]; xs: fp32 [M, K / group] row-major.
+ */
+void sgqo_quant_token_group(const uint16_t* x, int64_t M, int64_t K, int group,
+                            int ue8m0, float eps, uint8_t* xq, float* xs) {
+    int64_t G = K / group;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t j = 0; j < G; ++j) {
+            const uint16_t* xr = x + m * K + j * group;
+            float amax = 0.0f;
+            for (int i = 0; i < group; ++i) {
+                float a = fabsf(sgqo_bf16_to_f32(xr[i]));
+                if (a > amax) amax = a;
+            }
+            float s = sgqo_group_scale(amax, eps, ue8m0);
+            xs[m * G + j] = s;
+            for (int i = 0; i < group; ++i)
+                xq[m * K + j * group + i] = orc_quant_one(sgqo_bf16_to_f32(xr[i]), s);
+        }
+    }
+}
+
+/*
+ * Weight block quantisation.  w: bf16 bits [N, K].  One scale per
+ * [blk_n, blk_k] tile; the last N-tile may be ragged and uses the rows that
+ * exist.  wq: E4M3 codes [N, K]; ws: fp32 [ceil(N / blk_n), K / blk_k].
+ */
+void sgqo_quant_weight_block(const uint16_t* w, int64_t N, int64_t K, int blk_n,
+                             int blk_k, int ue8m0, float eps, uint8_t* wq, float* ws) {
+    int64_t NB = (N + blk_n - 1) / blk_n, KB = K / blk_k;
+    for (int64_t nb = 0; nb < NB; ++nb) {
+        int64_t n0 = nb * blk_n, n1 = n0 + blk_n < N ? n0 + blk_n : N;
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            int64_t k0 = kb * blk_k;
+            float amax = 0.0f;
+            for (int64_t n = n0; n < n1; ++n)
+                for (int64_t k = k0; k < k0 + blk_k; ++k) {
+                    float a = fabsf(sgqo_bf16_to_f32(w[n * K + k]));
+                    if (a > amax) amax = a;
+                }
+            float s = sgqo_group_scale(amax, eps, ue8m0);
+            ws[nb * KB + kb] = s;
+            for (int64_t n = n0; n < n1; ++n)
+                for (int64_t k = k0; k < k0 + blk_k; ++k)
+                    wq[n * K + k] = orc_quant_one(sgqo_bf16_to_f32(w[n * K + k]), s);
+        }
+    }
+}
+
+/*
+ * D[m, n] = sum_k (dec(Aq[m,k]) * As[m, k / a_group]) * (dec(Wq[n,k]) * Ws[n / blk_n, k / blk_k])
+ * in fp64, and bound[m, n] = sum_k |a_deq| * |w_deq| (for the error bound).
+ * Aq: [M, K]; As: [M, K / a_group]; Wq: [N, K]; Ws: [ceil(N/blk_n), K/blk_k].
+ * Outputs are [M, N] row-major fp64.  bound may be NULL.
+ */
+void sgqo_gemm(const uint8_t* aq, const float* as, const uint8_t* wq, const float* ws,
+               int64_t M, int64_t N, int64_t K, int a_group, int blk_n, int blk_k,
+               double* d, double* bound) {
+    int64_t AG = K / a_group, KB = K / blk_k;
+    double* adeq = (double*)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            adeq[m * K + k] = sgqo_e4m3_decode(aq[m * K + k]) * (double)as[m * AG + k / a_group];
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        double* wrow = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+        for (int64_t n = 0; n < N; ++n) {
+            for (int64_t k = 0; k < K; ++k)
+                wrow[k] = sgqo_e4m3_decode(wq[n * K + k]) * (double)ws[(n / blk_n) * KB + k / blk_k];
+            for (int64_t m = 0; m < M; ++m) {
+                const double* ar = adeq + m * K;
+                double acc = 0.0, b = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    acc += ar[k] * wrow[k];
+                    b += fabs(ar[k]) * fabs(wrow[k]);
+                }
+                d[m * N + n] = acc;
+                if (bound) bound[m * N + n] = b;
+            }
+        }
+        free(wrow);
+    }
+    free(adeq);
+}
