@@ -1,0 +1,408 @@
+"""Benchmark of the W8A8 FP8 block-scaled linear layer on GB300.
+
+One step = one pass of the whole hot path (per-token-group quantisation of
+the activations, then the block-scaled GEMM) over one batch of the workload.
+Default workload: "decode_block32" -- M in {1, 4, 16, 64} tokens against one
+N=7168, K=2048 weight with [32,32] UE8M0 blocks and UE8M0 activation groups of
+32, i.e. four quantise+GEMM pairs per step.  The metric is the GEMM family's
+algorithmic bytes per second (Aq + As + Wq + Ws + D per GEMM, plus the quant
+bytes x + codes + scales), with TFLOP/s alongside.
+
+Timing: inputs resident in HBM; CUDA graphs of whole steps replayed on one
+stream between CUDA events; the weights rotate over enough copies to exceed
+twice the L2 size, so every step streams its weights from HBM.  `e2e` times
+the same steps through the public API with the activation copied in from
+pinned host memory and D read back to the host inside the timed region.
+
+`--impl reference` times the CPU oracle (test infrastructure) on a bounded
+sample of the same workload, on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from fp8_block_scaled_sgq_gb300 import synth  # noqa: E402
+
+METRIC = "block-scaled FP8 GEMM TFLOPS & GB/s vs GB300 roofline, M=1–8192; quant GB/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, path: str | None):
+        self.index, self.path, self.proc = index, path, None
+
+    def __enter__(self):
+        try:
+            out = open(self.path, "w") if self.path else subprocess.PIPE
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=out, stderr=subprocess.DEVNULL, text=True)
+            self._out = out
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            o, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            o, _ = self.proc.communicate()
+        if self.path:
+            self._out.close()
+            self.text = open(self.path).read()
+        else:
+            self.text = o or ""
+        return False
+
+    def summary(self):
+        rows = []
+        for line in self.text.strip().splitlines():
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, _, flags in rows:
+            for n, v in zip(names, flags):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- our arm
+
+def build_problem(cases, device, n_rot):
+    import fp8_block_scaled_sgq_gb300 as sgq
+    c0 = cases[0]
+    w = c0.w().to(device)
+    wq, ws = sgq.quant_weight_block(w, c0.blk_n, c0.blk_k, c0.ue8m0)
+    del w
+    wrot = [(wq, ws)] + [(wq.clone(), ws.clone()) for _ in range(n_rot - 1)]
+    per = []
+    for c in cases:
+        x = c.x().to(device)
+        xq = torch.empty((c.M, c.K), dtype=torch.uint8, device=device)
+        xs = torch.empty((c.M, c.K // c.group), dtype=torch.float32, device=device)
+        d = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
+        per.append((c, x, xq, xs, d))
+    return wrot, per
+
+
+def step_fn(sgq, per, wq, ws, stream, gemm_only=False):
+    for c, x, xq, xs, d in per:
+        if not gemm_only:
+            sgq.sgq_quant_token_group(x, c.M, c.K, c.group, c.ue8m0, xq, xs, stream)
+        sgq.sgq_fp8_block_gemm(xq, xs, wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, stream)
+
+
+def run_ours(args, ws_, rank, local):
+    import fp8_block_scaled_sgq_gb300 as sgq
+    from fp8_block_scaled_sgq_gb300 import build as sgq_build
+    if not os.path.exists(sgq_build.LIB):
+        raise SystemExit("libsgq.so is not built; run __graft_entry__.build() first")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init(ws_, "nccl")
+    cases = synth.WORKLOADS[args.workload]
+    if len({(c.N, c.K, c.blk_n, c.blk_k) for c in cases}) != 1:
+        raise SystemExit("workload mixes weight shapes")
+    c0 = cases[0]
+    wbytes = c0.N * c0.K + 4 * math.ceil(c0.N / c0.blk_n) * (c0.K // c0.blk_k)
+    n_rot = max(2, math.ceil(2 * L2_BYTES / wbytes) + 1)
+    wrot, per = build_problem(cases, device, n_rot)
+    stream = torch.cuda.Stream(device)
+    sptr = stream.cuda_stream
+
+    gemm_bytes = sum(c.gemm_bytes() for c in cases)
+    quant_bytes = sum(c.quant_bytes() for c in cases)
+    step_bytes = gemm_bytes + quant_bytes
+    step_flops = sum(c.flops() for c in cases)
+
+    # warm-up outside capture (first split-K call allocates the workspace)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step_fn(sgq, per, *wrot[i % n_rot], sptr)
+    stream.synchronize()
+    if sgq.sgq_device_status(sptr) != 0:
+        raise SystemExit("device status not OK after warm-up")
+
+    def capture(gemm_only):
+        graphs = []
+        for r in range(n_rot):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    step_fn(sgq, per, *wrot[r], torch.cuda.current_stream().cuda_stream, gemm_only)
+            graphs.append(g)
+        return graphs
+
+    graphs = capture(False)
+    ggraphs = capture(True)
+
+    def timed(gl, steps):
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                gl[i % n_rot].replay()
+        stream.synchronize()
+        barrier(ws_)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(steps):
+                gl[i % n_rot].replay()
+            e1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        barrier(ws_)
+        return e0.elapsed_time(e1) / steps   # ms per step
+
+    launches0 = sgq.sgq_launch_count()
+    with ClockSampler(local, os.path.join(args.out_dir, f"clocks_rank{rank}.csv") if args.out_dir else None) as cs:
+        ms_step = timed(graphs, args.steps)
+        ms_gemm = timed(ggraphs, args.steps)
+    clocks = cs.summary()
+    ms_step = max_over_ranks(ms_step, ws_, device)
+    ms_gemm = max_over_ranks(ms_gemm, ws_, device)
+    gpu_launches = 2 * len(cases) * args.steps   # quant + GEMM per case per step (graph replays)
+    assert sgq.sgq_launch_count() == launches0   # replays do not call the library
+
+    # end to end through the public API: H2D of x, quant + GEMM, D2H of D, every step
+    hx = [x.cpu().pin_memory() for _, x, _, _, _ in per]
+    hd = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for *_, d in per]
+    for i in range(args.warmup):
+        _e2e_step(sgq, per, wrot[i % n_rot], hx, hd, stream)
+    barrier(ws_)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _e2e_step(sgq, per, wrot[i % n_rot], hx, hd, stream)
+    t_e2e = (time.perf_counter() - t0) / args.steps
+    t_e2e = max_over_ranks(t_e2e, ws_, device)
+    if sgq.sgq_device_status(sptr) != 0:
+        raise SystemExit("device status not OK after timing")
+    h2d = sum(c.M * c.K * 2 for c in cases)
+    d2h = sum(c.M * c.N * 2 for c in cases)
+
+    pk = peaks()
+    gemm_gbs = gemm_bytes / (ms_gemm * 1e-3) / 1e9
+    value = ws_ * step_bytes / (ms_step * 1e-3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws_,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8e4m3 x fp8e4m3 -> fp32 accumulate -> bf16",
+        "data": "synthetic (seeded; x ~ N(0,1), W ~ N(0,0.02) bf16, quantised on the GPU)",
+        "config": {"workload": args.workload, "M": [c.M for c in cases], "N": c0.N, "K": c0.K,
+                   "recipe": [1, c0.blk_n, c0.blk_k], "ue8m0": c0.ue8m0,
+                   "l2": f"weights rotate over {n_rot} copies ({n_rot * wbytes / 2**20:.0f} MiB > 2x L2)",
+                   "parallelism": f"replicas x{ws_}"},
+        "tflops": round(ws_ * step_flops / (ms_step * 1e-3) / 1e12, 3),
+        "gemm": {"ms_per_step": round(ms_gemm, 5), "gbs": round(gemm_gbs, 1),
+                 "tflops": round(step_flops / (ms_gemm * 1e-3) / 1e12, 3),
+                 "us_per_launch": round(ms_gemm * 1e3 / len(cases), 3)},
+        "roofline": {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gemm_gbs / pk["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "fp8_block_gemm_kernel (swap-AB, split-K)", "peak_source": pk["source"]},
+        "e2e": {"value": round(ws_ * step_bytes / t_e2e / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(t_e2e * 1e3, 4)},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+    return result
+
+
+def _e2e_step(sgq, per, wrot_r, hx, hd, stream):
+    wq, ws = wrot_r
+    with torch.cuda.stream(stream):
+        for (c, x, xq, xs, d), h_x, h_d in zip(per, hx, hd):
+            x.copy_(h_x, non_blocking=True)
+            sgq.sgq_quant_token_group(x, c.M, c.K, c.group, c.ue8m0, xq, xs, stream.cuda_stream)
+            sgq.sgq_fp8_block_gemm(xq, xs, wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, stream.cuda_stream)
+            h_d.copy_(d, non_blocking=True)
+    stream.synchronize()
+
+
+# ----------------------------------------------------------------- oracle timing
+
+def oracle_step(cases, data, rows_frac):
+    """One pass of the oracle over a sample: quantise x and evaluate the GEMM on
+    the first ceil(rows_frac * M) rows of each case."""
+    import oracle
+    done = 0.0
+    for c, x, wq, ws in data:
+        m = max(1, math.ceil(rows_frac * c.M))
+        xs_ = x[:m]
+        aq, a_s = oracle.quant_token_group(xs_, c.group, c.ue8m0)
+        oracle.gemm(aq, a_s, wq, ws, c.blk_n, c.blk_k, with_bound=False)
+        cc = synth.Case(c.name, m, c.N, c.K, c.blk_n, c.blk_k, c.ue8m0)
+        done += cc.gemm_bytes() + cc.quant_bytes()
+    return done
+
+
+def oracle_data(cases):
+    import oracle
+    c0 = cases[0]
+    wq, ws = oracle.quant_weight_block(c0.w(), c0.blk_n, c0.blk_k, c0.ue8m0)
+    return [(c, c.x(), wq, ws) for c in cases]
+
+
+def cpu_baseline(cases, budget_s=12.0):
+    import oracle
+    data = oracle_data(cases)
+    t0 = time.perf_counter()
+    b = oracle_step(cases, data, 1.0)
+    dt = time.perf_counter() - t0
+    reps = 1
+    while time.perf_counter() - t0 < budget_s and reps < 20:
+        b += oracle_step(cases, data, 1.0)
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} full step(s) of the workload (quantise + fp64 GEMM, all rows), "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, ws_, rank):
+    import oracle
+    if ws_ > 1:
+        dist_init(ws_, "gloo")
+        barrier(ws_)
+        if rank != 0:
+            return None
+    cases = synth.WORKLOADS[args.workload]
+    data = oracle_data(cases)
+    t0 = time.perf_counter()
+    oracle_step(cases, data, 1.0)
+    full = time.perf_counter() - t0
+    # bound each step to ~2 s of CPU work
+    frac = min(1.0, 2.0 / max(full, 1e-9))
+    for _ in range(args.warmup):
+        oracle_step(cases, data, frac)
+    t0 = time.perf_counter()
+    b = 0.0
+    for _ in range(args.steps):
+        b += oracle_step(cases, data, frac)
+    dt = time.perf_counter() - t0
+    v = b / dt / 1e9
+    sample = f"first {frac:.3g} of the rows of each GEMM of the workload per step"
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": ws_,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, same recipe)",
+            "config": {"workload": args.workload, "M": [c.M for c in cases], "N": cases[0].N, "K": cases[0].K,
+                       "recipe": [1, cases[0].blk_n, cases[0].blk_k], "ue8m0": cases[0].ue8m0},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_block32", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out-dir", default=None, help="directory for clock samples")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    ws_, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, ws_, rank)
+        if res is not None and rank == 0:
+            print(json.dumps(res))
+        return
+    res = run_ours(args, ws_, rank, local)
+    if rank == 0:
+        if ws_ == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(synth.WORKLOADS[args.workload])
+        print(json.dumps(res))
+    if ws_ > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

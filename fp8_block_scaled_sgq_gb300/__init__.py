@@ -1,0 +1,50 @@
+"""GB300 (sm_103a) W8A8 FP8 block-scaled linear layer.
+
+The compute lives in ``libsgq.so`` (hand-written CUDA behind the C ABI of
+``include/sgq.h``).  This package holds the ctypes binding (``binding``), the
+nvcc build (``build``), seeded synthetic inputs (``synth``) and a few
+torch-facing helpers below that only allocate outputs and call the binding.
+"""
+from __future__ import annotations
+
+from .binding import (  # noqa: F401
+    EXPORTS, SGQ_GEMM_DEFAULT, SGQ_GEMM_FORCE_PROMOTE, SgqError, load_library, sgq_device_status,
+    sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_launch_count, sgq_quant_token_group,
+    sgq_quant_weight_block, sgq_version, status_string)
+
+
+def quant_token_group(x, group: int, ue8m0: bool, stream=None):
+    """bf16 [M, K] CUDA tensor -> (uint8 E4M3 codes [M, K], fp32 scales [M, K/group])."""
+    import torch
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    xs = torch.empty((M, K // group), dtype=torch.float32, device=x.device)
+    sgq_quant_token_group(x, M, K, group, ue8m0, xq, xs, stream)
+    return xq, xs
+
+
+def quant_weight_block(w, blk_n: int, blk_k: int, ue8m0: bool, stream=None):
+    """bf16 [N, K] CUDA tensor -> (uint8 E4M3 [N, K], fp32 [ceil(N/blk_n), K/blk_k])."""
+    import torch
+    N, K = w.shape
+    wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    ws = torch.empty(((N + blk_n - 1) // blk_n, K // blk_k), dtype=torch.float32, device=w.device)
+    sgq_quant_weight_block(w, N, K, blk_n, blk_k, ue8m0, wq, ws, stream)
+    return wq, ws
+
+
+def fp8_block_gemm(aq, a_s, wq, ws, blk_n: int, blk_k: int, out=None, flags: int = 0, stream=None):
+    """D = (Aq*As)(Wq*Ws)^T as a bf16 [M, N] CUDA tensor."""
+    import torch
+    M, K = aq.shape
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    sgq_fp8_block_gemm_ex(aq, a_s, wq, ws, out, M, N, K, blk_n, blk_k, flags, stream)
+    return out
+
+
+def w8a8_linear(x, wq, ws, blk_n: int, blk_k: int, ue8m0: bool, out=None, stream=None):
+    """Quantise x per token group of blk_k, then the block-scaled GEMM."""
+    xq, xs = quant_token_group(x, blk_k, ue8m0, stream)
+    return fp8_block_gemm(xq, xs, wq, ws, blk_n, blk_k, out=out, stream=stream)

@@ -1,0 +1,141 @@
+"""ctypes binding of ``libsgq.so`` -- argument marshalling only.
+
+Each function has the name and argument order of the C call in
+``include/sgq.h``.  Tensor arguments may be torch CUDA tensors (their
+``data_ptr()`` is passed) or raw integer device addresses; ``stream`` may be a
+``torch.cuda.Stream``, a raw ``cudaStream_t`` integer, or None for the current
+torch stream.  A non-OK status raises :class:`SgqError`.  There is no
+fallback: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsgq.so")
+
+SGQ_OK = 0
+SGQ_ERR_INVALID_ARG = 1
+SGQ_ERR_UNSUPPORTED = 2
+SGQ_ERR_MISALIGNED = 3
+SGQ_ERR_CUDA = 4
+SGQ_ERR_TIMEOUT = 5
+
+SGQ_GEMM_DEFAULT = 0
+SGQ_GEMM_FORCE_PROMOTE = 1
+
+# Symbols declared in include/sgq.h (checked by the tests).
+EXPORTS = (
+    "sgq_quant_token_group",
+    "sgq_quant_weight_block",
+    "sgq_fp8_block_gemm",
+    "sgq_fp8_block_gemm_ex",
+    "sgq_status_string",
+    "sgq_device_status",
+    "sgq_launch_count",
+    "sgq_version",
+)
+
+
+class SgqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libsgq.so (built by ``fp8_block_scaled_sgq_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA extension not built: {path} is missing "
+                               "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        lib = ctypes.CDLL(path)
+        P, i64, ci, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+        lib.sgq_quant_token_group.argtypes = [P, i64, i64, ci, ci, P, P, P]
+        lib.sgq_quant_weight_block.argtypes = [P, i64, i64, ci, ci, ci, P, P, P]
+        lib.sgq_fp8_block_gemm.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, P]
+        lib.sgq_fp8_block_gemm_ex.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, u32, P]
+        for f in ("sgq_quant_token_group", "sgq_quant_weight_block", "sgq_fp8_block_gemm",
+                  "sgq_fp8_block_gemm_ex"):
+            getattr(lib, f).restype = ci
+        lib.sgq_status_string.argtypes = [ci]
+        lib.sgq_status_string.restype = ctypes.c_char_p
+        lib.sgq_device_status.argtypes = [P]
+        lib.sgq_device_status.restype = ci
+        lib.sgq_launch_count.argtypes = []
+        lib.sgq_launch_count.restype = ctypes.c_uint64
+        lib.sgq_version.argtypes = []
+        lib.sgq_version.restype = ci
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    raise TypeError(f"expected a tensor or an int address, got {type(t)!r}")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != SGQ_OK:
+        raise SgqError(rc, what)
+
+
+def status_string(status: int) -> str:
+    return load_library().sgq_status_string(status).decode()
+
+
+def sgq_quant_token_group(x, M, K, group, ue8m0, xq, xs, stream=None):
+    _check(load_library().sgq_quant_token_group(_ptr(x), M, K, group, int(ue8m0), _ptr(xq), _ptr(xs),
+                                                _stream(stream)), "sgq_quant_token_group")
+
+
+def sgq_quant_weight_block(w, N, K, blk_n, blk_k, ue8m0, wq, ws, stream=None):
+    _check(load_library().sgq_quant_weight_block(_ptr(w), N, K, blk_n, blk_k, int(ue8m0), _ptr(wq),
+                                                 _ptr(ws), _stream(stream)), "sgq_quant_weight_block")
+
+
+def sgq_fp8_block_gemm(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, stream=None):
+    _check(load_library().sgq_fp8_block_gemm(_ptr(Aq), _ptr(As), _ptr(Wq), _ptr(Ws), _ptr(D), M, N, K,
+                                             blk_n, blk_k, _stream(stream)), "sgq_fp8_block_gemm")
+
+
+def sgq_fp8_block_gemm_ex(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags, stream=None):
+    _check(load_library().sgq_fp8_block_gemm_ex(_ptr(Aq), _ptr(As), _ptr(Wq), _ptr(Ws), _ptr(D), M, N,
+                                                K, blk_n, blk_k, flags, _stream(stream)),
+           "sgq_fp8_block_gemm_ex")
+
+
+def sgq_device_status(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device status code."""
+    return int(load_library().sgq_device_status(_stream(stream)))
+
+
+def sgq_launch_count() -> int:
+    return int(load_library().sgq_launch_count())
+
+
+def sgq_version() -> int:
+    return int(load_library().sgq_version())

@@ -1,0 +1,118 @@
+// C-ABI entry points: argument validation, then the kernel launchers.
+// Every check happens on the host before anything is enqueued; nothing
+// aborts or falls back.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "sgq_internal.h"
+
+namespace sgq {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+DeviceInfo g_dev[64];
+bool g_dev_ok[64] = {};
+std::mutex g_dev_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+void note_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+sgq_status device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ok[dev]) {
+        DeviceInfo d;
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return SGQ_ERR_CUDA;
+        g_dev[dev] = d;
+        g_dev_ok[dev] = true;
+    }
+    *out = g_dev[dev];
+    return SGQ_OK;
+}
+
+}  // namespace sgq
+
+using sgq::aligned16;
+
+extern "C" {
+
+sgq_status sgq_quant_token_group(const void* x, int64_t M, int64_t K, int group, int ue8m0, void* xq,
+                                 float* xs, sgq_stream_t stream) {
+    if (M < 0 || K <= 0 || (group != 32 && group != 128) || K % group != 0 || (ue8m0 != 0 && ue8m0 != 1))
+        return SGQ_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) / 1 || M * K > (int64_t(1) << 40)) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!x || !xq || !xs) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(xs)) return SGQ_ERR_MISALIGNED;
+    return sgq::launch_quant_token_group(x, M, K, group, ue8m0, xq, xs,
+                                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgq_status sgq_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n, int blk_k, int ue8m0,
+                                  void* wq, float* ws, sgq_stream_t stream) {
+    if (N < 0 || K <= 0 || (blk_n != 32 && blk_n != 128) || (blk_k != 32 && blk_k != 128) ||
+        K % blk_k != 0 || (ue8m0 != 0 && ue8m0 != 1))
+        return SGQ_ERR_INVALID_ARG;
+    if ((N + blk_n - 1) / blk_n > 65535 || K / blk_k > (int64_t(1) << 31) - 1) return SGQ_ERR_INVALID_ARG;
+    if (N == 0) return SGQ_OK;
+    if (!w || !wq || !ws) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(wq) || !aligned16(ws)) return SGQ_ERR_MISALIGNED;
+    return sgq::launch_quant_weight_block(w, N, K, blk_n, blk_k, ue8m0, wq, ws,
+                                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgq_status sgq_fp8_block_gemm_ex(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D,
+                                 int64_t M, int64_t N, int64_t K, int blk_n, int blk_k, uint32_t flags,
+                                 sgq_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || (blk_n != 32 && blk_n != 128) || (blk_k != 32 && blk_k != 128) ||
+        K % blk_k != 0 || N % 8 != 0 || (flags & ~uint32_t(SGQ_GEMM_FORCE_PROMOTE)) != 0)
+        return SGQ_ERR_INVALID_ARG;
+    // int32 indexing inside the kernel
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!Aq || !As || !Wq || !Ws || !D) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(Aq) || !aligned16(As) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(D))
+        return SGQ_ERR_MISALIGNED;
+    return sgq::launch_fp8_block_gemm(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags,
+                                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgq_status sgq_fp8_block_gemm(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D,
+                              int64_t M, int64_t N, int64_t K, int blk_n, int blk_k, sgq_stream_t stream) {
+    return sgq_fp8_block_gemm_ex(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, stream);
+}
+
+const char* sgq_status_string(sgq_status s) {
+    switch (s) {
+        case SGQ_OK: return "SGQ_OK";
+        case SGQ_ERR_INVALID_ARG: return "SGQ_ERR_INVALID_ARG";
+        case SGQ_ERR_UNSUPPORTED: return "SGQ_ERR_UNSUPPORTED";
+        case SGQ_ERR_MISALIGNED: return "SGQ_ERR_MISALIGNED";
+        case SGQ_ERR_CUDA: return "SGQ_ERR_CUDA";
+        case SGQ_ERR_TIMEOUT: return "SGQ_ERR_TIMEOUT";
+    }
+    return "SGQ_ERR_UNKNOWN";
+}
+
+sgq_status sgq_device_status(sgq_stream_t stream) {
+    return sgq::read_and_clear_device_status(reinterpret_cast<cudaStream_t>(stream));
+}
+
+uint64_t sgq_launch_count(void) { return sgq::g_launches.load(std::memory_order_relaxed); }
+
+int sgq_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+// Per-token-group activation quantisation and per-block weight quantisation,
+// bf16 -> FP8 E4M3 codes + fp32 scales, for sm_103a.
+//
+// The rule ("Sgl project Sglang GEMM Interface", Quantization Routines:
+// sgl_per_token_group_quant_8bit with group size, eps, fp8_min/fp8_max and
+// the UE8M0 scale format; UE8M0 activation rounding from sglang PR #42604,
+// Modifications) for each group:
+//   s = max(amax, eps) / 448   (IEEE fp32 division), optionally rounded up to
+//   a power of two; code = E4M3 RNE of clamp(x / s, -448, 448).
+// The conversion instruction saturates to +-448, which is the clamp.
+//
+// Memory path: 16-byte bf16 loads (8 elements per thread), a warp-shuffle
+// amax over the lanes of one group, packed 8-byte code stores and one
+// coalesced fp32 scale store per group.  The kernel is HBM-bound.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "sgq_internal.h"
+
+namespace sgq {
+namespace {
+
+constexpr float kFp8Max = 448.0f;
+constexpr float kEps = 1e-10f;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// s = max(amax, eps) / 448, optionally rounded up to a power of two (by bits).
+template <bool kUe8m0>
+__device__ __forceinline__ float group_scale(float amax) {
+    float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
+    if (kUe8m0) {
+        uint32_t u = __float_as_uint(s);
+        if (u & 0x7FFFFFu) u = (u & 0xFF800000u) + 0x800000u;
+        s = __uint_as_float(u);
+    }
+    return s;
+}
+
+// x / s for all 8 values, then E4M3 with saturation, packed little-endian.
+template <bool kUe8m0>
+__device__ __forceinline__ uint2 quantize8(const float (&v)[8], float s) {
+    float q[8];
+    if (kUe8m0) {
+        // s = 2^e exactly, so 1/s = 2^-e is exact and x * (1/s) is the
+        // correctly rounded x / s.
+        const float r = __uint_as_float((254u - (__float_as_uint(s) >> 23)) << 23);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(v[i], r);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(v[i], s);
+    }
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_fp8x2_storage_t c =
+            __nv_cvt_float2_to_fp8x2(make_float2(q[2 * i], q[2 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+        p[i] = static_cast<uint32_t>(c);
+    }
+    return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+__device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+    v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+    v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+
+// One thread per 8 consecutive elements; kTpg = group/8 consecutive lanes own
+// one group.  Loop trip counts are warp-uniform so the shuffles see full warps.
+template <int kGroup, bool kUe8m0>
+__global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __restrict__ x,
+                                                                uint2* __restrict__ xq,
+                                                                float* __restrict__ xs,
+                                                                int64_t nvec) {
+    // Let a programmatically-dependent GEMM start its weight prefetch now; it
+    // still waits for this grid to finish before it reads xq / xs.
+    ptx::launch_dependents();
+    constexpr int kTpg = kGroup / 8;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t base = warp * 32; base < nvec; base += nwarps * 32) {
+        const int64_t v = base + lane;
+        const bool active = v < nvec;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (active) w = __ldg(x + v);
+        float f[8];
+        unpack8(w, f);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+        for (int off = kTpg / 2; off > 0; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        const float s = group_scale<kUe8m0>(amax);
+        if (active) {
+            xq[v] = quantize8<kUe8m0>(f, s);
+            if ((lane % kTpg) == 0) xs[v / kTpg] = s;
+        }
+    }
+}
+
+// One CTA per [blk_n, blk_k] weight tile: block-wide amax, then quantise.
+template <int kBlkN, int kBlkK, bool kUe8m0>
+__global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint16_t* __restrict__ w,
+                                                                 uint8_t* __restrict__ wq,
+                                                                 float* __restrict__ ws, int64_t N,
+                                                                 int64_t K) {
+    constexpr int kVecPerRow = kBlkK / 8;
+    constexpr int kVecs = kBlkN * kVecPerRow;
+    constexpr int kPer = (kVecs + 255) / 256;
+    __shared__ float red[8];
+    const int64_t nb = blockIdx.y, kb = blockIdx.x;
+    const int64_t KB = K / kBlkK;
+    uint4 data[kPer];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int idx = threadIdx.x + i * 256;
+        const int r = idx / kVecPerRow, c = idx % kVecPerRow;
+        const int64_t n = nb * kBlkN + r;
+        data[i] = make_uint4(0, 0, 0, 0);
+        if (idx < kVecs && n < N)
+            data[i] = __ldg(reinterpret_cast<const uint4*>(w + n * K + kb * kBlkK) + c);
+        float f[8];
+        unpack8(data[i], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    const float s = group_scale<kUe8m0>(amax);
+    if (threadIdx.x == 0) ws[nb * KB + kb] = s;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int idx = threadIdx.x + i * 256;
+        const int r = idx / kVecPerRow, c = idx % kVecPerRow;
+        const int64_t n = nb * kBlkN + r;
+        if (idx < kVecs && n < N) {
+            float f[8];
+            unpack8(data[i], f);
+            reinterpret_cast<uint2*>(wq + n * K + kb * kBlkK)[c] = quantize8<kUe8m0>(f, s);
+        }
+    }
+}
+
+template <int G, bool U>
+sgq_status launch_tg(const void* x, int64_t M, int64_t K, void* xq, float* xs, cudaStream_t st) {
+    const int64_t nvec = M * K / 8;
+    DeviceInfo di;
+    sgq_status rc = device_info(&di);
+    if (rc != SGQ_OK) return rc;
+    const int64_t warps_needed = (nvec + 31) / 32;
+    int64_t blocks = (warps_needed + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(di.sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    quant_token_group_kernel<G, U><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const uint4*>(x), static_cast<uint2*>(xq), xs, nvec);
+    if (cudaGetLastError() != cudaSuccess) return SGQ_ERR_CUDA;
+    note_launch();
+    return SGQ_OK;
+}
+
+template <int BN, int BK, bool U>
+sgq_status launch_wb(const void* w, int64_t N, int64_t K, void* wq, float* ws, cudaStream_t st) {
+    dim3 grid(static_cast<unsigned>(K / BK), static_cast<unsigned>((N + BN - 1) / BN));
+    quant_weight_block_kernel<BN, BK, U><<<grid, 256, 0, st>>>(
+        static_cast<const uint16_t*>(w), static_cast<uint8_t*>(wq), ws, N, K);
+    if (cudaGetLastError() != cudaSuccess) return SGQ_ERR_CUDA;
+    note_launch();
+    return SGQ_OK;
+}
+
+}  // namespace
+
+sgq_status launch_quant_token_group(const void* x, int64_t M, int64_t K, int group, int ue8m0,
+                                    void* xq, float* xs, cudaStream_t st) {
+    if (group == 32) return ue8m0 ? launch_tg<32, true>(x, M, K, xq, xs, st)
+                                  : launch_tg<32, false>(x, M, K, xq, xs, st);
+    return ue8m0 ? launch_tg<128, true>(x, M, K, xq, xs, st)
+                 : launch_tg<128, false>(x, M, K, xq, xs, st);
+}
+
+sgq_status launch_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n, int blk_k,
+                                     int ue8m0, void* wq, float* ws, cudaStream_t st) {
+#define SGQ_WB(bn, bk)                                                               \
+    if (blk_n == bn && blk_k == bk)                                                  \
+        return ue8m0 ? launch_wb<bn, bk, true>(w, N, K, wq, ws, st)                  \
+                     : launch_wb<bn, bk, false>(w, N, K, wq, ws, st);
+    SGQ_WB(32, 32)
+    SGQ_WB(32, 128)
+    SGQ_WB(128, 32)
+    SGQ_WB(128, 128)
+#undef SGQ_WB
+    return SGQ_ERR_INVALID_ARG;
+}
+
+}  // namespace sgq

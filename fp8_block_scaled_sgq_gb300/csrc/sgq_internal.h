@@ -1,0 +1,31 @@
+// Internal host-side interface between the C-ABI layer and the kernel files.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include "../../include/sgq.h"
+
+namespace sgq {
+
+// Per-device facts, queried once.
+struct DeviceInfo {
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+sgq_status device_info(DeviceInfo* out);
+
+// Count of kernel launches made by the library (for benchmarks).
+void note_launch(int n = 1);
+
+sgq_status launch_quant_token_group(const void* x, int64_t M, int64_t K, int group,
+                                    int ue8m0, void* xq, float* xs, cudaStream_t stream);
+sgq_status launch_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n,
+                                     int blk_k, int ue8m0, void* wq, float* ws,
+                                     cudaStream_t stream);
+sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq,
+                                 const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
+                                 int blk_n, int blk_k, uint32_t flags, cudaStream_t stream);
+// Reads and clears the device status word of the current device (after a sync).
+sgq_status read_and_clear_device_status(cudaStream_t stream);
+
+}  // namespace sgq

@@ -1,0 +1,157 @@
+/*
+ * sgq.h -- C ABI of the GB300 (sm_103a) W8A8 FP8 block-scaled linear layer.
+ *
+ * The layer has two steps, each one call:
+ *
+ *   1. sgq_quant_token_group: per-token-group activation quantisation,
+ *      bf16 -> FP8 E4M3 codes plus one fp32 scale per group.
+ *   2. sgq_fp8_block_gemm:   D = (Aq * As)(Wq * Ws)^T, fp32 accumulation,
+ *      bf16 output, for the [1,128]/[128,128] and [1,32]/[32,32] recipes.
+ *
+ * plus sgq_quant_weight_block, the offline weight quantiser that produces the
+ * block-scaled weights the GEMM consumes.
+ *
+ * Conventions shared by every call:
+ *  - Every tensor argument is a DEVICE pointer to contiguous row-major data,
+ *    owned by the caller (the library never frees or keeps it).  Pointers must
+ *    be 16-byte aligned, else SGQ_ERR_MISALIGNED.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  The host call returns once the kernels are enqueued;
+ *    errors found on the device are reported later by sgq_device_status.
+ *  - Nothing aborts, asserts or falls back: every call returns an sgq_status.
+ *    Arguments are checked on the host before anything is launched.
+ *  - E4M3 is the OCP FP8 "E4M3FN" format (largest finite 448, no infinities).
+ *    Scales are fp32.  A "UE8M0" scale is an fp32 value that is an exact
+ *    power of two; it is converted to its 8-bit exponent byte only inside the
+ *    GEMM.
+ *  - The library allocates device memory only once per device, on first use
+ *    of a GEMM shape that needs a split-K workspace (and a 4-byte status
+ *    word).  That first use must not happen inside a CUDA stream capture;
+ *    if it does, the call returns SGQ_ERR_UNSUPPORTED.
+ */
+#ifndef SGQ_H_
+#define SGQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA. */
+typedef struct CUstream_st* sgq_stream_t;
+
+typedef enum {
+    SGQ_OK = 0,
+    SGQ_ERR_INVALID_ARG = 1,   /* bad size, null pointer, unsupported value */
+    SGQ_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve */
+    SGQ_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    SGQ_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    SGQ_ERR_TIMEOUT = 5        /* a device-side wait ran out (reported by sgq_device_status) */
+} sgq_status;
+
+/* Flags for sgq_fp8_block_gemm_ex. */
+#define SGQ_GEMM_DEFAULT 0u
+/* Never use the block-scale MMA; apply every scale in the fp32 promotion
+ * step.  Results stay within the same tolerance; meant for testing. */
+#define SGQ_GEMM_FORCE_PROMOTE 1u
+
+/*
+ * Per-token-group quantisation.
+ *
+ * Defined by "Sgl project Sglang GEMM Interface", Description / Quantization
+ * Routines (sgl_per_token_group_quant_8bit: group size, epsilon, clipping
+ * range, UE8M0 scale format) and the "UE8M0 activation rounding" of sglang
+ * PR #42604 "[SM90] Use native block32 DeepGEMM for DeepSeek-V4.1",
+ * Modifications.  For row m and group j (columns j*group .. j*group+group-1):
+ *
+ *   amax    = max |x[m, k]| over the group
+ *   s       = max(amax, 1e-10) / 448           (fp32, correctly rounded)
+ *   if ue8m0: s = smallest power of two >= s
+ *   xs[m,j] = s
+ *   xq[m,k] = E4M3_RNE(clamp(x[m,k] / s, -448, 448))   (fp32 division)
+ *
+ * x:  bf16 [M, K].   xq: uint8 E4M3 codes [M, K].   xs: fp32 [M, K/group].
+ * group in {32, 128}; K % group == 0; M >= 0 (M == 0 is a no-op); ue8m0 in
+ * {0, 1}.  Inputs are finite (NaN/Inf in x give unspecified codes).
+ */
+sgq_status sgq_quant_token_group(const void* x, int64_t M, int64_t K, int group,
+                                 int ue8m0, void* xq, float* xs, sgq_stream_t stream);
+
+/*
+ * Weight block quantisation (offline; produces the GEMM's Wq/Ws).
+ *
+ * One scale per [blk_n, blk_k] tile of W, stored [n_blocks, k_blocks]:
+ * sglang PR #42604, Motivation ([32,32] and [128,128] weight blocks) and the
+ * vLLM "scaled_mm" API page, XPUFp8BlockScaledMMKernel
+ * (process_weights_after_loading: "[n_blocks, k_blocks]", one value per
+ * block tile; ragged N keeps ceil(N/blk_n) rows).  The rule per tile is the
+ * one of sgq_quant_token_group with amax taken over the whole tile (the last
+ * N-tile uses only the rows that exist).
+ *
+ * w: bf16 [N, K].  wq: uint8 E4M3 [N, K].  ws: fp32 [ceil(N/blk_n), K/blk_k].
+ * blk_n in {32, 128}, blk_k in {32, 128}, K % blk_k == 0, N >= 0.
+ */
+sgq_status sgq_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n,
+                                  int blk_k, int ue8m0, void* wq, float* ws,
+                                  sgq_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM, "NT" form.
+ *
+ * Defined by the vLLM "scaled_mm" API page, AiterInt8ScaledMMLinearKernel.
+ * apply_weights docstring (output = mm(scale_a * a, scale_b * b) with
+ * numpy-style broadcasting of the scales) in the layout of sglang PR #42604,
+ * Modifications: fp8_gemm_nt((Aq, As), (Wq, Ws), D, recipe=(1, blk_n, blk_k)),
+ * B given as [N, K]:
+ *
+ *   D[m,n] = bf16_RNE( sum_k  Aq[m,k] * As[m, k/blk_k]
+ *                            * Wq[n,k] * Ws[n/blk_n, k/blk_k] )
+ *
+ * with fp32 accumulation (any order).  The activation group size equals blk_k.
+ *
+ * Aq: uint8 E4M3 [M, K].          As: fp32 [M, K/blk_k].
+ * Wq: uint8 E4M3 [N, K].          Ws: fp32 [ceil(N/blk_n), K/blk_k].
+ * D:  bf16 [M, N] (written, never read).
+ * blk_n in {32, 128}; blk_k in {32, 128}; K % blk_k == 0; K > 0; N % 8 == 0
+ * (16-byte D rows); N may be ragged with respect to blk_n; M >= 0 (M == 0 is
+ * a no-op).  Scales must be finite and > 0.
+ *
+ * When every scale of a 128-wide K step is an exact power of two (UE8M0),
+ * the GEMM applies it inside the tensor-core block-scale MMA; any other fp32
+ * scale is applied in an fp32 promotion step.  Both give the same result up
+ * to fp32 rounding.  The GEMM may begin reading Wq and Ws before the
+ * immediately preceding sgq_quant_token_group on the same stream has
+ * finished (programmatic dependent launch); it reads Aq/As only after.
+ */
+sgq_status sgq_fp8_block_gemm(const void* Aq, const float* As, const void* Wq,
+                              const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
+                              int blk_n, int blk_k, sgq_stream_t stream);
+
+/* sgq_fp8_block_gemm with SGQ_GEMM_* flags. */
+sgq_status sgq_fp8_block_gemm_ex(const void* Aq, const float* As, const void* Wq,
+                                 const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
+                                 int blk_n, int blk_k, uint32_t flags, sgq_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sgq_status_string(sgq_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns SGQ_OK, SGQ_ERR_TIMEOUT (a bounded
+ * device-side wait ran out; the kernel returned early and its outputs are
+ * undefined) or SGQ_ERR_CUDA (the synchronisation itself failed).
+ */
+sgq_status sgq_device_status(sgq_stream_t stream);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t sgq_launch_count(void);
+
+/* Library ABI version (major * 100 + minor). */
+int sgq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGQ_H_ */

@@ -1,0 +1,148 @@
+"""GPU block-scaled GEMM vs the CPU oracle under the stated tolerance:
+||D - Dref||_F / ||Dref||_F <= 5e-3 and |D - Dref| <= 2^-7 |Dref| + 1e-4 sum_k |a||w|
+(D read as fp64; Dref, the bound: fp64 oracle on the same codes and scales)."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_sgq_gb300 as sgq
+from fp8_block_scaled_sgq_gb300 import synth
+
+import oracle
+from common import check_gemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+FLAGS = [sgq.SGQ_GEMM_DEFAULT, sgq.SGQ_GEMM_FORCE_PROMOTE]
+
+
+@functools.lru_cache(maxsize=8)
+def weights(N, K, bn, bk, ue, seed=0):
+    w = synth.weight(N, K, seed)
+    wq, ws = oracle.quant_weight_block(w, bn, bk, ue)
+    return wq, ws
+
+
+def run_gpu(aq, a_s, wq, ws, bn, bk, flags=0):
+    d = sgq.fp8_block_gemm(torch.from_numpy(aq).cuda(), torch.from_numpy(a_s).cuda(),
+                           torch.from_numpy(wq).cuda(), torch.from_numpy(ws).cuda(), bn, bk, flags=flags)
+    assert sgq.sgq_device_status() == 0
+    return d
+
+
+def case_check(c, flags_list=(0,), rows=None):
+    """Quantise x with the oracle, run the GPU GEMM on the full problem, compare
+    (all rows, or a sample of rows the oracle computes one by one)."""
+    x = c.x()
+    aq, a_s = oracle.quant_token_group(x, c.group, c.ue8m0)
+    wq, ws = weights(c.N, c.K, c.blk_n, c.blk_k, c.ue8m0, c.seed)
+    r = np.arange(c.M) if rows is None else rows
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, c.blk_n, c.blk_k)
+    for fl in flags_list:
+        d = run_gpu(aq, a_s, wq, ws, c.blk_n, c.blk_k, fl)
+        check_gemm(d[torch.from_numpy(r).cuda()], dref, bound, f"{c.name} flags={fl}")
+
+
+def test_tiny_fp32_scales():
+    c = synth.WORKLOADS["tiny"][0]
+    case_check(c, FLAGS)
+
+
+@pytest.mark.parametrize("idx", range(4))
+def test_decode_block32(idx):
+    case_check(synth.WORKLOADS["decode_block32"][idx], FLAGS)
+
+
+def test_prefill_block128_sampled():
+    c = synth.WORKLOADS["prefill_block128"][0]
+    case_check(c, FLAGS, rows=sample_rows(c.M, 12))
+
+
+def test_prefill_block32_sampled():
+    c = synth.WORKLOADS["prefill_block32"][0]
+    case_check(c, FLAGS, rows=sample_rows(c.M, 12))
+
+
+SWEEP = synth.WORKLOADS["sweep"]
+
+
+@pytest.mark.parametrize("idx", range(len(SWEEP)), ids=[c.name for c in SWEEP])
+def test_sweep(idx):
+    c = SWEEP[idx]
+    rows = None if c.M <= 128 else sample_rows(c.M, 10, seed=idx)
+    case_check(c, (0,), rows=rows)
+
+
+RAGGED = [(1, 8, 32, 32, 32), (3, 136, 96, 32, 32), (17, 264, 160, 32, 32), (65, 200, 256, 128, 128),
+          (129, 136, 384, 128, 128), (200, 520, 2080, 32, 32), (64, 1032, 128, 128, 32),
+          (300, 72, 640, 32, 128), (33, 256, 4096, 128, 128)]
+
+
+@pytest.mark.parametrize("M,N,K,bn,bk", RAGGED)
+@pytest.mark.parametrize("pow2", [True, False])
+def test_ragged_shapes(M, N, K, bn, bk, pow2):
+    c = synth.Case("ragged", M, N, K, bn, bk, pow2, seed=M + N + K)
+    x = c.x()
+    w = c.w()
+    aq, a_s = oracle.quant_token_group(x, bk, pow2)
+    wq, ws = oracle.quant_weight_block(w, bn, bk, pow2)
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, bn, bk)
+    for fl in FLAGS:
+        check_gemm(run_gpu(aq, a_s, wq, ws, bn, bk, fl), dref, bound, f"M={M} N={N} K={K} fl={fl}")
+
+
+@pytest.mark.parametrize("M", [5, 200])
+@pytest.mark.parametrize("bk", [32, 128])
+def test_mixed_pow2_and_fp32_scales(M, bk):
+    """Some K stages all power-of-two, others not: the kernel switches between
+    the block-scale MMA and promotion inside one tile."""
+    N, K, bn = 264, 1024, 128
+    x = synth.activation(M, K, seed=11)
+    w = synth.weight(N, K, seed=11)
+    aq, a_s = oracle.quant_token_group(x, bk, True)
+    wq, ws = oracle.quant_weight_block(w, bn, bk, True)
+    rng = np.random.default_rng(M + bk)
+    kcols = a_s.shape[1]
+    stage_cols = 128 // bk
+    for st in range(K // 128):
+        if rng.random() < 0.5:   # make this stage's weight scales non-power-of-two
+            ws[:, st * stage_cols:(st + 1) * stage_cols] *= np.float32(1.3)
+    ws[0, kcols - 1] = np.float32(0.7) * ws[0, kcols - 1]   # last stage mixed too
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, bn, bk)
+    check_gemm(run_gpu(aq, a_s, wq, ws, bn, bk), dref, bound, f"mixed M={M} bk={bk}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 4096])
+def test_deterministic(M):
+    """Split-K sums partials in a fixed order: repeated calls are bitwise equal."""
+    N, K = 7168, 2048
+    x = synth.activation(M, K, seed=3)
+    aq, a_s = oracle.quant_token_group(x, 32, True)
+    wq, ws = weights(N, K, 32, 32, True)
+    args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+    d0 = sgq.fp8_block_gemm(*args, 32, 32)
+    for _ in range(3):
+        d1 = sgq.fp8_block_gemm(*args, 32, 32)
+        assert torch.equal(d0, d1)
+
+
+def test_linear_end_to_end_on_device():
+    """Quant kernel feeding the GEMM on one stream (the programmatic-launch pair)."""
+    c = synth.WORKLOADS["decode_block32"][2]
+    x = c.x()
+    wq, ws = weights(c.N, c.K, c.blk_n, c.blk_k, True)
+    d = sgq.w8a8_linear(x.cuda(), torch.from_numpy(wq).cuda(), torch.from_numpy(ws).cuda(), 32, 32, True)
+    aq, a_s = oracle.quant_token_group(x, 32, True)
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, 32, 32)
+    check_gemm(d, dref, bound, "w8a8_linear")
+    assert sgq.sgq_device_status() == 0
+
+
+def test_m_zero_is_noop():
+    d = sgq.fp8_block_gemm(torch.empty((0, 256), dtype=torch.uint8, device="cuda"),
+                           torch.empty((0, 2), dtype=torch.float32, device="cuda"),
+                           torch.zeros((128, 256), dtype=torch.uint8, device="cuda"),
+                           torch.ones((1, 2), dtype=torch.float32, device="cuda"), 128, 128)
+    assert d.shape == (0, 128)
