@@ -198,18 +198,19 @@ def run_ours(args, ws_, rank, local):
     if sgq.sgq_device_status(sptr) != 0:
         raise SystemExit("device status not OK after warm-up")
 
-    def capture(gemm_only):
+    def capture(fn):
         graphs = []
         for r in range(n_rot):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(stream):
                 with torch.cuda.graph(g, stream=stream):
-                    step_fn(sgq, per, *wrot[r], torch.cuda.current_stream().cuda_stream, gemm_only)
+                    fn(r, torch.cuda.current_stream().cuda_stream)
             graphs.append(g)
         return graphs
 
-    graphs = capture(False)
-    ggraphs = capture(True)
+    graphs = capture(lambda r, sp: step_fn(sgq, per, *wrot[r], sp))
+    case_graphs = [capture(lambda r, sp, i=i: step_fn(sgq, per[i:i + 1], *wrot[r], sp, gemm_only=True))
+                   for i in range(len(per))]
 
     def timed(gl, steps):
         with torch.cuda.stream(stream):
@@ -230,13 +231,25 @@ def run_ours(args, ws_, rank, local):
         barrier(ws_)
         return e0.elapsed_time(e1) / steps   # ms per step
 
+    def preheat(seconds):
+        t_end = time.perf_counter() + seconds
+        i = 0
+        while time.perf_counter() < t_end:
+            with torch.cuda.stream(stream):
+                for _ in range(50):
+                    graphs[i % n_rot].replay()
+                    i += 1
+            stream.synchronize()
+
     launches0 = sgq.sgq_launch_count()
     with ClockSampler(local, os.path.join(args.out_dir, f"clocks_rank{rank}.csv") if args.out_dir else None) as cs:
+        preheat(args.preheat)
         ms_step = timed(graphs, args.steps)
-        ms_gemm = timed(ggraphs, args.steps)
+        ms_case = [timed(cg, args.steps) for cg in case_graphs]
     clocks = cs.summary()
     ms_step = max_over_ranks(ms_step, ws_, device)
-    ms_gemm = max_over_ranks(ms_gemm, ws_, device)
+    ms_case = [max_over_ranks(t, ws_, device) for t in ms_case]
+    ms_gemm = sum(ms_case)
     gpu_launches = 2 * len(cases) * args.steps   # quant + GEMM per case per step (graph replays)
     assert sgq.sgq_launch_count() == launches0   # replays do not call the library
 
@@ -279,7 +292,10 @@ def run_ours(args, ws_, rank, local):
         "tflops": round(ws_ * step_flops / (ms_step * 1e-3) / 1e12, 3),
         "gemm": {"ms_per_step": round(ms_gemm, 5), "gbs": round(gemm_gbs, 1),
                  "tflops": round(step_flops / (ms_gemm * 1e-3) / 1e12, 3),
-                 "us_per_launch": round(ms_gemm * 1e3 / len(cases), 3)},
+                 "per_case": [{"M": c.M, "us": round(t * 1e3, 3),
+                               "gbs": round(c.gemm_bytes() / (t * 1e-3) / 1e9, 1),
+                               "tflops": round(c.flops() / (t * 1e-3) / 1e12, 2)}
+                              for c, t in zip(cases, ms_case)]},
         "roofline": {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gemm_gbs / pk["hbm_gbs"], 4), "traffic": None,
                      "kernel": "fp8_block_gemm_kernel (swap-AB, split-K)", "peak_source": pk["source"]},
@@ -386,6 +402,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_block32", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--preheat", type=float, default=1.5,
+                    help="seconds of identical load before the timed region (clock sampling)")
     ap.add_argument("--out-dir", default=None, help="directory for clock samples")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -295,76 +295,141 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ---------------------------------------------------------- scale loader
+        // Two-phase software pipeline.  Issue: the raw fp32 scales of up to
+        // kStages jobs are fetched with cp.async (one commit group per job)
+        // as soon as their slot is free.  Finish: when the oldest job's copies
+        // have landed, its scales are checked for the power-of-two property,
+        // packed into UE8M0 words in tcgen05.cp order and handed to the MMA
+        // warp.  Global-load latency is paid once per ring, not per stage.
         ptx::grid_dependency_wait();
-        JobIter it;
-        it.begin(a);
-        int stage = 0;
-        uint32_t phase = 0;
-        const int col_groups = kSwap ? BN : (BN + a.blk_n - 1) / a.blk_n;
-        while (it.valid(a)) {
-            if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 3)) break;
-            SfSlot<BN>& slot = sf[stage];
-            const int q0 = it.kb * 4;
-            const int nq = min(4, (a.K - it.kb * kBK) / 32);
-            const int row0 = it.tr * kBM, col0 = it.tc * BN;
+        const bool blk128 = a.blk_k == 128;
+        const int nld = blk128 ? 1 : 4;           // distinct scale chunks per stage
+        auto issue_raw = [&](SfSlot<BN>& slot, const JobIter& j) {
+            const int q0 = j.kb * 4;
+            const int nq = min(4, (a.K - j.kb * kBK) / 32);
+            const int row0 = j.tr * kBM, col0 = j.tc * BN;
+            if (!kSwap) {
+                // A operand = activation rows: one scale per row and chunk
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = lane + 32 * i, g = row0 + r;
+                    for (int c = 0; c < nld; ++c) {
+                        float* dst = &slot.lane_raw[c][r];
+                        if (c < nq && g < a.rows)
+                            ptx::cp_async_4(ptx::smem_u32(dst),
+                                            a.As + static_cast<int64_t>(g) * a.ks + ((q0 + c) * 32) / a.blk_k);
+                        else
+                            *dst = 1.0f;
+                    }
+                }
+                // B operand = weight rows: one scale per n-block and chunk
+                const int ngrp = (BN + a.blk_n - 1) / a.blk_n;
+                for (int idx = lane; idx < ngrp * nld; idx += 32) {
+                    const int gi = idx / nld, c = idx - gi * nld, g = col0 + gi * a.blk_n;
+                    float* dst = &slot.col_raw[c][gi];
+                    if (c < nq && g < a.cols)
+                        ptx::cp_async_4(ptx::smem_u32(dst),
+                                        a.Ws + static_cast<int64_t>(g / a.blk_n) * a.ks + ((q0 + c) * 32) / a.blk_k);
+                    else
+                        *dst = 1.0f;
+                }
+            } else {
+                // A operand = weight rows: one scale per n-block and chunk
+                const int nblk = kBM / a.blk_n;
+                for (int idx = lane; idx < nblk * nld; idx += 32) {
+                    const int bi = idx / nld, c = idx - bi * nld, g = row0 + bi * a.blk_n;
+                    float* dst = &slot.lane_raw[c][bi];
+                    if (c < nq && g < a.rows)
+                        ptx::cp_async_4(ptx::smem_u32(dst),
+                                        a.Ws + static_cast<int64_t>(g / a.blk_n) * a.ks + ((q0 + c) * 32) / a.blk_k);
+                    else
+                        *dst = 1.0f;
+                }
+                // B operand = token rows: one scale per token and chunk
+                for (int idx = lane; idx < BN * nld; idx += 32) {
+                    const int t = idx / nld, c = idx - t * nld, g = col0 + t;
+                    float* dst = &slot.col_raw[c][t];
+                    if (c < nq && g < a.cols)
+                        ptx::cp_async_4(ptx::smem_u32(dst),
+                                        a.As + static_cast<int64_t>(g) * a.ks + ((q0 + c) * 32) / a.blk_k);
+                    else
+                        *dst = 1.0f;
+                }
+            }
+        };
+        auto convert = [&](SfSlot<BN>& slot) {
             bool ok = true;
-            // A-operand rows: lane owns rows lane, lane+32, lane+64, lane+96.
             uint32_t w4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = lane + 32 * i;
-                const int g = row0 + r;
+                const int li = kSwap ? r / a.blk_n : r;
                 uint32_t word = 0;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    float s = 1.0f;
-                    if (j < nq && g < a.rows) s = kSwap ? wt_scale(a, g, q0 + j) : act_scale(a, g, q0 + j);
-                    slot.lane_raw[j][r] = s;
+                    const float s = slot.lane_raw[blk128 ? 0 : j][li];
                     ok &= is_pow2_scale(s);
                     word |= ((__float_as_uint(s) >> 23) & 0xFFu) << (8 * j);
                 }
                 w4[i] = word;
             }
             *reinterpret_cast<uint4*>(&slot.sfa[lane * 4]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            // B-operand rows, in 128-row chunks.
 #pragma unroll
             for (int h = 0; h < C::kSfbCopies; ++h) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int c = h * 128 + lane + 32 * i;
-                    const int g = col0 + c;
-                    uint32_t word = 0;
+                    uint32_t word = 0x7F7F7F7Fu;   // 2^0 for rows past the tile
+                    if (c < BN) {
+                        const int ci = kSwap ? c : c / a.blk_n;
+                        word = 0;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float s = 1.0f;
-                        if (j < nq && c < BN && g < a.cols)
-                            s = kSwap ? act_scale(a, g, q0 + j) : wt_scale(a, g, q0 + j);
-                        ok &= is_pow2_scale(s);
-                        word |= ((__float_as_uint(s) >> 23) & 0xFFu) << (8 * j);
+                        for (int j = 0; j < 4; ++j) {
+                            const float s = slot.col_raw[blk128 ? 0 : j][ci];
+                            ok &= is_pow2_scale(s);
+                            word |= ((__float_as_uint(s) >> 23) & 0xFFu) << (8 * j);
+                        }
                     }
                     w4[i] = word;
                 }
                 *reinterpret_cast<uint4*>(&slot.sfb[h * 128 + lane * 4]) =
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            // Raw fp32 scales of the B operand, one per row group.
-            for (int gi = lane; gi < col_groups; gi += 32) {
-                const int g = kSwap ? col0 + gi : col0 + gi * a.blk_n;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float s = 1.0f;
-                    if (j < nq && g < a.cols) s = kSwap ? act_scale(a, g, q0 + j) : wt_scale(a, g, q0 + j);
-                    slot.col_raw[j][gi] = s;
-                }
-            }
             const bool all_ok = __all_sync(0xFFFFFFFFu, ok);
             if (lane == 0) slot.pow2 = all_ok ? 1u : 0u;
+        };
+        JobIter iss, fin;
+        iss.begin(a);
+        fin.begin(a);
+        uint32_t n_iss = 0, n_fin = 0;
+        bool failed = false;
+        while (fin.valid(a) && !failed) {
+            while (iss.valid(a) && n_iss - n_fin < static_cast<uint32_t>(kStages)) {
+                const int si = static_cast<int>(n_iss % kStages);
+                const uint32_t par = ((n_iss / kStages) & 1u) ^ 1u;
+                if (n_iss != n_fin) {
+                    if (!ptx::mbar_try_wait(empty_bar(si), par)) break;   // finish something first
+                } else if (!wait_bar(empty_bar(si), par, sync, 3)) {
+                    failed = true;
+                    break;
+                }
+                issue_raw(sf[si], iss);
+                ptx::cp_async_commit();
+                ++n_iss;
+                iss.next(a);
+            }
+            if (failed) break;
+            const int sf_i = static_cast<int>(n_fin % kStages);
+            ptx::cp_async_wait_pending(static_cast<int>(n_iss - n_fin) - 1);
+            __syncwarp();
+            convert(sf[sf_i]);
             ptx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(full_bar(stage));
-            it.next(a);
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            if (lane == 0) ptx::mbar_arrive(full_bar(sf_i));
+            ++n_fin;
+            fin.next(a);
         }
+        ptx::cp_async_wait_pending(0);
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -372,8 +437,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint32_t idesc_mx = ptx::idesc_mxf8(kBM, BN);
         const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
         const int col_group = kSwap ? 1 : a.blk_n;
-        const int lane_group = kSwap ? a.blk_n : 1;
-        (void)lane_group;
         JobIter it;
         it.begin(a);
         int stage = 0;
@@ -443,7 +506,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (!wait_bar(acce_bar(b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     const int j = gidx;  // scale chunk (blk_k == 128: chunk 0 holds the block scale)
-                    for (int r = lane; r < 128; r += 32) info[b].lane_s[r] = slot.lane_raw[j][r];
+                    for (int r = lane; r < 128; r += 32)
+                        info[b].lane_s[r] = slot.lane_raw[j][kSwap ? r / a.blk_n : r];
                     for (int c = lane; c < BN; c += 32) info[b].col_s[c] = slot.col_raw[j][c / col_group];
                     const bool last = it.last_kb() && gidx == ngroups - 1;
                     if (lane == 0) info[b].flags = kInfoPromote | (last ? kInfoLast : 0u);

@@ -1,0 +1,73 @@
+"""The multi-rank host logic of bench.py (replicas, barrier, max-over-ranks
+timing) on CPU with the gloo backend, world size 2."""
+import os
+import socket
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    ws, r, local = bench.dist_env()
+    assert (ws, r, local) == (world, rank, rank)
+    bench.dist_init(ws, "gloo")
+    bench.barrier(ws)
+    t = bench.max_over_ranks(1.5 + rank, ws, torch.device("cpu"))
+    bench.barrier(ws)
+    q.put((rank, t))
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_and_barrier():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 2.5), (1, 2.5)]
+
+
+def test_reference_arm_other_ranks_exit(monkeypatch, capsys):
+    """Under torchrun only rank 0 prints the reference line; others return None."""
+    import bench
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_ref_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(300)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got[1] is None
+    assert got[0]["impl"] == "reference" and got[0]["value"] > 0
+
+
+def _ref_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import argparse
+    import bench
+    args = argparse.Namespace(workload="tiny", steps=1, warmup=1)
+    res = bench.run_reference(args, world, rank)
+    q.put((rank, res))
+    if dist.is_initialized():
+        dist.destroy_process_group()
