@@ -1,0 +1,12 @@
+// Instantiates the block-scaled GEMM for the [128,128] weight-block recipe
+// (activation groups of 128).
+#include "gemm_kernel.cuh"
+
+namespace sgq {
+namespace gemm {
+sgq_status dispatch_128_128(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                           int grid, cudaStream_t st) {
+    return dispatch<128, 128>(swap, bn, ta, tb, a, grid, st);
+}
+}  // namespace gemm
+}  // namespace sgq

@@ -1,0 +1,12 @@
+// Instantiates the block-scaled GEMM for the [32,32] weight-block recipe
+// (activation groups of 32).
+#include "gemm_kernel.cuh"
+
+namespace sgq {
+namespace gemm {
+sgq_status dispatch_32_32(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                           int grid, cudaStream_t st) {
+    return dispatch<32, 32>(swap, bn, ta, tb, a, grid, st);
+}
+}  // namespace gemm
+}  // namespace sgq

@@ -1,0 +1,217 @@
+// Host side of the block-scaled FP8 GEMM: launch plan (tile shape, split-K),
+// TMA tensor maps, the split-K workspace and the device status word.  The
+// kernel itself is in gemm_kernel.cuh; gemm_b*.cu instantiate it per recipe.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "gemm_kernel.cuh"
+
+namespace sgq {
+
+__device__ uint32_t g_gemm_status;
+
+namespace gemm {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+sgq_status get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode ? SGQ_OK : SGQ_ERR_CUDA;
+}
+
+// 2-D map over a [rows, K] uint8 matrix, box = 128 K-bytes x box_rows rows,
+// 128-byte swizzle (the UMMA K-major SW128 layout).
+sgq_status make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
+}
+
+// Split-K workspace, one per device, created on first need.
+constexpr size_t kWsBytes = size_t(64) << 20;
+constexpr int kMaxCounters = 1 << 16;
+struct DevWs {
+    float* partial = nullptr;
+    uint32_t* counters = nullptr;
+};
+DevWs g_ws[64];
+std::mutex g_ws_mu;
+
+sgq_status get_workspace(cudaStream_t st, DevWs* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (!g_ws[dev].partial) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return SGQ_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return SGQ_ERR_UNSUPPORTED;
+        void* p = nullptr;
+        void* c = nullptr;
+        if (cudaMalloc(&p, kWsBytes) != cudaSuccess) return SGQ_ERR_CUDA;
+        if (cudaMalloc(&c, kMaxCounters * sizeof(uint32_t)) != cudaSuccess) {
+            cudaFree(p);
+            return SGQ_ERR_CUDA;
+        }
+        if (cudaMemset(c, 0, kMaxCounters * sizeof(uint32_t)) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(p);
+            cudaFree(c);
+            return SGQ_ERR_CUDA;
+        }
+        g_ws[dev].partial = static_cast<float*>(p);
+        g_ws[dev].counters = static_cast<uint32_t*>(c);
+    }
+    *out = g_ws[dev];
+    return SGQ_OK;
+}
+
+struct Plan {
+    bool swap;
+    int bn, tiles_r, tiles_c, kb_total, kb_per_split, splits, items, grid;
+};
+
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    return v ? std::atoi(v) : dflt;
+}
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
+    Plan p{};
+    p.swap = M <= 64;
+    p.bn = p.swap ? (M <= 16 ? 16 : (M <= 32 ? 32 : 64)) : 256;
+    const int64_t rows = p.swap ? N : M, cols = p.swap ? M : N;
+    p.tiles_r = static_cast<int>((rows + kBM - 1) / kBM);
+    p.tiles_c = static_cast<int>((cols + p.bn - 1) / p.bn);
+    p.kb_total = static_cast<int>((K + kBK - 1) / kBK);
+    const int64_t tiles = int64_t(p.tiles_r) * p.tiles_c;
+    static const int ovh = env_int("SGQ_SPLIT_OVERHEAD", 2);
+    static const int forced = env_int("SGQ_SPLITS", 0);
+    int best_s = 1;
+    double best = 1e300;
+    const int max_s = p.kb_total < 32 ? p.kb_total : 32;
+    for (int s = 1; s <= max_s; ++s) {
+        const int kbp = (p.kb_total + s - 1) / s;
+        if ((p.kb_total + kbp - 1) / kbp != s) continue;   // every split non-empty
+        const int64_t items = tiles * s;
+        if (s > 1 && (tiles > kMaxCounters ||
+                      size_t(items) * kBM * p.bn * sizeof(float) > kWsBytes))
+            continue;
+        const int64_t waves = (items + sm_count - 1) / sm_count;
+        const double cost = double(waves) * (kbp + ovh) + (s > 1 ? 0.5 : 0.0);
+        if (forced > 0 ? s == forced : cost < best) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    p.splits = best_s;
+    p.kb_per_split = (p.kb_total + best_s - 1) / best_s;
+    p.items = static_cast<int>(tiles * best_s);
+    p.grid = p.items < sm_count ? p.items : sm_count;
+    return p;
+}
+
+// Address of the device status word on the current device.
+uint32_t* g_status_ptr[64] = {};
+std::mutex g_status_mu;
+
+}  // namespace
+
+sgq_status status_word(uint32_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_gemm_status) != cudaSuccess) return SGQ_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return SGQ_OK;
+}
+}  // namespace gemm
+
+sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq, const float* Ws,
+                                 void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                 uint32_t flags, cudaStream_t st) {
+    if (gemm::get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
+    DeviceInfo di;
+    sgq_status rc = device_info(&di);
+    if (rc != SGQ_OK) return rc;
+    if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
+    const gemm::Plan p = gemm::make_plan(M, N, K, di.sm_count);
+    gemm::GemmArgs a{};
+    a.As = As;
+    a.Ws = Ws;
+    a.D = static_cast<__nv_bfloat16*>(D);
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.ks = static_cast<int>(K / blk_k);
+    a.rows = static_cast<int>(p.swap ? N : M);
+    a.cols = static_cast<int>(p.swap ? M : N);
+    a.tiles_r = p.tiles_r;
+    a.tiles_c = p.tiles_c;
+    a.kb_total = p.kb_total;
+    a.kb_per_split = p.kb_per_split;
+    a.splits = p.splits;
+    a.items = p.items;
+    a.group_r = 16;
+    a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
+    rc = gemm::status_word(&a.status);
+    if (rc != SGQ_OK) return rc;
+    if (p.splits > 1) {
+        gemm::DevWs ws;
+        rc = gemm::get_workspace(st, &ws);
+        if (rc != SGQ_OK) return rc;
+        a.partial = ws.partial;
+        a.counters = ws.counters;
+    }
+    CUtensorMap ta, tb;
+    const void* opA = p.swap ? Wq : Aq;
+    const void* opB = p.swap ? Aq : Wq;
+    if (gemm::make_tmap(&ta, opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (gemm::make_tmap(&tb, opB, a.cols, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.bn, ta, tb, a, p.grid, st);
+    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.bn, ta, tb, a, p.grid, st);
+    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.bn, ta, tb, a, p.grid, st);
+    return gemm::dispatch_128_128(p.swap, p.bn, ta, tb, a, p.grid, st);
+}
+
+sgq_status read_and_clear_device_status(cudaStream_t st) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SGQ_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(v)) != cudaSuccess) return SGQ_ERR_CUDA;
+    if (v == 0) return SGQ_OK;
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(zero)) != cudaSuccess) return SGQ_ERR_CUDA;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && gemm::g_ws[dev].counters) {
+        // an aborted split-K launch may have left arrival counts behind
+        if (cudaMemset(gemm::g_ws[dev].counters, 0, gemm::kMaxCounters * sizeof(uint32_t)) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess)
+            return SGQ_ERR_CUDA;
+    }
+    return (v & gemm::kStatusTimeout) ? SGQ_ERR_TIMEOUT : SGQ_ERR_CUDA;
+}
+
+}  // namespace sgq

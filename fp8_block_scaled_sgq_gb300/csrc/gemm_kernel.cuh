@@ -1,4 +1,4 @@
-// Block-scaled FP8 GEMM for sm_103a:  D = (Aq * As)(Wq * Ws)^T, bf16 out.
+// Block-scaled FP8 GEMM kernel for sm_103a:  D = (Aq * As)(Wq * Ws)^T, bf16 out.
 //
 // Defined by the vLLM "scaled_mm" API page (AiterInt8ScaledMMLinearKernel.
 // apply_weights docstring: output = mm(scale_a * a, scale_b * b), scales
@@ -12,44 +12,38 @@
 //   warp 1      MMA issuer: one thread issues tcgen05.mma into a TMEM
 //               accumulator.  For each 128-wide K stage:
 //                 - if every scale of the stage is an exact power of two,
-//                   the scales are converted to UE8M0 bytes, copied to TMEM
-//                   (tcgen05.cp) and applied inside the block-scaled MMA
-//                   (kind::mxf8f6f4, one scale per row per 32-wide K chunk);
-//                   consecutive such stages accumulate in TMEM;
-//                 - otherwise the stage's partial product for each scale
-//                   group is formed unscaled (kind::f8f6f4) and handed to the
-//                   epilogue, which applies the fp32 scales ("promotion").
-//   warp 2      scale loader: reads As/Ws for the stage, checks the
-//               power-of-two property, writes the UE8M0 words (laid out for
-//               tcgen05.cp) and the raw fp32 scales into the stage's slot.
+//                   the UE8M0 bytes are copied to TMEM (tcgen05.cp) and
+//                   applied inside the block-scaled MMA (kind::mxf8f6f4, one
+//                   scale per row per 32-wide K chunk); consecutive such
+//                   stages accumulate in TMEM;
+//                 - otherwise each scale group's partial product is formed
+//                   unscaled (kind::f8f6f4) and handed to the epilogue, which
+//                   applies the fp32 scales ("promotion").
+//   warp 2      scale loader: fetches As/Ws for the stages ahead with
+//               cp.async, checks the power-of-two property, and writes the
+//               UE8M0 words (laid out for tcgen05.cp) into the stage's slot.
 //   warps 3-10  epilogue: tcgen05.ld of the accumulator (each warp its TMEM
-//               lane quadrant and half of the columns), fp32 promotion
-//               and accumulation in registers, bf16 store, or an fp32
-//               split-K partial plus a last-arriver reduction.
+//               lane quadrant and half of the columns), fp32 promotion and
+//               accumulation in registers, bf16 store, or an fp32 split-K
+//               partial plus a last-arriver reduction in split order.
 // Small M (<= 64) runs "swap-AB": the weight rows fill the 128-row MMA M
 // dimension and the tokens the MMA N dimension (16/32/64), with split-K over
-// the persistent grid so all SMs stream weights.
+// the persistent grid so the weights stream through all SMs.
 //
 // Every wait on an mbarrier is bounded; on time-out the CTA records a status
-// word, stops issuing work and exits through the normal teardown.
+// word, stops issuing work and leaves through the normal teardown.
+#pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <cstdint>
-#include <cstdlib>
-#include <cstring>
-#include <mutex>
 
 #include "ptx.cuh"
 #include "sgq_internal.h"
 
 namespace sgq {
-
-__device__ uint32_t g_gemm_status;
-
-namespace {
+namespace gemm {
 
 constexpr int kBM = 128;          // MMA M: rows of the "A" operand per tile
 constexpr int kBK = 128;          // K elements (bytes) per pipeline stage
@@ -61,15 +55,14 @@ constexpr uint64_t kTimeoutNs = 1ull << 30;
 
 constexpr uint32_t kInfoPromote = 1u;
 constexpr uint32_t kInfoLast = 2u;
-
 constexpr uint32_t kStatusTimeout = 1u;
 
 template <int BN>
 struct alignas(128) SfSlot {
     uint32_t sfa[128];                  // UE8M0 words of the A operand (tcgen05.cp order)
     uint32_t sfb[BN < 128 ? 128 : BN];  // UE8M0 words of the B operand
-    float lane_raw[4][128];             // fp32 scale per A row, per 32-wide K chunk
-    float col_raw[4][64];               // fp32 scale per B row group, per chunk
+    float lane_raw[4][128];             // fp32 scales of the A operand, per chunk
+    float col_raw[4][64];               // fp32 scales of the B operand, per chunk
     uint32_t pow2;                      // every scale of the stage is 2^e
 };
 
@@ -87,26 +80,12 @@ struct GemmArgs {
     __nv_bfloat16* D;
     float* partial;       // split-K workspace
     uint32_t* counters;   // split-K arrival counters (self-resetting)
-    int M, N, K, blk_n, blk_k, ks;   // ks = K / blk_k (columns of As and Ws)
+    uint32_t* status;     // device status word
+    int M, N, K, ks;      // ks = K / blk_k (columns of As and Ws)
     int rows, cols;       // extents of the MMA A operand and B operand
     int tiles_r, tiles_c, kb_total, kb_per_split, splits, items, group_r;
     int force_promote;
 };
-
-// Scale of activation row m for the 32-wide K chunk q.
-__device__ __forceinline__ float act_scale(const GemmArgs& a, int m, int q) {
-    return __ldg(a.As + static_cast<int64_t>(m) * a.ks + (q * 32) / a.blk_k);
-}
-// Scale of weight row n for the 32-wide K chunk q.
-__device__ __forceinline__ float wt_scale(const GemmArgs& a, int n, int q) {
-    return __ldg(a.Ws + static_cast<int64_t>(n / a.blk_n) * a.ks + (q * 32) / a.blk_k);
-}
-
-__device__ __forceinline__ bool is_pow2_scale(float s) {
-    const uint32_t b = __float_as_uint(s);
-    const uint32_t e = b >> 23;
-    return (b & 0x007FFFFFu) == 0 && e != 0 && e < 0xFFu;  // sign 0, normal, mantissa 0
-}
 
 // Walks the (item, k-stage) jobs of one CTA in order.
 struct JobIter {
@@ -131,20 +110,24 @@ struct JobIter {
     }
     __device__ bool valid(const GemmArgs& a) const { return item < a.items; }
     __device__ bool last_kb() const { return kb + 1 == kb1; }
-    __device__ void next(const GemmArgs& a) {
+    __device__ bool first_kb(const GemmArgs& a) const { return kb == split * a.kb_per_split; }
+    // Advances one stage; returns true when it moved to a new item.
+    __device__ bool next(const GemmArgs& a) {
         if (++kb >= kb1) {
             item += gridDim.x;
             if (item < a.items) load(a);
+            return true;
         }
+        return false;
     }
 };
 
 struct Sync {
     volatile uint32_t* abort_flag;
+    uint32_t* status;
 };
 
-__device__ bool wait_bar(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
     const uint64_t t0 = ptx::globaltimer();
     uint32_t spins = 0;
     while (true) {
@@ -153,11 +136,15 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, const Sync& s, uint32_t 
             if (*s.abort_flag) return false;
             if (ptx::globaltimer() - t0 > kTimeoutNs) {
                 *s.abort_flag = 1u;
-                atomicOr(&g_gemm_status, kStatusTimeout | (where << 8));
+                atomicOr(s.status, kStatusTimeout | (where << 8));
                 return false;
             }
         }
     }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, s, where);
 }
 
 __device__ __forceinline__ bool epi_any(bool pred) {
@@ -177,7 +164,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int BN, int kStages, bool kSwap, int kAccBufs>
+// Bits of a scale that must be zero for it to be a UE8M0 value 2^e (sign and
+// mantissa), and its exponent byte.
+__device__ __forceinline__ uint32_t scale_bad_bits(uint32_t b) {
+    const uint32_t e = b >> 23;
+    return (b & 0x807FFFFFu) | static_cast<uint32_t>(e == 0u || e == 0xFFu);
+}
+
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK>
 struct Cfg {
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
@@ -185,6 +179,10 @@ struct Cfg {
     static constexpr int kCols = BN / 2;  // accumulator columns per epilogue thread
     static constexpr int kLd = kCols < 16 ? kCols : 16;
     static constexpr int kSfbCopies = BN > 128 ? BN / 128 : 1;
+    static constexpr int kNld = kBlkK == 128 ? 1 : 4;    // distinct scale chunks per stage
+    static constexpr int kScalesPerStage = kBK / kBlkK;  // As/Ws columns per stage
+    static constexpr int kColGroups = kSwap ? BN : (BN + kBlkN - 1) / kBlkN;
+    static constexpr int kLaneGroups = kSwap ? kBM / kBlkN : kBM;
     static constexpr size_t kOffA = 0;
     static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
     static constexpr size_t kOffSf = kOffB + size_t(kStages) * kBBytes;
@@ -196,14 +194,16 @@ struct Cfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(kAccBufs * BN <= int(kSfCol), "TMEM budget");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
+    static_assert(kColGroups <= 64, "raw column-scale slot");
+    static_assert(kStages <= 8, "cp.async group depth");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int BN, int kStages, bool kSwap, int kAccBufs>
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs>;
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    Sync sync{reinterpret_cast<volatile uint32_t*>(misc + 1)};
+    const Sync sync{reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -257,40 +257,39 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // The weight operand does not depend on the preceding kernel, so the
         // weight halves of the first kStages stages go out before the
         // programmatic-dependency wait; activations only after it.
-        const CUtensorMap* tmW = kSwap ? &tmA : &tmB;
-        const CUtensorMap* tmX = kSwap ? &tmB : &tmA;
-        auto w_dst = [&](int s) { return ptx::smem_u32(kSwap ? sA + s * C::kABytes : sB + s * C::kBBytes); };
-        auto x_dst = [&](int s) { return ptx::smem_u32(kSwap ? sB + s * C::kBBytes : sA + s * C::kABytes); };
-        auto w_row = [&](const JobIter& j) { return kSwap ? j.tr * kBM : j.tc * BN; };
-        auto x_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : j.tr * kBM; };
-        JobIter it;
-        it.begin(a);
-        JobIter pre = it;
-        int npre = 0;
-        while (npre < kStages && pre.valid(a)) {
-            if (lane == 0) {
+        if (lane == 0) {
+            const CUtensorMap* tmW = kSwap ? &tmA : &tmB;
+            const CUtensorMap* tmX = kSwap ? &tmB : &tmA;
+            const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
+            auto w_dst = [&](int s) { return kSwap ? sA0 + s * C::kABytes : sB0 + s * C::kBBytes; };
+            auto x_dst = [&](int s) { return kSwap ? sB0 + s * C::kBBytes : sA0 + s * C::kABytes; };
+            auto w_row = [&](const JobIter& j) { return kSwap ? j.tr * kBM : j.tc * BN; };
+            auto x_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : j.tr * kBM; };
+            JobIter it;
+            it.begin(a);
+            JobIter pre = it;
+            int npre = 0;
+            while (npre < kStages && pre.valid(a)) {
                 ptx::mbar_arrive_expect_tx(full_bar(npre), C::kStageBytes);
                 ptx::tma_load_2d(w_dst(npre), tmW, pre.kb * kBK, w_row(pre), full_bar(npre));
+                pre.next(a);
+                ++npre;
             }
-            pre.next(a);
-            ++npre;
-        }
-        if (lane == 0) ptx::grid_dependency_wait();
-        for (int s = 0; s < npre; ++s) {
-            if (lane == 0) ptx::tma_load_2d(x_dst(s), tmX, it.kb * kBK, x_row(it), full_bar(s));
-            it.next(a);
-        }
-        int stage = npre % kStages;
-        uint32_t phase = npre / kStages;
-        while (it.valid(a)) {
-            if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 1)) break;
-            if (lane == 0) {
+            ptx::grid_dependency_wait();
+            for (int s = 0; s < npre; ++s) {
+                ptx::tma_load_2d(x_dst(s), tmX, it.kb * kBK, x_row(it), full_bar(s));
+                it.next(a);
+            }
+            int stage = npre % kStages;
+            uint32_t phase = npre / kStages;
+            while (it.valid(a)) {
+                if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 1)) break;
                 ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
                 ptx::tma_load_2d(w_dst(stage), tmW, it.kb * kBK, w_row(it), full_bar(stage));
                 ptx::tma_load_2d(x_dst(stage), tmX, it.kb * kBK, x_row(it), full_bar(stage));
+                it.next(a);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
-            it.next(a);
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -301,75 +300,99 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // have landed, its scales are checked for the power-of-two property,
         // packed into UE8M0 words in tcgen05.cp order and handed to the MMA
         // warp.  Global-load latency is paid once per ring, not per stage.
+        //
+        // Per item, each lane precomputes the scale rows it fetches:
+        //   lane side (A operand): activation rows lane+32i (normal), or the
+        //     (n-block, chunk) pair `lane` of the tile (swap);
+        //   column side (B operand): the (n-block, chunk) pair `lane`
+        //     (normal), or (token, chunk) pairs lane+32j (swap).
+        constexpr int kNld = C::kNld;
+        constexpr int kLaneLoads = kSwap ? 1 : 4;        // source rows per lane
+        constexpr int kLaneChunks = kSwap ? 1 : kNld;    // chunks fetched per source row
+        constexpr int kColLoads = kSwap ? (BN * kNld + 31) / 32 : 1;
         ptx::grid_dependency_wait();
-        const bool blk128 = a.blk_k == 128;
-        const int nld = blk128 ? 1 : 4;           // distinct scale chunks per stage
-        auto issue_raw = [&](SfSlot<BN>& slot, const JobIter& j) {
-            const int q0 = j.kb * 4;
-            const int nq = min(4, (a.K - j.kb * kBK) / 32);
+        const float* lane_src[kLaneLoads];
+        uint32_t lane_dst[kLaneLoads];
+        int lane_chunk[kLaneLoads];
+        const float* col_src[kColLoads];
+        uint32_t col_dst[kColLoads];
+        int col_chunk[kColLoads];
+        auto setup_item = [&](const JobIter& j) {
             const int row0 = j.tr * kBM, col0 = j.tc * BN;
             if (!kSwap) {
-                // A operand = activation rows: one scale per row and chunk
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int r = lane + 32 * i, g = row0 + r;
-                    for (int c = 0; c < nld; ++c) {
-                        float* dst = &slot.lane_raw[c][r];
-                        if (c < nq && g < a.rows)
-                            ptx::cp_async_4(ptx::smem_u32(dst),
-                                            a.As + static_cast<int64_t>(g) * a.ks + ((q0 + c) * 32) / a.blk_k);
-                        else
-                            *dst = 1.0f;
-                    }
+                    const int g = row0 + lane + 32 * i;
+                    lane_src[i] = g < a.rows ? a.As + static_cast<int64_t>(g) * a.ks : nullptr;
+                    lane_dst[i] = ptx::smem_u32(&sf[0].lane_raw[0][lane + 32 * i]);
+                    lane_chunk[i] = 0;
                 }
-                // B operand = weight rows: one scale per n-block and chunk
-                const int ngrp = (BN + a.blk_n - 1) / a.blk_n;
-                for (int idx = lane; idx < ngrp * nld; idx += 32) {
-                    const int gi = idx / nld, c = idx - gi * nld, g = col0 + gi * a.blk_n;
-                    float* dst = &slot.col_raw[c][gi];
-                    if (c < nq && g < a.cols)
-                        ptx::cp_async_4(ptx::smem_u32(dst),
-                                        a.Ws + static_cast<int64_t>(g / a.blk_n) * a.ks + ((q0 + c) * 32) / a.blk_k);
-                    else
-                        *dst = 1.0f;
-                }
+                const int gi = lane / kNld, c = lane % kNld;
+                const int g = col0 + gi * kBlkN;
+                col_src[0] = (gi < C::kColGroups && g < a.cols)
+                                 ? a.Ws + static_cast<int64_t>(g / kBlkN) * a.ks + c : nullptr;
+                col_dst[0] = ptx::smem_u32(&sf[0].col_raw[c][gi < 64 ? gi : 0]);
+                col_chunk[0] = gi < C::kColGroups ? c : 4;
             } else {
-                // A operand = weight rows: one scale per n-block and chunk
-                const int nblk = kBM / a.blk_n;
-                for (int idx = lane; idx < nblk * nld; idx += 32) {
-                    const int bi = idx / nld, c = idx - bi * nld, g = row0 + bi * a.blk_n;
-                    float* dst = &slot.lane_raw[c][bi];
-                    if (c < nq && g < a.rows)
-                        ptx::cp_async_4(ptx::smem_u32(dst),
-                                        a.Ws + static_cast<int64_t>(g / a.blk_n) * a.ks + ((q0 + c) * 32) / a.blk_k);
-                    else
-                        *dst = 1.0f;
-                }
-                // B operand = token rows: one scale per token and chunk
-                for (int idx = lane; idx < BN * nld; idx += 32) {
-                    const int t = idx / nld, c = idx - t * nld, g = col0 + t;
-                    float* dst = &slot.col_raw[c][t];
-                    if (c < nq && g < a.cols)
-                        ptx::cp_async_4(ptx::smem_u32(dst),
-                                        a.As + static_cast<int64_t>(g) * a.ks + ((q0 + c) * 32) / a.blk_k);
-                    else
-                        *dst = 1.0f;
+                const int bi = lane / kNld, c = lane % kNld;
+                const int g = row0 + bi * kBlkN;
+                lane_src[0] = (bi < C::kLaneGroups && g < a.rows)
+                                  ? a.Ws + static_cast<int64_t>(g / kBlkN) * a.ks + c : nullptr;
+                lane_dst[0] = ptx::smem_u32(&sf[0].lane_raw[c][bi < 128 ? bi : 0]);
+                lane_chunk[0] = bi < C::kLaneGroups ? c : 4;
+#pragma unroll
+                for (int jj = 0; jj < kColLoads; ++jj) {
+                    const int idx = lane + 32 * jj;
+                    const int t = idx / kNld, cc = idx % kNld;
+                    const int g = col0 + t;
+                    col_src[jj] = (t < BN && g < a.cols) ? a.As + static_cast<int64_t>(g) * a.ks + cc : nullptr;
+                    col_dst[jj] = ptx::smem_u32(&sf[0].col_raw[cc][t < 64 ? t : 0]);
+                    col_chunk[jj] = t < BN ? cc : 4;
                 }
             }
         };
+        // chunk == 4 marks a lane/slot with nothing to fetch
+        auto issue_raw = [&](int si, const JobIter& j) {
+            const uint32_t slot_off = static_cast<uint32_t>(si * sizeof(SfSlot<BN>));
+            const int nq = min(4, (a.K - j.kb * kBK) / 32);
+            const int soff = j.kb * C::kScalesPerStage;
+#pragma unroll
+            for (int i = 0; i < kLaneLoads; ++i) {
+                if (lane_chunk[i] >= 4) continue;
+#pragma unroll
+                for (int cc = 0; cc < kLaneChunks; ++cc) {
+                    // normal: chunk cc of row i lives at lane_raw[cc][row] (+512 B per chunk);
+                    // swap: this lane's (n-block, chunk) pair is fixed per item
+                    const int c = kSwap ? lane_chunk[i] : cc;
+                    const uint32_t dst = lane_dst[i] + slot_off + static_cast<uint32_t>(kSwap ? 0 : cc * 512);
+                    if (lane_src[i] != nullptr && c < nq)
+                        ptx::cp_async_4(dst, lane_src[i] + soff + (kSwap ? 0 : cc));
+                    else
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst), "f"(1.0f) : "memory");
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kColLoads; ++i) {
+                if (col_chunk[i] >= 4) continue;
+                if (col_src[i] != nullptr && col_chunk[i] < nq)
+                    ptx::cp_async_4(col_dst[i] + slot_off, col_src[i] + soff);
+                else
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(col_dst[i] + slot_off), "f"(1.0f) : "memory");
+            }
+        };
         auto convert = [&](SfSlot<BN>& slot) {
-            bool ok = true;
+            uint32_t bad = 0;
             uint32_t w4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = lane + 32 * i;
-                const int li = kSwap ? r / a.blk_n : r;
+                const int li = kSwap ? r / kBlkN : r;
                 uint32_t word = 0;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float s = slot.lane_raw[blk128 ? 0 : j][li];
-                    ok &= is_pow2_scale(s);
-                    word |= ((__float_as_uint(s) >> 23) & 0xFFu) << (8 * j);
+                    const uint32_t b = __float_as_uint(slot.lane_raw[kNld == 1 ? 0 : j][li]);
+                    bad |= scale_bad_bits(b);
+                    word |= (b >> 23) << (8 * j);
                 }
                 w4[i] = word;
             }
@@ -381,13 +404,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const int c = h * 128 + lane + 32 * i;
                     uint32_t word = 0x7F7F7F7Fu;   // 2^0 for rows past the tile
                     if (c < BN) {
-                        const int ci = kSwap ? c : c / a.blk_n;
+                        const int ci = kSwap ? c : c / kBlkN;
                         word = 0;
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const float s = slot.col_raw[blk128 ? 0 : j][ci];
-                            ok &= is_pow2_scale(s);
-                            word |= ((__float_as_uint(s) >> 23) & 0xFFu) << (8 * j);
+                            const uint32_t b = __float_as_uint(slot.col_raw[kNld == 1 ? 0 : j][ci]);
+                            bad |= scale_bad_bits(b);
+                            word |= (b >> 23) << (8 * j);
                         }
                     }
                     w4[i] = word;
@@ -395,12 +418,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 *reinterpret_cast<uint4*>(&slot.sfb[h * 128 + lane * 4]) =
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            const bool all_ok = __all_sync(0xFFFFFFFFu, ok);
+            const bool all_ok = __all_sync(0xFFFFFFFFu, bad == 0u);
             if (lane == 0) slot.pow2 = all_ok ? 1u : 0u;
         };
         JobIter iss, fin;
         iss.begin(a);
         fin.begin(a);
+        if (iss.valid(a)) setup_item(iss);
         uint32_t n_iss = 0, n_fin = 0;
         bool failed = false;
         while (fin.valid(a) && !failed) {
@@ -413,10 +437,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     failed = true;
                     break;
                 }
-                issue_raw(sf[si], iss);
+                issue_raw(si, iss);
                 ptx::cp_async_commit();
                 ++n_iss;
-                iss.next(a);
+                if (iss.next(a) && iss.valid(a)) setup_item(iss);
             }
             if (failed) break;
             const int sf_i = static_cast<int>(n_fin % kStages);
@@ -433,16 +457,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        const uint32_t idesc_f8 = ptx::idesc_f8(kBM, BN);
-        const uint32_t idesc_mx = ptx::idesc_mxf8(kBM, BN);
+        constexpr uint32_t idesc_f8 = ptx::idesc_f8(kBM, BN);
+        constexpr uint32_t idesc_mx = ptx::idesc_mxf8(kBM, BN);
         const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
-        const int col_group = kSwap ? 1 : a.blk_n;
+        constexpr int kColGroup = kSwap ? 1 : kBlkN;
         JobIter it;
         it.begin(a);
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t seg = 0;     // accumulator segments issued so far
-        uint32_t mx_used = 0; // block-scaled stages issued so far (scale-slot parity)
+        uint32_t seg = 0;      // accumulator segments issued so far
+        uint32_t mx_used = 0;  // block-scaled stages issued so far (scale-slot parity)
         bool failed = false;
         bool seg_open = false;
         bool first = true;
@@ -451,12 +475,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // Hands the open accumulator segment to the epilogue.
         auto close_segment = [&](uint32_t flags) {
             const int b = acc_buf(seg);
-            if (lane == 0) info[b].flags = flags;
-            __syncwarp();
             if (lane == 0) {
+                info[b].flags = flags;
                 ptx::mbar_arrive(accf_bar(b));
                 ptx::tc_commit(accf_bar(b));
             }
+            __syncwarp();
             ++seg;
         };
         while (it.valid(a) && !failed) {
@@ -485,11 +509,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                 ptx::smem_desc(ptx::smem_u32(slot.sfb + 128 * h), 128, 128,
                                                                ptx::kLayoutNone));
                     const uint32_t d = tmem + static_cast<uint32_t>(acc_buf(seg) * BN);
+                    const uint64_t ad0 = ptx::smem_desc(a_st, 16, 1024, ptx::kLayoutSw128);
+                    const uint64_t bd0 = ptx::smem_desc(b_st, 16, 1024, ptx::kLayoutSw128);
                     for (int j = 0; j < nq; ++j) {
-                        const uint64_t ad = ptx::smem_desc(a_st + 32u * j, 16, 1024, ptx::kLayoutSw128);
-                        const uint64_t bd = ptx::smem_desc(b_st + 32u * j, 16, 1024, ptx::kLayoutSw128);
-                        ptx::mma_mxf8(d, ad, bd, ptx::idesc_sf_ids(idesc_mx, j, j), t_sfa, t_sfb,
-                                      first ? 0u : 1u);
+                        // +32 bytes along K inside the swizzle atom = +2 in the start field
+                        ptx::mma_mxf8(d, ad0 + 2u * j, bd0 + 2u * j, ptx::idesc_sf_ids(idesc_mx, j, j), t_sfa,
+                                      t_sfb, first ? 0u : 1u);
                         first = false;
                     }
                 }
@@ -499,30 +524,32 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     close_segment(0u);
                     seg_open = false;
                 }
-                const int ngroups = a.blk_k == 128 ? 1 : nq;
-                const int steps = a.blk_k == 128 ? nq : 1;
+                constexpr bool kBlk128 = kBlkK == 128;
+                const int ngroups = kBlk128 ? 1 : nq;
+                const int steps = kBlk128 ? nq : 1;
                 for (int gidx = 0; gidx < ngroups; ++gidx) {
                     const int b = acc_buf(seg);
                     if (!wait_bar(acce_bar(b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     const int j = gidx;  // scale chunk (blk_k == 128: chunk 0 holds the block scale)
                     for (int r = lane; r < 128; r += 32)
-                        info[b].lane_s[r] = slot.lane_raw[j][kSwap ? r / a.blk_n : r];
-                    for (int c = lane; c < BN; c += 32) info[b].col_s[c] = slot.col_raw[j][c / col_group];
+                        info[b].lane_s[r] = slot.lane_raw[j][kSwap ? r / kBlkN : r];
+                    for (int c = lane; c < BN; c += 32) info[b].col_s[c] = slot.col_raw[j][c / kColGroup];
                     const bool last = it.last_kb() && gidx == ngroups - 1;
                     if (lane == 0) info[b].flags = kInfoPromote | (last ? kInfoLast : 0u);
                     __syncwarp();
                     if (lane == 0) {
                         const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                        const uint64_t ad0 = ptx::smem_desc(a_st, 16, 1024, ptx::kLayoutSw128);
+                        const uint64_t bd0 = ptx::smem_desc(b_st, 16, 1024, ptx::kLayoutSw128);
                         for (int t = 0; t < steps; ++t) {
                             const int jj = gidx * steps + t;   // 32-wide chunk inside the stage
-                            const uint64_t ad = ptx::smem_desc(a_st + 32u * jj, 16, 1024, ptx::kLayoutSw128);
-                            const uint64_t bd = ptx::smem_desc(b_st + 32u * jj, 16, 1024, ptx::kLayoutSw128);
-                            ptx::mma_f8(d, ad, bd, idesc_f8, t > 0 ? 1u : 0u);
+                            ptx::mma_f8(d, ad0 + 2u * jj, bd0 + 2u * jj, idesc_f8, t > 0 ? 1u : 0u);
                         }
                         ptx::mbar_arrive(accf_bar(b));
                         ptx::tc_commit(accf_bar(b));
                     }
+                    __syncwarp();
                     ++seg;
                 }
                 if (failed) break;
@@ -666,8 +693,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             }
             // advance to the next item (skip the remaining k-stages of this one)
-            const int cur = it.item;
-            while (it.valid(a) && it.item == cur) it.next(a);
+            while (it.valid(a) && !it.next(a)) {
+            }
         }
     }
 
@@ -679,128 +706,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
 }
 
-// ======================================================================== host
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-sgq_status get_encoder() {
-    std::call_once(g_encode_once, [] {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    return g_encode ? SGQ_OK : SGQ_ERR_CUDA;
-}
-
-// 2-D map over a [rows, K] uint8 matrix, box = 128 K-bytes x box_rows rows,
-// 128-byte swizzle (the UMMA K-major SW128 layout).
-sgq_status make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int box_rows) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
-}
-
-// Split-K workspace, one per device, created on first need.
-constexpr size_t kWsBytes = size_t(64) << 20;
-constexpr int kMaxCounters = 1 << 16;
-struct DevWs {
-    float* partial = nullptr;
-    uint32_t* counters = nullptr;
-};
-DevWs g_ws[64];
-std::mutex g_ws_mu;
-
-sgq_status get_workspace(cudaStream_t st, DevWs* out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_ws_mu);
-    if (!g_ws[dev].partial) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return SGQ_ERR_CUDA;
-        if (cs != cudaStreamCaptureStatusNone) return SGQ_ERR_UNSUPPORTED;
-        void* p = nullptr;
-        void* c = nullptr;
-        if (cudaMalloc(&p, kWsBytes) != cudaSuccess) return SGQ_ERR_CUDA;
-        if (cudaMalloc(&c, kMaxCounters * sizeof(uint32_t)) != cudaSuccess) {
-            cudaFree(p);
-            return SGQ_ERR_CUDA;
-        }
-        if (cudaMemset(c, 0, kMaxCounters * sizeof(uint32_t)) != cudaSuccess ||
-            cudaDeviceSynchronize() != cudaSuccess) {
-            cudaFree(p);
-            cudaFree(c);
-            return SGQ_ERR_CUDA;
-        }
-        g_ws[dev].partial = static_cast<float*>(p);
-        g_ws[dev].counters = static_cast<uint32_t*>(c);
-    }
-    *out = g_ws[dev];
-    return SGQ_OK;
-}
-
-struct Plan {
-    bool swap;
-    int bn, tiles_r, tiles_c, kb_total, kb_per_split, splits, items, grid;
-};
-
-int env_int(const char* name, int dflt) {
-    const char* v = std::getenv(name);
-    return v ? std::atoi(v) : dflt;
-}
-
-Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
-    Plan p{};
-    p.swap = M <= 64;
-    p.bn = p.swap ? (M <= 16 ? 16 : (M <= 32 ? 32 : 64)) : 256;
-    const int64_t rows = p.swap ? N : M, cols = p.swap ? M : N;
-    p.tiles_r = static_cast<int>((rows + kBM - 1) / kBM);
-    p.tiles_c = static_cast<int>((cols + p.bn - 1) / p.bn);
-    p.kb_total = static_cast<int>((K + kBK - 1) / kBK);
-    const int64_t tiles = int64_t(p.tiles_r) * p.tiles_c;
-    static const int ovh = env_int("SGQ_SPLIT_OVERHEAD", 2);
-    static const int forced = env_int("SGQ_SPLITS", 0);
-    int best_s = 1;
-    double best = 1e300;
-    const int max_s = p.kb_total < 32 ? p.kb_total : 32;
-    for (int s = 1; s <= max_s; ++s) {
-        const int kbp = (p.kb_total + s - 1) / s;
-        if ((p.kb_total + kbp - 1) / kbp != s) continue;   // every split non-empty
-        const int64_t items = tiles * s;
-        if (s > 1 && (tiles > kMaxCounters ||
-                      size_t(items) * kBM * p.bn * sizeof(float) > kWsBytes))
-            continue;
-        const int64_t waves = (items + sm_count - 1) / sm_count;
-        const double cost = double(waves) * (kbp + ovh) + (s > 1 ? 0.5 : 0.0);
-        if (forced > 0 ? s == forced : cost < best) {
-            best = cost;
-            best_s = s;
-        }
-    }
-    p.splits = best_s;
-    p.kb_per_split = (p.kb_total + best_s - 1) / best_s;
-    p.items = static_cast<int>(tiles * best_s);
-    p.grid = p.items < sm_count ? p.items : sm_count;
-    return p;
-}
-
-template <int BN, int kStages, bool kSwap, int kAccBufs>
-sgq_status run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int grid,
-               cudaStream_t st) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs>;
-    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs>;
+// Launches one instantiation with programmatic stream serialisation.
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK>
+sgq_status run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int grid, cudaStream_t st) {
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK>;
+    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK>;
     static bool configured[64] = {};
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    if (!configured[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(C::kSmem)) != cudaSuccess)
             return SGQ_ERR_CUDA;
@@ -821,73 +735,22 @@ sgq_status run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& arg
     return SGQ_OK;
 }
 
-}  // namespace
-
-sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq, const float* Ws,
-                                 void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
-                                 uint32_t flags, cudaStream_t st) {
-    if (get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
-    DeviceInfo di;
-    sgq_status rc = device_info(&di);
-    if (rc != SGQ_OK) return rc;
-    if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
-    const Plan p = make_plan(M, N, K, di.sm_count);
-    GemmArgs a{};
-    a.As = As;
-    a.Ws = Ws;
-    a.D = static_cast<__nv_bfloat16*>(D);
-    a.M = static_cast<int>(M);
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.blk_n = blk_n;
-    a.blk_k = blk_k;
-    a.ks = static_cast<int>(K / blk_k);
-    a.rows = static_cast<int>(p.swap ? N : M);
-    a.cols = static_cast<int>(p.swap ? M : N);
-    a.tiles_r = p.tiles_r;
-    a.tiles_c = p.tiles_c;
-    a.kb_total = p.kb_total;
-    a.kb_per_split = p.kb_per_split;
-    a.splits = p.splits;
-    a.items = p.items;
-    a.group_r = 16;
-    a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
-    if (p.splits > 1) {
-        DevWs ws;
-        rc = get_workspace(st, &ws);
-        if (rc != SGQ_OK) return rc;
-        a.partial = ws.partial;
-        a.counters = ws.counters;
-    }
-    CUtensorMap ta, tb;
-    const void* opA = p.swap ? Wq : Aq;
-    const void* opB = p.swap ? Aq : Wq;
-    if (make_tmap(&ta, opA, a.rows, K, kBM) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (make_tmap(&tb, opB, a.cols, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (!p.swap) return run<256, 4, false, 1>(ta, tb, a, p.grid, st);
-    switch (p.bn) {
-        case 16: return run<16, 8, true, 2>(ta, tb, a, p.grid, st);
-        case 32: return run<32, 8, true, 2>(ta, tb, a, p.grid, st);
-        default: return run<64, 7, true, 2>(ta, tb, a, p.grid, st);
+// One translation unit per [blk_n, blk_k] recipe instantiates all tile shapes.
+template <int kBlkN, int kBlkK>
+sgq_status dispatch(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                    int grid, cudaStream_t st) {
+    if (!swap) return run<256, 4, false, 1, kBlkN, kBlkK>(ta, tb, a, grid, st);
+    switch (bn) {
+        case 16: return run<16, 8, true, 2, kBlkN, kBlkK>(ta, tb, a, grid, st);
+        case 32: return run<32, 8, true, 2, kBlkN, kBlkK>(ta, tb, a, grid, st);
+        default: return run<64, 7, true, 2, kBlkN, kBlkK>(ta, tb, a, grid, st);
     }
 }
 
-sgq_status read_and_clear_device_status(cudaStream_t st) {
-    if (cudaStreamSynchronize(st) != cudaSuccess) return SGQ_ERR_CUDA;
-    uint32_t v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(v)) != cudaSuccess) return SGQ_ERR_CUDA;
-    if (v == 0) return SGQ_OK;
-    const uint32_t zero = 0;
-    if (cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(zero)) != cudaSuccess) return SGQ_ERR_CUDA;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && g_ws[dev].counters) {
-        // an aborted split-K launch may have left arrival counts behind
-        if (cudaMemset(g_ws[dev].counters, 0, kMaxCounters * sizeof(uint32_t)) != cudaSuccess ||
-            cudaDeviceSynchronize() != cudaSuccess)
-            return SGQ_ERR_CUDA;
-    }
-    return (v & kStatusTimeout) ? SGQ_ERR_TIMEOUT : SGQ_ERR_CUDA;
-}
+sgq_status dispatch_32_32(bool, int, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_32_128(bool, int, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_128_32(bool, int, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_128_128(bool, int, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 
+}  // namespace gemm
 }  // namespace sgq
