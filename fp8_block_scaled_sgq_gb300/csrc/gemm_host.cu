@@ -14,6 +14,9 @@
 namespace sgq {
 
 __device__ uint32_t g_gemm_status;
+#ifdef SGQ_TRACE
+__device__ unsigned long long g_gemm_trace[1024 * gemm::kTraceSlots];
+#endif
 
 namespace gemm {
 namespace {
@@ -178,6 +181,13 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
     rc = gemm::status_word(&a.status);
     if (rc != SGQ_OK) return rc;
+#ifdef SGQ_TRACE
+    {
+        void* tp = nullptr;
+        if (cudaGetSymbolAddress(&tp, g_gemm_trace) != cudaSuccess) return SGQ_ERR_CUDA;
+        a.trace = static_cast<unsigned long long*>(tp);
+    }
+#endif
     if (p.splits > 1) {
         gemm::DevWs ws;
         rc = gemm::get_workspace(st, &ws);
@@ -215,3 +225,15 @@ sgq_status read_and_clear_device_status(cudaStream_t st) {
 }
 
 }  // namespace sgq
+
+#ifdef SGQ_TRACE
+// Development builds only: copies the per-CTA event trace of the last GEMM.
+extern "C" int sgq_trace_read(void* host, uint64_t bytes) {
+    if (bytes > sizeof(unsigned long long) * 1024 * sgq::gemm::kTraceSlots) return 1;
+    return cudaMemcpyFromSymbol(host, sgq::g_gemm_trace, bytes) == cudaSuccess ? 0 : 4;
+}
+extern "C" int sgq_trace_clear(void) {
+    static unsigned long long zeros[1024 * sgq::gemm::kTraceSlots];
+    return cudaMemcpyToSymbol(sgq::g_gemm_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 4;
+}
+#endif

@@ -81,6 +81,7 @@ struct GemmArgs {
     float* partial;       // split-K workspace
     uint32_t* counters;   // split-K arrival counters (self-resetting)
     uint32_t* status;     // device status word
+    unsigned long long* trace;  // per-CTA event timestamps (SGQ_TRACE builds only)
     int M, N, K, ks;      // ks = K / blk_k (columns of As and Ws)
     int rows, cols;       // extents of the MMA A operand and B operand
     int tiles_r, tiles_c, kb_total, kb_per_split, splits, items, group_r;
@@ -121,6 +122,19 @@ struct JobIter {
         return false;
     }
 };
+
+// Optional event trace for development builds (-DSGQ_TRACE): one row of
+// kTraceSlots globaltimer stamps per CTA.  Compiled out otherwise.
+constexpr int kTraceSlots = 256;
+__device__ __forceinline__ void trace_ev(const GemmArgs& a, int slot) {
+#ifdef SGQ_TRACE
+    if (a.trace != nullptr && slot >= 0 && slot < kTraceSlots)
+        a.trace[blockIdx.x * kTraceSlots + slot] = ptx::globaltimer();
+#else
+    (void)a;
+    (void)slot;
+#endif
+}
 
 struct Sync {
     volatile uint32_t* abort_flag;
@@ -251,6 +265,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
+    if (threadIdx.x == 0) trace_ev(a, 0);
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
@@ -276,14 +291,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 ++npre;
             }
             ptx::grid_dependency_wait();
+            trace_ev(a, 1);
             for (int s = 0; s < npre; ++s) {
                 ptx::tma_load_2d(x_dst(s), tmX, it.kb * kBK, x_row(it), full_bar(s));
                 it.next(a);
             }
             int stage = npre % kStages;
             uint32_t phase = npre / kStages;
+            int nj = npre;
             while (it.valid(a)) {
                 if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 1)) break;
+                trace_ev(a, 2 + (nj++ & 31));
                 ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
                 ptx::tma_load_2d(w_dst(stage), tmW, it.kb * kBK, w_row(it), full_bar(stage));
                 ptx::tma_load_2d(x_dst(stage), tmX, it.kb * kBK, x_row(it), full_bar(stage));
@@ -449,7 +467,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             convert(sf[sf_i]);
             ptx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(full_bar(sf_i));
+            if (lane == 0) {
+                ptx::mbar_arrive(full_bar(sf_i));
+                trace_ev(a, 64 + (n_fin & 31));
+            }
             ++n_fin;
             fin.next(a);
         }
@@ -467,6 +488,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         uint32_t phase = 0;
         uint32_t seg = 0;      // accumulator segments issued so far
         uint32_t mx_used = 0;  // block-scaled stages issued so far (scale-slot parity)
+        uint32_t mma_jobs = 0;
         bool failed = false;
         bool seg_open = false;
         bool first = true;
@@ -486,6 +508,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         while (it.valid(a) && !failed) {
             if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
             ptx::tc_fence_after();
+            if (lane == 0) trace_ev(a, 32 + (mma_jobs++ & 31));
             SfSlot<BN>& slot = sf[stage];
             const int nq = min(4, (a.K - it.kb * kBK) / 32);
             const uint32_t a_st = sA0 + stage * C::kABytes;
@@ -584,6 +607,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         JobIter it;
         it.begin(a);
         uint32_t seg = 0;
+        uint32_t n_items = 0;
         float acc[kCols];
         while (it.valid(a)) {
             bool failed = false;
@@ -620,6 +644,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (flags & kInfoLast) break;
             }
             if (epi_any(failed || *sync.abort_flag)) break;
+            if (epi_tid == 0) trace_ev(a, 96 + 4 * (n_items & 31));
             // ------------------------------------------------ output
             const int row0 = it.tr * kBM, col0 = it.tc * BN;
             const int grow = row0 + r_in_tile;   // global row of the MMA A operand
@@ -635,6 +660,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 __threadfence();
                 epi_sync();
                 if (epi_tid == 0) {
+                    trace_ev(a, 97 + 4 * (n_items & 31));
                     const uint32_t old = atomicAdd(a.counters + it.tile, 1u);
                     misc[2] = (old == static_cast<uint32_t>(a.splits - 1)) ? 1u : 0u;
                 }
@@ -692,6 +718,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
+            if (epi_tid == 0) trace_ev(a, 98 + 4 * (n_items & 31));
+            ++n_items;
             // advance to the next item (skip the remaining k-stages of this one)
             while (it.valid(a) && !it.next(a)) {
             }
@@ -700,6 +728,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) trace_ev(a, 255);
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
