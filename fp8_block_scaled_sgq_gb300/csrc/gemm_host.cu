@@ -49,6 +49,19 @@ sgq_status make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, i
     return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
 }
 
+// 2-D map over a [rows, ks] fp32 scale matrix; box = 4 columns (16 bytes) x
+// box_rows rows, no swizzle.  Rows past the matrix read as zero.
+sgq_status make_scale_map(CUtensorMap* m, const float* ptr, int64_t rows, int64_t ks, int box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(ks), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ks) * sizeof(float)};
+    cuuint32_t box[2] = {4u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
+}
+
 // Split-K workspace, one per device, created on first need.
 constexpr size_t kWsBytes = size_t(64) << 20;
 constexpr int kMaxCounters = 1 << 16;
@@ -195,15 +208,28 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
         a.partial = ws.partial;
         a.counters = ws.counters;
     }
-    CUtensorMap ta, tb;
+    // maps: A operand, B operand, A-operand scales, B-operand scales
+    CUtensorMap maps[4];
     const void* opA = p.swap ? Wq : Aq;
     const void* opB = p.swap ? Aq : Wq;
-    if (gemm::make_tmap(&ta, opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (gemm::make_tmap(&tb, opB, a.cols, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.bn, ta, tb, a, p.grid, st);
-    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.bn, ta, tb, a, p.grid, st);
-    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.bn, ta, tb, a, p.grid, st);
-    return gemm::dispatch_128_128(p.swap, p.bn, ta, tb, a, p.grid, st);
+    if (gemm::make_tmap(&maps[0], opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+    // Scale rows are TMA-loadable when their pitch is a multiple of 16 bytes.
+    const bool scale_tma = (a.ks % 4) == 0;
+    maps[2] = maps[0];
+    maps[3] = maps[1];
+    if (scale_tma) {
+        const int64_t nb = (N + blk_n - 1) / blk_n;
+        if (gemm::make_scale_map(&maps[2], p.swap ? Ws : As, p.swap ? nb : M, a.ks,
+                                 p.swap ? gemm::kBM / blk_n : gemm::kBM) != SGQ_OK ||
+            gemm::make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks,
+                                 p.swap ? p.bn : p.bn / blk_n) != SGQ_OK)
+            return SGQ_ERR_CUDA;
+    }
+    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+    return gemm::dispatch_128_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
 }
 
 sgq_status read_and_clear_device_status(cudaStream_t st) {

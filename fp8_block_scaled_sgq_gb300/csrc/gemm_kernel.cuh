@@ -61,9 +61,15 @@ template <int BN>
 struct alignas(128) SfSlot {
     uint32_t sfa[128];                  // UE8M0 words of the A operand (tcgen05.cp order)
     uint32_t sfb[BN < 128 ? 128 : BN];  // UE8M0 words of the B operand
-    float lane_raw[4][128];             // fp32 scales of the A operand, per chunk
-    float col_raw[4][64];               // fp32 scales of the B operand, per chunk
+    // Raw fp32 scales of the stage, one row per scale row and 4 columns:
+    //   lane_raw: A operand -- activation rows (normal) or weight n-blocks (swap)
+    //   col_raw:  B operand -- weight n-blocks (normal) or tokens (swap)
+    // Column j holds 32-wide K chunk j; when one scale covers the whole stage
+    // (blk_k = 128) it sits in column `kcol`.
+    float lane_raw[128][4];
+    float col_raw[64][4];
     uint32_t pow2;                      // every scale of the stage is 2^e
+    uint32_t kcol;
 };
 
 template <int BN>
@@ -185,7 +191,7 @@ __device__ __forceinline__ uint32_t scale_bad_bits(uint32_t b) {
     return (b & 0x807FFFFFu) | static_cast<uint32_t>(e == 0u || e == 0xFFu);
 }
 
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK>
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
 struct Cfg {
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
@@ -197,12 +203,16 @@ struct Cfg {
     static constexpr int kScalesPerStage = kBK / kBlkK;  // As/Ws columns per stage
     static constexpr int kColGroups = kSwap ? BN : (BN + kBlkN - 1) / kBlkN;
     static constexpr int kLaneGroups = kSwap ? kBM / kBlkN : kBM;
+    // rows of the scale boxes loaded per stage (16 bytes = 4 scale columns each)
+    static constexpr int kLaneScaleRows = kSwap ? kBM / kBlkN : kBM;
+    static constexpr int kColScaleRows = kSwap ? BN : (BN + kBlkN - 1) / kBlkN;
+    static constexpr uint32_t kScaleBytes = 16u * (kLaneScaleRows + kColScaleRows);
     static constexpr size_t kOffA = 0;
     static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
     static constexpr size_t kOffSf = kOffB + size_t(kStages) * kBBytes;
     static constexpr size_t kOffInfo = kOffSf + size_t(kStages) * sizeof(SfSlot<BN>);
     static constexpr size_t kOffBar = kOffInfo + size_t(kAccBufs) * sizeof(Info<BN>);
-    static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;
+    static constexpr int kNumBars = 3 * kStages + 2 * kAccBufs + 1;
     static constexpr size_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr size_t kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
@@ -213,11 +223,12 @@ struct Cfg {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK>
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
 __global__ void __launch_bounds__(kNumThreads, 1)
-    fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK>;
+    fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                          const GemmArgs a) {
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,6 +246,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kStages + kAccBufs + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
+    auto sraw_bar = [&](int s) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 1 + s); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -250,12 +262,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_init(acce_bar(b), 8);   // one arrive per epilogue warp
         }
         ptx::mbar_init(drain_bar, 1);
+        for (int s = 0; s < kStages; ++s) ptx::mbar_init(sraw_bar(s), 1);   // raw scales landed (TMA)
         misc[1] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        if (kScaleTma) {
+            ptx::prefetch_tmap(&tmSA);
+            ptx::prefetch_tmap(&tmSB);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
@@ -265,7 +282,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
-    if (threadIdx.x == 0) trace_ev(a, 0);
+    if (threadIdx.x == 0) {
+        trace_ev(a, 0);
+        // The next kernel on the stream may launch now; it still waits for this
+        // grid to finish (griddepcontrol.wait) before touching its outputs.
+        ptx::launch_dependents();
+    }
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
@@ -275,25 +297,44 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (lane == 0) {
             const CUtensorMap* tmW = kSwap ? &tmA : &tmB;
             const CUtensorMap* tmX = kSwap ? &tmB : &tmA;
+            const CUtensorMap* tmWs = kSwap ? &tmSA : &tmSB;   // weight scales
+            const CUtensorMap* tmXs = kSwap ? &tmSB : &tmSA;   // activation scales
             const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
             auto w_dst = [&](int s) { return kSwap ? sA0 + s * C::kABytes : sB0 + s * C::kBBytes; };
             auto x_dst = [&](int s) { return kSwap ? sB0 + s * C::kBBytes : sA0 + s * C::kABytes; };
             auto w_row = [&](const JobIter& j) { return kSwap ? j.tr * kBM : j.tc * BN; };
             auto x_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : j.tr * kBM; };
+            // scale boxes: 4 columns starting at a 16-byte aligned column
+            auto s_col = [&](const JobIter& j) { return (j.kb * C::kScalesPerStage) & ~3; };
+            auto ws_dst = [&](int s) { return ptx::smem_u32(kSwap ? &sf[s].lane_raw[0][0] : &sf[s].col_raw[0][0]); };
+            auto xs_dst = [&](int s) { return ptx::smem_u32(kSwap ? &sf[s].col_raw[0][0] : &sf[s].lane_raw[0][0]); };
+            auto ws_row = [&](const JobIter& j) { return kSwap ? j.tr * (kBM / kBlkN) : j.tc * (BN / kBlkN); };
+            auto xs_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : j.tr * kBM; };
+            auto load_w = [&](int s, const JobIter& j) {
+                ptx::mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
+                if (kScaleTma) {
+                    ptx::mbar_arrive_expect_tx(sraw_bar(s), C::kScaleBytes);
+                    ptx::tma_load_2d(ws_dst(s), tmWs, s_col(j), ws_row(j), sraw_bar(s));
+                }
+                ptx::tma_load_2d(w_dst(s), tmW, j.kb * kBK, w_row(j), full_bar(s));
+            };
+            auto load_x = [&](int s, const JobIter& j) {
+                if (kScaleTma) ptx::tma_load_2d(xs_dst(s), tmXs, s_col(j), xs_row(j), sraw_bar(s));
+                ptx::tma_load_2d(x_dst(s), tmX, j.kb * kBK, x_row(j), full_bar(s));
+            };
             JobIter it;
             it.begin(a);
             JobIter pre = it;
             int npre = 0;
             while (npre < kStages && pre.valid(a)) {
-                ptx::mbar_arrive_expect_tx(full_bar(npre), C::kStageBytes);
-                ptx::tma_load_2d(w_dst(npre), tmW, pre.kb * kBK, w_row(pre), full_bar(npre));
+                load_w(npre, pre);
                 pre.next(a);
                 ++npre;
             }
             ptx::grid_dependency_wait();
             trace_ev(a, 1);
             for (int s = 0; s < npre; ++s) {
-                ptx::tma_load_2d(x_dst(s), tmX, it.kb * kBK, x_row(it), full_bar(s));
+                load_x(s, it);
                 it.next(a);
             }
             int stage = npre % kStages;
@@ -301,10 +342,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int nj = npre;
             while (it.valid(a)) {
                 if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 1)) break;
-                trace_ev(a, 2 + (nj++ & 31));
-                ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-                ptx::tma_load_2d(w_dst(stage), tmW, it.kb * kBK, w_row(it), full_bar(stage));
-                ptx::tma_load_2d(x_dst(stage), tmX, it.kb * kBK, x_row(it), full_bar(stage));
+                trace_ev(a, 8 + (nj++ & 31));
+                load_w(stage, it);
+                load_x(stage, it);
                 it.next(a);
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
@@ -312,105 +352,34 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ---------------------------------------------------------- scale loader
-        // Two-phase software pipeline.  Issue: the raw fp32 scales of up to
-        // kStages jobs are fetched with cp.async (one commit group per job)
-        // as soon as their slot is free.  Finish: when the oldest job's copies
-        // have landed, its scales are checked for the power-of-two property,
-        // packed into UE8M0 words in tcgen05.cp order and handed to the MMA
-        // warp.  Global-load latency is paid once per ring, not per stage.
+        // Turns each stage's raw fp32 scales into UE8M0 words in tcgen05.cp
+        // order, checks the power-of-two property, and releases the stage to
+        // the MMA warp (second arrival on its full barrier).
         //
-        // Per item, each lane precomputes the scale rows it fetches:
-        //   lane side (A operand): activation rows lane+32i (normal), or the
-        //     (n-block, chunk) pair `lane` of the tile (swap);
-        //   column side (B operand): the (n-block, chunk) pair `lane`
-        //     (normal), or (token, chunk) pairs lane+32j (swap).
+        // Fast path (kScaleTma): the producer loads the raw scale boxes with
+        // TMA together with the operand tiles, so they arrive kStages ahead;
+        // this warp only converts.  Fallback (scale rows not 16-byte aligned):
+        // this warp fetches the raw scales itself with cp.async, up to kStages
+        // jobs ahead of the conversion.
         constexpr int kNld = C::kNld;
-        constexpr int kLaneLoads = kSwap ? 1 : 4;        // source rows per lane
-        constexpr int kLaneChunks = kSwap ? 1 : kNld;    // chunks fetched per source row
-        constexpr int kColLoads = kSwap ? (BN * kNld + 31) / 32 : 1;
-        ptx::grid_dependency_wait();
-        const float* lane_src[kLaneLoads];
-        uint32_t lane_dst[kLaneLoads];
-        int lane_chunk[kLaneLoads];
-        const float* col_src[kColLoads];
-        uint32_t col_dst[kColLoads];
-        int col_chunk[kColLoads];
-        auto setup_item = [&](const JobIter& j) {
+        auto convert = [&](SfSlot<BN>& slot, const JobIter& j, int kcol) {
             const int row0 = j.tr * kBM, col0 = j.tc * BN;
-            if (!kSwap) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int g = row0 + lane + 32 * i;
-                    lane_src[i] = g < a.rows ? a.As + static_cast<int64_t>(g) * a.ks : nullptr;
-                    lane_dst[i] = ptx::smem_u32(&sf[0].lane_raw[0][lane + 32 * i]);
-                    lane_chunk[i] = 0;
-                }
-                const int gi = lane / kNld, c = lane % kNld;
-                const int g = col0 + gi * kBlkN;
-                col_src[0] = (gi < C::kColGroups && g < a.cols)
-                                 ? a.Ws + static_cast<int64_t>(g / kBlkN) * a.ks + c : nullptr;
-                col_dst[0] = ptx::smem_u32(&sf[0].col_raw[c][gi < 64 ? gi : 0]);
-                col_chunk[0] = gi < C::kColGroups ? c : 4;
-            } else {
-                const int bi = lane / kNld, c = lane % kNld;
-                const int g = row0 + bi * kBlkN;
-                lane_src[0] = (bi < C::kLaneGroups && g < a.rows)
-                                  ? a.Ws + static_cast<int64_t>(g / kBlkN) * a.ks + c : nullptr;
-                lane_dst[0] = ptx::smem_u32(&sf[0].lane_raw[c][bi < 128 ? bi : 0]);
-                lane_chunk[0] = bi < C::kLaneGroups ? c : 4;
-#pragma unroll
-                for (int jj = 0; jj < kColLoads; ++jj) {
-                    const int idx = lane + 32 * jj;
-                    const int t = idx / kNld, cc = idx % kNld;
-                    const int g = col0 + t;
-                    col_src[jj] = (t < BN && g < a.cols) ? a.As + static_cast<int64_t>(g) * a.ks + cc : nullptr;
-                    col_dst[jj] = ptx::smem_u32(&sf[0].col_raw[cc][t < 64 ? t : 0]);
-                    col_chunk[jj] = t < BN ? cc : 4;
-                }
-            }
-        };
-        // chunk == 4 marks a lane/slot with nothing to fetch
-        auto issue_raw = [&](int si, const JobIter& j) {
-            const uint32_t slot_off = static_cast<uint32_t>(si * sizeof(SfSlot<BN>));
-            const int nq = min(4, (a.K - j.kb * kBK) / 32);
-            const int soff = j.kb * C::kScalesPerStage;
-#pragma unroll
-            for (int i = 0; i < kLaneLoads; ++i) {
-                if (lane_chunk[i] >= 4) continue;
-#pragma unroll
-                for (int cc = 0; cc < kLaneChunks; ++cc) {
-                    // normal: chunk cc of row i lives at lane_raw[cc][row] (+512 B per chunk);
-                    // swap: this lane's (n-block, chunk) pair is fixed per item
-                    const int c = kSwap ? lane_chunk[i] : cc;
-                    const uint32_t dst = lane_dst[i] + slot_off + static_cast<uint32_t>(kSwap ? 0 : cc * 512);
-                    if (lane_src[i] != nullptr && c < nq)
-                        ptx::cp_async_4(dst, lane_src[i] + soff + (kSwap ? 0 : cc));
-                    else
-                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst), "f"(1.0f) : "memory");
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kColLoads; ++i) {
-                if (col_chunk[i] >= 4) continue;
-                if (col_src[i] != nullptr && col_chunk[i] < nq)
-                    ptx::cp_async_4(col_dst[i] + slot_off, col_src[i] + soff);
-                else
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(col_dst[i] + slot_off), "f"(1.0f) : "memory");
-            }
-        };
-        auto convert = [&](SfSlot<BN>& slot) {
             uint32_t bad = 0;
             uint32_t w4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = lane + 32 * i;
                 const int li = kSwap ? r / kBlkN : r;
-                uint32_t word = 0;
+                const bool valid = (kSwap ? row0 + li * kBlkN : row0 + r) < a.rows;
+                uint32_t word = 0x7F7F7F7Fu;   // 2^0 for rows past the matrix
+                if (valid) {
+                    word = 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t b = __float_as_uint(slot.lane_raw[kNld == 1 ? 0 : j][li]);
-                    bad |= scale_bad_bits(b);
-                    word |= (b >> 23) << (8 * j);
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t b = __float_as_uint(slot.lane_raw[li][kNld == 1 ? kcol : q]);
+                        bad |= scale_bad_bits(b);
+                        word |= (b >> 23) << (8 * q);
+                    }
                 }
                 w4[i] = word;
             }
@@ -420,15 +389,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int c = h * 128 + lane + 32 * i;
-                    uint32_t word = 0x7F7F7F7Fu;   // 2^0 for rows past the tile
-                    if (c < BN) {
-                        const int ci = kSwap ? c : c / kBlkN;
+                    uint32_t word = 0x7F7F7F7Fu;
+                    const int ci = kSwap ? c : c / kBlkN;
+                    if (c < BN && (kSwap ? col0 + c : col0 + ci * kBlkN) < a.cols) {
                         word = 0;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t b = __float_as_uint(slot.col_raw[kNld == 1 ? 0 : j][ci]);
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t b = __float_as_uint(slot.col_raw[ci][kNld == 1 ? kcol : q]);
                             bad |= scale_bad_bits(b);
-                            word |= (b >> 23) << (8 * j);
+                            word |= (b >> 23) << (8 * q);
                         }
                     }
                     w4[i] = word;
@@ -437,44 +406,144 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
             const bool all_ok = __all_sync(0xFFFFFFFFu, bad == 0u);
-            if (lane == 0) slot.pow2 = all_ok ? 1u : 0u;
-        };
-        JobIter iss, fin;
-        iss.begin(a);
-        fin.begin(a);
-        if (iss.valid(a)) setup_item(iss);
-        uint32_t n_iss = 0, n_fin = 0;
-        bool failed = false;
-        while (fin.valid(a) && !failed) {
-            while (iss.valid(a) && n_iss - n_fin < static_cast<uint32_t>(kStages)) {
-                const int si = static_cast<int>(n_iss % kStages);
-                const uint32_t par = ((n_iss / kStages) & 1u) ^ 1u;
-                if (n_iss != n_fin) {
-                    if (!ptx::mbar_try_wait(empty_bar(si), par)) break;   // finish something first
-                } else if (!wait_bar(empty_bar(si), par, sync, 3)) {
-                    failed = true;
-                    break;
-                }
-                issue_raw(si, iss);
-                ptx::cp_async_commit();
-                ++n_iss;
-                if (iss.next(a) && iss.valid(a)) setup_item(iss);
-            }
-            if (failed) break;
-            const int sf_i = static_cast<int>(n_fin % kStages);
-            ptx::cp_async_wait_pending(static_cast<int>(n_iss - n_fin) - 1);
-            __syncwarp();
-            convert(sf[sf_i]);
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
             if (lane == 0) {
-                ptx::mbar_arrive(full_bar(sf_i));
-                trace_ev(a, 64 + (n_fin & 31));
+                slot.pow2 = all_ok ? 1u : 0u;
+                slot.kcol = static_cast<uint32_t>(kcol);
             }
-            ++n_fin;
-            fin.next(a);
+        };
+        if (kScaleTma) {
+            JobIter it;
+            it.begin(a);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t nfin = 0;
+            while (it.valid(a)) {
+                if (!wait_bar(sraw_bar(stage), phase, sync, 3)) break;
+                convert(sf[stage], it, kNld == 1 ? (it.kb & 3) : 0);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(full_bar(stage));
+                    trace_ev(a, 72 + (nfin & 31));
+                }
+                ++nfin;
+                it.next(a);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+        } else {
+            // Per item, each lane precomputes the scale rows it fetches:
+            //   lane side (A operand): activation rows lane+32i (normal), or the
+            //     (n-block, chunk) pair `lane` of the tile (swap);
+            //   column side (B operand): the (n-block, chunk) pair `lane`
+            //     (normal), or (token, chunk) pairs lane+32j (swap).
+            constexpr int kLaneLoads = kSwap ? 1 : 4;        // source rows per lane
+            constexpr int kLaneChunks = kSwap ? 1 : kNld;    // chunks fetched per source row
+            constexpr int kColLoads = kSwap ? (BN * kNld + 31) / 32 : 1;
+            ptx::grid_dependency_wait();
+            const float* lane_src[kLaneLoads];
+            uint32_t lane_dst[kLaneLoads];
+            int lane_chunk[kLaneLoads];
+            const float* col_src[kColLoads];
+            uint32_t col_dst[kColLoads];
+            int col_chunk[kColLoads];
+            auto setup_item = [&](const JobIter& j) {
+                const int row0 = j.tr * kBM, col0 = j.tc * BN;
+                if (!kSwap) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int g = row0 + lane + 32 * i;
+                        lane_src[i] = g < a.rows ? a.As + static_cast<int64_t>(g) * a.ks : nullptr;
+                        lane_dst[i] = ptx::smem_u32(&sf[0].lane_raw[lane + 32 * i][0]);
+                        lane_chunk[i] = 0;
+                    }
+                    const int gi = lane / kNld, c = lane % kNld;
+                    const int g = col0 + gi * kBlkN;
+                    col_src[0] = (gi < C::kColGroups && g < a.cols)
+                                     ? a.Ws + static_cast<int64_t>(g / kBlkN) * a.ks + c : nullptr;
+                    col_dst[0] = ptx::smem_u32(&sf[0].col_raw[gi < 64 ? gi : 0][c]);
+                    col_chunk[0] = gi < C::kColGroups ? c : 4;
+                } else {
+                    const int bi = lane / kNld, c = lane % kNld;
+                    const int g = row0 + bi * kBlkN;
+                    lane_src[0] = (bi < C::kLaneGroups && g < a.rows)
+                                      ? a.Ws + static_cast<int64_t>(g / kBlkN) * a.ks + c : nullptr;
+                    lane_dst[0] = ptx::smem_u32(&sf[0].lane_raw[bi < 128 ? bi : 0][c]);
+                    lane_chunk[0] = bi < C::kLaneGroups ? c : 4;
+#pragma unroll
+                    for (int jj = 0; jj < kColLoads; ++jj) {
+                        const int idx = lane + 32 * jj;
+                        const int t = idx / kNld, cc = idx % kNld;
+                        const int g = col0 + t;
+                        col_src[jj] = (t < BN && g < a.cols) ? a.As + static_cast<int64_t>(g) * a.ks + cc : nullptr;
+                        col_dst[jj] = ptx::smem_u32(&sf[0].col_raw[t < 64 ? t : 0][cc]);
+                        col_chunk[jj] = t < BN ? cc : 4;
+                    }
+                }
+            };
+            // chunk == 4 marks a lane/slot with nothing to fetch
+            auto issue_raw = [&](int si, const JobIter& j) {
+                const uint32_t slot_off = static_cast<uint32_t>(si * sizeof(SfSlot<BN>));
+                const int nq = min(4, (a.K - j.kb * kBK) / 32);
+                const int soff = j.kb * C::kScalesPerStage;
+#pragma unroll
+                for (int i = 0; i < kLaneLoads; ++i) {
+                    if (lane_chunk[i] >= 4) continue;
+#pragma unroll
+                    for (int cc = 0; cc < kLaneChunks; ++cc) {
+                        const int c = kSwap ? lane_chunk[i] : cc;
+                        const uint32_t dst = lane_dst[i] + slot_off + static_cast<uint32_t>(kSwap ? 0 : cc * 4);
+                        if (lane_src[i] != nullptr && c < nq)
+                            ptx::cp_async_4(dst, lane_src[i] + soff + (kSwap ? 0 : cc));
+                        else
+                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst), "f"(1.0f) : "memory");
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kColLoads; ++i) {
+                    if (col_chunk[i] >= 4) continue;
+                    if (col_src[i] != nullptr && col_chunk[i] < nq)
+                        ptx::cp_async_4(col_dst[i] + slot_off, col_src[i] + soff);
+                    else
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(col_dst[i] + slot_off), "f"(1.0f) : "memory");
+                }
+            };
+            JobIter iss, fin;
+            iss.begin(a);
+            fin.begin(a);
+            if (iss.valid(a)) setup_item(iss);
+            uint32_t n_iss = 0, n_fin = 0;
+            bool failed = false;
+            while (fin.valid(a) && !failed) {
+                while (iss.valid(a) && n_iss - n_fin < static_cast<uint32_t>(kStages)) {
+                    const int si = static_cast<int>(n_iss % kStages);
+                    const uint32_t par = ((n_iss / kStages) & 1u) ^ 1u;
+                    if (n_iss != n_fin) {
+                        if (!ptx::mbar_try_wait(empty_bar(si), par)) break;   // finish something first
+                    } else if (!wait_bar(empty_bar(si), par, sync, 3)) {
+                        failed = true;
+                        break;
+                    }
+                    issue_raw(si, iss);
+                    ptx::cp_async_commit();
+                    ++n_iss;
+                    if (iss.next(a) && iss.valid(a)) setup_item(iss);
+                }
+                if (failed) break;
+                const int sf_i = static_cast<int>(n_fin % kStages);
+                ptx::cp_async_wait_pending(static_cast<int>(n_iss - n_fin) - 1);
+                __syncwarp();
+                convert(sf[sf_i], fin, 0);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(full_bar(sf_i));
+                    trace_ev(a, 72 + (n_fin & 31));
+                }
+                ++n_fin;
+                fin.next(a);
+            }
+            ptx::cp_async_wait_pending(0);
         }
-        ptx::cp_async_wait_pending(0);
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -508,7 +577,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         while (it.valid(a) && !failed) {
             if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
             ptx::tc_fence_after();
-            if (lane == 0) trace_ev(a, 32 + (mma_jobs++ & 31));
+            if (lane == 0) trace_ev(a, 40 + (mma_jobs++ & 31));
             SfSlot<BN>& slot = sf[stage];
             const int nq = min(4, (a.K - it.kb * kBK) / 32);
             const uint32_t a_st = sA0 + stage * C::kABytes;
@@ -555,9 +624,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (!wait_bar(acce_bar(b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     const int j = gidx;  // scale chunk (blk_k == 128: chunk 0 holds the block scale)
+                    const int q = C::kNld == 1 ? static_cast<int>(slot.kcol) : j;
                     for (int r = lane; r < 128; r += 32)
-                        info[b].lane_s[r] = slot.lane_raw[j][kSwap ? r / kBlkN : r];
-                    for (int c = lane; c < BN; c += 32) info[b].col_s[c] = slot.col_raw[j][c / kColGroup];
+                        info[b].lane_s[r] = slot.lane_raw[kSwap ? r / kBlkN : r][q];
+                    for (int c = lane; c < BN; c += 32) info[b].col_s[c] = slot.col_raw[c / kColGroup][q];
                     const bool last = it.last_kb() && gidx == ngroups - 1;
                     if (lane == 0) info[b].flags = kInfoPromote | (last ? kInfoLast : 0u);
                     __syncwarp();
@@ -644,7 +714,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (flags & kInfoLast) break;
             }
             if (epi_any(failed || *sync.abort_flag)) break;
-            if (epi_tid == 0) trace_ev(a, 96 + 4 * (n_items & 31));
+            if (epi_tid == 0) trace_ev(a, 104 + 4 * (n_items & 31));
             // ------------------------------------------------ output
             const int row0 = it.tr * kBM, col0 = it.tc * BN;
             const int grow = row0 + r_in_tile;   // global row of the MMA A operand
@@ -660,7 +730,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 __threadfence();
                 epi_sync();
                 if (epi_tid == 0) {
-                    trace_ev(a, 97 + 4 * (n_items & 31));
+                    trace_ev(a, 105 + 4 * (n_items & 31));
                     const uint32_t old = atomicAdd(a.counters + it.tile, 1u);
                     misc[2] = (old == static_cast<uint32_t>(a.splits - 1)) ? 1u : 0u;
                 }
@@ -718,7 +788,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
-            if (epi_tid == 0) trace_ev(a, 98 + 4 * (n_items & 31));
+            if (epi_tid == 0) trace_ev(a, 106 + 4 * (n_items & 31));
             ++n_items;
             // advance to the next item (skip the remaining k-stages of this one)
             while (it.valid(a) && !it.next(a)) {
@@ -736,10 +806,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 }
 
 // Launches one instantiation with programmatic stream serialisation.
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK>
-sgq_status run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int grid, cudaStream_t st) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK>;
-    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK>;
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
+sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStream_t st) {
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma>;
+    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma>;
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
@@ -759,27 +829,34 @@ sgq_status run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& arg
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, args) != cudaSuccess) return SGQ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], args) != cudaSuccess)
+        return SGQ_ERR_CUDA;
     note_launch();
     return SGQ_OK;
 }
 
 // One translation unit per [blk_n, blk_k] recipe instantiates all tile shapes.
-template <int kBlkN, int kBlkK>
-sgq_status dispatch(bool swap, int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                    int grid, cudaStream_t st) {
-    if (!swap) return run<256, 4, false, 1, kBlkN, kBlkK>(ta, tb, a, grid, st);
+// maps: A operand, B operand, A-operand scales, B-operand scales.
+template <int kBlkN, int kBlkK, bool kScaleTma>
+sgq_status dispatch_tile(bool swap, int bn, const CUtensorMap* maps, const GemmArgs& a, int grid, cudaStream_t st) {
+    if (!swap) return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
     switch (bn) {
-        case 16: return run<16, 8, true, 2, kBlkN, kBlkK>(ta, tb, a, grid, st);
-        case 32: return run<32, 8, true, 2, kBlkN, kBlkK>(ta, tb, a, grid, st);
-        default: return run<64, 7, true, 2, kBlkN, kBlkK>(ta, tb, a, grid, st);
+        case 16: return run<16, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
+        case 32: return run<32, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
+        default: return run<64, 7, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
     }
 }
+template <int kBlkN, int kBlkK>
+sgq_status dispatch(bool swap, int bn, bool scale_tma, const CUtensorMap* maps, const GemmArgs& a, int grid,
+                    cudaStream_t st) {
+    return scale_tma ? dispatch_tile<kBlkN, kBlkK, true>(swap, bn, maps, a, grid, st)
+                     : dispatch_tile<kBlkN, kBlkK, false>(swap, bn, maps, a, grid, st);
+}
 
-sgq_status dispatch_32_32(bool, int, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_32_128(bool, int, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_128_32(bool, int, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_128_128(bool, int, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_32_32(bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_32_128(bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_128_32(bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_128_128(bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
 
 }  // namespace gemm
 }  // namespace sgq

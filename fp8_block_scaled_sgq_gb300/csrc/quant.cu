@@ -79,6 +79,10 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
                                                                 uint2* __restrict__ xq,
                                                                 float* __restrict__ xs,
                                                                 int64_t nvec) {
+    // Launched with programmatic stream serialisation: the launch overlaps the
+    // previous kernel on the stream, so wait for it before touching memory
+    // (x may be its output; xq/xs may still be read by it).
+    ptx::grid_dependency_wait();
     // Let a programmatically-dependent GEMM start its weight prefetch now; it
     // still waits for this grid to finish before it reads xq / xs.
     ptx::launch_dependents();
@@ -166,9 +170,18 @@ sgq_status launch_tg(const void* x, int64_t M, int64_t K, void* xq, float* xs, c
     int64_t blocks = (warps_needed + 7) / 8;
     const int64_t cap = static_cast<int64_t>(di.sm_count) * 8;
     if (blocks > cap) blocks = cap;
-    quant_token_group_kernel<G, U><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        static_cast<const uint4*>(x), static_cast<uint2*>(xq), xs, nvec);
-    if (cudaGetLastError() != cudaSuccess) return SGQ_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, quant_token_group_kernel<G, U>, static_cast<const uint4*>(x),
+                           static_cast<uint2*>(xq), xs, nvec) != cudaSuccess)
+        return SGQ_ERR_CUDA;
     note_launch();
     return SGQ_OK;
 }

@@ -120,9 +120,16 @@ sgq_status sgq_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n
  * When every scale of a 128-wide K step is an exact power of two (UE8M0),
  * the GEMM applies it inside the tensor-core block-scale MMA; any other fp32
  * scale is applied in an fp32 promotion step.  Both give the same result up
- * to fp32 rounding.  The GEMM may begin reading Wq and Ws before the
- * immediately preceding sgq_quant_token_group on the same stream has
- * finished (programmatic dependent launch); it reads Aq/As only after.
+ * to fp32 rounding.
+ *
+ * Launch overlap (programmatic dependent launch): the GEMM and
+ * sgq_quant_token_group are launched so that each may start while the
+ * previous kernel on the stream is still running.  sgq_quant_token_group
+ * touches memory only after that kernel has finished.  The GEMM starts
+ * reading Wq and Ws at once and reads Aq/As, and writes D, only after the
+ * previous kernel has finished -- so Wq/Ws must not be written by the kernel
+ * launched immediately before the GEMM on the same stream (a copy or memset
+ * of the weights is fine).
  */
 sgq_status sgq_fp8_block_gemm(const void* Aq, const float* As, const void* Wq,
                               const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
