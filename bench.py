@@ -207,24 +207,23 @@ def run_ours(args, ws_, rank, local):
     if sgq.sgq_device_status(sptr) != 0:
         raise SystemExit("device status not OK after warm-up")
 
-    def capture(fn):
-        graphs = []
-        for r in range(n_rot):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                with torch.cuda.graph(g, stream=stream):
-                    fn(r, torch.cuda.current_stream().cuda_stream)
-            graphs.append(g)
-        return graphs
-
-    graphs = capture(lambda r, sp: step_fn(sgq, per, *wrot[r], sp))
-    case_graphs = [capture(lambda r, sp, i=i: step_fn(sgq, per[i:i + 1], *wrot[r], sp, gemm_only=True))
-                   for i in range(len(per))]
-
-    def timed(gl, steps):
+    def capture(fn, steps):
+        """One CUDA graph holding exactly `steps` steps, weights rotating."""
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            for i in range(args.warmup):
-                gl[i % n_rot].replay()
+            with torch.cuda.graph(g, stream=stream):
+                sp = torch.cuda.current_stream().cuda_stream
+                for i in range(steps):
+                    fn(i % n_rot, sp)
+        return g
+
+    def full_step(r, sp):
+        step_fn(sgq, per, *wrot[r], sp)
+
+    def timed(g, steps):
+        # warm-up replay, then exactly one replay (= `steps` steps) between events
+        with torch.cuda.stream(stream):
+            g.replay()
         stream.synchronize()
         barrier(ws_)
         torch.cuda.synchronize()
@@ -232,28 +231,28 @@ def run_ours(args, ws_, rank, local):
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for i in range(steps):
-                gl[i % n_rot].replay()
+            g.replay()
             e1.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
         barrier(ws_)
         return e0.elapsed_time(e1) / steps   # ms per step
 
+    graph = capture(full_step, args.steps)
+    case_graphs = [capture(lambda r, sp, i=i: step_fn(sgq, per[i:i + 1], *wrot[r], sp, gemm_only=True),
+                           args.steps) for i in range(len(per))]
+
     def preheat(seconds):
         t_end = time.perf_counter() + seconds
-        i = 0
         while time.perf_counter() < t_end:
             with torch.cuda.stream(stream):
-                for _ in range(50):
-                    graphs[i % n_rot].replay()
-                    i += 1
+                graph.replay()
             stream.synchronize()
 
     launches0 = sgq.sgq_launch_count()
     with ClockSampler(local, os.path.join(args.out_dir, f"clocks_rank{rank}.csv") if args.out_dir else None) as cs:
         preheat(args.preheat)
-        ms_step = timed(graphs, args.steps)
+        ms_step = timed(graph, args.steps)
         ms_case = [timed(cg, args.steps) for cg in case_graphs]
     clocks = cs.summary()
     ms_step = max_over_ranks(ms_step, ws_, device)
@@ -266,7 +265,7 @@ def run_ours(args, ws_, rank, local):
     hx = [x.cpu().pin_memory() for _, x, _, _, _ in per]
     hd = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for *_, d in per]
     for i in range(args.warmup):
-        _e2e_step(sgq, per, wrot[i % n_rot], hx, hd, stream)
+        _e2e_step(sgq, per, wrot[i % n_rot], hx, hd, stream)   # e2e warm-up
     barrier(ws_)
     t0 = time.perf_counter()
     for i in range(args.steps):

@@ -147,12 +147,13 @@ struct Sync {
     uint32_t* status;
 };
 
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where,
+                                              bool backoff) {
     const uint64_t t0 = ptx::globaltimer();
     uint32_t spins = 0;
     while (true) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((++spins & 31u) == 0) {
+        if ((++spins & 15u) == 0) {
             if (*s.abort_flag) return false;
             if (ptx::globaltimer() - t0 > kTimeoutNs) {
                 *s.abort_flag = 1u;
@@ -160,11 +161,25 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, con
                 return false;
             }
         }
+        if (backoff && spins > 8) __nanosleep(64);
     }
 }
+// Single-thread bounded wait.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, s, where);
+    return wait_slow(bar, parity, s, where, false);
+}
+// Warp-wide bounded wait: lane 0 polls (the other lanes park at the warp
+// barrier, keeping shared-memory traffic off the TMA path), then the result is
+// broadcast.  __syncwarp orders lane 0's acquire before the other lanes' reads.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where,
+                                              bool backoff) {
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31) == 0 && !ptx::mbar_try_wait(bar, parity))
+        ok = wait_slow(bar, parity, s, where, backoff) ? 1u : 0u;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();
+    return ok != 0;
 }
 
 __device__ __forceinline__ bool epi_any(bool pred) {
@@ -418,7 +433,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t phase = 0;
             uint32_t nfin = 0;
             while (it.valid(a)) {
-                if (!wait_bar(sraw_bar(stage), phase, sync, 3)) break;
+                if (!wait_bar_warp(sraw_bar(stage), phase, sync, 3, false)) break;
                 convert(sf[stage], it, kNld == 1 ? (it.kb & 3) : 0);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -519,7 +534,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t par = ((n_iss / kStages) & 1u) ^ 1u;
                     if (n_iss != n_fin) {
                         if (!ptx::mbar_try_wait(empty_bar(si), par)) break;   // finish something first
-                    } else if (!wait_bar(empty_bar(si), par, sync, 3)) {
+                    } else if (!wait_bar_warp(empty_bar(si), par, sync, 3, false)) {
                         failed = true;
                         break;
                     }
@@ -575,7 +590,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ++seg;
         };
         while (it.valid(a) && !failed) {
-            if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
+            if (!wait_bar_warp(full_bar(stage), phase, sync, 2, false)) { failed = true; break; }
             ptx::tc_fence_after();
             if (lane == 0) trace_ev(a, 40 + (mma_jobs++ & 31));
             SfSlot<BN>& slot = sf[stage];
@@ -585,7 +600,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const bool mx = slot.pow2 != 0u && !a.force_promote;
             if (mx) {
                 if (!seg_open) {
-                    if (!wait_bar(acce_bar(acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
+                    if (!wait_bar_warp(acce_bar(acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2, false)) { failed = true; break; }
                     ptx::tc_fence_after();
                     seg_open = true;
                     first = true;
@@ -621,7 +636,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int steps = kBlk128 ? nq : 1;
                 for (int gidx = 0; gidx < ngroups; ++gidx) {
                     const int b = acc_buf(seg);
-                    if (!wait_bar(acce_bar(b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
+                    if (!wait_bar_warp(acce_bar(b), acc_par(seg) ^ 1u, sync, 2, false)) { failed = true; break; }
                     ptx::tc_fence_after();
                     const int j = gidx;  // scale chunk (blk_k == 128: chunk 0 holds the block scale)
                     const int q = C::kNld == 1 ? static_cast<int>(slot.kcol) : j;
@@ -685,7 +700,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             while (true) {
                 const int b = static_cast<int>(seg % kAccBufs);
                 const uint32_t par = (seg / kAccBufs) & 1u;
-                if (!wait_bar(accf_bar(b), par, sync, 4)) { failed = true; break; }
+                if (!wait_bar_warp(accf_bar(b), par, sync, 4, true)) { failed = true; break; }
                 ptx::tc_fence_after();
                 const uint32_t flags = info[b].flags;
                 const bool promote = (flags & kInfoPromote) != 0u;
@@ -796,8 +811,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
     }
 
+    if (lane == 0) trace_ev(a, 232 + warp);
     ptx::tc_fence_before();
     __syncthreads();
+    if (lane == 0) trace_ev(a, 244 + warp);
     if (threadIdx.x == 0) trace_ev(a, 255);
     if (warp == 1) {
         ptx::tc_fence_after();
