@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t phase = 0;
             uint32_t nfin = 0;
             while (it.valid(a)) {
-                if (!wait_bar_warp(sraw_bar(stage), phase, sync, 3, false)) break;
+                if (!wait_bar(sraw_bar(stage), phase, sync, 3)) break;
                 convert(sf[stage], it, kNld == 1 ? (it.kb & 3) : 0);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t par = ((n_iss / kStages) & 1u) ^ 1u;
                     if (n_iss != n_fin) {
                         if (!ptx::mbar_try_wait(empty_bar(si), par)) break;   // finish something first
-                    } else if (!wait_bar_warp(empty_bar(si), par, sync, 3, false)) {
+                    } else if (!wait_bar(empty_bar(si), par, sync, 3)) {
                         failed = true;
                         break;
                     }
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ++seg;
         };
         while (it.valid(a) && !failed) {
-            if (!wait_bar_warp(full_bar(stage), phase, sync, 2, false)) { failed = true; break; }
+            if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
             ptx::tc_fence_after();
             if (lane == 0) trace_ev(a, 40 + (mma_jobs++ & 31));
             SfSlot<BN>& slot = sf[stage];
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const bool mx = slot.pow2 != 0u && !a.force_promote;
             if (mx) {
                 if (!seg_open) {
-                    if (!wait_bar_warp(acce_bar(acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2, false)) { failed = true; break; }
+                    if (!wait_bar(acce_bar(acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     seg_open = true;
                     first = true;
@@ -636,7 +636,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int steps = kBlk128 ? nq : 1;
                 for (int gidx = 0; gidx < ngroups; ++gidx) {
                     const int b = acc_buf(seg);
-                    if (!wait_bar_warp(acce_bar(b), acc_par(seg) ^ 1u, sync, 2, false)) { failed = true; break; }
+                    if (!wait_bar(acce_bar(b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     const int j = gidx;  // scale chunk (blk_k == 128: chunk 0 holds the block scale)
                     const int q = C::kNld == 1 ? static_cast<int>(slot.kcol) : j;
