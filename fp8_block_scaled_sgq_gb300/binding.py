@@ -32,6 +32,7 @@ EXPORTS = (
     "sgq_quant_weight_block",
     "sgq_fp8_block_gemm",
     "sgq_fp8_block_gemm_ex",
+    "sgq_fp8_block_gemm_noalloc",
     "sgq_status_string",
     "sgq_device_status",
     "sgq_launch_count",
@@ -64,8 +65,9 @@ def load_library(path: str = LIB_PATH):
         lib.sgq_quant_weight_block.argtypes = [P, i64, i64, ci, ci, ci, P, P, P]
         lib.sgq_fp8_block_gemm.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, P]
         lib.sgq_fp8_block_gemm_ex.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, u32, P]
+        lib.sgq_fp8_block_gemm_noalloc.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, P]
         for f in ("sgq_quant_token_group", "sgq_quant_weight_block", "sgq_fp8_block_gemm",
-                  "sgq_fp8_block_gemm_ex"):
+                  "sgq_fp8_block_gemm_ex", "sgq_fp8_block_gemm_noalloc"):
             getattr(lib, f).restype = ci
         lib.sgq_status_string.argtypes = [ci]
         lib.sgq_status_string.restype = ctypes.c_char_p
@@ -126,6 +128,14 @@ def sgq_fp8_block_gemm_ex(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags, strea
     _check(load_library().sgq_fp8_block_gemm_ex(_ptr(Aq), _ptr(As), _ptr(Wq), _ptr(Ws), _ptr(D), M, N,
                                                 K, blk_n, blk_k, flags, _stream(stream)),
            "sgq_fp8_block_gemm_ex")
+
+
+def sgq_fp8_block_gemm_noalloc(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, stream=None):
+    """The GEMM with its split-K scratch in the library's fixed device array
+    (for callers that cannot let the library allocate device memory)."""
+    _check(load_library().sgq_fp8_block_gemm_noalloc(_ptr(Aq), _ptr(As), _ptr(Wq), _ptr(Ws), _ptr(D), M, N,
+                                                     K, blk_n, blk_k, _stream(stream)),
+           "sgq_fp8_block_gemm_noalloc")
 
 
 def sgq_device_status(stream=None) -> int:

@@ -95,6 +95,22 @@ sgq_status sgq_fp8_block_gemm(const void* Aq, const float* As, const void* Wq, c
     return sgq_fp8_block_gemm_ex(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, stream);
 }
 
+sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq, const float* Ws,
+                                      void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                      sgq_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || (blk_n != 32 && blk_n != 128) || (blk_k != 32 && blk_k != 128) ||
+        K % blk_k != 0 || N % 8 != 0)
+        return SGQ_ERR_INVALID_ARG;
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!Aq || !As || !Wq || !Ws || !D) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(Aq) || !aligned16(As) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(D))
+        return SGQ_ERR_MISALIGNED;
+    return sgq::launch_fp8_block_gemm_noalloc(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k,
+                                              reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char* sgq_status_string(sgq_status s) {
     switch (s) {
         case SGQ_OK: return "SGQ_OK";

@@ -232,6 +232,108 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     return gemm::dispatch_128_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the GEMM launch.
+//
+// Some callers cannot let a library allocate device memory: a serving engine
+// that reserves nearly all of HBM for its own pool up front (a later
+// cudaMalloc fails, or fragments that pool), or a host whose allocator must
+// account for every byte.  For them the split-K scratch (fp32 partial tiles
+// plus arrival counters) lives in this fixed file-scope array instead of the
+// workspace that sgq_fp8_block_gemm allocates on first use.  The array is
+// part of the module image, so every GPU that loads the library holds it
+// until the process exits.
+constexpr size_t kNoAllocCounterBytes = 16384 * sizeof(uint32_t);      // 64 KiB of counters
+constexpr size_t kNoAllocPartialBytes = size_t(16) << 20;               // 16 MiB of partials
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocCounterBytes + kNoAllocPartialBytes];
+
+namespace {
+unsigned char* g_noalloc_ptr[64] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device.  The host-side
+// name is only a stand-in; the address is looked up once per device, with
+// that device current.
+sgq_status noalloc_scratch(unsigned char** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SGQ_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return SGQ_OK;
+}
+}  // namespace
+
+sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq, const float* Ws,
+                                         void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                         cudaStream_t st) {
+    if (gemm::get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
+    DeviceInfo di;
+    sgq_status rc = device_info(&di);
+    if (rc != SGQ_OK) return rc;
+    if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
+    // Same launch plan as sgq_fp8_block_gemm, so both give the same result.
+    const gemm::Plan p = gemm::make_plan(M, N, K, di.sm_count);
+    gemm::GemmArgs a{};
+    a.As = As;
+    a.Ws = Ws;
+    a.D = static_cast<__nv_bfloat16*>(D);
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.ks = static_cast<int>(K / blk_k);
+    a.rows = static_cast<int>(p.swap ? N : M);
+    a.cols = static_cast<int>(p.swap ? M : N);
+    a.tiles_r = p.tiles_r;
+    a.tiles_c = p.tiles_c;
+    a.kb_total = p.kb_total;
+    a.kb_per_split = p.kb_per_split;
+    a.splits = p.splits;
+    a.items = p.items;
+    a.group_r = 16;
+    a.force_promote = 0;
+    rc = gemm::status_word(&a.status);
+    if (rc != SGQ_OK) return rc;
+    if (p.splits > 1) {
+        const size_t tiles = size_t(p.tiles_r) * size_t(p.tiles_c);
+        const size_t part_bytes = size_t(p.items) * gemm::kBM * size_t(p.bn) * sizeof(float);
+        if (tiles * sizeof(uint32_t) > kNoAllocCounterBytes || part_bytes > kNoAllocPartialBytes)
+            return SGQ_ERR_UNSUPPORTED;   // needs more scratch than the fixed array holds
+        unsigned char* base = nullptr;
+        rc = noalloc_scratch(&base);
+        if (rc != SGQ_OK) return rc;
+        a.counters = reinterpret_cast<uint32_t*>(base);
+        a.partial = reinterpret_cast<float*>(base + kNoAllocCounterBytes);
+        // The array keeps the previous call's contents; the counters must
+        // start at zero (a call that ended early may have left some set).
+        if (cudaMemsetAsync(a.counters, 0, tiles * sizeof(uint32_t), st) != cudaSuccess) return SGQ_ERR_CUDA;
+    }
+    CUtensorMap maps[4];
+    const void* opA = p.swap ? Wq : Aq;
+    const void* opB = p.swap ? Aq : Wq;
+    if (gemm::make_tmap(&maps[0], opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+    const bool scale_tma = (a.ks % 4) == 0;
+    maps[2] = maps[0];
+    maps[3] = maps[1];
+    if (scale_tma) {
+        const int64_t nb = (N + blk_n - 1) / blk_n;
+        if (gemm::make_scale_map(&maps[2], p.swap ? Ws : As, p.swap ? nb : M, a.ks,
+                                 p.swap ? gemm::kBM / blk_n : gemm::kBM) != SGQ_OK ||
+            gemm::make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks,
+                                 p.swap ? p.bn : p.bn / blk_n) != SGQ_OK)
+            return SGQ_ERR_CUDA;
+    }
+    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+    return gemm::dispatch_128_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+}
+
 sgq_status read_and_clear_device_status(cudaStream_t st) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return SGQ_ERR_CUDA;
     uint32_t v = 0;

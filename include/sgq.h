@@ -140,6 +140,37 @@ sgq_status sgq_fp8_block_gemm_ex(const void* Aq, const float* As, const void* Wq
                                  const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
                                  int blk_n, int blk_k, uint32_t flags, sgq_stream_t stream);
 
+/*
+ * sgq_fp8_block_gemm without any device allocation.  No counterpart in the
+ * paper: this is a deployment variant of the GEMM above.
+ *
+ * Who needs it: callers that cannot let a library allocate device memory --
+ * a serving engine that reserves nearly all of HBM for its own memory pool
+ * up front (a later cudaMalloc fails or fragments that pool), or a host whose
+ * allocator must account for every byte.  sgq_fp8_block_gemm allocates a
+ * split-K workspace on first use; this entry point instead keeps that
+ * scratch in a fixed device array that is part of the library image
+ * (16 MiB of fp32 partial tiles plus 64 KiB of arrival counters), held by
+ * every GPU that loads the library until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Same arguments, result and launch plan as sgq_fp8_block_gemm (flags =
+ * SGQ_GEMM_DEFAULT).  A shape whose launch plan needs more scratch than the
+ * fixed array holds is rejected with SGQ_ERR_UNSUPPORTED before anything is
+ * launched; shapes that need no split-K (large M, or few K blocks) never touch
+ * the array.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any CUDA stream capture.
+ * Every call shares the one array and it keeps the previous call's contents:
+ * each call clears the arrival counters it uses (an asynchronous memset on
+ * `stream`), and calls that overlap on the GPU -- on different streams, or
+ * from several host threads -- race on the array and must be avoided.
+ */
+sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq,
+                                      const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
+                                      int blk_n, int blk_k, sgq_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sgq_status_string(sgq_status s);
 
