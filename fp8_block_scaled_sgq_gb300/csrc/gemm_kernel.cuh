@@ -434,6 +434,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t nfin = 0;
             while (it.valid(a)) {
                 if (!wait_bar(sraw_bar(stage), phase, sync, 3)) break;
+                if (lane == 0) trace_ev(a, 104 + (nfin & 31));
                 convert(sf[stage], it, kNld == 1 ? (it.kb & 3) : 0);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -729,7 +730,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (flags & kInfoLast) break;
             }
             if (epi_any(failed || *sync.abort_flag)) break;
-            if (epi_tid == 0) trace_ev(a, 104 + 4 * (n_items & 31));
+            if (epi_tid == 0) trace_ev(a, 136 + 4 * (n_items & 15));
             // ------------------------------------------------ output
             const int row0 = it.tr * kBM, col0 = it.tc * BN;
             const int grow = row0 + r_in_tile;   // global row of the MMA A operand
@@ -745,7 +746,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 __threadfence();
                 epi_sync();
                 if (epi_tid == 0) {
-                    trace_ev(a, 105 + 4 * (n_items & 31));
+                    trace_ev(a, 137 + 4 * (n_items & 15));
                     const uint32_t old = atomicAdd(a.counters + it.tile, 1u);
                     misc[2] = (old == static_cast<uint32_t>(a.splits - 1)) ? 1u : 0u;
                 }
@@ -803,7 +804,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
-            if (epi_tid == 0) trace_ev(a, 106 + 4 * (n_items & 31));
+            if (epi_tid == 0) trace_ev(a, 138 + 4 * (n_items & 15));
             ++n_items;
             // advance to the next item (skip the remaining k-stages of this one)
             while (it.valid(a) && !it.next(a)) {
