@@ -192,6 +192,8 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     a.items = p.items;
     a.group_r = 16;
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
+    static const int krot = gemm::env_int("SGQ_KROT", 0);
+    a.krot = krot;
     rc = gemm::status_word(&a.status);
     if (rc != SGQ_OK) return rc;
 #ifdef SGQ_TRACE
@@ -296,6 +298,8 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
     a.items = p.items;
     a.group_r = 16;
     a.force_promote = 0;
+    static const int krot = gemm::env_int("SGQ_KROT", 0);
+    a.krot = krot;
     rc = gemm::status_word(&a.status);
     if (rc != SGQ_OK) return rc;
     if (p.splits > 1) {

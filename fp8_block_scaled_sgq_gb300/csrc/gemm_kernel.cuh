@@ -92,11 +92,15 @@ struct GemmArgs {
     int rows, cols;       // extents of the MMA A operand and B operand
     int tiles_r, tiles_c, kb_total, kb_per_split, splits, items, group_r;
     int force_promote;
+    int krot;             // rotate the K-stage order per tile
 };
 
-// Walks the (item, k-stage) jobs of one CTA in order.
+// Walks the (item, k-stage) jobs of one CTA in order.  Within an item the
+// K stages are visited in a rotated order (starting at an offset derived from
+// the tile) when a.krot is set, so CTAs that share an operand tile do not all
+// request the same lines at the same moment.
 struct JobIter {
-    int item, kb, kb1;
+    int item, kb, kb0, nkb, pos, rot;
     int tile, split, tr, tc;
     __device__ void load(const GemmArgs& a) {
         split = item % a.splits;
@@ -108,39 +112,31 @@ struct JobIter {
         const int in = tile - g * per_group;
         tr = first + in % gm;
         tc = in / gm;
-        kb = split * a.kb_per_split;
-        kb1 = min(a.kb_total, kb + a.kb_per_split);
+        kb0 = split * a.kb_per_split;
+        nkb = min(a.kb_total, kb0 + a.kb_per_split) - kb0;
+        rot = a.krot ? tile % nkb : 0;
+        pos = 0;
+        kb = kb0 + rot;
     }
     __device__ void begin(const GemmArgs& a) {
         item = blockIdx.x;
         if (item < a.items) load(a);
     }
     __device__ bool valid(const GemmArgs& a) const { return item < a.items; }
-    __device__ bool last_kb() const { return kb + 1 == kb1; }
-    __device__ bool first_kb(const GemmArgs& a) const { return kb == split * a.kb_per_split; }
+    __device__ bool last_kb() const { return pos + 1 == nkb; }
     // Advances one stage; returns true when it moved to a new item.
     __device__ bool next(const GemmArgs& a) {
-        if (++kb >= kb1) {
+        if (++pos >= nkb) {
             item += gridDim.x;
             if (item < a.items) load(a);
             return true;
         }
+        int r = pos + rot;
+        if (r >= nkb) r -= nkb;
+        kb = kb0 + r;
         return false;
     }
 };
-
-// Optional event trace for development builds (-DSGQ_TRACE): one row of
-// kTraceSlots globaltimer stamps per CTA.  Compiled out otherwise.
-constexpr int kTraceSlots = 256;
-__device__ __forceinline__ void trace_ev(const GemmArgs& a, int slot) {
-#ifdef SGQ_TRACE
-    if (a.trace != nullptr && slot >= 0 && slot < kTraceSlots)
-        a.trace[blockIdx.x * kTraceSlots + slot] = ptx::globaltimer();
-#else
-    (void)a;
-    (void)slot;
-#endif
-}
 
 struct Sync {
     volatile uint32_t* abort_flag;
