@@ -138,6 +138,19 @@ struct JobIter {
     }
 };
 
+// Optional event trace for development builds (-DSGQ_TRACE): one row of
+// kTraceSlots globaltimer stamps per CTA.  Compiled out otherwise.
+constexpr int kTraceSlots = 256;
+__device__ __forceinline__ void trace_ev(const GemmArgs& a, int slot) {
+#ifdef SGQ_TRACE
+    if (a.trace != nullptr && slot >= 0 && slot < kTraceSlots)
+        a.trace[blockIdx.x * kTraceSlots + slot] = ptx::globaltimer();
+#else
+    (void)a;
+    (void)slot;
+#endif
+}
+
 struct Sync {
     volatile uint32_t* abort_flag;
     uint32_t* status;
