@@ -355,12 +355,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 pre.next(a);
                 ++npre;
             }
+            trace_ev(a, 2);
             ptx::grid_dependency_wait();
             trace_ev(a, 1);
             for (int s = 0; s < npre; ++s) {
                 load_x(s, it);
                 it.next(a);
             }
+            trace_ev(a, 3);
             int stage = npre % kStages;
             uint32_t phase = npre / kStages;
             int nj = npre;
