@@ -674,7 +674,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 if (failed) break;
             }
-            if (lane == 0) ptx::tc_commit(empty_bar(stage));  // frees the stage when its MMAs finish
+            if (lane == 0) {
+                ptx::tc_commit(empty_bar(stage));  // frees the stage when its MMAs finish
+                trace_ev(a, 200 + ((mma_jobs - 1) & 15));
+            }
             __syncwarp();
             const bool item_end = it.last_kb();
             it.next(a);
