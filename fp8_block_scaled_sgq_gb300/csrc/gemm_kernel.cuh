@@ -318,7 +318,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // The weight operand does not depend on the preceding kernel, so the
         // weight halves of the first kStages stages go out before the
         // programmatic-dependency wait; activations only after it.
-        if (lane == 0) {
+        // The whole warp runs the loop; lane 0 issues through predicated asm.
+        {
+            const uint32_t leader = lane == 0 ? 1u : 0u;
             const CUtensorMap* tmW = kSwap ? &tmA : &tmB;
             const CUtensorMap* tmX = kSwap ? &tmB : &tmA;
             const CUtensorMap* tmWs = kSwap ? &tmSA : &tmSB;   // weight scales
@@ -335,16 +337,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             auto ws_row = [&](const JobIter& j) { return kSwap ? j.tr * (kBM / kBlkN) : j.tc * (BN / kBlkN); };
             auto xs_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : j.tr * kBM; };
             auto load_w = [&](int s, const JobIter& j) {
-                ptx::mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
+                ptx::mbar_arrive_expect_tx_if(leader, full_bar(s), C::kStageBytes);
                 if (kScaleTma) {
-                    ptx::mbar_arrive_expect_tx(sraw_bar(s), C::kScaleBytes);
-                    ptx::tma_load_2d(ws_dst(s), tmWs, s_col(j), ws_row(j), sraw_bar(s));
+                    ptx::mbar_arrive_expect_tx_if(leader, sraw_bar(s), C::kScaleBytes);
+                    ptx::tma_load_2d_if(leader, ws_dst(s), tmWs, s_col(j), ws_row(j), sraw_bar(s));
                 }
-                ptx::tma_load_2d(w_dst(s), tmW, j.kb * kBK, w_row(j), full_bar(s));
+                ptx::tma_load_2d_if(leader, w_dst(s), tmW, j.kb * kBK, w_row(j), full_bar(s));
             };
             auto load_x = [&](int s, const JobIter& j) {
-                if (kScaleTma) ptx::tma_load_2d(xs_dst(s), tmXs, s_col(j), xs_row(j), sraw_bar(s));
-                ptx::tma_load_2d(x_dst(s), tmX, j.kb * kBK, x_row(j), full_bar(s));
+                if (kScaleTma) ptx::tma_load_2d_if(leader, xs_dst(s), tmXs, s_col(j), xs_row(j), sraw_bar(s));
+                ptx::tma_load_2d_if(leader, x_dst(s), tmX, j.kb * kBK, x_row(j), full_bar(s));
             };
             JobIter it;
             it.begin(a);
@@ -355,20 +357,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 pre.next(a);
                 ++npre;
             }
-            trace_ev(a, 2);
+            if (lane == 0) trace_ev(a, 2);
             ptx::grid_dependency_wait();
-            trace_ev(a, 1);
+            if (lane == 0) trace_ev(a, 1);
             for (int s = 0; s < npre; ++s) {
                 load_x(s, it);
                 it.next(a);
             }
-            trace_ev(a, 3);
+            if (lane == 0) trace_ev(a, 3);
             int stage = npre % kStages;
             uint32_t phase = npre / kStages;
             int nj = npre;
             while (it.valid(a)) {
                 if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 1)) break;
-                trace_ev(a, 8 + (nj++ & 31));
+                if (lane == 0) trace_ev(a, 8 + (nj & 31));
+                ++nj;
                 load_w(stage, it);
                 load_x(stage, it);
                 it.next(a);
@@ -574,9 +577,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
+        // The whole warp runs this loop in lock-step; every tcgen05 instruction
+        // is issued by lane 0 through a predicate inside the asm, so the warp
+        // never diverges and descriptors stay warp-uniform.
         constexpr uint32_t idesc_f8 = ptx::idesc_f8(kBM, BN);
         constexpr uint32_t idesc_mx = ptx::idesc_mxf8(kBM, BN);
         const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
+        const uint32_t leader = lane == 0 ? 1u : 0u;
         constexpr int kColGroup = kSwap ? 1 : kBlkN;
         JobIter it;
         it.begin(a);
@@ -587,54 +594,54 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         uint32_t mma_jobs = 0;
         bool failed = false;
         bool seg_open = false;
-        bool first = true;
+        uint32_t acc_flag = 0;  // 0 for the first MMA of an open segment
         auto acc_buf = [&](uint32_t u) { return static_cast<int>(u % kAccBufs); };
         auto acc_par = [&](uint32_t u) { return (u / kAccBufs) & 1u; };
         // Hands the open accumulator segment to the epilogue.
         auto close_segment = [&](uint32_t flags) {
             const int b = acc_buf(seg);
-            if (lane == 0) {
-                info[b].flags = flags;
-                ptx::mbar_arrive(accf_bar(b));
-                ptx::tc_commit(accf_bar(b));
-            }
+            if (lane == 0) info[b].flags = flags;
             __syncwarp();
+            ptx::mbar_arrive_if(leader, accf_bar(b));
+            ptx::tc_commit_if(leader, accf_bar(b));
             ++seg;
         };
         while (it.valid(a) && !failed) {
             if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
             ptx::tc_fence_after();
-            if (lane == 0) trace_ev(a, 40 + (mma_jobs++ & 31));
+            if (lane == 0) trace_ev(a, 40 + (mma_jobs & 31));
+            ++mma_jobs;
             SfSlot<BN>& slot = sf[stage];
             const int nq = min(4, (a.K - it.kb * kBK) / 32);
             const uint32_t a_st = sA0 + stage * C::kABytes;
             const uint32_t b_st = sB0 + stage * C::kBBytes;
+            const uint64_t ad0 = ptx::smem_desc(a_st, 16, 1024, ptx::kLayoutSw128);
+            const uint64_t bd0 = ptx::smem_desc(b_st, 16, 1024, ptx::kLayoutSw128);
             const bool mx = slot.pow2 != 0u && !a.force_promote;
             if (mx) {
                 if (!seg_open) {
                     if (!wait_bar(acce_bar(acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     seg_open = true;
-                    first = true;
+                    acc_flag = 0;
                 }
-                if (lane == 0) {
-                    const uint32_t sfs = kSfCol + 16u * (mx_used & 1u);
-                    const uint32_t t_sfa = tmem + sfs, t_sfb = tmem + sfs + 4u;
-                    ptx::tmem_cp_32x128b_x4(t_sfa, ptx::smem_desc(ptx::smem_u32(slot.sfa), 128, 128,
-                                                                  ptx::kLayoutNone));
+                const uint32_t sfs = kSfCol + 16u * (mx_used & 1u);
+                const uint32_t t_sfa = tmem + sfs, t_sfb = tmem + sfs + 4u;
+                ptx::tmem_cp_32x128b_x4_if(leader, t_sfa,
+                                           ptx::smem_desc(ptx::smem_u32(slot.sfa), 128, 128, ptx::kLayoutNone));
 #pragma unroll
-                    for (int h = 0; h < C::kSfbCopies; ++h)
-                        ptx::tmem_cp_32x128b_x4(t_sfb + 4u * h,
-                                                ptx::smem_desc(ptx::smem_u32(slot.sfb + 128 * h), 128, 128,
-                                                               ptx::kLayoutNone));
-                    const uint32_t d = tmem + static_cast<uint32_t>(acc_buf(seg) * BN);
-                    const uint64_t ad0 = ptx::smem_desc(a_st, 16, 1024, ptx::kLayoutSw128);
-                    const uint64_t bd0 = ptx::smem_desc(b_st, 16, 1024, ptx::kLayoutSw128);
-                    for (int j = 0; j < nq; ++j) {
+                for (int h = 0; h < C::kSfbCopies; ++h)
+                    ptx::tmem_cp_32x128b_x4_if(leader, t_sfb + 4u * h,
+                                               ptx::smem_desc(ptx::smem_u32(slot.sfb + 128 * h), 128, 128,
+                                                              ptx::kLayoutNone));
+                const uint32_t d = tmem + static_cast<uint32_t>(acc_buf(seg) * BN);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (j < nq) {
                         // +32 bytes along K inside the swizzle atom = +2 in the start field
-                        ptx::mma_mxf8(d, ad0 + 2u * j, bd0 + 2u * j, ptx::idesc_sf_ids(idesc_mx, j, j), t_sfa,
-                                      t_sfb, first ? 0u : 1u);
-                        first = false;
+                        ptx::mma_mxf8_if(leader, d, ad0 + 2u * j, bd0 + 2u * j, ptx::idesc_sf_ids(idesc_mx, j, j),
+                                         t_sfa, t_sfb, acc_flag);
+                        acc_flag = 1;
                     }
                 }
                 ++mx_used;
@@ -658,27 +665,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const bool last = it.last_kb() && gidx == ngroups - 1;
                     if (lane == 0) info[b].flags = kInfoPromote | (last ? kInfoLast : 0u);
                     __syncwarp();
-                    if (lane == 0) {
-                        const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
-                        const uint64_t ad0 = ptx::smem_desc(a_st, 16, 1024, ptx::kLayoutSw128);
-                        const uint64_t bd0 = ptx::smem_desc(b_st, 16, 1024, ptx::kLayoutSw128);
-                        for (int t = 0; t < steps; ++t) {
-                            const int jj = gidx * steps + t;   // 32-wide chunk inside the stage
-                            ptx::mma_f8(d, ad0 + 2u * jj, bd0 + 2u * jj, idesc_f8, t > 0 ? 1u : 0u);
-                        }
-                        ptx::mbar_arrive(accf_bar(b));
-                        ptx::tc_commit(accf_bar(b));
+                    const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                    for (int t = 0; t < steps; ++t) {
+                        const int jj = gidx * steps + t;   // 32-wide chunk inside the stage
+                        ptx::mma_f8_if(leader, d, ad0 + 2u * jj, bd0 + 2u * jj, idesc_f8, t > 0 ? 1u : 0u);
                     }
-                    __syncwarp();
+                    ptx::mbar_arrive_if(leader, accf_bar(b));
+                    ptx::tc_commit_if(leader, accf_bar(b));
                     ++seg;
                 }
                 if (failed) break;
             }
-            if (lane == 0) {
-                ptx::tc_commit(empty_bar(stage));  // frees the stage when its MMAs finish
-                trace_ev(a, 200 + ((mma_jobs - 1) & 15));
-            }
-            __syncwarp();
+            ptx::tc_commit_if(leader, empty_bar(stage));  // frees the stage when its MMAs finish
+            if (lane == 0) trace_ev(a, 200 + ((mma_jobs - 1) & 15));
             const bool item_end = it.last_kb();
             it.next(a);
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -688,10 +687,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         }
         // Let every tcgen05 op issued above land before teardown.
-        if (lane == 0) {
-            ptx::tc_commit(drain_bar);
-            wait_bar(drain_bar, 0, sync, 5);
-        }
+        ptx::tc_commit_if(leader, drain_bar);
+        if (lane == 0) wait_bar(drain_bar, 0, sync, 5);
         __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue

@@ -180,6 +180,65 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+// ------------------------------------------------------------------ predicated issue
+// Variants executed by a whole converged warp; only lanes with `pred` != 0
+// perform the operation.  Keeping the warp converged lets the compiler keep
+// descriptors and addresses warp-uniform, which makes tcgen05/TMA issue much
+// cheaper than from a diverged single-lane branch.  Callers pass one fixed
+// lane so that MMAs and the commits that track them come from one thread.
+__device__ __forceinline__ void mma_f8_if(uint32_t pred, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.b32 p, %5, 0;\nsetp.ne.b32 q, %4, 0;\n"
+        "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, q;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(pred)
+        : "memory");
+}
+__device__ __forceinline__ void mma_mxf8_if(uint32_t pred, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.b32 p, %7, 0;\nsetp.ne.b32 q, %6, 0;\n"
+        "@p tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], q;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(pred)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_cp_32x128b_x4_if(uint32_t pred, uint32_t taddr, uint64_t sdesc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %2, 0;\n"
+        "@p tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}" ::"r"(taddr), "l"(sdesc), "r"(pred)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_if(uint32_t pred, uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %1, 0;\n"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar),
+        "r"(pred)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_if(uint32_t pred, uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %1, 0;\n@p mbarrier.arrive.shared::cta.b64 _, [%0];\n}" ::"r"(bar),
+        "r"(pred)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t pred, uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %2, 0;\n"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}" ::"r"(bar), "r"(bytes), "r"(pred)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_if(uint32_t pred, uint32_t dst, const CUtensorMap* m, int32_t x,
+                                               int32_t y, uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %5, 0;\n"
+        "@p cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar), "r"(pred)
+        : "memory");
+}
+
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor (tcgen05 form): start >> 4 in [0,14),
 // leading byte offset >> 4 in [16,30), stride byte offset >> 4 in [32,46),
