@@ -606,17 +606,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::tc_commit_if(leader, accf_bar(b));
             ++seg;
         };
+        // Descriptors are linear in the start address: a stage's descriptor is
+        // the stage-0 descriptor plus (stage offset >> 4).
+        const uint64_t ad_base = ptx::smem_desc(sA0, 16, 1024, ptx::kLayoutSw128);
+        const uint64_t bd_base = ptx::smem_desc(sB0, 16, 1024, ptx::kLayoutSw128);
+        const uint64_t sfa_base = ptx::smem_desc(ptx::smem_u32(sf[0].sfa), 128, 128, ptx::kLayoutNone);
+        const uint64_t sfb_base = ptx::smem_desc(ptx::smem_u32(sf[0].sfb), 128, 128, ptx::kLayoutNone);
+        constexpr uint32_t kSlotStep = sizeof(SfSlot<BN>) >> 4;
+        // A K stage shorter than 128 exists only when K % 128 != 0 (last stage).
+        const bool ragged_k = (a.K % kBK) != 0;
         while (it.valid(a) && !failed) {
             if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
             ptx::tc_fence_after();
             if (lane == 0) trace_ev(a, 40 + (mma_jobs & 31));
             ++mma_jobs;
             SfSlot<BN>& slot = sf[stage];
-            const int nq = min(4, (a.K - it.kb * kBK) / 32);
-            const uint32_t a_st = sA0 + stage * C::kABytes;
-            const uint32_t b_st = sB0 + stage * C::kBBytes;
-            const uint64_t ad0 = ptx::smem_desc(a_st, 16, 1024, ptx::kLayoutSw128);
-            const uint64_t bd0 = ptx::smem_desc(b_st, 16, 1024, ptx::kLayoutSw128);
+            const int nq = ragged_k ? min(4, (a.K - it.kb * kBK) / 32) : 4;
+            const uint64_t ad0 = ad_base + static_cast<uint64_t>(stage * (C::kABytes >> 4));
+            const uint64_t bd0 = bd_base + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
             const bool mx = slot.pow2 != 0u && !a.force_promote;
             if (mx) {
                 if (!seg_open) {
@@ -627,23 +634,25 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 const uint32_t sfs = kSfCol + 16u * (mx_used & 1u);
                 const uint32_t t_sfa = tmem + sfs, t_sfb = tmem + sfs + 4u;
-                ptx::tmem_cp_32x128b_x4_if(leader, t_sfa,
-                                           ptx::smem_desc(ptx::smem_u32(slot.sfa), 128, 128, ptx::kLayoutNone));
+                const uint64_t slot_off = static_cast<uint64_t>(stage) * kSlotStep;
+                ptx::tmem_cp_32x128b_x4_if(leader, t_sfa, sfa_base + slot_off);
 #pragma unroll
                 for (int h = 0; h < C::kSfbCopies; ++h)
-                    ptx::tmem_cp_32x128b_x4_if(leader, t_sfb + 4u * h,
-                                               ptx::smem_desc(ptx::smem_u32(slot.sfb + 128 * h), 128, 128,
-                                                              ptx::kLayoutNone));
+                    ptx::tmem_cp_32x128b_x4_if(leader, t_sfb + 4u * h, sfb_base + slot_off + 32u * h);
                 const uint32_t d = tmem + static_cast<uint32_t>(acc_buf(seg) * BN);
+                if (nq == 4) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (j < nq) {
+                    for (int j = 0; j < 4; ++j) {
                         // +32 bytes along K inside the swizzle atom = +2 in the start field
                         ptx::mma_mxf8_if(leader, d, ad0 + 2u * j, bd0 + 2u * j, ptx::idesc_sf_ids(idesc_mx, j, j),
-                                         t_sfa, t_sfb, acc_flag);
-                        acc_flag = 1;
+                                         t_sfa, t_sfb, j == 0 ? acc_flag : 1u);
                     }
+                } else {
+                    for (int j = 0; j < nq; ++j)
+                        ptx::mma_mxf8_if(leader, d, ad0 + 2u * j, bd0 + 2u * j, ptx::idesc_sf_ids(idesc_mx, j, j),
+                                         t_sfa, t_sfb, j == 0 ? acc_flag : 1u);
                 }
+                acc_flag = 1;
                 ++mx_used;
             } else {
                 if (seg_open) {
