@@ -47,7 +47,7 @@ namespace gemm {
 
 constexpr int kBM = 128;          // MMA M: rows of the "A" operand per tile
 constexpr int kBK = 128;          // K elements (bytes) per pipeline stage
-constexpr int kNumThreads = 352;  // 11 warps
+constexpr int kNumThreads = 384;  // 12 warps
 constexpr int kEpiWarp0 = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 480;  // two 16-column scale-factor slots at 480 and 496
@@ -215,6 +215,26 @@ __device__ __forceinline__ uint32_t scale_bad_bits(uint32_t b) {
     return (b & 0x807FFFFFu) | static_cast<uint32_t>(e == 0u || e == 0xFFu);
 }
 
+// UE8M0 word of one scale row: byte q = exponent byte of the chunk-q scale
+// (kNld == 1: the one scale at column kcol, repeated).  `bad` collects any
+// scale that is not a positive normal power of two.
+__device__ __forceinline__ uint32_t has_zero_byte(uint32_t w) { return (w - 0x01010101u) & ~w & 0x80808080u; }
+template <int kNld>
+__device__ __forceinline__ uint32_t sf_word(const float* row, int kcol, uint32_t& bad) {
+    if (kNld == 1) {
+        const uint32_t b = __float_as_uint(row[kcol]);
+        const uint32_t w = __byte_perm(b << 1, 0u, 0x3333);
+        bad |= (b & 0x807FFFFFu) | has_zero_byte(w) | has_zero_byte(~w);
+        return w;
+    }
+    const uint4 v = *reinterpret_cast<const uint4*>(row);
+    const uint32_t lo = __byte_perm(v.x << 1, v.y << 1, 0x0073);
+    const uint32_t hi = __byte_perm(v.z << 1, v.w << 1, 0x0073);
+    const uint32_t w = __byte_perm(lo, hi, 0x5410);
+    bad |= ((v.x | v.y | v.z | v.w) & 0x807FFFFFu) | has_zero_byte(w) | has_zero_byte(~w);
+    return w;
+}
+
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
 struct Cfg {
     static constexpr int kABytes = kBM * kBK;
@@ -379,7 +399,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 2) {
+    } else if (warp == 2 || warp == 11) {
         // ---------------------------------------------------------- scale loader
         // Turns each stage's raw fp32 scales into UE8M0 words in tcgen05.cp
         // order, checks the power-of-two property, and releases the stage to
@@ -400,17 +420,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int r = lane + 32 * i;
                 const int li = kSwap ? r / kBlkN : r;
                 const bool valid = (kSwap ? row0 + li * kBlkN : row0 + r) < a.rows;
-                uint32_t word = 0x7F7F7F7Fu;   // 2^0 for rows past the matrix
-                if (valid) {
-                    word = 0;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t b = __float_as_uint(slot.lane_raw[li][kNld == 1 ? kcol : q]);
-                        bad |= scale_bad_bits(b);
-                        word |= (b >> 23) << (8 * q);
-                    }
-                }
-                w4[i] = word;
+                w4[i] = valid ? sf_word<kNld>(&slot.lane_raw[li][0], kcol, bad) : 0x7F7F7F7Fu;  // 2^0 past the end
             }
             *reinterpret_cast<uint4*>(&slot.sfa[lane * 4]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
 #pragma unroll
@@ -418,18 +428,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int c = h * 128 + lane + 32 * i;
-                    uint32_t word = 0x7F7F7F7Fu;
                     const int ci = kSwap ? c : c / kBlkN;
-                    if (c < BN && (kSwap ? col0 + c : col0 + ci * kBlkN) < a.cols) {
-                        word = 0;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint32_t b = __float_as_uint(slot.col_raw[ci][kNld == 1 ? kcol : q]);
-                            bad |= scale_bad_bits(b);
-                            word |= (b >> 23) << (8 * q);
-                        }
-                    }
-                    w4[i] = word;
+                    const bool valid = c < BN && (kSwap ? col0 + c : col0 + ci * kBlkN) < a.cols;
+                    w4[i] = valid ? sf_word<kNld>(&slot.col_raw[ci < 64 ? ci : 0][0], kcol, bad) : 0x7F7F7F7Fu;
                 }
                 *reinterpret_cast<uint4*>(&slot.sfb[h * 128 + lane * 4]) =
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -441,12 +442,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         };
         if (kScaleTma) {
+            // Two converter warps (2 and 11) take alternate stages.
+            const uint32_t sub = warp == 2 ? 0u : 1u;
             JobIter it;
             it.begin(a);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t nfin = 0;
             while (it.valid(a)) {
+                if ((nfin & 1u) != sub) {
+                    ++nfin;
+                    it.next(a);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    continue;
+                }
                 if (!wait_bar(sraw_bar(stage), phase, sync, 3)) break;
                 if (lane == 0) trace_ev(a, 104 + (nfin & 31));
                 convert(sf[stage], it, kNld == 1 ? (it.kb & 3) : 0);
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 it.next(a);
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
-        } else {
+        } else if (warp == 2) {
             // Per item, each lane precomputes the scale rows it fetches:
             //   lane side (A operand): activation rows lane+32i (normal), or the
             //     (n-block, chunk) pair `lane` of the tile (swap);
@@ -832,10 +841,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
     }
 
-    if (lane == 0) trace_ev(a, 232 + warp);
+    if (lane == 0 && warp < 11) trace_ev(a, 232 + warp);
     ptx::tc_fence_before();
     __syncthreads();
-    if (lane == 0) trace_ev(a, 244 + warp);
+    if (lane == 0 && warp < 11) trace_ev(a, 244 + warp);
     if (threadIdx.x == 0) trace_ev(a, 255);
     if (warp == 1) {
         ptx::tc_fence_after();
