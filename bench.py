@@ -50,6 +50,34 @@ def peaks():
             "source": "fallback"}
 
 
+def kernel_source_digest() -> str:
+    """sha256 over the CUDA sources, to tie ncu counters to the build they came from."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "fp8_block_scaled_sgq_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture per workload (profiles/ holds the summary and the command).  Valid
+# only for the kernel sources they were taken on; otherwise reported as null.
+MEASURED_TRAFFIC = {
+    "decode_block32": {"bytes_per_launch": 14841000, "src": "39a0bfca7e391338",
+                       "profile": "profiles/launches_decode_block32.md"},
+}
+
+
+def measured_traffic(workload: str):
+    t = MEASURED_TRAFFIC.get(workload)
+    if t is None or t["src"] != kernel_source_digest():
+        return None
+    return t["bytes_per_launch"]
+
+
 def workload_unit(cases):
     """("TFLOP/s", 1e12, "flops") for tensor-bound workloads, else ("GB/s", 1e9, "bytes")."""
     pk = peaks()
@@ -286,13 +314,13 @@ def run_ours(args, ws_, rank, local):
     if tensor_bound:
         unit, scale, to_unit = "TFLOP/s", 1e12, step_flops
         roof = {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": round(fp8_peak, 1),
-                "unit": "TFLOP/s", "frac": round(gemm_tf / fp8_peak, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(gemm_tf / fp8_peak, 4), "traffic": measured_traffic(args.workload),
                 "kernel": "fp8_block_gemm_kernel (128x256 tiles)",
                 "peak_source": f"{pk['source']} bf16 burst x 2 (fp8:bf16 nominal)"}
     else:
         unit, scale, to_unit = "GB/s", 1e9, step_bytes
         roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(gemm_gbs / pk["hbm_gbs"], 4), "traffic": None,
+                "frac": round(gemm_gbs / pk["hbm_gbs"], 4), "traffic": measured_traffic(args.workload),
                 "kernel": "fp8_block_gemm_kernel (swap-AB, split-K)", "peak_source": pk["source"]}
     value = ws_ * to_unit / (ms_step * 1e-3) / scale
     result = {
