@@ -112,7 +112,8 @@ int env_int(const char* name, int dflt) {
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
     Plan p{};
-    p.swap = M <= 64;
+    static const int swap_max = env_int("SGQ_SWAP_MAX", 64);
+    p.swap = M <= swap_max;
     p.bn = p.swap ? (M <= 16 ? 16 : (M <= 32 ? 32 : 64)) : 256;
     const int64_t rows = p.swap ? N : M, cols = p.swap ? M : N;
     p.tiles_r = static_cast<int>((rows + kBM - 1) / kBM);

@@ -769,9 +769,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // partials in split order (deterministic) and stores the tile.
                 float* part = a.partial + (static_cast<int64_t>(it.tile) * a.splits + it.split) * (kBM * BN) +
                               r_in_tile * BN + c_begin;
+                // rows past the operand's end carry nothing: neither written nor read
+                const bool live = grow < a.rows;
+                if (live) {
 #pragma unroll
-                for (int c = 0; c < kCols; c += 4)
-                    *reinterpret_cast<float4*>(part + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                    for (int c = 0; c < kCols; c += 4)
+                        *reinterpret_cast<float4*>(part + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                }
                 __threadfence();
                 epi_sync();
                 if (epi_tid == 0) {
@@ -781,7 +785,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 epi_sync();
                 store = misc[2] != 0u;
-                if (store) {
+                if (store && live) {
                     __threadfence();
                     const float* base = a.partial + static_cast<int64_t>(it.tile) * a.splits * (kBM * BN) +
                                         r_in_tile * BN + c_begin;
@@ -805,8 +809,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             acc[c + 3] += v.w;
                         }
                     }
-                    if (epi_tid == 0) a.counters[it.tile] = 0u;   // ready for the next launch
                 }
+                if (store && epi_tid == 0) a.counters[it.tile] = 0u;   // ready for the next launch
             }
             if (store && !kSwap) {
                 if (grow < a.M) {

@@ -79,13 +79,14 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
                                                                 uint2* __restrict__ xq,
                                                                 float* __restrict__ xs,
                                                                 int64_t nvec) {
+    // Let a programmatically-dependent GEMM launch now, so that its weight
+    // prefetch overlaps this kernel; it still waits for this grid to finish
+    // before it reads xq / xs.
+    ptx::launch_dependents();
     // Launched with programmatic stream serialisation: the launch overlaps the
     // previous kernel on the stream, so wait for it before touching memory
     // (x may be its output; xq/xs may still be read by it).
     ptx::grid_dependency_wait();
-    // Let a programmatically-dependent GEMM start its weight prefetch now; it
-    // still waits for this grid to finish before it reads xq / xs.
-    ptx::launch_dependents();
     constexpr int kTpg = kGroup / 8;
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;

@@ -124,12 +124,15 @@ sgq_status sgq_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n
  *
  * Launch overlap (programmatic dependent launch): the GEMM and
  * sgq_quant_token_group are launched so that each may start while the
- * previous kernel on the stream is still running.  sgq_quant_token_group
- * touches memory only after that kernel has finished.  The GEMM starts
- * reading Wq and Ws at once and reads Aq/As, and writes D, only after the
- * previous kernel has finished -- so Wq/Ws must not be written by the kernel
- * launched immediately before the GEMM on the same stream (a copy or memset
- * of the weights is fine).
+ * previous kernel on the stream is still running, and each lets its own
+ * successor start as soon as it has started.  sgq_quant_token_group touches
+ * memory only after the previous kernel has finished.  The GEMM reads Aq/As,
+ * and writes D, only after the previous kernel has finished, but it starts
+ * reading Wq and Ws at once, possibly while earlier kernels of an unbroken
+ * run of sgq kernels on the stream are still running.  So Wq/Ws must not be
+ * written by any kernel on the stream after the last host synchronisation
+ * (or non-kernel stream operation: copy, memset) that precedes the GEMM;
+ * weights written once at load time meet this.
  */
 sgq_status sgq_fp8_block_gemm(const void* Aq, const float* As, const void* Wq,
                               const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
