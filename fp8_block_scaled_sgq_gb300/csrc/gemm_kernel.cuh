@@ -47,8 +47,9 @@ namespace gemm {
 
 constexpr int kBM = 128;          // MMA M: rows of the "A" operand per tile
 constexpr int kBK = 128;          // K elements (bytes) per pipeline stage
-constexpr int kNumThreads = 384;  // 12 warps
+constexpr int kNumThreads = 384;  // 12 warps; configurations with two MMA warps add warp 12
 constexpr int kEpiWarp0 = 3;
+constexpr int kMma2Warp = 12;     // second MMA issuer (two-issuer configurations)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 480;  // two 16-column scale-factor slots at 480 and 496
 constexpr uint64_t kTimeoutNs = 1ull << 30;
@@ -237,6 +238,11 @@ __device__ __forceinline__ uint32_t sf_word(const float* row, int kcol, uint32_t
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
 struct Cfg {
+    // Swap-AB tiles are narrow (N <= 64): an MMA costs about as much to issue
+    // as a full-width one, so two warps issue alternate K stages of each item
+    // into separate accumulators, which the epilogue adds in a fixed order.
+    static constexpr int kMmaWarps = kSwap ? 2 : 1;
+    static constexpr int kThreads = kNumThreads + 32 * (kMmaWarps - 1);
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -255,12 +261,12 @@ struct Cfg {
     static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
     static constexpr size_t kOffSf = kOffB + size_t(kStages) * kBBytes;
     static constexpr size_t kOffInfo = kOffSf + size_t(kStages) * sizeof(SfSlot<BN>);
-    static constexpr size_t kOffBar = kOffInfo + size_t(kAccBufs) * sizeof(Info<BN>);
-    static constexpr int kNumBars = 3 * kStages + 2 * kAccBufs + 1;
+    static constexpr size_t kOffBar = kOffInfo + size_t(kMmaWarps * kAccBufs) * sizeof(Info<BN>);
+    static constexpr int kNumBars = 3 * kStages + (2 * kAccBufs + 1) * kMmaWarps;
     static constexpr size_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr size_t kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-    static_assert(kAccBufs * BN <= int(kSfCol), "TMEM budget");
+    static_assert(kMmaWarps * kAccBufs * BN <= int(kSfCol) - 32 * (kMmaWarps - 1), "TMEM budget");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
     static_assert(kColGroups <= 64, "raw column-scale slot");
     static_assert(kStages <= 8, "cp.async group depth");
@@ -268,7 +274,7 @@ struct Cfg {
 };
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma>::kThreads), 1)
     fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                           const GemmArgs a) {
@@ -287,10 +293,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t bar0 = ptx::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kStages + kAccBufs + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
-    auto sraw_bar = [&](int s) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 1 + s); };
+    // accumulator barriers per (MMA warp m, buffer b)
+    constexpr int kMW = C::kMmaWarps;
+    auto accf_bar = [&](int m, int b) { return bar0 + 8u * (2 * kStages + m * kAccBufs + b); };
+    auto acce_bar = [&](int m, int b) { return bar0 + 8u * (2 * kStages + (kMW + m) * kAccBufs + b); };
+    auto drain_bar = [&](int m) { return bar0 + 8u * (2 * kStages + 2 * kMW * kAccBufs + m); };
+    auto sraw_bar = [&](int s) { return bar0 + 8u * (2 * kStages + (2 * kAccBufs + 1) * kMW + s); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -301,11 +309,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_init(full_bar(s), 2);   // producer expect_tx + scale loader
             ptx::mbar_init(empty_bar(s), 1);  // tcgen05.commit
         }
-        for (int b = 0; b < kAccBufs; ++b) {
-            ptx::mbar_init(accf_bar(b), 2);   // MMA thread arrive + tcgen05.commit
-            ptx::mbar_init(acce_bar(b), 8);   // one arrive per epilogue warp
+        for (int m = 0; m < kMW; ++m) {
+            for (int b = 0; b < kAccBufs; ++b) {
+                ptx::mbar_init(accf_bar(m, b), 2);   // MMA thread arrive + tcgen05.commit
+                ptx::mbar_init(acce_bar(m, b), 8);   // one arrive per epilogue warp
+            }
+            ptx::mbar_init(drain_bar(m), 1);
         }
-        ptx::mbar_init(drain_bar, 1);
         for (int s = 0; s < kStages; ++s) ptx::mbar_init(sraw_bar(s), 1);   // raw scales landed (TMA)
         misc[1] = 0;
         ptx::fence_mbar_init();
@@ -584,11 +594,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::cp_async_wait_pending(0);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || (kMW > 1 && warp == kMma2Warp)) {
         // ---------------------------------------------------------- MMA issuer
         // The whole warp runs this loop in lock-step; every tcgen05 instruction
         // is issued by lane 0 through a predicate inside the asm, so the warp
-        // never diverges and descriptors stay warp-uniform.
+        // never diverges and descriptors stay warp-uniform.  With two issuers,
+        // issuer mw takes the K stages at positions pos % 2 == mw of each item
+        // and owns accumulators, scale slots and barriers of its own.
+        const int mw = warp == 1 ? 0 : 1;
         constexpr uint32_t idesc_f8 = ptx::idesc_f8(kBM, BN);
         constexpr uint32_t idesc_mx = ptx::idesc_mxf8(kBM, BN);
         const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
@@ -606,13 +619,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         uint32_t acc_flag = 0;  // 0 for the first MMA of an open segment
         auto acc_buf = [&](uint32_t u) { return static_cast<int>(u % kAccBufs); };
         auto acc_par = [&](uint32_t u) { return (u / kAccBufs) & 1u; };
+        Info<BN>* my_info = info + mw * kAccBufs;
+        const uint32_t acc_col0 = static_cast<uint32_t>(mw * kAccBufs * BN);
+        const uint32_t sf_col0 = kSfCol - 32u * static_cast<uint32_t>(mw);
         // Hands the open accumulator segment to the epilogue.
         auto close_segment = [&](uint32_t flags) {
             const int b = acc_buf(seg);
-            if (lane == 0) info[b].flags = flags;
+            if (lane == 0) my_info[b].flags = flags;
             __syncwarp();
-            ptx::mbar_arrive_if(leader, accf_bar(b));
-            ptx::tc_commit_if(leader, accf_bar(b));
+            ptx::mbar_arrive_if(leader, accf_bar(mw, b));
+            ptx::tc_commit_if(leader, accf_bar(mw, b));
             ++seg;
         };
         // Descriptors are linear in the start address: a stage's descriptor is
@@ -625,6 +641,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // A K stage shorter than 128 exists only when K % 128 != 0 (last stage).
         const bool ragged_k = (a.K % kBK) != 0;
         while (it.valid(a) && !failed) {
+            if (kMW > 1 && (it.pos % kMW) != mw) {   // the other issuer's stage
+                it.next(a);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                continue;
+            }
+            // this issuer's last stage of the item
+            const bool my_last = it.pos + kMW >= it.nkb;
             if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
             ptx::tc_fence_after();
             if (lane == 0) trace_ev(a, 40 + (mma_jobs & 31));
@@ -636,19 +659,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const bool mx = slot.pow2 != 0u && !a.force_promote;
             if (mx) {
                 if (!seg_open) {
-                    if (!wait_bar(acce_bar(acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
+                    if (!wait_bar(acce_bar(mw, acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     seg_open = true;
                     acc_flag = 0;
                 }
-                const uint32_t sfs = kSfCol + 16u * (mx_used & 1u);
+                const uint32_t sfs = sf_col0 + 16u * (mx_used & 1u);
                 const uint32_t t_sfa = tmem + sfs, t_sfb = tmem + sfs + 4u;
                 const uint64_t slot_off = static_cast<uint64_t>(stage) * kSlotStep;
                 ptx::tmem_cp_32x128b_x4_if(leader, t_sfa, sfa_base + slot_off);
 #pragma unroll
                 for (int h = 0; h < C::kSfbCopies; ++h)
                     ptx::tmem_cp_32x128b_x4_if(leader, t_sfb + 4u * h, sfb_base + slot_off + 32u * h);
-                const uint32_t d = tmem + static_cast<uint32_t>(acc_buf(seg) * BN);
+                const uint32_t d = tmem + acc_col0 + static_cast<uint32_t>(acc_buf(seg) * BN);
                 if (nq == 4) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -673,40 +696,39 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int steps = kBlk128 ? nq : 1;
                 for (int gidx = 0; gidx < ngroups; ++gidx) {
                     const int b = acc_buf(seg);
-                    if (!wait_bar(acce_bar(b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
+                    if (!wait_bar(acce_bar(mw, b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     const int j = gidx;  // scale chunk (blk_k == 128: chunk 0 holds the block scale)
                     const int q = C::kNld == 1 ? static_cast<int>(slot.kcol) : j;
                     for (int r = lane; r < 128; r += 32)
-                        info[b].lane_s[r] = slot.lane_raw[kSwap ? r / kBlkN : r][q];
-                    for (int c = lane; c < BN; c += 32) info[b].col_s[c] = slot.col_raw[c / kColGroup][q];
-                    const bool last = it.last_kb() && gidx == ngroups - 1;
-                    if (lane == 0) info[b].flags = kInfoPromote | (last ? kInfoLast : 0u);
+                        my_info[b].lane_s[r] = slot.lane_raw[kSwap ? r / kBlkN : r][q];
+                    for (int c = lane; c < BN; c += 32) my_info[b].col_s[c] = slot.col_raw[c / kColGroup][q];
+                    const bool last = my_last && gidx == ngroups - 1;
+                    if (lane == 0) my_info[b].flags = kInfoPromote | (last ? kInfoLast : 0u);
                     __syncwarp();
-                    const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                    const uint32_t d = tmem + acc_col0 + static_cast<uint32_t>(b * BN);
                     for (int t = 0; t < steps; ++t) {
                         const int jj = gidx * steps + t;   // 32-wide chunk inside the stage
                         ptx::mma_f8_if(leader, d, ad0 + 2u * jj, bd0 + 2u * jj, idesc_f8, t > 0 ? 1u : 0u);
                     }
-                    ptx::mbar_arrive_if(leader, accf_bar(b));
-                    ptx::tc_commit_if(leader, accf_bar(b));
+                    ptx::mbar_arrive_if(leader, accf_bar(mw, b));
+                    ptx::tc_commit_if(leader, accf_bar(mw, b));
                     ++seg;
                 }
                 if (failed) break;
             }
             ptx::tc_commit_if(leader, empty_bar(stage));  // frees the stage when its MMAs finish
             if (lane == 0) trace_ev(a, 200 + ((mma_jobs - 1) & 15));
-            const bool item_end = it.last_kb();
             it.next(a);
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
-            if (item_end && seg_open) {
+            if (my_last && seg_open) {
                 close_segment(kInfoLast);
                 seg_open = false;
             }
         }
         // Let every tcgen05 op issued above land before teardown.
-        ptx::tc_commit_if(leader, drain_bar);
-        if (lane == 0) wait_bar(drain_bar, 0, sync, 5);
+        ptx::tc_commit_if(leader, drain_bar(mw));
+        if (lane == 0) wait_bar(drain_bar(mw), 0, sync, 5);
         __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
@@ -721,42 +743,100 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         JobIter it;
         it.begin(a);
-        uint32_t seg = 0;
+        uint32_t seg0 = 0, seg1 = 0;   // segments consumed per MMA issuer
         uint32_t n_items = 0;
         float acc[kCols];
-        while (it.valid(a)) {
-            bool failed = false;
-            bool first = true;
-            while (true) {
-                const int b = static_cast<int>(seg % kAccBufs);
-                const uint32_t par = (seg / kAccBufs) & 1u;
-                if (!wait_bar_warp(accf_bar(b), par, sync, 4, true)) { failed = true; break; }
-                ptx::tc_fence_after();
-                const uint32_t flags = info[b].flags;
-                const bool promote = (flags & kInfoPromote) != 0u;
-                const float ls = promote ? info[b].lane_s[r_in_tile] : 1.0f;
+        float acc1[kCols];             // second issuer's sum (two-issuer configurations)
+        // Adds one accumulator segment of issuer m into `dst` (first: overwrite).
+        auto consume = [&](int m, uint32_t sg, bool first, float (&dst)[kCols]) {
+            const int b = static_cast<int>(sg % kAccBufs);
+            const Info<BN>& inf = info[m * kAccBufs + b];
+            const uint32_t flags = inf.flags;
+            const bool promote = (flags & kInfoPromote) != 0u;
+            const float ls = promote ? inf.lane_s[r_in_tile] : 1.0f;
+            const uint32_t col = static_cast<uint32_t>((m * kAccBufs + b) * BN + c_begin);
 #pragma unroll
-                for (int c0 = 0; c0 < kCols; c0 += kLd) {
-                    uint32_t r[kLd];
-                    ptx::tmem_ld<kLd>(t_lane + static_cast<uint32_t>(b * BN + c_begin + c0), r);
-                    ptx::tmem_wait_ld();
+            for (int c0 = 0; c0 < kCols; c0 += kLd) {
+                uint32_t r[kLd];
+                ptx::tmem_ld<kLd>(t_lane + col + static_cast<uint32_t>(c0), r);
+                ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < kLd; ++i) {
-                        const float v = __uint_as_float(r[i]);
-                        if (promote) {
-                            const float sc = ls * info[b].col_s[c_begin + c0 + i];
-                            acc[c0 + i] = first ? v * sc : fmaf(v, sc, acc[c0 + i]);
-                        } else {
-                            acc[c0 + i] = first ? v : acc[c0 + i] + v;
-                        }
+                for (int i = 0; i < kLd; ++i) {
+                    const float v = __uint_as_float(r[i]);
+                    if (promote) {
+                        const float sc = ls * inf.col_s[c_begin + c0 + i];
+                        dst[c0 + i] = first ? v * sc : fmaf(v, sc, dst[c0 + i]);
+                    } else {
+                        dst[c0 + i] = first ? v : dst[c0 + i] + v;
                     }
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(acce_bar(b));
-                ++seg;
-                first = false;
-                if (flags & kInfoLast) break;
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acce_bar(m, b));
+            return (flags & kInfoLast) != 0u;
+        };
+        while (it.valid(a)) {
+            bool failed = false;
+            if (kMW == 1) {
+                bool first = true;
+                while (true) {
+                    const int b = static_cast<int>(seg0 % kAccBufs);
+                    if (!wait_bar_warp(accf_bar(0, b), (seg0 / kAccBufs) & 1u, sync, 4, true)) {
+                        failed = true;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const bool last = consume(0, seg0, first, acc);
+                    ++seg0;
+                    first = false;
+                    if (last) break;
+                }
+            } else {
+                // Issuer 1 has stages in the item only when it has two or more.
+                bool done0 = false, done1 = it.nkb < 2;
+                bool first0 = true, first1 = true;
+                while (!(done0 && done1)) {
+                    // lane 0 polls both issuers' next segment; take whichever is ready
+                    int pick = -1;
+                    if (lane == 0) {
+                        const uint64_t t0 = ptx::globaltimer();
+                        uint32_t spins = 0;
+                        while (true) {
+                            if (!done0 && ptx::mbar_test_wait(accf_bar(0, static_cast<int>(seg0 % kAccBufs)),
+                                                              (seg0 / kAccBufs) & 1u)) { pick = 0; break; }
+                            if (!done1 && ptx::mbar_test_wait(accf_bar(1, static_cast<int>(seg1 % kAccBufs)),
+                                                              (seg1 / kAccBufs) & 1u)) { pick = 1; break; }
+                            if ((++spins & 15u) == 0) {
+                                if (*sync.abort_flag) break;
+                                if (ptx::globaltimer() - t0 > kTimeoutNs) {
+                                    *sync.abort_flag = 1u;
+                                    atomicOr(sync.status, kStatusTimeout | (4u << 8));
+                                    break;
+                                }
+                            }
+                            if (spins > 8) __nanosleep(64);
+                        }
+                    }
+                    pick = __shfl_sync(0xFFFFFFFFu, pick, 0);
+                    __syncwarp();
+                    if (pick < 0) { failed = true; break; }
+                    ptx::tc_fence_after();
+                    if (pick == 0) {
+                        done0 = consume(0, seg0, first0, acc);
+                        ++seg0;
+                        first0 = false;
+                    } else {
+                        done1 = consume(1, seg1, first1, acc1);
+                        ++seg1;
+                        first1 = false;
+                    }
+                }
+                // fixed order: issuer 0's sum + issuer 1's sum
+                if (!failed && it.nkb >= 2) {
+#pragma unroll
+                    for (int c = 0; c < kCols; ++c) acc[c] += acc1[c];
+                }
             }
             if (epi_any(failed || *sync.abort_flag)) break;
             if (epi_tid == 0) trace_ev(a, 136 + 4 * (n_items & 15));
@@ -767,46 +847,77 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (a.splits > 1) {
                 // fp32 partial of this split; the last split to arrive sums all
                 // partials in split order (deterministic) and stores the tile.
-                float* part = a.partial + (static_cast<int64_t>(it.tile) * a.splits + it.split) * (kBM * BN) +
-                              r_in_tile * BN + c_begin;
-                // rows past the operand's end carry nothing: neither written nor read
+                // Rows past the operand's end carry nothing: neither written nor read.
                 const bool live = grow < a.rows;
-                if (live) {
+                const int64_t tile_base = static_cast<int64_t>(it.tile) * a.splits * (kBM * BN);
+                if (kSwap) {
+                    // column-major tile: one column of a warp's 32 rows is one 128-byte line
+                    float* part = a.partial + tile_base + (static_cast<int64_t>(it.split) * BN + c_begin) * kBM +
+                                  r_in_tile;
+                    if (live) {
 #pragma unroll
-                    for (int c = 0; c < kCols; c += 4)
-                        *reinterpret_cast<float4*>(part + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                        for (int c = 0; c < kCols; ++c) part[c * kBM] = acc[c];
+                    }
+                } else {
+                    float* part = a.partial + tile_base + static_cast<int64_t>(it.split) * (kBM * BN) +
+                                  r_in_tile * BN + c_begin;
+                    if (live) {
+#pragma unroll
+                        for (int c = 0; c < kCols; c += 4)
+                            *reinterpret_cast<float4*>(part + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                    }
                 }
-                __threadfence();
                 epi_sync();
                 if (epi_tid == 0) {
                     trace_ev(a, 137 + 4 * (n_items & 15));
+                    // The barrier orders every epilogue thread's partial before this
+                    // fence, which releases them with the arrival; the last arriver's
+                    // fence after the atomic acquires the other splits' partials.
+                    __threadfence();
                     const uint32_t old = atomicAdd(a.counters + it.tile, 1u);
-                    misc[2] = (old == static_cast<uint32_t>(a.splits - 1)) ? 1u : 0u;
+                    const bool last_split = old == static_cast<uint32_t>(a.splits - 1);
+                    if (last_split) __threadfence();
+                    misc[2] = last_split ? 1u : 0u;
                 }
                 epi_sync();
                 store = misc[2] != 0u;
                 if (store && live) {
-                    __threadfence();
-                    const float* base = a.partial + static_cast<int64_t>(it.tile) * a.splits * (kBM * BN) +
-                                        r_in_tile * BN + c_begin;
-                    // p_0 + p_1 + ... in split order, all read back from L2
+                    if (kSwap) {
+                        // p_0 + p_1 + ... in split order; this split's own term from registers
+                        const float* base = a.partial + tile_base + static_cast<int64_t>(c_begin) * kBM + r_in_tile;
+                        float (&sum)[kCols] = acc1;   // free once the issuers' sums are combined
+                        for (int sp = 0; sp < a.splits; ++sp) {
+                            const float* p = base + static_cast<int64_t>(sp) * (BN * kBM);
+                            const bool own = sp == it.split;
 #pragma unroll
-                    for (int c = 0; c < kCols; c += 4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4*>(base + c));
-                        acc[c] = v.x;
-                        acc[c + 1] = v.y;
-                        acc[c + 2] = v.z;
-                        acc[c + 3] = v.w;
-                    }
-                    for (int s = 1; s < a.splits; ++s) {
-                        const float* p = base + static_cast<int64_t>(s) * (kBM * BN);
+                            for (int c = 0; c < kCols; ++c) {
+                                const float v = own ? acc[c] : __ldcg(p + c * kBM);
+                                sum[c] = sp == 0 ? v : sum[c] + v;
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < kCols; ++c) acc[c] = sum[c];
+                    } else {
+                        const float* base = a.partial + tile_base + r_in_tile * BN + c_begin;
+                        // p_0 + p_1 + ... in split order, all read back from L2
 #pragma unroll
                         for (int c = 0; c < kCols; c += 4) {
-                            const float4 v = __ldcg(reinterpret_cast<const float4*>(p + c));
-                            acc[c] += v.x;
-                            acc[c + 1] += v.y;
-                            acc[c + 2] += v.z;
-                            acc[c + 3] += v.w;
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(base + c));
+                            acc[c] = v.x;
+                            acc[c + 1] = v.y;
+                            acc[c + 2] = v.z;
+                            acc[c + 3] = v.w;
+                        }
+                        for (int sp = 1; sp < a.splits; ++sp) {
+                            const float* p = base + static_cast<int64_t>(sp) * (kBM * BN);
+#pragma unroll
+                            for (int c = 0; c < kCols; c += 4) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4*>(p + c));
+                                acc[c] += v.x;
+                                acc[c + 1] += v.y;
+                                acc[c + 2] += v.z;
+                                acc[c + 3] += v.w;
+                            }
                         }
                     }
                 }
@@ -872,7 +983,7 @@ sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStre
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kNumThreads);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
