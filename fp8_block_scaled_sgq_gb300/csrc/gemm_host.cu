@@ -112,6 +112,8 @@ int env_int(const char* name, int dflt) {
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
     Plan p{};
+    static const int grid_max = env_int("SGQ_GRID_MAX", 0);
+    if (grid_max > 0 && grid_max < sm_count) sm_count = grid_max;
     static const int swap_max = env_int("SGQ_SWAP_MAX", 64);
     p.swap = M <= swap_max;
     p.bn = p.swap ? (M <= 16 ? 16 : (M <= 32 ? 32 : 64)) : 256;

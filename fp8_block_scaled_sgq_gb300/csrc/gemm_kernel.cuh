@@ -243,6 +243,10 @@ struct Cfg {
     // into separate accumulators, which the epilogue adds in a fixed order.
     static constexpr int kMmaWarps = kSwap ? 2 : 1;
     static constexpr int kThreads = kNumThreads + 32 * (kMmaWarps - 1);
+    // Weight stages loaded before the programmatic-dependency wait.  Loads of
+    // one SM leave in issue order, so a deep weight prefetch delays the first
+    // activation tiles behind it; the swap-AB (decode) tiles start with none.
+    static constexpr int kPrefetch = kSwap ? 0 : kStages;
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         // The weight operand does not depend on the preceding kernel, so the
-        // weight halves of the first kStages stages go out before the
+        // weight halves of the first C::kPrefetch stages go out before the
         // programmatic-dependency wait; activations only after it.
         // The whole warp runs the loop; lane 0 issues through predicated asm.
         {
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             it.begin(a);
             JobIter pre = it;
             int npre = 0;
-            while (npre < kStages && pre.valid(a)) {
+            while (npre < C::kPrefetch && pre.valid(a)) {
                 load_w(npre, pre);
                 pre.next(a);
                 ++npre;
