@@ -102,6 +102,7 @@ sgq_status get_workspace(cudaStream_t st, DevWs* out) {
 
 struct Plan {
     bool swap;
+    bool pair;   // CTA pairs on 256 x 256 tiles (cluster of two, cta_group::2)
     int bn, tiles_r, tiles_c, kb_total, kb_per_split, splits, items, grid;
 };
 
@@ -110,7 +111,7 @@ int env_int(const char* name, int dflt) {
     return v ? std::atoi(v) : dflt;
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count) {
     Plan p{};
     static const int grid_max = env_int("SGQ_GRID_MAX", 0);
     if (grid_max > 0 && grid_max < sm_count) sm_count = grid_max;
@@ -145,6 +146,19 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
     p.kb_per_split = (p.kb_total + best_s - 1) / best_s;
     p.items = static_cast<int>(tiles * best_s);
     p.grid = p.items < sm_count ? p.items : sm_count;
+    // Large M: pairs of CTAs can share 256 x 256 tiles, each loading half of
+    // the weight tile, which cuts the operand bytes every SM pulls per FLOP by
+    // a third.  Needs one split and TMA-loadable scale rows.  Off unless
+    // SGQ_PAIR=1: with per-stage scale boxes the pair's stages are bound by
+    // TMA operations per SM, not by bytes, and the single-CTA tiles are faster.
+    static const int pair_on = env_int("SGQ_PAIR", 0);
+    p.pair = pair_on != 0 && !p.swap && p.splits == 1 && M > kBM && ((K / blk_k) % 4) == 0;
+    if (p.pair) {
+        p.tiles_r = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
+        p.items = p.tiles_r * p.tiles_c;
+        const int pairs = p.items < sm_count / 2 ? p.items : sm_count / 2;
+        p.grid = 2 * pairs;
+    }
     return p;
 }
 
@@ -176,7 +190,7 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     sgq_status rc = device_info(&di);
     if (rc != SGQ_OK) return rc;
     if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
-    const gemm::Plan p = gemm::make_plan(M, N, K, di.sm_count);
+    const gemm::Plan p = gemm::make_plan(M, N, K, blk_k, di.sm_count);
     gemm::GemmArgs a{};
     a.As = As;
     a.Ws = Ws;
@@ -218,7 +232,7 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     const void* opA = p.swap ? Wq : Aq;
     const void* opB = p.swap ? Aq : Wq;
     if (gemm::make_tmap(&maps[0], opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
     // Scale rows are TMA-loadable when their pitch is a multiple of 16 bytes.
     const bool scale_tma = (a.ks % 4) == 0;
     maps[2] = maps[0];
@@ -231,10 +245,10 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
                                  p.swap ? p.bn : p.bn / blk_n) != SGQ_OK)
             return SGQ_ERR_CUDA;
     }
-    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
-    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
-    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
-    return gemm::dispatch_128_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
+    return gemm::dispatch_128_128(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -282,7 +296,7 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
     if (rc != SGQ_OK) return rc;
     if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
     // Same launch plan as sgq_fp8_block_gemm, so both give the same result.
-    const gemm::Plan p = gemm::make_plan(M, N, K, di.sm_count);
+    const gemm::Plan p = gemm::make_plan(M, N, K, blk_k, di.sm_count);
     gemm::GemmArgs a{};
     a.As = As;
     a.Ws = Ws;
@@ -323,7 +337,7 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
     const void* opA = p.swap ? Wq : Aq;
     const void* opB = p.swap ? Aq : Wq;
     if (gemm::make_tmap(&maps[0], opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
     const bool scale_tma = (a.ks % 4) == 0;
     maps[2] = maps[0];
     maps[3] = maps[1];
@@ -335,10 +349,10 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
                                  p.swap ? p.bn : p.bn / blk_n) != SGQ_OK)
             return SGQ_ERR_CUDA;
     }
-    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
-    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
-    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
-    return gemm::dispatch_128_128(p.swap, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
+    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
+    return gemm::dispatch_128_128(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
 }
 
 sgq_status read_and_clear_device_status(cudaStream_t st) {

@@ -71,6 +71,9 @@ struct alignas(128) SfSlot {
     float col_raw[64][4];
     uint32_t pow2;                      // every scale of the stage is 2^e
     uint32_t kcol;
+    // CTA pair: the peer's pow2 flag (word 0), staged in the peer's slot and
+    // copied into the leader's slot by the transfer that signals the stage.
+    alignas(16) uint32_t xfer[4];
 };
 
 template <int BN>
@@ -101,7 +104,7 @@ struct GemmArgs {
 // the tile) when a.krot is set, so CTAs that share an operand tile do not all
 // request the same lines at the same moment.
 struct JobIter {
-    int item, kb, kb0, nkb, pos, rot;
+    int item, kb, kb0, nkb, pos, rot, step;
     int tile, split, tr, tc;
     __device__ void load(const GemmArgs& a) {
         split = item % a.splits;
@@ -119,8 +122,10 @@ struct JobIter {
         pos = 0;
         kb = kb0 + rot;
     }
-    __device__ void begin(const GemmArgs& a) {
-        item = blockIdx.x;
+    // first item and stride: the CTA's (or CTA pair's) index and count
+    __device__ void begin(const GemmArgs& a, int first, int stride) {
+        item = first;
+        step = stride;
         if (item < a.items) load(a);
     }
     __device__ bool valid(const GemmArgs& a) const { return item < a.items; }
@@ -128,7 +133,7 @@ struct JobIter {
     // Advances one stage; returns true when it moved to a new item.
     __device__ bool next(const GemmArgs& a) {
         if (++pos >= nkb) {
-            item += gridDim.x;
+            item += step;
             if (item < a.items) load(a);
             return true;
         }
@@ -157,12 +162,18 @@ struct Sync {
     uint32_t* status;
 };
 
+// kCl: acquire at cluster scope (barriers that the other CTA of a pair arrives on).
+template <bool kCl>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+    return kCl ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+}
+template <bool kCl>
 static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where,
                                               bool backoff) {
     const uint64_t t0 = ptx::globaltimer();
     uint32_t spins = 0;
     while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (try_wait_scoped<kCl>(bar, parity)) return true;
         if ((++spins & 15u) == 0) {
             if (*s.abort_flag) return false;
             if (ptx::globaltimer() - t0 > kTimeoutNs) {
@@ -175,18 +186,20 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, con
     }
 }
 // Single-thread bounded wait.
+template <bool kCl = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, s, where, false);
+    if (try_wait_scoped<kCl>(bar, parity)) return true;
+    return wait_slow<kCl>(bar, parity, s, where, false);
 }
 // Warp-wide bounded wait: lane 0 polls (the other lanes park at the warp
 // barrier, keeping shared-memory traffic off the TMA path), then the result is
 // broadcast.  __syncwarp orders lane 0's acquire before the other lanes' reads.
+template <bool kCl = false>
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where,
                                               bool backoff) {
     uint32_t ok = 1;
-    if ((threadIdx.x & 31) == 0 && !ptx::mbar_try_wait(bar, parity))
-        ok = wait_slow(bar, parity, s, where, backoff) ? 1u : 0u;
+    if ((threadIdx.x & 31) == 0 && !try_wait_scoped<kCl>(bar, parity))
+        ok = wait_slow<kCl>(bar, parity, s, where, backoff) ? 1u : 0u;
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     __syncwarp();
     return ok != 0;
@@ -236,7 +249,7 @@ __device__ __forceinline__ uint32_t sf_word(const float* row, int kcol, uint32_t
     return w;
 }
 
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair>
 struct Cfg {
     // Swap-AB tiles are narrow (N <= 64): an MMA costs about as much to issue
     // as a full-width one, so two warps issue alternate K stages of each item
@@ -247,9 +260,14 @@ struct Cfg {
     // one SM leave in issue order, so a deep weight prefetch delays the first
     // activation tiles behind it; the swap-AB (decode) tiles start with none.
     static constexpr int kPrefetch = kSwap ? 0 : kStages;
+    // CTA pair (cluster of two, cta_group::2): the tile is 256 x BN; each CTA
+    // holds 128 A rows and BN/2 B rows per stage, the leader issues the MMAs.
+    static constexpr int kCG = kPair ? 2 : 1;
+    static constexpr int kTileRows = kBM * kCG;            // A rows per tile
     static constexpr int kABytes = kBM * kBK;
-    static constexpr int kBBytes = BN * kBK;
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBBytes = (BN / kCG) * kBK;       // B bytes per CTA and stage
+    static constexpr uint32_t kXferBytes = kPair ? 16u : 0u;      // the peer's scale-ready transfer
+    static constexpr int kStageBytes = kCG * (kABytes + kBBytes) + kXferBytes;   // bytes the full barrier expects
     static constexpr int kCols = BN / 2;  // accumulator columns per epilogue thread
     static constexpr int kLd = kCols < 16 ? kCols : 16;
     static constexpr int kSfbCopies = BN > 128 ? BN / 128 : 1;
@@ -272,17 +290,19 @@ struct Cfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(kMmaWarps * kAccBufs * BN <= int(kSfCol) - 32 * (kMmaWarps - 1), "TMEM budget");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
+    static_assert(!kPair || (!kSwap && BN == 256 && kScaleTma && kAccBufs == 1), "CTA-pair configuration");
     static_assert(kColGroups <= 64, "raw column-scale slot");
     static_assert(kStages <= 8, "cp.async group depth");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
-__global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma>::kThreads), 1)
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair>
+__global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>::kThreads), 1)
     fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                           const GemmArgs a) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma>;
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>;
+    constexpr int kCG = C::kCG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -307,16 +327,28 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Sync sync{reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
+    // CTA pair: rank 0 leads (issues every tcgen05 op of the pair); a pair
+    // walks the items with index blockIdx.x / 2.
+    const uint32_t rank = kPair ? ptx::cluster_rank() : 0u;
+    const int first_item = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int item_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    // first activation row of this CTA's share of the tile
+    auto a_row0 = [&](const JobIter& j) { return j.tr * C::kTileRows + static_cast<int>(rank) * kBM; };
+    // the same barrier in the leader (cluster address)
+    auto at_leader = [&](uint32_t bar) { return kPair ? ptx::mapa(bar, 0u) : bar; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(full_bar(s), 2);   // producer expect_tx + scale loader
+            // producer expect_tx + scale loader (pair: the peer's scale loader
+            // signals with a transfer counted in the expected bytes)
+            ptx::mbar_init(full_bar(s), 2);
             ptx::mbar_init(empty_bar(s), 1);  // tcgen05.commit
         }
         for (int m = 0; m < kMW; ++m) {
             for (int b = 0; b < kAccBufs; ++b) {
                 ptx::mbar_init(accf_bar(m, b), 2);   // MMA thread arrive + tcgen05.commit
-                ptx::mbar_init(acce_bar(m, b), 8);   // one arrive per epilogue warp
+                // one arrive per epilogue warp (pair leader: of both CTAs)
+                ptx::mbar_init(acce_bar(m, b), kPair ? 16 : 8);
             }
             ptx::mbar_init(drain_bar(m), 1);
         }
@@ -333,11 +365,12 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc_g<kCG>(ptx::smem_u32(misc), kTmemCols);
+        ptx::tmem_relinquish_g<kCG>();
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if (kPair) ptx::cluster_sync();   // both CTAs' barriers exist before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
     if (threadIdx.x == 0) {
@@ -362,28 +395,38 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
             auto w_dst = [&](int s) { return kSwap ? sA0 + s * C::kABytes : sB0 + s * C::kBBytes; };
             auto x_dst = [&](int s) { return kSwap ? sB0 + s * C::kBBytes : sA0 + s * C::kABytes; };
-            auto w_row = [&](const JobIter& j) { return kSwap ? j.tr * kBM : j.tc * BN; };
-            auto x_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : j.tr * kBM; };
+            auto w_row = [&](const JobIter& j) {
+                return kSwap ? j.tr * kBM : j.tc * BN + static_cast<int>(rank) * (BN / kCG);
+            };
+            auto x_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : a_row0(j); };
             // scale boxes: 4 columns starting at a 16-byte aligned column
             auto s_col = [&](const JobIter& j) { return (j.kb * C::kScalesPerStage) & ~3; };
             auto ws_dst = [&](int s) { return ptx::smem_u32(kSwap ? &sf[s].lane_raw[0][0] : &sf[s].col_raw[0][0]); };
             auto xs_dst = [&](int s) { return ptx::smem_u32(kSwap ? &sf[s].col_raw[0][0] : &sf[s].lane_raw[0][0]); };
             auto ws_row = [&](const JobIter& j) { return kSwap ? j.tr * (kBM / kBlkN) : j.tc * (BN / kBlkN); };
-            auto xs_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : j.tr * kBM; };
+            auto xs_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : a_row0(j); };
+            // Operand tiles signal the stage's full barrier; with a CTA pair both
+            // CTAs' tiles land on the leader's, which expects the bytes of both.
+            auto load_tile = [&](uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, int s) {
+                if (kPair)
+                    ptx::tma_load_2d_pair_if(leader, dst, m, x, y, at_leader(full_bar(s)));
+                else
+                    ptx::tma_load_2d_if(leader, dst, m, x, y, full_bar(s));
+            };
             auto load_w = [&](int s, const JobIter& j) {
-                ptx::mbar_arrive_expect_tx_if(leader, full_bar(s), C::kStageBytes);
+                ptx::mbar_arrive_expect_tx_if(leader && rank == 0u, full_bar(s), C::kStageBytes);
                 if (kScaleTma) {
                     ptx::mbar_arrive_expect_tx_if(leader, sraw_bar(s), C::kScaleBytes);
                     ptx::tma_load_2d_if(leader, ws_dst(s), tmWs, s_col(j), ws_row(j), sraw_bar(s));
                 }
-                ptx::tma_load_2d_if(leader, w_dst(s), tmW, j.kb * kBK, w_row(j), full_bar(s));
+                load_tile(w_dst(s), tmW, j.kb * kBK, w_row(j), s);
             };
             auto load_x = [&](int s, const JobIter& j) {
                 if (kScaleTma) ptx::tma_load_2d_if(leader, xs_dst(s), tmXs, s_col(j), xs_row(j), sraw_bar(s));
-                ptx::tma_load_2d_if(leader, x_dst(s), tmX, j.kb * kBK, x_row(j), full_bar(s));
+                load_tile(x_dst(s), tmX, j.kb * kBK, x_row(j), s);
             };
             JobIter it;
-            it.begin(a);
+            it.begin(a, first_item, item_step);
             JobIter pre = it;
             int npre = 0;
             while (npre < C::kPrefetch && pre.valid(a)) {
@@ -426,7 +469,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         // jobs ahead of the conversion.
         constexpr int kNld = C::kNld;
         auto convert = [&](SfSlot<BN>& slot, const JobIter& j, int kcol) {
-            const int row0 = j.tr * kBM, col0 = j.tc * BN;
+            const int row0 = kSwap ? j.tr * kBM : a_row0(j), col0 = j.tc * BN;
             uint32_t bad = 0;
             uint32_t w4[4];
 #pragma unroll
@@ -453,13 +496,18 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             if (lane == 0) {
                 slot.pow2 = all_ok ? 1u : 0u;
                 slot.kcol = static_cast<uint32_t>(kcol);
+                // pair: the leader decides per stage from both halves' flags
+                if (kPair && rank != 0u) {
+                    slot.xfer[0] = all_ok ? 1u : 0u;
+                    slot.xfer[1] = slot.xfer[2] = slot.xfer[3] = 0u;
+                }
             }
         };
         if (kScaleTma) {
             // Two converter warps (2 and 11) take alternate stages.
             const uint32_t sub = warp == 2 ? 0u : 1u;
             JobIter it;
-            it.begin(a);
+            it.begin(a, first_item, item_step);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t nfin = 0;
@@ -476,7 +524,16 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::mbar_arrive(full_bar(stage));
+                    if (kPair && rank != 0u) {
+                        // the peer signals the leader's barrier with a 16-byte
+                        // async copy of its flag word; the warp's fences above
+                        // order the scale words before it
+                        const uint32_t x = ptx::smem_u32(&sf[stage].xfer[0]);
+                        ptx::bulk_copy_to_cluster_if(1u, ptx::mapa(x, 0u), x, C::kXferBytes,
+                                                     at_leader(full_bar(stage)));
+                    } else {
+                        ptx::mbar_arrive(full_bar(stage));
+                    }
                     trace_ev(a, 72 + (nfin & 31));
                 }
                 ++nfin;
@@ -500,7 +557,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             uint32_t col_dst[kColLoads];
             int col_chunk[kColLoads];
             auto setup_item = [&](const JobIter& j) {
-                const int row0 = j.tr * kBM, col0 = j.tc * BN;
+                const int row0 = kSwap ? j.tr * kBM : a_row0(j), col0 = j.tc * BN;
                 if (!kSwap) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -561,8 +618,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 }
             };
             JobIter iss, fin;
-            iss.begin(a);
-            fin.begin(a);
+            iss.begin(a, first_item, item_step);
+            fin.begin(a, first_item, item_step);
             if (iss.valid(a)) setup_item(iss);
             uint32_t n_iss = 0, n_fin = 0;
             bool failed = false;
@@ -605,14 +662,15 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         // never diverges and descriptors stay warp-uniform.  With two issuers,
         // issuer mw takes the K stages at positions pos % 2 == mw of each item
         // and owns accumulators, scale slots and barriers of its own.
+        // With a CTA pair only the leader's warp issues (for both CTAs).
         const int mw = warp == 1 ? 0 : 1;
-        constexpr uint32_t idesc_f8 = ptx::idesc_f8(kBM, BN);
-        constexpr uint32_t idesc_mx = ptx::idesc_mxf8(kBM, BN);
+        constexpr uint32_t idesc_f8 = ptx::idesc_f8(C::kTileRows, BN);
+        constexpr uint32_t idesc_mx = ptx::idesc_mxf8(C::kTileRows, BN);
         const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
         const uint32_t leader = lane == 0 ? 1u : 0u;
         constexpr int kColGroup = kSwap ? 1 : kBlkN;
         JobIter it;
-        it.begin(a);
+        it.begin(a, first_item, item_step);
         int stage = 0;
         uint32_t phase = 0;
         uint32_t seg = 0;      // accumulator segments issued so far
@@ -626,13 +684,23 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         Info<BN>* my_info = info + mw * kAccBufs;
         const uint32_t acc_col0 = static_cast<uint32_t>(mw * kAccBufs * BN);
         const uint32_t sf_col0 = kSfCol - 32u * static_cast<uint32_t>(mw);
+        // Signals segment b to the epilogue(s): the MMA thread's arrive (after
+        // the Info writes; pair: also on the peer's barrier, release at cluster
+        // scope) and a commit that fires when the MMAs are done (both CTAs).
+        auto hand_over = [&](int b) {
+            ptx::mbar_arrive_if(leader, accf_bar(mw, b));
+            if (kPair) ptx::mbar_arrive_cluster_if(leader, ptx::mapa(accf_bar(mw, b), 1u));
+            ptx::tc_commit_g_if<kCG>(leader, accf_bar(mw, b));
+        };
         // Hands the open accumulator segment to the epilogue.
         auto close_segment = [&](uint32_t flags) {
             const int b = acc_buf(seg);
-            if (lane == 0) my_info[b].flags = flags;
+            if (lane == 0) {
+                my_info[b].flags = flags;
+                if (kPair) ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(&my_info[b].flags), 1u), flags);
+            }
             __syncwarp();
-            ptx::mbar_arrive_if(leader, accf_bar(mw, b));
-            ptx::tc_commit_if(leader, accf_bar(mw, b));
+            hand_over(b);
             ++seg;
         };
         // Descriptors are linear in the start address: a stage's descriptor is
@@ -644,7 +712,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         constexpr uint32_t kSlotStep = sizeof(SfSlot<BN>) >> 4;
         // A K stage shorter than 128 exists only when K % 128 != 0 (last stage).
         const bool ragged_k = (a.K % kBK) != 0;
-        while (it.valid(a) && !failed) {
+        while ((!kPair || rank == 0u) && it.valid(a) && !failed) {
             if (kMW > 1 && (it.pos % kMW) != mw) {   // the other issuer's stage
                 it.next(a);
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -652,7 +720,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             }
             // this issuer's last stage of the item
             const bool my_last = it.pos + kMW >= it.nkb;
-            if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
+            if (!wait_bar<kPair>(full_bar(stage), phase, sync, 2)) { failed = true; break; }
             ptx::tc_fence_after();
             if (lane == 0) trace_ev(a, 40 + (mma_jobs & 31));
             ++mma_jobs;
@@ -660,10 +728,14 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             const int nq = ragged_k ? min(4, (a.K - it.kb * kBK) / 32) : 4;
             const uint64_t ad0 = ad_base + static_cast<uint64_t>(stage * (C::kABytes >> 4));
             const uint64_t bd0 = bd_base + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
-            const bool mx = slot.pow2 != 0u && !a.force_promote;
+            // pair: block-scaled only when the scales of both CTAs' stages are 2^e
+            const bool mx = slot.pow2 != 0u && !a.force_promote && (!kPair || slot.xfer[0] != 0u);
             if (mx) {
                 if (!seg_open) {
-                    if (!wait_bar(acce_bar(mw, acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
+                    if (!wait_bar<kPair>(acce_bar(mw, acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) {
+                        failed = true;
+                        break;
+                    }
                     ptx::tc_fence_after();
                     seg_open = true;
                     acc_flag = 0;
@@ -671,22 +743,24 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 const uint32_t sfs = sf_col0 + 16u * (mx_used & 1u);
                 const uint32_t t_sfa = tmem + sfs, t_sfb = tmem + sfs + 4u;
                 const uint64_t slot_off = static_cast<uint64_t>(stage) * kSlotStep;
-                ptx::tmem_cp_32x128b_x4_if(leader, t_sfa, sfa_base + slot_off);
+                ptx::tmem_cp_g_if<kCG>(leader, t_sfa, sfa_base + slot_off);
 #pragma unroll
                 for (int h = 0; h < C::kSfbCopies; ++h)
-                    ptx::tmem_cp_32x128b_x4_if(leader, t_sfb + 4u * h, sfb_base + slot_off + 32u * h);
+                    ptx::tmem_cp_g_if<kCG>(leader, t_sfb + 4u * h, sfb_base + slot_off + 32u * h);
                 const uint32_t d = tmem + acc_col0 + static_cast<uint32_t>(acc_buf(seg) * BN);
                 if (nq == 4) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         // +32 bytes along K inside the swizzle atom = +2 in the start field
-                        ptx::mma_mxf8_if(leader, d, ad0 + 2u * j, bd0 + 2u * j, ptx::idesc_sf_ids(idesc_mx, j, j),
-                                         t_sfa, t_sfb, j == 0 ? acc_flag : 1u);
+                        ptx::mma_mxf8_g_if<kCG>(leader, d, ad0 + 2u * j, bd0 + 2u * j,
+                                                ptx::idesc_sf_ids(idesc_mx, j, j), t_sfa, t_sfb,
+                                                j == 0 ? acc_flag : 1u);
                     }
                 } else {
                     for (int j = 0; j < nq; ++j)
-                        ptx::mma_mxf8_if(leader, d, ad0 + 2u * j, bd0 + 2u * j, ptx::idesc_sf_ids(idesc_mx, j, j),
-                                         t_sfa, t_sfb, j == 0 ? acc_flag : 1u);
+                        ptx::mma_mxf8_g_if<kCG>(leader, d, ad0 + 2u * j, bd0 + 2u * j,
+                                                ptx::idesc_sf_ids(idesc_mx, j, j), t_sfa, t_sfb,
+                                                j == 0 ? acc_flag : 1u);
                 }
                 acc_flag = 1;
                 ++mx_used;
@@ -700,28 +774,39 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 const int steps = kBlk128 ? nq : 1;
                 for (int gidx = 0; gidx < ngroups; ++gidx) {
                     const int b = acc_buf(seg);
-                    if (!wait_bar(acce_bar(mw, b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
+                    if (!wait_bar<kPair>(acce_bar(mw, b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
                     ptx::tc_fence_after();
                     const int j = gidx;  // scale chunk (blk_k == 128: chunk 0 holds the block scale)
                     const int q = C::kNld == 1 ? static_cast<int>(slot.kcol) : j;
+                    const bool last = my_last && gidx == ngroups - 1;
+                    const uint32_t flags = kInfoPromote | (last ? kInfoLast : 0u);
                     for (int r = lane; r < 128; r += 32)
                         my_info[b].lane_s[r] = slot.lane_raw[kSwap ? r / kBlkN : r][q];
                     for (int c = lane; c < BN; c += 32) my_info[b].col_s[c] = slot.col_raw[c / kColGroup][q];
-                    const bool last = my_last && gidx == ngroups - 1;
-                    if (lane == 0) my_info[b].flags = kInfoPromote | (last ? kInfoLast : 0u);
+                    if (lane == 0) my_info[b].flags = flags;
+                    if (kPair) {
+                        // the peer's Info: its own row scales, the same column scales
+                        for (int r = lane; r < 128; r += 32)
+                            ptx::st_cluster_f32(ptx::mapa(ptx::smem_u32(&my_info[b].lane_s[r]), 1u),
+                                                ptx::ld_cluster_f32(ptx::mapa(ptx::smem_u32(&slot.lane_raw[r][q]), 1u)));
+                        for (int c = lane; c < BN; c += 32)
+                            ptx::st_cluster_f32(ptx::mapa(ptx::smem_u32(&my_info[b].col_s[c]), 1u),
+                                                slot.col_raw[c / kColGroup][q]);
+                        if (lane == 0) ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(&my_info[b].flags), 1u), flags);
+                        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+                    }
                     __syncwarp();
                     const uint32_t d = tmem + acc_col0 + static_cast<uint32_t>(b * BN);
                     for (int t = 0; t < steps; ++t) {
                         const int jj = gidx * steps + t;   // 32-wide chunk inside the stage
-                        ptx::mma_f8_if(leader, d, ad0 + 2u * jj, bd0 + 2u * jj, idesc_f8, t > 0 ? 1u : 0u);
+                        ptx::mma_f8_g_if<kCG>(leader, d, ad0 + 2u * jj, bd0 + 2u * jj, idesc_f8, t > 0 ? 1u : 0u);
                     }
-                    ptx::mbar_arrive_if(leader, accf_bar(mw, b));
-                    ptx::tc_commit_if(leader, accf_bar(mw, b));
+                    hand_over(b);
                     ++seg;
                 }
                 if (failed) break;
             }
-            ptx::tc_commit_if(leader, empty_bar(stage));  // frees the stage when its MMAs finish
+            ptx::tc_commit_g_if<kCG>(leader, empty_bar(stage));  // frees the stage (both CTAs) when its MMAs finish
             if (lane == 0) trace_ev(a, 200 + ((mma_jobs - 1) & 15));
             it.next(a);
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -731,8 +816,10 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             }
         }
         // Let every tcgen05 op issued above land before teardown.
-        ptx::tc_commit_if(leader, drain_bar(mw));
-        if (lane == 0) wait_bar(drain_bar(mw), 0, sync, 5);
+        if (!kPair || rank == 0u) {
+            ptx::tc_commit_local_g_if<kCG>(leader, drain_bar(mw));
+            if (lane == 0) wait_bar(drain_bar(mw), 0, sync, 5);
+        }
         __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
@@ -746,7 +833,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         const int epi_tid = ew * 32 + lane;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         JobIter it;
-        it.begin(a);
+        it.begin(a, first_item, item_step);
         uint32_t seg0 = 0, seg1 = 0;   // segments consumed per MMA issuer
         uint32_t n_items = 0;
         float acc[kCols];
@@ -777,7 +864,11 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(acce_bar(m, b));
+            // the accumulator may be overwritten: tell the issuing CTA
+            if (kPair && rank != 0u)
+                ptx::mbar_arrive_cluster_if(lane == 0 ? 1u : 0u, at_leader(acce_bar(m, b)));
+            else if (lane == 0)
+                ptx::mbar_arrive(acce_bar(m, b));
             return (flags & kInfoLast) != 0u;
         };
         while (it.valid(a)) {
@@ -786,7 +877,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 bool first = true;
                 while (true) {
                     const int b = static_cast<int>(seg0 % kAccBufs);
-                    if (!wait_bar_warp(accf_bar(0, b), (seg0 / kAccBufs) & 1u, sync, 4, true)) {
+                    if (!wait_bar_warp<kPair>(accf_bar(0, b), (seg0 / kAccBufs) & 1u, sync, 4, true)) {
                         failed = true;
                         break;
                     }
@@ -845,7 +936,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             if (epi_any(failed || *sync.abort_flag)) break;
             if (epi_tid == 0) trace_ev(a, 136 + 4 * (n_items & 15));
             // ------------------------------------------------ output
-            const int row0 = it.tr * kBM, col0 = it.tc * BN;
+            const int row0 = kSwap ? it.tr * kBM : a_row0(it), col0 = it.tc * BN;
             const int grow = row0 + r_in_tile;   // global row of the MMA A operand
             bool store = true;
             if (a.splits > 1) {
@@ -965,36 +1056,58 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
     __syncthreads();
     if (lane == 0 && warp < 11) trace_ev(a, 244 + warp);
     if (threadIdx.x == 0) trace_ev(a, 255);
+    // A pair's leader writes the peer's TMEM and reads its shared memory until
+    // its drain completes: neither CTA leaves before both are here.
+    if (kPair) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        ptx::tmem_dealloc_g<kCG>(tmem, kTmemCols);
     }
 }
 
-// Launches one instantiation with programmatic stream serialisation.
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma>
+// Launches one instantiation with programmatic stream serialisation (CTA
+// pairs: as clusters of two, at most as many pairs as can be resident).
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair = false>
 sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStream_t st) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma>;
-    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma>;
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>;
+    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>;
     static bool configured[64] = {};
+    static int max_pairs[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = kPair ? 2 : 1;
     if (!configured[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(C::kSmem)) != cudaSuccess)
             return SGQ_ERR_CUDA;
+        if (kPair) {
+            cudaLaunchConfig_t q = cfg;
+            q.gridDim = dim3(static_cast<unsigned>(grid));
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1) return SGQ_ERR_CUDA;
+            max_pairs[dev] = n;
+        }
         configured[dev] = true;
     }
-    cudaLaunchConfig_t cfg = {};
+    if (kPair) {
+        int pairs = grid / 2;
+        if (pairs > max_pairs[dev]) pairs = max_pairs[dev];
+        if (pairs > args.items) pairs = args.items;
+        grid = 2 * pairs;
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(C::kThreads);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], args) != cudaSuccess)
         return SGQ_ERR_CUDA;
     note_launch();
@@ -1003,8 +1116,17 @@ sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStre
 
 // One translation unit per [blk_n, blk_k] recipe instantiates all tile shapes.
 // maps: A operand, B operand, A-operand scales, B-operand scales.
+// Pair tiles (256 x 256, cta_group::2) need TMA-loaded scales.
+constexpr int kPairStages = 6;
 template <int kBlkN, int kBlkK, bool kScaleTma>
-sgq_status dispatch_tile(bool swap, int bn, const CUtensorMap* maps, const GemmArgs& a, int grid, cudaStream_t st) {
+sgq_status dispatch_tile(bool swap, bool pair, int bn, const CUtensorMap* maps, const GemmArgs& a, int grid,
+                         cudaStream_t st) {
+    if (pair) {
+        if constexpr (kScaleTma)
+            return run<256, kPairStages, false, 1, kBlkN, kBlkK, true, true>(maps, a, grid, st);
+        else
+            return SGQ_ERR_UNSUPPORTED;
+    }
     if (!swap) return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
     switch (bn) {
         case 16: return run<16, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
@@ -1013,16 +1135,16 @@ sgq_status dispatch_tile(bool swap, int bn, const CUtensorMap* maps, const GemmA
     }
 }
 template <int kBlkN, int kBlkK>
-sgq_status dispatch(bool swap, int bn, bool scale_tma, const CUtensorMap* maps, const GemmArgs& a, int grid,
-                    cudaStream_t st) {
-    return scale_tma ? dispatch_tile<kBlkN, kBlkK, true>(swap, bn, maps, a, grid, st)
-                     : dispatch_tile<kBlkN, kBlkK, false>(swap, bn, maps, a, grid, st);
+sgq_status dispatch(bool swap, bool pair, int bn, bool scale_tma, const CUtensorMap* maps, const GemmArgs& a,
+                    int grid, cudaStream_t st) {
+    return scale_tma ? dispatch_tile<kBlkN, kBlkK, true>(swap, pair, bn, maps, a, grid, st)
+                     : dispatch_tile<kBlkN, kBlkK, false>(swap, pair, bn, maps, a, grid, st);
 }
 
-sgq_status dispatch_32_32(bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_32_128(bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_128_32(bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_128_128(bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_32_32(bool, bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_32_128(bool, bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_128_32(bool, bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_128_128(bool, bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
 
 }  // namespace gemm
 }  // namespace sgq

@@ -251,6 +251,184 @@ __device__ __forceinline__ void tma_load_2d_if(uint32_t pred, uint32_t dst, cons
         : "memory");
 }
 
+
+// ------------------------------------------------------------------ CTA pairs
+// A cluster of two CTAs (ranks 0 and 1) drives one tcgen05 unit pair: rank 0
+// (the leader) issues every MMA, scale copy and commit with .cta_group::2;
+// both CTAs allocate the same TMEM columns.  A pair-issued op reads operand
+// A rows 0-127 and the first half of the B columns from the leader's shared
+// memory and the rest from the peer's, at the same offsets; the scale copy
+// fills each CTA's TMEM from its own shared memory; each CTA's accumulator
+// holds its 128 rows and all N columns.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive (release at cluster scope) on an mbarrier given by its cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster_if(uint32_t pred, uint32_t cluster_bar) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %1, 0;\n"
+        "@p mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n}" ::"r"(cluster_bar), "r"(pred)
+        : "memory");
+}
+// Bounded-wait building block with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// TMA tile load into this CTA's shared memory whose completion is signalled
+// on an mbarrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair_if(uint32_t pred, uint32_t dst, const CUtensorMap* m, int32_t x,
+                                                    int32_t y, uint32_t cluster_bar) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %5, 0;\n"
+        "@p cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(cluster_bar), "r"(pred)
+        : "memory");
+}
+
+// Bulk copy (async proxy) of `bytes` (multiple of 16) from this CTA's shared
+// memory to another CTA's, completing `bytes` of transactions on an mbarrier
+// in the destination CTA.  Used as a cheap cross-CTA signal with payload: the
+// copy's completion also orders this thread's earlier shared-memory writes
+// (published to the async proxy by fence.proxy.async) before the receiver.
+__device__ __forceinline__ void bulk_copy_to_cluster_if(uint32_t pred, uint32_t dst_cluster, uint32_t src_cta,
+                                                        uint32_t bytes, uint32_t cluster_bar) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "@p cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}" ::"r"(
+            dst_cluster),
+        "r"(src_cta), "r"(bytes), "r"(cluster_bar), "r"(pred)
+        : "memory");
+}
+
+// tcgen05 forms for one CTA (CG = 1) or a CTA pair (CG = 2).  Every tcgen05
+// instruction of a kernel uses the same group size.
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_g(uint32_t dst_smem, uint32_t ncols) {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                     : "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_g() {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_g(uint32_t taddr, uint32_t ncols) {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+template <int CG>
+__device__ __forceinline__ void mma_f8_g_if(uint32_t pred, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    if constexpr (CG == 1) {
+        mma_f8_if(pred, d_tmem, adesc, bdesc, idesc, accumulate);
+    } else {
+        asm volatile(
+            "{\n.reg .pred p, q;\nsetp.ne.b32 p, %5, 0;\nsetp.ne.b32 q, %4, 0;\n"
+            "@p tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, q;\n}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(pred)
+            : "memory");
+    }
+}
+template <int CG>
+__device__ __forceinline__ void mma_mxf8_g_if(uint32_t pred, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    if constexpr (CG == 1) {
+        mma_mxf8_if(pred, d_tmem, adesc, bdesc, idesc, sfa_tmem, sfb_tmem, accumulate);
+    } else {
+        asm volatile(
+            "{\n.reg .pred p, q;\nsetp.ne.b32 p, %7, 0;\nsetp.ne.b32 q, %6, 0;\n"
+            "@p tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+            " [%0], %1, %2, %3, [%4], [%5], q;\n}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(pred)
+            : "memory");
+    }
+}
+template <int CG>
+__device__ __forceinline__ void tmem_cp_g_if(uint32_t pred, uint32_t taddr, uint64_t sdesc) {
+    if constexpr (CG == 1) {
+        tmem_cp_32x128b_x4_if(pred, taddr, sdesc);
+    } else {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %2, 0;\n"
+            "@p tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n}" ::"r"(taddr), "l"(sdesc), "r"(pred)
+            : "memory");
+    }
+}
+// Commit: CG = 1 arrives on this CTA's `bar`; CG = 2 arrives on `bar` (same
+// offset) in both CTAs of the pair.
+template <int CG>
+__device__ __forceinline__ void tc_commit_g_if(uint32_t pred, uint32_t bar) {
+    if constexpr (CG == 1) {
+        tc_commit_if(pred, bar);
+    } else {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %1, 0;\n"
+            "@p tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %2;\n}" ::"r"(
+                bar),
+            "r"(pred), "h"(static_cast<uint16_t>(3))
+            : "memory");
+    }
+}
+// Commit arriving on this CTA's `bar` only (pair form: the leader's own barrier).
+template <int CG>
+__device__ __forceinline__ void tc_commit_local_g_if(uint32_t pred, uint32_t bar) {
+    if constexpr (CG == 1) {
+        tc_commit_if(pred, bar);
+    } else {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %1, 0;\n"
+            "@p tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar),
+            "r"(pred)
+            : "memory");
+    }
+}
+
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor (tcgen05 form): start >> 4 in [0,14),
 // leading byte offset >> 4 in [16,30), stride byte offset >> 4 in [32,46),

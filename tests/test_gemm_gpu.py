@@ -114,6 +114,25 @@ def test_mixed_pow2_and_fp32_scales(M, bk):
     check_gemm(run_gpu(aq, a_s, wq, ws, bn, bk), dref, bound, f"mixed M={M} bk={bk}")
 
 
+@pytest.mark.parametrize("rows", [(130, 140), (3, 9), (250, 256)])
+@pytest.mark.parametrize("bk", [32, 128])
+def test_pair_tile_one_half_not_pow2(rows, bk):
+    """Large-M tiles are computed by pairs of CTAs, each holding half of the
+    rows.  Activation scales that are not powers of two in only one half of a
+    tile (rows 128-255 of the first tile, or 0-127) must send the whole tile's
+    stage to the promotion path, for both halves."""
+    M, N, K, bn = 300, 520, 1024, 128
+    x = synth.activation(M, K, seed=5)
+    w = synth.weight(N, K, seed=5)
+    aq, a_s = oracle.quant_token_group(x, bk, True)
+    wq, ws = oracle.quant_weight_block(w, bn, bk, True)
+    stage_cols = 128 // bk
+    for st in (1, 4, 5):
+        a_s[rows[0]:rows[1], st * stage_cols:(st + 1) * stage_cols] *= np.float32(1.3)
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, bn, bk)
+    check_gemm(run_gpu(aq, a_s, wq, ws, bn, bk), dref, bound, f"half rows={rows} bk={bk}")
+
+
 @pytest.mark.parametrize("M", [1, 16, 64, 4096])
 def test_deterministic(M):
     """Split-K sums partials in a fixed order: repeated calls are bitwise equal."""
