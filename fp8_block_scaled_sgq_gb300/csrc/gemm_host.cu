@@ -49,12 +49,14 @@ sgq_status make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, i
     return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
 }
 
-// 2-D map over a [rows, ks] fp32 scale matrix; box = 4 columns (16 bytes) x
-// box_rows rows, no swizzle.  Rows past the matrix read as zero.
-sgq_status make_scale_map(CUtensorMap* m, const float* ptr, int64_t rows, int64_t ks, int box_rows) {
+// 2-D map over a [rows, ks] fp32 scale matrix; box = box_cols columns (a
+// multiple of 4, i.e. of 16 bytes) x box_rows rows, no swizzle.  Rows and
+// columns past the matrix read as zero.
+sgq_status make_scale_map(CUtensorMap* m, const float* ptr, int64_t rows, int64_t ks, int box_rows,
+                          int box_cols) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(ks), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ks) * sizeof(float)};
-    cuuint32_t box[2] = {4u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -152,7 +154,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count) {
     // SGQ_PAIR=1: with per-stage scale boxes the pair's stages are bound by
     // TMA operations per SM, not by bytes, and the single-CTA tiles are faster.
     static const int pair_on = env_int("SGQ_PAIR", 0);
-    p.pair = pair_on != 0 && !p.swap && p.splits == 1 && M > kBM && ((K / blk_k) % 4) == 0;
+    const int64_t ks = K / blk_k;
+    p.pair = pair_on != 0 && !p.swap && p.splits == 1 && M > kBM && (ks % 4) == 0 &&
+             ks >= (blk_k == 128 ? 8 : 16);   // the kernel's TMA scale-group path
     if (p.pair) {
         p.tiles_r = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
         p.items = p.tiles_r * p.tiles_c;
@@ -209,8 +213,6 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     a.items = p.items;
     a.group_r = 16;
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
-    static const int krot = gemm::env_int("SGQ_KROT", 0);
-    a.krot = krot;
     rc = gemm::status_word(&a.status);
     if (rc != SGQ_OK) return rc;
 #ifdef SGQ_TRACE
@@ -233,16 +235,21 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     const void* opB = p.swap ? Aq : Wq;
     if (gemm::make_tmap(&maps[0], opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
     if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
-    // Scale rows are TMA-loadable when their pitch is a multiple of 16 bytes.
-    const bool scale_tma = (a.ks % 4) == 0;
+    // Scale rows are TMA-loadable when their pitch is a multiple of 16 bytes
+    // and they are at least one box (one group of K stages) wide: a box wider
+    // than the matrix's rows is not used.
+    static const int scale_tma_on = gemm::env_int("SGQ_SCALE_TMA", 1);
+    const int gcols = blk_k == 128 ? 8 : 16;
+    const bool scale_tma = scale_tma_on != 0 && (a.ks % 4) == 0 && a.ks >= gcols;
     maps[2] = maps[0];
     maps[3] = maps[1];
     if (scale_tma) {
         const int64_t nb = (N + blk_n - 1) / blk_n;
+        // one box = the scales of a group of four K stages (see the kernel)
         if (gemm::make_scale_map(&maps[2], p.swap ? Ws : As, p.swap ? nb : M, a.ks,
-                                 p.swap ? gemm::kBM / blk_n : gemm::kBM) != SGQ_OK ||
+                                 p.swap ? gemm::kBM / blk_n : gemm::kBM, gcols) != SGQ_OK ||
             gemm::make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks,
-                                 p.swap ? p.bn : p.bn / blk_n) != SGQ_OK)
+                                 p.swap ? p.bn : p.bn / blk_n, gcols) != SGQ_OK)
             return SGQ_ERR_CUDA;
     }
     if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
@@ -315,8 +322,6 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
     a.items = p.items;
     a.group_r = 16;
     a.force_promote = 0;
-    static const int krot = gemm::env_int("SGQ_KROT", 0);
-    a.krot = krot;
     rc = gemm::status_word(&a.status);
     if (rc != SGQ_OK) return rc;
     if (p.splits > 1) {
@@ -338,15 +343,21 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
     const void* opB = p.swap ? Aq : Wq;
     if (gemm::make_tmap(&maps[0], opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
     if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
-    const bool scale_tma = (a.ks % 4) == 0;
+    // Scale rows are TMA-loadable when their pitch is a multiple of 16 bytes
+    // and they are at least one box (one group of K stages) wide: a box wider
+    // than the matrix's rows is not used.
+    static const int scale_tma_on = gemm::env_int("SGQ_SCALE_TMA", 1);
+    const int gcols = blk_k == 128 ? 8 : 16;
+    const bool scale_tma = scale_tma_on != 0 && (a.ks % 4) == 0 && a.ks >= gcols;
     maps[2] = maps[0];
     maps[3] = maps[1];
     if (scale_tma) {
         const int64_t nb = (N + blk_n - 1) / blk_n;
+        // one box = the scales of a group of four K stages (see the kernel)
         if (gemm::make_scale_map(&maps[2], p.swap ? Ws : As, p.swap ? nb : M, a.ks,
-                                 p.swap ? gemm::kBM / blk_n : gemm::kBM) != SGQ_OK ||
+                                 p.swap ? gemm::kBM / blk_n : gemm::kBM, gcols) != SGQ_OK ||
             gemm::make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks,
-                                 p.swap ? p.bn : p.bn / blk_n) != SGQ_OK)
+                                 p.swap ? p.bn : p.bn / blk_n, gcols) != SGQ_OK)
             return SGQ_ERR_CUDA;
     }
     if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);

@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -58,7 +59,7 @@ constexpr uint32_t kInfoPromote = 1u;
 constexpr uint32_t kInfoLast = 2u;
 constexpr uint32_t kStatusTimeout = 1u;
 
-template <int BN>
+template <int BN, int kLaneRows, int kColRows>
 struct alignas(128) SfSlot {
     uint32_t sfa[128];                  // UE8M0 words of the A operand (tcgen05.cp order)
     uint32_t sfb[BN < 128 ? 128 : BN];  // UE8M0 words of the B operand
@@ -66,14 +67,24 @@ struct alignas(128) SfSlot {
     //   lane_raw: A operand -- activation rows (normal) or weight n-blocks (swap)
     //   col_raw:  B operand -- weight n-blocks (normal) or tokens (swap)
     // Column j holds 32-wide K chunk j; when one scale covers the whole stage
-    // (blk_k = 128) it sits in column `kcol`.
-    float lane_raw[128][4];
-    float col_raw[64][4];
+    // (blk_k = 128) it sits in column `kcol`.  With grouped scale loads these
+    // are filled only for stages that need the fp32 promotion step.
+    float lane_raw[kLaneRows][4];
+    float col_raw[kColRows][4];
     uint32_t pow2;                      // every scale of the stage is 2^e
     uint32_t kcol;
     // CTA pair: the peer's pow2 flag (word 0), staged in the peer's slot and
     // copied into the leader's slot by the transfer that signals the stage.
     alignas(16) uint32_t xfer[4];
+};
+
+// Raw fp32 scales of up to four consecutive K stages of one item, loaded by
+// one TMA box per operand: row r, column c = the scale column of the box's
+// first column + c.  Both arrays are TMA destinations: 128-byte aligned.
+template <int kLaneRows, int kColRows, int kW>
+struct alignas(128) ScaleGroup {
+    alignas(128) float lane[kLaneRows][kW];
+    alignas(128) float col[kColRows][kW];
 };
 
 template <int BN>
@@ -96,15 +107,11 @@ struct GemmArgs {
     int rows, cols;       // extents of the MMA A operand and B operand
     int tiles_r, tiles_c, kb_total, kb_per_split, splits, items, group_r;
     int force_promote;
-    int krot;             // rotate the K-stage order per tile
 };
 
-// Walks the (item, k-stage) jobs of one CTA in order.  Within an item the
-// K stages are visited in a rotated order (starting at an offset derived from
-// the tile) when a.krot is set, so CTAs that share an operand tile do not all
-// request the same lines at the same moment.
+// Walks the (item, k-stage) jobs of one CTA (or CTA pair) in order.
 struct JobIter {
-    int item, kb, kb0, nkb, pos, rot, step;
+    int item, kb, kb0, nkb, pos, step;
     int tile, split, tr, tc;
     __device__ void load(const GemmArgs& a) {
         split = item % a.splits;
@@ -118,9 +125,8 @@ struct JobIter {
         tc = in / gm;
         kb0 = split * a.kb_per_split;
         nkb = min(a.kb_total, kb0 + a.kb_per_split) - kb0;
-        rot = a.krot ? tile % nkb : 0;
         pos = 0;
-        kb = kb0 + rot;
+        kb = kb0;
     }
     // first item and stride: the CTA's (or CTA pair's) index and count
     __device__ void begin(const GemmArgs& a, int first, int stride) {
@@ -137,9 +143,7 @@ struct JobIter {
             if (item < a.items) load(a);
             return true;
         }
-        int r = pos + rot;
-        if (r >= nkb) r -= nkb;
-        kb = kb0 + r;
+        kb = kb0 + pos;
         return false;
     }
 };
@@ -275,16 +279,26 @@ struct Cfg {
     static constexpr int kScalesPerStage = kBK / kBlkK;  // As/Ws columns per stage
     static constexpr int kColGroups = kSwap ? BN : (BN + kBlkN - 1) / kBlkN;
     static constexpr int kLaneGroups = kSwap ? kBM / kBlkN : kBM;
-    // rows of the scale boxes loaded per stage (16 bytes = 4 scale columns each)
+    // rows of the raw scale boxes (A-operand side, B-operand side)
     static constexpr int kLaneScaleRows = kSwap ? kBM / kBlkN : kBM;
     static constexpr int kColScaleRows = kSwap ? BN : (BN + kBlkN - 1) / kBlkN;
-    static constexpr uint32_t kScaleBytes = 16u * (kLaneScaleRows + kColScaleRows);
+    using Slot = SfSlot<BN, kLaneScaleRows, kColScaleRows>;
+    // Grouped scale loads (TMA path): each TMA operation costs an SM about the
+    // same time whatever its size, so one box per operand brings the scales of
+    // kG consecutive stages.  Box: kGW columns (for one scale per stage, 8, so
+    // that a group starting at any column fits behind a 16-byte aligned start).
+    static constexpr int kG = 4;
+    static constexpr int kGW = kScalesPerStage == 1 ? 8 : kG * kScalesPerStage;
+    using Group = ScaleGroup<kLaneScaleRows, kColScaleRows, kGW>;
+    static constexpr int kGBufs = 2;
+    static constexpr uint32_t kGroupBytes = 4u * kGW * (kLaneScaleRows + kColScaleRows);
     static constexpr size_t kOffA = 0;
     static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
     static constexpr size_t kOffSf = kOffB + size_t(kStages) * kBBytes;
-    static constexpr size_t kOffInfo = kOffSf + size_t(kStages) * sizeof(SfSlot<BN>);
+    static constexpr size_t kOffGrp = kOffSf + size_t(kStages) * sizeof(Slot);
+    static constexpr size_t kOffInfo = kOffGrp + (kScaleTma ? size_t(kGBufs) * sizeof(Group) : 0);
     static constexpr size_t kOffBar = kOffInfo + size_t(kMmaWarps * kAccBufs) * sizeof(Info<BN>);
-    static constexpr int kNumBars = 3 * kStages + (2 * kAccBufs + 1) * kMmaWarps;
+    static constexpr int kNumBars = 3 * kStages + (2 * kAccBufs + 1) * kMmaWarps + 2 * kGBufs;
     static constexpr size_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr size_t kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
@@ -292,6 +306,10 @@ struct Cfg {
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
     static_assert(!kPair || (!kSwap && BN == 256 && kScaleTma && kAccBufs == 1), "CTA-pair configuration");
     static_assert(kColGroups <= 64, "raw column-scale slot");
+    static_assert(kGW * 4 % 16 == 0, "scale box row: whole 16-byte units");
+    static_assert(offsetof(Group, lane) % 128 == 0 && offsetof(Group, col) % 128 == 0 && sizeof(Group) % 128 == 0,
+                  "TMA destinations in a scale group start on 128-byte boundaries");
+    static_assert(kOffGrp % 128 == 0, "scale groups start on a 128-byte boundary");
     static_assert(kStages <= 8, "cp.async group depth");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -308,7 +326,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + C::kOffA;
     uint8_t* sB = smem + C::kOffB;
-    SfSlot<BN>* sf = reinterpret_cast<SfSlot<BN>*>(smem + C::kOffSf);
+    typename C::Slot* sf = reinterpret_cast<typename C::Slot*>(smem + C::kOffSf);
+    typename C::Group* grp = reinterpret_cast<typename C::Group*>(smem + C::kOffGrp);
     Info<BN>* info = reinterpret_cast<Info<BN>*>(smem + C::kOffInfo);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -323,6 +342,9 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
     auto acce_bar = [&](int m, int b) { return bar0 + 8u * (2 * kStages + (kMW + m) * kAccBufs + b); };
     auto drain_bar = [&](int m) { return bar0 + 8u * (2 * kStages + 2 * kMW * kAccBufs + m); };
     auto sraw_bar = [&](int s) { return bar0 + 8u * (2 * kStages + (2 * kAccBufs + 1) * kMW + s); };
+    // scale-group ring: loaded (TMA) / released (both scale warps)
+    auto gfull_bar = [&](int d) { return bar0 + 8u * (3 * kStages + (2 * kAccBufs + 1) * kMW + d); };
+    auto gempty_bar = [&](int d) { return bar0 + 8u * (3 * kStages + (2 * kAccBufs + 1) * kMW + C::kGBufs + d); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -352,7 +374,11 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             }
             ptx::mbar_init(drain_bar(m), 1);
         }
-        for (int s = 0; s < kStages; ++s) ptx::mbar_init(sraw_bar(s), 1);   // raw scales landed (TMA)
+        for (int s = 0; s < kStages; ++s) ptx::mbar_init(sraw_bar(s), 1);   // raw scales landed (cp.async path)
+        for (int d = 0; d < C::kGBufs; ++d) {
+            ptx::mbar_init(gfull_bar(d), 1);    // producer expect_tx
+            ptx::mbar_init(gempty_bar(d), 2);   // one arrive per scale warp
+        }
         misc[1] = 0;
         ptx::fence_mbar_init();
     }
@@ -399,10 +425,6 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 return kSwap ? j.tr * kBM : j.tc * BN + static_cast<int>(rank) * (BN / kCG);
             };
             auto x_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : a_row0(j); };
-            // scale boxes: 4 columns starting at a 16-byte aligned column
-            auto s_col = [&](const JobIter& j) { return (j.kb * C::kScalesPerStage) & ~3; };
-            auto ws_dst = [&](int s) { return ptx::smem_u32(kSwap ? &sf[s].lane_raw[0][0] : &sf[s].col_raw[0][0]); };
-            auto xs_dst = [&](int s) { return ptx::smem_u32(kSwap ? &sf[s].col_raw[0][0] : &sf[s].lane_raw[0][0]); };
             auto ws_row = [&](const JobIter& j) { return kSwap ? j.tr * (kBM / kBlkN) : j.tc * (BN / kBlkN); };
             auto xs_row = [&](const JobIter& j) { return kSwap ? j.tc * BN : a_row0(j); };
             // Operand tiles signal the stage's full barrier; with a CTA pair both
@@ -415,15 +437,29 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             };
             auto load_w = [&](int s, const JobIter& j) {
                 ptx::mbar_arrive_expect_tx_if(leader && rank == 0u, full_bar(s), C::kStageBytes);
-                if (kScaleTma) {
-                    ptx::mbar_arrive_expect_tx_if(leader, sraw_bar(s), C::kScaleBytes);
-                    ptx::tma_load_2d_if(leader, ws_dst(s), tmWs, s_col(j), ws_row(j), sraw_bar(s));
-                }
                 load_tile(w_dst(s), tmW, j.kb * kBK, w_row(j), s);
             };
             auto load_x = [&](int s, const JobIter& j) {
-                if (kScaleTma) ptx::tma_load_2d_if(leader, xs_dst(s), tmXs, s_col(j), xs_row(j), sraw_bar(s));
                 load_tile(x_dst(s), tmX, j.kb * kBK, x_row(j), s);
+            };
+            // Scale group: at the first stage of every kG-stage group of an item,
+            // one box per operand with the raw scales of the whole group.
+            uint32_t gcount = 0;
+            bool group_ok = true;
+            auto load_group = [&](const JobIter& j) {
+                if (!kScaleTma || (j.pos % C::kG) != 0) return;
+                const int d = static_cast<int>(gcount % C::kGBufs);
+                if (!wait_bar(gempty_bar(d), ((gcount / C::kGBufs) & 1u) ^ 1u, sync, 1)) {
+                    group_ok = false;
+                    return;
+                }
+                const int gx = (j.kb * C::kScalesPerStage) & ~3;   // 16-byte aligned first column
+                typename C::Group& g = grp[d];
+                ptx::mbar_arrive_expect_tx_if(leader, gfull_bar(d), C::kGroupBytes);
+                const uint32_t lane_dst = ptx::smem_u32(&g.lane[0][0]), col_dst = ptx::smem_u32(&g.col[0][0]);
+                ptx::tma_load_2d_if(leader, kSwap ? lane_dst : col_dst, tmWs, gx, ws_row(j), gfull_bar(d));
+                ptx::tma_load_2d_if(leader, kSwap ? col_dst : lane_dst, tmXs, gx, xs_row(j), gfull_bar(d));
+                ++gcount;
             };
             JobIter it;
             it.begin(a, first_item, item_step);
@@ -437,7 +473,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             if (lane == 0) trace_ev(a, 2);
             ptx::grid_dependency_wait();
             if (lane == 0) trace_ev(a, 1);
-            for (int s = 0; s < npre; ++s) {
+            for (int s = 0; s < npre && group_ok; ++s) {
+                load_group(it);
                 load_x(s, it);
                 it.next(a);
             }
@@ -445,10 +482,11 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             int stage = npre % kStages;
             uint32_t phase = npre / kStages;
             int nj = npre;
-            while (it.valid(a)) {
+            while (it.valid(a) && group_ok) {
                 if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 1)) break;
                 if (lane == 0) trace_ev(a, 8 + (nj & 31));
                 ++nj;
+                load_group(it);
                 load_w(stage, it);
                 load_x(stage, it);
                 it.next(a);
@@ -468,7 +506,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         // this warp fetches the raw scales itself with cp.async, up to kStages
         // jobs ahead of the conversion.
         constexpr int kNld = C::kNld;
-        auto convert = [&](SfSlot<BN>& slot, const JobIter& j, int kcol) {
+        constexpr int kLR = C::kLaneScaleRows, kCR = C::kColScaleRows;
+        auto convert = [&](typename C::Slot& slot, const JobIter& j, int kcol) {
             const int row0 = kSwap ? j.tr * kBM : a_row0(j), col0 = j.tc * BN;
             uint32_t bad = 0;
             uint32_t w4[4];
@@ -487,7 +526,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                     const int c = h * 128 + lane + 32 * i;
                     const int ci = kSwap ? c : c / kBlkN;
                     const bool valid = c < BN && (kSwap ? col0 + c : col0 + ci * kBlkN) < a.cols;
-                    w4[i] = valid ? sf_word<kNld>(&slot.col_raw[ci < 64 ? ci : 0][0], kcol, bad) : 0x7F7F7F7Fu;
+                    w4[i] = valid ? sf_word<kNld>(&slot.col_raw[ci < kCR ? ci : 0][0], kcol, bad) : 0x7F7F7F7Fu;
                 }
                 *reinterpret_cast<uint4*>(&slot.sfb[h * 128 + lane * 4]) =
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -503,38 +542,103 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 }
             }
         };
+        // Grouped path: converts stage j from the group buffer g, whose column 0
+        // is scale column gx; keeps the stage's raw scales in the slot when the
+        // fp32 promotion step may need them.
+        auto convert_g = [&](typename C::Slot& slot, const JobIter& j, const typename C::Group& g, int c0,
+                             bool keep_raw) {
+            const int row0 = kSwap ? j.tr * kBM : a_row0(j), col0 = j.tc * BN;
+            uint32_t bad = 0;
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+                const int li = kSwap ? r / kBlkN : r;
+                const bool valid = (kSwap ? row0 + li * kBlkN : row0 + r) < a.rows;
+                w4[i] = valid ? sf_word<kNld>(&g.lane[li][c0], 0, bad) : 0x7F7F7F7Fu;  // 2^0 past the end
+            }
+            *reinterpret_cast<uint4*>(&slot.sfa[lane * 4]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+#pragma unroll
+            for (int h = 0; h < C::kSfbCopies; ++h) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = h * 128 + lane + 32 * i;
+                    const int ci = kSwap ? c : c / kBlkN;
+                    const bool valid = c < BN && (kSwap ? col0 + c : col0 + ci * kBlkN) < a.cols;
+                    w4[i] = valid ? sf_word<kNld>(&g.col[ci < kCR ? ci : 0][c0], 0, bad) : 0x7F7F7F7Fu;
+                }
+                *reinterpret_cast<uint4*>(&slot.sfb[h * 128 + lane * 4]) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            const bool all_ok = __all_sync(0xFFFFFFFFu, bad == 0u);
+            if (keep_raw || !all_ok) {
+                // chunk q of the stage -> raw column q (one scale per stage: column 0)
+                for (int r = lane; r < kLR; r += 32)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) slot.lane_raw[r][q] = q < kNld ? g.lane[r][c0 + q] : 0.0f;
+                for (int r = lane; r < kCR; r += 32)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) slot.col_raw[r][q] = q < kNld ? g.col[r][c0 + q] : 0.0f;
+            }
+            if (lane == 0) {
+                slot.pow2 = all_ok ? 1u : 0u;
+                slot.kcol = 0u;
+                if (kPair && rank != 0u) {   // the leader decides per stage from both halves' flags
+                    slot.xfer[0] = all_ok ? 1u : 0u;
+                    slot.xfer[1] = slot.xfer[2] = slot.xfer[3] = 0u;
+                }
+            }
+        };
         if (kScaleTma) {
-            // Two converter warps (2 and 11) take alternate stages.
+            // Two converter warps (2 and 11) take alternate stages.  A stage is
+            // converted once its slot is free (empty barrier) and its scale
+            // group has landed; each warp releases a group once past its end.
             const uint32_t sub = warp == 2 ? 0u : 1u;
+            // A pair's promotion path reads the peer's raw scales: keep them always.
+            const bool keep_raw = kPair || a.force_promote != 0;
             JobIter it;
             it.begin(a, first_item, item_step);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t nfin = 0;
+            uint32_t gcount = 0;
+            int gx = 0;
+            bool gready = false;
             while (it.valid(a)) {
-                if ((nfin & 1u) != sub) {
-                    ++nfin;
-                    it.next(a);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                    continue;
+                const int d = static_cast<int>(gcount % C::kGBufs);
+                if ((it.pos % C::kG) == 0) {
+                    gx = (it.kb * C::kScalesPerStage) & ~3;
+                    gready = false;
                 }
-                if (!wait_bar(sraw_bar(stage), phase, sync, 3)) break;
-                if (lane == 0) trace_ev(a, 104 + (nfin & 31));
-                convert(sf[stage], it, kNld == 1 ? (it.kb & 3) : 0);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (kPair && rank != 0u) {
-                        // the peer signals the leader's barrier with a 16-byte
-                        // async copy of its flag word; the warp's fences above
-                        // order the scale words before it
-                        const uint32_t x = ptx::smem_u32(&sf[stage].xfer[0]);
-                        ptx::bulk_copy_to_cluster_if(1u, ptx::mapa(x, 0u), x, C::kXferBytes,
-                                                     at_leader(full_bar(stage)));
-                    } else {
-                        ptx::mbar_arrive(full_bar(stage));
+                const bool gend = (it.pos % C::kG) == C::kG - 1 || it.last_kb();
+                if ((nfin & 1u) == sub) {
+                    if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 3)) break;
+                    if (!gready) {
+                        if (!wait_bar(gfull_bar(d), (gcount / C::kGBufs) & 1u, sync, 3)) break;
+                        gready = true;
                     }
-                    trace_ev(a, 72 + (nfin & 31));
+                    if (lane == 0) trace_ev(a, 104 + (nfin & 31));
+                    convert_g(sf[stage], it, grp[d], it.kb * C::kScalesPerStage - gx, keep_raw);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (kPair && rank != 0u) {
+                            // the peer signals the leader's barrier with a 16-byte
+                            // async copy of its flag word; the warp's fences above
+                            // order the scale words before it
+                            const uint32_t x = ptx::smem_u32(&sf[stage].xfer[0]);
+                            ptx::bulk_copy_to_cluster_if(1u, ptx::mapa(x, 0u), x, C::kXferBytes,
+                                                         at_leader(full_bar(stage)));
+                        } else {
+                            ptx::mbar_arrive(full_bar(stage));
+                        }
+                        trace_ev(a, 72 + (nfin & 31));
+                    }
+                }
+                if (gend) {
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(gempty_bar(d));
+                    ++gcount;
                 }
                 ++nfin;
                 it.next(a);
@@ -570,14 +674,14 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                     const int g = col0 + gi * kBlkN;
                     col_src[0] = (gi < C::kColGroups && g < a.cols)
                                      ? a.Ws + static_cast<int64_t>(g / kBlkN) * a.ks + c : nullptr;
-                    col_dst[0] = ptx::smem_u32(&sf[0].col_raw[gi < 64 ? gi : 0][c]);
+                    col_dst[0] = ptx::smem_u32(&sf[0].col_raw[gi < kCR ? gi : 0][c]);
                     col_chunk[0] = gi < C::kColGroups ? c : 4;
                 } else {
                     const int bi = lane / kNld, c = lane % kNld;
                     const int g = row0 + bi * kBlkN;
                     lane_src[0] = (bi < C::kLaneGroups && g < a.rows)
                                       ? a.Ws + static_cast<int64_t>(g / kBlkN) * a.ks + c : nullptr;
-                    lane_dst[0] = ptx::smem_u32(&sf[0].lane_raw[bi < 128 ? bi : 0][c]);
+                    lane_dst[0] = ptx::smem_u32(&sf[0].lane_raw[bi < kLR ? bi : 0][c]);
                     lane_chunk[0] = bi < C::kLaneGroups ? c : 4;
 #pragma unroll
                     for (int jj = 0; jj < kColLoads; ++jj) {
@@ -585,14 +689,14 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                         const int t = idx / kNld, cc = idx % kNld;
                         const int g = col0 + t;
                         col_src[jj] = (t < BN && g < a.cols) ? a.As + static_cast<int64_t>(g) * a.ks + cc : nullptr;
-                        col_dst[jj] = ptx::smem_u32(&sf[0].col_raw[t < 64 ? t : 0][cc]);
+                        col_dst[jj] = ptx::smem_u32(&sf[0].col_raw[t < kCR ? t : 0][cc]);
                         col_chunk[jj] = t < BN ? cc : 4;
                     }
                 }
             };
             // chunk == 4 marks a lane/slot with nothing to fetch
             auto issue_raw = [&](int si, const JobIter& j) {
-                const uint32_t slot_off = static_cast<uint32_t>(si * sizeof(SfSlot<BN>));
+                const uint32_t slot_off = static_cast<uint32_t>(si * sizeof(typename C::Slot));
                 const int nq = min(4, (a.K - j.kb * kBK) / 32);
                 const int soff = j.kb * C::kScalesPerStage;
 #pragma unroll
@@ -709,7 +813,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         const uint64_t bd_base = ptx::smem_desc(sB0, 16, 1024, ptx::kLayoutSw128);
         const uint64_t sfa_base = ptx::smem_desc(ptx::smem_u32(sf[0].sfa), 128, 128, ptx::kLayoutNone);
         const uint64_t sfb_base = ptx::smem_desc(ptx::smem_u32(sf[0].sfb), 128, 128, ptx::kLayoutNone);
-        constexpr uint32_t kSlotStep = sizeof(SfSlot<BN>) >> 4;
+        constexpr uint32_t kSlotStep = sizeof(typename C::Slot) >> 4;
         // A K stage shorter than 128 exists only when K % 128 != 0 (last stage).
         const bool ragged_k = (a.K % kBK) != 0;
         while ((!kPair || rank == 0u) && it.valid(a) && !failed) {
@@ -724,7 +828,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             ptx::tc_fence_after();
             if (lane == 0) trace_ev(a, 40 + (mma_jobs & 31));
             ++mma_jobs;
-            SfSlot<BN>& slot = sf[stage];
+            typename C::Slot& slot = sf[stage];
             const int nq = ragged_k ? min(4, (a.K - it.kb * kBK) / 32) : 4;
             const uint64_t ad0 = ad_base + static_cast<uint64_t>(stage * (C::kABytes >> 4));
             const uint64_t bd0 = bd_base + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
@@ -1117,11 +1221,12 @@ sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStre
 // One translation unit per [blk_n, blk_k] recipe instantiates all tile shapes.
 // maps: A operand, B operand, A-operand scales, B-operand scales.
 // Pair tiles (256 x 256, cta_group::2) need TMA-loaded scales.
-constexpr int kPairStages = 6;
 template <int kBlkN, int kBlkK, bool kScaleTma>
 sgq_status dispatch_tile(bool swap, bool pair, int bn, const CUtensorMap* maps, const GemmArgs& a, int grid,
                          cudaStream_t st) {
     if (pair) {
+        // six stages fit beside [128,128]-recipe scale groups, five beside [32,32]
+        constexpr int kPairStages = kBlkK == 32 ? 5 : 6;
         if constexpr (kScaleTma)
             return run<256, kPairStages, false, 1, kBlkN, kBlkK, true, true>(maps, a, grid, st);
         else
