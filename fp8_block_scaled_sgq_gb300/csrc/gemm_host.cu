@@ -212,6 +212,8 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     a.splits = p.splits;
     a.items = p.items;
     a.group_r = 16;
+    static const int prefetch = gemm::env_int("SGQ_PREFETCH", -1);
+    a.prefetch = prefetch;
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
     rc = gemm::status_word(&a.status);
     if (rc != SGQ_OK) return rc;
@@ -321,6 +323,8 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
     a.splits = p.splits;
     a.items = p.items;
     a.group_r = 16;
+    static const int prefetch = gemm::env_int("SGQ_PREFETCH", -1);
+    a.prefetch = prefetch;
     a.force_promote = 0;
     rc = gemm::status_word(&a.status);
     if (rc != SGQ_OK) return rc;

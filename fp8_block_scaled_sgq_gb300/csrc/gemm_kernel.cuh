@@ -48,11 +48,7 @@ namespace gemm {
 
 constexpr int kBM = 128;          // MMA M: rows of the "A" operand per tile
 constexpr int kBK = 128;          // K elements (bytes) per pipeline stage
-constexpr int kNumThreads = 384;  // 12 warps; configurations with two MMA warps add warp 12
-constexpr int kEpiWarp0 = 3;
-constexpr int kMma2Warp = 12;     // second MMA issuer (two-issuer configurations)
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = 480;  // two 16-column scale-factor slots at 480 and 496
+constexpr int kEpiWarp0 = 3;      // warps: 0 producer, 1 MMA, 2 scale, 3.. epilogue, then scale 2, MMA 2
 constexpr uint64_t kTimeoutNs = 1ull << 30;
 
 constexpr uint32_t kInfoPromote = 1u;
@@ -107,6 +103,7 @@ struct GemmArgs {
     int rows, cols;       // extents of the MMA A operand and B operand
     int tiles_r, tiles_c, kb_total, kb_per_split, splits, items, group_r;
     int force_promote;
+    int prefetch;         // < 0: the configuration's weight prefetch depth; else at most this many stages
 };
 
 // Walks the (item, k-stage) jobs of one CTA (or CTA pair) in order.
@@ -209,17 +206,20 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
     return ok != 0;
 }
 
+// Named barrier 1 over the epilogue warps (kThr threads).
+template <int kThr>
 __device__ __forceinline__ bool epi_any(bool pred) {
     uint32_t r;
     asm volatile(
         "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\n"
-        "bar.red.or.pred p, 1, 256, q;\nselp.u32 %0, 1, 0, p;\n}"
+        "bar.red.or.pred p, 1, %2, q;\nselp.u32 %0, 1, 0, p;\n}"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred))
+        : "r"(static_cast<uint32_t>(pred)), "n"(kThr)
         : "memory");
     return r != 0;
 }
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+template <int kThr>
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThr) : "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -259,11 +259,25 @@ struct Cfg {
     // as a full-width one, so two warps issue alternate K stages of each item
     // into separate accumulators, which the epilogue adds in a fixed order.
     static constexpr int kMmaWarps = kSwap ? 2 : 1;
-    static constexpr int kThreads = kNumThreads + 32 * (kMmaWarps - 1);
+    // Two CTAs per SM (registers, shared memory, TMEM sized for it; four
+    // epilogue warps, one per TMEM lane quadrant) would let the next GEMM on
+    // the stream become resident and stream its weights while this one runs.
+    // Measured on decode tiles it is slower (the two GEMMs' loads share the
+    // SM's TMA queue and the activation tiles wait behind the next GEMM's
+    // weights), so no configuration uses it; the layout stays parametrised.
+    static constexpr bool kTwoPerSm = false;
+    static constexpr int kEpiWarps = kTwoPerSm ? 4 : 8;
+    static constexpr int kSf2Warp = kEpiWarp0 + kEpiWarps;         // second scale warp
+    static constexpr int kMma2Warp = kSf2Warp + 1;                 // second MMA issuer (swap-AB)
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + 1 + (kMmaWarps - 1));
+    static constexpr int kMinBlocks = kTwoPerSm ? 2 : 1;
+    // TMEM: accumulators from column 0, then two 16-column scale slots per issuer
+    static constexpr uint32_t kTmemCols = kTwoPerSm ? 128u : 512u;
+    static constexpr uint32_t kSfCol = kTmemCols - 32u;
     // Weight stages loaded before the programmatic-dependency wait.  Loads of
     // one SM leave in issue order, so a deep weight prefetch delays the first
     // activation tiles behind it; the swap-AB (decode) tiles start with none.
-    static constexpr int kPrefetch = kSwap ? 0 : kStages;
+    static constexpr int kPrefetch = (kSwap && !kTwoPerSm) ? 0 : kStages;
     // CTA pair (cluster of two, cta_group::2): the tile is 256 x BN; each CTA
     // holds 128 A rows and BN/2 B rows per stage, the leader issues the MMAs.
     static constexpr int kCG = kPair ? 2 : 1;
@@ -272,7 +286,7 @@ struct Cfg {
     static constexpr int kBBytes = (BN / kCG) * kBK;       // B bytes per CTA and stage
     static constexpr uint32_t kXferBytes = kPair ? 16u : 0u;      // the peer's scale-ready transfer
     static constexpr int kStageBytes = kCG * (kABytes + kBBytes) + kXferBytes;   // bytes the full barrier expects
-    static constexpr int kCols = BN / 2;  // accumulator columns per epilogue thread
+    static constexpr int kCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogue thread
     static constexpr int kLd = kCols < 16 ? kCols : 16;
     static constexpr int kSfbCopies = BN > 128 ? BN / 128 : 1;
     static constexpr int kNld = kBlkK == 128 ? 1 : 4;    // distinct scale chunks per stage
@@ -303,6 +317,7 @@ struct Cfg {
     static constexpr size_t kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(kMmaWarps * kAccBufs * BN <= int(kSfCol) - 32 * (kMmaWarps - 1), "TMEM budget");
+    static_assert(!kTwoPerSm || kSmem <= 113 * 1024, "two CTAs per SM: shared memory");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
     static_assert(!kPair || (!kSwap && BN == 256 && kScaleTma && kAccBufs == 1), "CTA-pair configuration");
     static_assert(kColGroups <= 64, "raw column-scale slot");
@@ -315,7 +330,8 @@ struct Cfg {
 };
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair>
-__global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>::kThreads), 1)
+__global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>::kThreads),
+                                  (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>::kMinBlocks))
     fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                           const GemmArgs a) {
@@ -370,7 +386,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             for (int b = 0; b < kAccBufs; ++b) {
                 ptx::mbar_init(accf_bar(m, b), 2);   // MMA thread arrive + tcgen05.commit
                 // one arrive per epilogue warp (pair leader: of both CTAs)
-                ptx::mbar_init(acce_bar(m, b), kPair ? 16 : 8);
+                ptx::mbar_init(acce_bar(m, b), C::kEpiWarps * (kPair ? 2 : 1));
             }
             ptx::mbar_init(drain_bar(m), 1);
         }
@@ -391,7 +407,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc_g<kCG>(ptx::smem_u32(misc), kTmemCols);
+        ptx::tmem_alloc_g<kCG>(ptx::smem_u32(misc), C::kTmemCols);
         ptx::tmem_relinquish_g<kCG>();
     }
     ptx::tc_fence_before();
@@ -465,7 +481,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             it.begin(a, first_item, item_step);
             JobIter pre = it;
             int npre = 0;
-            while (npre < C::kPrefetch && pre.valid(a)) {
+            const int prefetch = a.prefetch >= 0 && a.prefetch < C::kPrefetch ? a.prefetch : C::kPrefetch;
+            while (npre < prefetch && pre.valid(a)) {
                 load_w(npre, pre);
                 pre.next(a);
                 ++npre;
@@ -494,7 +511,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             }
         }
         __syncwarp();
-    } else if (warp == 2 || warp == 11) {
+    } else if (warp == 2 || warp == C::kSf2Warp) {
         // ---------------------------------------------------------- scale loader
         // Turns each stage's raw fp32 scales into UE8M0 words in tcgen05.cp
         // order, checks the power-of-two property, and releases the stage to
@@ -759,7 +776,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             ptx::cp_async_wait_pending(0);
         }
         __syncwarp();
-    } else if (warp == 1 || (kMW > 1 && warp == kMma2Warp)) {
+    } else if (warp == 1 || (kMW > 1 && warp == C::kMma2Warp)) {
         // ---------------------------------------------------------- MMA issuer
         // The whole warp runs this loop in lock-step; every tcgen05 instruction
         // is issued by lane 0 through a predicate inside the asm, so the warp
@@ -787,7 +804,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         auto acc_par = [&](uint32_t u) { return (u / kAccBufs) & 1u; };
         Info<BN>* my_info = info + mw * kAccBufs;
         const uint32_t acc_col0 = static_cast<uint32_t>(mw * kAccBufs * BN);
-        const uint32_t sf_col0 = kSfCol - 32u * static_cast<uint32_t>(mw);
+        const uint32_t sf_col0 = C::kSfCol - 32u * static_cast<uint32_t>(mw);
         // Signals segment b to the epilogue(s): the MMA thread's arrive (after
         // the Info writes; pair: also on the peer's barrier, release at cluster
         // scope) and a commit that fires when the MMAs are done (both CTAs).
@@ -929,9 +946,9 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         // ---------------------------------------------------------- epilogue
         constexpr int kCols = C::kCols;
         constexpr int kLd = C::kLd;
-        const int ew = warp - kEpiWarp0;          // 0..7
+        const int ew = warp - kEpiWarp0;          // 0 .. kEpiWarps-1
         const int quad = warp & 3;                // TMEM lane quadrant this warp may access
-        const int half = ew >> 2;                 // which half of the columns
+        const int half = ew >> 2;                 // which half of the columns (8 warps)
         const int r_in_tile = quad * 32 + lane;   // accumulator row (TMEM lane)
         const int c_begin = half * kCols;
         const int epi_tid = ew * 32 + lane;
@@ -1037,7 +1054,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                     for (int c = 0; c < kCols; ++c) acc[c] += acc1[c];
                 }
             }
-            if (epi_any(failed || *sync.abort_flag)) break;
+            if (epi_any<C::kEpiWarps * 32>(failed || *sync.abort_flag)) break;
             if (epi_tid == 0) trace_ev(a, 136 + 4 * (n_items & 15));
             // ------------------------------------------------ output
             const int row0 = kSwap ? it.tr * kBM : a_row0(it), col0 = it.tc * BN;
@@ -1066,7 +1083,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                             *reinterpret_cast<float4*>(part + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
                     }
                 }
-                epi_sync();
+                epi_sync<C::kEpiWarps * 32>();
                 if (epi_tid == 0) {
                     trace_ev(a, 137 + 4 * (n_items & 15));
                     // The barrier orders every epilogue thread's partial before this
@@ -1078,7 +1095,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                     if (last_split) __threadfence();
                     misc[2] = last_split ? 1u : 0u;
                 }
-                epi_sync();
+                epi_sync<C::kEpiWarps * 32>();
                 store = misc[2] != 0u;
                 if (store && live) {
                     if (kSwap) {
@@ -1155,17 +1172,17 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         }
     }
 
-    if (lane == 0 && warp < 11) trace_ev(a, 232 + warp);
+    if (lane == 0 && warp < 12) trace_ev(a, 232 + warp);
     ptx::tc_fence_before();
     __syncthreads();
-    if (lane == 0 && warp < 11) trace_ev(a, 244 + warp);
+    if (lane == 0 && warp < 11) trace_ev(a, 244 + warp);   // slot 255 is the end stamp
     if (threadIdx.x == 0) trace_ev(a, 255);
     // A pair's leader writes the peer's TMEM and reads its shared memory until
     // its drain completes: neither CTA leaves before both are here.
     if (kPair) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc_g<kCG>(tmem, kTmemCols);
+        ptx::tmem_dealloc_g<kCG>(tmem, C::kTmemCols);
     }
 }
 

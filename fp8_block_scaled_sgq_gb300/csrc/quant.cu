@@ -88,26 +88,38 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
     // (x may be its output; xq/xs may still be read by it).
     ptx::grid_dependency_wait();
     constexpr int kTpg = kGroup / 8;
+    // Each warp iteration loads kUnroll warp-wide chunks of 32 vectors before
+    // processing any, so every thread keeps kUnroll 16-byte loads in flight
+    // (an HBM-bound stream needs tens of KB outstanding per SM).
+    constexpr int kUnroll = 4;
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t base = warp * 32; base < nvec; base += nwarps * 32) {
-        const int64_t v = base + lane;
-        const bool active = v < nvec;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (active) w = __ldg(x + v);
-        float f[8];
-        unpack8(w, f);
-        float amax = 0.0f;
+    const int64_t stride = nwarps * 32;
+    for (int64_t base = warp * 32; base < nvec; base += stride * kUnroll) {
+        uint4 w[kUnroll];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t v = base + u * stride + lane;
+            w[u] = v < nvec ? __ldg(x + v) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int off = kTpg / 2; off > 0; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-        const float s = group_scale<kUe8m0>(amax);
-        if (active) {
-            xq[v] = quantize8<kUe8m0>(f, s);
-            if ((lane % kTpg) == 0) xs[v / kTpg] = s;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t v = base + u * stride + lane;
+            const bool active = v < nvec;
+            float f[8];
+            unpack8(w[u], f);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+            for (int off = kTpg / 2; off > 0; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+            const float s = group_scale<kUe8m0>(amax);
+            if (active) {
+                xq[v] = quantize8<kUe8m0>(f, s);
+                if ((lane % kTpg) == 0) xs[v / kTpg] = s;
+            }
         }
     }
 }
@@ -167,9 +179,20 @@ sgq_status launch_tg(const void* x, int64_t M, int64_t K, void* xq, float* xs, c
     DeviceInfo di;
     sgq_status rc = device_info(&di);
     if (rc != SGQ_OK) return rc;
+    // One wave of resident CTAs at most (grid-stride loop beyond that).
+    static int resident[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    if (resident[dev] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_token_group_kernel<G, U>, 256, 0) != cudaSuccess ||
+            n < 1)
+            return SGQ_ERR_CUDA;
+        resident[dev] = n;
+    }
     const int64_t warps_needed = (nvec + 31) / 32;
     int64_t blocks = (warps_needed + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(di.sm_count) * 8;
+    const int64_t cap = static_cast<int64_t>(di.sm_count) * resident[dev];
     if (blocks > cap) blocks = cap;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
