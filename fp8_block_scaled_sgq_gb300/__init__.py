@@ -8,7 +8,8 @@ torch-facing helpers below that only allocate outputs and call the binding.
 from __future__ import annotations
 
 from .binding import (  # noqa: F401
-    EXPORTS, SGQ_GEMM_DEFAULT, SGQ_GEMM_FORCE_PROMOTE, SgqError, load_library, sgq_device_status,
+    EXPORTS, SGQ_GEMM_DEFAULT, SGQ_GEMM_FORCE_PROMOTE, SGQ_GEMM_ISSUE_ALT, SGQ_GEMM_ISSUE_SINGLE, SgqError,
+    load_library, sgq_device_status,
     sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_launch_count, sgq_quant_token_group,
     sgq_quant_weight_block, sgq_version, status_string)
 

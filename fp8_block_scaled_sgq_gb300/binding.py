@@ -25,6 +25,8 @@ SGQ_ERR_TIMEOUT = 5
 
 SGQ_GEMM_DEFAULT = 0
 SGQ_GEMM_FORCE_PROMOTE = 1
+SGQ_GEMM_ISSUE_ALT = 2
+SGQ_GEMM_ISSUE_SINGLE = 4
 
 # Symbols declared in include/sgq.h (checked by the tests).
 EXPORTS = (

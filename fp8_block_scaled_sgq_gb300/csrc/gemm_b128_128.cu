@@ -4,9 +4,9 @@
 
 namespace sgq {
 namespace gemm {
-sgq_status dispatch_128_128(bool swap, bool pair, int bn, bool scale_tma, const CUtensorMap* maps, const GemmArgs& a,
-                           int grid, cudaStream_t st) {
-    return dispatch<128, 128>(swap, pair, bn, scale_tma, maps, a, grid, st);
+sgq_status dispatch_128_128(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, int grid,
+                           cudaStream_t st) {
+    return dispatch<128, 128>(v, maps, a, grid, st);
 }
 }  // namespace gemm
 }  // namespace sgq

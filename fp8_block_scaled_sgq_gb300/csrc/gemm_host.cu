@@ -105,6 +105,7 @@ sgq_status get_workspace(cudaStream_t st, DevWs* out) {
 struct Plan {
     bool swap;
     bool pair;   // CTA pairs on 256 x 256 tiles (cluster of two, cta_group::2)
+    bool alt;    // 128 x 256 tiles with two alternating MMA issuers
     int bn, tiles_r, tiles_c, kb_total, kb_per_split, splits, items, grid;
 };
 
@@ -157,6 +158,13 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count) {
     const int64_t ks = K / blk_k;
     p.pair = pair_on != 0 && !p.swap && p.splits == 1 && M > kBM && (ks % 4) == 0 &&
              ks >= (blk_k == 128 ? 8 : 16);   // the kernel's TMA scale-group path
+    // Two alternating MMA issuers (one scale warp): measured faster for the
+    // [*,128] recipe with long K (4096 x 7168 x 7168: 207 -> 185 us), slower for
+    // [*,32] (the single scale warp's conversion then bounds the stage) and for
+    // short K (per-tile costs dominate).  SGQ_ALT=0/1 forces it off/on.
+    static const int alt_env = env_int("SGQ_ALT", -1);
+    const bool alt_auto = blk_k == 128 && p.kb_total >= 32;
+    p.alt = !p.swap && !p.pair && (alt_env < 0 ? alt_auto : alt_env != 0);
     if (p.pair) {
         p.tiles_r = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
         p.items = p.tiles_r * p.tiles_c;
@@ -186,96 +194,19 @@ sgq_status status_word(uint32_t** out) {
 }
 }  // namespace gemm
 
-sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq, const float* Ws,
-                                 void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
-                                 uint32_t flags, cudaStream_t st) {
-    if (gemm::get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
-    DeviceInfo di;
-    sgq_status rc = device_info(&di);
-    if (rc != SGQ_OK) return rc;
-    if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
-    const gemm::Plan p = gemm::make_plan(M, N, K, blk_k, di.sm_count);
-    gemm::GemmArgs a{};
-    a.As = As;
-    a.Ws = Ws;
-    a.D = static_cast<__nv_bfloat16*>(D);
-    a.M = static_cast<int>(M);
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.ks = static_cast<int>(K / blk_k);
-    a.rows = static_cast<int>(p.swap ? N : M);
-    a.cols = static_cast<int>(p.swap ? M : N);
-    a.tiles_r = p.tiles_r;
-    a.tiles_c = p.tiles_c;
-    a.kb_total = p.kb_total;
-    a.kb_per_split = p.kb_per_split;
-    a.splits = p.splits;
-    a.items = p.items;
-    a.group_r = 16;
-    static const int prefetch = gemm::env_int("SGQ_PREFETCH", -1);
-    a.prefetch = prefetch;
-    a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
-    rc = gemm::status_word(&a.status);
-    if (rc != SGQ_OK) return rc;
-#ifdef SGQ_TRACE
-    {
-        void* tp = nullptr;
-        if (cudaGetSymbolAddress(&tp, g_gemm_trace) != cudaSuccess) return SGQ_ERR_CUDA;
-        a.trace = static_cast<unsigned long long*>(tp);
-    }
-#endif
-    if (p.splits > 1) {
-        gemm::DevWs ws;
-        rc = gemm::get_workspace(st, &ws);
-        if (rc != SGQ_OK) return rc;
-        a.partial = ws.partial;
-        a.counters = ws.counters;
-    }
-    // maps: A operand, B operand, A-operand scales, B-operand scales
-    CUtensorMap maps[4];
-    const void* opA = p.swap ? Wq : Aq;
-    const void* opB = p.swap ? Aq : Wq;
-    if (gemm::make_tmap(&maps[0], opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
-    // Scale rows are TMA-loadable when their pitch is a multiple of 16 bytes
-    // and they are at least one box (one group of K stages) wide: a box wider
-    // than the matrix's rows is not used.
-    static const int scale_tma_on = gemm::env_int("SGQ_SCALE_TMA", 1);
-    const int gcols = blk_k == 128 ? 8 : 16;
-    const bool scale_tma = scale_tma_on != 0 && (a.ks % 4) == 0 && a.ks >= gcols;
-    maps[2] = maps[0];
-    maps[3] = maps[1];
-    if (scale_tma) {
-        const int64_t nb = (N + blk_n - 1) / blk_n;
-        // one box = the scales of a group of four K stages (see the kernel)
-        if (gemm::make_scale_map(&maps[2], p.swap ? Ws : As, p.swap ? nb : M, a.ks,
-                                 p.swap ? gemm::kBM / blk_n : gemm::kBM, gcols) != SGQ_OK ||
-            gemm::make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks,
-                                 p.swap ? p.bn : p.bn / blk_n, gcols) != SGQ_OK)
-            return SGQ_ERR_CUDA;
-    }
-    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
-    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
-    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
-    return gemm::dispatch_128_128(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
-}
+namespace gemm {
+namespace {
 
-// ---------------------------------------------------------------------------
-// Allocation-free variant of the GEMM launch.
-//
-// Some callers cannot let a library allocate device memory: a serving engine
-// that reserves nearly all of HBM for its own pool up front (a later
-// cudaMalloc fails, or fragments that pool), or a host whose allocator must
-// account for every byte.  For them the split-K scratch (fp32 partial tiles
-// plus arrival counters) lives in this fixed file-scope array instead of the
-// workspace that sgq_fp8_block_gemm allocates on first use.  The array is
-// part of the module image, so every GPU that loads the library holds it
-// until the process exits.
+// Split-K scratch of the allocation-free entry point: a fixed file-scope
+// array instead of the workspace that sgq_fp8_block_gemm allocates on first
+// use.  Some callers cannot let a library allocate device memory (a serving
+// engine that reserves nearly all of HBM for its own pool up front, or a host
+// whose allocator must account for every byte).  The array is part of the
+// module image, so every GPU that loads the library holds it until the
+// process exits.
 constexpr size_t kNoAllocCounterBytes = 16384 * sizeof(uint32_t);      // 64 KiB of counters
 constexpr size_t kNoAllocPartialBytes = size_t(16) << 20;               // 16 MiB of partials
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocCounterBytes + kNoAllocPartialBytes];
-
-namespace {
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocCounterBytes + kNoAllocPartialBytes];
 unsigned char* g_noalloc_ptr[64] = {};
 std::mutex g_noalloc_mu;
 
@@ -294,19 +225,21 @@ sgq_status noalloc_scratch(unsigned char** out) {
     *out = g_noalloc_ptr[dev];
     return SGQ_OK;
 }
-}  // namespace
 
-sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq, const float* Ws,
-                                         void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
-                                         cudaStream_t st) {
-    if (gemm::get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
+// Plans and launches one GEMM.  noalloc: split-K scratch from the fixed array
+// (its counters cleared by an asynchronous memset), else the per-device
+// workspace.
+sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D, int64_t M,
+                  int64_t N, int64_t K, int blk_n, int blk_k, uint32_t flags, bool noalloc, cudaStream_t st) {
+    if (get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
     DeviceInfo di;
     sgq_status rc = device_info(&di);
     if (rc != SGQ_OK) return rc;
     if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
-    // Same launch plan as sgq_fp8_block_gemm, so both give the same result.
-    const gemm::Plan p = gemm::make_plan(M, N, K, blk_k, di.sm_count);
-    gemm::GemmArgs a{};
+    Plan p = make_plan(M, N, K, blk_k, di.sm_count);
+    if (flags & SGQ_GEMM_ISSUE_ALT) p.alt = !p.swap && !p.pair;
+    if (flags & SGQ_GEMM_ISSUE_SINGLE) p.alt = false;
+    GemmArgs a{};
     a.As = As;
     a.Ws = Ws;
     a.D = static_cast<__nv_bfloat16*>(D);
@@ -323,34 +256,50 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
     a.splits = p.splits;
     a.items = p.items;
     a.group_r = 16;
-    static const int prefetch = gemm::env_int("SGQ_PREFETCH", -1);
+    static const int prefetch = env_int("SGQ_PREFETCH", -1);
     a.prefetch = prefetch;
-    a.force_promote = 0;
-    rc = gemm::status_word(&a.status);
+    a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
+    rc = status_word(&a.status);
     if (rc != SGQ_OK) return rc;
-    if (p.splits > 1) {
-        const size_t tiles = size_t(p.tiles_r) * size_t(p.tiles_c);
-        const size_t part_bytes = size_t(p.items) * gemm::kBM * size_t(p.bn) * sizeof(float);
-        if (tiles * sizeof(uint32_t) > kNoAllocCounterBytes || part_bytes > kNoAllocPartialBytes)
-            return SGQ_ERR_UNSUPPORTED;   // needs more scratch than the fixed array holds
-        unsigned char* base = nullptr;
-        rc = noalloc_scratch(&base);
-        if (rc != SGQ_OK) return rc;
-        a.counters = reinterpret_cast<uint32_t*>(base);
-        a.partial = reinterpret_cast<float*>(base + kNoAllocCounterBytes);
-        // The array keeps the previous call's contents; the counters must
-        // start at zero (a call that ended early may have left some set).
-        if (cudaMemsetAsync(a.counters, 0, tiles * sizeof(uint32_t), st) != cudaSuccess) return SGQ_ERR_CUDA;
+#ifdef SGQ_TRACE
+    {
+        void* tp = nullptr;
+        if (cudaGetSymbolAddress(&tp, g_gemm_trace) != cudaSuccess) return SGQ_ERR_CUDA;
+        a.trace = static_cast<unsigned long long*>(tp);
     }
+#endif
+    if (p.splits > 1) {
+        if (noalloc) {
+            const size_t tiles = size_t(p.tiles_r) * size_t(p.tiles_c);
+            const size_t part_bytes = size_t(p.items) * kBM * size_t(p.bn) * sizeof(float);
+            if (tiles * sizeof(uint32_t) > kNoAllocCounterBytes || part_bytes > kNoAllocPartialBytes)
+                return SGQ_ERR_UNSUPPORTED;   // needs more scratch than the fixed array holds
+            unsigned char* base = nullptr;
+            rc = noalloc_scratch(&base);
+            if (rc != SGQ_OK) return rc;
+            a.counters = reinterpret_cast<uint32_t*>(base);
+            a.partial = reinterpret_cast<float*>(base + kNoAllocCounterBytes);
+            // The array keeps the previous call's contents; the counters must
+            // start at zero (a call that ended early may have left some set).
+            if (cudaMemsetAsync(a.counters, 0, tiles * sizeof(uint32_t), st) != cudaSuccess) return SGQ_ERR_CUDA;
+        } else {
+            DevWs ws;
+            rc = get_workspace(st, &ws);
+            if (rc != SGQ_OK) return rc;
+            a.partial = ws.partial;
+            a.counters = ws.counters;
+        }
+    }
+    // maps: A operand, B operand, A-operand scales, B-operand scales
     CUtensorMap maps[4];
     const void* opA = p.swap ? Wq : Aq;
     const void* opB = p.swap ? Aq : Wq;
-    if (gemm::make_tmap(&maps[0], opA, a.rows, K, gemm::kBM) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (gemm::make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (make_tmap(&maps[0], opA, a.rows, K, kBM) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
     // Scale rows are TMA-loadable when their pitch is a multiple of 16 bytes
     // and they are at least one box (one group of K stages) wide: a box wider
     // than the matrix's rows is not used.
-    static const int scale_tma_on = gemm::env_int("SGQ_SCALE_TMA", 1);
+    static const int scale_tma_on = env_int("SGQ_SCALE_TMA", 1);
     const int gcols = blk_k == 128 ? 8 : 16;
     const bool scale_tma = scale_tma_on != 0 && (a.ks % 4) == 0 && a.ks >= gcols;
     maps[2] = maps[0];
@@ -358,16 +307,33 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
     if (scale_tma) {
         const int64_t nb = (N + blk_n - 1) / blk_n;
         // one box = the scales of a group of four K stages (see the kernel)
-        if (gemm::make_scale_map(&maps[2], p.swap ? Ws : As, p.swap ? nb : M, a.ks,
-                                 p.swap ? gemm::kBM / blk_n : gemm::kBM, gcols) != SGQ_OK ||
-            gemm::make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks,
-                                 p.swap ? p.bn : p.bn / blk_n, gcols) != SGQ_OK)
+        if (make_scale_map(&maps[2], p.swap ? Ws : As, p.swap ? nb : M, a.ks, p.swap ? kBM / blk_n : kBM,
+                           gcols) != SGQ_OK ||
+            make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks, p.swap ? p.bn : p.bn / blk_n,
+                           gcols) != SGQ_OK)
             return SGQ_ERR_CUDA;
     }
-    if (blk_n == 32 && blk_k == 32) return gemm::dispatch_32_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
-    if (blk_n == 32 && blk_k == 128) return gemm::dispatch_32_128(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
-    if (blk_n == 128 && blk_k == 32) return gemm::dispatch_128_32(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
-    return gemm::dispatch_128_128(p.swap, p.pair, p.bn, scale_tma, maps, a, p.grid, st);
+    const Variant v{p.swap, p.pair, p.alt, scale_tma, p.bn};
+    if (blk_n == 32 && blk_k == 32) return dispatch_32_32(v, maps, a, p.grid, st);
+    if (blk_n == 32 && blk_k == 128) return dispatch_32_128(v, maps, a, p.grid, st);
+    if (blk_n == 128 && blk_k == 32) return dispatch_128_32(v, maps, a, p.grid, st);
+    return dispatch_128_128(v, maps, a, p.grid, st);
+}
+
+}  // namespace
+}  // namespace gemm
+
+sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq, const float* Ws,
+                                 void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                 uint32_t flags, cudaStream_t st) {
+    return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags, false, st);
+}
+
+// Same launch plan as launch_fp8_block_gemm, so both give the same result.
+sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq, const float* Ws,
+                                         void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                         cudaStream_t st) {
+    return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, true, st);
 }
 
 sgq_status read_and_clear_device_status(cudaStream_t st) {

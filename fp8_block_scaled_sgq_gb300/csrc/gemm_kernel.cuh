@@ -58,7 +58,7 @@ constexpr uint32_t kStatusTimeout = 1u;
 template <int BN, int kLaneRows, int kColRows>
 struct alignas(128) SfSlot {
     uint32_t sfa[128];                  // UE8M0 words of the A operand (tcgen05.cp order)
-    uint32_t sfb[BN < 128 ? 128 : BN];  // UE8M0 words of the B operand
+    uint32_t sfb[(BN + 127) / 128 * 128];  // UE8M0 words of the B operand (128 per tcgen05.cp)
     // Raw fp32 scales of the stage, one row per scale row and 4 columns:
     //   lane_raw: A operand -- activation rows (normal) or weight n-blocks (swap)
     //   col_raw:  B operand -- weight n-blocks (normal) or tokens (swap)
@@ -253,12 +253,16 @@ __device__ __forceinline__ uint32_t sf_word(const float* row, int kcol, uint32_t
     return w;
 }
 
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair>
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair,
+          bool kAlt>
 struct Cfg {
     // Swap-AB tiles are narrow (N <= 64): an MMA costs about as much to issue
     // as a full-width one, so two warps issue alternate K stages of each item
     // into separate accumulators, which the epilogue adds in a fixed order.
-    static constexpr int kMmaWarps = kSwap ? 2 : 1;
+    // kAlt (wide tiles): two warps take turns issuing the K stages into the
+    // one accumulator, each preparing its next stage while the other issues.
+    static constexpr int kMmaWarps = (kSwap || kAlt) ? 2 : 1;
+    static constexpr int kAccSets = kSwap ? kMmaWarps : 1;   // accumulator sets (one per swap issuer)
     // Two CTAs per SM (registers, shared memory, TMEM sized for it; four
     // epilogue warps, one per TMEM lane quadrant) would let the next GEMM on
     // the stream become resident and stream its weights while this one runs.
@@ -267,9 +271,14 @@ struct Cfg {
     // weights), so no configuration uses it; the layout stays parametrised.
     static constexpr bool kTwoPerSm = false;
     static constexpr int kEpiWarps = kTwoPerSm ? 4 : 8;
-    static constexpr int kSf2Warp = kEpiWarp0 + kEpiWarps;         // second scale warp
-    static constexpr int kMma2Warp = kSf2Warp + 1;                 // second MMA issuer (swap-AB)
-    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + 1 + (kMmaWarps - 1));
+    // Scale warps: two take alternate stages; with alternating issuers one
+    // does all stages and the second's place goes to the second issuer (a
+    // 13th warp would cap registers at 128, as one SM sub-partition would
+    // hold four warps, and the 128-column epilogue would spill).
+    static constexpr int kSfWarps = kAlt ? 1 : 2;
+    static constexpr int kSf2Warp = kEpiWarp0 + kEpiWarps;                    // second scale warp
+    static constexpr int kMma2Warp = kEpiWarp0 + kEpiWarps + (kSfWarps - 1);  // second MMA issuer
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + (kSfWarps - 1) + (kMmaWarps - 1));
     static constexpr int kMinBlocks = kTwoPerSm ? 2 : 1;
     // TMEM: accumulators from column 0, then two 16-column scale slots per issuer
     static constexpr uint32_t kTmemCols = kTwoPerSm ? 128u : 512u;
@@ -288,7 +297,7 @@ struct Cfg {
     static constexpr int kStageBytes = kCG * (kABytes + kBBytes) + kXferBytes;   // bytes the full barrier expects
     static constexpr int kCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogue thread
     static constexpr int kLd = kCols < 16 ? kCols : 16;
-    static constexpr int kSfbCopies = BN > 128 ? BN / 128 : 1;
+    static constexpr int kSfbCopies = (BN + 127) / 128;
     static constexpr int kNld = kBlkK == 128 ? 1 : 4;    // distinct scale chunks per stage
     static constexpr int kScalesPerStage = kBK / kBlkK;  // As/Ws columns per stage
     static constexpr int kColGroups = kSwap ? BN : (BN + kBlkN - 1) / kBlkN;
@@ -311,12 +320,14 @@ struct Cfg {
     static constexpr size_t kOffSf = kOffB + size_t(kStages) * kBBytes;
     static constexpr size_t kOffGrp = kOffSf + size_t(kStages) * sizeof(Slot);
     static constexpr size_t kOffInfo = kOffGrp + (kScaleTma ? size_t(kGBufs) * sizeof(Group) : 0);
-    static constexpr size_t kOffBar = kOffInfo + size_t(kMmaWarps * kAccBufs) * sizeof(Info<BN>);
-    static constexpr int kNumBars = 3 * kStages + (2 * kAccBufs + 1) * kMmaWarps + 2 * kGBufs;
+    static constexpr size_t kOffBar = kOffInfo + size_t(kAccSets * kAccBufs) * sizeof(Info<BN>);
+    static constexpr int kHandBar0 = 3 * kStages + (2 * kAccBufs + 1) * kMmaWarps + 2 * kGBufs;
+    static constexpr int kNumBars = kHandBar0 + (kAlt ? 2 : 0);
     static constexpr size_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr size_t kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-    static_assert(kMmaWarps * kAccBufs * BN <= int(kSfCol) - 32 * (kMmaWarps - 1), "TMEM budget");
+    static_assert(kAccSets * kAccBufs * BN <= int(kSfCol) - 32 * (kMmaWarps - 1), "TMEM budget");
+    static_assert(!kAlt || (!kSwap && !kPair), "alternating issuers: single-CTA wide tiles");
     static_assert(!kTwoPerSm || kSmem <= 113 * 1024, "two CTAs per SM: shared memory");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
     static_assert(!kPair || (!kSwap && BN == 256 && kScaleTma && kAccBufs == 1), "CTA-pair configuration");
@@ -329,13 +340,14 @@ struct Cfg {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair>
-__global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>::kThreads),
-                                  (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>::kMinBlocks))
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair,
+          bool kAlt>
+__global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>::kThreads),
+                                  (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>::kMinBlocks))
     fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                           const GemmArgs a) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>;
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>;
     constexpr int kCG = C::kCG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -347,7 +359,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
     Info<BN>* info = reinterpret_cast<Info<BN>*>(smem + C::kOffInfo);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
-    // misc[0]: TMEM base, misc[1]: abort flag, misc[2]: epilogue broadcast
+    // misc[0]: TMEM base, misc[1]: abort flag, misc[2]: epilogue broadcast,
+    // misc[4..5]: accumulator state passed between alternating issuers
 
     const uint32_t bar0 = ptx::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -361,6 +374,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
     // scale-group ring: loaded (TMA) / released (both scale warps)
     auto gfull_bar = [&](int d) { return bar0 + 8u * (3 * kStages + (2 * kAccBufs + 1) * kMW + d); };
     auto gempty_bar = [&](int d) { return bar0 + 8u * (3 * kStages + (2 * kAccBufs + 1) * kMW + C::kGBufs + d); };
+    // alternating issuers: the turn token of issuer w
+    auto hand_bar = [&](uint32_t w) { return bar0 + 8u * (C::kHandBar0 + w); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -393,9 +408,15 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         for (int s = 0; s < kStages; ++s) ptx::mbar_init(sraw_bar(s), 1);   // raw scales landed (cp.async path)
         for (int d = 0; d < C::kGBufs; ++d) {
             ptx::mbar_init(gfull_bar(d), 1);    // producer expect_tx
-            ptx::mbar_init(gempty_bar(d), 2);   // one arrive per scale warp
+            ptx::mbar_init(gempty_bar(d), C::kSfWarps);   // one arrive per scale warp
+        }
+        if (kAlt) {
+            ptx::mbar_init(hand_bar(0), 1);
+            ptx::mbar_init(hand_bar(1), 1);
         }
         misc[1] = 0;
+        misc[4] = 0;
+        misc[5] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -511,7 +532,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             }
         }
         __syncwarp();
-    } else if (warp == 2 || warp == C::kSf2Warp) {
+    } else if (warp == 2 || (C::kSfWarps > 1 && warp == C::kSf2Warp)) {
         // ---------------------------------------------------------- scale loader
         // Turns each stage's raw fp32 scales into UE8M0 words in tcgen05.cp
         // order, checks the power-of-two property, and releases the stage to
@@ -607,9 +628,10 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             }
         };
         if (kScaleTma) {
-            // Two converter warps (2 and 11) take alternate stages.  A stage is
-            // converted once its slot is free (empty barrier) and its scale
-            // group has landed; each warp releases a group once past its end.
+            // The converter warps (2, and 11 unless it issues MMAs) take
+            // alternate stages.  A stage is converted once its slot is free
+            // (empty barrier) and its scale group has landed; each warp
+            // releases a group once past its end.
             const uint32_t sub = warp == 2 ? 0u : 1u;
             // A pair's promotion path reads the peer's raw scales: keep them always.
             const bool keep_raw = kPair || a.force_promote != 0;
@@ -628,7 +650,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                     gready = false;
                 }
                 const bool gend = (it.pos % C::kG) == C::kG - 1 || it.last_kb();
-                if ((nfin & 1u) == sub) {
+                if ((nfin % C::kSfWarps) == sub) {
                     if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 3)) break;
                     if (!gready) {
                         if (!wait_bar(gfull_bar(d), (gcount / C::kGBufs) & 1u, sync, 3)) break;
@@ -775,6 +797,168 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             }
             ptx::cp_async_wait_pending(0);
         }
+        __syncwarp();
+    } else if (kAlt && (warp == 1 || warp == C::kMma2Warp)) {
+        // ------------------------------------------------- alternating MMA issuers
+        // One MMA instruction keeps its issuing warp busy about as long as the
+        // tensor core takes to execute it, so whatever else a single issuer does
+        // per K stage (operand wait, scale-factor copies, commit) leaves the
+        // tensor core idle.  Here two warps share the one accumulator and take
+        // turns: warp 1 issues K stages 0, 2, 4, ... of the CTA's job stream,
+        // warp 12 stages 1, 3, 5, ...  Before its turn a warp waits for its
+        // stage's operands and copies the stage's scale factors into TMEM slots
+        // of its own, overlapping the other warp's MMAs.  The turn passes with a
+        // token: tcgen05.fence::before_thread_sync and an mbarrier arrive by the
+        // holder, a bounded wait and tcgen05.fence::after_thread_sync by the
+        // next, which orders the next warp's MMAs after the holder's.  The token
+        // carries the accumulator state (segments issued; segment open;
+        // accumulate flag) in shared memory.  The MMA sequence is the one a
+        // single issuer would produce.
+        const uint32_t mw = warp == 1 ? 0u : 1u;
+        constexpr uint32_t idesc_f8 = ptx::idesc_f8(kBM, BN);
+        constexpr uint32_t idesc_mx = ptx::idesc_mxf8(kBM, BN);
+        const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
+        const uint32_t leader = lane == 0 ? 1u : 0u;
+        volatile uint32_t* state = misc + 4;   // [0] segments issued, [1] bit 0 open, bit 1 accumulate
+        JobIter it;
+        it.begin(a, first_item, item_step);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t n = 0;        // position in the job stream (both warps count every stage)
+        uint32_t turns = 0;    // turns taken by this warp
+        uint32_t mx_used = 0;  // this warp's block-scaled stages (its scale-slot parity)
+        bool failed = false;
+        auto acc_buf = [&](uint32_t u) { return static_cast<int>(u % kAccBufs); };
+        auto acc_par = [&](uint32_t u) { return (u / kAccBufs) & 1u; };
+        const uint32_t sf_col0 = C::kSfCol - 32u * mw;
+        auto hand_over = [&](int b) {
+            ptx::mbar_arrive_if(leader, accf_bar(0, b));
+            ptx::tc_commit_g_if<1>(leader, accf_bar(0, b));
+        };
+        // Publishes the state and passes the turn to the other warp.
+        auto pass_turn = [&](uint32_t seg, uint32_t flags) {
+            if (lane == 0) {
+                state[0] = seg;
+                state[1] = flags;
+            }
+            __syncwarp();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive_if(leader, hand_bar(mw ^ 1u));
+        };
+        const uint64_t ad_base = ptx::smem_desc(sA0, 16, 1024, ptx::kLayoutSw128);
+        const uint64_t bd_base = ptx::smem_desc(sB0, 16, 1024, ptx::kLayoutSw128);
+        const uint64_t sfa_base = ptx::smem_desc(ptx::smem_u32(sf[0].sfa), 128, 128, ptx::kLayoutNone);
+        const uint64_t sfb_base = ptx::smem_desc(ptx::smem_u32(sf[0].sfb), 128, 128, ptx::kLayoutNone);
+        constexpr uint32_t kSlotStep = sizeof(typename C::Slot) >> 4;
+        const bool ragged_k = (a.K % kBK) != 0;
+        while (it.valid(a) && !failed) {
+            if ((n & 1u) != mw) {   // the other warp's stage
+                it.next(a);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                ++n;
+                continue;
+            }
+            const bool item_last = it.last_kb();
+            if (!wait_bar(full_bar(stage), phase, sync, 2)) { failed = true; break; }
+            ptx::tc_fence_after();
+            if (lane == 0) trace_ev(a, 40 + (n & 31));
+            typename C::Slot& slot = sf[stage];
+            const int nq = ragged_k ? min(4, (a.K - it.kb * kBK) / 32) : 4;
+            const uint64_t ad0 = ad_base + static_cast<uint64_t>(stage * (C::kABytes >> 4));
+            const uint64_t bd0 = bd_base + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
+            const bool mx = slot.pow2 != 0u && !a.force_promote;
+            const uint32_t t_sfa = tmem + sf_col0 + 16u * (mx_used & 1u), t_sfb = t_sfa + 4u;
+            if (mx) {
+                const uint64_t slot_off = static_cast<uint64_t>(stage) * kSlotStep;
+                ptx::tmem_cp_g_if<1>(leader, t_sfa, sfa_base + slot_off);
+#pragma unroll
+                for (int h = 0; h < C::kSfbCopies; ++h)
+                    ptx::tmem_cp_g_if<1>(leader, t_sfb + 4u * h, sfb_base + slot_off + 32u * h);
+                ++mx_used;
+            }
+            // take the turn (the first stage of the job stream needs none)
+            if (n != 0) {
+                const uint32_t r = turns - (mw == 0 ? 1u : 0u);   // tokens received before this one
+                if (!wait_bar_warp(hand_bar(mw), r & 1u, sync, 6, false)) { failed = true; break; }
+                ptx::tc_fence_after();
+            }
+            if (lane == 0) trace_ev(a, 216 + (n & 15));
+            ++turns;
+            uint32_t seg = state[0];
+            const uint32_t st_flags = state[1];
+            bool seg_open = (st_flags & 1u) != 0u;
+            uint32_t acc_flag = (st_flags >> 1) & 1u;
+            if (mx) {
+                if (!seg_open) {
+                    if (!wait_bar(acce_bar(0, acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
+                    ptx::tc_fence_after();
+                    acc_flag = 0;
+                }
+                const int b = acc_buf(seg);
+                const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                if (nq == 4) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        ptx::mma_mxf8_g_if<1>(leader, d, ad0 + 2u * j, bd0 + 2u * j,
+                                              ptx::idesc_sf_ids(idesc_mx, j, j), t_sfa, t_sfb,
+                                              j == 0 ? acc_flag : 1u);
+                } else {
+                    for (int j = 0; j < nq; ++j)
+                        ptx::mma_mxf8_g_if<1>(leader, d, ad0 + 2u * j, bd0 + 2u * j,
+                                              ptx::idesc_sf_ids(idesc_mx, j, j), t_sfa, t_sfb,
+                                              j == 0 ? acc_flag : 1u);
+                }
+                // The item's last stage closes the segment.  The state handed on
+                // already shows it closed; the epilogue is signalled right after.
+                pass_turn(item_last ? seg + 1u : seg, item_last ? 0u : 3u);
+                if (lane == 0) trace_ev(a, 200 + (n & 15));
+                ptx::tc_commit_g_if<1>(leader, empty_bar(stage));
+                if (item_last) {
+                    if (lane == 0) info[b].flags = kInfoLast;
+                    __syncwarp();
+                    hand_over(b);
+                }
+            } else {
+                if (seg_open) {   // hand the open block-scaled segment to the epilogue
+                    const int b = acc_buf(seg);
+                    if (lane == 0) info[b].flags = 0u;
+                    __syncwarp();
+                    hand_over(b);
+                    ++seg;
+                }
+                constexpr bool kBlk128 = kBlkK == 128;
+                const int ngroups = kBlk128 ? 1 : nq;
+                const int steps = kBlk128 ? nq : 1;
+                for (int gidx = 0; gidx < ngroups; ++gidx) {
+                    const int b = acc_buf(seg);
+                    if (!wait_bar(acce_bar(0, b), acc_par(seg) ^ 1u, sync, 2)) { failed = true; break; }
+                    ptx::tc_fence_after();
+                    const int q = C::kNld == 1 ? static_cast<int>(slot.kcol) : gidx;
+                    const bool last = item_last && gidx == ngroups - 1;
+                    for (int r = lane; r < 128; r += 32) info[b].lane_s[r] = slot.lane_raw[r][q];
+                    for (int c = lane; c < BN; c += 32) info[b].col_s[c] = slot.col_raw[c / kBlkN][q];
+                    if (lane == 0) info[b].flags = kInfoPromote | (last ? kInfoLast : 0u);
+                    __syncwarp();
+                    const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                    for (int t = 0; t < steps; ++t) {
+                        const int jj = gidx * steps + t;
+                        ptx::mma_f8_g_if<1>(leader, d, ad0 + 2u * jj, bd0 + 2u * jj, idesc_f8, t > 0 ? 1u : 0u);
+                    }
+                    hand_over(b);
+                    ++seg;
+                }
+                if (failed) break;
+                pass_turn(seg, 0u);
+                if (lane == 0) trace_ev(a, 200 + (n & 15));
+                ptx::tc_commit_g_if<1>(leader, empty_bar(stage));
+            }
+            it.next(a);
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            ++n;
+        }
+        // Let every tcgen05 op issued above land before teardown.
+        ptx::tc_commit_local_g_if<1>(leader, drain_bar(static_cast<int>(mw)));
+        if (lane == 0) wait_bar(drain_bar(static_cast<int>(mw)), 0, sync, 5);
         __syncwarp();
     } else if (warp == 1 || (kMW > 1 && warp == C::kMma2Warp)) {
         // ---------------------------------------------------------- MMA issuer
@@ -994,7 +1178,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         };
         while (it.valid(a)) {
             bool failed = false;
-            if (kMW == 1) {
+            if (C::kAccSets == 1) {
                 bool first = true;
                 while (true) {
                     const int b = static_cast<int>(seg0 % kAccBufs);
@@ -1188,10 +1372,11 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
 
 // Launches one instantiation with programmatic stream serialisation (CTA
 // pairs: as clusters of two, at most as many pairs as can be resident).
-template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair = false>
+template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair = false,
+          bool kAlt = false>
 sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStream_t st) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>;
-    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair>;
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>;
+    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>;
     static bool configured[64] = {};
     static int max_pairs[64] = {};
     int dev = 0;
@@ -1235,13 +1420,21 @@ sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStre
     return SGQ_OK;
 }
 
+// Which kernel configuration a launch uses (chosen by the host's plan).
+struct Variant {
+    bool swap;        // swap-AB narrow tiles (decode)
+    bool pair;        // 256 x 256 tiles on CTA pairs
+    bool alt;         // 128 x 256 tiles with two alternating MMA issuers
+    bool scale_tma;   // scale boxes loaded by TMA
+    int bn;           // MMA N of the swap-AB tile
+};
+
 // One translation unit per [blk_n, blk_k] recipe instantiates all tile shapes.
 // maps: A operand, B operand, A-operand scales, B-operand scales.
 // Pair tiles (256 x 256, cta_group::2) need TMA-loaded scales.
 template <int kBlkN, int kBlkK, bool kScaleTma>
-sgq_status dispatch_tile(bool swap, bool pair, int bn, const CUtensorMap* maps, const GemmArgs& a, int grid,
-                         cudaStream_t st) {
-    if (pair) {
+sgq_status dispatch_tile(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, int grid, cudaStream_t st) {
+    if (v.pair) {
         // six stages fit beside [128,128]-recipe scale groups, five beside [32,32]
         constexpr int kPairStages = kBlkK == 32 ? 5 : 6;
         if constexpr (kScaleTma)
@@ -1249,24 +1442,26 @@ sgq_status dispatch_tile(bool swap, bool pair, int bn, const CUtensorMap* maps, 
         else
             return SGQ_ERR_UNSUPPORTED;
     }
-    if (!swap) return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
-    switch (bn) {
+    if (!v.swap) {
+        if (v.alt) return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma, false, true>(maps, a, grid, st);
+        return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
+    }
+    switch (v.bn) {
         case 16: return run<16, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
         case 32: return run<32, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
         default: return run<64, 7, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
     }
 }
 template <int kBlkN, int kBlkK>
-sgq_status dispatch(bool swap, bool pair, int bn, bool scale_tma, const CUtensorMap* maps, const GemmArgs& a,
-                    int grid, cudaStream_t st) {
-    return scale_tma ? dispatch_tile<kBlkN, kBlkK, true>(swap, pair, bn, maps, a, grid, st)
-                     : dispatch_tile<kBlkN, kBlkK, false>(swap, pair, bn, maps, a, grid, st);
+sgq_status dispatch(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, int grid, cudaStream_t st) {
+    return v.scale_tma ? dispatch_tile<kBlkN, kBlkK, true>(v, maps, a, grid, st)
+                       : dispatch_tile<kBlkN, kBlkK, false>(v, maps, a, grid, st);
 }
 
-sgq_status dispatch_32_32(bool, bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_32_128(bool, bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_128_32(bool, bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_128_128(bool, bool, int, bool, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_32_32(const Variant&, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_32_128(const Variant&, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_128_32(const Variant&, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_128_128(const Variant&, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
 
 }  // namespace gemm
 }  // namespace sgq

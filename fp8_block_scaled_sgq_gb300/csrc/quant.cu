@@ -1,13 +1,6 @@
 // Per-token-group activation quantisation and per-block weight quantisation,
-// bf16 -> FP8 E4M3 codes + fp32 scales, for sm_103a.
-//
-// The rule ("Sgl project Sglang GEMM Interface", Quantization Routines:
-// sgl_per_token_group_quant_8bit with group size, eps, fp8_min/fp8_max and
-// the UE8M0 scale format; UE8M0 activation rounding from sglang PR #42604,
-// Modifications) for each group:
-//   s = max(amax, eps) / 448   (IEEE fp32 division), optionally rounded up to
-//   a power of two; code = E4M3 RNE of clamp(x / s, -448, 448).
-// The conversion instruction saturates to +-448, which is the clamp.
+// bf16 -> FP8 E4M3 codes + fp32 scales, for sm_103a.  The per-group rule is in
+// quant_math.cuh.
 //
 // Memory path: 16-byte bf16 loads (8 elements per thread), a warp-shuffle
 // amax over the lanes of one group, packed 8-byte code stores and one
@@ -18,59 +11,15 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "quant_math.cuh"
 #include "sgq_internal.h"
 
 namespace sgq {
 namespace {
 
-constexpr float kFp8Max = 448.0f;
-constexpr float kEps = 1e-10f;
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// s = max(amax, eps) / 448, optionally rounded up to a power of two (by bits).
-template <bool kUe8m0>
-__device__ __forceinline__ float group_scale(float amax) {
-    float s = __fdiv_rn(fmaxf(amax, kEps), kFp8Max);
-    if (kUe8m0) {
-        uint32_t u = __float_as_uint(s);
-        if (u & 0x7FFFFFu) u = (u & 0xFF800000u) + 0x800000u;
-        s = __uint_as_float(u);
-    }
-    return s;
-}
-
-// x / s for all 8 values, then E4M3 with saturation, packed little-endian.
-template <bool kUe8m0>
-__device__ __forceinline__ uint2 quantize8(const float (&v)[8], float s) {
-    float q[8];
-    if (kUe8m0) {
-        // s = 2^e exactly, so 1/s = 2^-e is exact and x * (1/s) is the
-        // correctly rounded x / s.
-        const float r = __uint_as_float((254u - (__float_as_uint(s) >> 23)) << 23);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(v[i], r);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(v[i], s);
-    }
-    uint32_t p[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __nv_fp8x2_storage_t c =
-            __nv_cvt_float2_to_fp8x2(make_float2(q[2 * i], q[2 * i + 1]), __NV_SATFINITE, __NV_E4M3);
-        p[i] = static_cast<uint32_t>(c);
-    }
-    return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
-}
-
-__device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {
-    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
-    v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
-    v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-}
+using qm::group_scale;
+using qm::quantize8;
+using qm::unpack8;
 
 // One thread per 8 consecutive elements; kTpg = group/8 consecutive lanes own
 // one group.  Loop trip counts are warp-uniform so the shuffles see full warps.
@@ -115,9 +64,9 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
 #pragma unroll
             for (int off = kTpg / 2; off > 0; off >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-            const float s = group_scale<kUe8m0>(amax);
+            const float s = group_scale(amax, kUe8m0);
             if (active) {
-                xq[v] = quantize8<kUe8m0>(f, s);
+                xq[v] = quantize8(f, s, kUe8m0);
                 if ((lane % kTpg) == 0) xs[v / kTpg] = s;
             }
         }
@@ -158,7 +107,7 @@ __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint16_t*
     amax = red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-    const float s = group_scale<kUe8m0>(amax);
+    const float s = group_scale(amax, kUe8m0);
     if (threadIdx.x == 0) ws[nb * KB + kb] = s;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
@@ -168,7 +117,7 @@ __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint16_t*
         if (idx < kVecs && n < N) {
             float f[8];
             unpack8(data[i], f);
-            reinterpret_cast<uint2*>(wq + n * K + kb * kBlkK)[c] = quantize8<kUe8m0>(f, s);
+            reinterpret_cast<uint2*>(wq + n * K + kb * kBlkK)[c] = quantize8(f, s, kUe8m0);
         }
     }
 }

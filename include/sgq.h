@@ -55,6 +55,11 @@ typedef enum {
 /* Never use the block-scale MMA; apply every scale in the fp32 promotion
  * step.  Results stay within the same tolerance; meant for testing. */
 #define SGQ_GEMM_FORCE_PROMOTE 1u
+/* Wide tiles (M > 64) only: force two alternating MMA-issuing warps, or a
+ * single one, instead of the launch plan's choice.  Both issue the same MMA
+ * sequence, so the result is bit-identical either way; meant for testing. */
+#define SGQ_GEMM_ISSUE_ALT 2u
+#define SGQ_GEMM_ISSUE_SINGLE 4u
 
 /*
  * Per-token-group quantisation.

@@ -165,3 +165,47 @@ def test_m_zero_is_noop():
                            torch.zeros((128, 256), dtype=torch.uint8, device="cuda"),
                            torch.ones((1, 2), dtype=torch.float32, device="cuda"), 128, 128)
     assert d.shape == (0, 128)
+
+
+ISSUE = [(300, 520, 1024, 128, 128), (129, 136, 384, 128, 128), (200, 520, 2080, 32, 32),
+         (257, 1032, 4128, 128, 32), (1000, 264, 8192, 32, 128)]
+
+
+@pytest.mark.parametrize("M,N,K,bn,bk", ISSUE)
+@pytest.mark.parametrize("scales", ["pow2", "fp32", "mixed"])
+def test_alternating_issuers_bit_identical(M, N, K, bn, bk, scales):
+    """Wide tiles issued by two alternating MMA warps give the same bits as one
+    issuer (the same MMA sequence into the one accumulator), and match the
+    oracle; with power-of-two, fp32 and mixed scales (promotion segments
+    closed by either warp), ragged M, N and K."""
+    x = synth.activation(M, K, seed=M + K)
+    w = synth.weight(N, K, seed=N + K)
+    aq, a_s = oracle.quant_token_group(x, bk, scales != "fp32")
+    wq, ws = oracle.quant_weight_block(w, bn, bk, scales != "fp32")
+    if scales == "mixed":
+        stage_cols = 128 // bk
+        rng = np.random.default_rng(M + N)
+        for st in range((K + 127) // 128):
+            if rng.random() < 0.4:
+                ws[:, st * stage_cols:(st + 1) * stage_cols] *= np.float32(1.3)
+    args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+    d_alt = sgq.fp8_block_gemm(*args, bn, bk, flags=sgq.SGQ_GEMM_ISSUE_ALT)
+    d_one = sgq.fp8_block_gemm(*args, bn, bk, flags=sgq.SGQ_GEMM_ISSUE_SINGLE)
+    assert sgq.sgq_device_status() == 0
+    assert torch.equal(d_alt, d_one)
+    r = sample_rows(M, 16, seed=M)
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
+    check_gemm(d_alt[torch.from_numpy(r).cuda()], dref, bound, f"alt M={M} N={N} K={K} {scales}")
+
+
+def test_alternating_issuers_prefill_block128():
+    """The full prefill [128,128] shape: alternating and single issuers agree bitwise."""
+    c = synth.WORKLOADS["prefill_block128"][0]
+    x = c.x()
+    aq, a_s = oracle.quant_token_group(x, c.group, c.ue8m0)
+    wq, ws = weights(c.N, c.K, c.blk_n, c.blk_k, c.ue8m0, c.seed)
+    args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+    d_alt = sgq.fp8_block_gemm(*args, c.blk_n, c.blk_k, flags=sgq.SGQ_GEMM_ISSUE_ALT)
+    d_one = sgq.fp8_block_gemm(*args, c.blk_n, c.blk_k, flags=sgq.SGQ_GEMM_ISSUE_SINGLE)
+    assert sgq.sgq_device_status() == 0
+    assert torch.equal(d_alt, d_one)
