@@ -10,7 +10,7 @@ from __future__ import annotations
 from .binding import (  # noqa: F401
     EXPORTS, SGQ_GEMM_DEFAULT, SGQ_GEMM_FORCE_PROMOTE, SGQ_GEMM_ISSUE_ALT, SGQ_GEMM_ISSUE_SINGLE, SgqError,
     load_library, sgq_device_status,
-    sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_launch_count, sgq_quant_token_group,
+    sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_fp8_block_linear, sgq_launch_count, sgq_quant_token_group,
     sgq_quant_weight_block, sgq_version, status_string)
 
 
@@ -46,6 +46,26 @@ def fp8_block_gemm(aq, a_s, wq, ws, blk_n: int, blk_k: int, out=None, flags: int
 
 
 def w8a8_linear(x, wq, ws, blk_n: int, blk_k: int, ue8m0: bool, out=None, stream=None):
-    """Quantise x per token group of blk_k, then the block-scaled GEMM."""
+    """Quantise x per token group of blk_k, then the block-scaled GEMM (two calls)."""
     xq, xs = quant_token_group(x, blk_k, ue8m0, stream)
     return fp8_block_gemm(xq, xs, wq, ws, blk_n, blk_k, out=out, stream=stream)
+
+
+def fp8_block_linear(x, wq, ws, blk_n: int, blk_k: int, ue8m0: bool, out=None, xq=None, xs=None, stream=None):
+    """The same result as w8a8_linear through sgq_fp8_block_linear: one kernel
+    at decode-sized M (xq/xs optional outputs), else two (xq/xs allocated here
+    as scratch when not given)."""
+    import torch
+    M, K = x.shape
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    try:
+        sgq_fp8_block_linear(x, ue8m0, wq, ws, out, M, N, K, blk_n, blk_k, xq, xs, stream)
+    except SgqError as e:
+        if e.status != 2 or xq is not None:   # SGQ_ERR_UNSUPPORTED: needs scratch
+            raise
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+        xs = torch.empty((M, K // blk_k), dtype=torch.float32, device=x.device)
+        sgq_fp8_block_linear(x, ue8m0, wq, ws, out, M, N, K, blk_n, blk_k, xq, xs, stream)
+    return out

@@ -35,6 +35,7 @@ EXPORTS = (
     "sgq_fp8_block_gemm",
     "sgq_fp8_block_gemm_ex",
     "sgq_fp8_block_gemm_noalloc",
+    "sgq_fp8_block_linear",
     "sgq_status_string",
     "sgq_device_status",
     "sgq_launch_count",
@@ -68,8 +69,9 @@ def load_library(path: str = LIB_PATH):
         lib.sgq_fp8_block_gemm.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, P]
         lib.sgq_fp8_block_gemm_ex.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, u32, P]
         lib.sgq_fp8_block_gemm_noalloc.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, P]
+        lib.sgq_fp8_block_linear.argtypes = [P, ci, P, P, P, i64, i64, i64, ci, ci, P, P, P]
         for f in ("sgq_quant_token_group", "sgq_quant_weight_block", "sgq_fp8_block_gemm",
-                  "sgq_fp8_block_gemm_ex", "sgq_fp8_block_gemm_noalloc"):
+                  "sgq_fp8_block_gemm_ex", "sgq_fp8_block_gemm_noalloc", "sgq_fp8_block_linear"):
             getattr(lib, f).restype = ci
         lib.sgq_status_string.argtypes = [ci]
         lib.sgq_status_string.restype = ctypes.c_char_p
@@ -138,6 +140,13 @@ def sgq_fp8_block_gemm_noalloc(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, stream=
     _check(load_library().sgq_fp8_block_gemm_noalloc(_ptr(Aq), _ptr(As), _ptr(Wq), _ptr(Ws), _ptr(D), M, N,
                                                      K, blk_n, blk_k, _stream(stream)),
            "sgq_fp8_block_gemm_noalloc")
+
+
+def sgq_fp8_block_linear(x, ue8m0, Wq, Ws, D, M, N, K, blk_n, blk_k, xq=None, xs=None, stream=None):
+    """Quantise-and-multiply (one kernel at decode-sized M); xq/xs optional outputs."""
+    _check(load_library().sgq_fp8_block_linear(_ptr(x), int(ue8m0), _ptr(Wq), _ptr(Ws), _ptr(D), M, N, K,
+                                               blk_n, blk_k, _ptr(xq), _ptr(xs), _stream(stream)),
+           "sgq_fp8_block_linear")
 
 
 def sgq_device_status(stream=None) -> int:

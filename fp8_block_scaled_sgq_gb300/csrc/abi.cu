@@ -113,6 +113,24 @@ sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const voi
                                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+sgq_status sgq_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const float* Ws, void* D, int64_t M,
+                                int64_t N, int64_t K, int blk_n, int blk_k, void* xq, float* xs,
+                                sgq_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || (blk_n != 32 && blk_n != 128) || (blk_k != 32 && blk_k != 128) ||
+        K % blk_k != 0 || N % 8 != 0 || (ue8m0 != 0 && ue8m0 != 1))
+        return SGQ_ERR_INVALID_ARG;
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return SGQ_ERR_INVALID_ARG;
+    if ((xq == nullptr) != (xs == nullptr)) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!x || !Wq || !Ws || !D) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(D) || (xq && !aligned16(xq)) ||
+        (xs && !aligned16(xs)))
+        return SGQ_ERR_MISALIGNED;
+    return sgq::launch_fp8_block_linear(x, ue8m0, Wq, Ws, D, M, N, K, blk_n, blk_k, xq, xs,
+                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char* sgq_status_string(sgq_status s) {
     switch (s) {
         case SGQ_OK: return "SGQ_OK";

@@ -4,9 +4,9 @@
 
 namespace sgq {
 namespace gemm {
-sgq_status dispatch_32_128(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, int grid,
+sgq_status dispatch_32_128(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const FuseArgs& fz, int grid,
                            cudaStream_t st) {
-    return dispatch<32, 128>(v, maps, a, grid, st);
+    return dispatch<32, 128>(v, maps, a, fz, grid, st);
 }
 }  // namespace gemm
 }  // namespace sgq

@@ -49,6 +49,20 @@ sgq_status make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, i
     return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
 }
 
+// 2-D map over a [rows, K] bf16 matrix (fused quantisation's activations),
+// box = 128 K-elements x box_rows rows, no swizzle; rows past the matrix read
+// as zero.
+sgq_status make_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
+}
+
 // 2-D map over a [rows, ks] fp32 scale matrix; box = box_cols columns (a
 // multiple of 4, i.e. of 16 bytes) x box_rows rows, no swizzle.  Rows and
 // columns past the matrix read as zero.
@@ -131,7 +145,11 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count) {
     int best_s = 1;
     double best = 1e300;
     const int max_s = p.kb_total < 32 ? p.kb_total : 32;
-    for (int s = 1; s <= max_s; ++s) {
+    // Wide tiles keep one split: their single accumulator buffer serialises a
+    // split's epilogue with the next item's MMAs, and the measured split-K
+    // runs were slower (2048 x 1536 x 7168: 44.6 us unsplit, 88.8 us in three).
+    const int max_split = (p.swap || forced > 0) ? max_s : 1;   // SGQ_SPLITS may still force one
+    for (int s = 1; s <= max_split; ++s) {
         const int kbp = (p.kb_total + s - 1) / s;
         if ((p.kb_total + kbp - 1) / kbp != s) continue;   // every split non-empty
         const int64_t items = tiles * s;
@@ -226,11 +244,23 @@ sgq_status noalloc_scratch(unsigned char** out) {
     return SGQ_OK;
 }
 
+// Fused quantisation request: bf16 activations, the UE8M0 choice and the
+// optional code / scale outputs.
+struct Fuse {
+    const void* x;
+    int ue8m0;
+    void* xq;
+    float* xs;
+};
+
 // Plans and launches one GEMM.  noalloc: split-K scratch from the fixed array
 // (its counters cleared by an asynchronous memset), else the per-device
-// workspace.
+// workspace.  fuse (Aq/As unused): the activations are quantised inside the
+// GEMM when the plan is a swap-AB one with TMA-loadable weight scales, else
+// SGQ_ERR_UNSUPPORTED is returned before anything is launched.
 sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D, int64_t M,
-                  int64_t N, int64_t K, int blk_n, int blk_k, uint32_t flags, bool noalloc, cudaStream_t st) {
+                  int64_t N, int64_t K, int blk_n, int blk_k, uint32_t flags, bool noalloc, const Fuse* fuse,
+                  cudaStream_t st) {
     if (get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
     DeviceInfo di;
     sgq_status rc = device_info(&di);
@@ -239,6 +269,9 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     Plan p = make_plan(M, N, K, blk_k, di.sm_count);
     if (flags & SGQ_GEMM_ISSUE_ALT) p.alt = !p.swap && !p.pair;
     if (flags & SGQ_GEMM_ISSUE_SINGLE) p.alt = false;
+    const int64_t ks_all = K / blk_k;
+    const bool scale_tma_ok = (ks_all % 4) == 0 && ks_all >= (blk_k == 128 ? 8 : 16);
+    if (fuse && !(p.swap && scale_tma_ok)) return SGQ_ERR_UNSUPPORTED;
     GemmArgs a{};
     a.As = As;
     a.Ws = Ws;
@@ -259,6 +292,12 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     static const int prefetch = env_int("SGQ_PREFETCH", -1);
     a.prefetch = prefetch;
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
+    FuseArgs fz{};
+    if (fuse) {
+        fz.ue8m0 = fuse->ue8m0;
+        fz.xq_out = static_cast<uint8_t*>(fuse->xq);
+        fz.xs_out = fuse->xs;
+    }
     rc = status_word(&a.status);
     if (rc != SGQ_OK) return rc;
 #ifdef SGQ_TRACE
@@ -295,13 +334,17 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     const void* opA = p.swap ? Wq : Aq;
     const void* opB = p.swap ? Aq : Wq;
     if (make_tmap(&maps[0], opA, a.rows, K, kBM) != SGQ_OK) return SGQ_ERR_CUDA;
-    if (make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+    if (fuse) {
+        if (make_bf16_map(&maps[1], fuse->x, M, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+    } else if (make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) {
+        return SGQ_ERR_CUDA;
+    }
     // Scale rows are TMA-loadable when their pitch is a multiple of 16 bytes
     // and they are at least one box (one group of K stages) wide: a box wider
     // than the matrix's rows is not used.
     static const int scale_tma_on = env_int("SGQ_SCALE_TMA", 1);
     const int gcols = blk_k == 128 ? 8 : 16;
-    const bool scale_tma = scale_tma_on != 0 && (a.ks % 4) == 0 && a.ks >= gcols;
+    const bool scale_tma = (scale_tma_on != 0 || fuse) && (a.ks % 4) == 0 && a.ks >= gcols;
     maps[2] = maps[0];
     maps[3] = maps[1];
     if (scale_tma) {
@@ -309,15 +352,15 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
         // one box = the scales of a group of four K stages (see the kernel)
         if (make_scale_map(&maps[2], p.swap ? Ws : As, p.swap ? nb : M, a.ks, p.swap ? kBM / blk_n : kBM,
                            gcols) != SGQ_OK ||
-            make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks, p.swap ? p.bn : p.bn / blk_n,
-                           gcols) != SGQ_OK)
+            (!fuse && make_scale_map(&maps[3], p.swap ? As : Ws, p.swap ? M : nb, a.ks,
+                                     p.swap ? p.bn : p.bn / blk_n, gcols) != SGQ_OK))
             return SGQ_ERR_CUDA;
     }
-    const Variant v{p.swap, p.pair, p.alt, scale_tma, p.bn};
-    if (blk_n == 32 && blk_k == 32) return dispatch_32_32(v, maps, a, p.grid, st);
-    if (blk_n == 32 && blk_k == 128) return dispatch_32_128(v, maps, a, p.grid, st);
-    if (blk_n == 128 && blk_k == 32) return dispatch_128_32(v, maps, a, p.grid, st);
-    return dispatch_128_128(v, maps, a, p.grid, st);
+    const Variant v{p.swap, p.pair, p.alt, scale_tma, fuse != nullptr, p.bn};
+    if (blk_n == 32 && blk_k == 32) return dispatch_32_32(v, maps, a, fz, p.grid, st);
+    if (blk_n == 32 && blk_k == 128) return dispatch_32_128(v, maps, a, fz, p.grid, st);
+    if (blk_n == 128 && blk_k == 32) return dispatch_128_32(v, maps, a, fz, p.grid, st);
+    return dispatch_128_128(v, maps, a, fz, p.grid, st);
 }
 
 }  // namespace
@@ -326,14 +369,31 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
 sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq, const float* Ws,
                                  void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
                                  uint32_t flags, cudaStream_t st) {
-    return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags, false, st);
+    return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags, false, nullptr, st);
 }
 
 // Same launch plan as launch_fp8_block_gemm, so both give the same result.
 sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq, const float* Ws,
                                          void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
                                          cudaStream_t st) {
-    return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, true, st);
+    return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, true, nullptr, st);
+}
+
+// Quantise-and-multiply.  Decode-sized M (swap-AB plans with TMA-loadable
+// weight scales): one kernel that quantises its activation tiles itself
+// (writing xq/xs too when given).  Otherwise the quantisation kernel into
+// the caller's xq/xs, then the GEMM; without xq/xs that is unsupported.
+sgq_status launch_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const float* Ws, void* D, int64_t M,
+                                   int64_t N, int64_t K, int blk_n, int blk_k, void* xq, float* xs,
+                                   cudaStream_t st) {
+    const gemm::Fuse f{x, ue8m0, xq, xs};
+    const sgq_status rc =
+        gemm::launch(nullptr, nullptr, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, false, &f, st);
+    if (rc != SGQ_ERR_UNSUPPORTED) return rc;
+    if (!xq || !xs) return SGQ_ERR_UNSUPPORTED;
+    const sgq_status q = launch_quant_token_group(x, M, K, blk_k, ue8m0, xq, xs, st);
+    if (q != SGQ_OK) return q;
+    return launch_fp8_block_gemm(xq, xs, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, st);
 }
 
 sgq_status read_and_clear_device_status(cudaStream_t st) {

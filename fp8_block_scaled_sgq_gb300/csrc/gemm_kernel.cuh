@@ -41,6 +41,7 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "quant_math.cuh"
 #include "sgq_internal.h"
 
 namespace sgq {
@@ -104,6 +105,16 @@ struct GemmArgs {
     int tiles_r, tiles_c, kb_total, kb_per_split, splits, items, group_r;
     int force_promote;
     int prefetch;         // < 0: the configuration's weight prefetch depth; else at most this many stages
+};
+
+// Fused quantisation only: UE8M0 rounding of the activation scales, and
+// optional outputs for the codes [M, K] and scales [M, K/blk_k] (written by the
+// CTAs of the first weight tile row; null: not written).  A parameter of its
+// own: growing GemmArgs costs the other configurations registers.
+struct FuseArgs {
+    uint8_t* xq_out;
+    float* xs_out;
+    int ue8m0;
 };
 
 // Walks the (item, k-stage) jobs of one CTA (or CTA pair) in order.
@@ -254,7 +265,7 @@ __device__ __forceinline__ uint32_t sf_word(const float* row, int kcol, uint32_t
 }
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair,
-          bool kAlt>
+          bool kAlt, bool kFuse>
 struct Cfg {
     // Swap-AB tiles are narrow (N <= 64): an MMA costs about as much to issue
     // as a full-width one, so two warps issue alternate K stages of each item
@@ -294,7 +305,18 @@ struct Cfg {
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = (BN / kCG) * kBK;       // B bytes per CTA and stage
     static constexpr uint32_t kXferBytes = kPair ? 16u : 0u;      // the peer's scale-ready transfer
-    static constexpr int kStageBytes = kCG * (kABytes + kBBytes) + kXferBytes;   // bytes the full barrier expects
+    // Fused quantisation (swap-AB): the producer brings the bf16 activation
+    // tile of each stage (kXBytes) to a staging buffer; the scale warps write
+    // its E4M3 codes into the stage's B tile.  The full barrier then counts
+    // only the weight tile's bytes.
+    static constexpr int kXBytes = kFuse ? BN * kBK * 2 : 0;
+    // The epilogue warps quantise, all of them on each stage in turn (kQW
+    // warps per stage, kQGroups stages at a time): the first stage, which the
+    // MMAs wait for, is ready soonest that way (measured: one warp per stage,
+    // eight stages at a time, was slower).
+    static constexpr int kQW = kEpiWarps;
+    static constexpr int kQGroups = kEpiWarps / kQW;
+    static constexpr int kStageBytes = kFuse ? kABytes : kCG * (kABytes + kBBytes) + kXferBytes;
     static constexpr int kCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogue thread
     static constexpr int kLd = kCols < 16 ? kCols : 16;
     static constexpr int kSfbCopies = (BN + 127) / 128;
@@ -314,20 +336,24 @@ struct Cfg {
     static constexpr int kGW = kScalesPerStage == 1 ? 8 : kG * kScalesPerStage;
     using Group = ScaleGroup<kLaneScaleRows, kColScaleRows, kGW>;
     static constexpr int kGBufs = 2;
-    static constexpr uint32_t kGroupBytes = 4u * kGW * (kLaneScaleRows + kColScaleRows);
+    static constexpr uint32_t kGroupBytes = 4u * kGW * (kLaneScaleRows + (kFuse ? 0 : kColScaleRows));
     static constexpr size_t kOffA = 0;
     static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
-    static constexpr size_t kOffSf = kOffB + size_t(kStages) * kBBytes;
+    static constexpr size_t kOffX = kOffB + size_t(kStages) * kBBytes;
+    static constexpr size_t kOffSf = kOffX + size_t(kStages) * kXBytes;
     static constexpr size_t kOffGrp = kOffSf + size_t(kStages) * sizeof(Slot);
     static constexpr size_t kOffInfo = kOffGrp + (kScaleTma ? size_t(kGBufs) * sizeof(Group) : 0);
     static constexpr size_t kOffBar = kOffInfo + size_t(kAccSets * kAccBufs) * sizeof(Info<BN>);
     static constexpr int kHandBar0 = 3 * kStages + (2 * kAccBufs + 1) * kMmaWarps + 2 * kGBufs;
-    static constexpr int kNumBars = kHandBar0 + (kAlt ? 2 : 0);
+    static constexpr int kQBar0 = kHandBar0 + (kAlt ? 2 : 0);
+    static constexpr int kNumBars = kQBar0 + (kFuse ? kStages : 0);
     static constexpr size_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr size_t kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(kAccSets * kAccBufs * BN <= int(kSfCol) - 32 * (kMmaWarps - 1), "TMEM budget");
     static_assert(!kAlt || (!kSwap && !kPair), "alternating issuers: single-CTA wide tiles");
+    static_assert(!kFuse || (kSwap && kScaleTma), "fused quantisation: swap-AB tiles with TMA scale groups");
+    static_assert(kOffX % 1024 == 0 && kOffSf % 128 == 0, "staging and slots aligned");
     static_assert(!kTwoPerSm || kSmem <= 113 * 1024, "two CTAs per SM: shared memory");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
     static_assert(!kPair || (!kSwap && BN == 256 && kScaleTma && kAccBufs == 1), "CTA-pair configuration");
@@ -341,19 +367,21 @@ struct Cfg {
 };
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair,
-          bool kAlt>
-__global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>::kThreads),
-                                  (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>::kMinBlocks))
+          bool kAlt, bool kFuse>
+__global__ void __launch_bounds__(
+    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>::kThreads),
+    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>::kMinBlocks))
     fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                          const GemmArgs a) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>;
+                          const GemmArgs a, const FuseArgs fz) {
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>;
     constexpr int kCG = C::kCG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + C::kOffA;
     uint8_t* sB = smem + C::kOffB;
+    uint8_t* sX = smem + C::kOffX;   // bf16 activation staging (fused quantisation)
     typename C::Slot* sf = reinterpret_cast<typename C::Slot*>(smem + C::kOffSf);
     typename C::Group* grp = reinterpret_cast<typename C::Group*>(smem + C::kOffGrp);
     Info<BN>* info = reinterpret_cast<Info<BN>*>(smem + C::kOffInfo);
@@ -376,6 +404,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
     auto gempty_bar = [&](int d) { return bar0 + 8u * (3 * kStages + (2 * kAccBufs + 1) * kMW + C::kGBufs + d); };
     // alternating issuers: the turn token of issuer w
     auto hand_bar = [&](uint32_t w) { return bar0 + 8u * (C::kHandBar0 + w); };
+    // fused quantisation: stage s's codes and scales written (epilogue warps)
+    auto qdone_bar = [&](int s) { return bar0 + 8u * (C::kQBar0 + s); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -414,6 +444,8 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
             ptx::mbar_init(hand_bar(0), 1);
             ptx::mbar_init(hand_bar(1), 1);
         }
+        if constexpr (kFuse)
+            for (int s = 0; s < kStages; ++s) ptx::mbar_init(qdone_bar(s), C::kQW);
         misc[1] = 0;
         misc[4] = 0;
         misc[5] = 0;
@@ -442,6 +474,49 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         // grid to finish (griddepcontrol.wait) before touching its outputs.
         ptx::launch_dependents();
     }
+
+    // Fused quantisation of stage s (job j), by the epilogue warps (nthr
+    // threads, this one tid): the bf16 tile [BN tokens x 128] in the staging
+    // buffer becomes E4M3 codes in the stage's B tile (the 128-byte swizzled
+    // layout the TMA would have written) and fp32 group scales in the slot's
+    // col_raw, 0 for groups past K or tokens past M (as the scale box would
+    // read them).  One thread per 8 elements; kBlkK/8 neighbouring lanes share
+    // a group (shuffle amax), as in the stand-alone quantisation kernel, so
+    // the codes and scales are the same.
+    auto quantize_stage = [&](int s, const JobIter& j, typename C::Slot& slot, int tid, int nthr) {
+        static_assert(!kFuse || (BN * 16) % (C::kQW * 32) == 0, "uniform trip count");
+        if constexpr (!kFuse) return;
+        constexpr int kTpg = kBlkK / 8;
+        const uint8_t* xs = sX + s * C::kXBytes;
+        uint8_t* bq = sB + s * C::kBBytes;
+        const int col0 = j.tc * BN;
+        const int kbase = j.kb * kBK;
+        const bool ue = fz.ue8m0 != 0;
+        const bool out = fz.xq_out != nullptr && j.tr == 0;
+        const int lane_id = tid & 31;
+        for (int v = tid; v < BN * 16; v += nthr) {   // trip count uniform: nthr divides BN * 16
+            const int tk = v >> 4, c = v & 15;
+            const uint4 w = *reinterpret_cast<const uint4*>(xs + tk * 256 + c * 16);
+            float f[8];
+            qm::unpack8(w, f);
+            float amax = qm::amax8(f);
+#pragma unroll
+            for (int off = kTpg / 2; off > 0; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+            const float sc = qm::group_scale(amax, ue);
+            const uint2 q = qm::quantize8(f, sc, ue);
+            *reinterpret_cast<uint2*>(bq + tk * 128 + ((((c >> 1) ^ (tk & 7)) << 4) | ((c & 1) << 3))) = q;
+            const int gq = (c * 8) / kBlkK;               // scale column within the stage
+            const bool kin = kbase + gq * kBlkK < a.K;    // the group lies inside K
+            const bool tin = col0 + tk < a.M;
+            if ((lane_id % kTpg) == 0) slot.col_raw[tk][gq] = (kin && tin) ? sc : 0.0f;
+            if (out && kin && tin) {
+                const int64_t row = col0 + tk;
+                *reinterpret_cast<uint2*>(fz.xq_out + row * a.K + kbase + c * 8) = q;
+                if ((lane_id % kTpg) == 0) fz.xs_out[row * a.ks + j.kb * C::kScalesPerStage + gq] = sc;
+            }
+        }
+    };
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
@@ -477,7 +552,14 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 load_tile(w_dst(s), tmW, j.kb * kBK, w_row(j), s);
             };
             auto load_x = [&](int s, const JobIter& j) {
-                load_tile(x_dst(s), tmX, j.kb * kBK, x_row(j), s);
+                if constexpr (kFuse) {
+                    // bf16 tile to the staging buffer, on its own barrier
+                    const uint32_t xb = sraw_bar(s);
+                    ptx::mbar_arrive_expect_tx_if(leader, xb, C::kXBytes);
+                    ptx::tma_load_2d_if(leader, ptx::smem_u32(sX) + s * C::kXBytes, tmX, j.kb * kBK, x_row(j), xb);
+                } else {
+                    load_tile(x_dst(s), tmX, j.kb * kBK, x_row(j), s);
+                }
             };
             // Scale group: at the first stage of every kG-stage group of an item,
             // one box per operand with the raw scales of the whole group.
@@ -495,7 +577,9 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 ptx::mbar_arrive_expect_tx_if(leader, gfull_bar(d), C::kGroupBytes);
                 const uint32_t lane_dst = ptx::smem_u32(&g.lane[0][0]), col_dst = ptx::smem_u32(&g.col[0][0]);
                 ptx::tma_load_2d_if(leader, kSwap ? lane_dst : col_dst, tmWs, gx, ws_row(j), gfull_bar(d));
-                ptx::tma_load_2d_if(leader, kSwap ? col_dst : lane_dst, tmXs, gx, xs_row(j), gfull_bar(d));
+                // (fused quantisation computes the activation scales itself)
+                if constexpr (!kFuse)
+                    ptx::tma_load_2d_if(leader, kSwap ? col_dst : lane_dst, tmXs, gx, xs_row(j), gfull_bar(d));
                 ++gcount;
             };
             JobIter it;
@@ -583,9 +667,12 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         // Grouped path: converts stage j from the group buffer g, whose column 0
         // is scale column gx; keeps the stage's raw scales in the slot when the
         // fp32 promotion step may need them.
+        // Fused quantisation: the B-side (token) scales come from the slot, where
+        // quantize_stage left them.
         auto convert_g = [&](typename C::Slot& slot, const JobIter& j, const typename C::Group& g, int c0,
                              bool keep_raw) {
             const int row0 = kSwap ? j.tr * kBM : a_row0(j), col0 = j.tc * BN;
+
             uint32_t bad = 0;
             uint32_t w4[4];
 #pragma unroll
@@ -603,7 +690,11 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                     const int c = h * 128 + lane + 32 * i;
                     const int ci = kSwap ? c : c / kBlkN;
                     const bool valid = c < BN && (kSwap ? col0 + c : col0 + ci * kBlkN) < a.cols;
-                    w4[i] = valid ? sf_word<kNld>(&g.col[ci < kCR ? ci : 0][c0], 0, bad) : 0x7F7F7F7Fu;
+                    const int cr = ci < kCR ? ci : 0;
+                    if constexpr (kFuse)
+                        w4[i] = valid ? sf_word<kNld>(&slot.col_raw[cr][0], 0, bad) : 0x7F7F7F7Fu;
+                    else
+                        w4[i] = valid ? sf_word<kNld>(&g.col[cr][c0], 0, bad) : 0x7F7F7F7Fu;
                 }
                 *reinterpret_cast<uint4*>(&slot.sfb[h * 128 + lane * 4]) =
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -614,9 +705,10 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                 for (int r = lane; r < kLR; r += 32)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) slot.lane_raw[r][q] = q < kNld ? g.lane[r][c0 + q] : 0.0f;
-                for (int r = lane; r < kCR; r += 32)
+                if constexpr (!kFuse)
+                    for (int r = lane; r < kCR; r += 32)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) slot.col_raw[r][q] = q < kNld ? g.col[r][c0 + q] : 0.0f;
+                        for (int q = 0; q < 4; ++q) slot.col_raw[r][q] = q < kNld ? g.col[r][c0 + q] : 0.0f;
             }
             if (lane == 0) {
                 slot.pow2 = all_ok ? 1u : 0u;
@@ -655,6 +747,10 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
                     if (!gready) {
                         if (!wait_bar(gfull_bar(d), (gcount / C::kGBufs) & 1u, sync, 3)) break;
                         gready = true;
+                    }
+                    // fused: the epilogue warps have quantised the stage
+                    if constexpr (kFuse) {
+                        if (!wait_bar(qdone_bar(stage), phase, sync, 3)) break;
                     }
                     if (lane == 0) trace_ev(a, 104 + (nfin & 31));
                     convert_g(sf[stage], it, grp[d], it.kb * C::kScalesPerStage - gx, keep_raw);
@@ -1143,6 +1239,7 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         uint32_t n_items = 0;
         float acc[kCols];
         float acc1[kCols];             // second issuer's sum (two-issuer configurations)
+        uint32_t qn = 0;               // fused quantisation: stages quantised so far
         // Adds one accumulator segment of issuer m into `dst` (first: overwrite).
         auto consume = [&](int m, uint32_t sg, bool first, float (&dst)[kCols]) {
             const int b = static_cast<int>(sg % kAccBufs);
@@ -1178,6 +1275,32 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
         };
         while (it.valid(a)) {
             bool failed = false;
+            if constexpr (kFuse) {
+                // Quantise this item's activation tiles as they land, before
+                // waiting for its accumulators: warp group qg (kQW warps) takes
+                // the item's stages p with p % kQGroups == qg, in order.
+                const int qg = ew / C::kQW;
+                const int qt = (ew % C::kQW) * 32 + lane;
+                JobIter q = it;
+                for (int p = 0; p < it.nkb && !failed; ++p) {
+                    const uint32_t n = qn + static_cast<uint32_t>(p);
+                    if (p % C::kQGroups == qg) {
+                        const int s = static_cast<int>(n % kStages);
+                        const uint32_t ph = (n / kStages) & 1u;
+                        if (!wait_bar_warp(empty_bar(s), ph ^ 1u, sync, 4, false) ||
+                            !wait_bar_warp(sraw_bar(s), ph, sync, 4, false)) {
+                            failed = true;
+                            break;
+                        }
+                        quantize_stage(s, q, sf[s], qt, C::kQW * 32);
+                        ptx::fence_proxy_async_smem();   // codes: read by the MMA (async proxy)
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(qdone_bar(s));
+                    }
+                    q.next(a);
+                }
+                qn += static_cast<uint32_t>(it.nkb);
+            }
             if (C::kAccSets == 1) {
                 bool first = true;
                 while (true) {
@@ -1373,10 +1496,10 @@ __global__ void __launch_bounds__((Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlk
 // Launches one instantiation with programmatic stream serialisation (CTA
 // pairs: as clusters of two, at most as many pairs as can be resident).
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair = false,
-          bool kAlt = false>
-sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStream_t st) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>;
-    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt>;
+          bool kAlt = false, bool kFuse = false>
+sgq_status run(const CUtensorMap* maps, const GemmArgs& args, const FuseArgs& fz, int grid, cudaStream_t st) {
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>;
+    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>;
     static bool configured[64] = {};
     static int max_pairs[64] = {};
     int dev = 0;
@@ -1414,7 +1537,7 @@ sgq_status run(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStre
         grid = 2 * pairs;
     }
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], args) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], args, fz) != cudaSuccess)
         return SGQ_ERR_CUDA;
     note_launch();
     return SGQ_OK;
@@ -1426,6 +1549,7 @@ struct Variant {
     bool pair;        // 256 x 256 tiles on CTA pairs
     bool alt;         // 128 x 256 tiles with two alternating MMA issuers
     bool scale_tma;   // scale boxes loaded by TMA
+    bool fuse;        // swap-AB tiles that quantise the bf16 activations themselves
     int bn;           // MMA N of the swap-AB tile
 };
 
@@ -1433,35 +1557,49 @@ struct Variant {
 // maps: A operand, B operand, A-operand scales, B-operand scales.
 // Pair tiles (256 x 256, cta_group::2) need TMA-loaded scales.
 template <int kBlkN, int kBlkK, bool kScaleTma>
-sgq_status dispatch_tile(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, int grid, cudaStream_t st) {
+sgq_status dispatch_tile(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const FuseArgs& fz, int grid,
+                         cudaStream_t st) {
+    if (v.fuse) {
+        // the bf16 staging buffer takes the place of one to three ring stages
+        if constexpr (kScaleTma) {
+            switch (v.bn) {
+                case 16: return run<16, 8, true, 2, kBlkN, kBlkK, true, false, false, true>(maps, a, fz, grid, st);
+                case 32: return run<32, 7, true, 2, kBlkN, kBlkK, true, false, false, true>(maps, a, fz, grid, st);
+                default: return run<64, 5, true, 2, kBlkN, kBlkK, true, false, false, true>(maps, a, fz, grid, st);
+            }
+        } else {
+            return SGQ_ERR_UNSUPPORTED;
+        }
+    }
     if (v.pair) {
         // six stages fit beside [128,128]-recipe scale groups, five beside [32,32]
         constexpr int kPairStages = kBlkK == 32 ? 5 : 6;
         if constexpr (kScaleTma)
-            return run<256, kPairStages, false, 1, kBlkN, kBlkK, true, true>(maps, a, grid, st);
+            return run<256, kPairStages, false, 1, kBlkN, kBlkK, true, true>(maps, a, fz, grid, st);
         else
             return SGQ_ERR_UNSUPPORTED;
     }
     if (!v.swap) {
-        if (v.alt) return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma, false, true>(maps, a, grid, st);
-        return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
+        if (v.alt) return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma, false, true>(maps, a, fz, grid, st);
+        return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma>(maps, a, fz, grid, st);
     }
     switch (v.bn) {
-        case 16: return run<16, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
-        case 32: return run<32, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
-        default: return run<64, 7, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, grid, st);
+        case 16: return run<16, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, fz, grid, st);
+        case 32: return run<32, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, fz, grid, st);
+        default: return run<64, 7, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, fz, grid, st);
     }
 }
 template <int kBlkN, int kBlkK>
-sgq_status dispatch(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, int grid, cudaStream_t st) {
-    return v.scale_tma ? dispatch_tile<kBlkN, kBlkK, true>(v, maps, a, grid, st)
-                       : dispatch_tile<kBlkN, kBlkK, false>(v, maps, a, grid, st);
+sgq_status dispatch(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const FuseArgs& fz, int grid,
+                    cudaStream_t st) {
+    return v.scale_tma ? dispatch_tile<kBlkN, kBlkK, true>(v, maps, a, fz, grid, st)
+                       : dispatch_tile<kBlkN, kBlkK, false>(v, maps, a, fz, grid, st);
 }
 
-sgq_status dispatch_32_32(const Variant&, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_32_128(const Variant&, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_128_32(const Variant&, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
-sgq_status dispatch_128_128(const Variant&, const CUtensorMap*, const GemmArgs&, int, cudaStream_t);
+sgq_status dispatch_32_32(const Variant&, const CUtensorMap*, const GemmArgs&, const FuseArgs&, int, cudaStream_t);
+sgq_status dispatch_32_128(const Variant&, const CUtensorMap*, const GemmArgs&, const FuseArgs&, int, cudaStream_t);
+sgq_status dispatch_128_32(const Variant&, const CUtensorMap*, const GemmArgs&, const FuseArgs&, int, cudaStream_t);
+sgq_status dispatch_128_128(const Variant&, const CUtensorMap*, const GemmArgs&, const FuseArgs&, int, cudaStream_t);
 
 }  // namespace gemm
 }  // namespace sgq

@@ -28,6 +28,9 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
 sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq,
                                          const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
                                          int blk_n, int blk_k, cudaStream_t stream);
+sgq_status launch_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const float* Ws, void* D,
+                                   int64_t M, int64_t N, int64_t K, int blk_n, int blk_k, void* xq,
+                                   float* xs, cudaStream_t stream);
 // Reads and clears the device status word of the current device (after a sync).
 sgq_status read_and_clear_device_status(cudaStream_t stream);
 

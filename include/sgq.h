@@ -179,6 +179,32 @@ sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const voi
                                       const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
                                       int blk_n, int blk_k, sgq_stream_t stream);
 
+/*
+ * Quantise-and-multiply: the whole W8A8 linear layer in one call.
+ *
+ *   D = sgq_fp8_block_gemm(quant(x), Wq, Ws)   with
+ *   quant(x) = sgq_quant_token_group(x, group = blk_k, ue8m0)
+ *
+ * x: bf16 [M, K] (device).  Wq, Ws, D, M, N, K, blk_n, blk_k: as for
+ * sgq_fp8_block_gemm.  xq (uint8 E4M3 [M, K]) and xs (fp32 [M, K/blk_k]):
+ * both NULL or both given; when given they receive the quantised activations,
+ * bit-identical to sgq_quant_token_group's.  The result D is bit-identical to
+ * sgq_quant_token_group followed by sgq_fp8_block_gemm.
+ *
+ * No counterpart in the pages as one call; it fuses the two steps above.  For
+ * decode-sized M (M <= 64) with K/blk_k a multiple of 4 and at least 8 (blk_k
+ * = 128) or 16 (blk_k = 32) -- every decode shape the pages use -- it is ONE
+ * kernel: the GEMM's scale warps quantise each bf16 activation tile in
+ * shared memory, so the codes never go through HBM and a launch disappears.
+ * Any other shape runs the two kernels back to back and then needs xq/xs as
+ * scratch; without them it returns SGQ_ERR_UNSUPPORTED before launching.
+ * Errors and the launch-overlap contract: as for sgq_fp8_block_gemm (x is
+ * read only after the preceding kernel has finished).
+ */
+sgq_status sgq_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const float* Ws,
+                                void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                void* xq, float* xs, sgq_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sgq_status_string(sgq_status s);
 

@@ -106,6 +106,25 @@ def test_gemm_validation(lib):
     assert lib.sgq_fp8_block_gemm(A, B, C, D, E, 16, 256, 512, 128, 64, S) == INV
 
 
+def test_linear_validation(lib):
+    INV, MIS, OK = binding.SGQ_ERR_INVALID_ARG, binding.SGQ_ERR_MISALIGNED, binding.SGQ_OK
+    f = binding.load_library().sgq_fp8_block_linear
+    args = lambda **k: [k.get("x", A), k.get("ue", 1), k.get("Wq", C), k.get("Ws", D), k.get("D", E),
+                        k.get("M", 16), k.get("N", 256), k.get("K", 512), k.get("bn", 128), k.get("bk", 128),
+                        k.get("xq", None), k.get("xs", None), S]
+    assert f(*args(ue=2)) == INV                 # ue8m0 not 0/1
+    assert f(*args(bk=64)) == INV
+    assert f(*args(K=96)) == INV                 # K % blk_k
+    assert f(*args(N=260)) == INV                # N % 8
+    assert f(*args(xq=B)) == INV                 # xq without xs
+    assert f(*args(xs=B)) == INV                 # xs without xq
+    assert f(*args(x=None)) == INV
+    assert f(*args(Ws=None)) == INV
+    assert f(*args(x=A + 2)) == MIS
+    assert f(*args(xq=B + 8, xs=B)) == MIS
+    assert f(*args(M=0, x=None, D=None)) == OK   # M == 0: no-op
+
+
 def test_binding_raises(lib):
     with pytest.raises(sgq.SgqError) as ei:
         sgq.sgq_quant_token_group(A, 4, 96, 128, 0, B, C, stream=S)
