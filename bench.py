@@ -204,6 +204,18 @@ def step_fn(sgq, per, wq, ws, stream, gemm_only=False):
         sgq.sgq_fp8_block_gemm(xq, xs, wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, stream)
 
 
+def fused_step_fn(sgq, per, wq, ws, stream):
+    """The same layer through sgq_fp8_block_linear (one kernel per case at
+    decode-sized M; codes and scales stay on chip)."""
+    for c, x, _, _, d in per:
+        sgq.sgq_fp8_block_linear(x, int(c.ue8m0), wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, None, None, stream)
+
+
+def fusable(cases):
+    return all(c.M <= 64 and (c.K // c.blk_k) % 4 == 0 and c.K // c.blk_k >= (8 if c.blk_k == 128 else 16)
+               for c in cases)
+
+
 def run_ours(args, ws_, rank, local):
     import fp8_block_scaled_sgq_gb300 as sgq
     from fp8_block_scaled_sgq_gb300 import build as sgq_build
@@ -267,6 +279,8 @@ def run_ours(args, ws_, rank, local):
         return e0.elapsed_time(e1) / steps   # ms per step
 
     graph = capture(full_step, args.steps)
+    fused_graph = (capture(lambda r, sp: fused_step_fn(sgq, per, *wrot[r], sp), args.steps)
+                   if fusable(cases) else None)
     case_graphs = [capture(lambda r, sp, i=i: step_fn(sgq, per[i:i + 1], *wrot[r], sp, gemm_only=True),
                            args.steps) for i in range(len(per))]
 
@@ -282,10 +296,13 @@ def run_ours(args, ws_, rank, local):
         preheat(args.preheat)
         ms_step = timed(graph, args.steps)
         ms_case = [timed(cg, args.steps) for cg in case_graphs]
+        ms_fused = timed(fused_graph, args.steps) if fused_graph is not None else None
     clocks = cs.summary()
     ms_step = max_over_ranks(ms_step, ws_, device)
     ms_case = [max_over_ranks(t, ws_, device) for t in ms_case]
     ms_gemm = sum(ms_case)
+    if ms_fused is not None:
+        ms_fused = max_over_ranks(ms_fused, ws_, device)
     gpu_launches = 2 * len(cases) * args.steps   # quant + GEMM per case per step (graph replays)
     assert sgq.sgq_launch_count() == launches0   # replays do not call the library
 
@@ -355,6 +372,13 @@ def run_ours(args, ws_, rank, local):
         "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
+    if ms_fused is not None:
+        # algorithmic bytes of the fused layer: x, weights, D (no Aq/As round trip)
+        fused_bytes = sum(2 * c.M * c.K + c.N * c.K + 4 * math.ceil(c.N / c.blk_n) * (c.K // c.blk_k)
+                          + 2 * c.M * c.N for c in cases)
+        result["fused"] = {"entry": "sgq_fp8_block_linear", "ms_per_step": round(ms_fused, 5),
+                           "gbs": round(ws_ * fused_bytes / (ms_fused * 1e-3) / 1e9, 2),
+                           "launches_per_step": len(cases)}
     return result
 
 

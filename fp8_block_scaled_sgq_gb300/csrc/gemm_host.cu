@@ -49,20 +49,6 @@ sgq_status make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, i
     return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
 }
 
-// 2-D map over a [rows, K] bf16 matrix (fused quantisation's activations),
-// box = 128 K-elements x box_rows rows, no swizzle; rows past the matrix read
-// as zero.
-sgq_status make_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int box_rows) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
-}
-
 // 2-D map over a [rows, ks] fp32 scale matrix; box = box_cols columns (a
 // multiple of 4, i.e. of 16 bytes) x box_rows rows, no swizzle.  Rows and
 // columns past the matrix read as zero.
@@ -294,6 +280,7 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
     FuseArgs fz{};
     if (fuse) {
+        fz.x = static_cast<const uint16_t*>(fuse->x);
         fz.ue8m0 = fuse->ue8m0;
         fz.xq_out = static_cast<uint8_t*>(fuse->xq);
         fz.xs_out = fuse->xs;
@@ -335,7 +322,7 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     const void* opB = p.swap ? Aq : Wq;
     if (make_tmap(&maps[0], opA, a.rows, K, kBM) != SGQ_OK) return SGQ_ERR_CUDA;
     if (fuse) {
-        if (make_bf16_map(&maps[1], fuse->x, M, K, p.bn) != SGQ_OK) return SGQ_ERR_CUDA;
+        maps[1] = maps[0];   // the activations are read by the kernel's threads, not by TMA
     } else if (make_tmap(&maps[1], opB, a.cols, K, p.pair ? p.bn / 2 : p.bn) != SGQ_OK) {
         return SGQ_ERR_CUDA;
     }
@@ -383,12 +370,17 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
 // weight scales): one kernel that quantises its activation tiles itself
 // (writing xq/xs too when given).  Otherwise the quantisation kernel into
 // the caller's xq/xs, then the GEMM; without xq/xs that is unsupported.
+// Every weight tile re-quantises its CTA's activations, so with M > 32 the
+// single kernel is slower than the pair (measured at N=7168, K=2048: 18.5 vs
+// 12.5 us at M=64); there it is used only when no scratch is given.
 sgq_status launch_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const float* Ws, void* D, int64_t M,
                                    int64_t N, int64_t K, int blk_n, int blk_k, void* xq, float* xs,
                                    cudaStream_t st) {
+    const bool prefer_pair = M > 32 && xq && xs;
     const gemm::Fuse f{x, ue8m0, xq, xs};
     const sgq_status rc =
-        gemm::launch(nullptr, nullptr, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, false, &f, st);
+        prefer_pair ? SGQ_ERR_UNSUPPORTED
+                    : gemm::launch(nullptr, nullptr, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, false, &f, st);
     if (rc != SGQ_ERR_UNSUPPORTED) return rc;
     if (!xq || !xs) return SGQ_ERR_UNSUPPORTED;
     const sgq_status q = launch_quant_token_group(x, M, K, blk_k, ue8m0, xq, xs, st);

@@ -107,11 +107,12 @@ struct GemmArgs {
     int prefetch;         // < 0: the configuration's weight prefetch depth; else at most this many stages
 };
 
-// Fused quantisation only: UE8M0 rounding of the activation scales, and
-// optional outputs for the codes [M, K] and scales [M, K/blk_k] (written by the
+// Fused quantisation only: the bf16 activations, UE8M0 rounding of the
+// activation scales, and optional outputs for the codes [M, K] and scales [M, K/blk_k] (written by the
 // CTAs of the first weight tile row; null: not written).  A parameter of its
 // own: growing GemmArgs costs the other configurations registers.
 struct FuseArgs {
+    const uint16_t* x;   // bf16 activations [M, K]
     uint8_t* xq_out;
     float* xs_out;
     int ue8m0;
@@ -297,7 +298,9 @@ struct Cfg {
     // Weight stages loaded before the programmatic-dependency wait.  Loads of
     // one SM leave in issue order, so a deep weight prefetch delays the first
     // activation tiles behind it; the swap-AB (decode) tiles start with none.
-    static constexpr int kPrefetch = (kSwap && !kTwoPerSm) ? 0 : kStages;
+    // With fused quantisation no activation tile goes through the TMA, so all
+    // ring stages of weights (and their scale boxes) go out before the wait.
+    static constexpr int kPrefetch = kFuse ? kStages : ((kSwap && !kTwoPerSm) ? 0 : kStages);
     // CTA pair (cluster of two, cta_group::2): the tile is 256 x BN; each CTA
     // holds 128 A rows and BN/2 B rows per stage, the leader issues the MMAs.
     static constexpr int kCG = kPair ? 2 : 1;
@@ -305,17 +308,13 @@ struct Cfg {
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = (BN / kCG) * kBK;       // B bytes per CTA and stage
     static constexpr uint32_t kXferBytes = kPair ? 16u : 0u;      // the peer's scale-ready transfer
-    // Fused quantisation (swap-AB): the producer brings the bf16 activation
-    // tile of each stage (kXBytes) to a staging buffer; the scale warps write
-    // its E4M3 codes into the stage's B tile.  The full barrier then counts
-    // only the weight tile's bytes.
-    static constexpr int kXBytes = kFuse ? BN * kBK * 2 : 0;
-    // The epilogue warps quantise, all of them on each stage in turn (kQW
-    // warps per stage, kQGroups stages at a time): the first stage, which the
-    // MMAs wait for, is ready soonest that way (measured: one warp per stage,
-    // eight stages at a time, was slower).
+    // Fused quantisation (swap-AB): the epilogue warps read each stage's bf16
+    // activation tile with plain loads and write its E4M3 codes into the
+    // stage's B tile; the full barrier counts only the weight tile's bytes.
+    // The epilogue warps quantise, all of them on each stage in turn: the
+    // first stage, which the MMAs wait for, is ready soonest that way
+    // (measured: one warp per stage, eight stages at a time, was slower).
     static constexpr int kQW = kEpiWarps;
-    static constexpr int kQGroups = kEpiWarps / kQW;
     static constexpr int kStageBytes = kFuse ? kABytes : kCG * (kABytes + kBBytes) + kXferBytes;
     static constexpr int kCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogue thread
     static constexpr int kLd = kCols < 16 ? kCols : 16;
@@ -334,13 +333,12 @@ struct Cfg {
     // that a group starting at any column fits behind a 16-byte aligned start).
     static constexpr int kG = 4;
     static constexpr int kGW = kScalesPerStage == 1 ? 8 : kG * kScalesPerStage;
-    using Group = ScaleGroup<kLaneScaleRows, kColScaleRows, kGW>;
+    using Group = ScaleGroup<kLaneScaleRows, kFuse ? 1 : kColScaleRows, kGW>;   // fused: no token box
     static constexpr int kGBufs = 2;
     static constexpr uint32_t kGroupBytes = 4u * kGW * (kLaneScaleRows + (kFuse ? 0 : kColScaleRows));
     static constexpr size_t kOffA = 0;
     static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
-    static constexpr size_t kOffX = kOffB + size_t(kStages) * kBBytes;
-    static constexpr size_t kOffSf = kOffX + size_t(kStages) * kXBytes;
+    static constexpr size_t kOffSf = kOffB + size_t(kStages) * kBBytes;
     static constexpr size_t kOffGrp = kOffSf + size_t(kStages) * sizeof(Slot);
     static constexpr size_t kOffInfo = kOffGrp + (kScaleTma ? size_t(kGBufs) * sizeof(Group) : 0);
     static constexpr size_t kOffBar = kOffInfo + size_t(kAccSets * kAccBufs) * sizeof(Info<BN>);
@@ -353,7 +351,7 @@ struct Cfg {
     static_assert(kAccSets * kAccBufs * BN <= int(kSfCol) - 32 * (kMmaWarps - 1), "TMEM budget");
     static_assert(!kAlt || (!kSwap && !kPair), "alternating issuers: single-CTA wide tiles");
     static_assert(!kFuse || (kSwap && kScaleTma), "fused quantisation: swap-AB tiles with TMA scale groups");
-    static_assert(kOffX % 1024 == 0 && kOffSf % 128 == 0, "staging and slots aligned");
+    static_assert(kOffSf % 128 == 0, "scale slots aligned");
     static_assert(!kTwoPerSm || kSmem <= 113 * 1024, "two CTAs per SM: shared memory");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
     static_assert(!kPair || (!kSwap && BN == 256 && kScaleTma && kAccBufs == 1), "CTA-pair configuration");
@@ -381,7 +379,6 @@ __global__ void __launch_bounds__(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + C::kOffA;
     uint8_t* sB = smem + C::kOffB;
-    uint8_t* sX = smem + C::kOffX;   // bf16 activation staging (fused quantisation)
     typename C::Slot* sf = reinterpret_cast<typename C::Slot*>(smem + C::kOffSf);
     typename C::Group* grp = reinterpret_cast<typename C::Group*>(smem + C::kOffGrp);
     Info<BN>* info = reinterpret_cast<Info<BN>*>(smem + C::kOffInfo);
@@ -475,46 +472,45 @@ __global__ void __launch_bounds__(
         ptx::launch_dependents();
     }
 
-    // Fused quantisation of stage s (job j), by the epilogue warps (nthr
-    // threads, this one tid): the bf16 tile [BN tokens x 128] in the staging
-    // buffer becomes E4M3 codes in the stage's B tile (the 128-byte swizzled
-    // layout the TMA would have written) and fp32 group scales in the slot's
-    // col_raw, 0 for groups past K or tokens past M (as the scale box would
-    // read them).  One thread per 8 elements; kBlkK/8 neighbouring lanes share
-    // a group (shuffle amax), as in the stand-alone quantisation kernel, so
-    // the codes and scales are the same.
-    auto quantize_stage = [&](int s, const JobIter& j, typename C::Slot& slot, int tid, int nthr) {
-        static_assert(!kFuse || (BN * 16) % (C::kQW * 32) == 0, "uniform trip count");
-        if constexpr (!kFuse) return;
+    // Fused quantisation, by the epilogue warps: vector v (8 consecutive
+    // elements; v = token * 16 + chunk) of stage s's bf16 activation tile,
+    // held in registers, becomes 8 E4M3 codes in the stage's B tile (the
+    // 128-byte swizzled layout the TMA would have written), and its group's
+    // fp32 scale goes to the slot's col_raw, 0 for groups past K or tokens past
+    // M (as the scale box would read them).  kBlkK/8 neighbouring lanes share a
+    // group (shuffle amax), as in the stand-alone quantisation kernel, so the
+    // codes and scales are the same.
+    constexpr int kVpt = kFuse ? BN * 16 / (C::kEpiWarps * 32) : 1;   // vectors per thread and stage
+    auto x_vec = [&](const JobIter& j, int v) -> uint4 {
+        const int tk = v >> 4, c = v & 15;
+        const int row = j.tc * BN + tk, k = j.kb * kBK + c * 8;
+        if (row >= a.M || k >= a.K) return make_uint4(0, 0, 0, 0);
+        return __ldg(reinterpret_cast<const uint4*>(fz.x + static_cast<int64_t>(row) * a.K + k));
+    };
+    auto quantize_vec = [&](const uint4& w, int v, int s, const JobIter& j, typename C::Slot& slot) {
         constexpr int kTpg = kBlkK / 8;
-        const uint8_t* xs = sX + s * C::kXBytes;
         uint8_t* bq = sB + s * C::kBBytes;
         const int col0 = j.tc * BN;
         const int kbase = j.kb * kBK;
         const bool ue = fz.ue8m0 != 0;
-        const bool out = fz.xq_out != nullptr && j.tr == 0;
-        const int lane_id = tid & 31;
-        for (int v = tid; v < BN * 16; v += nthr) {   // trip count uniform: nthr divides BN * 16
-            const int tk = v >> 4, c = v & 15;
-            const uint4 w = *reinterpret_cast<const uint4*>(xs + tk * 256 + c * 16);
-            float f[8];
-            qm::unpack8(w, f);
-            float amax = qm::amax8(f);
+        const int tk = v >> 4, c = v & 15;
+        float f[8];
+        qm::unpack8(w, f);
+        float amax = qm::amax8(f);
 #pragma unroll
-            for (int off = kTpg / 2; off > 0; off >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-            const float sc = qm::group_scale(amax, ue);
-            const uint2 q = qm::quantize8(f, sc, ue);
-            *reinterpret_cast<uint2*>(bq + tk * 128 + ((((c >> 1) ^ (tk & 7)) << 4) | ((c & 1) << 3))) = q;
-            const int gq = (c * 8) / kBlkK;               // scale column within the stage
-            const bool kin = kbase + gq * kBlkK < a.K;    // the group lies inside K
-            const bool tin = col0 + tk < a.M;
-            if ((lane_id % kTpg) == 0) slot.col_raw[tk][gq] = (kin && tin) ? sc : 0.0f;
-            if (out && kin && tin) {
-                const int64_t row = col0 + tk;
-                *reinterpret_cast<uint2*>(fz.xq_out + row * a.K + kbase + c * 8) = q;
-                if ((lane_id % kTpg) == 0) fz.xs_out[row * a.ks + j.kb * C::kScalesPerStage + gq] = sc;
-            }
+        for (int off = kTpg / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        const float sc = qm::group_scale(amax, ue);
+        const uint2 q = qm::quantize8(f, sc, ue);
+        *reinterpret_cast<uint2*>(bq + tk * 128 + ((((c >> 1) ^ (tk & 7)) << 4) | ((c & 1) << 3))) = q;
+        const int gq = (c * 8) / kBlkK;               // scale column within the stage
+        const bool kin = kbase + gq * kBlkK < a.K;    // the group lies inside K
+        const bool tin = col0 + tk < a.M;
+        const bool leader_lane = (v % kTpg) == 0;
+        if (leader_lane) slot.col_raw[tk][gq] = (kin && tin) ? sc : 0.0f;
+        if (fz.xq_out != nullptr && j.tr == 0 && kin && tin) {
+            const int64_t row = col0 + tk;
+            *reinterpret_cast<uint2*>(fz.xq_out + row * a.K + kbase + c * 8) = q;
+            if (leader_lane) fz.xs_out[row * a.ks + j.kb * C::kScalesPerStage + gq] = sc;
         }
     };
 
@@ -552,14 +548,7 @@ __global__ void __launch_bounds__(
                 load_tile(w_dst(s), tmW, j.kb * kBK, w_row(j), s);
             };
             auto load_x = [&](int s, const JobIter& j) {
-                if constexpr (kFuse) {
-                    // bf16 tile to the staging buffer, on its own barrier
-                    const uint32_t xb = sraw_bar(s);
-                    ptx::mbar_arrive_expect_tx_if(leader, xb, C::kXBytes);
-                    ptx::tma_load_2d_if(leader, ptx::smem_u32(sX) + s * C::kXBytes, tmX, j.kb * kBK, x_row(j), xb);
-                } else {
-                    load_tile(x_dst(s), tmX, j.kb * kBK, x_row(j), s);
-                }
+                if constexpr (!kFuse) load_tile(x_dst(s), tmX, j.kb * kBK, x_row(j), s);
             };
             // Scale group: at the first stage of every kG-stage group of an item,
             // one box per operand with the raw scales of the whole group.
@@ -588,6 +577,7 @@ __global__ void __launch_bounds__(
             int npre = 0;
             const int prefetch = a.prefetch >= 0 && a.prefetch < C::kPrefetch ? a.prefetch : C::kPrefetch;
             while (npre < prefetch && pre.valid(a)) {
+                if constexpr (kFuse) load_group(pre);   // weight scales only: static like the weights
                 load_w(npre, pre);
                 pre.next(a);
                 ++npre;
@@ -596,8 +586,10 @@ __global__ void __launch_bounds__(
             ptx::grid_dependency_wait();
             if (lane == 0) trace_ev(a, 1);
             for (int s = 0; s < npre && group_ok; ++s) {
-                load_group(it);
-                load_x(s, it);
+                if constexpr (!kFuse) {
+                    load_group(it);
+                    load_x(s, it);
+                }
                 it.next(a);
             }
             if (lane == 0) trace_ev(a, 3);
@@ -668,7 +660,7 @@ __global__ void __launch_bounds__(
         // is scale column gx; keeps the stage's raw scales in the slot when the
         // fp32 promotion step may need them.
         // Fused quantisation: the B-side (token) scales come from the slot, where
-        // quantize_stage left them.
+        // the epilogue warps left them.
         auto convert_g = [&](typename C::Slot& slot, const JobIter& j, const typename C::Group& g, int c0,
                              bool keep_raw) {
             const int row0 = kSwap ? j.tr * kBM : a_row0(j), col0 = j.tc * BN;
@@ -1240,6 +1232,7 @@ __global__ void __launch_bounds__(
         float acc[kCols];
         float acc1[kCols];             // second issuer's sum (two-issuer configurations)
         uint32_t qn = 0;               // fused quantisation: stages quantised so far
+        bool dep_done = false;         // ... and the wait for the preceding grid
         // Adds one accumulator segment of issuer m into `dst` (first: overwrite).
         auto consume = [&](int m, uint32_t sg, bool first, float (&dst)[kCols]) {
             const int b = static_cast<int>(sg % kAccBufs);
@@ -1276,28 +1269,48 @@ __global__ void __launch_bounds__(
         while (it.valid(a)) {
             bool failed = false;
             if constexpr (kFuse) {
-                // Quantise this item's activation tiles as they land, before
-                // waiting for its accumulators: warp group qg (kQW warps) takes
-                // the item's stages p with p % kQGroups == qg, in order.
-                const int qg = ew / C::kQW;
-                const int qt = (ew % C::kQW) * 32 + lane;
+                // Quantise this item's activation tiles before waiting for its
+                // accumulators: the loads of up to kBatch stages are issued
+                // first, then each stage is written once its ring slot is free.
+                constexpr int kBatch = 8 / kVpt;
+                if (!dep_done) {
+                    ptx::grid_dependency_wait();   // x may be the preceding kernel's output
+                    dep_done = true;
+                    if (epi_tid == 0) trace_ev(a, 4);
+                }
                 JobIter q = it;
-                for (int p = 0; p < it.nkb && !failed; ++p) {
-                    const uint32_t n = qn + static_cast<uint32_t>(p);
-                    if (p % C::kQGroups == qg) {
-                        const int s = static_cast<int>(n % kStages);
-                        const uint32_t ph = (n / kStages) & 1u;
-                        if (!wait_bar_warp(empty_bar(s), ph ^ 1u, sync, 4, false) ||
-                            !wait_bar_warp(sraw_bar(s), ph, sync, 4, false)) {
-                            failed = true;
-                            break;
-                        }
-                        quantize_stage(s, q, sf[s], qt, C::kQW * 32);
-                        ptx::fence_proxy_async_smem();   // codes: read by the MMA (async proxy)
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(qdone_bar(s));
+                for (int p0 = 0; p0 < it.nkb && !failed; p0 += kBatch) {
+                    uint4 xv[kBatch][kVpt];
+                    JobIter ql = q;
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b) {
+                        const bool live = p0 + b < it.nkb;
+#pragma unroll
+                        for (int i = 0; i < kVpt; ++i)
+                            xv[b][i] = live ? x_vec(ql, epi_tid + i * C::kEpiWarps * 32) : make_uint4(0, 0, 0, 0);
+                        if (live && p0 + b + 1 < it.nkb) ql.next(a);
                     }
-                    q.next(a);
+                    // each stage is released as soon as it is written: the MMAs
+                    // start on the first one (measured faster than one release
+                    // per batch)
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b) {
+                        if (p0 + b < it.nkb && !failed) {
+                            const uint32_t n = qn + static_cast<uint32_t>(p0 + b);
+                            const int s = static_cast<int>(n % kStages);
+                            if (!wait_bar_warp(empty_bar(s), ((n / kStages) & 1u) ^ 1u, sync, 4, false)) {
+                                failed = true;
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < kVpt; ++i)
+                                    quantize_vec(xv[b][i], epi_tid + i * C::kEpiWarps * 32, s, q, sf[s]);
+                                ptx::fence_proxy_async_smem();   // codes: read by the MMA (async proxy)
+                                __syncwarp();
+                                if (lane == 0) ptx::mbar_arrive(qdone_bar(s));
+                                if (p0 + b + 1 < it.nkb) q.next(a);
+                            }
+                        }
+                    }
                 }
                 qn += static_cast<uint32_t>(it.nkb);
             }
@@ -1560,12 +1573,11 @@ template <int kBlkN, int kBlkK, bool kScaleTma>
 sgq_status dispatch_tile(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const FuseArgs& fz, int grid,
                          cudaStream_t st) {
     if (v.fuse) {
-        // the bf16 staging buffer takes the place of one to three ring stages
         if constexpr (kScaleTma) {
             switch (v.bn) {
                 case 16: return run<16, 8, true, 2, kBlkN, kBlkK, true, false, false, true>(maps, a, fz, grid, st);
-                case 32: return run<32, 7, true, 2, kBlkN, kBlkK, true, false, false, true>(maps, a, fz, grid, st);
-                default: return run<64, 5, true, 2, kBlkN, kBlkK, true, false, false, true>(maps, a, fz, grid, st);
+                case 32: return run<32, 8, true, 2, kBlkN, kBlkK, true, false, false, true>(maps, a, fz, grid, st);
+                default: return run<64, 8, true, 2, kBlkN, kBlkK, true, false, false, true>(maps, a, fz, grid, st);
             }
         } else {
             return SGQ_ERR_UNSUPPORTED;

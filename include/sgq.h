@@ -192,12 +192,14 @@ sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const voi
  * sgq_quant_token_group followed by sgq_fp8_block_gemm.
  *
  * No counterpart in the pages as one call; it fuses the two steps above.  For
- * decode-sized M (M <= 64) with K/blk_k a multiple of 4 and at least 8 (blk_k
- * = 128) or 16 (blk_k = 32) -- every decode shape the pages use -- it is ONE
- * kernel: the GEMM's scale warps quantise each bf16 activation tile in
- * shared memory, so the codes never go through HBM and a launch disappears.
- * Any other shape runs the two kernels back to back and then needs xq/xs as
- * scratch; without them it returns SGQ_ERR_UNSUPPORTED before launching.
+ * decode-sized M with K/blk_k a multiple of 4 and at least 8 (blk_k = 128) or
+ * 16 (blk_k = 32) -- every decode shape the pages use -- it is ONE kernel
+ * when M <= 32, or when M <= 64 and xq/xs are NULL: the GEMM's epilogue warps
+ * quantise each bf16 activation tile into shared memory, so the codes never
+ * go through HBM and a launch disappears.  Any other shape (and 32 < M <= 64
+ * with xq/xs given, where the pair is faster) runs the two kernels back to
+ * back with xq/xs as scratch; without them it returns SGQ_ERR_UNSUPPORTED
+ * before launching.
  * Errors and the launch-overlap contract: as for sgq_fp8_block_gemm (x is
  * read only after the preceding kernel has finished).
  */

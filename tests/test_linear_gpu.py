@@ -1,7 +1,7 @@
 """Quantise-and-multiply (sgq_fp8_block_linear) on the GPU.
 
-At decode-sized M it is one kernel whose scale warps quantise the bf16
-activation tiles in shared memory.  Its codes and scales must equal the
+At decode-sized M it is one kernel whose epilogue warps quantise the bf16
+activation tiles into shared memory.  Its codes and scales must equal the
 stand-alone quantisation kernel's (and the oracle's) bit for bit, and its D
 must equal the two-call path's (quantisation kernel, then the GEMM) bit for
 bit, since the MMAs see the same operands in the same order.  D is also
@@ -44,7 +44,7 @@ def make(M, N, K, bn, bk, ue, seed):
     return x, wq, ws
 
 
-@pytest.mark.parametrize("M", [1, 4, 16, 33, 64])
+@pytest.mark.parametrize("M", [1, 4, 16, 32, 33, 64])
 @pytest.mark.parametrize("bn,bk", RECIPES)
 @pytest.mark.parametrize("ue", [True, False])
 def test_fused_matches_two_calls_and_oracle(M, bn, bk, ue):
@@ -57,6 +57,9 @@ def test_fused_matches_two_calls_and_oracle(M, bn, bk, ue):
     assert torch.equal(xq1, xq2)
     assert torch.equal(xs1, xs2)
     assert torch.equal(d1, d2)
+    # without the xq/xs outputs every M <= 64 runs as one kernel
+    d0, _, _ = fused(xd, wqd, wsd, bn, bk, ue, outputs=False)
+    assert torch.equal(d0, d2)
     aq, a_s = oracle.quant_token_group(x, bk, ue)
     assert np.array_equal(xq1.cpu().numpy(), aq)
     assert np.array_equal(xs1.cpu().numpy(), a_s)
