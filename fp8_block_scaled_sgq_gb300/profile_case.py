@@ -1,11 +1,13 @@
 """Runs one quantise + GEMM case of a workload a few times, for profilers.
 
-    python -m fp8_block_scaled_sgq_gb300.profile_case WORKLOAD [INDEX] [--iters N]
+    python -m fp8_block_scaled_sgq_gb300.profile_case WORKLOAD [INDEX] [--iters N] [--fused]
 
 WORKLOAD/INDEX pick a case from ``synth.WORKLOADS`` (e.g. ``decode_block32 2``
 is M=16, N=7168, K=2048 with [32,32] blocks).  Each iteration launches the
 activation quantisation kernel, then the block-scaled GEMM, on one stream.
-The weight is quantised once up front (one extra launch).  The run ends with
+With --fused each iteration is one sgq_fp8_block_linear call instead (one
+kernel at decode-sized M).  The weight is quantised once up front (one extra
+launch).  The run ends with
 the device status word checked and one line of wall-clock timing, which is
 not a benchmark number (use bench.py for those).
 """
@@ -25,6 +27,7 @@ def main() -> None:
     ap.add_argument("workload", choices=sorted(synth.WORKLOADS))
     ap.add_argument("index", type=int, nargs="?", default=0)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--fused", action="store_true")
     args = ap.parse_args()
     c = synth.WORKLOADS[args.workload][args.index]
     dev = torch.device("cuda:0")
@@ -43,14 +46,17 @@ def main() -> None:
     binding.sgq_quant_weight_block(w, N, K, c.blk_n, c.blk_k, int(c.ue8m0), wq, ws, s)
     t0 = time.perf_counter()
     for _ in range(args.iters):
-        binding.sgq_quant_token_group(x, M, K, c.group, int(c.ue8m0), xq, xs, s)
-        binding.sgq_fp8_block_gemm(xq, xs, wq, ws, d, M, N, K, c.blk_n, c.blk_k, s)
+        if args.fused:
+            binding.sgq_fp8_block_linear(x, int(c.ue8m0), wq, ws, d, M, N, K, c.blk_n, c.blk_k, None, None, s)
+        else:
+            binding.sgq_quant_token_group(x, M, K, c.group, int(c.ue8m0), xq, xs, s)
+            binding.sgq_fp8_block_gemm(xq, xs, wq, ws, d, M, N, K, c.blk_n, c.blk_k, s)
     st.synchronize()
     wall = time.perf_counter() - t0
     status = binding.sgq_device_status(s)
     if status != 0:
         raise RuntimeError(f"device status {binding.status_string(status)}")
-    print(json.dumps({"case": c.name, "M": M, "N": N, "K": K, "blk": [c.blk_n, c.blk_k],
+    print(json.dumps({"case": c.name, "fused": args.fused, "M": M, "N": N, "K": K, "blk": [c.blk_n, c.blk_k],
                       "iters": args.iters, "wall_ms": round(wall * 1e3, 3)}))
 
 
