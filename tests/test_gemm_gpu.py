@@ -168,7 +168,8 @@ def test_m_zero_is_noop():
 
 
 ISSUE = [(300, 520, 1024, 128, 128), (129, 136, 384, 128, 128), (200, 520, 2080, 32, 32),
-         (257, 1032, 4128, 128, 32), (1000, 264, 8192, 32, 128)]
+         (257, 1032, 4128, 128, 32), (1000, 264, 8192, 32, 128), (300, 520, 2048, 32, 32),
+         (257, 1032, 4096, 128, 32)]
 
 
 @pytest.mark.parametrize("M,N,K,bn,bk", ISSUE)
