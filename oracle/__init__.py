@@ -15,6 +15,10 @@ builds it with gcc on first use and wraps it with numpy arrays:
 * ``gemm`` -- D = mm(As*Aq, (Ws*Wq)^T) in fp64 (vLLM scaled_mm page,
   AiterInt8ScaledMMLinearKernel.apply_weights docstring) plus the bound
   sum_k |a_deq||w_deq| used by the error criterion.
+* ``quant_per_token`` / ``quant_per_tensor`` / ``scaled_mm`` -- the
+  per-token and per-tensor quantisers and fp8_scaled_mm (per-tensor or per-row
+  A scales, per-tensor or per-column B scales, optional bias) of "Sgl project
+  Sglang GEMM Interface", Quantization Routines and Signature.
 """
 from __future__ import annotations
 
@@ -77,6 +81,12 @@ def _load():
         lib.sgqo_quant_weight_block.restype = None
         lib.sgqo_gemm.argtypes = [P, P, P, P, i64, i64, i64, ci, ci, ci, P, P]
         lib.sgqo_gemm.restype = None
+        lib.sgqo_quant_per_token.argtypes = [P, i64, i64, cf, P, P]
+        lib.sgqo_quant_per_token.restype = None
+        lib.sgqo_quant_per_tensor.argtypes = [P, i64, ci, cf, P, P]
+        lib.sgqo_quant_per_tensor.restype = None
+        lib.sgqo_scaled_mm.argtypes = [P, P, i64, P, P, i64, P, i64, i64, i64, P, P]
+        lib.sgqo_scaled_mm.restype = None
         lib.sgqo_num_threads.argtypes = []
         lib.sgqo_num_threads.restype = ci
         _lib = lib
@@ -169,4 +179,44 @@ def gemm(aq, a_s, wq, ws, blk_n: int, blk_k: int, a_group: int | None = None,
     b = np.empty((M, N), dtype=np.float64) if with_bound else None
     _load().sgqo_gemm(_ptr(aq), _ptr(a_s), _ptr(wq), _ptr(ws), M, N, K, a_group,
                       blk_n, blk_k, _ptr(d), _ptr(b) if b is not None else None)
+    return (d, b) if with_bound else d
+
+
+def quant_per_token(x, eps: float = EPS):
+    """x: bf16 [M, K] -> (codes uint8 [M, K], scales fp32 [M]), one scale per row."""
+    xb = _as_bf16_bits(x)
+    M, K = xb.shape
+    xq = np.empty((M, K), dtype=np.uint8)
+    xs = np.empty((M,), dtype=np.float32)
+    _load().sgqo_quant_per_token(_ptr(xb), M, K, eps, _ptr(xq), _ptr(xs))
+    return xq, xs
+
+
+def quant_per_tensor(x, scale=None, eps: float = EPS):
+    """x: bf16 [...] -> (codes uint8 [...], scale fp32 [1]).  scale=None:
+    dynamic (amax over the tensor); else the given static scale."""
+    xb = _as_bf16_bits(x)
+    xq = np.empty(xb.shape, dtype=np.uint8)
+    s = np.array([0.0 if scale is None else scale], dtype=np.float32)
+    _load().sgqo_quant_per_tensor(_ptr(xb), xb.size, 0 if scale is None else 1, eps, _ptr(xq), _ptr(s))
+    return xq, s
+
+
+def scaled_mm(aq, sa, wq, sb, bias=None, with_bound: bool = True):
+    """fp64 D [M, N] = (Aq Wq^T) * sa * sb + bias (sa: 1 or M values, sb: 1 or N,
+    bias: bf16 [N] or None), and the bound [M, N]."""
+    aq = np.ascontiguousarray(aq, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32).reshape(-1)
+    sb = np.ascontiguousarray(sb, dtype=np.float32).reshape(-1)
+    M, K = aq.shape
+    N = wq.shape[0]
+    if sa.size not in (1, M) or sb.size not in (1, N):
+        raise ValueError("sa must have 1 or M values, sb 1 or N")
+    bb = None if bias is None else _as_bf16_bits(bias).reshape(-1)
+    d = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64) if with_bound else None
+    _load().sgqo_scaled_mm(_ptr(aq), _ptr(sa), sa.size, _ptr(wq), _ptr(sb), sb.size,
+                           _ptr(bb) if bb is not None else None, M, N, K, _ptr(d),
+                           _ptr(b) if b is not None else None)
     return (d, b) if with_bound else d

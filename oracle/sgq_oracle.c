@@ -21,6 +21,11 @@
  *    [128,128] blocks), and the vLLM "scaled_mm" API page,
  *    XPUFp8BlockScaledMMKernel.process_weights_after_loading ("[n_blocks,
  *    k_blocks] (one value per block tile)").
+ *  - Per-token and per-tensor quantisation (sgl_per_token_quant_fp8,
+ *    sgl_per_tensor_quant_fp8 with static or dynamic scaling: "Sgl project
+ *    Sglang GEMM Interface", Quantization Routines and Signature) and the
+ *    scaled GEMM fp8_scaled_mm (same page: per-tensor or per-row scale_a,
+ *    per-tensor or per-column scale_b, optional bias, output dtype).
  *  - The GEMM: the vLLM "scaled_mm" API page,
  *    AiterInt8ScaledMMLinearKernel.apply_weights docstring: the output is
  *    mm(scale_a * a, scale_b * b) with numpy-style broadcasting of the scales,
@@ -238,4 +243,71 @@ void sgqo_gemm(const uint8_t* aq, const float* as, const uint8_t* wq, const floa
         free(wrow);
     }
     free(adeq);
+}
+
+/*
+ * Per-token quantisation (sgl_per_token_quant_fp8): one scale per row, the
+ * group rule above with the group spanning the whole row.  The routine has no
+ * UE8M0 option.  x: bf16 bits [M, K]; xq: [M, K]; xs: fp32 [M].
+ */
+void sgqo_quant_per_token(const uint16_t* x, int64_t M, int64_t K, float eps, uint8_t* xq, float* xs) {
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t* xr = x + m * K;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(sgqo_bf16_to_f32(xr[k]));
+            if (a > amax) amax = a;
+        }
+        float s = sgqo_group_scale(amax, eps, 0);
+        xs[m] = s;
+        for (int64_t k = 0; k < K; ++k) xq[m * K + k] = orc_quant_one(sgqo_bf16_to_f32(xr[k]), s);
+    }
+}
+
+/*
+ * Per-tensor quantisation (sgl_per_tensor_quant_fp8).  Dynamic (is_static =
+ * 0): one scale max(amax over all n elements, eps) / 448, written to *s.
+ * Static: *s is the caller's scale and only the codes are produced.
+ */
+void sgqo_quant_per_tensor(const uint16_t* x, int64_t n, int is_static, float eps, uint8_t* xq, float* s) {
+    if (!is_static) {
+        float amax = 0.0f;
+        for (int64_t i = 0; i < n; ++i) {
+            float a = fabsf(sgqo_bf16_to_f32(x[i]));
+            if (a > amax) amax = a;
+        }
+        *s = sgqo_group_scale(amax, eps, 0);
+    }
+    float sc = *s;
+    for (int64_t i = 0; i < n; ++i) xq[i] = orc_quant_one(sgqo_bf16_to_f32(x[i]), sc);
+}
+
+/*
+ * Scaled GEMM (fp8_scaled_mm), B given as [N, K]:
+ *   D[m, n] = (sum_k dec(Aq[m,k]) * dec(Wq[n,k])) * sa[m or 0] * sb[n or 0] + bias[n]
+ * in fp64 (the scales broadcast numpy-style: sa has 1 or M values, sb 1 or N;
+ * bias: bf16 bits [N] or NULL), and bound[m, n] = sum_k |a_deq| |w_deq| with the
+ * scales applied.  Outputs [M, N] row-major fp64; bound may be NULL.
+ */
+void sgqo_scaled_mm(const uint8_t* aq, const float* sa, int64_t sa_n, const uint8_t* wq, const float* sb,
+                    int64_t sb_n, const uint16_t* bias, int64_t M, int64_t N, int64_t K, double* d,
+                    double* bound) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        const double bn = sb[sb_n == 1 ? 0 : n];
+        const double bias_n = bias ? (double)sgqo_bf16_to_f32(bias[n]) : 0.0;
+        for (int64_t m = 0; m < M; ++m) {
+            const double am = sa[sa_n == 1 ? 0 : m];
+            double acc = 0.0, b = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double av = sgqo_e4m3_decode(aq[m * K + k]), wv = sgqo_e4m3_decode(wq[n * K + k]);
+                acc += av * wv;
+                b += fabs(av) * fabs(wv);
+            }
+            d[m * N + n] = acc * am * bn + bias_n;
+            if (bound) bound[m * N + n] = b * fabs(am * bn);
+        }
+    }
 }

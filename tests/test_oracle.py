@@ -330,3 +330,99 @@ def test_gemm_block_index_mapping():
         for n in range(N):
             want = sum(32 * a_s[m, kb] * ws[n // bn, kb] for kb in range(4))
             assert d[m, n] == want
+
+
+# ---------------------------------------------------------------- per-token / per-tensor / fp8_scaled_mm
+# ("Sgl project Sglang GEMM Interface": sgl_per_token_quant_fp8, sgl_per_tensor_quant_fp8, fp8_scaled_mm)
+
+def _rand_bf16(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def test_per_token_is_group_quant_over_the_whole_row():
+    x = _rand_bf16((7, 96), 1)
+    x[3] = 0.0                                     # an all-zero row: eps scale, zero codes
+    q, s = oracle.quant_per_token(x)
+    qg, sg = oracle.quant_token_group(x, 96, False)
+    assert np.array_equal(q, qg) and np.array_equal(s, sg[:, 0])
+    xf = x.float().numpy()
+    amax = np.abs(xf).max(axis=1).astype(np.float32)
+    want = np.maximum(amax, np.float32(oracle.EPS)) / np.float32(448.0)   # one fp32 division
+    assert np.array_equal(f32_bits(s), f32_bits(want))
+    assert not q[3].any()
+
+
+def test_per_token_rows_are_independent():
+    x = _rand_bf16((5, 64), 2)
+    q, s = oracle.quant_per_token(x)
+    x2 = x.clone()
+    x2[1] *= 8                                     # changes only row 1
+    q2, s2 = oracle.quant_per_token(x2)
+    keep = [0, 2, 3, 4]
+    assert np.array_equal(q[keep], q2[keep]) and np.array_equal(s[keep], s2[keep])
+    assert np.array_equal(q[1], q2[1]) and s2[1] == np.float32(8) * s[1]   # exact power-of-two rescale
+
+
+def test_per_tensor_dynamic_is_one_group_over_everything():
+    x = _rand_bf16((6, 32), 3)
+    q, s = oracle.quant_per_tensor(x)
+    flat = x.reshape(1, -1)
+    qg, sg = oracle.quant_token_group(flat, flat.shape[1], False)
+    assert np.array_equal(q.reshape(1, -1), qg) and s[0] == sg[0, 0]
+
+
+def test_per_tensor_static_uses_the_given_scale():
+    x = _rand_bf16((4, 48), 4, scale=3.0)
+    s = np.float32(0.0213)
+    q, s_out = oracle.quant_per_tensor(x, scale=float(s))
+    assert s_out[0] == s
+    xf = x.float().numpy()
+    want = oracle.e4m3_encode(np.clip(xf / s, -448.0, 448.0).astype(np.float32))   # fp32 division, clip, RNE
+    assert np.array_equal(q, want)
+    # lossless on an E4M3 grid with a power-of-two scale
+    codes = np.arange(0, 0x7F, dtype=np.uint8)
+    grid = oracle.e4m3_decode(codes) * 0.25
+    xb = torch.tensor(grid, dtype=torch.float32).to(torch.bfloat16)
+    assert np.array_equal(xb.float().numpy(), grid.astype(np.float32))   # representable in bf16
+    q2, _ = oracle.quant_per_tensor(xb.reshape(1, -1), scale=0.25)
+    assert np.array_equal(oracle.e4m3_decode(q2.reshape(-1)) * 0.25, grid)
+
+
+@pytest.mark.parametrize("per_row,per_col,with_bias", [(True, True, True), (False, False, False),
+                                                       (True, False, True), (False, True, False)])
+def test_scaled_mm_brute_force(per_row, per_col, with_bias):
+    rng = np.random.default_rng(7)
+    M, N, K = 3, 5, 8                              # M != N: a swapped scale vector fails
+    aq = rng.integers(0, 256, size=(M, K), dtype=np.uint8)
+    wq = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+    aq[(aq & 0x7F) == 0x7F] = 0x10                 # no NaN codes
+    wq[(wq & 0x7F) == 0x7F] = 0x22
+    sa = rng.uniform(0.5, 2.0, size=M if per_row else 1).astype(np.float32)
+    sb = rng.uniform(0.5, 2.0, size=N if per_col else 1).astype(np.float32)
+    bias = torch.tensor(rng.uniform(-3, 3, size=N), dtype=torch.float32).to(torch.bfloat16) if with_bias else None
+    d, b = oracle.scaled_mm(aq, sa, wq, sb, bias)
+    dec = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    for m in range(M):
+        for n in range(N):
+            acc = sum(float(dec[aq[m, k]]) * float(dec[wq[n, k]]) for k in range(K))
+            ref = acc * float(sa[m if per_row else 0]) * float(sb[n if per_col else 0])
+            if with_bias:
+                ref += float(bias[n].float())
+            assert d[m, n] == pytest.approx(ref, rel=1e-13, abs=1e-13)
+            bb = sum(abs(float(dec[aq[m, k]])) * abs(float(dec[wq[n, k]])) for k in range(K))
+            assert b[m, n] == pytest.approx(bb * abs(float(sa[m if per_row else 0]) * float(sb[n if per_col else 0])),
+                                            rel=1e-13)
+
+
+def test_scaled_mm_per_tensor_equals_block_gemm_with_constant_scales():
+    x = _rand_bf16((4, 64), 8)
+    w = _rand_bf16((6, 64), 9, scale=0.02)
+    aq, sa = oracle.quant_per_tensor(x)
+    wq, sb = oracle.quant_per_tensor(w)
+    d, _ = oracle.scaled_mm(aq, sa, wq, sb)
+    d2, _ = oracle.gemm(aq, np.full((4, 2), sa[0], np.float32), wq, np.full((1, 2), sb[0], np.float32), 32, 32)
+    assert np.allclose(d, d2, rtol=1e-12, atol=0)
+    bias = _rand_bf16((6,), 10)
+    db, _ = oracle.scaled_mm(aq, sa, wq, sb, bias)
+    assert np.allclose(db - d, np.broadcast_to(bias.float().numpy().astype(np.float64), d.shape), rtol=0, atol=1e-12)
