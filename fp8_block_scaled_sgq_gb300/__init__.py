@@ -10,7 +10,8 @@ from __future__ import annotations
 from .binding import (  # noqa: F401
     EXPORTS, SGQ_GEMM_DEFAULT, SGQ_GEMM_FORCE_PROMOTE, SGQ_GEMM_ISSUE_ALT, SGQ_GEMM_ISSUE_SINGLE, SgqError,
     load_library, sgq_device_status,
-    sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_fp8_block_linear, sgq_launch_count, sgq_quant_token_group,
+    sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_fp8_block_linear, sgq_fp8_scaled_mm,
+    sgq_quant_per_tensor, sgq_quant_per_token, sgq_launch_count, sgq_quant_token_group,
     sgq_quant_weight_block, sgq_version, status_string)
 
 
@@ -68,4 +69,36 @@ def fp8_block_linear(x, wq, ws, blk_n: int, blk_k: int, ue8m0: bool, out=None, x
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
         xs = torch.empty((M, K // blk_k), dtype=torch.float32, device=x.device)
         sgq_fp8_block_linear(x, ue8m0, wq, ws, out, M, N, K, blk_n, blk_k, xq, xs, stream)
+    return out
+
+
+def quant_per_token(x, stream=None):
+    """bf16 [M, K] CUDA tensor -> (E4M3 codes [M, K], fp32 scales [M])."""
+    import torch
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    sgq_quant_per_token(x, M, K, xq, xs, stream)
+    return xq, xs
+
+
+def quant_per_tensor(x, scale=None, stream=None):
+    """bf16 CUDA tensor -> (E4M3 codes, fp32 scale [1]); scale=None: dynamic."""
+    import torch
+    xq = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    xs = torch.empty((4,), dtype=torch.float32, device=x.device)   # 16-byte aligned; [0] is the scale
+    if scale is not None:
+        xs[0] = float(scale)
+    sgq_quant_per_tensor(x, x.numel(), scale is not None, xq, xs, stream)
+    return xq, xs[:1]
+
+
+def fp8_scaled_mm(aq, sa, wq, sb, bias=None, out=None, stream=None):
+    """D = bf16((Aq Wq^T) * sa * sb + bias): sa of 1 or M values, sb of 1 or N."""
+    import torch
+    M, K = aq.shape
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    sgq_fp8_scaled_mm(aq, sa, sa.numel(), wq, sb, sb.numel(), bias, out, M, N, K, stream)
     return out

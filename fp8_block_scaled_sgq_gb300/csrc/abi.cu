@@ -113,6 +113,39 @@ sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const voi
                                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+sgq_status sgq_quant_per_token(const void* x, int64_t M, int64_t K, void* xq, float* xs, sgq_stream_t stream) {
+    if (M < 0 || K <= 0 || K % 16 != 0 || M >= (int64_t(1) << 31) || M * K > (int64_t(1) << 40))
+        return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!x || !xq || !xs) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(xs)) return SGQ_ERR_MISALIGNED;
+    return sgq::launch_quant_per_token(x, M, K, xq, xs, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgq_status sgq_quant_per_tensor(const void* x, int64_t n, int is_static, void* xq, float* xs, sgq_stream_t stream) {
+    if (n < 0 || n % 16 != 0 || n > (int64_t(1) << 40) || (is_static != 0 && is_static != 1))
+        return SGQ_ERR_INVALID_ARG;
+    if (n == 0) return SGQ_OK;
+    if (!x || !xq || !xs) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(xs)) return SGQ_ERR_MISALIGNED;
+    return sgq::launch_quant_per_tensor(x, n, is_static, xq, xs, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgq_status sgq_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, const void* Wq, const float* sb,
+                             int64_t sb_n, const void* bias, void* D, int64_t M, int64_t N, int64_t K,
+                             sgq_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || K % 32 != 0 || N % 8 != 0) return SGQ_ERR_INVALID_ARG;
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return SGQ_ERR_INVALID_ARG;
+    if ((sa_n != 1 && sa_n != M) || (sb_n != 1 && sb_n != N)) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!Aq || !sa || !Wq || !sb || !D) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(Aq) || !aligned16(sa) || !aligned16(Wq) || !aligned16(sb) || !aligned16(D) ||
+        (bias && !aligned16(bias)))
+        return SGQ_ERR_MISALIGNED;
+    return sgq::launch_fp8_scaled_mm(Aq, sa, sa_n, Wq, sb, sb_n, bias, D, M, N, K,
+                                     reinterpret_cast<cudaStream_t>(stream));
+}
+
 sgq_status sgq_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const float* Ws, void* D, int64_t M,
                                 int64_t N, int64_t K, int blk_n, int blk_k, void* xq, float* xs,
                                 sgq_stream_t stream) {

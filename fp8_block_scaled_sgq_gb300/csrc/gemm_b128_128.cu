@@ -4,7 +4,7 @@
 
 namespace sgq {
 namespace gemm {
-sgq_status dispatch_128_128(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const FuseArgs& fz, int grid,
+sgq_status dispatch_128_128(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const ExtArgs& fz, int grid,
                            cudaStream_t st) {
     return dispatch<128, 128>(v, maps, a, fz, grid, st);
 }

@@ -239,6 +239,15 @@ struct Fuse {
     float* xs;
 };
 
+// Per-channel scaling request (fp8_scaled_mm).
+struct Chan {
+    const float* sa;
+    int64_t sa_n;
+    const float* sb;
+    int64_t sb_n;
+    const void* bias;
+};
+
 // Plans and launches one GEMM.  noalloc: split-K scratch from the fixed array
 // (its counters cleared by an asynchronous memset), else the per-device
 // workspace.  fuse (Aq/As unused): the activations are quantised inside the
@@ -246,7 +255,7 @@ struct Fuse {
 // SGQ_ERR_UNSUPPORTED is returned before anything is launched.
 sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D, int64_t M,
                   int64_t N, int64_t K, int blk_n, int blk_k, uint32_t flags, bool noalloc, const Fuse* fuse,
-                  cudaStream_t st) {
+                  cudaStream_t st, const Chan* chan = nullptr) {
     if (get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
     DeviceInfo di;
     sgq_status rc = device_info(&di);
@@ -255,6 +264,10 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     Plan p = make_plan(M, N, K, blk_k, di.sm_count);
     if (flags & SGQ_GEMM_ISSUE_ALT) p.alt = !p.swap && !p.pair;
     if (flags & SGQ_GEMM_ISSUE_SINGLE) p.alt = false;
+    if (chan) {   // plain tiles: no scale boxes, one issuer
+        p.alt = false;
+        p.pair = false;
+    }
     const int64_t ks_all = K / blk_k;
     const bool scale_tma_ok = (ks_all % 4) == 0 && ks_all >= (blk_k == 128 ? 8 : 16);
     if (fuse && !(p.swap && scale_tma_ok)) return SGQ_ERR_UNSUPPORTED;
@@ -278,7 +291,14 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     static const int prefetch = env_int("SGQ_PREFETCH", -1);
     a.prefetch = prefetch;
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
-    FuseArgs fz{};
+    ExtArgs fz{};
+    if (chan) {
+        fz.sa = chan->sa;
+        fz.sb = chan->sb;
+        fz.sa_n = static_cast<int>(chan->sa_n);
+        fz.sb_n = static_cast<int>(chan->sb_n);
+        fz.bias = static_cast<const uint16_t*>(chan->bias);
+    }
     if (fuse) {
         fz.x = static_cast<const uint16_t*>(fuse->x);
         fz.ue8m0 = fuse->ue8m0;
@@ -331,7 +351,7 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     // than the matrix's rows is not used.
     static const int scale_tma_on = env_int("SGQ_SCALE_TMA", 1);
     const int gcols = blk_k == 128 ? 8 : 16;
-    const bool scale_tma = (scale_tma_on != 0 || fuse) && (a.ks % 4) == 0 && a.ks >= gcols;
+    const bool scale_tma = !chan && (scale_tma_on != 0 || fuse) && (a.ks % 4) == 0 && a.ks >= gcols;
     maps[2] = maps[0];
     maps[3] = maps[1];
     if (scale_tma) {
@@ -343,7 +363,8 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
                                      p.swap ? p.bn : p.bn / blk_n, gcols) != SGQ_OK))
             return SGQ_ERR_CUDA;
     }
-    const Variant v{p.swap, p.pair, p.alt, scale_tma, fuse != nullptr, p.bn};
+    const Variant v{p.swap, p.pair, p.alt, scale_tma, fuse != nullptr, chan != nullptr, p.bn};
+    if (chan) return dispatch_chan(v, maps, a, fz, p.grid, st);
     if (blk_n == 32 && blk_k == 32) return dispatch_32_32(v, maps, a, fz, p.grid, st);
     if (blk_n == 32 && blk_k == 128) return dispatch_32_128(v, maps, a, fz, p.grid, st);
     if (blk_n == 128 && blk_k == 32) return dispatch_128_32(v, maps, a, fz, p.grid, st);
@@ -364,6 +385,15 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
                                          void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
                                          cudaStream_t st) {
     return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, true, nullptr, st);
+}
+
+// fp8_scaled_mm: D = (Aq Wq^T) * sa * sb + bias.  The plan is the block GEMM's
+// for blk_k = 128 (the scale arguments of the block path stay unused).
+sgq_status launch_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, const void* Wq, const float* sb,
+                                int64_t sb_n, const void* bias, void* D, int64_t M, int64_t N, int64_t K,
+                                cudaStream_t st) {
+    const gemm::Chan c{sa, sa_n, sb, sb_n, bias};
+    return gemm::launch(Aq, nullptr, Wq, nullptr, D, M, N, K, 128, 128, SGQ_GEMM_DEFAULT, false, nullptr, st, &c);
 }
 
 // Quantise-and-multiply.  Decode-sized M (swap-AB plans with TMA-loadable

@@ -107,15 +107,23 @@ struct GemmArgs {
     int prefetch;         // < 0: the configuration's weight prefetch depth; else at most this many stages
 };
 
-// Fused quantisation only: the bf16 activations, UE8M0 rounding of the
-// activation scales, and optional outputs for the codes [M, K] and scales [M, K/blk_k] (written by the
-// CTAs of the first weight tile row; null: not written).  A parameter of its
-// own: growing GemmArgs costs the other configurations registers.
-struct FuseArgs {
+// Arguments only some configurations read, in a parameter of their own
+// (growing GemmArgs costs the other configurations registers).
+//  - Fused quantisation: the bf16 activations, UE8M0 rounding of the
+//    activation scales, and optional outputs for the codes [M, K] and scales
+//    [M, K/blk_k] (written by the CTAs of the first weight tile row; null: not
+//    written).
+//  - Per-channel scaling (fp8_scaled_mm): A scales (1 or M values), B scales
+//    (1 or N values) and an optional bf16 bias [N].
+struct ExtArgs {
     const uint16_t* x;   // bf16 activations [M, K]
     uint8_t* xq_out;
     float* xs_out;
     int ue8m0;
+    const float* sa;
+    const float* sb;
+    const uint16_t* bias;
+    int sa_n, sb_n;
 };
 
 // Walks the (item, k-stage) jobs of one CTA (or CTA pair) in order.
@@ -266,7 +274,7 @@ __device__ __forceinline__ uint32_t sf_word(const float* row, int kcol, uint32_t
 }
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair,
-          bool kAlt, bool kFuse>
+          bool kAlt, bool kFuse, bool kChan>
 struct Cfg {
     // Swap-AB tiles are narrow (N <= 64): an MMA costs about as much to issue
     // as a full-width one, so two warps issue alternate K stages of each item
@@ -351,6 +359,7 @@ struct Cfg {
     static_assert(kAccSets * kAccBufs * BN <= int(kSfCol) - 32 * (kMmaWarps - 1), "TMEM budget");
     static_assert(!kAlt || (!kSwap && !kPair), "alternating issuers: single-CTA wide tiles");
     static_assert(!kFuse || (kSwap && kScaleTma), "fused quantisation: swap-AB tiles with TMA scale groups");
+    static_assert(!kChan || (!kPair && !kAlt && !kFuse && !kScaleTma), "per-channel scaling: plain tiles");
     static_assert(kOffSf % 128 == 0, "scale slots aligned");
     static_assert(!kTwoPerSm || kSmem <= 113 * 1024, "two CTAs per SM: shared memory");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
@@ -365,14 +374,14 @@ struct Cfg {
 };
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair,
-          bool kAlt, bool kFuse>
+          bool kAlt, bool kFuse, bool kChan>
 __global__ void __launch_bounds__(
-    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>::kThreads),
-    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>::kMinBlocks))
+    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>::kThreads),
+    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>::kMinBlocks))
     fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                          const GemmArgs a, const FuseArgs fz) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>;
+                          const GemmArgs a, const ExtArgs fz) {
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>;
     constexpr int kCG = C::kCG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(
         for (int s = 0; s < kStages; ++s) {
             // producer expect_tx + scale loader (pair: the peer's scale loader
             // signals with a transfer counted in the expected bytes)
-            ptx::mbar_init(full_bar(s), 2);
+            ptx::mbar_init(full_bar(s), kChan ? 1 : 2);   // per-channel scaling: no scale warps
             ptx::mbar_init(empty_bar(s), 1);  // tcgen05.commit
         }
         for (int m = 0; m < kMW; ++m) {
@@ -608,7 +617,7 @@ __global__ void __launch_bounds__(
             }
         }
         __syncwarp();
-    } else if (warp == 2 || (C::kSfWarps > 1 && warp == C::kSf2Warp)) {
+    } else if (!kChan && (warp == 2 || (C::kSfWarps > 1 && warp == C::kSf2Warp))) {
         // ---------------------------------------------------------- scale loader
         // Turns each stage's raw fp32 scales into UE8M0 words in tcgen05.cp
         // order, checks the power-of-two property, and releases the stage to
@@ -1048,6 +1057,8 @@ __global__ void __launch_bounds__(
         ptx::tc_commit_local_g_if<1>(leader, drain_bar(static_cast<int>(mw)));
         if (lane == 0) wait_bar(drain_bar(static_cast<int>(mw)), 0, sync, 5);
         __syncwarp();
+    } else if (kChan && (warp == 2 || warp == C::kSf2Warp)) {
+        // per-channel scaling: no per-stage scales, so no scale warps
     } else if (warp == 1 || (kMW > 1 && warp == C::kMma2Warp)) {
         // ---------------------------------------------------------- MMA issuer
         // The whole warp runs this loop in lock-step; every tcgen05 instruction
@@ -1121,8 +1132,9 @@ __global__ void __launch_bounds__(
             const int nq = ragged_k ? min(4, (a.K - it.kb * kBK) / 32) : 4;
             const uint64_t ad0 = ad_base + static_cast<uint64_t>(stage * (C::kABytes >> 4));
             const uint64_t bd0 = bd_base + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
-            // pair: block-scaled only when the scales of both CTAs' stages are 2^e
-            const bool mx = slot.pow2 != 0u && !a.force_promote && (!kPair || slot.xfer[0] != 0u);
+            // pair: block-scaled only when the scales of both CTAs' stages are 2^e;
+            // per-channel scaling accumulates unscaled MMAs over the whole K range
+            const bool mx = kChan || (slot.pow2 != 0u && !a.force_promote && (!kPair || slot.xfer[0] != 0u));
             if (mx) {
                 if (!seg_open) {
                     if (!wait_bar<kPair>(acce_bar(mw, acc_buf(seg)), acc_par(seg) ^ 1u, sync, 2)) {
@@ -1135,12 +1147,16 @@ __global__ void __launch_bounds__(
                 }
                 const uint32_t sfs = sf_col0 + 16u * (mx_used & 1u);
                 const uint32_t t_sfa = tmem + sfs, t_sfb = tmem + sfs + 4u;
+                const uint32_t d = tmem + acc_col0 + static_cast<uint32_t>(acc_buf(seg) * BN);
+                if constexpr (kChan) {
+                    for (int j = 0; j < nq; ++j)
+                        ptx::mma_f8_g_if<kCG>(leader, d, ad0 + 2u * j, bd0 + 2u * j, idesc_f8, j == 0 ? acc_flag : 1u);
+                } else {
                 const uint64_t slot_off = static_cast<uint64_t>(stage) * kSlotStep;
                 ptx::tmem_cp_g_if<kCG>(leader, t_sfa, sfa_base + slot_off);
 #pragma unroll
                 for (int h = 0; h < C::kSfbCopies; ++h)
                     ptx::tmem_cp_g_if<kCG>(leader, t_sfb + 4u * h, sfb_base + slot_off + 32u * h);
-                const uint32_t d = tmem + acc_col0 + static_cast<uint32_t>(acc_buf(seg) * BN);
                 if (nq == 4) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -1154,6 +1170,7 @@ __global__ void __launch_bounds__(
                         ptx::mma_mxf8_g_if<kCG>(leader, d, ad0 + 2u * j, bd0 + 2u * j,
                                                 ptx::idesc_sf_ids(idesc_mx, j, j), t_sfa, t_sfb,
                                                 j == 0 ? acc_flag : 1u);
+                }
                 }
                 acc_flag = 1;
                 ++mx_used;
@@ -1459,6 +1476,22 @@ __global__ void __launch_bounds__(
                 }
                 if (store && epi_tid == 0) a.counters[it.tile] = 0u;   // ready for the next launch
             }
+            if constexpr (kChan) {
+                // D = acc * sa * sb + bias: the MMA rows are tokens (weights when swapped)
+                if (store && grow < a.rows) {
+                    const float row_s = kSwap ? fz.sb[fz.sb_n == 1 ? 0 : grow] : fz.sa[fz.sa_n == 1 ? 0 : grow];
+                    const float row_b = (kSwap && fz.bias) ? __uint_as_float(uint32_t(fz.bias[grow]) << 16) : 0.0f;
+#pragma unroll
+                    for (int c = 0; c < kCols; ++c) {
+                        const int gc = col0 + c_begin + c;   // token (swapped) or output column
+                        if (gc < a.cols) {
+                            const float col_s = kSwap ? fz.sa[fz.sa_n == 1 ? 0 : gc] : fz.sb[fz.sb_n == 1 ? 0 : gc];
+                            const float col_b = (!kSwap && fz.bias) ? __uint_as_float(uint32_t(fz.bias[gc]) << 16) : 0.0f;
+                            acc[c] = fmaf(acc[c] * row_s, col_s, row_b + col_b);
+                        }
+                    }
+                }
+            }
             if (store && !kSwap) {
                 if (grow < a.M) {
                     __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
@@ -1509,10 +1542,10 @@ __global__ void __launch_bounds__(
 // Launches one instantiation with programmatic stream serialisation (CTA
 // pairs: as clusters of two, at most as many pairs as can be resident).
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair = false,
-          bool kAlt = false, bool kFuse = false>
-sgq_status run(const CUtensorMap* maps, const GemmArgs& args, const FuseArgs& fz, int grid, cudaStream_t st) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>;
-    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse>;
+          bool kAlt = false, bool kFuse = false, bool kChan = false>
+sgq_status run(const CUtensorMap* maps, const GemmArgs& args, const ExtArgs& fz, int grid, cudaStream_t st) {
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>;
+    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>;
     static bool configured[64] = {};
     static int max_pairs[64] = {};
     int dev = 0;
@@ -1563,6 +1596,7 @@ struct Variant {
     bool alt;         // 128 x 256 tiles with two alternating MMA issuers
     bool scale_tma;   // scale boxes loaded by TMA
     bool fuse;        // swap-AB tiles that quantise the bf16 activations themselves
+    bool chan;        // per-channel scaling (fp8_scaled_mm): unscaled MMAs, scales in the epilogue
     int bn;           // MMA N of the swap-AB tile
 };
 
@@ -1570,7 +1604,7 @@ struct Variant {
 // maps: A operand, B operand, A-operand scales, B-operand scales.
 // Pair tiles (256 x 256, cta_group::2) need TMA-loaded scales.
 template <int kBlkN, int kBlkK, bool kScaleTma>
-sgq_status dispatch_tile(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const FuseArgs& fz, int grid,
+sgq_status dispatch_tile(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const ExtArgs& fz, int grid,
                          cudaStream_t st) {
     if (v.fuse) {
         if constexpr (kScaleTma) {
@@ -1602,16 +1636,17 @@ sgq_status dispatch_tile(const Variant& v, const CUtensorMap* maps, const GemmAr
     }
 }
 template <int kBlkN, int kBlkK>
-sgq_status dispatch(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const FuseArgs& fz, int grid,
+sgq_status dispatch(const Variant& v, const CUtensorMap* maps, const GemmArgs& a, const ExtArgs& fz, int grid,
                     cudaStream_t st) {
     return v.scale_tma ? dispatch_tile<kBlkN, kBlkK, true>(v, maps, a, fz, grid, st)
                        : dispatch_tile<kBlkN, kBlkK, false>(v, maps, a, fz, grid, st);
 }
 
-sgq_status dispatch_32_32(const Variant&, const CUtensorMap*, const GemmArgs&, const FuseArgs&, int, cudaStream_t);
-sgq_status dispatch_32_128(const Variant&, const CUtensorMap*, const GemmArgs&, const FuseArgs&, int, cudaStream_t);
-sgq_status dispatch_128_32(const Variant&, const CUtensorMap*, const GemmArgs&, const FuseArgs&, int, cudaStream_t);
-sgq_status dispatch_128_128(const Variant&, const CUtensorMap*, const GemmArgs&, const FuseArgs&, int, cudaStream_t);
+sgq_status dispatch_32_32(const Variant&, const CUtensorMap*, const GemmArgs&, const ExtArgs&, int, cudaStream_t);
+sgq_status dispatch_32_128(const Variant&, const CUtensorMap*, const GemmArgs&, const ExtArgs&, int, cudaStream_t);
+sgq_status dispatch_128_32(const Variant&, const CUtensorMap*, const GemmArgs&, const ExtArgs&, int, cudaStream_t);
+sgq_status dispatch_128_128(const Variant&, const CUtensorMap*, const GemmArgs&, const ExtArgs&, int, cudaStream_t);
+sgq_status dispatch_chan(const Variant&, const CUtensorMap*, const GemmArgs&, const ExtArgs&, int, cudaStream_t);
 
 }  // namespace gemm
 }  // namespace sgq

@@ -122,6 +122,99 @@ __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint16_t*
     }
 }
 
+// ---------------------------------------------------------------------------
+// Per-token quantisation (sgl_per_token_quant_fp8, "Sgl project Sglang GEMM
+// Interface", Quantization Routines): one scale per row, the group rule with
+// the group spanning the whole row.  One CTA per row (grid-stride over rows):
+// an amax pass over the row's 16-byte vectors, a block reduction, then a
+// second pass (the row is still in L1/L2) that writes the codes.
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+    const int w = threadIdx.x >> 5;
+    __syncthreads();   // red may still be read from the previous row
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    float m = red[0];
+#pragma unroll
+    for (int i = 1; i < kRowThreads / 32; ++i) m = fmaxf(m, red[i]);
+    return m;
+}
+
+__global__ void __launch_bounds__(kRowThreads) quant_per_token_kernel(const uint4* __restrict__ x,
+                                                                      uint2* __restrict__ xq,
+                                                                      float* __restrict__ xs, int64_t M,
+                                                                      int64_t vpr) {
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+    __shared__ float red[kRowThreads / 32];
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+        const uint4* xr = x + m * vpr;
+        float amax = 0.0f;
+        for (int64_t v = threadIdx.x; v < vpr; v += kRowThreads) {
+            float f[8];
+            unpack8(__ldg(xr + v), f);
+            amax = fmaxf(amax, qm::amax8(f));
+        }
+        const float s = group_scale(block_max(amax, red), false);
+        if (threadIdx.x == 0) xs[m] = s;
+        for (int64_t v = threadIdx.x; v < vpr; v += kRowThreads) {
+            float f[8];
+            unpack8(__ldg(xr + v), f);
+            xq[m * vpr + v] = quantize8(f, s, false);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Per-tensor quantisation (sgl_per_tensor_quant_fp8, same page: static or
+// dynamic scaling).  Dynamic: the first kernel writes one amax per CTA to a
+// fixed device array; the second kernel's CTAs each reduce those partials to
+// the same scale (CTA 0 stores it) and quantise.  Static: only the second
+// kernel, with the caller's scale.
+constexpr int kAmaxParts = 1024;
+__device__ float g_amax_parts[kAmaxParts];
+
+__global__ void __launch_bounds__(kRowThreads) amax_partial_kernel(const uint4* __restrict__ x, int64_t nvec) {
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+    __shared__ float red[kRowThreads / 32];
+    float amax = 0.0f;
+    for (int64_t v = blockIdx.x * int64_t(kRowThreads) + threadIdx.x; v < nvec;
+         v += int64_t(gridDim.x) * kRowThreads) {
+        float f[8];
+        unpack8(__ldg(x + v), f);
+        amax = fmaxf(amax, qm::amax8(f));
+    }
+    amax = block_max(amax, red);
+    if (threadIdx.x == 0) g_amax_parts[blockIdx.x] = amax;
+}
+
+__global__ void __launch_bounds__(kRowThreads) quant_per_tensor_kernel(const uint4* __restrict__ x,
+                                                                       uint2* __restrict__ xq, float* xs,
+                                                                       int64_t nvec, int nparts, int is_static) {
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();   // the partials (or the caller's scale) are ready
+    __shared__ float red[kRowThreads / 32];
+    float s;
+    if (is_static) {
+        s = xs[0];
+    } else {
+        float amax = 0.0f;
+        for (int i = threadIdx.x; i < nparts; i += kRowThreads) amax = fmaxf(amax, g_amax_parts[i]);
+        s = group_scale(block_max(amax, red), false);
+        if (blockIdx.x == 0 && threadIdx.x == 0) xs[0] = s;
+    }
+    for (int64_t v = blockIdx.x * int64_t(kRowThreads) + threadIdx.x; v < nvec;
+         v += int64_t(gridDim.x) * kRowThreads) {
+        float f[8];
+        unpack8(__ldg(x + v), f);
+        xq[v] = quantize8(f, s, false);
+    }
+}
+
 template <int G, bool U>
 sgq_status launch_tg(const void* x, int64_t M, int64_t K, void* xq, float* xs, cudaStream_t st) {
     const int64_t nvec = M * K / 8;
@@ -169,6 +262,18 @@ sgq_status launch_wb(const void* w, int64_t N, int64_t K, void* wq, float* ws, c
     return SGQ_OK;
 }
 
+cudaLaunchConfig_t pdl_config(cudaLaunchAttribute* attr, int blocks, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
 }  // namespace
 
 sgq_status launch_quant_token_group(const void* x, int64_t M, int64_t K, int group, int ue8m0,
@@ -191,6 +296,45 @@ sgq_status launch_quant_weight_block(const void* w, int64_t N, int64_t K, int bl
     SGQ_WB(128, 128)
 #undef SGQ_WB
     return SGQ_ERR_INVALID_ARG;
+}
+
+sgq_status launch_quant_per_token(const void* x, int64_t M, int64_t K, void* xq, float* xs, cudaStream_t st) {
+    DeviceInfo di;
+    sgq_status rc = device_info(&di);
+    if (rc != SGQ_OK) return rc;
+    const int64_t cap = int64_t(di.sm_count) * 8;
+    const int blocks = static_cast<int>(M < cap ? M : cap);
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(attr, blocks, st);
+    if (cudaLaunchKernelEx(&cfg, quant_per_token_kernel, static_cast<const uint4*>(x), static_cast<uint2*>(xq), xs,
+                           M, K / 8) != cudaSuccess)
+        return SGQ_ERR_CUDA;
+    note_launch();
+    return SGQ_OK;
+}
+
+sgq_status launch_quant_per_tensor(const void* x, int64_t n, int is_static, void* xq, float* xs, cudaStream_t st) {
+    DeviceInfo di;
+    sgq_status rc = device_info(&di);
+    if (rc != SGQ_OK) return rc;
+    const int64_t nvec = n / 8;
+    int64_t blocks = (nvec + kRowThreads - 1) / kRowThreads;
+    const int64_t cap = int64_t(di.sm_count) * 4 < kAmaxParts ? int64_t(di.sm_count) * 4 : kAmaxParts;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchAttribute attr[1];
+    if (!is_static) {
+        cudaLaunchConfig_t cfg = pdl_config(attr, static_cast<int>(blocks), st);
+        if (cudaLaunchKernelEx(&cfg, amax_partial_kernel, static_cast<const uint4*>(x), nvec) != cudaSuccess)
+            return SGQ_ERR_CUDA;
+        note_launch();
+    }
+    cudaLaunchConfig_t cfg = pdl_config(attr, static_cast<int>(blocks), st);
+    if (cudaLaunchKernelEx(&cfg, quant_per_tensor_kernel, static_cast<const uint4*>(x), static_cast<uint2*>(xq), xs,
+                           nvec, static_cast<int>(blocks), is_static) != cudaSuccess)
+        return SGQ_ERR_CUDA;
+    note_launch();
+    return SGQ_OK;
 }
 
 }  // namespace sgq

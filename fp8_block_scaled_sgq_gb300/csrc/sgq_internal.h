@@ -22,6 +22,10 @@ sgq_status launch_quant_token_group(const void* x, int64_t M, int64_t K, int gro
 sgq_status launch_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n,
                                      int blk_k, int ue8m0, void* wq, float* ws,
                                      cudaStream_t stream);
+sgq_status launch_quant_per_token(const void* x, int64_t M, int64_t K, void* xq, float* xs,
+                                  cudaStream_t stream);
+sgq_status launch_quant_per_tensor(const void* x, int64_t n, int is_static, void* xq, float* xs,
+                                   cudaStream_t stream);
 sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq,
                                  const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
                                  int blk_n, int blk_k, uint32_t flags, cudaStream_t stream);
@@ -31,6 +35,9 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
 sgq_status launch_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const float* Ws, void* D,
                                    int64_t M, int64_t N, int64_t K, int blk_n, int blk_k, void* xq,
                                    float* xs, cudaStream_t stream);
+sgq_status launch_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, const void* Wq,
+                                const float* sb, int64_t sb_n, const void* bias, void* D, int64_t M,
+                                int64_t N, int64_t K, cudaStream_t stream);
 // Reads and clears the device status word of the current device (after a sync).
 sgq_status read_and_clear_device_status(cudaStream_t stream);
 

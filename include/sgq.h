@@ -207,6 +207,37 @@ sgq_status sgq_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const 
                                 void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
                                 void* xq, float* xs, sgq_stream_t stream);
 
+/*
+ * Per-token and per-tensor quantisation, and the per-tensor / per-channel
+ * scaled GEMM: "Sgl project Sglang GEMM Interface", Quantization Routines and
+ * Signature (sgl_per_token_quant_fp8, sgl_per_tensor_quant_fp8 with static or
+ * dynamic scaling, fp8_scaled_mm with per-tensor or per-row scale_a,
+ * per-tensor or per-column scale_b, optional bias).  The quantisation rule is
+ * sgq_quant_token_group's with the group spanning a whole row (per token) or
+ * the whole tensor (per tensor, dynamic); there is no UE8M0 option.
+ *
+ * sgq_quant_per_token: x bf16 [M, K] -> xq E4M3 [M, K], xs fp32 [M].
+ *   K > 0, K % 16 == 0, M >= 0 (M == 0 is a no-op).
+ * sgq_quant_per_tensor: x bf16 [n] (any shape, n elements) -> xq E4M3 [n].
+ *   is_static = 0: xs[0] receives max(amax, 1e-10) / 448 over the tensor.
+ *   is_static = 1: xs[0] is read as the scale.  n % 16 == 0.  Dynamic scaling
+ *   keeps per-block maxima in a fixed device array of the library: calls that
+ *   overlap on the GPU (other streams, other host threads) must be avoided.
+ * sgq_fp8_scaled_mm: D[m, n] = bf16((sum_k Aq[m,k] Wq[n,k]) * sa[m] * sb[n]
+ *   + bias[n]), fp32 accumulation, with sa of sa_n = 1 (per tensor) or M (per
+ *   row) values, sb of sb_n = 1 or N (per column) values, bias bf16 [N] or
+ *   NULL.  Aq [M, K] and Wq [N, K] E4M3 (B given as [N, K], like the block
+ *   GEMM).  K % 32 == 0, N % 8 == 0; pointers 16-byte aligned.  Launch
+ *   overlap and errors: as for sgq_fp8_block_gemm.
+ */
+sgq_status sgq_quant_per_token(const void* x, int64_t M, int64_t K, void* xq, float* xs,
+                               sgq_stream_t stream);
+sgq_status sgq_quant_per_tensor(const void* x, int64_t n, int is_static, void* xq, float* xs,
+                                sgq_stream_t stream);
+sgq_status sgq_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, const void* Wq,
+                             const float* sb, int64_t sb_n, const void* bias, void* D, int64_t M,
+                             int64_t N, int64_t K, sgq_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sgq_status_string(sgq_status s);
 

@@ -125,6 +125,31 @@ def test_linear_validation(lib):
     assert f(*args(M=0, x=None, D=None)) == OK   # M == 0: no-op
 
 
+def test_per_token_per_tensor_scaled_mm_validation(lib):
+    INV, MIS, OK = binding.SGQ_ERR_INVALID_ARG, binding.SGQ_ERR_MISALIGNED, binding.SGQ_OK
+    L = binding.load_library()
+    assert L.sgq_quant_per_token(A, 4, 40, B, C, S) == INV          # K % 16
+    assert L.sgq_quant_per_token(A, -1, 64, B, C, S) == INV
+    assert L.sgq_quant_per_token(None, 4, 64, B, C, S) == INV
+    assert L.sgq_quant_per_token(A + 8, 4, 64, B, C, S) == MIS
+    assert L.sgq_quant_per_token(A, 0, 64, None, None, S) == OK      # M == 0: no-op
+    assert L.sgq_quant_per_tensor(A, 40, 0, B, C, S) == INV          # n % 16
+    assert L.sgq_quant_per_tensor(A, 64, 2, B, C, S) == INV          # is_static not 0/1
+    assert L.sgq_quant_per_tensor(A, 64, 0, B, None, S) == INV
+    assert L.sgq_quant_per_tensor(A, 64, 1, B + 4, C, S) == MIS
+    assert L.sgq_quant_per_tensor(A, 0, 0, None, None, S) == OK
+    mm = lambda **k: L.sgq_fp8_scaled_mm(k.get("Aq", A), k.get("sa", B), k.get("sa_n", 16), k.get("Wq", C),
+                                         k.get("sb", D), k.get("sb_n", 1), k.get("bias", None), k.get("D", E),
+                                         k.get("M", 16), k.get("N", 256), k.get("K", 512), S)
+    assert mm(K=48) == INV                       # K % 32
+    assert mm(N=260) == INV                      # N % 8
+    assert mm(sa_n=3) == INV                     # neither 1 nor M
+    assert mm(sb_n=255) == INV                   # neither 1 nor N
+    assert mm(sa=None) == INV
+    assert mm(bias=E + 4) == MIS
+    assert mm(M=0, Aq=None, sa=None, D=None, sa_n=1) == OK
+
+
 def test_binding_raises(lib):
     with pytest.raises(sgq.SgqError) as ei:
         sgq.sgq_quant_token_group(A, 4, 96, 128, 0, B, C, stream=S)
