@@ -15,6 +15,9 @@ builds it with gcc on first use and wraps it with numpy arrays:
 * ``gemm`` -- D = mm(As*Aq, (Ws*Wq)^T) in fp64 (vLLM scaled_mm page,
   AiterInt8ScaledMMLinearKernel.apply_weights docstring) plus the bound
   sum_k |a_deq||w_deq| used by the error criterion.
+* ``quant_token_group_v2`` (with ``exp_tc`` / ``silu_mul``) -- the V2
+  per-token-group quantiser: fused SiLU-and-mul and masked M (same page,
+  Quantization Routines and Signature).
 * ``quant_per_token`` / ``quant_per_tensor`` / ``scaled_mm`` -- the
   per-token and per-tensor quantisers and fp8_scaled_mm (per-tensor or per-row
   A scales, per-tensor or per-column B scales, optional bias) of "Sgl project
@@ -87,6 +90,12 @@ def _load():
         lib.sgqo_quant_per_tensor.restype = None
         lib.sgqo_scaled_mm.argtypes = [P, P, i64, P, P, i64, P, i64, i64, i64, P, P]
         lib.sgqo_scaled_mm.restype = None
+        lib.sgqo_exp_tc.argtypes = [cf]
+        lib.sgqo_exp_tc.restype = cf
+        lib.sgqo_silu_mul.argtypes = [cf, cf]
+        lib.sgqo_silu_mul.restype = cf
+        lib.sgqo_quant_token_group_v2.argtypes = [P, i64, i64, i64, ci, P, ci, ci, cf, P, P]
+        lib.sgqo_quant_token_group_v2.restype = None
         lib.sgqo_num_threads.argtypes = []
         lib.sgqo_num_threads.restype = ci
         _lib = lib
@@ -220,3 +229,36 @@ def scaled_mm(aq, sa, wq, sb, bias=None, with_bound: bool = True):
                            _ptr(bb) if bb is not None else None, M, N, K, _ptr(d),
                            _ptr(b) if b is not None else None)
     return (d, b) if with_bound else d
+
+
+def exp_tc(x) -> np.ndarray:
+    """fp32 exp by Cody-Waite reduction and a degree-7 Taylor polynomial (elementwise)."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float32)
+    return np.array([lib.sgqo_exp_tc(float(v)) for v in x.reshape(-1)], dtype=np.float32).reshape(x.shape)
+
+
+def silu_mul(g, u) -> np.ndarray:
+    lib = _load()
+    g = np.asarray(g, dtype=np.float32)
+    u = np.broadcast_to(np.asarray(u, dtype=np.float32), g.shape)
+    return np.array([lib.sgqo_silu_mul(float(a), float(b)) for a, b in zip(g.reshape(-1), u.reshape(-1))],
+                    dtype=np.float32).reshape(g.shape)
+
+
+def quant_token_group_v2(x, group: int, ue8m0: bool, fuse: bool, masked_m=None, eps: float = EPS,
+                         xq=None, xs=None):
+    """x: bf16 [E, T, W] (W = 2H when fuse, else H) -> (codes [E, T, H], scales [E, T, H/group]).
+    Rows t >= masked_m[e] keep the contents of the given xq/xs (zeros when not given)."""
+    xb = _as_bf16_bits(x)
+    E, T, W = xb.shape
+    H = W // 2 if fuse else W
+    if H % group:
+        raise ValueError("H must be a multiple of group")
+    xq = np.zeros((E, T, H), dtype=np.uint8) if xq is None else np.ascontiguousarray(xq, dtype=np.uint8).copy()
+    xs = np.zeros((E, T, H // group), dtype=np.float32) if xs is None else \
+        np.ascontiguousarray(xs, dtype=np.float32).copy()
+    mm = None if masked_m is None else np.ascontiguousarray(masked_m, dtype=np.int32)
+    _load().sgqo_quant_token_group_v2(_ptr(xb), E, T, H, int(fuse), _ptr(mm) if mm is not None else None,
+                                      group, int(ue8m0), eps, _ptr(xq), _ptr(xs))
+    return xq, xs

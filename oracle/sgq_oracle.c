@@ -26,6 +26,14 @@
  *    Sglang GEMM Interface", Quantization Routines and Signature) and the
  *    scaled GEMM fp8_scaled_mm (same page: per-tensor or per-row scale_a,
  *    per-tensor or per-column scale_b, optional bias, output dtype).
+ *  - The V2 per-token-group quantiser's fused SiLU-and-mul and masked M (same
+ *    page, Quantization Routines: "a V2 variant ... that adds fused
+ *    SiLU-and-mul and masked M support"; Signature: fuse_silu_and_mul,
+ *    masked_m).  Reading: input rows [gate | up] of width 2H, y = silu(gate) *
+ *    up in fp32 with silu(g) = g / (1 + exp(-g)), quantised per group like x;
+ *    for a [E, T, .] input, rows t >= masked_m[e] of expert e are left
+ *    untouched.  exp is the Cody-Waite reduction with a degree-7 Taylor
+ *    polynomial below, so that GPU and CPU produce the same fp32 value.
  *  - The GEMM: the vLLM "scaled_mm" API page,
  *    AiterInt8ScaledMMLinearKernel.apply_weights docstring: the output is
  *    mm(scale_a * a, scale_b * b) with numpy-style broadcasting of the scales,
@@ -310,4 +318,85 @@ void sgqo_scaled_mm(const uint8_t* aq, const float* sa, int64_t sa_n, const uint
             if (bound) bound[m * N + n] = b * fabs(am * bn);
         }
     }
+}
+
+/*
+ * exp(x) in fp32 by a textbook method: x = k ln2 + r with k = rint(x / ln2)
+ * and ln2 split into a high part with a short mantissa and a low part (Cody &
+ * Waite's reduction), |r| <= ln2/2; e^r from its Taylor series to degree 7
+ * (1/n! rounded to fp32), Horner's scheme with fused multiply-adds; then
+ * scaled by 2^k through the exponent field.  Below -87.3 the result is 0,
+ * above 88.7 it is +inf.  Every step is one correctly rounded fp32 operation,
+ * so any IEEE implementation of the same steps gives the same bits.
+ */
+float sgqo_exp_tc(float x) {
+    if (x > 88.72f) return orc_float(0x7F800000u);
+    if (x < -87.33f) return 0.0f;
+    const float log2e = 1.44269504088896341f;
+    const float ln2_hi = 0.693145751953125f;        /* 12 significant bits: k * ln2_hi is exact */
+    const float ln2_lo = 1.42860682030941723e-6f;   /* ln2 - ln2_hi */
+    volatile float kx = x * log2e;
+    float k = rintf(kx);
+    float r = fmaf(-k, ln2_hi, x);
+    r = fmaf(-k, ln2_lo, r);
+    const float c7 = (float)(1.0 / 5040.0), c6 = (float)(1.0 / 720.0), c5 = (float)(1.0 / 120.0);
+    const float c4 = (float)(1.0 / 24.0), c3 = (float)(1.0 / 6.0), c2 = 0.5f;
+    float p = c7;
+    p = fmaf(p, r, c6);
+    p = fmaf(p, r, c5);
+    p = fmaf(p, r, c4);
+    p = fmaf(p, r, c3);
+    p = fmaf(p, r, c2);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    /* p in [0.7, 1.42]: multiply by 2^k in two steps so that 2^k itself stays normal */
+    int ki = (int)k;
+    int k1 = ki / 2, k2 = ki - k1;
+    volatile float q = p * orc_float((uint32_t)(k1 + 127) << 23);
+    float res = q;
+    volatile float q2 = res * orc_float((uint32_t)(k2 + 127) << 23);
+    return q2;
+}
+
+/* y = silu(g) * u = (g / (1 + exp(-g))) * u, each step one fp32 operation. */
+float sgqo_silu_mul(float g, float u) {
+    volatile float den = 1.0f + sgqo_exp_tc(-g);
+    volatile float s = g / den;
+    volatile float y = s * u;
+    return y;
+}
+
+/*
+ * V2 per-token-group quantisation.  x: bf16 bits [E, T, W] with W = 2H when
+ * fuse (rows [gate | up]) else W = H.  masked_m: int32 [E] or NULL (all T
+ * rows).  xq: [E, T, H] codes; xs: fp32 [E, T, H / group].  Rows of expert e
+ * from masked_m[e] on are not written.
+ */
+void sgqo_quant_token_group_v2(const uint16_t* x, int64_t E, int64_t T, int64_t H, int fuse,
+                               const int32_t* masked_m, int group, int ue8m0, float eps, uint8_t* xq,
+                               float* xs) {
+    const int64_t W = fuse ? 2 * H : H, G = H / group;
+    float* y = (float*)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+    for (int64_t e = 0; e < E; ++e) {
+        int64_t rows = masked_m ? (int64_t)masked_m[e] : T;
+        if (rows > T) rows = T;
+        for (int64_t t = 0; t < rows; ++t) {
+            const uint16_t* xr = x + (e * T + t) * W;
+            for (int64_t k = 0; k < H; ++k)
+                y[k] = fuse ? sgqo_silu_mul(sgqo_bf16_to_f32(xr[k]), sgqo_bf16_to_f32(xr[H + k]))
+                            : sgqo_bf16_to_f32(xr[k]);
+            const int64_t row = e * T + t;
+            for (int64_t j = 0; j < G; ++j) {
+                float amax = 0.0f;
+                for (int i = 0; i < group; ++i) {
+                    float a = fabsf(y[j * group + i]);
+                    if (a > amax) amax = a;
+                }
+                float s = sgqo_group_scale(amax, eps, ue8m0);
+                xs[row * G + j] = s;
+                for (int i = 0; i < group; ++i) xq[row * H + j * group + i] = orc_quant_one(y[j * group + i], s);
+            }
+        }
+    }
+    free(y);
 }

@@ -426,3 +426,92 @@ def test_scaled_mm_per_tensor_equals_block_gemm_with_constant_scales():
     bias = _rand_bf16((6,), 10)
     db, _ = oracle.scaled_mm(aq, sa, wq, sb, bias)
     assert np.allclose(db - d, np.broadcast_to(bias.float().numpy().astype(np.float64), d.shape), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- V2 quantiser: fused SiLU-and-mul, masked M
+# ("Sgl project Sglang GEMM Interface", Quantization Routines: the V2 variant of
+# sgl_per_token_group_quant_8bit; Signature: fuse_silu_and_mul, masked_m)
+
+def _ulp_diff(a, b):
+    ai = np.asarray(a, np.float32).view(np.int32).astype(np.int64)
+    bi = np.asarray(b, np.float32).view(np.int32).astype(np.int64)
+    return np.abs(ai - bi)
+
+
+def test_exp_within_two_ulp_and_monotone():
+    xs = np.linspace(-87.0, 88.5, 20001, dtype=np.float32)
+    e = oracle.exp_tc(xs)
+    ref = np.exp(xs.astype(np.float64)).astype(np.float32)          # correctly rounded to fp32 (almost always)
+    assert _ulp_diff(e, ref).max() <= 2
+    assert np.all(np.diff(e.astype(np.float64)) >= 0)
+    assert oracle.exp_tc(np.float32(0.0)) == np.float32(1.0)
+    assert oracle.exp_tc(np.float32(-100.0)) == 0.0 and np.isinf(oracle.exp_tc(np.float32(100.0)))
+
+
+def test_silu_identities():
+    g = np.linspace(-30, 30, 4001, dtype=np.float32)
+    s = oracle.silu_mul(g, 1.0)
+    ref = (g.astype(np.float64) / (1.0 + np.exp(-g.astype(np.float64))))
+    assert np.allclose(s, ref, rtol=3e-7, atol=1e-30)
+    sm = oracle.silu_mul(-g, 1.0)
+    assert np.allclose(s.astype(np.float64) - sm, g.astype(np.float64), rtol=1e-6, atol=1e-6)   # silu(x)-silu(-x)=x
+    big = np.array([17.0, 20.0, 100.0, 3.0e4], np.float32)
+    assert np.array_equal(oracle.silu_mul(big, 1.0), big)                   # e^-g below half an ulp of 1
+    assert oracle.silu_mul(np.float32(0.0), np.float32(5.0)) == 0.0
+    u = np.array([0.5, -2.0, 3.0, 7.0], np.float32)
+    assert np.array_equal(oracle.silu_mul(big, u), big * u)                 # exact products
+
+
+def _v2_input(E, T, H, fuse, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((E, T, 2 * H if fuse else H), generator=g).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("group,ue", [(32, True), (128, False)])
+def test_v2_without_fusion_or_mask_is_the_group_quantiser(group, ue):
+    x = _v2_input(3, 5, 256, False, 11)
+    q, s = oracle.quant_token_group_v2(x, group, ue, fuse=False)
+    qg, sg = oracle.quant_token_group(x.reshape(15, 256), group, ue)
+    assert np.array_equal(q.reshape(15, 256), qg) and np.array_equal(s.reshape(15, -1), sg)
+
+
+def test_v2_fused_with_saturated_gate_is_the_group_quantiser_of_the_gate():
+    H = 128
+    gate = (torch.rand((2, 4, H), generator=torch.Generator().manual_seed(12)) * 30 + 17).to(torch.bfloat16)
+    x = torch.cat([gate, torch.ones_like(gate)], dim=-1)
+    q, s = oracle.quant_token_group_v2(x, 32, True, fuse=True)
+    qg, sg = oracle.quant_token_group(gate.reshape(8, H), 32, True)
+    assert np.array_equal(q.reshape(8, H), qg) and np.array_equal(s.reshape(8, -1), sg)
+
+
+def test_v2_fused_matches_fp64_silu_mul_then_the_pinned_quantiser():
+    """y from an fp64 silu(gate) * up (rounded to fp32) quantised by the pinned
+    group rule: the codes agree except where the fp32 pipeline's last-ulp
+    difference moves a value across an E4M3 rounding boundary (none here)."""
+    E, T, H, group = 2, 3, 64, 32
+    x = _v2_input(E, T, H, True, 13)
+    q, s = oracle.quant_token_group_v2(x, group, False, fuse=True)
+    xf = x.float().numpy().astype(np.float64)
+    y = (xf[..., :H] / (1.0 + np.exp(-xf[..., :H])) * xf[..., H:]).astype(np.float32)
+    for e in range(E):
+        for t in range(T):
+            for j in range(H // group):
+                grp = y[e, t, j * group:(j + 1) * group]
+                sc = oracle.group_scale(np.abs(grp).max(), False)
+                assert _ulp_diff(s[e, t, j], sc) <= 2
+                want = oracle.e4m3_encode(np.clip(grp / s[e, t, j], -448, 448).astype(np.float32))
+                assert (q[e, t, j * group:(j + 1) * group] != want).sum() <= 1
+
+
+def test_v2_masked_rows_untouched():
+    E, T, H = 3, 6, 128
+    x = _v2_input(E, T, H, True, 14)
+    masked = np.array([0, 4, 6], np.int32)
+    sentinel_q = np.full((E, T, H), 0x5A, np.uint8)
+    sentinel_s = np.full((E, T, H // 32), -1.0, np.float32)
+    q, s = oracle.quant_token_group_v2(x, 32, True, fuse=True, masked_m=masked, xq=sentinel_q, xs=sentinel_s)
+    qa, sa = oracle.quant_token_group_v2(x, 32, True, fuse=True)
+    for e in range(E):
+        m = masked[e]
+        assert np.array_equal(q[e, :m], qa[e, :m]) and np.array_equal(s[e, :m], sa[e, :m])
+        assert (q[e, m:] == 0x5A).all() and (s[e, m:] == -1.0).all()
