@@ -11,7 +11,7 @@ from .binding import (  # noqa: F401
     EXPORTS, SGQ_GEMM_DEFAULT, SGQ_GEMM_FORCE_PROMOTE, SGQ_GEMM_ISSUE_ALT, SGQ_GEMM_ISSUE_SINGLE, SgqError,
     load_library, sgq_device_status,
     sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_fp8_block_linear, sgq_fp8_scaled_mm,
-    sgq_quant_per_tensor, sgq_quant_per_token, sgq_launch_count, sgq_quant_token_group,
+    sgq_quant_per_tensor, sgq_quant_per_token, sgq_quant_token_group_v2, sgq_launch_count, sgq_quant_token_group,
     sgq_quant_weight_block, sgq_version, status_string)
 
 
@@ -102,3 +102,16 @@ def fp8_scaled_mm(aq, sa, wq, sb, bias=None, out=None, stream=None):
         out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
     sgq_fp8_scaled_mm(aq, sa, sa.numel(), wq, sb, sb.numel(), bias, out, M, N, K, stream)
     return out
+
+
+def quant_token_group_v2(x, group: int, ue8m0: bool, fuse: bool, masked_m=None, xq=None, xs=None, stream=None):
+    """bf16 [E, T, W] CUDA tensor (W = 2H fused) -> (E4M3 [E, T, H], fp32 [E, T, H/group])."""
+    import torch
+    E, T, W = x.shape
+    H = W // 2 if fuse else W
+    if xq is None:
+        xq = torch.empty((E, T, H), dtype=torch.uint8, device=x.device)
+    if xs is None:
+        xs = torch.empty((E, T, H // group), dtype=torch.float32, device=x.device)
+    sgq_quant_token_group_v2(x, E, T, H, group, ue8m0, fuse, masked_m, xq, xs, stream)
+    return xq, xs

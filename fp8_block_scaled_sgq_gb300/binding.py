@@ -36,6 +36,7 @@ EXPORTS = (
     "sgq_fp8_block_gemm_ex",
     "sgq_fp8_block_gemm_noalloc",
     "sgq_fp8_block_linear",
+    "sgq_quant_token_group_v2",
     "sgq_quant_per_token",
     "sgq_quant_per_tensor",
     "sgq_fp8_scaled_mm",
@@ -73,12 +74,13 @@ def load_library(path: str = LIB_PATH):
         lib.sgq_fp8_block_gemm_ex.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, u32, P]
         lib.sgq_fp8_block_gemm_noalloc.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, P]
         lib.sgq_fp8_block_linear.argtypes = [P, ci, P, P, P, i64, i64, i64, ci, ci, P, P, P]
+        lib.sgq_quant_token_group_v2.argtypes = [P, i64, i64, i64, ci, ci, ci, P, P, P, P]
         lib.sgq_quant_per_token.argtypes = [P, i64, i64, P, P, P]
         lib.sgq_quant_per_tensor.argtypes = [P, i64, ci, P, P, P]
         lib.sgq_fp8_scaled_mm.argtypes = [P, P, i64, P, P, i64, P, P, i64, i64, i64, P]
         for f in ("sgq_quant_token_group", "sgq_quant_weight_block", "sgq_fp8_block_gemm",
                   "sgq_fp8_block_gemm_ex", "sgq_fp8_block_gemm_noalloc", "sgq_fp8_block_linear",
-                  "sgq_quant_per_token", "sgq_quant_per_tensor", "sgq_fp8_scaled_mm"):
+                  "sgq_quant_per_token", "sgq_quant_per_tensor", "sgq_fp8_scaled_mm", "sgq_quant_token_group_v2"):
             getattr(lib, f).restype = ci
         lib.sgq_status_string.argtypes = [ci]
         lib.sgq_status_string.restype = ctypes.c_char_p
@@ -154,6 +156,12 @@ def sgq_fp8_block_linear(x, ue8m0, Wq, Ws, D, M, N, K, blk_n, blk_k, xq=None, xs
     _check(load_library().sgq_fp8_block_linear(_ptr(x), int(ue8m0), _ptr(Wq), _ptr(Ws), _ptr(D), M, N, K,
                                                blk_n, blk_k, _ptr(xq), _ptr(xs), _stream(stream)),
            "sgq_fp8_block_linear")
+
+
+def sgq_quant_token_group_v2(x, E, T, H, group, ue8m0, fuse, masked_m, xq, xs, stream=None):
+    _check(load_library().sgq_quant_token_group_v2(_ptr(x), E, T, H, group, int(ue8m0), int(fuse), _ptr(masked_m),
+                                                   _ptr(xq), _ptr(xs), _stream(stream)),
+           "sgq_quant_token_group_v2")
 
 
 def sgq_quant_per_token(x, M, K, xq, xs, stream=None):

@@ -113,6 +113,22 @@ sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const voi
                                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+sgq_status sgq_quant_token_group_v2(const void* x, int64_t E, int64_t T, int64_t H, int group, int ue8m0,
+                                    int fuse_silu_and_mul, const int32_t* masked_m, void* xq, float* xs,
+                                    sgq_stream_t stream) {
+    if (E < 0 || T < 0 || H <= 0 || (group != 32 && group != 128) || H % group != 0 ||
+        (ue8m0 != 0 && ue8m0 != 1) || (fuse_silu_and_mul != 0 && fuse_silu_and_mul != 1))
+        return SGQ_ERR_INVALID_ARG;
+    if (E >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || E * T * H > (int64_t(1) << 40))
+        return SGQ_ERR_INVALID_ARG;
+    if (E == 0 || T == 0) return SGQ_OK;
+    if (!x || !xq || !xs) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(xs) || (masked_m && !aligned16(masked_m)))
+        return SGQ_ERR_MISALIGNED;
+    return sgq::launch_quant_token_group_v2(x, E, T, H, group, ue8m0, fuse_silu_and_mul, masked_m, xq, xs,
+                                            reinterpret_cast<cudaStream_t>(stream));
+}
+
 sgq_status sgq_quant_per_token(const void* x, int64_t M, int64_t K, void* xq, float* xs, sgq_stream_t stream) {
     if (M < 0 || K <= 0 || K % 16 != 0 || M >= (int64_t(1) << 31) || M * K > (int64_t(1) << 40))
         return SGQ_ERR_INVALID_ARG;

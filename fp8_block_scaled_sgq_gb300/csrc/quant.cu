@@ -123,6 +123,59 @@ __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint16_t*
 }
 
 // ---------------------------------------------------------------------------
+// V2 per-token-group quantisation ("Sgl project Sglang GEMM Interface",
+// Quantization Routines: the V2 variant of sgl_per_token_group_quant_8bit with
+// fused SiLU-and-mul and masked M).  x: bf16 [E, T, W] with W = 2H (rows
+// [gate | up]) when fused, else H; the quantised value is silu(gate) * up (or
+// x) in fp32.  Rows t >= masked_m[e] of expert e are skipped (not written).
+// One thread per 8 outputs, kTpg = group/8 lanes per group as above; a
+// warp's lanes never straddle a group (H % group == 0).
+template <int kGroup, bool kUe8m0, bool kFuse>
+__global__ void __launch_bounds__(256) quant_token_group_v2_kernel(const uint4* __restrict__ x,
+                                                                   const int32_t* __restrict__ masked_m,
+                                                                   uint2* __restrict__ xq, float* __restrict__ xs,
+                                                                   int64_t nvec, int64_t vpr, int64_t T) {
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+    constexpr int kTpg = kGroup / 8;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t base = warp * 32; base < nvec; base += nwarps * 32) {
+        const int64_t v = base + lane;
+        const int64_t row = v / vpr, c = v - row * vpr;
+        bool active = v < nvec;
+        if (active && masked_m != nullptr) {
+            const int64_t e = row / T;
+            active = row - e * T < static_cast<int64_t>(__ldg(masked_m + e));
+        }
+        float f[8];
+        if (active) {
+            if (kFuse) {
+                float g[8], u[8];
+                unpack8(__ldg(x + row * 2 * vpr + c), g);
+                unpack8(__ldg(x + row * 2 * vpr + vpr + c), u);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = qm::silu_mul(g[i], u[i]);
+            } else {
+                unpack8(__ldg(x + row * vpr + c), f);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+        }
+        float amax = qm::amax8(f);
+#pragma unroll
+        for (int off = kTpg / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        const float s = group_scale(amax, kUe8m0);
+        if (active) {
+            xq[v] = quantize8(f, s, kUe8m0);
+            if ((lane % kTpg) == 0) xs[v / kTpg] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Per-token quantisation (sgl_per_token_quant_fp8, "Sgl project Sglang GEMM
 // Interface", Quantization Routines): one scale per row, the group rule with
 // the group spanning the whole row.  One CTA per row (grid-stride over rows):
@@ -335,6 +388,39 @@ sgq_status launch_quant_per_tensor(const void* x, int64_t n, int is_static, void
         return SGQ_ERR_CUDA;
     note_launch();
     return SGQ_OK;
+}
+
+namespace {
+template <int G, bool U, bool F>
+sgq_status launch_v2(const void* x, int64_t E, int64_t T, int64_t H, const int32_t* masked_m, void* xq, float* xs,
+                     cudaStream_t st) {
+    DeviceInfo di;
+    sgq_status rc = device_info(&di);
+    if (rc != SGQ_OK) return rc;
+    const int64_t nvec = E * T * H / 8;
+    int64_t blocks = (nvec + 255) / 256;
+    const int64_t cap = int64_t(di.sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(attr, static_cast<int>(blocks), st);
+    cfg.blockDim = dim3(256);
+    if (cudaLaunchKernelEx(&cfg, quant_token_group_v2_kernel<G, U, F>, static_cast<const uint4*>(x), masked_m,
+                           static_cast<uint2*>(xq), xs, nvec, H / 8, T) != cudaSuccess)
+        return SGQ_ERR_CUDA;
+    note_launch();
+    return SGQ_OK;
+}
+}  // namespace
+
+sgq_status launch_quant_token_group_v2(const void* x, int64_t E, int64_t T, int64_t H, int group, int ue8m0,
+                                       int fuse, const int32_t* masked_m, void* xq, float* xs, cudaStream_t st) {
+#define SGQ_V2(g, u, f)                                                                  \
+    if (group == g && (ue8m0 != 0) == u && (fuse != 0) == f)                            \
+        return launch_v2<g, u, f>(x, E, T, H, masked_m, xq, xs, st);
+    SGQ_V2(32, false, false) SGQ_V2(32, false, true) SGQ_V2(32, true, false) SGQ_V2(32, true, true)
+    SGQ_V2(128, false, false) SGQ_V2(128, false, true) SGQ_V2(128, true, false) SGQ_V2(128, true, true)
+#undef SGQ_V2
+    return SGQ_ERR_INVALID_ARG;
 }
 
 }  // namespace sgq

@@ -71,5 +71,37 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
     return a;
 }
 
+// exp(x) in fp32 by a textbook method, for the fused SiLU-and-mul: x = k ln2 + r
+// with k = rint(x / ln2) and ln2 split into a short-mantissa high part and a low
+// part (Cody & Waite's reduction), e^r from its Taylor series to degree 7
+// (1/n! rounded to fp32) by Horner's scheme with fused multiply-adds, then
+// times 2^k in two exponent-field steps.  Below -87.33 the result is 0, above
+// 88.72 +inf.  Each step is one correctly rounded fp32 operation (explicit
+// intrinsics: nothing contracted), so the value is reproducible bit for bit.
+__device__ __forceinline__ float exp_tc(float x) {
+    if (x > 88.72f) return __uint_as_float(0x7F800000u);
+    if (x < -87.33f) return 0.0f;
+    const float k = rintf(__fmul_rn(x, 1.44269504088896341f));
+    float r = __fmaf_rn(-k, 0.693145751953125f, x);
+    r = __fmaf_rn(-k, 1.42860682030941723e-6f, r);
+    float p = static_cast<float>(1.0 / 5040.0);
+    p = __fmaf_rn(p, r, static_cast<float>(1.0 / 720.0));
+    p = __fmaf_rn(p, r, static_cast<float>(1.0 / 120.0));
+    p = __fmaf_rn(p, r, static_cast<float>(1.0 / 24.0));
+    p = __fmaf_rn(p, r, static_cast<float>(1.0 / 6.0));
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const int ki = static_cast<int>(k);
+    const int k1 = ki / 2, k2 = ki - k1;
+    p = __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(k1 + 127) << 23));
+    return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(k2 + 127) << 23));
+}
+
+// silu(g) * u = (g / (1 + exp(-g))) * u, one fp32 operation per step.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, exp_tc(-g))), u);
+}
+
 }  // namespace qm
 }  // namespace sgq

@@ -22,6 +22,9 @@ sgq_status launch_quant_token_group(const void* x, int64_t M, int64_t K, int gro
 sgq_status launch_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n,
                                      int blk_k, int ue8m0, void* wq, float* ws,
                                      cudaStream_t stream);
+sgq_status launch_quant_token_group_v2(const void* x, int64_t E, int64_t T, int64_t H, int group, int ue8m0,
+                                       int fuse, const int32_t* masked_m, void* xq, float* xs,
+                                       cudaStream_t stream);
 sgq_status launch_quant_per_token(const void* x, int64_t M, int64_t K, void* xq, float* xs,
                                   cudaStream_t stream);
 sgq_status launch_quant_per_tensor(const void* x, int64_t n, int is_static, void* xq, float* xs,

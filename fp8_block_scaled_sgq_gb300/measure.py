@@ -5,6 +5,8 @@
 PATH is one of
   quant_per_token   sgq_quant_per_token on x [M, K]            (GB/s: 2 B in + 1 B code per element + 4 B per row)
   quant_per_tensor  sgq_quant_per_tensor, dynamic, on x [M, K] (GB/s: 2 B in + 1 B code per element)
+  quant_v2          sgq_quant_token_group_v2, fused SiLU-and-mul, x [1, M, 2K] -> [1, M, K], group --blk, UE8M0
+                    (GB/s: 4 B in + 1 B code per output element + 4 B per group)
   scaled_mm         sgq_fp8_scaled_mm, per-row x per-column scales, bias   (TFLOP/s and GB/s)
   block_gemm        sgq_fp8_block_gemm with [B, B] blocks, UE8M0           (TFLOP/s and GB/s)
   linear            sgq_fp8_block_linear with [B, B] blocks, UE8M0         (GB/s of x + W + D)
@@ -29,7 +31,8 @@ L2_BYTES = 129 * 2 ** 20
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("path", choices=["quant_per_token", "quant_per_tensor", "scaled_mm", "block_gemm", "linear"])
+    ap.add_argument("path", choices=["quant_per_token", "quant_per_tensor", "quant_v2", "scaled_mm", "block_gemm",
+                                     "linear"])
     ap.add_argument("M", type=int)
     ap.add_argument("N", type=int)
     ap.add_argument("K", type=int)
@@ -41,20 +44,26 @@ def main() -> None:
     st = torch.cuda.Stream()
     s = st.cuda_stream
     quant = args.path.startswith("quant")
-    rot_bytes = M * K * 2 if quant else N * K
+    rot_bytes = (M * K * (4 if args.path == "quant_v2" else 2)) if quant else N * K
     n_rot = max(2, math.ceil(2 * L2_BYTES / rot_bytes) + 1)
     calls = []
     if quant:
-        xr = [synth.activation(M, K, seed=i).to(dev) for i in range(min(n_rot, 4))]
+        W = 2 * K if args.path == "quant_v2" else K
+        xr = [synth.activation(M, W, seed=i).to(dev) for i in range(min(n_rot, 4))]
         xr = [xr[i % len(xr)].clone() for i in range(n_rot)]
         xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
         sc = torch.empty((max(M, 4),), dtype=torch.float32, device=dev)
+        sc2 = torch.empty((M, K // blk), dtype=torch.float32, device=dev)
         for r in range(n_rot):
             if args.path == "quant_per_token":
                 calls.append(lambda sp, r=r: binding.sgq_quant_per_token(xr[r], M, K, xq, sc, sp))
+            elif args.path == "quant_v2":
+                calls.append(lambda sp, r=r: binding.sgq_quant_token_group_v2(xr[r], 1, M, K, blk, 1, 1, None, xq,
+                                                                             sc2, sp))
             else:
                 calls.append(lambda sp, r=r: binding.sgq_quant_per_tensor(xr[r], M * K, 0, xq, sc, sp))
-        moved = M * K * 3 + (4 * M if args.path == "quant_per_token" else 4)
+        moved = {"quant_per_token": M * K * 3 + 4 * M, "quant_per_tensor": M * K * 3 + 4,
+                 "quant_v2": M * K * 5 + 4 * M * (K // blk)}[args.path]
         flops = 0
     else:
         x = synth.activation(M, K, seed=1).to(dev)

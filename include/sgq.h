@@ -208,6 +208,24 @@ sgq_status sgq_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const 
                                 void* xq, float* xs, sgq_stream_t stream);
 
 /*
+ * V2 per-token-group quantisation: the same rule as sgq_quant_token_group,
+ * with the V2 options of "Sgl project Sglang GEMM Interface", Quantization
+ * Routines and Signature (fuse_silu_and_mul, masked_m).
+ *
+ * x: bf16 [E, T, W] row-major, W = 2H when fuse_silu_and_mul (each row is
+ * [gate | up]) else W = H.  The value quantised is y = silu(gate) * up in fp32
+ * with silu(g) = g / (1 + exp(-g)) (exp: Cody-Waite reduction and a degree-7
+ * Taylor polynomial, so the result is reproducible bit for bit), or x itself.
+ * xq: E4M3 [E, T, H]; xs: fp32 [E, T, H/group].  masked_m: int32 [E] on the
+ * device, or NULL for all T rows: rows t >= masked_m[e] of expert e are not
+ * read or written.  group in {32, 128}, H % group == 0, ue8m0 and
+ * fuse_silu_and_mul in {0, 1}.  E or T == 0 is a no-op.
+ */
+sgq_status sgq_quant_token_group_v2(const void* x, int64_t E, int64_t T, int64_t H, int group,
+                                    int ue8m0, int fuse_silu_and_mul, const int32_t* masked_m,
+                                    void* xq, float* xs, sgq_stream_t stream);
+
+/*
  * Per-token and per-tensor quantisation, and the per-tensor / per-channel
  * scaled GEMM: "Sgl project Sglang GEMM Interface", Quantization Routines and
  * Signature (sgl_per_token_quant_fp8, sgl_per_tensor_quant_fp8 with static or

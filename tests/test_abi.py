@@ -150,6 +150,21 @@ def test_per_token_per_tensor_scaled_mm_validation(lib):
     assert mm(M=0, Aq=None, sa=None, D=None, sa_n=1) == OK
 
 
+def test_v2_quant_validation(lib):
+    INV, MIS, OK = binding.SGQ_ERR_INVALID_ARG, binding.SGQ_ERR_MISALIGNED, binding.SGQ_OK
+    f = binding.load_library().sgq_quant_token_group_v2
+    args = lambda **k: [k.get("x", A), k.get("E", 2), k.get("T", 4), k.get("H", 256), k.get("group", 128),
+                        k.get("ue", 0), k.get("fuse", 1), k.get("mask", None), k.get("xq", B), k.get("xs", C), S]
+    assert f(*args(group=64)) == INV
+    assert f(*args(H=80, group=32)) == INV       # H % group
+    assert f(*args(ue=2)) == INV
+    assert f(*args(fuse=2)) == INV
+    assert f(*args(E=-1)) == INV
+    assert f(*args(x=None)) == INV
+    assert f(*args(mask=D + 4)) == MIS
+    assert f(*args(T=0, x=None, xq=None, xs=None)) == OK
+
+
 def test_binding_raises(lib):
     with pytest.raises(sgq.SgqError) as ei:
         sgq.sgq_quant_token_group(A, 4, 96, 128, 0, B, C, stream=S)
