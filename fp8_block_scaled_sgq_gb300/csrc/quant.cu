@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(256) quant_token_group_v2_kernel(const uint4* 
 // Interface", Quantization Routines): one scale per row, the group rule with
 // the group spanning the whole row.  One CTA per row (grid-stride over rows):
 // an amax pass over the row's 16-byte vectors, a block reduction, then a
-// second pass (the row is still in L1/L2) that writes the codes.
+// second pass that writes the codes.
 constexpr int kRowThreads = 256;
 
 __device__ __forceinline__ float block_max(float v, float* red) {
@@ -196,27 +196,104 @@ __device__ __forceinline__ float block_max(float v, float* red) {
     return m;
 }
 
-__global__ void __launch_bounds__(kRowThreads) quant_per_token_kernel(const uint4* __restrict__ x,
+// Rows of up to kRowThreads * kRowRegs vectors (K <= 8192) stay in registers
+// between the two passes; longer rows are read a second time (from L1/L2).
+// Six CTAs per SM keep about 80 KB of each SM's loads in flight.
+constexpr int kRowRegs = 4;
+
+__global__ void __launch_bounds__(kRowThreads, 6) quant_per_token_kernel(const uint4* __restrict__ x,
                                                                       uint2* __restrict__ xq,
                                                                       float* __restrict__ xs, int64_t M,
                                                                       int64_t vpr) {
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
     __shared__ float red[kRowThreads / 32];
+    const bool in_regs = vpr <= int64_t(kRowThreads) * kRowRegs;
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const uint4* xr = x + m * vpr;
         float amax = 0.0f;
-        for (int64_t v = threadIdx.x; v < vpr; v += kRowThreads) {
-            float f[8];
-            unpack8(__ldg(xr + v), f);
-            amax = fmaxf(amax, qm::amax8(f));
+        uint4 w[kRowRegs];
+        if (in_regs) {
+#pragma unroll
+            for (int i = 0; i < kRowRegs; ++i) {   // all loads in flight before any use
+                const int64_t v = threadIdx.x + int64_t(i) * kRowThreads;
+                w[i] = v < vpr ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < kRowRegs; ++i) {
+                float f[8];
+                unpack8(w[i], f);
+                amax = fmaxf(amax, qm::amax8(f));
+            }
+        } else {
+            for (int64_t v = threadIdx.x; v < vpr; v += kRowThreads) {
+                float f[8];
+                unpack8(__ldg(xr + v), f);
+                amax = fmaxf(amax, qm::amax8(f));
+            }
         }
         const float s = group_scale(block_max(amax, red), false);
         if (threadIdx.x == 0) xs[m] = s;
-        for (int64_t v = threadIdx.x; v < vpr; v += kRowThreads) {
+        if (in_regs) {
+#pragma unroll
+            for (int i = 0; i < kRowRegs; ++i) {
+                const int64_t v = threadIdx.x + int64_t(i) * kRowThreads;
+                if (v < vpr) {
+                    float f[8];
+                    unpack8(w[i], f);
+                    xq[m * vpr + v] = quantize8(f, s, false);
+                }
+            }
+        } else {
+            for (int64_t v = threadIdx.x; v < vpr; v += kRowThreads) {
+                float f[8];
+                unpack8(__ldg(xr + v), f);
+                xq[m * vpr + v] = quantize8(f, s, false);
+            }
+        }
+    }
+}
+
+// Short rows (K <= 2048: at most 8 vectors per lane): one warp per row, the
+// whole row in registers, a shuffle-only reduction, so a CTA has eight rows in
+// flight instead of one.
+constexpr int kWarpRowRegs = 8;
+
+__global__ void __launch_bounds__(kRowThreads) quant_per_token_warp_kernel(const uint4* __restrict__ x,
+                                                                           uint2* __restrict__ xq,
+                                                                           float* __restrict__ xs, int64_t M,
+                                                                           int64_t vpr) {
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = int64_t(gridDim.x) * (kRowThreads / 32);
+    for (int64_t m = int64_t(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5); m < M; m += nw) {
+        const uint4* xr = x + m * vpr;
+        uint4 w[kWarpRowRegs];
+#pragma unroll
+        for (int i = 0; i < kWarpRowRegs; ++i) {
+            const int64_t v = lane + 32 * i;
+            w[i] = v < vpr ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kWarpRowRegs; ++i) {
             float f[8];
-            unpack8(__ldg(xr + v), f);
-            xq[m * vpr + v] = quantize8(f, s, false);
+            unpack8(w[i], f);
+            amax = fmaxf(amax, qm::amax8(f));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        const float s = group_scale(amax, false);
+        if (lane == 0) xs[m] = s;
+#pragma unroll
+        for (int i = 0; i < kWarpRowRegs; ++i) {
+            const int64_t v = lane + 32 * i;
+            if (v < vpr) {
+                float f[8];
+                unpack8(w[i], f);
+                xq[m * vpr + v] = quantize8(f, s, false);
+            }
         }
     }
 }
@@ -355,12 +432,24 @@ sgq_status launch_quant_per_token(const void* x, int64_t M, int64_t K, void* xq,
     DeviceInfo di;
     sgq_status rc = device_info(&di);
     if (rc != SGQ_OK) return rc;
-    const int64_t cap = int64_t(di.sm_count) * 8;
-    const int blocks = static_cast<int>(M < cap ? M : cap);
+    const int64_t vpr = K / 8;
     cudaLaunchAttribute attr[1];
+    if (vpr <= 32 * kWarpRowRegs) {   // a warp per row
+        const int64_t want = (M + kRowThreads / 32 - 1) / (kRowThreads / 32);
+        const int64_t cap = int64_t(di.sm_count) * 8;
+        cudaLaunchConfig_t cfg = pdl_config(attr, static_cast<int>(want < cap ? want : cap), st);
+        if (cudaLaunchKernelEx(&cfg, quant_per_token_warp_kernel, static_cast<const uint4*>(x),
+                               static_cast<uint2*>(xq), xs, M, vpr) != cudaSuccess)
+            return SGQ_ERR_CUDA;
+        note_launch();
+        return SGQ_OK;
+    }
+    // one CTA per row (the hardware balances the waves), capped for huge M
+    const int64_t cap = int64_t(1) << 20;
+    const int blocks = static_cast<int>(M < cap ? M : cap);
     cudaLaunchConfig_t cfg = pdl_config(attr, blocks, st);
     if (cudaLaunchKernelEx(&cfg, quant_per_token_kernel, static_cast<const uint4*>(x), static_cast<uint2*>(xq), xs,
-                           M, K / 8) != cudaSuccess)
+                           M, vpr) != cudaSuccess)
         return SGQ_ERR_CUDA;
     note_launch();
     return SGQ_OK;
