@@ -106,6 +106,7 @@ struct Plan {
     bool swap;
     bool pair;   // CTA pairs on 256 x 256 tiles (cluster of two, cta_group::2)
     bool alt;    // 128 x 256 tiles with two alternating MMA issuers
+    bool ck;     // swap-AB with two K splits exchanged inside a cluster of two
     int bn, tiles_r, tiles_c, kb_total, kb_per_split, splits, items, grid;
 };
 
@@ -166,6 +167,14 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count) {
     // [*,128] recipe with long K (4096 x 7168 x 7168: 207 -> 185 us), slower for
     // [*,32] (the single scale warp's conversion then bounds the stage) and for
     // short K (per-tile costs dominate).  SGQ_ALT=0/1 forces it off/on.
+    // Two K splits of a swap-AB tile can run as a cluster of two that sums
+    // the partials in shared memory instead of through the global workspace.
+    // Measured faster when a CTA takes several items (24576 x 1536 at M = 16:
+    // 15.8 -> 13.2 us), level or slower with one item per CTA (7168 x 2048 at
+    // M = 32: 9.85 -> 10.24 us).  SGQ_CK=0/1 forces it off/on.
+    static const int ck_env = env_int("SGQ_CK", -1);
+    const bool ck_ok = p.swap && p.splits == 2 && p.bn <= 32;
+    p.ck = ck_ok && (ck_env < 0 ? p.items > p.grid : ck_env != 0);
     static const int alt_env = env_int("SGQ_ALT", -1);
     const bool alt_auto = blk_k == 128 && p.kb_total >= 32;
     p.alt = !p.swap && !p.pair && (alt_env < 0 ? alt_auto : alt_env != 0);
@@ -363,7 +372,8 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
                                      p.swap ? p.bn : p.bn / blk_n, gcols) != SGQ_OK))
             return SGQ_ERR_CUDA;
     }
-    const Variant v{p.swap, p.pair, p.alt, scale_tma, fuse != nullptr, chan != nullptr, p.bn};
+    const Variant v{p.swap, p.pair, p.alt, scale_tma, fuse != nullptr, chan != nullptr,
+                    p.ck && !fuse && !chan, p.bn};
     if (chan) return dispatch_chan(v, maps, a, fz, p.grid, st);
     if (blk_n == 32 && blk_k == 32) return dispatch_32_32(v, maps, a, fz, p.grid, st);
     if (blk_n == 32 && blk_k == 128) return dispatch_32_128(v, maps, a, fz, p.grid, st);

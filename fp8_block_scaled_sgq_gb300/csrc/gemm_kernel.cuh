@@ -274,7 +274,7 @@ __device__ __forceinline__ uint32_t sf_word(const float* row, int kcol, uint32_t
 }
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair,
-          bool kAlt, bool kFuse, bool kChan>
+          bool kAlt, bool kFuse, bool kChan, bool kCK>
 struct Cfg {
     // Swap-AB tiles are narrow (N <= 64): an MMA costs about as much to issue
     // as a full-width one, so two warps issue alternate K stages of each item
@@ -349,10 +349,15 @@ struct Cfg {
     static constexpr size_t kOffSf = kOffB + size_t(kStages) * kBBytes;
     static constexpr size_t kOffGrp = kOffSf + size_t(kStages) * sizeof(Slot);
     static constexpr size_t kOffInfo = kOffGrp + (kScaleTma ? size_t(kGBufs) * sizeof(Group) : 0);
-    static constexpr size_t kOffBar = kOffInfo + size_t(kAccSets * kAccBufs) * sizeof(Info<BN>);
+    // Split-K over a cluster of two (kCK): split 1's fp32 partial tile goes to
+    // split 0's shared memory in one bulk copy (both CTAs hold this buffer).
+    static constexpr int kCKBytes = kCK ? kBM * BN * 4 : 0;
+    static constexpr size_t kOffCK = kOffInfo + size_t(kAccSets * kAccBufs) * sizeof(Info<BN>);
+    static constexpr size_t kOffBar = kOffCK + size_t(kCKBytes);
     static constexpr int kHandBar0 = 3 * kStages + (2 * kAccBufs + 1) * kMmaWarps + 2 * kGBufs;
     static constexpr int kQBar0 = kHandBar0 + (kAlt ? 2 : 0);
-    static constexpr int kNumBars = kQBar0 + (kFuse ? kStages : 0);
+    static constexpr int kCKBar0 = kQBar0 + (kFuse ? kStages : 0);
+    static constexpr int kNumBars = kCKBar0 + (kCK ? 2 : 0);
     static constexpr size_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr size_t kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
@@ -360,6 +365,8 @@ struct Cfg {
     static_assert(!kAlt || (!kSwap && !kPair), "alternating issuers: single-CTA wide tiles");
     static_assert(!kFuse || (kSwap && kScaleTma), "fused quantisation: swap-AB tiles with TMA scale groups");
     static_assert(!kChan || (!kPair && !kAlt && !kFuse && !kScaleTma), "per-channel scaling: plain tiles");
+    static_assert(!kCK || (kSwap && !kPair && !kAlt), "cluster split-K: swap-AB tiles");
+    static_assert(kOffCK % 16 == 0, "bulk-copy buffer alignment");
     static_assert(kOffSf % 128 == 0, "scale slots aligned");
     static_assert(!kTwoPerSm || kSmem <= 113 * 1024, "two CTAs per SM: shared memory");
     static_assert(!kSwap || BN <= 64, "swap-AB token tile");
@@ -374,14 +381,14 @@ struct Cfg {
 };
 
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair,
-          bool kAlt, bool kFuse, bool kChan>
+          bool kAlt, bool kFuse, bool kChan, bool kCK>
 __global__ void __launch_bounds__(
-    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>::kThreads),
-    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>::kMinBlocks))
+    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan, kCK>::kThreads),
+    (Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan, kCK>::kMinBlocks))
     fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                           const GemmArgs a, const ExtArgs fz) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>;
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan, kCK>;
     constexpr int kCG = C::kCG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -412,6 +419,9 @@ __global__ void __launch_bounds__(
     auto hand_bar = [&](uint32_t w) { return bar0 + 8u * (C::kHandBar0 + w); };
     // fused quantisation: stage s's codes and scales written (epilogue warps)
     auto qdone_bar = [&](int s) { return bar0 + 8u * (C::kQBar0 + s); };
+    // cluster split-K: partial landed in split 0 / split 0 done reading (in split 1)
+    auto ckfull_bar = [&]() { return bar0 + 8u * C::kCKBar0; };
+    auto ckfree_bar = [&]() { return bar0 + 8u * (C::kCKBar0 + 1); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -452,6 +462,10 @@ __global__ void __launch_bounds__(
         }
         if constexpr (kFuse)
             for (int s = 0; s < kStages; ++s) ptx::mbar_init(qdone_bar(s), C::kQW);
+        if constexpr (kCK) {
+            ptx::mbar_init(ckfull_bar(), 1);   // split 0's expect_tx; the bulk copy brings the bytes
+            ptx::mbar_init(ckfree_bar(), 1);   // split 0's remote arrive
+        }
         misc[1] = 0;
         misc[4] = 0;
         misc[5] = 0;
@@ -471,7 +485,12 @@ __global__ void __launch_bounds__(
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (kPair) ptx::cluster_sync();   // both CTAs' barriers exist before any remote arrive
+    // Both CTAs' barriers exist before any remote arrive.  Cluster split-K
+    // only arrives here and waits just before its first remote operation (in
+    // the epilogue, or at exit): the weight stream does not wait on the peer.
+    if (kPair) ptx::cluster_sync();
+    if (kCK) ptx::cluster_arrive_relaxed();
+    bool ck_wait_pending = kCK;
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
     if (threadIdx.x == 0) {
@@ -1397,7 +1416,56 @@ __global__ void __launch_bounds__(
             const int row0 = kSwap ? it.tr * kBM : a_row0(it), col0 = it.tc * BN;
             const int grow = row0 + r_in_tile;   // global row of the MMA A operand
             bool store = true;
-            if (a.splits > 1) {
+            if (kCK && a.splits > 1) {
+                // The two K splits of the tile are the two CTAs of this cluster
+                // (item = tile * 2 + split, cluster = items 2c and 2c + 1).  Split
+                // 1 stages its fp32 partial in its own shared memory and sends
+                // it to split 0's in one bulk copy, which completes split 0's
+                // barrier; split 0 adds p_0 + p_1 (split order, as the global
+                // path) and stores.  Split 0 frees the buffer with a remote
+                // arrive before split 1 may send the next item's partial.
+                if (ck_wait_pending) {
+                    ptx::cluster_wait();
+                    ck_wait_pending = false;
+                }
+                float* ckbuf = reinterpret_cast<float*>(smem + C::kOffCK);
+                const uint32_t ckbuf_s = ptx::smem_u32(ckbuf);
+                const uint32_t ck_rank = ptx::cluster_rank();
+                bool ck_ok = true;
+                if (ck_rank == 1u) {
+                    if (n_items > 0)
+                        ck_ok = wait_bar_warp<true>(ckfree_bar(), (n_items - 1) & 1u, sync, 7, true);
+                    if (ck_ok) {
+#pragma unroll
+                        for (int c = 0; c < kCols; c += 4)
+                            *reinterpret_cast<float4*>(ckbuf + epi_tid * kCols + c) =
+                                make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                        ptx::fence_proxy_async_smem();   // read by the bulk copy (async proxy)
+                    }
+                    if (epi_any<C::kEpiWarps * 32>(!ck_ok)) break;
+                    if (epi_tid == 0)
+                        ptx::bulk_copy_to_cluster_if(1u, ptx::mapa(ckbuf_s, 0u), ckbuf_s, C::kCKBytes,
+                                                     ptx::mapa(ckfull_bar(), 0u));
+                    store = false;
+                } else {
+                    if (epi_tid == 0) ptx::mbar_arrive_expect_tx(ckfull_bar(), C::kCKBytes);
+                    ck_ok = wait_bar_warp<true>(ckfull_bar(), n_items & 1u, sync, 7, true);
+                    if (ck_ok) {
+#pragma unroll
+                        for (int c = 0; c < kCols; c += 4) {
+                            const float4 v = *reinterpret_cast<const float4*>(ckbuf + epi_tid * kCols + c);
+                            acc[c] += v.x;
+                            acc[c + 1] += v.y;
+                            acc[c + 2] += v.z;
+                            acc[c + 3] += v.w;
+                        }
+                    }
+                    if (epi_any<C::kEpiWarps * 32>(!ck_ok)) break;   // (also: every thread has read)
+                    // the peer waits for the buffer only before a next item
+                    if (epi_tid == 0 && it.item + it.step < a.items)
+                        ptx::mbar_arrive_cluster_if(1u, ptx::mapa(ckfree_bar(), 1u));
+                }
+            } else if (a.splits > 1) {
                 // fp32 partial of this split; the last split to arrive sums all
                 // partials in split order (deterministic) and stores the tile.
                 // Rows past the operand's end carry nothing: neither written nor read.
@@ -1532,7 +1600,16 @@ __global__ void __launch_bounds__(
     if (threadIdx.x == 0) trace_ev(a, 255);
     // A pair's leader writes the peer's TMEM and reads its shared memory until
     // its drain completes: neither CTA leaves before both are here.
+    // no CTA of a cluster leaves while the other may still address its shared memory
     if (kPair) ptx::cluster_sync();
+    if (kCK) {
+        // No remote arrive is in flight (the last item sends none) and split
+        // 0 has seen split 1's last bulk copy land, so execution order is all
+        // that is left to enforce.
+        if (ck_wait_pending) ptx::cluster_wait();
+        ptx::cluster_arrive_relaxed();
+        ptx::cluster_wait();
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc_g<kCG>(tmem, C::kTmemCols);
@@ -1542,10 +1619,12 @@ __global__ void __launch_bounds__(
 // Launches one instantiation with programmatic stream serialisation (CTA
 // pairs: as clusters of two, at most as many pairs as can be resident).
 template <int BN, int kStages, bool kSwap, int kAccBufs, int kBlkN, int kBlkK, bool kScaleTma, bool kPair = false,
-          bool kAlt = false, bool kFuse = false, bool kChan = false>
+          bool kAlt = false, bool kFuse = false, bool kChan = false, bool kCK = false>
 sgq_status run(const CUtensorMap* maps, const GemmArgs& args, const ExtArgs& fz, int grid, cudaStream_t st) {
-    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>;
-    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan>;
+    using C = Cfg<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan, kCK>;
+    auto kern = fp8_block_gemm_kernel<BN, kStages, kSwap, kAccBufs, kBlkN, kBlkK, kScaleTma, kPair, kAlt, kFuse, kChan,
+                                      kCK>;
+    constexpr bool kCluster = kPair || kCK;
     static bool configured[64] = {};
     static int max_pairs[64] = {};
     int dev = 0;
@@ -1562,12 +1641,12 @@ sgq_status run(const CUtensorMap* maps, const GemmArgs& args, const ExtArgs& fz,
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = kPair ? 2 : 1;
+    cfg.numAttrs = kCluster ? 2 : 1;
     if (!configured[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(C::kSmem)) != cudaSuccess)
             return SGQ_ERR_CUDA;
-        if (kPair) {
+        if (kCluster) {
             cudaLaunchConfig_t q = cfg;
             q.gridDim = dim3(static_cast<unsigned>(grid));
             int n = 0;
@@ -1576,10 +1655,11 @@ sgq_status run(const CUtensorMap* maps, const GemmArgs& args, const ExtArgs& fz,
         }
         configured[dev] = true;
     }
-    if (kPair) {
+    if (kCluster) {
+        // clusters of two: a CTA pair (one item each) or the two K splits of a tile
         int pairs = grid / 2;
         if (pairs > max_pairs[dev]) pairs = max_pairs[dev];
-        if (pairs > args.items) pairs = args.items;
+        if (pairs > (kPair ? args.items : args.items / 2)) pairs = kPair ? args.items : args.items / 2;
         grid = 2 * pairs;
     }
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -1597,6 +1677,7 @@ struct Variant {
     bool scale_tma;   // scale boxes loaded by TMA
     bool fuse;        // swap-AB tiles that quantise the bf16 activations themselves
     bool chan;        // per-channel scaling (fp8_scaled_mm): unscaled MMAs, scales in the epilogue
+    bool ck;          // swap-AB split-K over clusters of two (two splits exactly)
     int bn;           // MMA N of the swap-AB tile
 };
 
@@ -1628,6 +1709,11 @@ sgq_status dispatch_tile(const Variant& v, const CUtensorMap* maps, const GemmAr
     if (!v.swap) {
         if (v.alt) return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma, false, true>(maps, a, fz, grid, st);
         return run<256, 4, false, 1, kBlkN, kBlkK, kScaleTma>(maps, a, fz, grid, st);
+    }
+    if (v.ck) {   // two splits exchanged through shared memory (BN <= 32: room for the buffer)
+        if (v.bn == 16)
+            return run<16, 8, true, 2, kBlkN, kBlkK, kScaleTma, false, false, false, false, true>(maps, a, fz, grid, st);
+        return run<32, 8, true, 2, kBlkN, kBlkK, kScaleTma, false, false, false, false, true>(maps, a, fz, grid, st);
     }
     switch (v.bn) {
         case 16: return run<16, 8, true, 2, kBlkN, kBlkK, kScaleTma>(maps, a, fz, grid, st);

@@ -274,6 +274,14 @@ __device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Split cluster barrier: a relaxed arrive (nothing to publish beyond what a
+// fence.mbarrier_init already released) and the matching wait, taken later.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Arrive (release at cluster scope) on an mbarrier given by its cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster_if(uint32_t pred, uint32_t cluster_bar) {
     asm volatile(
