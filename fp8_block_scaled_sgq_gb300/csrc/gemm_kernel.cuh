@@ -51,6 +51,10 @@ constexpr int kBM = 128;          // MMA M: rows of the "A" operand per tile
 constexpr int kBK = 128;          // K elements (bytes) per pipeline stage
 constexpr int kEpiWarp0 = 3;      // warps: 0 producer, 1 MMA, 2 scale, 3.. epilogue, then scale 2, MMA 2
 constexpr uint64_t kTimeoutNs = 1ull << 30;
+// A wait reads the (global) abort flag only once it has lasted this long: the
+// load costs a memory round trip, which a wait that is about to complete
+// would add to its latency.
+constexpr uint64_t kAbortPollNs = 20000;
 
 constexpr uint32_t kInfoPromote = 1u;
 constexpr uint32_t kInfoLast = 2u;
@@ -196,8 +200,9 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, con
     while (true) {
         if (try_wait_scoped<kCl>(bar, parity)) return true;
         if ((++spins & 15u) == 0) {
-            if (*s.abort_flag) return false;
-            if (ptx::globaltimer() - t0 > kTimeoutNs) {
+            const uint64_t dt = ptx::globaltimer() - t0;
+            if (dt > kAbortPollNs && *s.abort_flag) return false;
+            if (dt > kTimeoutNs) {
                 *s.abort_flag = 1u;
                 atomicOr(s.status, kStatusTimeout | (where << 8));
                 return false;
@@ -1304,6 +1309,9 @@ __global__ void __launch_bounds__(
         };
         while (it.valid(a)) {
             bool failed = false;
+            // read now, used after the accumulators: the load's latency hides
+            // behind the waits instead of following them
+            const bool aborted_before = *sync.abort_flag != 0u;
             if constexpr (kFuse) {
                 // Quantise this item's activation tiles before waiting for its
                 // accumulators: the loads of up to kBatch stages are issued
@@ -1380,8 +1388,9 @@ __global__ void __launch_bounds__(
                             if (!done1 && ptx::mbar_test_wait(accf_bar(1, static_cast<int>(seg1 % kAccBufs)),
                                                               (seg1 / kAccBufs) & 1u)) { pick = 1; break; }
                             if ((++spins & 15u) == 0) {
-                                if (*sync.abort_flag) break;
-                                if (ptx::globaltimer() - t0 > kTimeoutNs) {
+                                const uint64_t dt = ptx::globaltimer() - t0;
+                                if (dt > kAbortPollNs && *sync.abort_flag) break;
+                                if (dt > kTimeoutNs) {
                                     *sync.abort_flag = 1u;
                                     atomicOr(sync.status, kStatusTimeout | (4u << 8));
                                     break;
@@ -1410,7 +1419,7 @@ __global__ void __launch_bounds__(
                     for (int c = 0; c < kCols; ++c) acc[c] += acc1[c];
                 }
             }
-            if (epi_any<C::kEpiWarps * 32>(failed || *sync.abort_flag)) break;
+            if (epi_any<C::kEpiWarps * 32>(failed || aborted_before)) break;
             if (epi_tid == 0) trace_ev(a, 136 + 4 * (n_items & 15));
             // ------------------------------------------------ output
             const int row0 = kSwap ? it.tr * kBM : a_row0(it), col0 = it.tc * BN;
@@ -1492,12 +1501,10 @@ __global__ void __launch_bounds__(
                 if (epi_tid == 0) {
                     trace_ev(a, 137 + 4 * (n_items & 15));
                     // The barrier orders every epilogue thread's partial before this
-                    // fence, which releases them with the arrival; the last arriver's
-                    // fence after the atomic acquires the other splits' partials.
-                    __threadfence();
-                    const uint32_t old = atomicAdd(a.counters + it.tile, 1u);
+                    // arrival, whose release publishes them; the last arriver's
+                    // acquire makes the other splits' partials visible.
+                    const uint32_t old = ptx::atom_add_acq_rel_gpu(a.counters + it.tile, 1u);
                     const bool last_split = old == static_cast<uint32_t>(a.splits - 1);
-                    if (last_split) __threadfence();
                     misc[2] = last_split ? 1u : 0u;
                 }
                 epi_sync<C::kEpiWarps * 32>();
