@@ -616,25 +616,37 @@ __global__ void __launch_bounds__(
                 ++npre;
             }
             if (lane == 0) trace_ev(a, 2);
-            ptx::grid_dependency_wait();
-            if (lane == 0) trace_ev(a, 1);
-            for (int s = 0; s < npre && group_ok; ++s) {
-                if constexpr (!kFuse) {
-                    load_group(it);
-                    load_x(s, it);
+            // Without a weight prefetch the wait sits inside the first loop
+            // iteration, after that stage's weight load: the loop's code is
+            // fetched while the warp waits, not after.
+            bool dep_waited = npre > 0;
+            if (dep_waited) {
+                ptx::grid_dependency_wait();
+                if (lane == 0) trace_ev(a, 1);
+                for (int s = 0; s < npre && group_ok; ++s) {
+                    if constexpr (!kFuse) {
+                        load_group(it);
+                        load_x(s, it);
+                    }
+                    it.next(a);
                 }
-                it.next(a);
             }
             if (lane == 0) trace_ev(a, 3);
             int stage = npre % kStages;
             uint32_t phase = npre / kStages;
             int nj = npre;
             while (it.valid(a) && group_ok) {
+                if (lane == 0 && nj == npre) trace_ev(a, 5);
                 if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 1)) break;
                 if (lane == 0) trace_ev(a, 8 + (nj & 31));
                 ++nj;
-                load_group(it);
                 load_w(stage, it);
+                if (!dep_waited) {
+                    ptx::grid_dependency_wait();
+                    dep_waited = true;
+                    if (lane == 0) trace_ev(a, 1);
+                }
+                load_group(it);
                 load_x(stage, it);
                 it.next(a);
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -1402,6 +1414,7 @@ __global__ void __launch_bounds__(
                     pick = __shfl_sync(0xFFFFFFFFu, pick, 0);
                     __syncwarp();
                     if (pick < 0) { failed = true; break; }
+                    if (epi_tid == 0) trace_ev(a, 139 + 4 * (n_items & 15));   // (the last pick stays)
                     ptx::tc_fence_after();
                     if (pick == 0) {
                         done0 = consume(0, seg0, first0, acc);
@@ -1455,10 +1468,12 @@ __global__ void __launch_bounds__(
                     if (epi_tid == 0)
                         ptx::bulk_copy_to_cluster_if(1u, ptx::mapa(ckbuf_s, 0u), ckbuf_s, C::kCKBytes,
                                                      ptx::mapa(ckfull_bar(), 0u));
+                    if (epi_tid == 0) trace_ev(a, 137 + 4 * (n_items & 15));
                     store = false;
                 } else {
                     if (epi_tid == 0) ptx::mbar_arrive_expect_tx(ckfull_bar(), C::kCKBytes);
                     ck_ok = wait_bar_warp<true>(ckfull_bar(), n_items & 1u, sync, 7, true);
+                    if (epi_tid == 0) trace_ev(a, 137 + 4 * (n_items & 15));
                     if (ck_ok) {
 #pragma unroll
                         for (int c = 0; c < kCols; c += 4) {
