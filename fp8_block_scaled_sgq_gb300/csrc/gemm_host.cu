@@ -115,41 +115,68 @@ int env_int(const char* name, int dflt) {
     return v ? std::atoi(v) : dflt;
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count) {
+// wide_only: keep the 128 x 256 tiles for M > 64 (the issue-mode testing
+// flags compare the wide tiles' two issue modes).
+Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, bool wide_only = false) {
     Plan p{};
     static const int grid_max = env_int("SGQ_GRID_MAX", 0);
     if (grid_max > 0 && grid_max < sm_count) sm_count = grid_max;
     static const int swap_max = env_int("SGQ_SWAP_MAX", 64);
-    p.swap = M <= swap_max;
-    p.bn = p.swap ? (M <= 16 ? 16 : (M <= 32 ? 32 : 64)) : 256;
-    const int64_t rows = p.swap ? N : M, cols = p.swap ? M : N;
-    p.tiles_r = static_cast<int>((rows + kBM - 1) / kBM);
-    p.tiles_c = static_cast<int>((cols + p.bn - 1) / p.bn);
-    p.kb_total = static_cast<int>((K + kBK - 1) / kBK);
-    const int64_t tiles = int64_t(p.tiles_r) * p.tiles_c;
+    static const int mid_swap = env_int("SGQ_MIDSWAP", 1);
     static const int ovh = env_int("SGQ_SPLIT_OVERHEAD", 2);
     static const int forced = env_int("SGQ_SPLITS", 0);
-    int best_s = 1;
-    double best = 1e300;
+    p.kb_total = static_cast<int>((K + kBK - 1) / kBK);
     const int max_s = p.kb_total < 32 ? p.kb_total : 32;
+    auto tiles_of = [&](bool swap, int bn) {
+        const int64_t rows = swap ? N : M, cols = swap ? M : N;
+        return ((rows + kBM - 1) / kBM) * ((cols + bn - 1) / bn);
+    };
+    // Best split count of a tile shape, and its cost in K stages of that shape.
     // Wide tiles keep one split: their single accumulator buffer serialises a
     // split's epilogue with the next item's MMAs, and the measured split-K
-    // runs were slower (2048 x 1536 x 7168: 44.6 us unsplit, 88.8 us in three).
-    const int max_split = (p.swap || forced > 0) ? max_s : 1;   // SGQ_SPLITS may still force one
-    for (int s = 1; s <= max_split; ++s) {
-        const int kbp = (p.kb_total + s - 1) / s;
-        if ((p.kb_total + kbp - 1) / kbp != s) continue;   // every split non-empty
-        const int64_t items = tiles * s;
-        if (s > 1 && (tiles > kMaxCounters ||
-                      size_t(items) * kBM * p.bn * sizeof(float) > kWsBytes))
-            continue;
-        const int64_t waves = (items + sm_count - 1) / sm_count;
-        const double cost = double(waves) * (kbp + ovh) + (s > 1 ? 0.5 : 0.0);
-        if (forced > 0 ? s == forced : cost < best) {
-            best = cost;
-            best_s = s;
+    // runs were slower (2048 x 1536 x 7168: 44.6 us unsplit, 88.8 us in three;
+    // 128 x 1536 x 7168: 35 us unsplit, 64 us in four).
+    auto best_split = [&](bool swap, int bn, double* cost_out) {
+        const int64_t tiles = tiles_of(swap, bn);
+        const int max_split = (swap || forced > 0) ? max_s : 1;   // SGQ_SPLITS may still force one
+        int best_s = 1;
+        double best = 1e300;
+        for (int s = 1; s <= max_split; ++s) {
+            const int kbp = (p.kb_total + s - 1) / s;
+            if ((p.kb_total + kbp - 1) / kbp != s) continue;   // every split non-empty
+            const int64_t items = tiles * s;
+            if (s > 1 && (tiles > kMaxCounters ||
+                          size_t(items) * kBM * bn * sizeof(float) > kWsBytes))
+                continue;
+            const int64_t waves = (items + sm_count - 1) / sm_count;
+            const double cost = double(waves) * (kbp + ovh) + (s > 1 ? 0.5 : 0.0);
+            if (forced > 0 ? s == forced : cost < best) {
+                best = cost;
+                best_s = s;
+            }
+        }
+        if (cost_out) *cost_out = best;
+        return best_s;
+    };
+    p.swap = M <= swap_max;
+    p.bn = p.swap ? (M <= 16 ? 16 : (M <= 32 ? 32 : 64)) : 256;
+    // Mid M with few wide tiles (128 x 1536 x 7168: 6 tiles for 152 SMs):
+    // swap-AB tiles of 64 tokens can split K where the wide tiles cannot.  A
+    // 128 x 64 K stage (four N=64 MMAs, bound by their issue) takes about
+    // 1/1.8 of a 128 x 256 one; the cheaper plan wins.
+    if (!p.swap && !wide_only && mid_swap != 0 && M <= 1024) {
+        double c_wide = 0.0, c_swap = 0.0;
+        best_split(false, 256, &c_wide);
+        best_split(true, 64, &c_swap);
+        if (c_swap < 1.8 * c_wide) {
+            p.swap = true;
+            p.bn = 64;
         }
     }
+    p.tiles_r = static_cast<int>(((p.swap ? N : M) + kBM - 1) / kBM);
+    p.tiles_c = static_cast<int>(((p.swap ? M : N) + p.bn - 1) / p.bn);
+    const int64_t tiles = int64_t(p.tiles_r) * p.tiles_c;
+    const int best_s = best_split(p.swap, p.bn, nullptr);
     p.splits = best_s;
     p.kb_per_split = (p.kb_total + best_s - 1) / best_s;
     p.items = static_cast<int>(tiles * best_s);
@@ -270,7 +297,7 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     sgq_status rc = device_info(&di);
     if (rc != SGQ_OK) return rc;
     if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
-    Plan p = make_plan(M, N, K, blk_k, di.sm_count);
+    Plan p = make_plan(M, N, K, blk_k, di.sm_count, (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0);
     if (flags & SGQ_GEMM_ISSUE_ALT) p.alt = !p.swap && !p.pair;
     if (flags & SGQ_GEMM_ISSUE_SINGLE) p.alt = false;
     if (chan) {   // plain tiles: no scale boxes, one issuer
@@ -279,7 +306,8 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     }
     const int64_t ks_all = K / blk_k;
     const bool scale_tma_ok = (ks_all % 4) == 0 && ks_all >= (blk_k == 128 ? 8 : 16);
-    if (fuse && !(p.swap && scale_tma_ok)) return SGQ_ERR_UNSUPPORTED;
+    // fused quantisation: swap-AB tiles of at most 64 tokens (the documented domain)
+    if (fuse && !(p.swap && M <= 64 && scale_tma_ok)) return SGQ_ERR_UNSUPPORTED;
     GemmArgs a{};
     a.As = As;
     a.Ws = Ws;

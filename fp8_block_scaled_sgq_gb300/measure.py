@@ -10,6 +10,16 @@ PATH is one of
   scaled_mm         sgq_fp8_scaled_mm, per-row x per-column scales, bias   (TFLOP/s and GB/s)
   block_gemm        sgq_fp8_block_gemm with [B, B] blocks, UE8M0           (TFLOP/s and GB/s)
   linear            sgq_fp8_block_linear with [B, B] blocks, UE8M0         (GB/s of x + W + D)
+  pair              sgq_quant_token_group then sgq_fp8_block_gemm, back to back on one stream
+                    (programmatic dependent launch), [B, B] blocks, UE8M0  (TFLOP/s; GB/s of the
+                    quantiser's and the GEMM's algorithmic bytes)
+
+    python -m fp8_block_scaled_sgq_gb300.measure --sweep [--reps R]
+
+times `pair` and `block_gemm` on every case of the M = 1..8192 sweep (N, K in
+{(24576, 1536), (1536, 7168)}, [128, 128] and [32, 32] blocks) and prints one
+JSON line per case, then a markdown table with each time's fraction of the
+roofline min(FP8 peak, arithmetic intensity x HBM peak) from the measured peaks.
 
 Timing: CUDA events around one replay of a CUDA graph holding `reps` calls on
 one stream, after a warm-up replay; weights (and, for the quantisers, inputs)
@@ -29,17 +39,61 @@ from . import binding, synth
 L2_BYTES = 129 * 2 ** 20
 
 
+PATHS = ["quant_per_token", "quant_per_tensor", "quant_v2", "scaled_mm", "block_gemm", "linear", "pair"]
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("path", choices=["quant_per_token", "quant_per_tensor", "quant_v2", "scaled_mm", "block_gemm",
-                                     "linear"])
-    ap.add_argument("M", type=int)
-    ap.add_argument("N", type=int)
-    ap.add_argument("K", type=int)
+    ap.add_argument("path", nargs="?", choices=PATHS)
+    ap.add_argument("M", type=int, nargs="?")
+    ap.add_argument("N", type=int, nargs="?")
+    ap.add_argument("K", type=int, nargs="?")
     ap.add_argument("--blk", type=int, default=128)
     ap.add_argument("--reps", type=int, default=50)
+    ap.add_argument("--sweep", action="store_true")
     args = ap.parse_args()
-    M, N, K, blk = args.M, args.N, args.K, args.blk
+    if args.sweep:
+        sweep(args.reps)
+        return
+    if args.path is None or args.K is None:
+        ap.error("PATH M N K are required without --sweep")
+    print(json.dumps(measure(args.path, args.M, args.N, args.K, args.blk, args.reps)), flush=True)
+
+
+def peaks() -> tuple:
+    """(HBM GB/s, FP8 TFLOP/s): the measured copy bandwidth and 2 x the measured bf16 rate."""
+    import os
+    p = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), 2.0 * float(d["bf16_tflops"])
+    return 6800.0, 3800.0
+
+
+def sweep(reps: int) -> None:
+    hbm, fp8 = peaks()
+    rows = []
+    for c in synth.WORKLOADS["sweep"]:
+        for path in ("pair", "block_gemm"):
+            r = measure(path, c.M, c.N, c.K, c.blk_k, reps)
+            flops = 2.0 * c.M * c.N * c.K
+            nbytes = c.gemm_bytes() + (c.quant_bytes() if path == "pair" else 0.0)
+            t_roof = max(flops / (fp8 * 1e12), nbytes / (hbm * 1e9)) * 1e6
+            r["roofline_frac"] = round(t_roof / r["us"], 3)
+            r["bound"] = "fp8" if flops / (fp8 * 1e12) > nbytes / (hbm * 1e9) else "hbm"
+            print(json.dumps(r), flush=True)
+            rows.append(r)
+    print("\n| N | K | blk | M | quant + GEMM us | GEMM us | GEMM TFLOP/s | GEMM GB/s | bound | "
+          "pair / GEMM fraction of roofline |")
+    print("|---|---|---|---|---|---|---|---|---|---|")
+    for i in range(0, len(rows), 2):
+        p, g = rows[i], rows[i + 1]
+        print(f"| {g['N']} | {g['K']} | {g['blk']} | {g['M']} | {p['us']:.2f} | {g['us']:.2f} | {g['tflops']:.1f} | "
+              f"{g['gbs']:.0f} | {g['bound']} | {p['roofline_frac']:.2f} / {g['roofline_frac']:.2f} |")
+
+
+def measure(path: str, M: int, N: int, K: int, blk: int, reps: int) -> dict:
+    args = argparse.Namespace(path=path, reps=reps)
     dev = torch.device("cuda:0")
     st = torch.cuda.Stream()
     s = st.cuda_stream
@@ -96,6 +150,17 @@ def main() -> None:
                     calls.append(lambda sp, r=r: binding.sgq_fp8_block_gemm(aq, as_, wrot[r][0], wrot[r][1], d, M, N,
                                                                            K, blk, blk, sp))
                 moved = M * K + 4 * M * (K // blk) + N * K + 4 * nb * kb + 2 * M * N
+            elif args.path == "pair":
+                aq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+                as_ = torch.empty((M, K // blk), dtype=torch.float32, device=dev)
+
+                def pair_call(sp, r):
+                    binding.sgq_quant_token_group(x, M, K, blk, 1, aq, as_, sp)
+                    binding.sgq_fp8_block_gemm(aq, as_, wrot[r][0], wrot[r][1], d, M, N, K, blk, blk, sp)
+                for r in range(n_rot):
+                    calls.append(lambda sp, r=r: pair_call(sp, r))
+                moved = (2 * M * K + M * K + 4 * M * (K // blk)) + (M * K + 4 * M * (K // blk) + N * K
+                                                                    + 4 * nb * kb + 2 * M * N)
             else:
                 for r in range(n_rot):
                     calls.append(lambda sp, r=r: binding.sgq_fp8_block_linear(x, 1, wrot[r][0], wrot[r][1], d, M, N,
@@ -129,8 +194,10 @@ def main() -> None:
     out = {"path": args.path, "M": M, "N": N, "K": K, "us": round(us, 3), "gbs": round(moved / us / 1e3, 1)}
     if flops:
         out["tflops"] = round(flops / us / 1e6, 2)
-        out["blk"] = blk if args.path in ("block_gemm", "linear") else None
-    print(json.dumps(out), flush=True)
+        out["blk"] = blk if args.path in ("block_gemm", "linear", "pair") else None
+    del calls, g
+    torch.cuda.empty_cache()
+    return out
 
 
 if __name__ == "__main__":

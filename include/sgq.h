@@ -57,7 +57,9 @@ typedef enum {
 #define SGQ_GEMM_FORCE_PROMOTE 1u
 /* Wide tiles (M > 64) only: force two alternating MMA-issuing warps, or a
  * single one, instead of the launch plan's choice.  Both issue the same MMA
- * sequence, so the result is bit-identical either way; meant for testing. */
+ * sequence, so the result is bit-identical either way; meant for testing.
+ * Either flag also keeps 64 < M <= 1024 on the wide tiles where the plan
+ * would take swap-AB tiles of 64 tokens. */
 #define SGQ_GEMM_ISSUE_ALT 2u
 #define SGQ_GEMM_ISSUE_SINGLE 4u
 

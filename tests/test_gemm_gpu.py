@@ -133,7 +133,7 @@ def test_pair_tile_one_half_not_pow2(rows, bk):
     check_gemm(run_gpu(aq, a_s, wq, ws, bn, bk), dref, bound, f"half rows={rows} bk={bk}")
 
 
-@pytest.mark.parametrize("M", [1, 16, 64, 4096])
+@pytest.mark.parametrize("M", [1, 16, 64, 128, 4096])
 def test_deterministic(M):
     """Split-K sums partials in a fixed order: repeated calls are bitwise equal."""
     N, K = 7168, 2048
