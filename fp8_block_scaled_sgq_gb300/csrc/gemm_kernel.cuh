@@ -1583,7 +1583,25 @@ __global__ void __launch_bounds__(
                 }
             }
             if (store && !kSwap) {
-                if (grow < a.M) {
+                // A thread owns one row: 32-byte stores (a full sector per row
+                // and half the store instructions) when D's rows allow them.
+                // The 16-byte stores measured 16% of a short-K GEMM's time
+                // (8192 x 24576 x 1536: 410 us, 344 us without any D store).
+                const bool v8 = (kCols % 16 == 0) &&
+                                ((reinterpret_cast<uintptr_t>(a.D) | (static_cast<uintptr_t>(a.N) * 2u)) & 31u) == 0;
+                if (grow < a.M && v8) {
+                    __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
+#pragma unroll
+                    for (int c = 0; c < kCols; c += 16) {
+                        const int gcol = col0 + c_begin + c;
+                        if (gcol < a.N) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(acc[c + 2 * i], acc[c + 2 * i + 1]);
+                            ptx::st_global_v8(drow + gcol, w);
+                        }
+                    }
+                } else if (grow < a.M) {
                     __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
 #pragma unroll
                     for (int c = 0; c < kCols; c += 8) {

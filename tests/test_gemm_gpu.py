@@ -210,3 +210,24 @@ def test_alternating_issuers_prefill_block128():
     d_one = sgq.fp8_block_gemm(*args, c.blk_n, c.blk_k, flags=sgq.SGQ_GEMM_ISSUE_SINGLE)
     assert sgq.sgq_device_status() == 0
     assert torch.equal(d_alt, d_one)
+
+
+@pytest.mark.parametrize("M,N,K,bk", [(300, 1024, 1024, 128), (200, 512, 2048, 32)])
+def test_wide_tile_store_alignment(M, N, K, bk):
+    """Wide tiles store D rows with 32-byte stores when D's base and row pitch
+    allow them, else with 16-byte ones: a D that starts 16 bytes past a 32-byte
+    boundary must give the same result as an aligned one."""
+    c = synth.Case("align", M, N, K, bk, bk, True, seed=M + K)
+    aq, a_s = oracle.quant_token_group(c.x(), bk, True)
+    wq, ws = weights(N, K, bk, bk, True)
+    args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+    d0 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    buf = torch.empty(M * N + 16, dtype=torch.bfloat16, device="cuda")
+    d1 = buf[8:8 + M * N].view(M, N)   # 16 bytes past the allocation's alignment
+    assert d1.data_ptr() % 32 == 16
+    for d in (d0, d1):
+        sgq.sgq_fp8_block_gemm_ex(*args, d, M, N, K, bk, bk, sgq.SGQ_GEMM_ISSUE_SINGLE)
+        assert sgq.sgq_device_status() == 0
+    assert torch.equal(d0, d1)
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, bk, bk)
+    check_gemm(d1, dref, bound, f"unaligned D M={M} N={N}")
