@@ -163,12 +163,14 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, bool wi
     // Mid M with few wide tiles (128 x 1536 x 7168: 6 tiles for 152 SMs):
     // swap-AB tiles of 64 tokens can split K where the wide tiles cannot.  A
     // 128 x 64 K stage (four N=64 MMAs, bound by their issue) takes about
-    // 1/1.8 of a 128 x 256 one; the cheaper plan wins.
+    // 1/1.8 of a 128 x 256 one, 1/1.5 where the wide tiles run two alternating
+    // issuers ([*,128], long K); the cheaper plan wins.
     if (!p.swap && !wide_only && mid_swap != 0 && M <= 1024) {
         double c_wide = 0.0, c_swap = 0.0;
         best_split(false, 256, &c_wide);
         best_split(true, 64, &c_swap);
-        if (c_swap < 1.8 * c_wide) {
+        const double wide_stage = (blk_k == 128 && p.kb_total >= 32) ? 1.5 : 1.8;
+        if (c_swap < wide_stage * c_wide) {
             p.swap = true;
             p.bn = 64;
         }
