@@ -1526,16 +1526,32 @@ __global__ void __launch_bounds__(
                 store = misc[2] != 0u;
                 if (store && live) {
                     if (kSwap) {
-                        // p_0 + p_1 + ... in split order; this split's own term from registers
+                        // p_0 + p_1 + ... in split order; this split's own term from
+                        // registers.  The loads of kSB splits go out before their
+                        // adds: one L2 round trip per kSB splits, not per split.
+                        constexpr int kSB = kCols <= 8 ? 4 : (kCols <= 16 ? 2 : 1);
                         const float* base = a.partial + tile_base + static_cast<int64_t>(c_begin) * kBM + r_in_tile;
                         float (&sum)[kCols] = acc1;   // free once the issuers' sums are combined
-                        for (int sp = 0; sp < a.splits; ++sp) {
-                            const float* p = base + static_cast<int64_t>(sp) * (BN * kBM);
-                            const bool own = sp == it.split;
+                        for (int sp0 = 0; sp0 < a.splits; sp0 += kSB) {
+                            float v[kSB][kCols];
 #pragma unroll
-                            for (int c = 0; c < kCols; ++c) {
-                                const float v = own ? acc[c] : __ldcg(p + c * kBM);
-                                sum[c] = sp == 0 ? v : sum[c] + v;
+                            for (int j = 0; j < kSB; ++j) {
+                                const int sp = sp0 + j;
+                                const bool load = sp < a.splits && sp != it.split;
+                                const float* p = base + static_cast<int64_t>(sp) * (BN * kBM);
+#pragma unroll
+                                for (int c = 0; c < kCols; ++c) v[j][c] = load ? __ldcg(p + c * kBM) : 0.0f;
+                            }
+#pragma unroll
+                            for (int j = 0; j < kSB; ++j) {
+                                const int sp = sp0 + j;
+                                if (sp < a.splits) {
+#pragma unroll
+                                    for (int c = 0; c < kCols; ++c) {
+                                        const float x = sp == it.split ? acc[c] : v[j][c];
+                                        sum[c] = sp == 0 ? x : sum[c] + x;
+                                    }
+                                }
                             }
                         }
 #pragma unroll
