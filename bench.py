@@ -12,7 +12,12 @@ Timing: inputs resident in HBM; CUDA graphs of whole steps replayed on one
 stream between CUDA events; the weights rotate over enough copies to exceed
 twice the L2 size, so every step streams its weights from HBM.  `e2e` times
 the same steps through the public API with the activation copied in from
-pinned host memory and D read back to the host inside the timed region.
+pinned host memory and D read back to the host inside the timed region: each
+step replays one CUDA graph holding the host-to-device copy of the step's
+activations (one pinned buffer), the quantisation and GEMM calls of every linear
+and the device-to-host copy of the outputs, then waits for it on the host (the
+way a decode loop runs).  `e2e.eager_ms_per_step` is the
+same step issued call by call from Python.
 
 `--impl reference` times the CPU oracle (test infrastructure) on a bounded
 sample of the same workload, on this host's cores.
@@ -306,17 +311,57 @@ def run_ours(args, ws_, rank, local):
     gpu_launches = 2 * len(cases) * args.steps   # quant + GEMM per case per step (graph replays)
     assert sgq.sgq_launch_count() == launches0   # replays do not call the library
 
-    # end to end through the public API: H2D of x, quant + GEMM, D2H of D, every step
-    hx = [x.cpu().pin_memory() for _, x, _, _, _ in per]
-    hd = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for *_, d in per]
+    # end to end through the public API: H2D of x, quant + GEMM, D2H of D, every
+    # step; the step's activations (and outputs) sit in one buffer each, so one
+    # copy per direction moves them
+    x_sizes = [x.numel() for _, x, _, _, _ in per]
+    d_sizes = [d.numel() for *_, d in per]
+    hx = torch.cat([x.reshape(-1).cpu() for _, x, _, _, _ in per]).pin_memory()
+    hd = torch.empty(sum(d_sizes), dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=device)
+    dd = torch.empty(sum(d_sizes), dtype=torch.bfloat16, device=device)
+    per_e2e, ox, od = [], 0, 0
+    for (c, x, xq, xs, d), nx, nd in zip(per, x_sizes, d_sizes):
+        per_e2e.append((c, dx[ox:ox + nx].view(x.shape), xq, xs, dd[od:od + nd].view(d.shape)))
+        ox, od = ox + nx, od + nd
+    per = per_e2e
+    hx, hd = (hx, dx), (hd, dd)
     for i in range(args.warmup):
         _e2e_step(sgq, per, wrot[i % n_rot], hx, hd, stream)   # e2e warm-up
+        stream.synchronize()
     barrier(ws_)
     t0 = time.perf_counter()
     for i in range(args.steps):
         _e2e_step(sgq, per, wrot[i % n_rot], hx, hd, stream)
-    t_e2e = (time.perf_counter() - t0) / args.steps
-    t_e2e = max_over_ranks(t_e2e, ws_, device)
+        stream.synchronize()
+    t_eager = max_over_ranks((time.perf_counter() - t0) / args.steps, ws_, device)
+    e2e_mode = "graph"
+    try:
+        e2e_graphs = []
+        for r in range(n_rot):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    _e2e_step(sgq, per, wrot[r], hx, hd, torch.cuda.current_stream())
+            e2e_graphs.append(g)
+    except RuntimeError as e:   # a PyTorch that cannot capture pinned-memory copies
+        print(f"e2e graph capture failed ({e}); timing the eager step", file=sys.stderr)
+        e2e_mode, e2e_graphs = "eager", None
+        torch.cuda.synchronize()
+    if e2e_graphs is not None:
+        for i in range(args.warmup):
+            with torch.cuda.stream(stream):
+                e2e_graphs[i % n_rot].replay()
+            stream.synchronize()
+        barrier(ws_)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            with torch.cuda.stream(stream):
+                e2e_graphs[i % n_rot].replay()
+            stream.synchronize()   # D is on the host before the next step
+        t_e2e = max_over_ranks((time.perf_counter() - t0) / args.steps, ws_, device)
+    else:
+        t_e2e = t_eager
     if sgq.sgq_device_status(sptr) != 0:
         raise SystemExit("device status not OK after timing")
     h2d = sum(c.M * c.K * 2 for c in cases)
@@ -368,7 +413,8 @@ def run_ours(args, ws_, rank, local):
         "roofline": roof,
         "e2e": {"value": round(ws_ * to_unit / t_e2e / scale, 2), "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(t_e2e * 1e3, 4)},
+                "ms_per_step": round(t_e2e * 1e3, 4), "mode": e2e_mode,
+                "eager_ms_per_step": round(t_eager * 1e3, 4)},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
@@ -383,14 +429,19 @@ def run_ours(args, ws_, rank, local):
 
 
 def _e2e_step(sgq, per, wrot_r, hx, hd, stream):
+    """One host-to-device copy of the step's activations, quantisation + GEMM
+    for every linear, one device-to-host copy of the outputs, on `stream` (the
+    caller waits).  hx / hd: (pinned host buffer, device buffer) pairs; the
+    device views of `per` lie in them."""
     wq, ws = wrot_r
     with torch.cuda.stream(stream):
-        for (c, x, xq, xs, d), h_x, h_d in zip(per, hx, hd):
-            x.copy_(h_x, non_blocking=True)
+        hd_host, hd_dev = hd
+        hx_host, hx_dev = hx
+        hx_dev.copy_(hx_host, non_blocking=True)
+        for c, x, xq, xs, d in per:
             sgq.sgq_quant_token_group(x, c.M, c.K, c.group, c.ue8m0, xq, xs, stream.cuda_stream)
             sgq.sgq_fp8_block_gemm(xq, xs, wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, stream.cuda_stream)
-            h_d.copy_(d, non_blocking=True)
-    stream.synchronize()
+        hd_host.copy_(hd_dev, non_blocking=True)
 
 
 # ----------------------------------------------------------------- oracle timing
