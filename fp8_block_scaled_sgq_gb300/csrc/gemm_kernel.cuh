@@ -1598,42 +1598,36 @@ __global__ void __launch_bounds__(
                     }
                 }
             }
-            if (store && !kSwap) {
+            if constexpr (!kSwap) {
                 // A thread owns one row: 32-byte stores (a full sector per row
-                // and half the store instructions) when D's rows allow them.
-                // The 16-byte stores measured 16% of a short-K GEMM's time
-                // (8192 x 24576 x 1536: 410 us, 344 us without any D store).
-                const bool v8 = (kCols % 16 == 0) &&
+                // and half the store instructions) when D's rows allow them,
+                // else two 16-byte ones.  The 16-byte stores alone measured 16%
+                // of a short-K GEMM's time (8192 x 24576 x 1536: 410 us, 344 us
+                // without any D store, 336 us with 32-byte stores).
+                // (not with per-channel scaling: its epilogue then spills)
+                static_assert(kCols % 16 == 0, "16-column store chunks");
+                const bool v8 = !kChan &&
                                 ((reinterpret_cast<uintptr_t>(a.D) | (static_cast<uintptr_t>(a.N) * 2u)) & 31u) == 0;
-                if (grow < a.M && v8) {
+                if (store && grow < a.M) {
                     __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
 #pragma unroll
                     for (int c = 0; c < kCols; c += 16) {
                         const int gcol = col0 + c_begin + c;
-                        if (gcol < a.N) {
-                            uint32_t w[8];
+                        uint32_t w[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(acc[c + 2 * i], acc[c + 2 * i + 1]);
-                            ptx::st_global_v8(drow + gcol, w);
-                        }
-                    }
-                } else if (grow < a.M) {
-                    __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
-#pragma unroll
-                    for (int c = 0; c < kCols; c += 8) {
-                        const int gcol = col0 + c_begin + c;
-                        if (gcol < a.N) {
-                            uint4 v;
-                            v.x = pack_bf16x2(acc[c], acc[c + 1]);
-                            v.y = pack_bf16x2(acc[c + 2], acc[c + 3]);
-                            v.z = pack_bf16x2(acc[c + 4], acc[c + 5]);
-                            v.w = pack_bf16x2(acc[c + 6], acc[c + 7]);
-                            *reinterpret_cast<uint4*>(drow + gcol) = v;
+                        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(acc[c + 2 * i], acc[c + 2 * i + 1]);
+                        if (v8) {
+                            if (gcol < a.N) ptx::st_global_v8(drow + gcol, w);
+                        } else {
+                            if (gcol < a.N)
+                                *reinterpret_cast<uint4*>(drow + gcol) = make_uint4(w[0], w[1], w[2], w[3]);
+                            if (gcol + 8 < a.N)
+                                *reinterpret_cast<uint4*>(drow + gcol + 8) = make_uint4(w[4], w[5], w[6], w[7]);
                         }
                     }
                 }
-            } else if (store) {
-                if (grow < a.N) {
+            } else {
+                if (store && grow < a.N) {
 #pragma unroll
                     for (int c = 0; c < kCols; ++c) {
                         const int m = col0 + c_begin + c;
