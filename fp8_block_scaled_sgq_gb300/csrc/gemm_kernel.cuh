@@ -170,7 +170,16 @@ struct JobIter {
 };
 
 // Optional event trace for development builds (-DSGQ_TRACE): one row of
-// kTraceSlots globaltimer stamps per CTA.  Compiled out otherwise.
+// kTraceSlots globaltimer stamps per CTA.  Compiled out otherwise.  Slots:
+//   0 CTA start, 1 producer past the grid-dependency wait, 2 its weight
+//   prefetch issued, 3 its prologue done, 4 epilogue past the wait (fused),
+//   5 producer entering its main loop, 8+j stage j issued (j mod 32),
+//   40+j MMA issuer saw stage j full, 72+j scale words of stage j ready,
+//   104+j scale warp saw stage j's raw scales (or its quantised codes),
+//   136/137/138/139 + 4i item i: accumulators read, split-K partial sent,
+//   item done, last accumulator segment picked (i mod 16), 200+j MMA job j
+//   issued, 216+j observed full barrier (alternating issuers), 232+w / 244+w
+//   warp w before / after the final barrier, 255 CTA end.
 constexpr int kTraceSlots = 256;
 __device__ __forceinline__ void trace_ev(const GemmArgs& a, int slot) {
 #ifdef SGQ_TRACE
