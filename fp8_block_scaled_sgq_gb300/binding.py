@@ -43,6 +43,7 @@ EXPORTS = (
     "sgq_status_string",
     "sgq_device_status",
     "sgq_launch_count",
+    "sgq_gemm_plan",
     "sgq_version",
 )
 
@@ -88,6 +89,8 @@ def load_library(path: str = LIB_PATH):
         lib.sgq_device_status.restype = ci
         lib.sgq_launch_count.argtypes = []
         lib.sgq_launch_count.restype = ctypes.c_uint64
+        lib.sgq_gemm_plan.argtypes = [i64, i64, i64, ci, ci, P]
+        lib.sgq_gemm_plan.restype = ci
         lib.sgq_version.argtypes = []
         lib.sgq_version.restype = ci
         _lib = lib
@@ -191,3 +194,14 @@ def sgq_launch_count() -> int:
 
 def sgq_version() -> int:
     return int(load_library().sgq_version())
+
+
+PLAN_FIELDS = ("swap", "bn", "splits", "items", "grid", "alt", "ck", "pair")
+
+
+def sgq_gemm_plan(M, N, K, blk_k, sm_count=152) -> dict:
+    """The GEMM's launch plan for this problem (host only; see include/sgq.h)."""
+    out = (ctypes.c_int32 * 8)()
+    _check(load_library().sgq_gemm_plan(M, N, K, blk_k, sm_count, ctypes.cast(out, ctypes.c_void_p)),
+           "sgq_gemm_plan")
+    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))

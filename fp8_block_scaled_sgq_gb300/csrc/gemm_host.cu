@@ -429,6 +429,14 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
 
 // fp8_scaled_mm: D = (Aq Wq^T) * sa * sb + bias.  The plan is the block GEMM's
 // for blk_k = 128 (the scale arguments of the block path stay unused).
+sgq_status gemm_plan_query(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out) {
+    const gemm::Plan p = gemm::make_plan(M, N, K, blk_k, sm_count);
+    const int32_t v[8] = {p.swap ? 1 : 0, p.bn, p.splits, p.items, p.grid, p.alt ? 1 : 0, p.ck ? 1 : 0,
+                          p.pair ? 1 : 0};
+    for (int i = 0; i < 8; ++i) out[i] = v[i];
+    return SGQ_OK;
+}
+
 sgq_status launch_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, const void* Wq, const float* sb,
                                 int64_t sb_n, const void* bias, void* D, int64_t M, int64_t N, int64_t K,
                                 cudaStream_t st) {

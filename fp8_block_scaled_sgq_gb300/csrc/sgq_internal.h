@@ -41,6 +41,10 @@ sgq_status launch_fp8_block_linear(const void* x, int ue8m0, const void* Wq, con
 sgq_status launch_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, const void* Wq,
                                 const float* sb, int64_t sb_n, const void* bias, void* D, int64_t M,
                                 int64_t N, int64_t K, cudaStream_t stream);
+// The GEMM's launch plan for a device with sm_count SMs (host only):
+// out[0..7] = swap-AB, BN, K splits, work items, grid, alternating issuers,
+// cluster split-K, CTA pairs.
+sgq_status gemm_plan_query(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out);
 // Reads and clears the device status word of the current device (after a sync).
 sgq_status read_and_clear_device_status(cudaStream_t stream);
 

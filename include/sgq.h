@@ -272,6 +272,18 @@ sgq_status sgq_device_status(sgq_stream_t stream);
 /* Number of kernels this library has launched in this process. */
 uint64_t sgq_launch_count(void);
 
+/*
+ * The launch plan sgq_fp8_block_gemm would use for this problem on a device
+ * with `sm_count` SMs; host only (no device is touched), for tests and tools.
+ * out (host, 8 entries, caller-owned): [0] 1 for swap-AB tiles (weights on the
+ * MMA's 128-row side), [1] tile width BN (tokens for swap-AB, else columns),
+ * [2] K splits, [3] work items (tiles x splits), [4] persistent grid before
+ * the occupancy cap, [5] 1 for two alternating MMA issuers, [6] 1 for split-K
+ * summed inside clusters of two, [7] 1 for CTA pairs.  SGQ_ERR_INVALID_ARG for
+ * out == NULL, M, N or K < 1, blk_k not 32 or 128, or sm_count < 1.
+ */
+sgq_status sgq_gemm_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out);
+
 /* Library ABI version (major * 100 + minor). */
 int sgq_version(void);
 
