@@ -469,10 +469,8 @@ def oracle_data(cases):
     return [(c, c.x(), wq, ws) for c in cases]
 
 
-def cpu_baseline(cases, budget_s=12.0, max_frac=1.0):
-    import oracle
-    unit, scale, key = workload_unit(cases)
-    data = oracle_data(cases)
+def _oracle_rate(cases, data, key, budget_s, max_frac):
+    """(work per second, passes, row fraction, seconds) of the oracle on a bounded sample."""
     t0 = time.perf_counter()
     first = oracle_step(cases, data, max_frac)
     step_s = time.perf_counter() - t0
@@ -484,10 +482,27 @@ def cpu_baseline(cases, budget_s=12.0, max_frac=1.0):
         b += oracle_step(cases, data, frac)[key]
         reps += 1
     dt = time.perf_counter() - t0
-    return {"value": round(b / dt / scale, 6), "unit": unit, "cores": oracle.num_threads(),
+    return b / dt, reps, frac, dt
+
+
+def cpu_baseline(cases, budget_s=12.0, max_frac=1.0):
+    """The oracle on all host cores, then on one core (a shorter sample)."""
+    import oracle
+    unit, scale, key = workload_unit(cases)
+    data = oracle_data(cases)
+    cores = oracle.num_threads()
+    rate, reps, frac, dt = _oracle_rate(cases, data, key, budget_s, max_frac)
+    oracle.set_num_threads(1)
+    try:
+        rate1, reps1, frac1, dt1 = _oracle_rate(cases, data, key, budget_s / 2, max_frac)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": round(rate / scale, 6), "unit": unit, "cores": cores,
             "kind": "oracle",
             "sample": f"{reps} pass(es) over the first {frac:.3g} of the rows of each GEMM of the "
-                      f"workload (quantise + fp64 GEMM), {dt:.1f} s"}
+                      f"workload (quantise + fp64 GEMM), {dt:.1f} s",
+            "single_core": {"value": round(rate1 / scale, 6), "cores": 1,
+                            "sample": f"{reps1} pass(es) over the first {frac1:.3g} of the rows, {dt1:.1f} s"}}
 
 
 def run_reference(args, ws_, rank):

@@ -98,6 +98,8 @@ def _load():
         lib.sgqo_quant_token_group_v2.restype = None
         lib.sgqo_num_threads.argtypes = []
         lib.sgqo_num_threads.restype = ci
+        lib.sgqo_set_num_threads.argtypes = [ci]
+        lib.sgqo_set_num_threads.restype = None
         _lib = lib
         return lib
 
@@ -108,6 +110,11 @@ def _ptr(a: np.ndarray):
 
 def num_threads() -> int:
     return int(_load().sgqo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops (n < 1: all processors); timing only."""
+    _load().sgqo_set_num_threads(int(n))
 
 
 def e4m3_encode(v) -> np.ndarray:

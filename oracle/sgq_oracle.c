@@ -74,6 +74,17 @@ int sgqo_num_threads(void) {
 #endif
 }
 
+/* Threads for the parallel loops that follow (n < 1: all processors).  Timing
+ * only: every loop computes each output on its own, so results do not depend
+ * on it. */
+void sgqo_set_num_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
+
 /* bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits. */
 float sgqo_bf16_to_f32(uint16_t h) { return orc_float((uint32_t)h << 16); }
 
