@@ -71,7 +71,7 @@ def kernel_source_digest() -> str:
 # capture per workload (profiles/ holds the summary and the command).  Valid
 # only for the kernel sources they were taken on; otherwise reported as null.
 MEASURED_TRAFFIC = {
-    "decode_block32": {"bytes_per_launch": 14838080, "src": "a25f06aa1bb6fabf",
+    "decode_block32": {"bytes_per_launch": 14838080, "src": "4d79d05d07191291",
                        "profile": "profiles/launches_decode_block32.md"},
 }
 

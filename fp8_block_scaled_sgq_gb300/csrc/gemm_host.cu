@@ -300,6 +300,12 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     if (rc != SGQ_OK) return rc;
     if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
     Plan p = make_plan(M, N, K, blk_k, di.sm_count, (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0);
+    // The allocation-free entry point's fixed array may be too small for the
+    // partials of a mid-M swap-AB plan; the 128 x 256-tile plan needs none.
+    if (noalloc && p.swap && M > 64 && p.splits > 1 &&
+        (size_t(p.items) * kBM * size_t(p.bn) * sizeof(float) > kNoAllocPartialBytes ||
+         size_t(p.tiles_r) * size_t(p.tiles_c) * sizeof(uint32_t) > kNoAllocCounterBytes))
+        p = make_plan(M, N, K, blk_k, di.sm_count, true);
     if (flags & SGQ_GEMM_ISSUE_ALT) p.alt = !p.swap && !p.pair;
     if (flags & SGQ_GEMM_ISSUE_SINGLE) p.alt = false;
     if (chan) {   // plain tiles: no scale boxes, one issuer

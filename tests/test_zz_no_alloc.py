@@ -46,3 +46,27 @@ def test_noalloc_matches_default_entry_point_twice(M):
         assert rc == binding.SGQ_OK, sgq.status_string(rc)
         assert sgq.sgq_device_status() == binding.SGQ_OK
         check_gemm(d, ref, bound, f"no-alloc call {call + 1}, M={M}")
+
+
+def test_noalloc_mid_m_plan_that_would_overflow_the_fixed_array():
+    """1024 x 1536 x 7168: the default plan takes swap-AB tiles of 64 tokens in
+    three K splits, whose partials (18.9 MB) exceed the fixed array; the
+    allocation-free entry point runs the 128 x 256-tile plan instead."""
+    from common import sample_rows
+    lib = binding.load_library()
+    M, N, K, blk = 1024, 1536, 7168, 32
+    p = sgq.sgq_gemm_plan(M, N, K, blk)
+    assert p["swap"] == 1 and p["items"] * 128 * p["bn"] * 4 > (16 << 20)
+    x = synth.activation(M, K, seed=22)
+    w = synth.weight(N, K, seed=22)
+    aq, a_s = oracle.quant_token_group(x, blk, True)
+    wq, ws = oracle.quant_weight_block(w, blk, blk, True)
+    rows = sample_rows(M, 8, seed=22)
+    dref, bound = oracle.gemm(aq[rows], a_s[rows], wq, ws, blk, blk)
+    t = [torch.from_numpy(v).cuda() for v in (aq, a_s, wq, ws)]
+    d = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc = lib.sgq_fp8_block_gemm_noalloc(*(v.data_ptr() for v in t), d.data_ptr(), M, N, K, blk, blk,
+                                        torch.cuda.current_stream().cuda_stream)
+    assert rc == binding.SGQ_OK, sgq.status_string(rc)
+    assert sgq.sgq_device_status() == binding.SGQ_OK
+    check_gemm(d[torch.from_numpy(rows).cuda()], dref, bound, "no-alloc mid-M")
