@@ -58,7 +58,16 @@ def test_reference_arm_other_ranks_exit(monkeypatch, capsys):
         assert p.exitcode == 0
     got = dict(q.get(timeout=10) for _ in range(2))
     assert got[1] is None
-    assert got[0]["impl"] == "reference" and got[0]["value"] > 0
+    line = got[0]
+    assert line["impl"] == "reference" and line["value"] > 0
+    # the bench line's contract keys, and the reference arm's own
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["n_gpus"] == 2 and line["higher_is_better"] is True and line["warmup"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"]["workload"] == "tiny"
 
 
 def _ref_worker(rank, world, port, q):
