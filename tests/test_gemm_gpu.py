@@ -231,3 +231,37 @@ def test_wide_tile_store_alignment(M, N, K, bk):
     assert torch.equal(d0, d1)
     dref, bound = oracle.gemm(aq, a_s, wq, ws, bk, bk)
     check_gemm(d1, dref, bound, f"unaligned D M={M} N={N}")
+
+
+_CK_CHILD = r"""
+import sys, numpy as np, torch
+import fp8_block_scaled_sgq_gb300 as sgq
+from fp8_block_scaled_sgq_gb300 import synth
+import oracle
+M, N, K, bk = (int(v) for v in sys.argv[1:5])
+aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=31), bk, True)
+wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, True)
+d = sgq.fp8_block_gemm(*(torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)), bk, bk)
+assert sgq.sgq_device_status() == 0
+np.save(sys.argv[5], d.view(torch.int16).cpu().numpy())
+"""
+
+
+@pytest.mark.parametrize("M,N,K,bk", [(16, 24576, 1536, 128), (8, 24576, 1536, 32)])
+def test_cluster_split_k_bit_identical(tmp_path, M, N, K, bk):
+    """Split-K inside clusters of two sums p0 + p1 as the global-workspace path
+    does: D equals that path's bit for bit (the child process plans with the
+    clusters off)."""
+    import os
+    import subprocess
+    import sys
+    assert sgq.sgq_gemm_plan(M, N, K, bk)["ck"] == 1
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, SGQ_CK="0", PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"))
+    out = str(tmp_path / "d_global.npy")
+    subprocess.run([sys.executable, "-c", _CK_CHILD, str(M), str(N), str(K), str(bk), out], env=env,
+                   check=True, timeout=600, cwd=root)
+    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=31), bk, True)
+    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, True)
+    d = run_gpu(aq, a_s, wq, ws, bk, bk)
+    assert np.array_equal(d.view(torch.int16).cpu().numpy(), np.load(out))
