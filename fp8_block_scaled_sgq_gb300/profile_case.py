@@ -1,9 +1,11 @@
 """Runs one quantise + GEMM case of a workload a few times, for profilers.
 
     python -m fp8_block_scaled_sgq_gb300.profile_case WORKLOAD [INDEX] [--iters N] [--fused]
+    python -m fp8_block_scaled_sgq_gb300.profile_case --shape M N K BLK [--iters N] [--fused]
 
 WORKLOAD/INDEX pick a case from ``synth.WORKLOADS`` (e.g. ``decode_block32 2``
-is M=16, N=7168, K=2048 with [32,32] blocks).  Each iteration launches the
+is M=16, N=7168, K=2048 with [32,32] blocks); --shape takes any shape with
+[BLK, BLK] blocks and UE8M0 scales (x ~ N(0,1), W ~ N(0,0.02)).  Each iteration launches the
 activation quantisation kernel, then the block-scaled GEMM, on one stream.
 With --fused each iteration is one sgq_fp8_block_linear call instead (one
 kernel at decode-sized M).  The weight is quantised once up front (one extra
@@ -24,12 +26,19 @@ from . import binding, synth
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("workload", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("workload", nargs="?", choices=sorted(synth.WORKLOADS))
     ap.add_argument("index", type=int, nargs="?", default=0)
+    ap.add_argument("--shape", type=int, nargs=4, metavar=("M", "N", "K", "BLK"))
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--fused", action="store_true")
     args = ap.parse_args()
-    c = synth.WORKLOADS[args.workload][args.index]
+    if args.shape:
+        M, N, K, blk = args.shape
+        c = synth.Case(f"shape_M{M}_N{N}_K{K}_b{blk}", M, N, K, blk, blk, True)
+    elif args.workload:
+        c = synth.WORKLOADS[args.workload][args.index]
+    else:
+        ap.error("give WORKLOAD [INDEX] or --shape M N K BLK")
     dev = torch.device("cuda:0")
     M, N, K = c.M, c.N, c.K
     x = c.x().to(dev)
