@@ -43,6 +43,7 @@ EXPORTS = (
     "sgq_status_string",
     "sgq_device_status",
     "sgq_launch_count",
+    "sgq_allocated_bytes",
     "sgq_gemm_plan",
     "sgq_version",
 )
@@ -89,6 +90,8 @@ def load_library(path: str = LIB_PATH):
         lib.sgq_device_status.restype = ci
         lib.sgq_launch_count.argtypes = []
         lib.sgq_launch_count.restype = ctypes.c_uint64
+        lib.sgq_allocated_bytes.argtypes = []
+        lib.sgq_allocated_bytes.restype = ctypes.c_uint64
         lib.sgq_gemm_plan.argtypes = [i64, i64, i64, ci, ci, P]
         lib.sgq_gemm_plan.restype = ci
         lib.sgq_version.argtypes = []
@@ -190,6 +193,10 @@ def sgq_device_status(stream=None) -> int:
 
 def sgq_launch_count() -> int:
     return int(load_library().sgq_launch_count())
+
+
+def sgq_allocated_bytes() -> int:
+    return int(load_library().sgq_allocated_bytes())
 
 
 def sgq_version() -> int:

@@ -198,12 +198,14 @@ sgq_status sgq_device_status(sgq_stream_t stream) {
 
 uint64_t sgq_launch_count(void) { return sgq::g_launches.load(std::memory_order_relaxed); }
 
+uint64_t sgq_allocated_bytes(void) { return sgq::allocated_bytes(); }
+
 sgq_status sgq_gemm_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out) {
     if (out == nullptr || M < 1 || N < 1 || K < 1 || (blk_k != 32 && blk_k != 128) || sm_count < 1)
         return SGQ_ERR_INVALID_ARG;
     return sgq::gemm_plan_query(M, N, K, blk_k, sm_count, out);
 }
 
-int sgq_version(void) { return 101; }
+int sgq_version(void) { return 102; }
 
 }  // extern "C"

@@ -115,9 +115,20 @@ int env_int(const char* name, int dflt) {
     return v ? std::atoi(v) : dflt;
 }
 
+// Split-K scratch a plan may use: bytes of fp32 partial tiles and arrival
+// counters (one per tile).  The default entry point's workspace, or the
+// allocation-free entry point's fixed array.
+struct ScratchLimit {
+    size_t partial_bytes;
+    size_t counters;
+};
+constexpr ScratchLimit kWsLimit{kWsBytes, size_t(kMaxCounters)};
+
 // wide_only: keep the 128 x 256 tiles for M > 64 (the issue-mode testing
-// flags compare the wide tiles' two issue modes).
-Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, bool wide_only = false) {
+// flags compare the wide tiles' two issue modes).  lim: the split-K scratch
+// available; split counts whose partials or counters exceed it are skipped.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, bool wide_only = false,
+               ScratchLimit lim = kWsLimit) {
     Plan p{};
     static const int grid_max = env_int("SGQ_GRID_MAX", 0);
     if (grid_max > 0 && grid_max < sm_count) sm_count = grid_max;
@@ -145,8 +156,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, bool wi
             const int kbp = (p.kb_total + s - 1) / s;
             if ((p.kb_total + kbp - 1) / kbp != s) continue;   // every split non-empty
             const int64_t items = tiles * s;
-            if (s > 1 && (tiles > kMaxCounters ||
-                          size_t(items) * kBM * bn * sizeof(float) > kWsBytes))
+            if (s > 1 && (size_t(tiles) > lim.counters ||
+                          size_t(items) * kBM * bn * sizeof(float) > lim.partial_bytes))
                 continue;
             const int64_t waves = (items + sm_count - 1) / sm_count;
             const double cost = double(waves) * (kbp + ovh) + (s > 1 ? 0.5 : 0.0);
@@ -299,13 +310,14 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     sgq_status rc = device_info(&di);
     if (rc != SGQ_OK) return rc;
     if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
-    Plan p = make_plan(M, N, K, blk_k, di.sm_count, (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0);
-    // The allocation-free entry point's fixed array may be too small for the
-    // partials of a mid-M swap-AB plan; the 128 x 256-tile plan needs none.
-    if (noalloc && p.swap && M > 64 && p.splits > 1 &&
-        (size_t(p.items) * kBM * size_t(p.bn) * sizeof(float) > kNoAllocPartialBytes ||
-         size_t(p.tiles_r) * size_t(p.tiles_c) * sizeof(uint32_t) > kNoAllocCounterBytes))
-        p = make_plan(M, N, K, blk_k, di.sm_count, true);
+    // The allocation-free entry point plans within its fixed array: split
+    // counts whose partials or counters would not fit are skipped, so such a
+    // shape runs with fewer K splits (or, at mid M, on the 128 x 256 tiles
+    // that need no split-K) instead of being refused.
+    const ScratchLimit lim = noalloc ? ScratchLimit{kNoAllocPartialBytes, kNoAllocCounterBytes / sizeof(uint32_t)}
+                                     : kWsLimit;
+    Plan p = make_plan(M, N, K, blk_k, di.sm_count, (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0,
+                       lim);
     if (flags & SGQ_GEMM_ISSUE_ALT) p.alt = !p.swap && !p.pair;
     if (flags & SGQ_GEMM_ISSUE_SINGLE) p.alt = false;
     if (chan) {   // plain tiles: no scale boxes, one issuer
@@ -426,7 +438,10 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
     return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags, false, nullptr, st);
 }
 
-// Same launch plan as launch_fp8_block_gemm, so both give the same result.
+// The launch plan of launch_fp8_block_gemm, except where that plan's split-K
+// partials would not fit the fixed array: then fewer K splits (or the 128 x
+// 256 tiles) are used, and D agrees with the default entry point's within the
+// GEMM tolerance rather than bit for bit.
 sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq, const float* Ws,
                                          void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
                                          cudaStream_t st) {
@@ -450,17 +465,17 @@ sgq_status launch_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, c
     return gemm::launch(Aq, nullptr, Wq, nullptr, D, M, N, K, 128, 128, SGQ_GEMM_DEFAULT, false, nullptr, st, &c);
 }
 
-// Quantise-and-multiply.  Decode-sized M (swap-AB plans with TMA-loadable
-// weight scales): one kernel that quantises its activation tiles itself
-// (writing xq/xs too when given).  Otherwise the quantisation kernel into
-// the caller's xq/xs, then the GEMM; without xq/xs that is unsupported.
-// Every weight tile re-quantises its CTA's activations, so with M > 32 the
-// single kernel is slower than the pair (measured at N=7168, K=2048: 18.5 vs
-// 12.5 us at M=64); there it is used only when no scratch is given.
+// Quantise-and-multiply.  With xq/xs given: the quantisation kernel into
+// them, then the GEMM (the faster path: every weight-tile CTA of the single
+// kernel re-quantises its share of the activations; measured at N=7168,
+// K=2048: 10.7 vs 9.7 us per linear at M=16, 18.5 vs 12.5 us at M=64).
+// Without them, decode-sized M (swap-AB plans with TMA-loadable weight
+// scales) runs one kernel that quantises its activation tiles itself; any
+// other shape is unsupported.
 sgq_status launch_fp8_block_linear(const void* x, int ue8m0, const void* Wq, const float* Ws, void* D, int64_t M,
                                    int64_t N, int64_t K, int blk_n, int blk_k, void* xq, float* xs,
                                    cudaStream_t st) {
-    const bool prefer_pair = M > 32 && xq && xs;
+    const bool prefer_pair = xq && xs;
     const gemm::Fuse f{x, ue8m0, xq, xs};
     const sgq_status rc =
         prefer_pair ? SGQ_ERR_UNSUPPORTED
@@ -470,6 +485,13 @@ sgq_status launch_fp8_block_linear(const void* x, int ue8m0, const void* Wq, con
     const sgq_status q = launch_quant_token_group(x, M, K, blk_k, ue8m0, xq, xs, st);
     if (q != SGQ_OK) return q;
     return launch_fp8_block_gemm(xq, xs, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, st);
+}
+
+uint64_t allocated_bytes() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lk(gemm::g_ws_mu);
+    return gemm::g_ws[dev].partial ? uint64_t(gemm::kWsBytes) + gemm::kMaxCounters * sizeof(uint32_t) : 0;
 }
 
 sgq_status read_and_clear_device_status(cudaStream_t st) {

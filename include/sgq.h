@@ -28,6 +28,12 @@
  *    of a GEMM shape that needs a split-K workspace (and a 4-byte status
  *    word).  That first use must not happen inside a CUDA stream capture;
  *    if it does, the call returns SGQ_ERR_UNSUPPORTED.
+ *  - That split-K workspace (fp32 partial tiles and arrival counters) is one
+ *    per device and shared by every GEMM call on it.  GEMMs that use split-K
+ *    must therefore not overlap on the GPU: calls on one stream are safe;
+ *    calls on different streams, or from several host threads, must be
+ *    ordered (events, or one stream per device).  sgq_gemm_plan tells which
+ *    shapes split K (out[2] > 1).
  */
 #ifndef SGQ_H_
 #define SGQ_H_
@@ -164,11 +170,15 @@ sgq_status sgq_fp8_block_gemm_ex(const void* Aq, const float* As, const void* Wq
  * every GPU that loads the library until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
- * Same arguments, result and launch plan as sgq_fp8_block_gemm (flags =
- * SGQ_GEMM_DEFAULT).  A shape whose launch plan needs more scratch than the
- * fixed array holds is rejected with SGQ_ERR_UNSUPPORTED before anything is
- * launched; shapes that need no split-K (large M, or few K blocks) never touch
- * the array.
+ * Same arguments as sgq_fp8_block_gemm (flags = SGQ_GEMM_DEFAULT) and the
+ * same launch plan wherever that plan's split-K partials and counters fit the
+ * fixed array; D is then bit-identical to sgq_fp8_block_gemm's.  Where they
+ * would not fit, the plan takes fewer K splits (or, for 64 < M <= 1024, the
+ * 128 x 256 tiles, which need no split-K), and D agrees with
+ * sgq_fp8_block_gemm's within the GEMM tolerance (a different fp32 summation
+ * order).  SGQ_ERR_UNSUPPORTED, before anything is launched, remains only for
+ * a plan that still needs more scratch than the array holds.  Shapes that need
+ * no split-K (large M, or few K blocks) never touch the array.
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any CUDA stream capture.
@@ -193,15 +203,14 @@ sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const voi
  * bit-identical to sgq_quant_token_group's.  The result D is bit-identical to
  * sgq_quant_token_group followed by sgq_fp8_block_gemm.
  *
- * No counterpart in the pages as one call; it fuses the two steps above.  For
- * decode-sized M with K/blk_k a multiple of 4 and at least 8 (blk_k = 128) or
- * 16 (blk_k = 32) -- every decode shape the pages use -- it is ONE kernel
- * when M <= 32, or when M <= 64 and xq/xs are NULL: the GEMM's epilogue warps
- * quantise each bf16 activation tile into shared memory, so the codes never
- * go through HBM and a launch disappears.  Any other shape (and 32 < M <= 64
- * with xq/xs given, where the pair is faster) runs the two kernels back to
- * back with xq/xs as scratch; without them it returns SGQ_ERR_UNSUPPORTED
- * before launching.
+ * No counterpart in the pages as one call; it fuses the two steps above.
+ * With xq/xs given it runs the two kernels back to back, with xq/xs as
+ * scratch (measured faster than the single kernel).  With xq/xs NULL, for
+ * decode-sized M (<= 64) with K/blk_k a multiple of 4 and at least 8
+ * (blk_k = 128) or 16 (blk_k = 32) -- every decode shape the pages use -- it
+ * is ONE kernel: the GEMM's epilogue warps quantise each bf16 activation tile
+ * into shared memory, so the codes never go through HBM and a launch
+ * disappears; any other shape returns SGQ_ERR_UNSUPPORTED before launching.
  * Errors and the launch-overlap contract: as for sgq_fp8_block_gemm (x is
  * read only after the preceding kernel has finished).
  */
@@ -271,6 +280,14 @@ sgq_status sgq_device_status(sgq_stream_t stream);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t sgq_launch_count(void);
+
+/*
+ * Bytes of device memory the library has allocated on the current device in
+ * this process (the split-K workspace and its counters; 0 until the first GEMM
+ * that needs them, and always 0 for a process that uses only the
+ * allocation-free GEMM and the quantisers).  Host only; 0 without a device.
+ */
+uint64_t sgq_allocated_bytes(void);
 
 /*
  * The launch plan sgq_fp8_block_gemm would use for this problem on a device

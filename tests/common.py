@@ -50,3 +50,20 @@ def sample_rows(M, n=12, seed=0):
     while len(rows) < n:
         rows.add(int(rng.integers(0, M)))
     return np.array(sorted(rows))
+
+
+def tile_rows(M, block=64, seed=0):
+    """One row in every `block`-row block of [0, M) -- with block = 64 that is
+    every 128-row tile of the wide GEMM plan and every 64-token tile of the
+    swap-AB plans -- at an offset inside the block that changes from block to
+    block, plus the first and last row of every 128-row tile boundary pair and
+    of the whole range."""
+    rows = set()
+    nblk = (M + block - 1) // block
+    for b in range(nblk):
+        off = (b * 37 + seed * 11 + 5) % block
+        rows.add(min(b * block + off, M - 1))
+    for r in (0, 1, 127, 128, M // 2, M - 129, M - 128, M - 1):
+        if 0 <= r < M:
+            rows.add(r)
+    return np.array(sorted(rows))

@@ -11,7 +11,7 @@ import fp8_block_scaled_sgq_gb300 as sgq
 from fp8_block_scaled_sgq_gb300 import synth
 
 import oracle
-from common import check_gemm, sample_rows
+from common import check_gemm, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -55,14 +55,16 @@ def test_decode_block32(idx):
     case_check(synth.WORKLOADS["decode_block32"][idx], FLAGS)
 
 
-def test_prefill_block128_sampled():
+def test_prefill_block128_every_tile():
+    """Full size; one row of every 64-row block (every M-tile of the wide
+    plan) is compared over all N columns."""
     c = synth.WORKLOADS["prefill_block128"][0]
-    case_check(c, FLAGS, rows=sample_rows(c.M, 12))
+    case_check(c, FLAGS, rows=tile_rows(c.M, seed=1))
 
 
-def test_prefill_block32_sampled():
+def test_prefill_block32_every_tile():
     c = synth.WORKLOADS["prefill_block32"][0]
-    case_check(c, FLAGS, rows=sample_rows(c.M, 12))
+    case_check(c, FLAGS, rows=tile_rows(c.M, seed=2))
 
 
 SWEEP = synth.WORKLOADS["sweep"]
@@ -71,7 +73,7 @@ SWEEP = synth.WORKLOADS["sweep"]
 @pytest.mark.parametrize("idx", range(len(SWEEP)), ids=[c.name for c in SWEEP])
 def test_sweep(idx):
     c = SWEEP[idx]
-    rows = None if c.M <= 128 else sample_rows(c.M, 10, seed=idx)
+    rows = None if c.M <= 128 else tile_rows(c.M, seed=idx)
     case_check(c, (0,), rows=rows)
 
 
@@ -117,10 +119,12 @@ def test_mixed_pow2_and_fp32_scales(M, bk):
 @pytest.mark.parametrize("rows", [(130, 140), (3, 9), (250, 256)])
 @pytest.mark.parametrize("bk", [32, 128])
 def test_pair_tile_one_half_not_pow2(rows, bk):
-    """Large-M tiles are computed by pairs of CTAs, each holding half of the
-    rows.  Activation scales that are not powers of two in only one half of a
-    tile (rows 128-255 of the first tile, or 0-127) must send the whole tile's
-    stage to the promotion path, for both halves."""
+    """Activation scales that are not powers of two in only part of the rows
+    of a wide tile (rows 128-255 of the first 256-row span, or 0-127): the
+    stage must take the promotion path for the rows that need it.  With CTA
+    pairs (SGQ_PAIR=1, tested below in a child process) each CTA of the pair
+    holds one half of a 256-row tile, and one half's non-power-of-two scales
+    must send the whole tile's stage to the promotion path, for both halves."""
     M, N, K, bn = 300, 520, 1024, 128
     x = synth.activation(M, K, seed=5)
     w = synth.weight(N, K, seed=5)
@@ -194,7 +198,7 @@ def test_alternating_issuers_bit_identical(M, N, K, bn, bk, scales):
     d_one = sgq.fp8_block_gemm(*args, bn, bk, flags=sgq.SGQ_GEMM_ISSUE_SINGLE)
     assert sgq.sgq_device_status() == 0
     assert torch.equal(d_alt, d_one)
-    r = sample_rows(M, 16, seed=M)
+    r = tile_rows(M, seed=M)
     dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
     check_gemm(d_alt[torch.from_numpy(r).cuda()], dref, bound, f"alt M={M} N={N} K={K} {scales}")
 
@@ -265,3 +269,56 @@ def test_cluster_split_k_bit_identical(tmp_path, M, N, K, bk):
     wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, True)
     d = run_gpu(aq, a_s, wq, ws, bk, bk)
     assert np.array_equal(d.view(torch.int16).cpu().numpy(), np.load(out))
+
+
+_PAIR_CHILD = r"""
+import sys, numpy as np, torch
+import fp8_block_scaled_sgq_gb300 as sgq
+from fp8_block_scaled_sgq_gb300 import synth
+import oracle
+from common import check_gemm, tile_rows
+cases = [(300, 520, 1024, 128, 128, "pow2"), (300, 520, 1024, 32, 32, "half"), (257, 1032, 4096, 128, 32, "mixed"),
+         (513, 264, 2048, 32, 32, "fp32"), (4096, 7168, 7168, 128, 128, "prefill")]
+for M, N, K, bn, bk, kind in cases:
+    assert sgq.sgq_gemm_plan(M, N, K, bk)["pair"] == 1, (M, N, K, bk)
+    if kind == "prefill":
+        c = synth.WORKLOADS["prefill_block128"][0]
+        x, w = c.x(), c.w()
+    else:
+        x, w = synth.activation(M, K, seed=M + 3), synth.weight(N, K, seed=N + 3)
+    ue = kind != "fp32"
+    aq, a_s = oracle.quant_token_group(x, bk, ue)
+    wq, ws = oracle.quant_weight_block(w, bn, bk, ue)
+    stage_cols = 128 // bk
+    if kind == "half":      # one half of the first 256-row tile not a power of two
+        for st in (1, 4, 5):
+            a_s[130:140, st * stage_cols:(st + 1) * stage_cols] *= np.float32(1.3)
+    if kind == "mixed":     # some stages' weight scales not powers of two
+        rng = np.random.default_rng(7)
+        for st in range(K // 128):
+            if rng.random() < 0.4:
+                ws[:, st * stage_cols:(st + 1) * stage_cols] *= np.float32(1.3)
+    d = sgq.fp8_block_gemm(*(torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)), bn, bk)
+    assert sgq.sgq_device_status() == 0
+    r = np.arange(M) if M <= 600 else tile_rows(M, seed=5)
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
+    check_gemm(d[torch.from_numpy(r).cuda()], dref, bound, f"pair M={M} N={N} K={K} {kind}")
+print("pair ok")
+"""
+
+
+def test_cta_pair_tiles_match_oracle():
+    """The opt-in CTA-pair plan (SGQ_PAIR=1: 256-row tiles on clusters of two,
+    cta_group::2 MMAs issued by the leader for both CTAs) on ragged, one-half
+    non-power-of-two, mixed-scale, fp32-scale and the full prefill [128,128]
+    shapes, against the oracle (every row of the ragged shapes; one row of
+    every 64-row block of the prefill shape).  Run in a child process, since
+    the launch plan reads its switches once per process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, SGQ_PAIR="1", SGQ_MIDSWAP="0", PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"))
+    r = subprocess.run([sys.executable, "-c", _PAIR_CHILD], env=env, cwd=root, timeout=900,
+                       capture_output=True, text=True)
+    assert r.returncode == 0 and "pair ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]

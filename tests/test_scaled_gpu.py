@@ -11,7 +11,7 @@ import fp8_block_scaled_sgq_gb300 as sgq
 from fp8_block_scaled_sgq_gb300 import synth
 
 import oracle
-from common import check_gemm, sample_rows
+from common import check_gemm, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -71,10 +71,24 @@ def test_scaled_mm_vs_oracle(M, N, K, mode):
     d = sgq.fp8_scaled_mm(torch.from_numpy(aq).cuda(), torch.from_numpy(sa).cuda(), torch.from_numpy(wq).cuda(),
                           torch.from_numpy(sb).cuda(), None if bias is None else bias.cuda())
     assert sgq.sgq_device_status() == 0
-    rows = np.arange(M) if M <= 200 else sample_rows(M, 12, seed=M)
+    rows = np.arange(M) if M <= 200 else tile_rows(M, seed=M)
     sa_r = sa if sa.size == 1 else sa[rows]
     dref, bound = oracle.scaled_mm(aq[rows], sa_r, wq, sb, bias)
     check_gemm(d[torch.from_numpy(rows).cuda()], dref, bound, f"scaled_mm M={M} N={N} K={K} {mode}")
+
+
+def test_scaled_mm_prefill_every_tile():
+    """Full prefill size (4096 x 7168 x 7168), per-row x per-column scales and
+    bias: one row of every 64-row block compared over all N columns."""
+    M, N, K = 4096, 7168, 7168
+    aq, sa, wq, sb = _operands(M, N, K, seed=9)
+    bias = synth.activation(1, N, seed=N).reshape(N)
+    d = sgq.fp8_scaled_mm(torch.from_numpy(aq).cuda(), torch.from_numpy(sa).cuda(), torch.from_numpy(wq).cuda(),
+                          torch.from_numpy(sb).cuda(), bias.cuda())
+    assert sgq.sgq_device_status() == 0
+    rows = tile_rows(M, seed=9)
+    dref, bound = oracle.scaled_mm(aq[rows], sa[rows], wq, sb, bias)
+    check_gemm(d[torch.from_numpy(rows).cuda()], dref, bound, "scaled_mm prefill")
 
 
 def test_scaled_mm_split_k_deterministic_and_end_to_end():
