@@ -67,20 +67,22 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
-# capture per workload (profiles/ holds the summary and the command).  Valid
-# only for the kernel sources they were taken on; otherwise reported as null.
-MEASURED_TRAFFIC = {
-    "decode_block32": {"bytes_per_launch": 14838080, "src": "4d79d05d07191291",
-                       "profile": "profiles/launches_decode_block32.md"},
-}
+# DRAM bytes (read + write) per launch of the dominant kernel, recorded by the
+# profiling step (one ncu capture per workload) with the digest of the kernel
+# sources it was taken on; a record for other sources reads as null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
 def measured_traffic(workload: str):
-    t = MEASURED_TRAFFIC.get(workload)
-    if t is None or t["src"] != kernel_source_digest():
+    """Bytes per launch for `workload` from the traffic record, or None."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
-    return t["bytes_per_launch"]
+    digest = kernel_source_digest()
+    for line in open(TRAFFIC_FILE):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == workload and f[1] == digest:
+            return int(f[2])
+    return None
 
 
 def workload_unit(cases):
@@ -185,6 +187,138 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- our arm
 
+def n_rotations(nbytes: float) -> int:
+    """Copies of an operand of `nbytes` whose cycle exceeds twice the L2 size."""
+    return max(2, math.ceil(2 * L2_BYTES / nbytes) + 1)
+
+
+class GraphTimer:
+    """CUDA graphs of library calls on one stream, timed with CUDA events.
+
+    Each graph holds `reps` calls (call i uses operand set i % len(calls)); it is
+    replayed once to warm up, then once between two events.  `launches` counts
+    the library's kernels of every replay made (the graph's kernels, counted
+    from the library's launch counter during capture, times its replays)."""
+
+    def __init__(self, sgq, stream):
+        self.sgq, self.stream, self.launches = sgq, stream, 0
+
+    def capture(self, calls, reps):
+        g = torch.cuda.CUDAGraph()
+        n0 = self.sgq.sgq_launch_count()
+        with torch.cuda.stream(self.stream):
+            with torch.cuda.graph(g, stream=self.stream):
+                sp = torch.cuda.current_stream().cuda_stream
+                for i in range(reps):
+                    calls[i % len(calls)](sp)
+        g.kernels = self.sgq.sgq_launch_count() - n0
+        return g
+
+    def replay_ms(self, g, reps, ws_=1):
+        """(warm-up replay) then one timed replay; ms per call."""
+        with torch.cuda.stream(self.stream):
+            g.replay()
+        self.stream.synchronize()
+        barrier(ws_)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            g.replay()
+            e1.record(self.stream)
+        self.stream.synchronize()
+        torch.cuda.synchronize()
+        barrier(ws_)
+        self.launches += 2 * g.kernels
+        return e0.elapsed_time(e1) / reps
+
+    def time(self, calls, reps, ws_=1):
+        g = self.capture(calls, reps)
+        ms = self.replay_ms(g, reps, ws_)
+        del g
+        return ms
+
+
+def roofline_frac(flops: float, nbytes: float, us: float):
+    """(bound, fraction) of min(FP8 peak, arithmetic intensity x HBM peak)."""
+    pk = peaks()
+    fp8 = 2.0 * pk["bf16_tflops"] * 1e12
+    t_fp8, t_hbm = flops / fp8, nbytes / (pk["hbm_gbs"] * 1e9)
+    return ("fp8" if t_fp8 > t_hbm else "hbm"), max(t_fp8, t_hbm) / (us * 1e-6)
+
+
+def gemm_cases(sgq, timer, device, reps, names):
+    """The metric's GEMM configurations: the M = 1..8192 sweep (two weight
+    shapes, both recipes) and the two prefill shapes; each timed as the GEMM
+    alone and as quantisation + GEMM back to back ("pair")."""
+    rows = []
+    groups = {}
+    for name in names:
+        for c in synth.WORKLOADS[name]:
+            groups.setdefault((c.N, c.K, c.blk_n, c.blk_k, c.ue8m0, c.seed), []).append(c)
+    for (N, K, bn, bk, ue, seed), cs in groups.items():
+        w = synth.weight(N, K, seed).to(device)
+        wq0, ws0 = sgq.quant_weight_block(w, bn, bk, ue)
+        del w
+        wbytes = N * K + 4 * math.ceil(N / bn) * (K // bk)
+        wrot = [(wq0, ws0)] + [(wq0.clone(), ws0.clone()) for _ in range(n_rotations(wbytes) - 1)]
+        for c in cs:
+            x = c.x().to(device)
+            xq = torch.empty((c.M, c.K), dtype=torch.uint8, device=device)
+            xs = torch.empty((c.M, c.K // c.group), dtype=torch.float32, device=device)
+            d = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
+            sgq.sgq_quant_token_group(x, c.M, c.K, c.group, int(c.ue8m0), xq, xs, timer.stream.cuda_stream)
+
+            def gemm(sp, r, c=c, xq=xq, xs=xs, d=d):
+                sgq.sgq_fp8_block_gemm(xq, xs, wrot[r][0], wrot[r][1], d, c.M, c.N, c.K, c.blk_n, c.blk_k, sp)
+
+            def pair(sp, r, c=c, x=x, xq=xq, xs=xs, d=d):
+                sgq.sgq_quant_token_group(x, c.M, c.K, c.group, int(c.ue8m0), xq, xs, sp)
+                gemm(sp, r)
+            for path, fn in (("gemm", gemm), ("pair", pair)):
+                calls = [lambda sp, r=r, fn=fn: fn(sp, r) for r in range(len(wrot))]
+                ms = timer.time(calls, reps)
+                us = ms * 1e3
+                nbytes = c.gemm_bytes() + (c.quant_bytes() if path == "pair" else 0.0)
+                bound, frac = roofline_frac(c.flops(), nbytes, us)
+                rows.append({"case": c.name, "path": path, "M": c.M, "N": c.N, "K": c.K,
+                             "recipe": [1, c.blk_n, c.blk_k], "us": round(us, 3),
+                             "tflops": round(c.flops() / us / 1e6, 2), "gbs": round(nbytes / us / 1e3, 1),
+                             "bound": bound, "frac": round(frac, 4)})
+            del x, xq, xs, d
+        del wrot, wq0, ws0
+        torch.cuda.empty_cache()
+    return rows
+
+
+QUANT_SHAPES = [(4096, 7168), (8192, 7168)]
+
+
+def quant_cases(sgq, timer, device, reps):
+    """sgq_quant_token_group alone at prefill sizes, both group sizes, UE8M0:
+    GB/s of 2 B read + 1 B code + 4/g B scale per element (inputs rotated over
+    more than twice the L2 size)."""
+    rows = []
+    for M, K in QUANT_SHAPES:
+        x0 = synth.activation(M, K, seed=7).to(device)
+        xr = [x0] + [x0.clone() for _ in range(n_rotations(2 * M * K) - 1)]
+        for g in (128, 32):
+            xq = torch.empty((M, K), dtype=torch.uint8, device=device)
+            xs = torch.empty((M, K // g), dtype=torch.float32, device=device)
+            calls = [lambda sp, x=x, g=g, xq=xq, xs=xs: sgq.sgq_quant_token_group(x, M, K, g, 1, xq, xs, sp)
+                     for x in xr]
+            us = timer.time(calls, reps) * 1e3
+            nbytes = 2 * M * K + M * K + 4 * M * K / g
+            rows.append({"case": f"quant_token_group_M{M}_K{K}_g{g}", "path": "quant", "M": M, "K": K,
+                         "group": g, "us": round(us, 3), "gbs": round(nbytes / us / 1e3, 1), "bound": "hbm",
+                         "frac": round(nbytes / us / 1e3 / peaks()["hbm_gbs"], 4)})
+            del xq, xs
+        del xr, x0
+        torch.cuda.empty_cache()
+    return rows
+
+
 def build_problem(cases, device, n_rot):
     import fp8_block_scaled_sgq_gb300 as sgq
     c0 = cases[0]
@@ -202,23 +336,28 @@ def build_problem(cases, device, n_rot):
     return wrot, per
 
 
-def step_fn(sgq, per, wq, ws, stream, gemm_only=False):
-    for c, x, xq, xs, d in per:
+def step_fn(sgq, per, wsets, stream, gemm_only=False):
+    """One step: quantisation + GEMM for every linear; linear j uses weight set
+    wsets[j] (each GEMM of a step streams its own copy of the weights)."""
+    for (c, x, xq, xs, d), (wq, ws) in zip(per, wsets):
         if not gemm_only:
             sgq.sgq_quant_token_group(x, c.M, c.K, c.group, c.ue8m0, xq, xs, stream)
         sgq.sgq_fp8_block_gemm(xq, xs, wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, stream)
 
 
-def fused_step_fn(sgq, per, wq, ws, stream):
+def fused_step_fn(sgq, per, wsets, stream):
     """The same layer through sgq_fp8_block_linear (one kernel per case at
     decode-sized M; codes and scales stay on chip)."""
-    for c, x, _, _, d in per:
+    for (c, x, _, _, d), (wq, ws) in zip(per, wsets):
         sgq.sgq_fp8_block_linear(x, int(c.ue8m0), wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, None, None, stream)
 
 
 def fusable(cases):
     return all(c.M <= 64 and (c.K // c.blk_k) % 4 == 0 and c.K // c.blk_k >= (8 if c.blk_k == 128 else 16)
                for c in cases)
+
+
+EXTRA_GEMM_WORKLOADS = ("sweep", "prefill_block128", "prefill_block32")
 
 
 def run_ours(args, ws_, rank, local):
@@ -234,60 +373,37 @@ def run_ours(args, ws_, rank, local):
         raise SystemExit("workload mixes weight shapes")
     c0 = cases[0]
     wbytes = c0.N * c0.K + 4 * math.ceil(c0.N / c0.blk_n) * (c0.K // c0.blk_k)
-    n_rot = max(2, math.ceil(2 * L2_BYTES / wbytes) + 1)
+    n_rot = n_rotations(wbytes)
     wrot, per = build_problem(cases, device, n_rot)
     stream = torch.cuda.Stream(device)
     sptr = stream.cuda_stream
+    timer = GraphTimer(sgq, stream)
+    nl = len(per)
+
+    def wsets(i):
+        """Weight copies of step i: one per linear, cycling through all copies."""
+        return [wrot[(i * nl + j) % n_rot] for j in range(nl)]
 
     gemm_bytes = sum(c.gemm_bytes() for c in cases)
     quant_bytes = sum(c.quant_bytes() for c in cases)
     step_bytes = gemm_bytes + quant_bytes
     step_flops = sum(c.flops() for c in cases)
 
-    # warm-up outside capture (first split-K call allocates the workspace)
+    # warm-up outside capture (the first split-K call allocates the workspace)
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
-            step_fn(sgq, per, *wrot[i % n_rot], sptr)
+            step_fn(sgq, per, wsets(i), sptr)
     stream.synchronize()
     if sgq.sgq_device_status(sptr) != 0:
         raise SystemExit("device status not OK after warm-up")
 
-    def capture(fn, steps):
-        """One CUDA graph holding exactly `steps` steps, weights rotating."""
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                sp = torch.cuda.current_stream().cuda_stream
-                for i in range(steps):
-                    fn(i % n_rot, sp)
-        return g
-
-    def full_step(r, sp):
-        step_fn(sgq, per, *wrot[r], sp)
-
-    def timed(g, steps):
-        # warm-up replay, then exactly one replay (= `steps` steps) between events
-        with torch.cuda.stream(stream):
-            g.replay()
-        stream.synchronize()
-        barrier(ws_)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize()
-        barrier(ws_)
-        return e0.elapsed_time(e1) / steps   # ms per step
-
-    graph = capture(full_step, args.steps)
-    fused_graph = (capture(lambda r, sp: fused_step_fn(sgq, per, *wrot[r], sp), args.steps)
-                   if fusable(cases) else None)
-    case_graphs = [capture(lambda r, sp, i=i: step_fn(sgq, per[i:i + 1], *wrot[r], sp, gemm_only=True),
-                           args.steps) for i in range(len(per))]
+    steps = args.steps
+    graph = timer.capture([lambda sp, i=i: step_fn(sgq, per, wsets(i), sp) for i in range(n_rot)], steps)
+    fused_graph = (timer.capture([lambda sp, i=i: fused_step_fn(sgq, per, wsets(i), sp) for i in range(n_rot)],
+                                 steps) if fusable(cases) else None)
+    # per linear: its GEMM alone, back to back, each call on the next weight copy
+    case_graphs = [timer.capture([lambda sp, j=j, r=r: step_fn(sgq, per[j:j + 1], [wrot[r]], sp, gemm_only=True)
+                                  for r in range(n_rot)], steps) for j in range(nl)]
 
     def preheat(seconds):
         t_end = time.perf_counter() + seconds
@@ -296,20 +412,24 @@ def run_ours(args, ws_, rank, local):
                 graph.replay()
             stream.synchronize()
 
-    launches0 = sgq.sgq_launch_count()
+    reps = max(20, steps)
+    extra = []
     with ClockSampler(local, os.path.join(args.out_dir, f"clocks_rank{rank}.csv") if args.out_dir else None) as cs:
         preheat(args.preheat)
-        ms_step = timed(graph, args.steps)
-        ms_case = [timed(cg, args.steps) for cg in case_graphs]
-        ms_fused = timed(fused_graph, args.steps) if fused_graph is not None else None
+        ms_step = timer.replay_ms(graph, steps, ws_)
+        ms_case = [timer.replay_ms(cg, steps, ws_) for cg in case_graphs]
+        ms_fused = timer.replay_ms(fused_graph, steps, ws_) if fused_graph is not None else None
+        if args.cases == "all" and ws_ == 1:
+            extra = gemm_cases(sgq, timer, device, reps, EXTRA_GEMM_WORKLOADS)
+            extra += quant_cases(sgq, timer, device, reps)
     clocks = cs.summary()
+    gpu_launches = timer.launches
     ms_step = max_over_ranks(ms_step, ws_, device)
     ms_case = [max_over_ranks(t, ws_, device) for t in ms_case]
     ms_gemm = sum(ms_case)
     if ms_fused is not None:
         ms_fused = max_over_ranks(ms_fused, ws_, device)
-    gpu_launches = 2 * len(cases) * args.steps   # quant + GEMM per case per step (graph replays)
-    assert sgq.sgq_launch_count() == launches0   # replays do not call the library
+    del graph, fused_graph, case_graphs
 
     # end to end through the public API: H2D of x, quant + GEMM, D2H of D, every
     # step; the step's activations (and outputs) sit in one buffer each, so one
@@ -327,14 +447,14 @@ def run_ours(args, ws_, rank, local):
     per = per_e2e
     hx, hd = (hx, dx), (hd, dd)
     for i in range(args.warmup):
-        _e2e_step(sgq, per, wrot[i % n_rot], hx, hd, stream)   # e2e warm-up
+        _e2e_step(sgq, per, wsets(i), hx, hd, stream)   # e2e warm-up
         stream.synchronize()
     barrier(ws_)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        _e2e_step(sgq, per, wrot[i % n_rot], hx, hd, stream)
+    for i in range(steps):
+        _e2e_step(sgq, per, wsets(i), hx, hd, stream)
         stream.synchronize()
-    t_eager = max_over_ranks((time.perf_counter() - t0) / args.steps, ws_, device)
+    t_eager = max_over_ranks((time.perf_counter() - t0) / steps, ws_, device)
     e2e_mode = "graph"
     try:
         e2e_graphs = []
@@ -342,7 +462,7 @@ def run_ours(args, ws_, rank, local):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(stream):
                 with torch.cuda.graph(g, stream=stream):
-                    _e2e_step(sgq, per, wrot[r], hx, hd, torch.cuda.current_stream())
+                    _e2e_step(sgq, per, wsets(r), hx, hd, torch.cuda.current_stream())
             e2e_graphs.append(g)
     except RuntimeError as e:   # a PyTorch that cannot capture pinned-memory copies
         print(f"e2e graph capture failed ({e}); timing the eager step", file=sys.stderr)
@@ -355,11 +475,11 @@ def run_ours(args, ws_, rank, local):
             stream.synchronize()
         barrier(ws_)
         t0 = time.perf_counter()
-        for i in range(args.steps):
+        for i in range(steps):
             with torch.cuda.stream(stream):
                 e2e_graphs[i % n_rot].replay()
             stream.synchronize()   # D is on the host before the next step
-        t_e2e = max_over_ranks((time.perf_counter() - t0) / args.steps, ws_, device)
+        t_e2e = max_over_ranks((time.perf_counter() - t0) / steps, ws_, device)
     else:
         t_e2e = t_eager
     if sgq.sgq_device_status(sptr) != 0:
@@ -383,14 +503,20 @@ def run_ours(args, ws_, rank, local):
         unit, scale, to_unit = "GB/s", 1e9, step_bytes
         roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(gemm_gbs / pk["hbm_gbs"], 4), "traffic": measured_traffic(args.workload),
-                "kernel": "fp8_block_gemm_kernel (swap-AB, split-K)", "peak_source": pk["source"]}
+                "kernel": "block-scaled GEMM, decode tiles (swap-AB, split-K)", "peak_source": pk["source"]}
     value = ws_ * to_unit / (ms_step * 1e-3) / scale
+    per_case = []
+    for c, t in zip(cases, ms_case):
+        us = t * 1e3
+        bound, frac = roofline_frac(c.flops(), c.gemm_bytes(), us)
+        per_case.append({"M": c.M, "us": round(us, 3), "gbs": round(c.gemm_bytes() / us / 1e3, 1),
+                         "tflops": round(c.flops() / us / 1e6, 2), "bound": bound, "frac": round(frac, 4)})
     result = {
         "metric": METRIC,
         "value": round(value, 2),
         "unit": unit,
         "n_gpus": ws_,
-        "steps": args.steps,
+        "steps": steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
         "higher_is_better": True,
@@ -400,16 +526,13 @@ def run_ours(args, ws_, rank, local):
         "data": "synthetic (seeded; x ~ N(0,1), W ~ N(0,0.02) bf16, quantised on the GPU)",
         "config": {"workload": args.workload, "M": [c.M for c in cases], "N": c0.N, "K": c0.K,
                    "recipe": [1, c0.blk_n, c0.blk_k], "ue8m0": c0.ue8m0,
-                   "l2": f"weights rotate over {n_rot} copies ({n_rot * wbytes / 2**20:.0f} MiB > 2x L2)",
+                   "l2": f"each GEMM of a step streams its own weight copy; copies rotate over {n_rot} "
+                         f"({n_rot * wbytes / 2**20:.0f} MiB > 2x L2)",
                    "parallelism": f"replicas x{ws_}"},
         "tflops": round(ws_ * step_flops / (ms_step * 1e-3) / 1e12, 3),
         "gbs": round(ws_ * step_bytes / (ms_step * 1e-3) / 1e9, 2),
         "gemm": {"ms_per_step": round(ms_gemm, 5), "gbs": round(gemm_gbs, 1),
-                 "tflops": round(gemm_tf, 3),
-                 "per_case": [{"M": c.M, "us": round(t * 1e3, 3),
-                               "gbs": round(c.gemm_bytes() / (t * 1e-3) / 1e9, 1),
-                               "tflops": round(c.flops() / (t * 1e-3) / 1e12, 2)}
-                              for c, t in zip(cases, ms_case)]},
+                 "tflops": round(gemm_tf, 3), "per_case": per_case},
         "roofline": roof,
         "e2e": {"value": round(ws_ * to_unit / t_e2e / scale, 2), "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -425,20 +548,34 @@ def run_ours(args, ws_, rank, local):
         result["fused"] = {"entry": "sgq_fp8_block_linear", "ms_per_step": round(ms_fused, 5),
                            "gbs": round(ws_ * fused_bytes / (ms_fused * 1e-3) / 1e9, 2),
                            "launches_per_step": len(cases)}
+    if extra:
+        result["cases"] = extra
+        result["cases_timing"] = (f"each case: a CUDA graph of {reps} calls (weights, or the quantiser's "
+                                  "input, rotated over more than twice the L2 size) after one warm-up replay; "
+                                  "fractions of min(FP8 peak, AI x HBM peak), FP8 = 2 x measured bf16 burst")
+        pre = {r["case"]: r for r in extra if r["path"] == "gemm"}
+        big = pre.get("sweep_N24576_K1536_b128_M8192"), pre.get("sweep_N1536_K7168_b128_M8192")
+        result["headline"] = {
+            "prefill_gemm": [{"case": r["case"], "tflops": r["tflops"], "frac_fp8": r["frac"]}
+                             for r in (pre.get("prefill_block128"), pre.get("prefill_block32")) + big if r],
+            "decode_gemm": {"M": [c.M for c in cases], "gbs": round(gemm_gbs, 1),
+                            "frac_hbm": round(gemm_gbs / pk["hbm_gbs"], 4)},
+            "quant": [{"case": r["case"], "gbs": r["gbs"], "frac_hbm": r["frac"]}
+                      for r in extra if r["path"] == "quant"],
+        }
     return result
 
 
-def _e2e_step(sgq, per, wrot_r, hx, hd, stream):
+def _e2e_step(sgq, per, wsets, hx, hd, stream):
     """One host-to-device copy of the step's activations, quantisation + GEMM
     for every linear, one device-to-host copy of the outputs, on `stream` (the
     caller waits).  hx / hd: (pinned host buffer, device buffer) pairs; the
     device views of `per` lie in them."""
-    wq, ws = wrot_r
     with torch.cuda.stream(stream):
         hd_host, hd_dev = hd
         hx_host, hx_dev = hx
         hx_dev.copy_(hx_host, non_blocking=True)
-        for c, x, xq, xs, d in per:
+        for (c, x, xq, xs, d), (wq, ws) in zip(per, wsets):
             sgq.sgq_quant_token_group(x, c.M, c.K, c.group, c.ue8m0, xq, xs, stream.cuda_stream)
             sgq.sgq_fp8_block_gemm(xq, xs, wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, stream.cuda_stream)
         hd_host.copy_(hd_dev, non_blocking=True)
@@ -552,6 +689,8 @@ def main():
     ap.add_argument("--preheat", type=float, default=1.5,
                     help="seconds of identical load before the timed region (clock sampling)")
     ap.add_argument("--out-dir", default=None, help="directory for clock samples")
+    ap.add_argument("--cases", choices=["all", "none"], default="all",
+                    help="all: also time the M=1..8192 sweep, the prefill GEMMs and the quantiser alone")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws_, rank, local = dist_env()
