@@ -251,24 +251,67 @@ np.save(sys.argv[5], d.view(torch.int16).cpu().numpy())
 """
 
 
-@pytest.mark.parametrize("M,N,K,bk", [(16, 24576, 1536, 128), (8, 24576, 1536, 32)])
-def test_cluster_split_k_bit_identical(tmp_path, M, N, K, bk):
-    """Split-K inside clusters of two sums p0 + p1 as the global-workspace path
-    does: D equals that path's bit for bit (the child process plans with the
-    clusters off)."""
+def _child_gemm(tmp_path, name, env_extra, M, N, K, bk):
     import os
     import subprocess
     import sys
-    assert sgq.sgq_gemm_plan(M, N, K, bk)["ck"] == 1
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, SGQ_CK="0", PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"))
-    out = str(tmp_path / "d_global.npy")
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"), **env_extra)
+    out = str(tmp_path / f"{name}.npy")
     subprocess.run([sys.executable, "-c", _CK_CHILD, str(M), str(N), str(K), str(bk), out], env=env,
                    check=True, timeout=600, cwd=root)
+    return np.load(out)
+
+
+@pytest.mark.parametrize("M,N,K,bk", [(16, 24576, 1536, 128), (8, 24576, 1536, 32)])
+def test_cluster_split_k_bit_identical(tmp_path, M, N, K, bk):
+    """With the stream-K decode kernel off (SGQ_DECODE=0) these shapes take the
+    persistent swap-AB tiles with two K splits summed inside clusters of two;
+    that sums p0 + p1 as the global-workspace path does, so D equals that
+    path's bit for bit (both run in child processes, which read the switches)."""
+    d_ck = _child_gemm(tmp_path, "ck", {"SGQ_DECODE": "0"}, M, N, K, bk)
+    d_global = _child_gemm(tmp_path, "global", {"SGQ_DECODE": "0", "SGQ_CK": "0"}, M, N, K, bk)
+    assert np.array_equal(d_ck, d_global)
+
+
+STREAMK = [(1, 24576, 128, 128, 128), (3, 24576, 256, 32, 32), (17, 136, 1024, 128, 32), (31, 264, 640, 32, 128),
+           (32, 1032, 7168, 32, 32), (2, 8, 2048, 128, 128), (5, 7168, 384, 32, 32), (24, 24576, 1536, 128, 32)]
+
+
+@pytest.mark.parametrize("M,N,K,bn,bk", STREAMK)
+@pytest.mark.parametrize("pow2", [True, False])
+def test_stream_k_decode_shapes(M, N, K, bn, bk, pow2):
+    """Shapes that exercise the stream-K decode kernel's schedule: one unit per
+    row tile (K = 128: every CTA stores whole tiles, several per CTA), ranges
+    that span two or more row tiles, row tiles shared by many CTAs
+    (1032 x 7168: 56 units per tile), ragged N and M, both recipes, with UE8M0
+    scales (block-scaled MMA) and fp32 scales (promotion step)."""
+    assert sgq.sgq_gemm_plan(M, N, K, bk)["streamk"] == 1
+    c = synth.Case("streamk", M, N, K, bn, bk, pow2, seed=M + N + K)
+    aq, a_s = oracle.quant_token_group(c.x(), bk, pow2)
+    wq, ws = oracle.quant_weight_block(c.w(), bn, bk, pow2)
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, bn, bk)
+    args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+    d0 = sgq.fp8_block_gemm(*args, bn, bk)
+    assert sgq.sgq_device_status() == 0
+    check_gemm(d0, dref, bound, f"stream-K M={M} N={N} K={K} [{bn},{bk}] pow2={pow2}")
+    # the reduction order is fixed: a second call gives the same bits
+    assert torch.equal(d0, sgq.fp8_block_gemm(*args, bn, bk))
+
+
+def test_stream_k_and_persistent_tiles_agree(tmp_path):
+    """The decode workload's M = 16 GEMM through the stream-K kernel and, in a
+    child process with SGQ_DECODE=0, through the persistent swap-AB tiles:
+    both within the tolerance of the oracle (their fp32 summation orders
+    differ, so the bits may too)."""
+    M, N, K, bk = 16, 7168, 2048, 32
+    d_old = _child_gemm(tmp_path, "persistent", {"SGQ_DECODE": "0"}, M, N, K, bk)
     aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=31), bk, True)
     wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, True)
-    d = run_gpu(aq, a_s, wq, ws, bk, bk)
-    assert np.array_equal(d.view(torch.int16).cpu().numpy(), np.load(out))
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, bk, bk)
+    d_new = run_gpu(aq, a_s, wq, ws, bk, bk)
+    check_gemm(d_new, dref, bound, "stream-K")
+    check_gemm(torch.from_numpy(d_old).view(torch.bfloat16), dref, bound, "persistent tiles")
 
 
 _PAIR_CHILD = r"""

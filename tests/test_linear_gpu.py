@@ -98,6 +98,8 @@ def test_fused_edge_values():
         d2, xq2, xs2 = two_call(x.cuda(), wqd, wsd, bn, bk, ue)
         d1, xq1, xs1 = fused(x.cuda(), wqd, wsd, bn, bk, ue)
         assert torch.equal(xq1, xq2) and torch.equal(xs1, xs2) and torch.equal(d1, d2)
+        d0, _, _ = fused(x.cuda(), wqd, wsd, bn, bk, ue, outputs=False)   # one kernel
+        assert torch.equal(d0, d2)
         aq, a_s = oracle.quant_token_group(x, bk, ue)
         assert np.array_equal(xq1.cpu().numpy(), aq) and np.array_equal(xs1.cpu().numpy(), a_s)
 

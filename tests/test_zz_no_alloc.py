@@ -40,8 +40,13 @@ def _operands(M, N, K, blk, seed):
 
 
 def _plan_fits(M, N, K, blk):
+    """Whether the default plan's split-K partials fit the fixed array (the
+    stream-K decode kernel keeps two partial tiles per CTA)."""
     p = sgq.sgq_gemm_plan(M, N, K, blk)
-    return p["splits"] == 1 or p["items"] * 128 * p["bn"] * 4 <= NOALLOC_PARTIAL_BYTES
+    if p["splits"] == 1:
+        return True
+    tiles = p["grid"] * 2 if p["streamk"] else p["items"]
+    return tiles * 128 * p["bn"] * 4 <= NOALLOC_PARTIAL_BYTES
 
 
 @pytest.mark.parametrize("M", [16, 4])
