@@ -251,17 +251,24 @@ DecPlan make_dec_plan(int64_t M, int64_t N, int64_t K, int sm_count, size_t max_
     if (!d.use) return d;
     d.bn = M <= 16 ? 16 : 32;
     d.units = d.tiles * d.kst;
-    d.grid = d.units < sm_count ? d.units : sm_count;
+    // About 16 units (one row tile of 2048 K) per CTA: a grid that leaves
+    // SMs free for the next GEMM's weight stream; at least one CTA per row
+    // tile, at most one per SM.  SGQ_DEC_UPC (tuning) sets the target.
+    static const int upc_env = env_int("SGQ_DEC_UPC", 16);
+    const int upc = upc_env > 0 ? upc_env : 16;
+    int g = (d.units + upc - 1) / upc;
+    if (g < d.tiles) g = d.tiles;
+    if (g > sm_count) g = sm_count;
+    if (g > d.units) g = d.units;
+    d.grid = g;
     d.max_parts = 1;
     d.split = false;
-    auto begin = [&](int c) { return static_cast<int>(int64_t(c) * d.units / d.grid); };
     auto owner = [&](int u) { return static_cast<int>((int64_t(u + 1) * d.grid - 1) / d.units); };
     for (int t = 0; t < d.tiles; ++t) {
         const int parts = owner((t + 1) * d.kst - 1) - owner(t * d.kst) + 1;
         if (parts > d.max_parts) d.max_parts = parts;
     }
     d.split = d.max_parts > 1;
-    (void)begin;
     return d;
 }
 
@@ -360,6 +367,7 @@ sgq_status launch_decode(const DecPlan& d, const void* Aq, const float* As, cons
     a.kst = d.kst;
     a.units = d.units;
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
+    a.stall_unit = (flags & SGQ_GEMM_TEST_TIMEOUT) ? 2 : -1;
     sgq_status rc = status_word(&a.status);
     if (rc != SGQ_OK) return rc;
     if (d.split) {
@@ -383,6 +391,13 @@ sgq_status launch_decode(const DecPlan& d, const void* Aq, const float* As, cons
             a.counters = ws.counters;
         }
     }
+#ifdef SGQ_TRACE
+    {
+        void* tp = nullptr;
+        if (cudaGetSymbolAddress(&tp, g_gemm_trace) != cudaSuccess) return SGQ_ERR_CUDA;
+        a.trace = static_cast<unsigned long long*>(tp);
+    }
+#endif
     CUtensorMap tmW;
     if (make_tmap(&tmW, Wq, N, K, dec::kRows) != SGQ_OK) return SGQ_ERR_CUDA;
     const bool quant = fuse != nullptr;
@@ -447,6 +462,7 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     a.prefetch = prefetch;
     a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
     ExtArgs fz{};
+    fz.stall_job = (flags & SGQ_GEMM_TEST_TIMEOUT) ? 5 : -1;
     if (chan) {
         fz.sa = chan->sa;
         fz.sb = chan->sb;

@@ -51,6 +51,7 @@ constexpr int kBM = 128;          // MMA M: rows of the "A" operand per tile
 constexpr int kBK = 128;          // K elements (bytes) per pipeline stage
 constexpr int kEpiWarp0 = 3;      // warps: 0 producer, 1 MMA, 2 scale, 3.. epilogue, then scale 2, MMA 2
 constexpr uint64_t kTimeoutNs = 1ull << 30;
+constexpr uint64_t kTestTimeoutNs = 1ull << 20;   // about 1 ms
 // A wait reads the (global) abort flag only once it has lasted this long: the
 // load costs a memory round trip, which a wait that is about to complete
 // would add to its latency.
@@ -128,6 +129,9 @@ struct ExtArgs {
     const float* sb;
     const uint16_t* bias;
     int sa_n, sb_n;
+    // Testing (SGQ_GEMM_TEST_TIMEOUT): CTA 0's producer never loads its job
+    // number stall_job (< 0: off), and waits give up after kTestTimeoutNs.
+    int stall_job;
 };
 
 // Walks the (item, k-stage) jobs of one CTA (or CTA pair) in order.
@@ -194,6 +198,7 @@ __device__ __forceinline__ void trace_ev(const GemmArgs& a, int slot) {
 struct Sync {
     volatile uint32_t* abort_flag;
     uint32_t* status;
+    uint64_t limit;   // ns a wait may last before the kernel gives up (kTimeoutNs unless testing)
 };
 
 // kCl: acquire at cluster scope (barriers that the other CTA of a pair arrives on).
@@ -211,7 +216,7 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, con
         if ((++spins & 15u) == 0) {
             const uint64_t dt = ptx::globaltimer() - t0;
             if (dt > kAbortPollNs && *s.abort_flag) return false;
-            if (dt > kTimeoutNs) {
+            if (dt > s.limit) {
                 *s.abort_flag = 1u;
                 atomicOr(s.status, kStatusTimeout | (where << 8));
                 return false;
@@ -439,7 +444,8 @@ __global__ void __launch_bounds__(
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const Sync sync{reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
+    const Sync sync{reinterpret_cast<volatile uint32_t*>(misc + 1), a.status,
+                    fz.stall_job >= 0 ? kTestTimeoutNs : kTimeoutNs};
     // CTA pair: rank 0 leads (issues every tcgen05 op of the pair); a pair
     // walks the items with index blockIdx.x / 2.
     const uint32_t rank = kPair ? ptx::cluster_rank() : 0u;
@@ -649,6 +655,11 @@ __global__ void __launch_bounds__(
                 if (!wait_bar(empty_bar(stage), phase ^ 1u, sync, 1)) break;
                 if (lane == 0) trace_ev(a, 8 + (nj & 31));
                 ++nj;
+                if (nj - 1 == fz.stall_job && blockIdx.x == 0) {   // testing: this job is never loaded
+                    it.next(a);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    continue;
+                }
                 load_w(stage, it);
                 if (!dep_waited) {
                     ptx::grid_dependency_wait();
@@ -1411,7 +1422,7 @@ __global__ void __launch_bounds__(
                             if ((++spins & 15u) == 0) {
                                 const uint64_t dt = ptx::globaltimer() - t0;
                                 if (dt > kAbortPollNs && *sync.abort_flag) break;
-                                if (dt > kTimeoutNs) {
+                                if (dt > sync.limit) {
                                     *sync.abort_flag = 1u;
                                     atomicOr(sync.status, kStatusTimeout | (4u << 8));
                                     break;

@@ -68,6 +68,14 @@ typedef enum {
  * would take swap-AB tiles of 64 tokens. */
 #define SGQ_GEMM_ISSUE_ALT 2u
 #define SGQ_GEMM_ISSUE_SINGLE 4u
+/* Testing only: the first CTA never loads one of its weight tiles (the third
+ * unit of the decode kernel, the sixth K stage of the persistent tiles), so
+ * its bounded waits run out, after about 1 ms instead of about 1 s.  The
+ * kernel then stops issuing work, lets its copies and tensor-core operations
+ * land, frees its tensor memory and returns; sgq_device_status reports
+ * SGQ_ERR_TIMEOUT and D is undefined.  The stream stays usable.  Needs a
+ * shape whose first CTA has that many units or stages. */
+#define SGQ_GEMM_TEST_TIMEOUT 8u
 
 /*
  * Per-token-group quantisation.

@@ -365,3 +365,27 @@ def test_cta_pair_tiles_match_oracle():
     r = subprocess.run([sys.executable, "-c", _PAIR_CHILD], env=env, cwd=root, timeout=900,
                        capture_output=True, text=True)
     assert r.returncode == 0 and "pair ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
+
+
+@pytest.mark.parametrize("M,N,K,bk,flags", [(16, 7168, 2048, 32, 0), (256, 256, 2048, 128, sgq.SGQ_GEMM_ISSUE_SINGLE)])
+def test_bounded_wait_times_out_and_the_stream_recovers(M, N, K, bk, flags):
+    """The bounded device-side waits: with SGQ_GEMM_TEST_TIMEOUT the first CTA
+    never loads one of its weight tiles, so the wait for it runs out (after
+    about 1 ms).  The kernel must return on its own, sgq_device_status must
+    report SGQ_ERR_TIMEOUT (once: reading clears it), and a normal GEMM on the
+    same stream right after must be correct -- for the stream-K decode kernel
+    (M = 16) and the persistent wide tiles (M = 256)."""
+    from fp8_block_scaled_sgq_gb300 import binding
+    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=41), bk, True)
+    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=41), bk, bk, True)
+    args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+    d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    sgq.sgq_fp8_block_gemm_ex(*args, d, M, N, K, bk, bk, flags | binding.SGQ_GEMM_TEST_TIMEOUT)
+    assert sgq.sgq_device_status() == binding.SGQ_ERR_TIMEOUT
+    assert sgq.sgq_device_status() == binding.SGQ_OK
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, bk, bk)
+    for _ in range(2):
+        d2 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        sgq.sgq_fp8_block_gemm_ex(*args, d2, M, N, K, bk, bk, flags)
+        assert sgq.sgq_device_status() == binding.SGQ_OK
+        check_gemm(d2, dref, bound, f"after the time-out M={M}")

@@ -49,11 +49,13 @@ def _plan_fits(M, N, K, blk):
     return tiles * 128 * p["bn"] * 4 <= NOALLOC_PARTIAL_BYTES
 
 
-@pytest.mark.parametrize("M", [16, 4])
-def test_noalloc_matches_default_entry_point_twice(M):
+@pytest.mark.parametrize("M,N,K", [(16, 1536, 7168), (4, 1536, 7168), (64, 7168, 2048)])
+def test_noalloc_matches_default_entry_point_twice(M, N, K):
+    """Decode shapes whose plans split K (the stream-K kernel at M <= 32, the
+    persistent swap-AB tiles at M = 64), so the fixed array is used."""
     build.build()
     lib = binding.load_library()
-    N, K, blk = 7168, 2048, 32
+    blk = 32
     assert sgq.sgq_gemm_plan(M, N, K, blk)["splits"] > 1   # the case exercises the fixed array
     assert _plan_fits(M, N, K, blk)                        # ... under the default plan
     aq, a_s, wq, ws = _operands(M, N, K, blk, 21)
@@ -112,7 +114,8 @@ from fp8_block_scaled_sgq_gb300 import binding, synth
 import oracle
 from common import check_gemm
 lib = binding.load_library()
-M, N, K, blk = 16, 7168, 2048, 32
+M, N, K, blk = 16, 1536, 7168, 32
+assert sgq.sgq_gemm_plan(M, N, K, blk)["splits"] > 1
 x, w = synth.activation(M, K, seed=23), synth.weight(N, K, seed=23)
 aq, a_s = oracle.quant_token_group(x, blk, True)
 wq, ws = oracle.quant_weight_block(w, blk, blk, True)
