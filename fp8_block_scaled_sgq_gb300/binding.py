@@ -204,12 +204,12 @@ def sgq_version() -> int:
     return int(load_library().sgq_version())
 
 
-PLAN_FIELDS = ("swap", "bn", "splits", "items", "grid", "alt", "ck", "pair", "streamk")
+PLAN_FIELDS = ("swap", "bn", "splits", "items", "grid", "alt", "ck", "pair")
 
 
 def sgq_gemm_plan(M, N, K, blk_k, sm_count=152) -> dict:
     """The GEMM's launch plan for this problem (host only; see include/sgq.h)."""
-    out = (ctypes.c_int32 * 9)()
+    out = (ctypes.c_int32 * 8)()
     _check(load_library().sgq_gemm_plan(M, N, K, blk_k, sm_count, ctypes.cast(out, ctypes.c_void_p)),
            "sgq_gemm_plan")
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))

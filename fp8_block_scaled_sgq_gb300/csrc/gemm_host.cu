@@ -9,7 +9,6 @@
 #include <cstdlib>
 #include <mutex>
 
-#include "gemm_decode.cuh"
 #include "gemm_kernel.cuh"
 
 namespace sgq {
@@ -228,50 +227,6 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, bool wi
     return p;
 }
 
-// Decode-sized M (<= 32 tokens, K a multiple of 128): the stream-K kernel of
-// gemm_decode.cuh.  units = row tiles x K stages of 128; a grid of at most
-// one CTA per SM, each taking units/grid consecutive units.  SGQ_DECODE=0
-// (tuning and testing) keeps those shapes on the persistent tiles above.
-struct DecPlan {
-    bool use;
-    int bn, tiles, kst, units, grid;
-    int max_parts;        // most CTAs contributing to one row tile
-    bool split;           // some row tile is split over several CTAs (needs scratch)
-};
-
-DecPlan make_dec_plan(int64_t M, int64_t N, int64_t K, int sm_count, size_t max_counters) {
-    DecPlan d{};
-    static const int dec_env = env_int("SGQ_DECODE", 1);
-    static const int grid_max = env_int("SGQ_GRID_MAX", 0);
-    if (grid_max > 0 && grid_max < sm_count) sm_count = grid_max;
-    d.tiles = static_cast<int>((N + dec::kRows - 1) / dec::kRows);
-    d.kst = static_cast<int>(K / dec::kUnitK);
-    d.use = dec_env != 0 && M <= 32 && K % dec::kUnitK == 0 && size_t(d.tiles) <= max_counters &&
-            int64_t(d.tiles) * d.kst < (int64_t(1) << 30);
-    if (!d.use) return d;
-    d.bn = M <= 16 ? 16 : 32;
-    d.units = d.tiles * d.kst;
-    // About 16 units (one row tile of 2048 K) per CTA: a grid that leaves
-    // SMs free for the next GEMM's weight stream; at least one CTA per row
-    // tile, at most one per SM.  SGQ_DEC_UPC (tuning) sets the target.
-    static const int upc_env = env_int("SGQ_DEC_UPC", 16);
-    const int upc = upc_env > 0 ? upc_env : 16;
-    int g = (d.units + upc - 1) / upc;
-    if (g < d.tiles) g = d.tiles;
-    if (g > sm_count) g = sm_count;
-    if (g > d.units) g = d.units;
-    d.grid = g;
-    d.max_parts = 1;
-    d.split = false;
-    auto owner = [&](int u) { return static_cast<int>((int64_t(u + 1) * d.grid - 1) / d.units); };
-    for (int t = 0; t < d.tiles; ++t) {
-        const int parts = owner((t + 1) * d.kst - 1) - owner(t * d.kst) + 1;
-        if (parts > d.max_parts) d.max_parts = parts;
-    }
-    d.split = d.max_parts > 1;
-    return d;
-}
-
 // Address of the device status word on the current device.
 uint32_t* g_status_ptr[64] = {};
 std::mutex g_status_mu;
@@ -342,69 +297,6 @@ struct Chan {
     const void* bias;
 };
 
-// Launches the decode-sized stream-K kernel (plan d): scratch for the split
-// row tiles' partials from the per-device workspace or, for the
-// allocation-free entry point, from the fixed array.
-sgq_status launch_decode(const DecPlan& d, const void* Aq, const float* As, const void* Wq, const float* Ws,
-                         void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k, uint32_t flags, bool noalloc,
-                         const Fuse* fuse, cudaStream_t st) {
-    dec::DecArgs a{};
-    a.Aq = static_cast<const uint8_t*>(Aq);
-    a.As = As;
-    if (fuse) {
-        a.x = static_cast<const uint16_t*>(fuse->x);
-        a.xq_out = static_cast<uint8_t*>(fuse->xq);
-        a.xs_out = fuse->xs;
-        a.ue8m0 = fuse->ue8m0;
-    }
-    a.Ws = Ws;
-    a.D = static_cast<__nv_bfloat16*>(D);
-    a.M = static_cast<int>(M);
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.ks = static_cast<int>(K / blk_k);
-    a.tiles = d.tiles;
-    a.kst = d.kst;
-    a.units = d.units;
-    a.force_promote = (flags & SGQ_GEMM_FORCE_PROMOTE) ? 1 : 0;
-    a.stall_unit = (flags & SGQ_GEMM_TEST_TIMEOUT) ? 2 : -1;
-    sgq_status rc = status_word(&a.status);
-    if (rc != SGQ_OK) return rc;
-    if (d.split) {
-        const size_t part_bytes = size_t(d.grid) * 2 * dec::kRows * size_t(d.bn) * sizeof(float);
-        if (noalloc) {
-            const size_t ctr_bytes = size_t(d.tiles) * sizeof(uint32_t);
-            if (ctr_bytes > kNoAllocCounterBytes || part_bytes > kNoAllocPartialBytes) return SGQ_ERR_UNSUPPORTED;
-            unsigned char* base = nullptr;
-            rc = noalloc_scratch(&base);
-            if (rc != SGQ_OK) return rc;
-            a.counters = reinterpret_cast<uint32_t*>(base);
-            a.partial = reinterpret_cast<float*>(base + kNoAllocCounterBytes);
-            // the array keeps the previous call's contents; the counters must start at zero
-            if (cudaMemsetAsync(a.counters, 0, ctr_bytes, st) != cudaSuccess) return SGQ_ERR_CUDA;
-        } else {
-            if (part_bytes > kWsBytes) return SGQ_ERR_UNSUPPORTED;
-            DevWs ws;
-            rc = get_workspace(st, &ws);
-            if (rc != SGQ_OK) return rc;
-            a.partial = ws.partial;
-            a.counters = ws.counters;
-        }
-    }
-#ifdef SGQ_TRACE
-    {
-        void* tp = nullptr;
-        if (cudaGetSymbolAddress(&tp, g_gemm_trace) != cudaSuccess) return SGQ_ERR_CUDA;
-        a.trace = static_cast<unsigned long long*>(tp);
-    }
-#endif
-    CUtensorMap tmW;
-    if (make_tmap(&tmW, Wq, N, K, dec::kRows) != SGQ_OK) return SGQ_ERR_CUDA;
-    const bool quant = fuse != nullptr;
-    return blk_n == 32 ? dec::dispatch_n32(blk_k, d.bn, quant, tmW, a, d.grid, st)
-                       : dec::dispatch_n128(blk_k, d.bn, quant, tmW, a, d.grid, st);
-}
-
 // Plans and launches one GEMM.  noalloc: split-K scratch from the fixed array
 // (its counters cleared by an asynchronous memset), else the per-device
 // workspace.  fuse (Aq/As unused): the activations are quantised inside the
@@ -418,11 +310,6 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     sgq_status rc = device_info(&di);
     if (rc != SGQ_OK) return rc;
     if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
-    if (!chan && (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) == 0) {
-        const DecPlan d = make_dec_plan(M, N, K, di.sm_count,
-                                        noalloc ? kNoAllocCounterBytes / sizeof(uint32_t) : size_t(kMaxCounters));
-        if (d.use) return launch_decode(d, Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags, noalloc, fuse, st);
-    }
     // The allocation-free entry point plans within its fixed array: split
     // counts whose partials or counters would not fit are skipped, so such a
     // shape runs with fewer K splits (or, at mid M, on the 128 x 256 tiles
@@ -565,18 +452,10 @@ sgq_status launch_fp8_block_gemm_noalloc(const void* Aq, const float* As, const 
 // fp8_scaled_mm: D = (Aq Wq^T) * sa * sb + bias.  The plan is the block GEMM's
 // for blk_k = 128 (the scale arguments of the block path stay unused).
 sgq_status gemm_plan_query(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out) {
-    const gemm::DecPlan d = gemm::make_dec_plan(M, N, K, sm_count, size_t(gemm::kMaxCounters));
-    if (d.use) {
-        // stream-K decode tiles: items = units (row tile x K stage), splits =
-        // the most CTAs sharing one row tile
-        const int32_t v[9] = {1, d.bn, d.max_parts, d.units, d.grid, 0, 0, 0, 1};
-        for (int i = 0; i < 9; ++i) out[i] = v[i];
-        return SGQ_OK;
-    }
     const gemm::Plan p = gemm::make_plan(M, N, K, blk_k, sm_count);
-    const int32_t v[9] = {p.swap ? 1 : 0, p.bn, p.splits, p.items, p.grid, p.alt ? 1 : 0, p.ck ? 1 : 0,
-                          p.pair ? 1 : 0, 0};
-    for (int i = 0; i < 9; ++i) out[i] = v[i];
+    const int32_t v[8] = {p.swap ? 1 : 0, p.bn, p.splits, p.items, p.grid, p.alt ? 1 : 0, p.ck ? 1 : 0,
+                          p.pair ? 1 : 0};
+    for (int i = 0; i < 8; ++i) out[i] = v[i];
     return SGQ_OK;
 }
 

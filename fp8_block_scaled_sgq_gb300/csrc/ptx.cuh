@@ -73,21 +73,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
-// Prefetch of a 2-D tile into L2 (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // ------------------------------------------------------------------ cp.async
 // 4-byte global -> shared copy through the LSU async path (Ampere-style).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-// 16-byte global -> shared copy through the LSU async path, bypassing L1.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -102,10 +91,7 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
         case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
         case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
         case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
-        case 7: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
-        case 8: asm volatile("cp.async.wait_group 8;" ::: "memory"); break;
-        case 9: asm volatile("cp.async.wait_group 9;" ::: "memory"); break;
-        default: asm volatile("cp.async.wait_group 10;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
     }
 }
 
@@ -265,57 +251,6 @@ __device__ __forceinline__ void tma_load_2d_if(uint32_t pred, uint32_t dst, cons
         : "memory");
 }
 
-
-// ------------------------------------------------------------------ elected issue
-// A converged warp elects one lane (elect.sync) for each of these; the same
-// lane is elected every time the whole warp is active, so MMAs and the commit
-// that tracks them come from one thread.
-
-// One block-scaled 128-wide K stage: the scale-factor copies of A and B into
-// TMEM, four K = 32 MMAs (byte j of each scale word for MMA j) accumulating
-// into d (the first one starts over when acc == 0), then a commit to `bar`.
-__device__ __forceinline__ void mx_stage_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t i0, uint32_t i1,
-                                               uint32_t i2, uint32_t i3, uint32_t sfa_t, uint32_t sfb_t,
-                                               uint64_t sfa_d, uint64_t sfb_d, uint32_t acc, uint32_t bar) {
-    asm volatile(
-        "{\n.reg .pred e, q, t;\n.reg .b64 a1, a2, a3, b1, b2, b3;\n"
-        "elect.sync _|e, 0xffffffff;\n"
-        "setp.ne.b32 q, %9, 0;\n"
-        "setp.eq.u32 t, %0, %0;\n"
-        "add.s64 a1, %1, 2;\nadd.s64 a2, %1, 4;\nadd.s64 a3, %1, 6;\n"
-        "add.s64 b1, %2, 2;\nadd.s64 b2, %2, 4;\nadd.s64 b3, %2, 6;\n"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%7], %11;\n"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%8], %12;\n"
-        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%7], [%8], q;\n"
-        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a1, b1, %4, [%7], [%8], t;\n"
-        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a2, b2, %5, [%7], [%8], t;\n"
-        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a3, b3, %6, [%7], [%8], t;\n"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n}" ::"r"(d),
-        "l"(a), "l"(b), "r"(i0), "r"(i1), "r"(i2), "r"(i3), "r"(sfa_t), "r"(sfb_t), "r"(acc), "r"(bar), "l"(sfa_d),
-        "l"(sfb_d)
-        : "memory");
-}
-// One unscaled K = 32 MMA (kind::f8f6f4).
-__device__ __forceinline__ void mma_f8_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n.reg .pred e, q;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 q, %4, 0;\n"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, q;\n}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// Commit (arrive on `bar` when this lane's earlier tcgen05 ops are done).
-__device__ __forceinline__ void commit_elect(uint32_t bar) {
-    asm volatile(
-        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
-        : "memory");
-}
-// mbarrier arrive by the elected lane.
-__device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
-    asm volatile(
-        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n@e mbarrier.arrive.shared::cta.b64 _, [%0];\n}" ::"r"(bar)
-        : "memory");
-}
 
 // ------------------------------------------------------------------ CTA pairs
 // A cluster of two CTAs (ranks 0 and 1) drives one tcgen05 unit pair: rank 0

@@ -68,13 +68,12 @@ typedef enum {
  * would take swap-AB tiles of 64 tokens. */
 #define SGQ_GEMM_ISSUE_ALT 2u
 #define SGQ_GEMM_ISSUE_SINGLE 4u
-/* Testing only: the first CTA never loads one of its weight tiles (the third
- * unit of the decode kernel, the sixth K stage of the persistent tiles), so
- * its bounded waits run out, after about 1 ms instead of about 1 s.  The
- * kernel then stops issuing work, lets its copies and tensor-core operations
- * land, frees its tensor memory and returns; sgq_device_status reports
- * SGQ_ERR_TIMEOUT and D is undefined.  The stream stays usable.  Needs a
- * shape whose first CTA has that many units or stages. */
+/* Testing only: the first CTA never loads the weight tile of its sixth K
+ * stage, so its bounded waits run out, after about 1 ms instead of about 1 s.
+ * The kernel then stops issuing work, lets its copies and tensor-core
+ * operations land, frees its tensor memory and returns; sgq_device_status
+ * reports SGQ_ERR_TIMEOUT and D is undefined.  The stream stays usable.
+ * Needs a shape whose first CTA has at least six K stages. */
 #define SGQ_GEMM_TEST_TIMEOUT 8u
 
 /*
@@ -300,16 +299,12 @@ uint64_t sgq_allocated_bytes(void);
 /*
  * The launch plan sgq_fp8_block_gemm would use for this problem on a device
  * with `sm_count` SMs; host only (no device is touched), for tests and tools.
- * out (host, 9 entries, caller-owned): [0] 1 for swap-AB tiles (weights on the
+ * out (host, 8 entries, caller-owned): [0] 1 for swap-AB tiles (weights on the
  * MMA's 128-row side), [1] tile width BN (tokens for swap-AB, else columns),
  * [2] K splits, [3] work items (tiles x splits), [4] persistent grid before
  * the occupancy cap, [5] 1 for two alternating MMA issuers, [6] 1 for split-K
- * summed inside clusters of two, [7] 1 for CTA pairs, [8] 1 for the stream-K
- * decode kernel (M <= 32, K a multiple of 128): then [3] counts units of 128
- * weight rows x 128 K, each CTA of the grid [4] takes [3]/[4] consecutive
- * units, and [2] is the most CTAs that share one row tile.
- * SGQ_ERR_INVALID_ARG for out == NULL, M, N or K < 1, blk_k not 32 or 128,
- * or sm_count < 1.
+ * summed inside clusters of two, [7] 1 for CTA pairs.  SGQ_ERR_INVALID_ARG for
+ * out == NULL, M, N or K < 1, blk_k not 32 or 128, or sm_count < 1.
  */
 sgq_status sgq_gemm_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out);
 

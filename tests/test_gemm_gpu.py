@@ -265,106 +265,39 @@ def _child_gemm(tmp_path, name, env_extra, M, N, K, bk):
 
 @pytest.mark.parametrize("M,N,K,bk", [(16, 24576, 1536, 128), (8, 24576, 1536, 32)])
 def test_cluster_split_k_bit_identical(tmp_path, M, N, K, bk):
-    """With the stream-K decode kernel off (SGQ_DECODE=0) these shapes take the
-    persistent swap-AB tiles with two K splits summed inside clusters of two;
-    that sums p0 + p1 as the global-workspace path does, so D equals that
-    path's bit for bit (both run in child processes, which read the switches)."""
-    d_ck = _child_gemm(tmp_path, "ck", {"SGQ_DECODE": "0"}, M, N, K, bk)
-    d_global = _child_gemm(tmp_path, "global", {"SGQ_DECODE": "0", "SGQ_CK": "0"}, M, N, K, bk)
-    assert np.array_equal(d_ck, d_global)
+    """Split-K inside clusters of two sums p0 + p1 as the global-workspace path
+    does: D equals that path's bit for bit (the child process plans with the
+    clusters off)."""
+    assert sgq.sgq_gemm_plan(M, N, K, bk)["ck"] == 1
+    d_global = _child_gemm(tmp_path, "global", {"SGQ_CK": "0"}, M, N, K, bk)
+    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=31), bk, True)
+    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, True)
+    d = run_gpu(aq, a_s, wq, ws, bk, bk)
+    assert np.array_equal(d.view(torch.int16).cpu().numpy(), d_global)
 
 
-STREAMK = [(1, 24576, 128, 128, 128), (3, 24576, 256, 32, 32), (17, 136, 1024, 128, 32), (31, 264, 640, 32, 128),
+DECODE_SHAPES = [(1, 24576, 128, 128, 128), (3, 24576, 256, 32, 32), (17, 136, 1024, 128, 32), (31, 264, 640, 32, 128),
            (32, 1032, 7168, 32, 32), (2, 8, 2048, 128, 128), (5, 7168, 384, 32, 32), (24, 24576, 1536, 128, 32)]
 
 
-@pytest.mark.parametrize("M,N,K,bn,bk", STREAMK)
+@pytest.mark.parametrize("M,N,K,bn,bk", DECODE_SHAPES)
 @pytest.mark.parametrize("pow2", [True, False])
-def test_stream_k_decode_shapes(M, N, K, bn, bk, pow2):
-    """Shapes that exercise the stream-K decode kernel's schedule: one unit per
-    row tile (K = 128: every CTA stores whole tiles, several per CTA), ranges
-    that span two or more row tiles, row tiles shared by many CTAs
-    (1032 x 7168: 56 units per tile), ragged N and M, both recipes, with UE8M0
-    scales (block-scaled MMA) and fp32 scales (promotion step)."""
-    assert sgq.sgq_gemm_plan(M, N, K, bk)["streamk"] == 1
-    c = synth.Case("streamk", M, N, K, bn, bk, pow2, seed=M + N + K)
+def test_decode_shapes(M, N, K, bn, bk, pow2):
+    """Decode-sized shapes of the swap-AB plans: one K stage (K = 128), long K
+    split many ways (1032 x 7168), a single row tile split over 16 CTAs
+    (N = 8, K = 2048), more row tiles than SMs (N = 24576), ragged N and M,
+    both recipes, UE8M0 scales (block-scaled MMA) and fp32 scales
+    (promotion); and the fixed split-K summation order: a second call gives
+    the same bits."""
+    c = synth.Case("decode", M, N, K, bn, bk, pow2, seed=M + N + K)
     aq, a_s = oracle.quant_token_group(c.x(), bk, pow2)
     wq, ws = oracle.quant_weight_block(c.w(), bn, bk, pow2)
     dref, bound = oracle.gemm(aq, a_s, wq, ws, bn, bk)
     args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
     d0 = sgq.fp8_block_gemm(*args, bn, bk)
     assert sgq.sgq_device_status() == 0
-    check_gemm(d0, dref, bound, f"stream-K M={M} N={N} K={K} [{bn},{bk}] pow2={pow2}")
-    # the reduction order is fixed: a second call gives the same bits
+    check_gemm(d0, dref, bound, f"decode M={M} N={N} K={K} [{bn},{bk}] pow2={pow2}")
     assert torch.equal(d0, sgq.fp8_block_gemm(*args, bn, bk))
-
-
-def test_stream_k_and_persistent_tiles_agree(tmp_path):
-    """The decode workload's M = 16 GEMM through the stream-K kernel and, in a
-    child process with SGQ_DECODE=0, through the persistent swap-AB tiles:
-    both within the tolerance of the oracle (their fp32 summation orders
-    differ, so the bits may too)."""
-    M, N, K, bk = 16, 7168, 2048, 32
-    d_old = _child_gemm(tmp_path, "persistent", {"SGQ_DECODE": "0"}, M, N, K, bk)
-    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=31), bk, True)
-    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, True)
-    dref, bound = oracle.gemm(aq, a_s, wq, ws, bk, bk)
-    d_new = run_gpu(aq, a_s, wq, ws, bk, bk)
-    check_gemm(d_new, dref, bound, "stream-K")
-    check_gemm(torch.from_numpy(d_old).view(torch.bfloat16), dref, bound, "persistent tiles")
-
-
-_PAIR_CHILD = r"""
-import sys, numpy as np, torch
-import fp8_block_scaled_sgq_gb300 as sgq
-from fp8_block_scaled_sgq_gb300 import synth
-import oracle
-from common import check_gemm, tile_rows
-cases = [(300, 520, 1024, 128, 128, "pow2"), (300, 520, 1024, 32, 32, "half"), (257, 1032, 4096, 128, 32, "mixed"),
-         (513, 264, 2048, 32, 32, "fp32"), (4096, 7168, 7168, 128, 128, "prefill")]
-for M, N, K, bn, bk, kind in cases:
-    assert sgq.sgq_gemm_plan(M, N, K, bk)["pair"] == 1, (M, N, K, bk)
-    if kind == "prefill":
-        c = synth.WORKLOADS["prefill_block128"][0]
-        x, w = c.x(), c.w()
-    else:
-        x, w = synth.activation(M, K, seed=M + 3), synth.weight(N, K, seed=N + 3)
-    ue = kind != "fp32"
-    aq, a_s = oracle.quant_token_group(x, bk, ue)
-    wq, ws = oracle.quant_weight_block(w, bn, bk, ue)
-    stage_cols = 128 // bk
-    if kind == "half":      # one half of the first 256-row tile not a power of two
-        for st in (1, 4, 5):
-            a_s[130:140, st * stage_cols:(st + 1) * stage_cols] *= np.float32(1.3)
-    if kind == "mixed":     # some stages' weight scales not powers of two
-        rng = np.random.default_rng(7)
-        for st in range(K // 128):
-            if rng.random() < 0.4:
-                ws[:, st * stage_cols:(st + 1) * stage_cols] *= np.float32(1.3)
-    d = sgq.fp8_block_gemm(*(torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)), bn, bk)
-    assert sgq.sgq_device_status() == 0
-    r = np.arange(M) if M <= 600 else tile_rows(M, seed=5)
-    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
-    check_gemm(d[torch.from_numpy(r).cuda()], dref, bound, f"pair M={M} N={N} K={K} {kind}")
-print("pair ok")
-"""
-
-
-def test_cta_pair_tiles_match_oracle():
-    """The opt-in CTA-pair plan (SGQ_PAIR=1: 256-row tiles on clusters of two,
-    cta_group::2 MMAs issued by the leader for both CTAs) on ragged, one-half
-    non-power-of-two, mixed-scale, fp32-scale and the full prefill [128,128]
-    shapes, against the oracle (every row of the ragged shapes; one row of
-    every 64-row block of the prefill shape).  Run in a child process, since
-    the launch plan reads its switches once per process."""
-    import os
-    import subprocess
-    import sys
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, SGQ_PAIR="1", SGQ_MIDSWAP="0", PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"))
-    r = subprocess.run([sys.executable, "-c", _PAIR_CHILD], env=env, cwd=root, timeout=900,
-                       capture_output=True, text=True)
-    assert r.returncode == 0 and "pair ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
 
 
 @pytest.mark.parametrize("M,N,K,bk,flags", [(16, 7168, 2048, 32, 0), (256, 256, 2048, 128, sgq.SGQ_GEMM_ISSUE_SINGLE)])
@@ -373,8 +306,8 @@ def test_bounded_wait_times_out_and_the_stream_recovers(M, N, K, bk, flags):
     never loads one of its weight tiles, so the wait for it runs out (after
     about 1 ms).  The kernel must return on its own, sgq_device_status must
     report SGQ_ERR_TIMEOUT (once: reading clears it), and a normal GEMM on the
-    same stream right after must be correct -- for the stream-K decode kernel
-    (M = 16) and the persistent wide tiles (M = 256)."""
+    same stream right after must be correct -- for the swap-AB decode tiles
+    with split-K (M = 16) and the wide tiles (M = 256)."""
     from fp8_block_scaled_sgq_gb300 import binding
     aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=41), bk, True)
     wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=41), bk, bk, True)

@@ -20,39 +20,27 @@ def plan(M, N, K, bk, sms=SMS):
     return sgq.sgq_gemm_plan(M, N, K, bk, sms)
 
 
-def test_decode_block32_stream_k():
-    """M <= 32 with K a multiple of 128: the stream-K decode kernel, one CTA per
-    SM, each taking 896 / 152 (5 or 6) consecutive units of 128 weight rows x
-    128 K; a row tile of 16 units is shared by at most four CTAs."""
+def test_decode_block32_swap_ab_two_splits():
     p = plan(16, 7168, 2048, 32)
-    assert p == {"swap": 1, "bn": 16, "splits": 4, "items": 896, "grid": 152, "alt": 0, "ck": 0, "pair": 0,
-                 "streamk": 1}
+    assert p == {"swap": 1, "bn": 16, "splits": 2, "items": 112, "grid": 112, "alt": 0, "ck": 0, "pair": 0}
 
 
-@pytest.mark.parametrize("M,bn,streamk", [(1, 16, 1), (16, 16, 1), (17, 32, 1), (32, 32, 1), (33, 64, 0),
-                                          (64, 64, 0)])
-def test_swap_ab_tile_width_follows_tokens(M, bn, streamk):
+@pytest.mark.parametrize("M,bn", [(1, 16), (16, 16), (17, 32), (32, 32), (33, 64), (64, 64)])
+def test_swap_ab_tile_width_follows_tokens(M, bn):
     p = plan(M, 7168, 2048, 32)
-    assert p["swap"] == 1 and p["bn"] == bn and p["streamk"] == streamk
-
-
-def test_stream_k_needs_whole_k_stages():
-    # K not a multiple of 128: the persistent swap-AB tiles
-    p = plan(16, 264, 160, 32)
-    assert p["streamk"] == 0 and p["swap"] == 1
+    assert p["swap"] == 1 and p["bn"] == bn
 
 
 def test_cluster_split_k_only_with_several_items_per_cta():
-    # M = 64 keeps the persistent swap-AB tiles; clusters need BN <= 32, so no
-    # configuration of the sweep's shapes takes them now: check the rule itself
-    p = plan(64, 24576, 1536, 128)
-    assert p["streamk"] == 0 and p["ck"] == 0
+    p = plan(16, 24576, 1536, 128)
+    assert p["swap"] == 1 and p["splits"] == 2 and p["items"] > p["grid"] and p["ck"] == 1
+    # one item per CTA: the global workspace path
+    assert plan(16, 7168, 2048, 128)["ck"] == 0
 
 
 def test_narrow_n_splits_k_across_the_grid():
     p = plan(1, 1536, 7168, 128)
-    assert p["swap"] == 1 and p["streamk"] == 1 and p["items"] == 12 * 56 and p["grid"] == 152
-    assert p["splits"] == 14   # 56 units per row tile, about 4.4 per CTA
+    assert p["swap"] == 1 and p["splits"] == 12 and p["items"] == 144 and p["grid"] == 144
 
 
 def test_mid_m_swap_ab_where_wide_tiles_leave_sms_idle():
@@ -80,15 +68,6 @@ SHAPES = list(itertools.product([1, 5, 16, 33, 64, 65, 128, 300, 512, 1024, 1025
 @pytest.mark.parametrize("M,N,K,bk", [s for s in SHAPES if s[2] % s[3] == 0])
 def test_plan_invariants(M, N, K, bk):
     p = plan(M, N, K, bk)
-    if p["streamk"]:
-        assert M <= 32 and K % 128 == 0 and p["swap"] == 1 and p["bn"] == (16 if M <= 16 else 32)
-        units = math.ceil(N / 128) * (K // 128)
-        assert p["items"] == units and p["grid"] == min(units, SMS)
-        per = units // p["grid"]
-        # the most CTAs one row tile of K / 128 units can span
-        assert 1 <= p["splits"] <= math.ceil((K // 128 - 1) / per) + 1
-        assert not (p["alt"] or p["ck"] or p["pair"])
-        return
     if p["swap"]:
         tiles = math.ceil(N / 128) * math.ceil(M / p["bn"])
         assert p["bn"] in (16, 32, 64)
@@ -114,11 +93,8 @@ def test_plan_invariants(M, N, K, bk):
 def test_grid_follows_the_sm_count():
     assert plan(4096, 7168, 7168, 128, sms=76)["grid"] == 76
     # more SMs, more K splits, still one wave
-    p = plan(64, 7168, 2048, 32, sms=1000)
+    p = plan(16, 7168, 2048, 32, sms=1000)
     assert p["splits"] > 2 and p["items"] <= 1000 and p["grid"] == p["items"]
-    # stream-K: one CTA per SM, or per unit when there are fewer units
-    assert plan(16, 7168, 2048, 32, sms=76)["grid"] == 76
-    assert plan(16, 256, 512, 128, sms=152)["grid"] == 8
 
 
 def test_plan_rejects_bad_arguments():

@@ -40,19 +40,14 @@ def _operands(M, N, K, blk, seed):
 
 
 def _plan_fits(M, N, K, blk):
-    """Whether the default plan's split-K partials fit the fixed array (the
-    stream-K decode kernel keeps two partial tiles per CTA)."""
+    """Whether the default plan's split-K partials fit the fixed array."""
     p = sgq.sgq_gemm_plan(M, N, K, blk)
-    if p["splits"] == 1:
-        return True
-    tiles = p["grid"] * 2 if p["streamk"] else p["items"]
-    return tiles * 128 * p["bn"] * 4 <= NOALLOC_PARTIAL_BYTES
+    return p["splits"] == 1 or p["items"] * 128 * p["bn"] * 4 <= NOALLOC_PARTIAL_BYTES
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 1536, 7168), (4, 1536, 7168), (64, 7168, 2048)])
 def test_noalloc_matches_default_entry_point_twice(M, N, K):
-    """Decode shapes whose plans split K (the stream-K kernel at M <= 32, the
-    persistent swap-AB tiles at M = 64), so the fixed array is used."""
+    """Decode shapes whose plans split K, so the fixed array is used."""
     build.build()
     lib = binding.load_library()
     blk = 32
