@@ -9,6 +9,7 @@ from __future__ import annotations
 
 from .binding import (  # noqa: F401
     EXPORTS, SGQ_GEMM_DEFAULT, SGQ_GEMM_FORCE_PROMOTE, SGQ_GEMM_ISSUE_ALT, SGQ_GEMM_ISSUE_SINGLE, SgqError,
+    SGQ_GEMM_SCALES_POW2, SGQ_GEMM_TEST_TIMEOUT,
     load_library, sgq_device_status,
     sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_fp8_block_linear, sgq_fp8_scaled_mm,
     sgq_quant_per_tensor, sgq_quant_per_token, sgq_quant_token_group_v2, sgq_launch_count, sgq_quant_token_group,

@@ -28,6 +28,7 @@ SGQ_GEMM_FORCE_PROMOTE = 1
 SGQ_GEMM_ISSUE_ALT = 2
 SGQ_GEMM_ISSUE_SINGLE = 4
 SGQ_GEMM_TEST_TIMEOUT = 8
+SGQ_GEMM_SCALES_POW2 = 16
 
 # Symbols declared in include/sgq.h (checked by the tests).
 EXPORTS = (

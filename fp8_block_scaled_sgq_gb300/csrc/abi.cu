@@ -79,7 +79,7 @@ sgq_status sgq_fp8_block_gemm_ex(const void* Aq, const float* As, const void* Wq
     if (M < 0 || N <= 0 || K <= 0 || (blk_n != 32 && blk_n != 128) || (blk_k != 32 && blk_k != 128) ||
         K % blk_k != 0 || N % 8 != 0 ||
         (flags & ~uint32_t(SGQ_GEMM_FORCE_PROMOTE | SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE |
-                           SGQ_GEMM_TEST_TIMEOUT)) != 0 ||
+                           SGQ_GEMM_TEST_TIMEOUT | SGQ_GEMM_SCALES_POW2)) != 0 ||
         (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) == (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE))
         return SGQ_ERR_INVALID_ARG;
     // int32 indexing inside the kernel

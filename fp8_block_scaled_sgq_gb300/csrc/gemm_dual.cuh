@@ -1,0 +1,463 @@
+// Prefill-sized block-scaled FP8 GEMM for sm_103a with power-of-two (UE8M0)
+// scales: D = (Aq * As)(Wq * Ws)^T, fp32 accumulation, bf16 out.
+//
+// The operation is the one of gemm_kernel.cuh (vLLM "scaled_mm" API page,
+// AiterInt8ScaledMMLinearKernel.apply_weights docstring, in the "NT" layout of
+// sglang PR #42604, Modifications: fp8_gemm_nt((Aq, As), (Wq, Ws), D,
+// recipe=(1, blk_n, blk_k))), for the case the PR's path uses -- every scale a
+// power of two -- so that all scales go through the block-scaled MMA
+// (kind::mxf8f6f4, one UE8M0 factor per row per 32-wide K chunk).
+//
+// Why a tile of 256 activation rows x BN weight rows with two accumulators:
+// one 128 x 256 x 32 MMA keeps an SM's tensor core busy ~70 ns, so a 128-row
+// tile needs its 48 KB per 128-wide K stage every ~280 ns -- more than the
+// ~120 GB/s an SM pulls from L2.  Two 128-row halves sharing one weight tile
+// need 60 KB per ~520 ns of MMA work, under that rate, and each half has its
+// own issuing warp and TMEM accumulator (2 x 224 columns, plus the scale
+// factors: TMEM's 512 columns hold no second buffer, so a tile's epilogue
+// does not overlap the next tile's first MMAs).
+//
+// Warps: 0 producer (TMA: the 256 x 128 activation box and the BN x 128 weight
+// box per K stage, 3-stage ring), 1 and 2 MMA issuers (half 0 / half 1),
+// 3 and 12 scale warps (UE8M0 words of half h's activation rows and of half
+// of the weight rows, loaded ahead with plain loads), 4-11 epilogue (two warps
+// per TMEM lane quadrant, half of the columns each).  Every wait is bounded;
+// on time-out the CTA records a status word and leaves through the normal
+// teardown.  A scale that is not a power of two sets a status bit instead of
+// being applied (the caller promised power-of-two scales).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "sgq_internal.h"
+
+namespace sgq {
+namespace dual {
+
+constexpr int kHalf = 128;                 // activation rows per half (MMA M)
+constexpr int kRowsA = 2 * kHalf;          // activation rows per tile
+constexpr int kBK = 128;                   // K bytes per stage
+constexpr int kStages = 3;
+constexpr int kWarps = 13;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kEpi0 = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 1ull << 30;
+constexpr uint64_t kAbortPollNs = 20000;
+constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusBadScale = 2u;
+
+struct DualArgs {
+    const float* As;        // fp32 [M, K / blk_k]
+    const float* Ws;        // fp32 [ceil(N / blk_n), K / blk_k]
+    __nv_bfloat16* D;       // bf16 [M, N]
+    uint32_t* status;       // device status word
+    int M, N, K, ks;        // ks = K / blk_k
+    int tiles_r, tiles_c, kst, tiles, group_r;
+};
+
+// UE8M0 words (tcgen05.cp order) of one stage: half h's 128 activation rows,
+// and the weight rows (two 128-row copies).
+struct alignas(128) Slot {
+    uint32_t sfa[2][128];
+    uint32_t sfb[256];
+};
+
+template <int BN>
+struct Cfg {
+    static constexpr int kABytes = kRowsA * kBK;
+    static constexpr int kBBytes = BN * kBK;
+    static constexpr size_t kOffA = 0;
+    static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
+    static constexpr size_t kOffSlot = kOffB + size_t(kStages) * kBBytes;
+    // barriers: full[kStages], empty[kStages], accf[2], acce[2], drain[2]
+    static constexpr size_t kOffBar = kOffSlot + size_t(kStages) * sizeof(Slot);
+    static constexpr int kNumBars = 2 * kStages + 6;
+    static constexpr size_t kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr size_t kSmem = kOffMisc + 64 + 1024;
+    // TMEM: accumulator h at columns [h*BN, (h+1)*BN), then two scale slots
+    // of 16 columns per issuer (A words at +0, B words at +4 .. +11)
+    static constexpr uint32_t kSfCol = 2u * BN;
+    static_assert(BN % 16 == 0 && BN <= 256 && BN > 128, "MMA N (two B scale copies)");
+    static_assert(kSfCol + 64u <= kTmemCols, "TMEM: two accumulators and the scale slots");
+    static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "128-byte swizzle atoms");
+    static_assert(kSmem <= 232448, "shared memory");
+    static constexpr int kColsPerWarp = BN / 2;       // epilogue: two warps per lane quadrant
+    static_assert(kColsPerWarp % 16 == 0, "16-column epilogue chunks");
+};
+
+struct Sync {
+    volatile uint32_t* abort_flag;
+    uint32_t* status;
+};
+
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
+    const uint64_t t0 = ptx::globaltimer();
+    uint32_t spins = 0;
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((++spins & 15u) == 0) {
+            const uint64_t dt = ptx::globaltimer() - t0;
+            if (dt > kAbortPollNs && *s.abort_flag) return false;
+            if (dt > kTimeoutNs) {
+                *s.abort_flag = 1u;
+                atomicOr(s.status, kStatusTimeout | (where << 8));
+                return false;
+            }
+        }
+        if (spins > 8) __nanosleep(32);
+    }
+}
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31) == 0 && !ptx::mbar_try_wait(bar, parity)) ok = wait_slow(bar, parity, s, where) ? 1u : 0u;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+// UE8M0 word of one scale row: byte q = exponent field of chunk q's scale
+// (one scale per stage: repeated); `bad` collects scales that are not
+// positive normal powers of two.
+__device__ __forceinline__ uint32_t zero_byte(uint32_t w) { return (w - 0x01010101u) & ~w & 0x80808080u; }
+template <int kSps>
+__device__ __forceinline__ uint32_t sf_word(const float4& v, uint32_t& bad) {
+    if constexpr (kSps == 1) {
+        const uint32_t b = __float_as_uint(v.x);
+        const uint32_t w = __byte_perm(b << 1, 0u, 0x3333);
+        bad |= (b & 0x807FFFFFu) | zero_byte(w) | zero_byte(~w);
+        return w;
+    } else {
+        const uint32_t x = __float_as_uint(v.x), y = __float_as_uint(v.y), z = __float_as_uint(v.z),
+                       q = __float_as_uint(v.w);
+        const uint32_t lo = __byte_perm(x << 1, y << 1, 0x0073);
+        const uint32_t hi = __byte_perm(z << 1, q << 1, 0x0073);
+        const uint32_t w = __byte_perm(lo, hi, 0x5410);
+        bad |= ((x | y | z | q) & 0x807FFFFFu) | zero_byte(w) | zero_byte(~w);
+        return w;
+    }
+}
+template <int kSps>
+__device__ __forceinline__ float4 load_scales(const float* p) {
+    if constexpr (kSps == 4) return __ldg(reinterpret_cast<const float4*>(p));
+    else return make_float4(__ldg(p), 0.0f, 0.0f, 0.0f);
+}
+
+// Tile t -> (row tile, column tile): column-major inside groups of group_r
+// row tiles, so the CTAs of one wave share weight tiles and activation rows.
+__device__ __forceinline__ void tile_coords(const DualArgs& a, int t, int& tr, int& tc) {
+    const int per_group = a.group_r * a.tiles_c;
+    const int g = t / per_group;
+    const int first = g * a.group_r;
+    const int gm = min(a.tiles_r - first, a.group_r);
+    const int in = t - g * per_group;
+    tr = first + in % gm;
+    tc = in / gm;
+}
+
+template <int BN, int kBlkN, int kBlkK>
+__global__ void __launch_bounds__(kThreads, 1)
+    dual_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const DualArgs a) {
+    using C = Cfg<BN>;
+    constexpr int kSps = kBK / kBlkK;      // scale columns per stage (1 or 4)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem + C::kOffA;
+    uint8_t* sB = smem + C::kOffB;
+    Slot* slot = reinterpret_cast<Slot*>(smem + C::kOffSlot);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);   // [0] TMEM base, [1] abort flag
+
+    const uint32_t bar0 = ptx::smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto accf_bar = [&](int h) { return bar0 + 8u * (2 * kStages + h); };
+    auto acce_bar = [&](int h) { return bar0 + 8u * (2 * kStages + 2 + h); };
+    auto drain_bar = [&](int h) { return bar0 + 8u * (2 * kStages + 4 + h); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const Sync sync{reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
+    const int first_tile = static_cast<int>(blockIdx.x);
+    const int tile_step = static_cast<int>(gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(full_bar(s), 3);    // producer expect_tx + the two scale warps
+            ptx::mbar_init(empty_bar(s), 2);   // a commit of each issuer
+        }
+        for (int h = 0; h < 2; ++h) {
+            ptx::mbar_init(accf_bar(h), 1);    // the issuer's commit after the tile's last stage
+            ptx::mbar_init(acce_bar(h), 8);    // one arrive per epilogue warp
+            ptx::mbar_init(drain_bar(h), 1);
+        }
+        misc[1] = 0;
+        ptx::fence_mbar_init();
+    }
+    // weight-row words past 224 (the second copy's tail) stay 2^0
+    for (int i = threadIdx.x; i < kStages * 256; i += kThreads) slot[i / 256].sfb[i % 256] = 0x7F7F7F7Fu;
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = misc[0];
+    // The next kernel on the stream may launch now; it still waits for this
+    // grid to finish before it touches anything this grid writes.
+    if (threadIdx.x == 0) ptx::launch_dependents();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        // The weight boxes of the first stages go out before the wait for the
+        // preceding grid (weights are static); the activation boxes after it.
+        const uint32_t leader = lane == 0 ? 1u : 0u;
+        const uint32_t a0 = ptx::smem_u32(sA), b0 = ptx::smem_u32(sB);
+        int n = 0;   // stage jobs issued
+        bool failed = false;
+        bool waited = false;
+        for (int t = first_tile; t < a.tiles && !failed; t += tile_step) {
+            int tr, tc;
+            tile_coords(a, t, tr, tc);
+            for (int kb = 0; kb < a.kst; ++kb, ++n) {
+                const int s = n % kStages, r = n / kStages;
+                if (r > 0 && !wait_warp(empty_bar(s), (r - 1) & 1, sync, 1)) {
+                    failed = true;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx_if(leader, full_bar(s), C::kABytes + C::kBBytes);
+                ptx::tma_load_2d_if(leader, b0 + s * C::kBBytes, &tmB, kb * kBK, tc * BN, full_bar(s));
+                if (!waited) {
+                    ptx::grid_dependency_wait();   // Aq may be the preceding kernel's output
+                    waited = true;
+                }
+                ptx::tma_load_2d_if(leader, a0 + s * C::kABytes, &tmA, kb * kBK, tr * kRowsA, full_bar(s));
+            }
+        }
+        if (!waited) ptx::grid_dependency_wait();
+    } else if (warp == 3 || warp == 12) {
+        // ------------------------------------------------------------ scale warps
+        // Half h: the UE8M0 words of activation rows h*128 .. +127 and of
+        // weight rows h*112 .. +111 of each stage, from scales loaded one stage
+        // ahead (all of a lane's loads in flight together).
+        const int h = warp == 3 ? 0 : 1;
+        constexpr int kBRowsPerWarp = BN / 2;
+        ptx::grid_dependency_wait();   // As may be the preceding kernel's output
+        // Raw scales of the next two stages are in flight while a stage is
+        // converted (registers p0 for stage n + 1, p1 for stage n + 2).
+        struct Raw {
+            float4 a[4], b[4];
+        };
+        auto load = [&](Raw& v, int t, int kb) {
+            if (t >= a.tiles) return;
+            int tr, tc;
+            tile_coords(a, t, tr, tc);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int row = tr * kRowsA + h * kHalf + lane + 32 * j;
+                v.a[j] = row < a.M ? load_scales<kSps>(a.As + static_cast<int64_t>(row) * a.ks + kb * kSps)
+                                   : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                const int i = lane + 32 * j;
+                const int n = tc * BN + h * kBRowsPerWarp + i;
+                v.b[j] = (i < kBRowsPerWarp && n < a.N)
+                             ? load_scales<kSps>(a.Ws + static_cast<int64_t>(n / kBlkN) * a.ks + kb * kSps)
+                             : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+            }
+        };
+        auto advance = [&](int& t, int& kb) {
+            if (++kb == a.kst) {
+                kb = 0;
+                t += tile_step;
+            }
+        };
+        int t = first_tile, kb = 0;        // stage being converted
+        int t1 = t, kb1 = kb;
+        advance(t1, kb1);                  // stage n + 1
+        int t2 = t1, kb2 = kb1;
+        advance(t2, kb2);                  // stage n + 2
+        Raw cur, p0, p1;
+        load(cur, t, kb);
+        load(p0, t1, kb1);
+        int n = 0;
+        uint32_t bad_all = 0;
+        while (t < a.tiles) {
+            load(p1, t2, kb2);
+            const int s = n % kStages, r = n / kStages;
+            if (r > 0 && !wait_warp(empty_bar(s), (r - 1) & 1, sync, 2)) break;
+            Slot& sl = slot[s];
+            uint32_t bad = 0;
+            uint32_t w4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w4[j] = sf_word<kSps>(cur.a[j], bad);
+            *reinterpret_cast<uint4*>(&sl.sfa[h][lane * 4]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = lane + 32 * j;
+                if (i < kBRowsPerWarp) {
+                    const int row = h * kBRowsPerWarp + i;   // weight row inside the tile
+                    sl.sfb[(row >> 7) * 128 + (row & 31) * 4 + ((row & 127) >> 5)] = sf_word<kSps>(cur.b[j], bad);
+                }
+            }
+            bad_all |= bad;
+            ptx::fence_proxy_async_smem();   // the words are read by tcgen05.cp
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(full_bar(s));
+            ++n;
+            cur = p0;
+            p0 = p1;
+            t = t1;
+            kb = kb1;
+            t1 = t2;
+            kb1 = kb2;
+            advance(t2, kb2);
+        }
+        // A scale that is not a power of two breaks the caller's promise.
+        if (__any_sync(0xFFFFFFFFu, bad_all != 0u) && lane == 0) atomicOr(a.status, kStatusBadScale);
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA issuers
+        const int h = warp - 1;
+        constexpr uint32_t idesc_mx = ptx::idesc_mxf8(kHalf, BN);
+        const uint64_t ad_base = ptx::smem_desc(ptx::smem_u32(sA) + h * (kHalf * kBK), 16, 1024, ptx::kLayoutSw128);
+        const uint64_t bd_base = ptx::smem_desc(ptx::smem_u32(sB), 16, 1024, ptx::kLayoutSw128);
+        const uint64_t sfa_base = ptx::smem_desc(ptx::smem_u32(slot[0].sfa[h]), 128, 128, ptx::kLayoutNone);
+        const uint64_t sfb_base = ptx::smem_desc(ptx::smem_u32(slot[0].sfb), 128, 128, ptx::kLayoutNone);
+        constexpr uint32_t kSlotStep = sizeof(Slot) >> 4;
+        const uint32_t d = tmem + static_cast<uint32_t>(h * BN);
+        int n = 0, ntile = 0;
+        bool failed = false;
+        for (int t = first_tile; t < a.tiles && !failed; t += tile_step, ++ntile) {
+            // the accumulator must have been read by the epilogue
+            if (ntile > 0 && !wait_warp(acce_bar(h), (ntile - 1) & 1, sync, 3)) break;
+            ptx::tc_fence_after();
+            for (int kb = 0; kb < a.kst; ++kb, ++n) {
+                const int s = n % kStages, r = n / kStages;
+                if (!wait_warp(full_bar(s), r & 1, sync, 4)) {
+                    failed = true;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t t_sfa = tmem + C::kSfCol + 32u * h + 16u * (n & 1), t_sfb = t_sfa + 4u;
+                const uint64_t so = static_cast<uint64_t>(s) * kSlotStep;
+                ptx::mx_stage2_elect(d, ad_base + static_cast<uint64_t>(s * (C::kABytes >> 4)),
+                                     bd_base + static_cast<uint64_t>(s * (C::kBBytes >> 4)),
+                                     ptx::idesc_sf_ids(idesc_mx, 0, 0), ptx::idesc_sf_ids(idesc_mx, 1, 1),
+                                     ptx::idesc_sf_ids(idesc_mx, 2, 2), ptx::idesc_sf_ids(idesc_mx, 3, 3), t_sfa,
+                                     t_sfb, sfa_base + so, sfb_base + so, kb > 0 ? 1u : 0u);
+                ptx::commit_elect(empty_bar(s));   // frees the stage once both halves' MMAs are done
+            }
+            if (failed) break;
+            ptx::commit_elect(accf_bar(h));        // the tile's accumulator is complete
+        }
+        ptx::commit_elect(drain_bar(h));           // every tcgen05 op lands before teardown
+        if (lane == 0) wait_slow(drain_bar(h), 0, sync, 5);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 4-11)
+        const int ew = warp - kEpi0;            // 0 .. 7
+        const int quad = warp & 3;              // TMEM lane quadrant
+        const int chalf = ew >> 2;              // which half of the columns
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        ptx::grid_dependency_wait();            // D may still be read by the preceding kernel
+        const bool v8 = ((reinterpret_cast<uintptr_t>(a.D) | (static_cast<uintptr_t>(a.N) * 2u)) & 31u) == 0;
+        int ntile = 0;
+        for (int t = first_tile; t < a.tiles; t += tile_step, ++ntile) {
+            int tr, tc;
+            tile_coords(a, t, tr, tc);
+            bool failed = false;
+            for (int h = 0; h < 2 && !failed; ++h) {
+                if (!wait_warp(accf_bar(h), ntile & 1, sync, 6)) {
+                    failed = true;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const int grow = tr * kRowsA + h * kHalf + quad * 32 + lane;
+                __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
+#pragma unroll
+                for (int c0 = 0; c0 < C::kColsPerWarp; c0 += 16) {
+                    const int cl = chalf * C::kColsPerWarp + c0;   // column inside the tile
+                    uint32_t rr[16];
+                    ptx::tmem_ld<16>(t_lane + static_cast<uint32_t>(h * BN + cl), rr);
+                    ptx::tmem_wait_ld();
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const __nv_bfloat162 p =
+                            __floats2bfloat162_rn(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
+                        w[i] = *reinterpret_cast<const uint32_t*>(&p);
+                    }
+                    const int gcol = tc * BN + cl;
+                    if (grow < a.M) {
+                        if (v8 && gcol + 16 <= a.N) {
+                            ptx::st_global_v8(drow + gcol, w);
+                        } else {
+                            if (gcol < a.N)
+                                *reinterpret_cast<uint4*>(drow + gcol) = make_uint4(w[0], w[1], w[2], w[3]);
+                            if (gcol + 8 < a.N)
+                                *reinterpret_cast<uint4*>(drow + gcol + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(acce_bar(h));
+            }
+            if (failed) break;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int BN, int kBlkN, int kBlkK>
+sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a, int grid, cudaStream_t st) {
+    using C = Cfg<BN>;
+    auto kern = dual_gemm_kernel<BN, kBlkN, kBlkK>;
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem)) !=
+            cudaSuccess)
+            return SGQ_ERR_CUDA;
+        configured[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a) != cudaSuccess) return SGQ_ERR_CUDA;
+    note_launch();
+    return SGQ_OK;
+}
+
+// Weight rows per tile: 224 (two 224-column accumulators and the scale slots
+// fill TMEM's 512 columns).
+constexpr int kBN = 224;
+
+sgq_status dispatch(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
+                    int grid, cudaStream_t st);
+
+}  // namespace dual
+}  // namespace sgq

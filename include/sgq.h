@@ -75,6 +75,16 @@ typedef enum {
  * reports SGQ_ERR_TIMEOUT and D is undefined.  The stream stays usable.
  * Needs a shape whose first CTA has at least six K stages. */
 #define SGQ_GEMM_TEST_TIMEOUT 8u
+/* The caller promises that every scale (As and Ws) is an exact power of two
+ * (UE8M0), as the quantisers produce with ue8m0 = 1.  Shapes on the wide
+ * tiles (M > 64, or the plan's choice for M <= 1024) with K a multiple of 128
+ * and at least one tile of 256 activation rows x 224 weight rows per SM then
+ * run on such tiles with two accumulators, every scale applied by the
+ * block-scaled MMA.  A scale that is
+ * not a power of two makes sgq_device_status report SGQ_ERR_INVALID_ARG (D is
+ * then undefined).  Results agree with the default path within the GEMM
+ * tolerance. */
+#define SGQ_GEMM_SCALES_POW2 16u
 
 /*
  * Per-token-group quantisation.
@@ -281,7 +291,9 @@ const char* sgq_status_string(sgq_status s);
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns SGQ_OK, SGQ_ERR_TIMEOUT (a bounded
  * device-side wait ran out; the kernel returned early and its outputs are
- * undefined) or SGQ_ERR_CUDA (the synchronisation itself failed).
+ * undefined), SGQ_ERR_INVALID_ARG (a GEMM called with SGQ_GEMM_SCALES_POW2
+ * met a scale that is not a power of two; its D is undefined) or
+ * SGQ_ERR_CUDA (the synchronisation itself failed).
  */
 sgq_status sgq_device_status(sgq_stream_t stream);
 

@@ -94,7 +94,7 @@ def test_gemm_validation(lib):
     assert g(*args(N=260)) == INV                # N % 8
     assert g(*args(N=0)) == INV
     assert g(*args(M=-1)) == INV
-    assert g(*args(flags=16)) == INV             # unknown flag
+    assert g(*args(flags=32)) == INV             # unknown flag
     assert g(*args(flags=6)) == INV              # both issue modes at once
     assert g(*args(M=1 << 31)) == INV
     assert g(*args(Aq=None)) == INV

@@ -322,3 +322,59 @@ def test_bounded_wait_times_out_and_the_stream_recovers(M, N, K, bk, flags):
         sgq.sgq_fp8_block_gemm_ex(*args, d2, M, N, K, bk, bk, flags)
         assert sgq.sgq_device_status() == binding.SGQ_OK
         check_gemm(d2, dref, bound, f"after the time-out M={M}")
+
+
+DUAL = [(300, 520, 1024, 128, 128), (513, 264, 2048, 32, 32), (4100, 7000, 1280, 128, 32), (257, 1032, 4096, 32, 128),
+        (2048, 448, 7168, 32, 32)]
+
+
+@pytest.mark.parametrize("M,N,K,bn,bk", DUAL)
+def test_scales_pow2_tiles_match_oracle(M, N, K, bn, bk):
+    """SGQ_GEMM_SCALES_POW2 (every scale a power of two): the wide-tile plans
+    run on 256 x 224 tiles with two accumulators.  Ragged M and N (partial row
+    and column tiles, N not a multiple of 224), both recipes and their mixes;
+    every row (or one of every 64-row block) against the oracle, and against
+    the default path within the same tolerance."""
+    c = synth.Case("dual", M, N, K, bn, bk, True, seed=M + N)
+    aq, a_s = oracle.quant_token_group(c.x(), bk, True)
+    wq, ws = oracle.quant_weight_block(c.w(), bn, bk, True)
+    args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+    d = sgq.fp8_block_gemm(*args, bn, bk, flags=sgq.SGQ_GEMM_SCALES_POW2)
+    assert sgq.sgq_device_status() == 0
+    r = np.arange(M) if M <= 600 else tile_rows(M, seed=M)
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
+    rr = torch.from_numpy(r).cuda()
+    check_gemm(d[rr], dref, bound, f"pow2 tiles M={M} N={N} K={K} [{bn},{bk}]")
+    check_gemm(sgq.fp8_block_gemm(*args, bn, bk)[rr], dref, bound, "default path")
+
+
+@pytest.mark.parametrize("name", ["prefill_block128", "prefill_block32"])
+def test_scales_pow2_prefill_every_tile(name):
+    """The prefill configurations (UE8M0 on both operands) through the
+    power-of-two tiles, one row of every 64-row block over all N columns."""
+    c = synth.WORKLOADS[name][0]
+    aq, a_s = oracle.quant_token_group(c.x(), c.group, c.ue8m0)
+    wq, ws = weights(c.N, c.K, c.blk_n, c.blk_k, c.ue8m0, c.seed)
+    d = run_gpu(aq, a_s, wq, ws, c.blk_n, c.blk_k, sgq.SGQ_GEMM_SCALES_POW2)
+    r = tile_rows(c.M, seed=3)
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, c.blk_n, c.blk_k)
+    check_gemm(d[torch.from_numpy(r).cuda()], dref, bound, f"{name} pow2 tiles")
+
+
+def test_scales_pow2_flag_reports_a_broken_promise():
+    """fp32 scales with SGQ_GEMM_SCALES_POW2: the device status reports
+    SGQ_ERR_INVALID_ARG (the promise was broken), and the next call is fine."""
+    from fp8_block_scaled_sgq_gb300 import binding
+    M, N, K, bk = 4096, 2240, 256, 128   # 16 x 10 tiles of 256 x 224: the power-of-two tiles run
+    assert sgq.sgq_gemm_plan(M, N, K, bk)["swap"] == 0
+    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=9), bk, False)
+    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=9), bk, bk, False)
+    args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+    d = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    sgq.sgq_fp8_block_gemm_ex(*args, d, M, N, K, bk, bk, binding.SGQ_GEMM_SCALES_POW2)
+    assert sgq.sgq_device_status() == binding.SGQ_ERR_INVALID_ARG
+    r = tile_rows(M, seed=9)
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bk, bk)
+    d2 = sgq.fp8_block_gemm(*args, bk, bk)
+    check_gemm(d2[torch.from_numpy(r).cuda()], dref, bound, "default path after the broken promise")
+    assert sgq.sgq_device_status() == 0
