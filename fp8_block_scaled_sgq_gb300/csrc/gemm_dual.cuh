@@ -12,10 +12,10 @@
 // one 128 x 256 x 32 MMA keeps an SM's tensor core busy ~70 ns, so a 128-row
 // tile needs its 48 KB per 128-wide K stage every ~280 ns -- more than the
 // ~120 GB/s an SM pulls from L2.  Two 128-row halves sharing one weight tile
-// need 60 KB per ~520 ns of MMA work, under that rate, and each half has its
-// own issuing warp and TMEM accumulator (2 x 224 columns, plus the scale
-// factors: TMEM's 512 columns hold no second buffer, so a tile's epilogue
-// does not overlap the next tile's first MMAs).
+// need 60 KB per ~520 ns of MMA work (BN = 224), under that rate, and each
+// half has its own issuing warp and TMEM accumulator (2 x BN columns, plus the
+// scale factors: TMEM's 512 columns hold no second buffer, so a tile's
+// epilogue does not overlap the next tile's first MMAs).
 //
 // Warps: 0 producer (TMA: the 256 x 128 activation box and the BN x 128 weight
 // box per K stage, 3-stage ring), 1 and 2 MMA issuers (half 0 / half 1),
@@ -453,11 +453,23 @@ sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a
 }
 
 // Weight rows per tile: 224 (two 224-column accumulators and the scale slots
-// fill TMEM's 512 columns).
-constexpr int kBN = 224;
+// fill TMEM's 512 columns) or 192; the host takes the width whose tiles fill
+// the grid's rounds best.
+constexpr int kBNWide = 224;
+constexpr int kBNNarrow = 192;
 
-sgq_status dispatch(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
-                    int grid, cudaStream_t st);
+template <int BN>
+sgq_status dispatch_bn(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
+                       int grid, cudaStream_t st) {
+    if (blk_n == 32)
+        return blk_k == 32 ? run<BN, 32, 32>(tmA, tmB, a, grid, st) : run<BN, 32, 128>(tmA, tmB, a, grid, st);
+    return blk_k == 32 ? run<BN, 128, 32>(tmA, tmB, a, grid, st) : run<BN, 128, 128>(tmA, tmB, a, grid, st);
+}
+// One translation unit per width (gemm_dual_224.cu, gemm_dual_192.cu).
+sgq_status dispatch_224(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
+                        int grid, cudaStream_t st);
+sgq_status dispatch_192(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
+                        int grid, cudaStream_t st);
 
 }  // namespace dual
 }  // namespace sgq

@@ -298,10 +298,27 @@ struct Chan {
     const void* bias;
 };
 
-// Launches the two-accumulator prefill GEMM (power-of-two scales): 256-row x
-// 224-column tiles over a persistent grid of at most one CTA per SM.
+// Tile width of the two-accumulator GEMM: 224 or 192 weight rows.  A K stage
+// of either is bound by its operand bytes in flight (256 + BN rows of 128
+// bytes), so the cost of a width is its rounds of tiles over the grid times
+// that: 4096 x 7168 takes 192 (608 tiles: exactly 4 rounds of 152 SMs, where
+// 224 makes 512 tiles, 3.4 rounds, so 4 of the longer stage; 168.6 vs 174.2
+// us), 8192 x 24576 takes 224 (24 rounds against 27; 280 vs 294 us).
+int dual_width(int64_t M, int64_t N, int sm_count) {
+    const int64_t tr = (M + dual::kRowsA - 1) / dual::kRowsA;
+    auto cost = [&](int bn) {
+        const int64_t tiles = tr * ((N + bn - 1) / bn);
+        return ((tiles + sm_count - 1) / sm_count) * (dual::kRowsA + bn);
+    };
+    return cost(dual::kBNNarrow) < cost(dual::kBNWide) ? dual::kBNNarrow : dual::kBNWide;
+}
+
+// Launches the two-accumulator prefill GEMM (power-of-two scales): tiles of
+// 256 activation rows x BN weight rows over a persistent grid of at most one
+// CTA per SM.
 sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D, int64_t M,
                        int64_t N, int64_t K, int blk_n, int blk_k, int sm_count, cudaStream_t st) {
+    const int bn = dual_width(M, N, sm_count);
     dual::DualArgs a{};
     a.As = As;
     a.Ws = Ws;
@@ -311,17 +328,18 @@ sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const fl
     a.K = static_cast<int>(K);
     a.ks = static_cast<int>(K / blk_k);
     a.tiles_r = static_cast<int>((M + dual::kRowsA - 1) / dual::kRowsA);
-    a.tiles_c = static_cast<int>((N + dual::kBN - 1) / dual::kBN);
+    a.tiles_c = static_cast<int>((N + bn - 1) / bn);
     a.kst = static_cast<int>(K / kBK);
     a.tiles = a.tiles_r * a.tiles_c;
     a.group_r = a.tiles_r < 16 ? a.tiles_r : 16;
     sgq_status rc = status_word(&a.status);
     if (rc != SGQ_OK) return rc;
     CUtensorMap maps[2];
-    if (make_tmap(&maps[0], Aq, M, K, dual::kRowsA) != SGQ_OK || make_tmap(&maps[1], Wq, N, K, dual::kBN) != SGQ_OK)
+    if (make_tmap(&maps[0], Aq, M, K, dual::kRowsA) != SGQ_OK || make_tmap(&maps[1], Wq, N, K, bn) != SGQ_OK)
         return SGQ_ERR_CUDA;
     const int grid = a.tiles < sm_count ? a.tiles : sm_count;
-    return dual::dispatch(blk_n, blk_k, maps[0], maps[1], a, grid, st);
+    return bn == dual::kBNNarrow ? dual::dispatch_192(blk_n, blk_k, maps[0], maps[1], a, grid, st)
+                                 : dual::dispatch_224(blk_n, blk_k, maps[0], maps[1], a, grid, st);
 }
 
 // Plans and launches one GEMM.  noalloc: split-K scratch from the fixed array
@@ -349,7 +367,7 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     // a wave of 256 x 224 tiles run on those, two accumulators per tile
     // (gemm_dual.cuh), K in whole stages.  (Fewer tiles than SMs: the 128-row
     // tiles keep more SMs busy; 2048 x 1536 x 7168 measured 35.4 vs 43.3 us.)
-    const int64_t dual_tiles = ((M + dual::kRowsA - 1) / dual::kRowsA) * ((N + dual::kBN - 1) / dual::kBN);
+    const int64_t dual_tiles = ((M + dual::kRowsA - 1) / dual::kRowsA) * ((N + dual::kBNWide - 1) / dual::kBNWide);
     if ((flags & SGQ_GEMM_SCALES_POW2) && !p.swap && !fuse && !chan && K % kBK == 0 && dual_tiles >= di.sm_count &&
         (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) == 0)
         return launch_dual(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, di.sm_count, st);

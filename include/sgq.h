@@ -79,8 +79,9 @@ typedef enum {
  * (UE8M0), as the quantisers produce with ue8m0 = 1.  Shapes on the wide
  * tiles (M > 64, or the plan's choice for M <= 1024) with K a multiple of 128
  * and at least one tile of 256 activation rows x 224 weight rows per SM then
- * run on such tiles with two accumulators, every scale applied by the
- * block-scaled MMA.  A scale that is
+ * run on tiles of 256 activation rows x 224 (or 192, whichever fills the
+ * grid's rounds better) weight rows with two accumulators, every scale
+ * applied by the block-scaled MMA.  A scale that is
  * not a power of two makes sgq_device_status report SGQ_ERR_INVALID_ARG (D is
  * then undefined).  Results agree with the default path within the GEMM
  * tolerance. */

@@ -325,14 +325,16 @@ def test_bounded_wait_times_out_and_the_stream_recovers(M, N, K, bk, flags):
 
 
 DUAL = [(300, 520, 1024, 128, 128), (513, 264, 2048, 32, 32), (4100, 7000, 1280, 128, 32), (257, 1032, 4096, 32, 128),
-        (2048, 448, 7168, 32, 32)]
+        (2048, 448, 7168, 32, 32), (4096, 7168, 512, 128, 128), (4200, 7000, 384, 32, 32)]
 
 
 @pytest.mark.parametrize("M,N,K,bn,bk", DUAL)
 def test_scales_pow2_tiles_match_oracle(M, N, K, bn, bk):
     """SGQ_GEMM_SCALES_POW2 (every scale a power of two): the wide-tile plans
-    run on 256 x 224 tiles with two accumulators.  Ragged M and N (partial row
-    and column tiles, N not a multiple of 224), both recipes and their mixes;
+    with a wave of tiles run on 256 x 224 or 256 x 192 tiles with two
+    accumulators (4096 x 7168 and 4200 x 7000 take the 192-wide tiles; the
+    small shapes keep the 128-row tiles).  Ragged M and N (partial row and
+    column tiles, N not a multiple of the width), both recipes and their mixes;
     every row (or one of every 64-row block) against the oracle, and against
     the default path within the same tolerance."""
     c = synth.Case("dual", M, N, K, bn, bk, True, seed=M + N)
