@@ -270,8 +270,11 @@ def gemm_cases(sgq, timer, device, reps, names):
             d = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
             sgq.sgq_quant_token_group(x, c.M, c.K, c.group, int(c.ue8m0), xq, xs, timer.stream.cuda_stream)
 
-            def gemm(sp, r, c=c, xq=xq, xs=xs, d=d):
-                sgq.sgq_fp8_block_gemm(xq, xs, wrot[r][0], wrot[r][1], d, c.M, c.N, c.K, c.blk_n, c.blk_k, sp)
+            # the configurations' scales are UE8M0: the caller may promise powers of two
+            fl = sgq.SGQ_GEMM_SCALES_POW2 if c.ue8m0 else sgq.SGQ_GEMM_DEFAULT
+
+            def gemm(sp, r, c=c, xq=xq, xs=xs, d=d, fl=fl):
+                sgq.sgq_fp8_block_gemm_ex(xq, xs, wrot[r][0], wrot[r][1], d, c.M, c.N, c.K, c.blk_n, c.blk_k, fl, sp)
 
             def pair(sp, r, c=c, x=x, xq=xq, xs=xs, d=d):
                 sgq.sgq_quant_token_group(x, c.M, c.K, c.group, int(c.ue8m0), xq, xs, sp)
@@ -283,7 +286,8 @@ def gemm_cases(sgq, timer, device, reps, names):
                 nbytes = c.gemm_bytes() + (c.quant_bytes() if path == "pair" else 0.0)
                 bound, frac = roofline_frac(c.flops(), nbytes, us)
                 rows.append({"case": c.name, "path": path, "M": c.M, "N": c.N, "K": c.K,
-                             "recipe": [1, c.blk_n, c.blk_k], "us": round(us, 3),
+                             "recipe": [1, c.blk_n, c.blk_k], "flags": "scales_pow2" if fl else "default",
+                             "us": round(us, 3),
                              "tflops": round(c.flops() / us / 1e6, 2), "gbs": round(nbytes / us / 1e3, 1),
                              "bound": bound, "frac": round(frac, 4)})
             del x, xq, xs, d

@@ -1,4 +1,4 @@
-"""Times one library path on one shape and prints a JSON line.
+"""Times one library entry point on one shape and prints a JSON line.
 
     python -m fp8_block_scaled_sgq_gb300.measure PATH M N K [--blk B] [--reps R]
 
@@ -14,12 +14,9 @@ PATH is one of
                     (programmatic dependent launch), [B, B] blocks, UE8M0  (TFLOP/s; GB/s of the
                     quantiser's and the GEMM's algorithmic bytes)
 
-    python -m fp8_block_scaled_sgq_gb300.measure --sweep [--reps R]
-
-times `pair` and `block_gemm` on every case of the M = 1..8192 sweep (N, K in
-{(24576, 1536), (1536, 7168)}, [128, 128] and [32, 32] blocks) and prints one
-JSON line per case, then a markdown table with each time's fraction of the
-roofline min(FP8 peak, arithmetic intensity x HBM peak) from the measured peaks.
+The metric's own configurations (the M = 1..8192 sweep, the prefill GEMMs and
+the quantiser at prefill sizes) are timed by bench.py; this times the other
+entry points, one shape at a time.
 
 Timing: CUDA events around one replay of a CUDA graph holding `reps` calls on
 one stream, after a warm-up replay; weights (and, for the quantisers, inputs)
@@ -44,52 +41,14 @@ PATHS = ["quant_per_token", "quant_per_tensor", "quant_v2", "scaled_mm", "block_
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("path", nargs="?", choices=PATHS)
-    ap.add_argument("M", type=int, nargs="?")
-    ap.add_argument("N", type=int, nargs="?")
-    ap.add_argument("K", type=int, nargs="?")
+    ap.add_argument("path", choices=PATHS)
+    ap.add_argument("M", type=int)
+    ap.add_argument("N", type=int)
+    ap.add_argument("K", type=int)
     ap.add_argument("--blk", type=int, default=128)
     ap.add_argument("--reps", type=int, default=50)
-    ap.add_argument("--sweep", action="store_true")
     args = ap.parse_args()
-    if args.sweep:
-        sweep(args.reps)
-        return
-    if args.path is None or args.K is None:
-        ap.error("PATH M N K are required without --sweep")
     print(json.dumps(measure(args.path, args.M, args.N, args.K, args.blk, args.reps)), flush=True)
-
-
-def peaks() -> tuple:
-    """(HBM GB/s, FP8 TFLOP/s): the measured copy bandwidth and 2 x the measured bf16 rate."""
-    import os
-    p = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")
-    if os.path.exists(p):
-        d = json.load(open(p))
-        return float(d["hbm_gbs"]), 2.0 * float(d["bf16_tflops"])
-    return 6800.0, 3800.0
-
-
-def sweep(reps: int) -> None:
-    hbm, fp8 = peaks()
-    rows = []
-    for c in synth.WORKLOADS["sweep"]:
-        for path in ("pair", "block_gemm"):
-            r = measure(path, c.M, c.N, c.K, c.blk_k, reps)
-            flops = 2.0 * c.M * c.N * c.K
-            nbytes = c.gemm_bytes() + (c.quant_bytes() if path == "pair" else 0.0)
-            t_roof = max(flops / (fp8 * 1e12), nbytes / (hbm * 1e9)) * 1e6
-            r["roofline_frac"] = round(t_roof / r["us"], 3)
-            r["bound"] = "fp8" if flops / (fp8 * 1e12) > nbytes / (hbm * 1e9) else "hbm"
-            print(json.dumps(r), flush=True)
-            rows.append(r)
-    print("\n| N | K | blk | M | quant + GEMM us | GEMM us | GEMM TFLOP/s | GEMM GB/s | bound | "
-          "pair / GEMM fraction of roofline |")
-    print("|---|---|---|---|---|---|---|---|---|---|")
-    for i in range(0, len(rows), 2):
-        p, g = rows[i], rows[i + 1]
-        print(f"| {g['N']} | {g['K']} | {g['blk']} | {g['M']} | {p['us']:.2f} | {g['us']:.2f} | {g['tflops']:.1f} | "
-              f"{g['gbs']:.0f} | {g['bound']} | {p['roofline_frac']:.2f} / {g['roofline_frac']:.2f} |")
 
 
 def measure(path: str, M: int, N: int, K: int, blk: int, reps: int) -> dict:

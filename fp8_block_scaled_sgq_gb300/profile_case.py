@@ -1,14 +1,15 @@
 """Runs one quantise + GEMM case of a workload a few times, for profilers.
 
-    python -m fp8_block_scaled_sgq_gb300.profile_case WORKLOAD [INDEX] [--iters N] [--fused]
-    python -m fp8_block_scaled_sgq_gb300.profile_case --shape M N K BLK [--iters N] [--fused]
+    python -m fp8_block_scaled_sgq_gb300.profile_case WORKLOAD [INDEX] [--iters N] [--fused | --quant-only] [--pow2]
+    python -m fp8_block_scaled_sgq_gb300.profile_case --shape M N K BLK [--iters N] [--fused | --quant-only] [--pow2]
 
 WORKLOAD/INDEX pick a case from ``synth.WORKLOADS`` (e.g. ``decode_block32 2``
 is M=16, N=7168, K=2048 with [32,32] blocks); --shape takes any shape with
 [BLK, BLK] blocks and UE8M0 scales (x ~ N(0,1), W ~ N(0,0.02)).  Each iteration launches the
 activation quantisation kernel, then the block-scaled GEMM, on one stream.
 With --fused each iteration is one sgq_fp8_block_linear call instead (one
-kernel at decode-sized M).  The weight is quantised once up front (one extra
+kernel at decode-sized M); with --quant-only only the quantisation kernel;
+--pow2 passes SGQ_GEMM_SCALES_POW2 to the GEMM.  The weight is quantised once up front (one extra
 launch).  The run ends with
 the device status word checked and one line of wall-clock timing, which is
 not a benchmark number (use bench.py for those).
@@ -31,6 +32,8 @@ def main() -> None:
     ap.add_argument("--shape", type=int, nargs=4, metavar=("M", "N", "K", "BLK"))
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--fused", action="store_true")
+    ap.add_argument("--quant-only", action="store_true", help="launch only the activation quantiser")
+    ap.add_argument("--pow2", action="store_true", help="GEMM with SGQ_GEMM_SCALES_POW2 (UE8M0 scales)")
     args = ap.parse_args()
     if args.shape:
         M, N, K, blk = args.shape
@@ -59,13 +62,16 @@ def main() -> None:
             binding.sgq_fp8_block_linear(x, int(c.ue8m0), wq, ws, d, M, N, K, c.blk_n, c.blk_k, None, None, s)
         else:
             binding.sgq_quant_token_group(x, M, K, c.group, int(c.ue8m0), xq, xs, s)
-            binding.sgq_fp8_block_gemm(xq, xs, wq, ws, d, M, N, K, c.blk_n, c.blk_k, s)
+            if not args.quant_only:
+                flags = binding.SGQ_GEMM_SCALES_POW2 if args.pow2 else binding.SGQ_GEMM_DEFAULT
+                binding.sgq_fp8_block_gemm_ex(xq, xs, wq, ws, d, M, N, K, c.blk_n, c.blk_k, flags, s)
     st.synchronize()
     wall = time.perf_counter() - t0
     status = binding.sgq_device_status(s)
     if status != 0:
         raise RuntimeError(f"device status {binding.status_string(status)}")
-    print(json.dumps({"case": c.name, "fused": args.fused, "M": M, "N": N, "K": K, "blk": [c.blk_n, c.blk_k],
+    print(json.dumps({"case": c.name, "fused": args.fused, "quant_only": args.quant_only, "pow2": args.pow2,
+                      "M": M, "N": N, "K": K, "blk": [c.blk_n, c.blk_k],
                       "iters": args.iters, "wall_ms": round(wall * 1e3, 3)}))
 
 
