@@ -243,24 +243,45 @@ import fp8_block_scaled_sgq_gb300 as sgq
 from fp8_block_scaled_sgq_gb300 import synth
 import oracle
 M, N, K, bk = (int(v) for v in sys.argv[1:5])
-aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=31), bk, True)
-wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, True)
+pow2, want_pair = sys.argv[6] == "1", int(sys.argv[7])
+aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=31), bk, pow2)
+wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, pow2)
+if want_pair >= 0:
+    assert sgq.sgq_gemm_plan(M, N, K, bk)["pair"] == want_pair
 d = sgq.fp8_block_gemm(*(torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)), bk, bk)
 assert sgq.sgq_device_status() == 0
 np.save(sys.argv[5], d.view(torch.int16).cpu().numpy())
 """
 
 
-def _child_gemm(tmp_path, name, env_extra, M, N, K, bk):
+def _child_gemm(tmp_path, name, env_extra, M, N, K, bk, pow2=True, want_pair=-1):
+    """D of one GEMM computed in a fresh process whose launch plan reads the
+    given environment switches (they are read once per process)."""
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"), **env_extra)
     out = str(tmp_path / f"{name}.npy")
-    subprocess.run([sys.executable, "-c", _CK_CHILD, str(M), str(N), str(K), str(bk), out], env=env,
-                   check=True, timeout=600, cwd=root)
+    subprocess.run([sys.executable, "-c", _CK_CHILD, str(M), str(N), str(K), str(bk), out, "1" if pow2 else "0",
+                    str(want_pair)], env=env, check=True, timeout=600, cwd=root)
     return np.load(out)
+
+
+@pytest.mark.parametrize("M,N,K,bk,pow2", [(300, 520, 1024, 128, True), (300, 520, 1024, 128, False),
+                                           (513, 264, 2048, 32, True), (1100, 520, 1024, 32, False),
+                                           (4100, 1032, 1536, 128, True)])
+def test_cta_pairs_match_oracle(tmp_path, M, N, K, bk, pow2):
+    """The opt-in CTA-pair tiles (SGQ_PAIR=1: 256 x 256 tiles on two SMs,
+    .cta_group::2): ragged M and N, both recipes, UE8M0 scales (block-scaled
+    MMA) and fp32 scales (promotion).  SGQ_MIDSWAP=0 keeps M <= 1024 off the
+    swap-AB tiles; the child process checks that its plan took pairs, and D is
+    checked against the oracle here."""
+    d = _child_gemm(tmp_path, "pair", {"SGQ_PAIR": "1", "SGQ_MIDSWAP": "0"}, M, N, K, bk, pow2, 1)
+    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=31), bk, pow2)
+    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=31), bk, bk, pow2)
+    dref, bound = oracle.gemm(aq, a_s, wq, ws, bk, bk)
+    check_gemm(torch.from_numpy(d).view(torch.bfloat16), dref, bound, f"pair M={M} N={N} K={K} bk={bk}")
 
 
 @pytest.mark.parametrize("M,N,K,bk", [(16, 24576, 1536, 128), (8, 24576, 1536, 32)])
