@@ -57,9 +57,23 @@ struct DualArgs {
     const float* Ws;        // fp32 [ceil(N / blk_n), K / blk_k]
     __nv_bfloat16* D;       // bf16 [M, N]
     uint32_t* status;       // device status word
+    float* partial;         // splits > 1: one fp32 partial tile per item (splits * per * 128 floats)
+    uint32_t* counters;     // splits > 1: one arrival count per tile, a multiple of 16 between launches
     int M, N, K, ks;        // ks = K / blk_k
     int tiles_r, tiles_c, kst, tiles, group_r;
+    int splits, kps, items; // K splits per tile (<= 16), K stages per split (every split non-empty), tiles x splits
+    int per;                // splits > 1: warp units (32 x 4 floats) per slice stride, 8 * ceil(BN / 4 / splits)
 };
+
+// Split-K exchange: shared memory for the slices a CTA receives from the
+// other splits plus its staged slice of D.  The host takes only split counts
+// whose (splits - 1) * 8 * ceil(BN / 4 / splits) units of 512 bytes and
+// 256 rows of 8 * ceil(BN / 4 / splits) + 8 bytes fit in it.
+constexpr int kRedArea = 212 * 1024;
+constexpr int red_need(int bn, int splits) {
+    const int ngmax = (bn / 4 + splits - 1) / splits;
+    return (splits - 1) * 8 * ngmax * 512 + 256 * (8 * ngmax + 8);
+}
 
 // UE8M0 words (tcgen05.cp order) of one stage: half h's 128 activation rows,
 // and the weight rows (two 128-row copies).
@@ -68,24 +82,32 @@ struct alignas(128) Slot {
     uint32_t sfb[256];
 };
 
-template <int BN>
+template <int BN, bool kSplit>
 struct Cfg {
     static constexpr int kABytes = kRowsA * kBK;
     static constexpr int kBBytes = BN * kBK;
     static constexpr size_t kOffA = 0;
     static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
-    static constexpr size_t kOffSlot = kOffB + size_t(kStages) * kBBytes;
-    // barriers: full[kStages], empty[kStages], accf[2], acce[2], drain[2]
+    static constexpr int kRingBytes = kStages * (kABytes + kBBytes);
+    // Split-K launches also hold the exchange area: the other splits' slices
+    // of the partial tile land over the operand ring (idle once a CTA's only
+    // item is accumulated) and past it.  Other launches stop at the ring, so
+    // the SM keeps more of its L1 (the scale warps read through it).
+    static constexpr size_t kAreaEnd = size_t(kSplit && kRedArea > kRingBytes ? kRedArea : kRingBytes);
+    static constexpr size_t kOffSlot = kAreaEnd;
+    // barriers: full[kStages], empty[kStages], accf[2], acce[2], drain[2], red
     static constexpr size_t kOffBar = kOffSlot + size_t(kStages) * sizeof(Slot);
-    static constexpr int kNumBars = 2 * kStages + 6;
+    static constexpr int kNumBars = 2 * kStages + 7;
     static constexpr size_t kOffMisc = kOffBar + 8 * kNumBars;
-    static constexpr size_t kSmem = kOffMisc + 64 + 1024;
+    // misc: 8 words (and, split-K, the 17 slice bounds), then alignment slack
+    static constexpr size_t kSmem = kOffMisc + (kSplit ? 128 : 64) + 1024;
     // TMEM: accumulator h at columns [h*BN, (h+1)*BN), then two scale slots
     // of 16 columns per issuer (A words at +0, B words at +4 .. +11)
     static constexpr uint32_t kSfCol = 2u * BN;
     static_assert(BN % 16 == 0 && BN <= 256 && BN > 128, "MMA N (two B scale copies)");
     static_assert(kSfCol + 64u <= kTmemCols, "TMEM: two accumulators and the scale slots");
     static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "128-byte swizzle atoms");
+    static_assert(kOffSlot % 128 == 0, "scale slots aligned");
     static_assert(kSmem <= 232448, "shared memory");
     static constexpr int kColsPerWarp = BN / 2;       // epilogue: two warps per lane quadrant
     static_assert(kColsPerWarp % 16 == 0, "16-column epilogue chunks");
@@ -160,11 +182,49 @@ __device__ __forceinline__ void tile_coords(const DualArgs& a, int t, int& tr, i
     tc = in / gm;
 }
 
-template <int BN, int kBlkN, int kBlkK>
+// Work item i = (tile i / splits, K split i % splits): K stages [kb0, kb1).
+// The splits of a tile are consecutive items, so with one item per CTA they
+// run at the same time on neighbouring CTAs.
+struct Item {
+    int t, sp, tr, tc, kb0, kb1;
+};
+// (The scale warps ask once per K stage: nothing to compute without split-K.)
+template <bool kSplit>
+__device__ __forceinline__ int item_tile(const DualArgs& a, int i) {
+    if constexpr (kSplit) return i / a.splits;
+    else return i;
+}
+template <bool kSplit>
+__device__ __forceinline__ int item_kb0(const DualArgs& a, int i) {
+    if constexpr (kSplit) return (i % a.splits) * a.kps;
+    else return 0;
+}
+template <bool kSplit>
+__device__ __forceinline__ int item_kb1(const DualArgs& a, int i) {
+    if constexpr (kSplit) return min(a.kst, item_kb0<true>(a, i) + a.kps);
+    else return a.kst;
+}
+template <bool kSplit>
+__device__ __forceinline__ Item item_at(const DualArgs& a, int i) {
+    Item it;
+    it.t = item_tile<kSplit>(a, i);
+    it.sp = i - it.t * a.splits;
+    tile_coords(a, it.t, it.tr, it.tc);
+    it.kb0 = item_kb0<kSplit>(a, i);
+    it.kb1 = item_kb1<kSplit>(a, i);
+    return it;
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(8 * 32) : "memory"); }
+
+// kSplit: K split over several CTAs per tile (splits > 1), with the partial
+// exchange in the epilogue; a separate instantiation, so that the plain
+// kernel's registers are allocated without it.
+template <int BN, int kBlkN, int kBlkK, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     dual_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const DualArgs a) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, kSplit>;
     constexpr int kSps = kBK / kBlkK;      // scale columns per stage (1 or 4)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,7 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sB = smem + C::kOffB;
     Slot* slot = reinterpret_cast<Slot*>(smem + C::kOffSlot);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);   // [0] TMEM base, [1] abort flag
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    // misc: [0] TMEM base, [1] abort flag, [2] split-K go, [3] an epilogue warp gave up;
+    // misc[8 + s], s = 0 .. splits: first column group of slice s (split-K)
 
     const uint32_t bar0 = ptx::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -180,12 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto accf_bar = [&](int h) { return bar0 + 8u * (2 * kStages + h); };
     auto acce_bar = [&](int h) { return bar0 + 8u * (2 * kStages + 2 + h); };
     auto drain_bar = [&](int h) { return bar0 + 8u * (2 * kStages + 4 + h); };
+    const uint32_t red_bar = bar0 + 8u * (2 * kStages + 6);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Sync sync{reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
-    const int first_tile = static_cast<int>(blockIdx.x);
-    const int tile_step = static_cast<int>(gridDim.x);
+    const int first_item = static_cast<int>(blockIdx.x);
+    const int item_step = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -197,7 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(acce_bar(h), 8);    // one arrive per epilogue warp
             ptx::mbar_init(drain_bar(h), 1);
         }
+        if constexpr (kSplit) ptx::mbar_init(red_bar, 1);
         misc[1] = 0;
+        if constexpr (kSplit) {
+            misc[3] = 0;
+            for (int sp = 0; sp <= a.splits && sp <= 16; ++sp) misc[8 + sp] = static_cast<uint32_t>(sp * (BN / 4) / a.splits);
+        }
         ptx::fence_mbar_init();
     }
     // weight-row words past 224 (the second copy's tail) stay 2^0
@@ -227,22 +295,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         int n = 0;   // stage jobs issued
         bool failed = false;
         bool waited = false;
-        for (int t = first_tile; t < a.tiles && !failed; t += tile_step) {
-            int tr, tc;
-            tile_coords(a, t, tr, tc);
-            for (int kb = 0; kb < a.kst; ++kb, ++n) {
+        for (int i = first_item; i < a.items && !failed; i += item_step) {
+            const Item it = item_at<kSplit>(a, i);
+            for (int kb = it.kb0; kb < it.kb1; ++kb, ++n) {
                 const int s = n % kStages, r = n / kStages;
                 if (r > 0 && !wait_warp(empty_bar(s), (r - 1) & 1, sync, 1)) {
                     failed = true;
                     break;
                 }
                 ptx::mbar_arrive_expect_tx_if(leader, full_bar(s), C::kABytes + C::kBBytes);
-                ptx::tma_load_2d_if(leader, b0 + s * C::kBBytes, &tmB, kb * kBK, tc * BN, full_bar(s));
+                ptx::tma_load_2d_if(leader, b0 + s * C::kBBytes, &tmB, kb * kBK, it.tc * BN, full_bar(s));
                 if (!waited) {
                     ptx::grid_dependency_wait();   // Aq may be the preceding kernel's output
                     waited = true;
                 }
-                ptx::tma_load_2d_if(leader, a0 + s * C::kABytes, &tmA, kb * kBK, tr * kRowsA, full_bar(s));
+                ptx::tma_load_2d_if(leader, a0 + s * C::kABytes, &tmA, kb * kBK, it.tr * kRowsA, full_bar(s));
             }
         }
         if (!waited) ptx::grid_dependency_wait();
@@ -259,10 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         struct Raw {
             float4 a[4], b[4];
         };
-        auto load = [&](Raw& v, int t, int kb) {
-            if (t >= a.tiles) return;
+        auto load = [&](Raw& v, int i, int kb) {
+            if (i >= a.items) return;
             int tr, tc;
-            tile_coords(a, t, tr, tc);
+            tile_coords(a, item_tile<kSplit>(a, i), tr, tc);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int row = tr * kRowsA + h * kHalf + lane + 32 * j;
@@ -275,13 +342,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
             }
         };
-        auto advance = [&](int& t, int& kb) {
-            if (++kb == a.kst) {
-                kb = 0;
-                t += tile_step;
+        auto advance = [&](int& i, int& kb) {
+            if (++kb == item_kb1<kSplit>(a, i)) {
+                i += item_step;
+                kb = item_kb0<kSplit>(a, i);
             }
         };
-        int t = first_tile, kb = 0;        // stage being converted
+        int t = first_item, kb = item_kb0<kSplit>(a, first_item);   // (item, stage) being converted
         int t1 = t, kb1 = kb;
         advance(t1, kb1);                  // stage n + 1
         int t2 = t1, kb2 = kb1;
@@ -291,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         load(p0, t1, kb1);
         int n = 0;
         uint32_t bad_all = 0;
-        while (t < a.tiles) {
+        while (t < a.items) {
             load(p1, t2, kb2);
             const int s = n % kStages, r = n / kStages;
             if (r > 0 && !wait_warp(empty_bar(s), (r - 1) & 1, sync, 2)) break;
@@ -336,11 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + static_cast<uint32_t>(h * BN);
         int n = 0, ntile = 0;
         bool failed = false;
-        for (int t = first_tile; t < a.tiles && !failed; t += tile_step, ++ntile) {
+        for (int i = first_item; i < a.items && !failed; i += item_step, ++ntile) {
             // the accumulator must have been read by the epilogue
             if (ntile > 0 && !wait_warp(acce_bar(h), (ntile - 1) & 1, sync, 3)) break;
             ptx::tc_fence_after();
-            for (int kb = 0; kb < a.kst; ++kb, ++n) {
+            const int kb0 = item_kb0<kSplit>(a, i), kb1 = item_kb1<kSplit>(a, i);
+            for (int kb = kb0; kb < kb1; ++kb, ++n) {
                 const int s = n % kStages, r = n / kStages;
                 if (!wait_warp(full_bar(s), r & 1, sync, 4)) {
                     failed = true;
@@ -353,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      bd_base + static_cast<uint64_t>(s * (C::kBBytes >> 4)),
                                      ptx::idesc_sf_ids(idesc_mx, 0, 0), ptx::idesc_sf_ids(idesc_mx, 1, 1),
                                      ptx::idesc_sf_ids(idesc_mx, 2, 2), ptx::idesc_sf_ids(idesc_mx, 3, 3), t_sfa,
-                                     t_sfb, sfa_base + so, sfb_base + so, kb > 0 ? 1u : 0u);
+                                     t_sfb, sfa_base + so, sfb_base + so, kb > kb0 ? 1u : 0u);
                 ptx::commit_elect(empty_bar(s));   // frees the stage once both halves' MMAs are done
             }
             if (failed) break;
@@ -366,53 +434,242 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue (warps 4-11)
         const int ew = warp - kEpi0;            // 0 .. 7
         const int quad = warp & 3;              // TMEM lane quadrant
-        const int chalf = ew >> 2;              // which half of the columns
+        const int chalf = ew >> 2;              // which half of the columns (split-K sum: which half of the rows)
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         ptx::grid_dependency_wait();            // D may still be read by the preceding kernel
         const bool v8 = ((reinterpret_cast<uintptr_t>(a.D) | (static_cast<uintptr_t>(a.N) * 2u)) & 31u) == 0;
+        volatile uint32_t* gave_up = misc + 3;
         int ntile = 0;
-        for (int t = first_tile; t < a.tiles; t += tile_step, ++ntile) {
-            int tr, tc;
-            tile_coords(a, t, tr, tc);
+        for (int i = first_item; i < a.items; i += item_step, ++ntile) {
+            const Item it = item_at<kSplit>(a, i);
             bool failed = false;
-            for (int h = 0; h < 2 && !failed; ++h) {
-                if (!wait_warp(accf_bar(h), ntile & 1, sync, 6)) {
-                    failed = true;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const int grow = tr * kRowsA + h * kHalf + quad * 32 + lane;
-                __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
-#pragma unroll
-                for (int c0 = 0; c0 < C::kColsPerWarp; c0 += 16) {
-                    const int cl = chalf * C::kColsPerWarp + c0;   // column inside the tile
-                    uint32_t rr[16];
-                    ptx::tmem_ld<16>(t_lane + static_cast<uint32_t>(h * BN + cl), rr);
-                    ptx::tmem_wait_ld();
-                    uint32_t w[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const __nv_bfloat162 p =
-                            __floats2bfloat162_rn(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
-                        w[i] = *reinterpret_cast<const uint32_t*>(&p);
+            if constexpr (!kSplit) {
+                for (int h = 0; h < 2 && !failed; ++h) {
+                    if (!wait_warp(accf_bar(h), ntile & 1, sync, 6)) {
+                        failed = true;
+                        break;
                     }
-                    const int gcol = tc * BN + cl;
-                    if (grow < a.M) {
-                        if (v8 && gcol + 16 <= a.N) {
-                            ptx::st_global_v8(drow + gcol, w);
-                        } else {
-                            if (gcol < a.N)
-                                *reinterpret_cast<uint4*>(drow + gcol) = make_uint4(w[0], w[1], w[2], w[3]);
-                            if (gcol + 8 < a.N)
-                                *reinterpret_cast<uint4*>(drow + gcol + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                    ptx::tc_fence_after();
+                    const int grow = it.tr * kRowsA + h * kHalf + quad * 32 + lane;
+                    __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
+#pragma unroll
+                    for (int c0 = 0; c0 < C::kColsPerWarp; c0 += 16) {
+                        const int cl = chalf * C::kColsPerWarp + c0;   // column inside the tile
+                        uint32_t rr[16];
+                        ptx::tmem_ld<16>(t_lane + static_cast<uint32_t>(h * BN + cl), rr);
+                        ptx::tmem_wait_ld();
+                        uint32_t w[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const __nv_bfloat162 p =
+                                __floats2bfloat162_rn(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
+                            w[j] = *reinterpret_cast<const uint32_t*>(&p);
+                        }
+                        const int gcol = it.tc * BN + cl;
+                        if (grow < a.M) {
+                            if (v8 && gcol + 16 <= a.N) {
+                                ptx::st_global_v8(drow + gcol, w);
+                            } else {
+                                if (gcol < a.N)
+                                    *reinterpret_cast<uint4*>(drow + gcol) = make_uint4(w[0], w[1], w[2], w[3]);
+                                if (gcol + 8 < a.N)
+                                    *reinterpret_cast<uint4*>(drow + gcol + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                            }
+                        }
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(acce_bar(h));
+                }
+                if (failed) break;
+                continue;
+            }
+            if constexpr (kSplit) {
+                // ---- split-K, deterministic.  The tile's BN / 4 column groups
+                // (four columns each) are cut into `splits` contiguous slices;
+                // split s sums slice s over all splits in split order
+                // (p_0 + p_1 + ...) and writes that slice of D.  Partials move in
+                // warp units (32 rows x 4 columns, 512 bytes) of row block rb
+                // (half h, lane quadrant) and group g, slice-major: slice s at
+                // unit s * per, then rb * (its groups) + (g - its first group).
+                // Every move is a bulk copy through shared memory: the operand
+                // ring is idle once the CTA's only item is accumulated.  The
+                // epilogue warps meet at named barriers from here on, so a warp
+                // that gave up says so and all of them leave together.
+                constexpr int G = BN / 4;
+                const int S = a.splits;
+                const volatile uint32_t* lo_tab = misc + 8;   // first group of each slice, and G at [S]
+                auto lo_of = [&](int s) { return static_cast<int>(lo_tab[s]); };
+                const int glo = lo_of(it.sp), ng = lo_of(it.sp + 1) - glo;   // this CTA's slice
+                const int64_t pstride = int64_t(S) * a.per * 128;             // floats per item's partial
+                const uint32_t stage = ptx::smem_u32(sA);
+                for (int h = 0; h < 2 && !failed; ++h) failed = !wait_warp(accf_bar(h), ntile & 1, sync, 6);
+                ptx::tc_fence_after();
+                if (!failed) {
+                    // The other slices' units of this partial, slice-major as in
+                    // global memory: this warp's groups gA .. gB of each slice.
+                    constexpr int kBatch = 8;
+                    const int gA = chalf * (G / 2), gB = gA + G / 2;
+                    for (int h = 0; h < 2; ++h) {
+                        const int rb = h * 4 + quad;
+                        const uint32_t t_h = t_lane + static_cast<uint32_t>(h * BN);
+                        for (int s = 0, jj = 0; s < S; ++s) {
+                            if (s == it.sp) continue;
+                            const int lo = lo_of(s), n = lo_of(s + 1) - lo;
+                            const int g0 = max(lo, gA), g1 = min(lo + n, gB);
+                            const uint32_t st0 = stage + static_cast<uint32_t>(((jj * a.per + rb * n - lo) * 32 + lane) * 16);
+                            ++jj;
+                            for (int gb = g0; gb < g1; gb += kBatch) {
+                                uint32_t v[kBatch][4];
+    #pragma unroll
+                                for (int b = 0; b < kBatch; ++b)
+                                    if (gb + b < g1) ptx::tmem_ld<4>(t_h + static_cast<uint32_t>((gb + b) * 4), v[b]);
+                                ptx::tmem_wait_ld();
+    #pragma unroll
+                                for (int b = 0; b < kBatch; ++b) {
+                                    if (gb + b >= g1) break;
+                                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(st0 + (gb + b) * 512),
+                                                 "r"(v[b][0]), "r"(v[b][1]), "r"(v[b][2]), "r"(v[b][3])
+                                                 : "memory");
+                                }
+                            }
+                        }
+                    }
+                }
+                if (failed && lane == 0) *gave_up = 1u;
+                ptx::fence_proxy_async_smem();   // the staged units are read by bulk copies
+                uint32_t* cnt = a.counters + it.t;
+                epi_sync();
+                if (*gave_up != 0u) break;
+                if (ew == 0 && lane == 0) {
+                    float* pbase = a.partial + static_cast<int64_t>(i) * pstride;
+                    for (int s = 0, jj = 0; s < S; ++s) {
+                        if (s == it.sp) continue;
+                        const uint32_t n = static_cast<uint32_t>(lo_of(s + 1) - lo_of(s));
+                        ptx::bulk_store(pbase + int64_t(s) * a.per * 128, stage + jj * a.per * 512, n * 8u * 512u);
+                        ++jj;
+                    }
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_all();            // written, and the staging area free again
+                    ptx::fence_proxy_async_all();
+                    // Arrival count: each launch adds `splits` per tile, and the
+                    // last arriver pads it to the next multiple of 16, so a launch
+                    // starts on a multiple of 16 and needs no reset.
+                    const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt, 1u);
+                    const uint32_t base = old & ~15u;
+                    if (old - base == static_cast<uint32_t>(S - 1) && S < 16) atomicAdd(cnt, 16u - static_cast<uint32_t>(S));
+                    const uint64_t t0 = ptx::globaltimer();
+                    uint32_t ok = 1;
+                    uint32_t spins = 0;
+                    while (ptx::ld_acquire_gpu(cnt) - base < static_cast<uint32_t>(S)) {
+                        if ((++spins & 15u) == 0 && ptx::globaltimer() - t0 > kTimeoutNs) {
+                            *sync.abort_flag = 1u;
+                            atomicOr(a.status, kStatusTimeout | (7u << 8));
+                            ok = 0;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    ptx::fence_proxy_async_all();   // before the bulk copies of the other partials
+                    misc[2] = ok;
+                    if (ok) {
+                        // this slice of every other split's partial, all in flight at once
+                        const uint32_t bytes = static_cast<uint32_t>(ng) * 8u * 512u;
+                        ptx::mbar_arrive_expect_tx(red_bar, bytes * static_cast<uint32_t>(S - 1));
+                        const float* tbase = a.partial + static_cast<int64_t>(it.t) * S * pstride + int64_t(it.sp) * a.per * 128;
+                        for (int j = 0, jj = 0; j < S; ++j) {
+                            if (j == it.sp) continue;
+                            ptx::bulk_load(stage + jj * bytes, tbase + j * pstride, bytes, red_bar);
+                            ++jj;
+                        }
+                    }
+                }
+                epi_sync();
+                if (*reinterpret_cast<volatile uint32_t*>(misc + 2) == 0u) break;
+                const bool ok = wait_warp(red_bar, 0, sync, 8);
+                if (!ok && lane == 0) {
+                    *gave_up = 1u;
+                    if (ew == 0) {   // the copies in flight land before the CTA leaves (bounded)
+                        const uint64_t t1 = ptx::globaltimer();
+                        while (!ptx::mbar_try_wait(red_bar, 0) && ptx::globaltimer() - t1 < (1ull << 26)) {
+                        }
+                    }
+                }
+                // D of the slice, bf16, staged row-major after the received units
+                const int dstride = ng * 8 + 8;   // bytes per staged row
+                const uint32_t dstage = stage + static_cast<uint32_t>((S - 1) * ng * 8 * 512);
+                if (ok) {
+                    // warp (quadrant, half chalf): rows chalf * 128 + quad * 32 + lane
+                    const int rb = chalf * 4 + quad;
+                    const uint32_t t_row = t_lane + static_cast<uint32_t>(chalf * BN + glo * 4);
+                    constexpr int kBatch = 8;
+                    for (int g0 = 0; g0 < ng; g0 += kBatch) {
+                        uint32_t own[kBatch][4];
+    #pragma unroll
+                        for (int b = 0; b < kBatch; ++b)
+                            if (g0 + b < ng) ptx::tmem_ld<4>(t_row + static_cast<uint32_t>((g0 + b) * 4), own[b]);
+                        ptx::tmem_wait_ld();
+    #pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            if (g0 + b >= ng) break;
+                            const uint32_t src = stage + ((rb * ng + g0 + b) * 32 + lane) * 16;
+                            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            for (int j = 0, jj = 0; j < S; ++j) {
+                                float4 v;
+                                if (j == it.sp) {
+                                    v = make_float4(__uint_as_float(own[b][0]), __uint_as_float(own[b][1]),
+                                                    __uint_as_float(own[b][2]), __uint_as_float(own[b][3]));
+                                } else {
+                                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                                                 : "r"(src + static_cast<uint32_t>(jj * ng * 8 * 512)));
+                                    ++jj;
+                                }
+                                if (j == 0) {
+                                    acc = v;
+                                } else {
+                                    acc.x += v.x;
+                                    acc.y += v.y;
+                                    acc.z += v.z;
+                                    acc.w += v.w;
+                                }
+                            }
+                            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                            const uint32_t at = dstage + static_cast<uint32_t>((chalf * 128 + quad * 32 + lane) * dstride + (g0 + b) * 8);
+                            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(at),
+                                         "r"(*reinterpret_cast<const uint32_t*>(&lo)),
+                                         "r"(*reinterpret_cast<const uint32_t*>(&hi))
+                                         : "memory");
                         }
                     }
                 }
                 ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(acce_bar(h));
+                epi_sync();   // the slice of D is staged (and TMEM read)
+                if (*gave_up != 0u) break;
+                // coalesced stores: a warp takes 32 / ng rows at a time, consecutive
+                // lanes consecutive groups of a row (ng <= 32 for two splits or more)
+                {
+                    const int rpi = 32 / ng;                  // rows per warp iteration
+                    const int lr = lane / ng, gi = lane - lr * ng;
+                    const int row0 = it.tr * kRowsA, col = it.tc * BN + (glo + gi) * 4;
+                    if (lr < rpi && col < a.N) {              // N % 8 == 0: the four columns are all inside
+                        for (int r = ew * rpi + lr; r < kRowsA; r += 8 * rpi) {
+                            const int row = row0 + r;
+                            if (row >= a.M) break;
+                            uint32_t x0, x1;
+                            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                                         : "=r"(x0), "=r"(x1)
+                                         : "r"(dstage + static_cast<uint32_t>(r * dstride + gi * 8)));
+                            *reinterpret_cast<uint2*>(a.D + static_cast<int64_t>(row) * a.N + col) = make_uint2(x0, x1);
+                        }
+                    }
+                }
+                if (lane == 0) {
+                    ptx::mbar_arrive(acce_bar(0));
+                    ptx::mbar_arrive(acce_bar(1));
+                }
             }
-            if (failed) break;
         }
     }
 
@@ -424,15 +681,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, int kBlkN, int kBlkK>
+template <int BN, int kBlkN, int kBlkK, bool kSplit>
 sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a, int grid, cudaStream_t st) {
-    using C = Cfg<BN>;
-    auto kern = dual_gemm_kernel<BN, kBlkN, kBlkK>;
+    using C = Cfg<BN, kSplit>;
+    constexpr size_t kSmem = C::kSmem;
+    auto kern = dual_gemm_kernel<BN, kBlkN, kBlkK, kSplit>;
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
     if (!configured[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem)) !=
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem)) !=
             cudaSuccess)
             return SGQ_ERR_CUDA;
         configured[dev] = true;
@@ -440,7 +698,7 @@ sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.dynamicSmemBytes = kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -458,18 +716,24 @@ sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a
 constexpr int kBNWide = 224;
 constexpr int kBNNarrow = 192;
 
-template <int BN>
+template <int BN, bool kSplit>
 sgq_status dispatch_bn(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
                        int grid, cudaStream_t st) {
     if (blk_n == 32)
-        return blk_k == 32 ? run<BN, 32, 32>(tmA, tmB, a, grid, st) : run<BN, 32, 128>(tmA, tmB, a, grid, st);
-    return blk_k == 32 ? run<BN, 128, 32>(tmA, tmB, a, grid, st) : run<BN, 128, 128>(tmA, tmB, a, grid, st);
+        return blk_k == 32 ? run<BN, 32, 32, kSplit>(tmA, tmB, a, grid, st)
+                           : run<BN, 32, 128, kSplit>(tmA, tmB, a, grid, st);
+    return blk_k == 32 ? run<BN, 128, 32, kSplit>(tmA, tmB, a, grid, st)
+                       : run<BN, 128, 128, kSplit>(tmA, tmB, a, grid, st);
 }
-// One translation unit per width (gemm_dual_224.cu, gemm_dual_192.cu).
+// One translation unit per width and kind (gemm_dual_{224,192}{,s}.cu).
 sgq_status dispatch_224(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
                         int grid, cudaStream_t st);
 sgq_status dispatch_192(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
                         int grid, cudaStream_t st);
+sgq_status dispatch_224_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const DualArgs& a, int grid, cudaStream_t st);
+sgq_status dispatch_192_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const DualArgs& a, int grid, cudaStream_t st);
 
 }  // namespace dual
 }  // namespace sgq

@@ -6,7 +6,7 @@ namespace sgq {
 namespace dual {
 sgq_status dispatch_224(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
                         int grid, cudaStream_t st) {
-    return dispatch_bn<224>(blk_n, blk_k, tmA, tmB, a, grid, st);
+    return dispatch_bn<224, false>(blk_n, blk_k, tmA, tmB, a, grid, st);
 }
 }  // namespace dual
 }  // namespace sgq

@@ -65,9 +65,12 @@ sgq_status make_scale_map(CUtensorMap* m, const float* ptr, int64_t rows, int64_
     return r == CUDA_SUCCESS ? SGQ_OK : SGQ_ERR_CUDA;
 }
 
-// Split-K workspace, one per device, created on first need.
+// Split-K workspace, one per device, created on first need.  The last
+// kDualCounters arrival counts belong to the two-accumulator tiles (their
+// counts are never reset, only kept at multiples of 16).
 constexpr size_t kWsBytes = size_t(64) << 20;
 constexpr int kMaxCounters = 1 << 16;
+constexpr int kDualCounters = 1024;
 struct DevWs {
     float* partial = nullptr;
     uint32_t* counters = nullptr;
@@ -123,7 +126,7 @@ struct ScratchLimit {
     size_t partial_bytes;
     size_t counters;
 };
-constexpr ScratchLimit kWsLimit{kWsBytes, size_t(kMaxCounters)};
+constexpr ScratchLimit kWsLimit{kWsBytes, size_t(kMaxCounters - kDualCounters)};
 
 // wide_only: keep the 128 x 256 tiles for M > 64 (the issue-mode testing
 // flags compare the wide tiles' two issue modes).  lim: the split-K scratch
@@ -313,11 +316,49 @@ int dual_width(int64_t M, int64_t N, int sm_count) {
     return cost(dual::kBNNarrow) < cost(dual::kBNWide) ? dual::kBNNarrow : dual::kBNWide;
 }
 
+// K splits of the two-accumulator tiles.  Where the tiles alone leave SMs
+// idle, each tile's K stages are dealt out to several CTAs of one wave (one
+// item per CTA: the kernel stages the partials in its idle operand ring),
+// which then sum their fp32 partials in split order (deterministic).  Cost of s
+// splits, in K-stage times: ceil(kst / s) stages plus, for s > 1, the partial
+// exchange (each CTA stores a 256 x BN fp32 tile and reads as much back,
+// about four stages' time); the smallest s with the least cost is taken.
+// SGQ_DUAL_SPLITS forces a count.
+int dual_splits(int64_t tiles, int kst, int sm_count, int bn, ScratchLimit lim) {
+    static const int forced = env_int("SGQ_DUAL_SPLITS", 0);
+    auto fits = [&](int sp) {
+        const size_t per = 8u * size_t((bn / 4 + sp - 1) / sp);
+        return size_t(tiles) * size_t(sp) * size_t(sp) * per * 512u <= lim.partial_bytes &&
+               tiles <= kDualCounters && sp <= 16 && dual::red_need(bn, sp) <= dual::kRedArea;
+    };
+    int best = 1;
+    if (forced > 0) {
+        best = forced < kst ? forced : kst;
+        while (best > 1 && tiles * best > sm_count) --best;   // one item per CTA (the kernel's rule)
+    } else {
+        int64_t best_cost = kst;
+        for (int sp = 2; sp <= 16 && sp <= kst && tiles * sp <= sm_count; ++sp) {
+            if (!fits(sp)) continue;
+            const int64_t cost = (kst + sp - 1) / sp + 4;
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = sp;
+            }
+        }
+    }
+    // within the scratch and shared memory, every split non-empty:
+    // (splits - 1) * ceil(kst / splits) < kst
+    while (best > 1 && (!fits(best) || int64_t(best - 1) * ((kst + best - 1) / best) >= kst)) --best;
+    return best;
+}
+
 // Launches the two-accumulator prefill GEMM (power-of-two scales): tiles of
 // 256 activation rows x BN weight rows over a persistent grid of at most one
-// CTA per SM.
+// CTA per SM, with K split over several CTAs where the tiles are fewer than
+// the SMs.
 sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D, int64_t M,
-                       int64_t N, int64_t K, int blk_n, int blk_k, int sm_count, cudaStream_t st) {
+                       int64_t N, int64_t K, int blk_n, int blk_k, int sm_count, bool allow_split, ScratchLimit lim,
+                       cudaStream_t st) {
     const int bn = dual_width(M, N, sm_count);
     dual::DualArgs a{};
     a.As = As;
@@ -332,14 +373,65 @@ sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const fl
     a.kst = static_cast<int>(K / kBK);
     a.tiles = a.tiles_r * a.tiles_c;
     a.group_r = a.tiles_r < 16 ? a.tiles_r : 16;
+    a.splits = allow_split ? dual_splits(a.tiles, a.kst, sm_count, bn, lim) : 1;
+    a.kps = (a.kst + a.splits - 1) / a.splits;
+    a.items = a.tiles * a.splits;
+    a.per = 8 * ((bn / 4 + a.splits - 1) / a.splits);
     sgq_status rc = status_word(&a.status);
     if (rc != SGQ_OK) return rc;
+    if (a.splits > 1) {
+        DevWs ws;
+        rc = get_workspace(st, &ws);
+        if (rc != SGQ_OK) return rc;
+        a.partial = ws.partial;
+        a.counters = ws.counters + (kMaxCounters - kDualCounters);
+    }
     CUtensorMap maps[2];
     if (make_tmap(&maps[0], Aq, M, K, dual::kRowsA) != SGQ_OK || make_tmap(&maps[1], Wq, N, K, bn) != SGQ_OK)
         return SGQ_ERR_CUDA;
-    const int grid = a.tiles < sm_count ? a.tiles : sm_count;
+    const int grid = a.items < sm_count ? a.items : sm_count;
+    if (a.splits > 1)
+        return bn == dual::kBNNarrow ? dual::dispatch_192_split(blk_n, blk_k, maps[0], maps[1], a, grid, st)
+                                     : dual::dispatch_224_split(blk_n, blk_k, maps[0], maps[1], a, grid, st);
     return bn == dual::kBNNarrow ? dual::dispatch_192(blk_n, blk_k, maps[0], maps[1], a, grid, st)
                                  : dual::dispatch_224(blk_n, blk_k, maps[0], maps[1], a, grid, st);
+}
+
+// Whether a GEMM with the power-of-two promise runs on the two-accumulator
+// tiles: 0 no, 1 yes with one K split, 2 yes with the K splits dual_splits
+// chooses.  Rules, from timings on GB300 (CUDA graphs of 20 calls, weights
+// from HBM; SGQ_DUAL=0/1 forces the choice):
+// - a wave of 256 x 224 tiles or more (and not a swap-AB plan): always
+//   (4096 x 7168 x 7168: 168.6 vs 174.2 us on the 128 x 256 tiles);
+// - M >= 128 and at least 0.6 of a wave: one split (700 x 7168 x 2048:
+//   19.7 vs 28.2 us; 128 x 24576 x 1536: 14.7 vs 16.9 us);
+// - M >= 768 with fewer tiles: K splits, where the split plan's estimate,
+//   0.8 us per K stage of a split plus ~2.5 us of pipeline fill plus ~9 us of
+//   partial exchange, is under 1/1.3 of the 128 x 256 tiles' estimate, rounds
+//   x (0.5 us per K stage + 3 us) (1024 x 1536 x 7168: 25.3 vs 36.7 us; at
+//   2048 x 1536 x 7168 and at M <= 512 the split plans measured no faster).
+int dual_mode(int64_t M, int64_t N, int64_t K, int blk_k, uint32_t flags, const Plan& p, int sm_count,
+              ScratchLimit lim) {
+    static const int dual_env = env_int("SGQ_DUAL", -1);
+    if (!(flags & SGQ_GEMM_SCALES_POW2) || K % kBK != 0 || M <= 64 ||
+        (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0)
+        return 0;
+    if (dual_env >= 0) return dual_env == 0 ? 0 : 2;
+    (void)blk_k;
+    const int64_t tr = (M + dual::kRowsA - 1) / dual::kRowsA;
+    const int64_t dual_tiles = tr * ((N + dual::kBNWide - 1) / dual::kBNWide);
+    if (!p.swap && dual_tiles >= sm_count) return 1;
+    if (M >= 128 && dual_tiles * 5 >= int64_t(sm_count) * 3) return 1;
+    if (M < 768) return 0;
+    const int bn = dual_width(M, N, sm_count);
+    const int64_t tiles = tr * ((N + bn - 1) / bn);
+    const int kst = static_cast<int>(K / kBK);
+    const int sp = dual_splits(tiles, kst, sm_count, bn, lim);
+    if (sp < 2) return 0;
+    const double est_dual = 0.8 * ((kst + sp - 1) / sp) + 2.5 + 9.0;
+    const int64_t t128 = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
+    const double est_wide = double((t128 + sm_count - 1) / sm_count) * (0.5 * kst + 3.0);
+    return est_wide > 1.3 * est_dual ? 2 : 0;
 }
 
 // Plans and launches one GEMM.  noalloc: split-K scratch from the fixed array
@@ -359,18 +451,16 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     // counts whose partials or counters would not fit are skipped, so such a
     // shape runs with fewer K splits (or, at mid M, on the 128 x 256 tiles
     // that need no split-K) instead of being refused.
-    const ScratchLimit lim = noalloc ? ScratchLimit{kNoAllocPartialBytes, kNoAllocCounterBytes / sizeof(uint32_t)}
-                                     : kWsLimit;
+    const ScratchLimit lim =
+        noalloc ? ScratchLimit{kNoAllocPartialBytes, kNoAllocCounterBytes / sizeof(uint32_t)} : kWsLimit;
     Plan p = make_plan(M, N, K, blk_k, di.sm_count, (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0,
                        lim);
-    // Power-of-two scales promised by the caller: wide-tile plans with at least
-    // a wave of 256 x 224 tiles run on those, two accumulators per tile
-    // (gemm_dual.cuh), K in whole stages.  (Fewer tiles than SMs: the 128-row
-    // tiles keep more SMs busy; 2048 x 1536 x 7168 measured 35.4 vs 43.3 us.)
-    const int64_t dual_tiles = ((M + dual::kRowsA - 1) / dual::kRowsA) * ((N + dual::kBNWide - 1) / dual::kBNWide);
-    if ((flags & SGQ_GEMM_SCALES_POW2) && !p.swap && !fuse && !chan && K % kBK == 0 && dual_tiles >= di.sm_count &&
-        (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) == 0)
-        return launch_dual(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, di.sm_count, st);
+    // Power-of-two scales promised by the caller: the two-accumulator tiles
+    // (gemm_dual.cuh, K in whole stages, M > 64) where they are measured
+    // faster than this plan.
+    if (int mode = dual_mode(M, N, K, blk_k, flags, p, di.sm_count, lim);
+        mode != 0 && !fuse && !chan)
+        return launch_dual(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, di.sm_count, mode == 2 && !noalloc, lim, st);
     if (flags & SGQ_GEMM_ISSUE_ALT) p.alt = !p.swap && !p.pair;
     if (flags & SGQ_GEMM_ISSUE_SINGLE) p.alt = false;
     if (chan) {   // plain tiles: no scale boxes, one issuer

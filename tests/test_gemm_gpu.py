@@ -346,7 +346,9 @@ def test_bounded_wait_times_out_and_the_stream_recovers(M, N, K, bk, flags):
 
 
 DUAL = [(300, 520, 1024, 128, 128), (513, 264, 2048, 32, 32), (4100, 7000, 1280, 128, 32), (257, 1032, 4096, 32, 128),
-        (2048, 448, 7168, 32, 32), (4096, 7168, 512, 128, 128), (4200, 7000, 384, 32, 32)]
+        (2048, 448, 7168, 32, 32), (4096, 7168, 512, 128, 128), (4200, 7000, 384, 32, 32),
+        (1024, 1536, 7168, 128, 128), (1000, 1032, 7168, 32, 128), (700, 7168, 2048, 32, 32),
+        (130, 24576, 1536, 128, 128)]
 
 
 @pytest.mark.parametrize("M,N,K,bn,bk", DUAL)
@@ -354,21 +356,69 @@ def test_scales_pow2_tiles_match_oracle(M, N, K, bn, bk):
     """SGQ_GEMM_SCALES_POW2 (every scale a power of two): the wide-tile plans
     with a wave of tiles run on 256 x 224 or 256 x 192 tiles with two
     accumulators (4096 x 7168 and 4200 x 7000 take the 192-wide tiles; the
-    small shapes keep the 128-row tiles).  Ragged M and N (partial row and
-    column tiles, N not a multiple of the width), both recipes and their mixes;
-    every row (or one of every 64-row block) against the oracle, and against
-    the default path within the same tolerance."""
+    small shapes keep the 128-row tiles); 700 x 7168 and 130 x 24576 (0.6 of a
+    wave) take them with one K split; 2048 x 448, 1024 x 1536 and 1000 x 1032
+    (fewer tiles, M >= 768) with K split over several CTAs that exchange
+    their partials.  Ragged M and N (partial row and column tiles, N not a
+    multiple of the width), both recipes and their mixes; every row (or one of
+    every 64-row block) against the oracle, and against the default path
+    within the same tolerance; a second call gives the same bits."""
     c = synth.Case("dual", M, N, K, bn, bk, True, seed=M + N)
     aq, a_s = oracle.quant_token_group(c.x(), bk, True)
     wq, ws = oracle.quant_weight_block(c.w(), bn, bk, True)
     args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
     d = sgq.fp8_block_gemm(*args, bn, bk, flags=sgq.SGQ_GEMM_SCALES_POW2)
     assert sgq.sgq_device_status() == 0
+    assert torch.equal(d, sgq.fp8_block_gemm(*args, bn, bk, flags=sgq.SGQ_GEMM_SCALES_POW2))
     r = np.arange(M) if M <= 600 else tile_rows(M, seed=M)
     dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
     rr = torch.from_numpy(r).cuda()
     check_gemm(d[rr], dref, bound, f"pow2 tiles M={M} N={N} K={K} [{bn},{bk}]")
     check_gemm(sgq.fp8_block_gemm(*args, bn, bk)[rr], dref, bound, "default path")
+
+
+_DUAL_CHILD = r"""
+import sys, numpy as np, torch
+import fp8_block_scaled_sgq_gb300 as sgq
+from fp8_block_scaled_sgq_gb300 import synth
+import oracle
+M, N, K, bn, bk = (int(v) for v in sys.argv[1:6])
+aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=43), bk, True)
+wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=43), bn, bk, True)
+args = [torch.from_numpy(t).cuda() for t in (aq, a_s, wq, ws)]
+d = sgq.fp8_block_gemm(*args, bn, bk, flags=sgq.SGQ_GEMM_SCALES_POW2)
+assert sgq.sgq_device_status() == 0
+assert torch.equal(d, sgq.fp8_block_gemm(*args, bn, bk, flags=sgq.SGQ_GEMM_SCALES_POW2))
+np.save(sys.argv[6], d.view(torch.int16).cpu().numpy())
+"""
+
+
+@pytest.mark.parametrize("splits", [2, 3, 5, 8, 16])
+@pytest.mark.parametrize("M,N,K,bn,bk", [(1000, 1032, 7168, 32, 128), (300, 1032, 7168, 128, 32),
+                                         (130, 448, 4096, 128, 128)])
+def test_dual_split_counts_match_oracle(tmp_path, M, N, K, bn, bk, splits):
+    """The two-accumulator tiles with K split over `splits` CTAs (forced with
+    SGQ_DUAL=1 SGQ_DUAL_SPLITS in a child process; the host lowers counts
+    beyond one wave of CTAs or whose exchange does not fit: 1000 x 1032 runs
+    at most 6, 300 x 1032 at most 12, 130 x 448 all of them).  Each split
+    count sums the partials in its own fixed order: D is checked against the
+    oracle on every 64-row block, and the child checks that a second call
+    gives the same bits."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"), SGQ_DUAL="1",
+               SGQ_DUAL_SPLITS=str(splits))
+    out = str(tmp_path / "d.npy")
+    subprocess.run([sys.executable, "-c", _DUAL_CHILD, str(M), str(N), str(K), str(bn), str(bk), out], env=env,
+                   check=True, timeout=600, cwd=root)
+    d = torch.from_numpy(np.load(out)).view(torch.bfloat16)
+    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=43), bk, True)
+    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=43), bn, bk, True)
+    r = tile_rows(M, seed=splits)
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
+    check_gemm(d[torch.from_numpy(r)], dref, bound, f"dual splits={splits} M={M} N={N} K={K}")
 
 
 @pytest.mark.parametrize("name", ["prefill_block128", "prefill_block32"])
