@@ -82,25 +82,31 @@ struct alignas(128) Slot {
     uint32_t sfb[256];
 };
 
-template <int BN, bool kSplit>
+template <int BN, bool kSplit, bool kPair = false>
 struct Cfg {
+    // kPair: a cluster of two CTAs shares a tile of 512 activation rows (256
+    // per CTA, as two 128-row halves) x BN weight rows (BN / 2 per CTA); the
+    // leader issues M = 256 MMAs over both CTAs' halves (.cta_group::2).
+    static constexpr int kSt = kPair ? 4 : kStages;           // ring stages
     static constexpr int kABytes = kRowsA * kBK;
-    static constexpr int kBBytes = BN * kBK;
+    static constexpr int kBBytes = (kPair ? BN / 2 : BN) * kBK;
     static constexpr size_t kOffA = 0;
-    static constexpr size_t kOffB = kOffA + size_t(kStages) * kABytes;
-    static constexpr int kRingBytes = kStages * (kABytes + kBBytes);
+    static constexpr size_t kOffB = kOffA + size_t(kSt) * kABytes;
+    static constexpr int kRingBytes = kSt * (kABytes + kBBytes);
     // Split-K launches also hold the exchange area: the other splits' slices
     // of the partial tile land over the operand ring (idle once a CTA's only
     // item is accumulated) and past it.  Other launches stop at the ring, so
     // the SM keeps more of its L1 (the scale warps read through it).
     static constexpr size_t kAreaEnd = size_t(kSplit && kRedArea > kRingBytes ? kRedArea : kRingBytes);
     static constexpr size_t kOffSlot = kAreaEnd;
-    // barriers: full[kStages], empty[kStages], accf[2], acce[2], drain[2], red
-    static constexpr size_t kOffBar = kOffSlot + size_t(kStages) * sizeof(Slot);
-    static constexpr int kNumBars = 2 * kStages + 7;
+    // barriers: full[kSt], empty[kSt], accf[2], acce[2], drain[2], red
+    static constexpr size_t kOffBar = kOffSlot + size_t(kSt) * sizeof(Slot);
+    static constexpr int kNumBars = 2 * kSt + 7;
     static constexpr size_t kOffMisc = kOffBar + 8 * kNumBars;
+    // pair: 16-byte signal buffers of the peer's two scale warps
+    static constexpr size_t kOffXfer = (kOffMisc + 64 + 15) & ~size_t(15);
     // misc: 8 words (and, split-K, the 17 slice bounds), then alignment slack
-    static constexpr size_t kSmem = kOffMisc + (kSplit ? 128 : 64) + 1024;
+    static constexpr size_t kSmem = (kPair ? kOffXfer + 32 : kOffMisc + (kSplit ? 128 : 64)) + 1024;
     // TMEM: accumulator h at columns [h*BN, (h+1)*BN), then two scale slots
     // of 16 columns per issuer (A words at +0, B words at +4 .. +11)
     static constexpr uint32_t kSfCol = 2u * BN;
@@ -109,6 +115,7 @@ struct Cfg {
     static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0, "128-byte swizzle atoms");
     static_assert(kOffSlot % 128 == 0, "scale slots aligned");
     static_assert(kSmem <= 232448, "shared memory");
+    static_assert(!(kSplit && kPair), "split-K runs on single-CTA tiles");
     static constexpr int kColsPerWarp = BN / 2;       // epilogue: two warps per lane quadrant
     static_assert(kColsPerWarp % 16 == 0, "16-column epilogue chunks");
 };
@@ -118,11 +125,19 @@ struct Sync {
     uint32_t* status;
 };
 
+// kCl: the barrier also receives arrivals from the other CTA of a pair
+// (acquire at cluster scope).
+template <bool kCl = false>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+    if constexpr (kCl) return ptx::mbar_try_wait_cluster(bar, parity);
+    else return ptx::mbar_try_wait(bar, parity);
+}
+template <bool kCl = false>
 static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
     const uint64_t t0 = ptx::globaltimer();
     uint32_t spins = 0;
     while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (try_wait_scoped<kCl>(bar, parity)) return true;
         if ((++spins & 15u) == 0) {
             const uint64_t dt = ptx::globaltimer() - t0;
             if (dt > kAbortPollNs && *s.abort_flag) return false;
@@ -135,9 +150,11 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, con
         if (spins > 8) __nanosleep(32);
     }
 }
+template <bool kCl = false>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Sync& s, uint32_t where) {
     uint32_t ok = 1;
-    if ((threadIdx.x & 31) == 0 && !ptx::mbar_try_wait(bar, parity)) ok = wait_slow(bar, parity, s, where) ? 1u : 0u;
+    if ((threadIdx.x & 31) == 0 && !try_wait_scoped<kCl>(bar, parity))
+        ok = wait_slow<kCl>(bar, parity, s, where) ? 1u : 0u;
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     __syncwarp();
     return ok != 0;
@@ -220,11 +237,13 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n
 // kSplit: K split over several CTAs per tile (splits > 1), with the partial
 // exchange in the epilogue; a separate instantiation, so that the plain
 // kernel's registers are allocated without it.
-template <int BN, int kBlkN, int kBlkK, bool kSplit>
+template <int BN, int kBlkN, int kBlkK, bool kSplit, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     dual_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const DualArgs a) {
-    using C = Cfg<BN, kSplit>;
+    using C = Cfg<BN, kSplit, kPair>;
+    constexpr int kCG = kPair ? 2 : 1;
+    constexpr int kTileRows = kRowsA * kCG;    // activation rows per tile (both CTAs of a pair)
     constexpr int kSps = kBK / kBlkK;      // scale columns per stage (1 or 4)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -238,26 +257,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t bar0 = ptx::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto accf_bar = [&](int h) { return bar0 + 8u * (2 * kStages + h); };
-    auto acce_bar = [&](int h) { return bar0 + 8u * (2 * kStages + 2 + h); };
-    auto drain_bar = [&](int h) { return bar0 + 8u * (2 * kStages + 4 + h); };
-    const uint32_t red_bar = bar0 + 8u * (2 * kStages + 6);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::kSt + s); };
+    auto accf_bar = [&](int h) { return bar0 + 8u * (2 * C::kSt + h); };
+    auto acce_bar = [&](int h) { return bar0 + 8u * (2 * C::kSt + 2 + h); };
+    auto drain_bar = [&](int h) { return bar0 + 8u * (2 * C::kSt + 4 + h); };
+    const uint32_t red_bar = bar0 + 8u * (2 * C::kSt + 6);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Sync sync{reinterpret_cast<volatile uint32_t*>(misc + 1), a.status};
-    const int first_item = static_cast<int>(blockIdx.x);
-    const int item_step = static_cast<int>(gridDim.x);
+    // pair: rank 0 leads (issues every tcgen05 op of the pair); a pair walks
+    // the items with index blockIdx.x / 2
+    const uint32_t rank = kPair ? ptx::cluster_rank() : 0u;
+    const int first_item = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int item_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    auto at_leader = [&](uint32_t bar) { return kPair ? ptx::mapa(bar, 0u) : bar; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kSt; ++s) {
             ptx::mbar_init(full_bar(s), 3);    // producer expect_tx + the two scale warps
             ptx::mbar_init(empty_bar(s), 2);   // a commit of each issuer
         }
         for (int h = 0; h < 2; ++h) {
             ptx::mbar_init(accf_bar(h), 1);    // the issuer's commit after the tile's last stage
-            ptx::mbar_init(acce_bar(h), 8);    // one arrive per epilogue warp
+            ptx::mbar_init(acce_bar(h), 8 * kCG);   // one arrive per epilogue warp (pair leader: of both CTAs)
             ptx::mbar_init(drain_bar(h), 1);
         }
         if constexpr (kSplit) ptx::mbar_init(red_bar, 1);
@@ -269,17 +292,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
     }
     // weight-row words past 224 (the second copy's tail) stay 2^0
-    for (int i = threadIdx.x; i < kStages * 256; i += kThreads) slot[i / 256].sfb[i % 256] = 0x7F7F7F7Fu;
+    for (int i = threadIdx.x; i < C::kSt * 256; i += kThreads) slot[i / 256].sfb[i % 256] = 0x7F7F7F7Fu;
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
-        ptx::tmem_relinquish();
+        if constexpr (kPair) {
+            ptx::tmem_alloc_g<2>(ptx::smem_u32(misc), kTmemCols);
+            ptx::tmem_relinquish_g<2>();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) ptx::cluster_sync();   // both CTAs' barriers exist before any remote operation
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
     // The next kernel on the stream may launch now; it still waits for this
@@ -298,18 +327,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = first_item; i < a.items && !failed; i += item_step) {
             const Item it = item_at<kSplit>(a, i);
             for (int kb = it.kb0; kb < it.kb1; ++kb, ++n) {
-                const int s = n % kStages, r = n / kStages;
-                if (r > 0 && !wait_warp(empty_bar(s), (r - 1) & 1, sync, 1)) {
+                const int s = n % C::kSt, r = n / C::kSt;
+                if (r > 0 && !wait_warp<kPair>(empty_bar(s), (r - 1) & 1, sync, 1)) {
                     failed = true;
                     break;
                 }
-                ptx::mbar_arrive_expect_tx_if(leader, full_bar(s), C::kABytes + C::kBBytes);
-                ptx::tma_load_2d_if(leader, b0 + s * C::kBBytes, &tmB, kb * kBK, it.tc * BN, full_bar(s));
+                // pair: both CTAs' boxes (and the peer's two scale signals) land on the leader's barrier
+                ptx::mbar_arrive_expect_tx_if(leader && rank == 0u, full_bar(s),
+                                              kCG * (C::kABytes + C::kBBytes) + (kPair ? 32 : 0));
+                const int brow = it.tc * BN + static_cast<int>(rank) * (BN / kCG);
+                const int arow = it.tr * kTileRows + static_cast<int>(rank) * kRowsA;
+                if constexpr (kPair)
+                    ptx::tma_load_2d_pair_if(leader, b0 + s * C::kBBytes, &tmB, kb * kBK, brow, at_leader(full_bar(s)));
+                else
+                    ptx::tma_load_2d_if(leader, b0 + s * C::kBBytes, &tmB, kb * kBK, brow, full_bar(s));
                 if (!waited) {
                     ptx::grid_dependency_wait();   // Aq may be the preceding kernel's output
                     waited = true;
                 }
-                ptx::tma_load_2d_if(leader, a0 + s * C::kABytes, &tmA, kb * kBK, it.tr * kRowsA, full_bar(s));
+                if constexpr (kPair)
+                    ptx::tma_load_2d_pair_if(leader, a0 + s * C::kABytes, &tmA, kb * kBK, arow, at_leader(full_bar(s)));
+                else
+                    ptx::tma_load_2d_if(leader, a0 + s * C::kABytes, &tmA, kb * kBK, arow, full_bar(s));
             }
         }
         if (!waited) ptx::grid_dependency_wait();
@@ -332,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(a, item_tile<kSplit>(a, i), tr, tc);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int row = tr * kRowsA + h * kHalf + lane + 32 * j;
+                const int row = tr * kTileRows + static_cast<int>(rank) * kRowsA + h * kHalf + lane + 32 * j;
                 v.a[j] = row < a.M ? load_scales<kSps>(a.As + static_cast<int64_t>(row) * a.ks + kb * kSps)
                                    : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
                 const int i = lane + 32 * j;
@@ -360,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t bad_all = 0;
         while (t < a.items) {
             load(p1, t2, kb2);
-            const int s = n % kStages, r = n / kStages;
-            if (r > 0 && !wait_warp(empty_bar(s), (r - 1) & 1, sync, 2)) break;
+            const int s = n % C::kSt, r = n / C::kSt;
+            if (r > 0 && !wait_warp<kPair>(empty_bar(s), (r - 1) & 1, sync, 2)) break;
             Slot& sl = slot[s];
             uint32_t bad = 0;
             uint32_t w4[4];
@@ -379,7 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             bad_all |= bad;
             ptx::fence_proxy_async_smem();   // the words are read by tcgen05.cp
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(full_bar(s));
+            if constexpr (kPair) {
+                if (rank == 0u) {
+                    if (lane == 0) ptx::mbar_arrive(full_bar(s));
+                } else {
+                    // The peer signals the leader with a 16-byte copy: its
+                    // completion also orders the words written above (made
+                    // visible to the async proxy by the fence) before the
+                    // leader's tcgen05.cp reads them.
+                    const uint32_t x = ptx::smem_u32(smem + C::kOffXfer + 16 * h);
+                    ptx::bulk_copy_to_cluster_if(lane == 0 ? 1u : 0u, ptx::mapa(x, 0u), x, 16u,
+                                                 at_leader(full_bar(s)));
+                }
+            } else {
+                if (lane == 0) ptx::mbar_arrive(full_bar(s));
+            }
             ++n;
             cur = p0;
             p0 = p1;
@@ -391,10 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // A scale that is not a power of two breaks the caller's promise.
         if (__any_sync(0xFFFFFFFFu, bad_all != 0u) && lane == 0) atomicOr(a.status, kStatusBadScale);
-    } else if (warp == 1 || warp == 2) {
+    } else if ((warp == 1 || warp == 2) && (!kPair || rank == 0u)) {
         // ------------------------------------------------------------ MMA issuers
         const int h = warp - 1;
-        constexpr uint32_t idesc_mx = ptx::idesc_mxf8(kHalf, BN);
+        constexpr uint32_t idesc_mx = ptx::idesc_mxf8(kHalf * kCG, BN);
         const uint64_t ad_base = ptx::smem_desc(ptx::smem_u32(sA) + h * (kHalf * kBK), 16, 1024, ptx::kLayoutSw128);
         const uint64_t bd_base = ptx::smem_desc(ptx::smem_u32(sB), 16, 1024, ptx::kLayoutSw128);
         const uint64_t sfa_base = ptx::smem_desc(ptx::smem_u32(slot[0].sfa[h]), 128, 128, ptx::kLayoutNone);
@@ -405,31 +458,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool failed = false;
         for (int i = first_item; i < a.items && !failed; i += item_step, ++ntile) {
             // the accumulator must have been read by the epilogue
-            if (ntile > 0 && !wait_warp(acce_bar(h), (ntile - 1) & 1, sync, 3)) break;
+            if (ntile > 0 && !wait_warp<kPair>(acce_bar(h), (ntile - 1) & 1, sync, 3)) break;
             ptx::tc_fence_after();
             const int kb0 = item_kb0<kSplit>(a, i), kb1 = item_kb1<kSplit>(a, i);
             for (int kb = kb0; kb < kb1; ++kb, ++n) {
-                const int s = n % kStages, r = n / kStages;
-                if (!wait_warp(full_bar(s), r & 1, sync, 4)) {
+                const int s = n % C::kSt, r = n / C::kSt;
+                if (!wait_warp<kPair>(full_bar(s), r & 1, sync, 4)) {
                     failed = true;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t t_sfa = tmem + C::kSfCol + 32u * h + 16u * (n & 1), t_sfb = t_sfa + 4u;
                 const uint64_t so = static_cast<uint64_t>(s) * kSlotStep;
-                ptx::mx_stage2_elect(d, ad_base + static_cast<uint64_t>(s * (C::kABytes >> 4)),
-                                     bd_base + static_cast<uint64_t>(s * (C::kBBytes >> 4)),
-                                     ptx::idesc_sf_ids(idesc_mx, 0, 0), ptx::idesc_sf_ids(idesc_mx, 1, 1),
-                                     ptx::idesc_sf_ids(idesc_mx, 2, 2), ptx::idesc_sf_ids(idesc_mx, 3, 3), t_sfa,
-                                     t_sfb, sfa_base + so, sfb_base + so, kb > kb0 ? 1u : 0u);
-                ptx::commit_elect(empty_bar(s));   // frees the stage once both halves' MMAs are done
+                if constexpr (kPair) {
+                    ptx::mx_stage2_elect_pair(d, ad_base + static_cast<uint64_t>(s * (C::kABytes >> 4)),
+                                              bd_base + static_cast<uint64_t>(s * (C::kBBytes >> 4)),
+                                              ptx::idesc_sf_ids(idesc_mx, 0, 0), ptx::idesc_sf_ids(idesc_mx, 1, 1),
+                                              ptx::idesc_sf_ids(idesc_mx, 2, 2), ptx::idesc_sf_ids(idesc_mx, 3, 3),
+                                              t_sfa, t_sfb, sfa_base + so, sfb_base + so, kb > kb0 ? 1u : 0u);
+                    ptx::commit_pair_elect(empty_bar(s));   // frees the stage in both CTAs
+                } else {
+                    ptx::mx_stage2_elect(d, ad_base + static_cast<uint64_t>(s * (C::kABytes >> 4)),
+                                         bd_base + static_cast<uint64_t>(s * (C::kBBytes >> 4)),
+                                         ptx::idesc_sf_ids(idesc_mx, 0, 0), ptx::idesc_sf_ids(idesc_mx, 1, 1),
+                                         ptx::idesc_sf_ids(idesc_mx, 2, 2), ptx::idesc_sf_ids(idesc_mx, 3, 3), t_sfa,
+                                         t_sfb, sfa_base + so, sfb_base + so, kb > kb0 ? 1u : 0u);
+                    ptx::commit_elect(empty_bar(s));   // frees the stage once both halves' MMAs are done
+                }
             }
             if (failed) break;
-            ptx::commit_elect(accf_bar(h));        // the tile's accumulator is complete
+            // the tile's accumulator is complete (pair: in both CTAs)
+            if constexpr (kPair) ptx::commit_pair_elect(accf_bar(h));
+            else ptx::commit_elect(accf_bar(h));
         }
-        ptx::commit_elect(drain_bar(h));           // every tcgen05 op lands before teardown
+        // every tcgen05 op lands before teardown
+        if constexpr (kPair) ptx::commit_pair_local_elect(drain_bar(h));
+        else ptx::commit_elect(drain_bar(h));
         if (lane == 0) wait_slow(drain_bar(h), 0, sync, 5);
         __syncwarp();
+    } else if (warp == 1 || warp == 2) {
+        // the pair's peer issues nothing
     } else {
         // ------------------------------------------------------------ epilogue (warps 4-11)
         const int ew = warp - kEpi0;            // 0 .. 7
@@ -445,12 +513,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool failed = false;
             if constexpr (!kSplit) {
                 for (int h = 0; h < 2 && !failed; ++h) {
-                    if (!wait_warp(accf_bar(h), ntile & 1, sync, 6)) {
+                    if (!wait_warp<kPair>(accf_bar(h), ntile & 1, sync, 6)) {
                         failed = true;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const int grow = it.tr * kRowsA + h * kHalf + quad * 32 + lane;
+                    const int grow = it.tr * kTileRows + static_cast<int>(rank) * kRowsA + h * kHalf + quad * 32 + lane;
                     __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
 #pragma unroll
                     for (int c0 = 0; c0 < C::kColsPerWarp; c0 += 16) {
@@ -479,7 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(acce_bar(h));
+                    if constexpr (kPair) {
+                        if (rank == 0u) {
+                            if (lane == 0) ptx::mbar_arrive(acce_bar(h));
+                        } else {
+                            ptx::mbar_arrive_cluster_if(lane == 0 ? 1u : 0u, at_leader(acce_bar(h)));
+                        }
+                    } else {
+                        if (lane == 0) ptx::mbar_arrive(acce_bar(h));
+                    }
                 }
                 if (failed) break;
                 continue;
@@ -675,17 +751,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) ptx::cluster_sync();   // no remote operation targets a CTA that has left
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        if constexpr (kPair) ptx::tmem_dealloc_g<2>(tmem, kTmemCols);
+        else ptx::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-template <int BN, int kBlkN, int kBlkK, bool kSplit>
+template <int BN, int kBlkN, int kBlkK, bool kSplit, bool kPair>
 sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a, int grid, cudaStream_t st) {
-    using C = Cfg<BN, kSplit>;
+    using C = Cfg<BN, kSplit, kPair>;
     constexpr size_t kSmem = C::kSmem;
-    auto kern = dual_gemm_kernel<BN, kBlkN, kBlkK, kSplit>;
+    auto kern = dual_gemm_kernel<BN, kBlkN, kBlkK, kSplit, kPair>;
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
@@ -700,11 +778,15 @@ sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = kPair ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a) != cudaSuccess) return SGQ_ERR_CUDA;
     note_launch();
     return SGQ_OK;
@@ -716,16 +798,16 @@ sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a
 constexpr int kBNWide = 224;
 constexpr int kBNNarrow = 192;
 
-template <int BN, bool kSplit>
+template <int BN, bool kSplit, bool kPair = false>
 sgq_status dispatch_bn(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
                        int grid, cudaStream_t st) {
     if (blk_n == 32)
-        return blk_k == 32 ? run<BN, 32, 32, kSplit>(tmA, tmB, a, grid, st)
-                           : run<BN, 32, 128, kSplit>(tmA, tmB, a, grid, st);
-    return blk_k == 32 ? run<BN, 128, 32, kSplit>(tmA, tmB, a, grid, st)
-                       : run<BN, 128, 128, kSplit>(tmA, tmB, a, grid, st);
+        return blk_k == 32 ? run<BN, 32, 32, kSplit, kPair>(tmA, tmB, a, grid, st)
+                           : run<BN, 32, 128, kSplit, kPair>(tmA, tmB, a, grid, st);
+    return blk_k == 32 ? run<BN, 128, 32, kSplit, kPair>(tmA, tmB, a, grid, st)
+                       : run<BN, 128, 128, kSplit, kPair>(tmA, tmB, a, grid, st);
 }
-// One translation unit per width and kind (gemm_dual_{224,192}{,s}.cu).
+// One translation unit per width and kind (gemm_dual_{224,192}{,s,p}.cu).
 sgq_status dispatch_224(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
                         int grid, cudaStream_t st);
 sgq_status dispatch_192(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
@@ -734,6 +816,10 @@ sgq_status dispatch_224_split(int blk_n, int blk_k, const CUtensorMap& tmA, cons
                               const DualArgs& a, int grid, cudaStream_t st);
 sgq_status dispatch_192_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const DualArgs& a, int grid, cudaStream_t st);
+sgq_status dispatch_224_pair(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const DualArgs& a, int grid, cudaStream_t st);
+sgq_status dispatch_192_pair(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const DualArgs& a, int grid, cudaStream_t st);
 
 }  // namespace dual
 }  // namespace sgq

@@ -307,11 +307,14 @@ struct Chan {
 // that: 4096 x 7168 takes 192 (608 tiles: exactly 4 rounds of 152 SMs, where
 // 224 makes 512 tiles, 3.4 rounds, so 4 of the longer stage; 168.6 vs 174.2
 // us), 8192 x 24576 takes 224 (24 rounds against 27; 280 vs 294 us).
-int dual_width(int64_t M, int64_t N, int sm_count) {
-    const int64_t tr = (M + dual::kRowsA - 1) / dual::kRowsA;
+// pair: tiles of 512 rows over the SM pairs, each CTA holding 256 rows and BN / 2.
+int dual_width(int64_t M, int64_t N, int sm_count, bool pair = false) {
+    const int rows = pair ? 2 * dual::kRowsA : dual::kRowsA;
+    const int units = pair ? sm_count / 2 : sm_count;
+    const int64_t tr = (M + rows - 1) / rows;
     auto cost = [&](int bn) {
         const int64_t tiles = tr * ((N + bn - 1) / bn);
-        return ((tiles + sm_count - 1) / sm_count) * (dual::kRowsA + bn);
+        return ((tiles + units - 1) / units) * (rows + bn);
     };
     return cost(dual::kBNNarrow) < cost(dual::kBNWide) ? dual::kBNNarrow : dual::kBNWide;
 }
@@ -357,9 +360,10 @@ int dual_splits(int64_t tiles, int kst, int sm_count, int bn, ScratchLimit lim) 
 // CTA per SM, with K split over several CTAs where the tiles are fewer than
 // the SMs.
 sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D, int64_t M,
-                       int64_t N, int64_t K, int blk_n, int blk_k, int sm_count, bool allow_split, ScratchLimit lim,
-                       cudaStream_t st) {
-    const int bn = dual_width(M, N, sm_count);
+                       int64_t N, int64_t K, int blk_n, int blk_k, int sm_count, bool allow_split, bool pair,
+                       ScratchLimit lim, cudaStream_t st) {
+    const int bn = dual_width(M, N, sm_count, pair);
+    const int rows = pair ? 2 * dual::kRowsA : dual::kRowsA;   // activation rows per tile
     dual::DualArgs a{};
     a.As = As;
     a.Ws = Ws;
@@ -368,12 +372,12 @@ sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const fl
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.ks = static_cast<int>(K / blk_k);
-    a.tiles_r = static_cast<int>((M + dual::kRowsA - 1) / dual::kRowsA);
+    a.tiles_r = static_cast<int>((M + rows - 1) / rows);
     a.tiles_c = static_cast<int>((N + bn - 1) / bn);
     a.kst = static_cast<int>(K / kBK);
     a.tiles = a.tiles_r * a.tiles_c;
     a.group_r = a.tiles_r < 16 ? a.tiles_r : 16;
-    a.splits = allow_split ? dual_splits(a.tiles, a.kst, sm_count, bn, lim) : 1;
+    a.splits = allow_split && !pair ? dual_splits(a.tiles, a.kst, sm_count, bn, lim) : 1;
     a.kps = (a.kst + a.splits - 1) / a.splits;
     a.items = a.tiles * a.splits;
     a.per = 8 * ((bn / 4 + a.splits - 1) / a.splits);
@@ -387,8 +391,14 @@ sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const fl
         a.counters = ws.counters + (kMaxCounters - kDualCounters);
     }
     CUtensorMap maps[2];
-    if (make_tmap(&maps[0], Aq, M, K, dual::kRowsA) != SGQ_OK || make_tmap(&maps[1], Wq, N, K, bn) != SGQ_OK)
+    if (make_tmap(&maps[0], Aq, M, K, dual::kRowsA) != SGQ_OK ||
+        make_tmap(&maps[1], Wq, N, K, pair ? bn / 2 : bn) != SGQ_OK)
         return SGQ_ERR_CUDA;
+    if (pair) {
+        const int pairs = a.items < sm_count / 2 ? a.items : sm_count / 2;
+        return bn == dual::kBNNarrow ? dual::dispatch_192_pair(blk_n, blk_k, maps[0], maps[1], a, 2 * pairs, st)
+                                     : dual::dispatch_224_pair(blk_n, blk_k, maps[0], maps[1], a, 2 * pairs, st);
+    }
     const int grid = a.items < sm_count ? a.items : sm_count;
     if (a.splits > 1)
         return bn == dual::kBNNarrow ? dual::dispatch_192_split(blk_n, blk_k, maps[0], maps[1], a, grid, st)
@@ -416,11 +426,17 @@ int dual_mode(int64_t M, int64_t N, int64_t K, int blk_k, uint32_t flags, const 
     if (!(flags & SGQ_GEMM_SCALES_POW2) || K % kBK != 0 || M <= 64 ||
         (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0)
         return 0;
-    if (dual_env >= 0) return dual_env == 0 ? 0 : 2;
-    (void)blk_k;
+    // SGQ_DUAL_PAIR=0/1 forces CTA pairs off/on for the wave-sized plans
+    static const int pair_env = env_int("SGQ_DUAL_PAIR", -1);
+    if (dual_env >= 0) return dual_env == 0 ? 0 : (pair_env > 0 ? 3 : 2);
     const int64_t tr = (M + dual::kRowsA - 1) / dual::kRowsA;
     const int64_t dual_tiles = tr * ((N + dual::kBNWide - 1) / dual::kBNWide);
-    if (!p.swap && dual_tiles >= sm_count) return 1;
+    // A wave of tiles: CTA pairs for the [*,128] recipe with long K (4096 x
+    // 7168 x 7168: 161.6 vs 169.2 us; the pair's longer per-stage handshake
+    // loses on short K and on [*,32], whose scale work per stage is larger:
+    // 8192 x 24576 x 1536 333 vs 308 us, 4096 x 4096 x 7168 [*,32] 105 vs 100 us).
+    if (!p.swap && dual_tiles >= sm_count)
+        return pair_env > 0 || (pair_env < 0 && blk_k == 128 && K >= 4096) ? 3 : 1;
     if (M >= 128 && dual_tiles * 5 >= int64_t(sm_count) * 3) return 1;
     if (M < 768) return 0;
     const int bn = dual_width(M, N, sm_count);
@@ -460,7 +476,8 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     // faster than this plan.
     if (int mode = dual_mode(M, N, K, blk_k, flags, p, di.sm_count, lim);
         mode != 0 && !fuse && !chan)
-        return launch_dual(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, di.sm_count, mode == 2 && !noalloc, lim, st);
+        return launch_dual(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, di.sm_count, mode == 2 && !noalloc, mode == 3,
+                           lim, st);
     if (flags & SGQ_GEMM_ISSUE_ALT) p.alt = !p.swap && !p.pair;
     if (flags & SGQ_GEMM_ISSUE_SINGLE) p.alt = false;
     if (chan) {   // plain tiles: no scale boxes, one issuer

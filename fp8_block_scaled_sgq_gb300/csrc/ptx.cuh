@@ -287,6 +287,48 @@ __device__ __forceinline__ void mx_stage2_elect(uint32_t d, uint64_t a, uint64_t
         "l"(a), "l"(b), "r"(i0), "r"(i1), "r"(i2), "r"(i3), "r"(sfa_t), "r"(sfb_t), "r"(acc), "l"(sfa_d), "l"(sfb_d)
         : "memory");
 }
+// mx_stage2_elect for a CTA pair (.cta_group::2, issued by the leader CTA):
+// each CTA's scale words go from its own shared memory to its own TMEM (same
+// addresses), and the M = 256 MMAs read A rows 0-127 and B rows 0 .. N/2-1
+// from the leader's shared memory, the rest from the peer's at the same offsets.
+__device__ __forceinline__ void mx_stage2_elect_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t i0, uint32_t i1,
+                                                     uint32_t i2, uint32_t i3, uint32_t sfa_t, uint32_t sfb_t,
+                                                     uint64_t sfa_d, uint64_t sfb_d, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred e, q, t;\n.reg .b64 a1, a2, a3, b1, b2, b3, s2;\n.reg .b32 t2;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "setp.ne.b32 q, %9, 0;\n"
+        "setp.eq.u32 t, %0, %0;\n"
+        "add.s64 a1, %1, 2;\nadd.s64 a2, %1, 4;\nadd.s64 a3, %1, 6;\n"
+        "add.s64 b1, %2, 2;\nadd.s64 b2, %2, 4;\nadd.s64 b3, %2, 6;\n"
+        "add.s64 s2, %11, 32;\nadd.u32 t2, %8, 4;\n"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%7], %10;\n"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%8], %11;\n"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t2], s2;\n"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%7], [%8], q;\n"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a1, b1, %4, [%7], [%8], t;\n"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a2, b2, %5, [%7], [%8], t;\n"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], a3, b3, %6, [%7], [%8], t;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(i0), "r"(i1), "r"(i2), "r"(i3), "r"(sfa_t), "r"(sfb_t), "r"(acc), "l"(sfa_d), "l"(sfb_d)
+        : "memory");
+}
+// Pair commit from one elected lane: arrives on `bar` (same offset) in both
+// CTAs when the leader's earlier tcgen05 ops are done.
+__device__ __forceinline__ void commit_pair_elect(uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+// Pair commit arriving on this (the leader) CTA's `bar` only.
+__device__ __forceinline__ void commit_pair_local_elect(uint32_t bar) {
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+        : "memory");
+}
 // Commit (arrive on `bar` when this lane's earlier tcgen05 ops are done).
 __device__ __forceinline__ void commit_elect(uint32_t bar) {
     asm volatile(

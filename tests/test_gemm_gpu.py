@@ -421,10 +421,36 @@ def test_dual_split_counts_match_oracle(tmp_path, M, N, K, bn, bk, splits):
     check_gemm(d[torch.from_numpy(r)], dref, bound, f"dual splits={splits} M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("M,N,K,bn,bk", [(4100, 7000, 1280, 128, 32), (4200, 7000, 384, 32, 32),
+                                         (4096, 7168, 512, 128, 128), (2100, 14000, 768, 32, 128)])
+def test_dual_cta_pairs_match_oracle(tmp_path, M, N, K, bn, bk):
+    """The two-accumulator tiles on CTA pairs (512 rows x BN per cluster of
+    two, .cta_group::2 MMAs issued by the leader over both CTAs' halves),
+    forced with SGQ_DUAL_PAIR=1 in a child process on shapes the default plan
+    keeps on single CTAs: ragged M and N (a partial 512-row tile, N not a
+    multiple of the width), short K, both recipes; D against the oracle on
+    every 64-row block, and a second call gives the same bits."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"), SGQ_DUAL_PAIR="1")
+    out = str(tmp_path / "d.npy")
+    subprocess.run([sys.executable, "-c", _DUAL_CHILD, str(M), str(N), str(K), str(bn), str(bk), out], env=env,
+                   check=True, timeout=600, cwd=root)
+    d = torch.from_numpy(np.load(out)).view(torch.bfloat16)
+    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=43), bk, True)
+    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=43), bn, bk, True)
+    r = tile_rows(M, seed=M)
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
+    check_gemm(d[torch.from_numpy(r)], dref, bound, f"dual pairs M={M} N={N} K={K} [{bn},{bk}]")
+
+
 @pytest.mark.parametrize("name", ["prefill_block128", "prefill_block32"])
 def test_scales_pow2_prefill_every_tile(name):
     """The prefill configurations (UE8M0 on both operands) through the
-    power-of-two tiles, one row of every 64-row block over all N columns."""
+    power-of-two tiles (block128: on CTA pairs, the default for [*,128] with
+    long K), one row of every 64-row block over all N columns."""
     c = synth.WORKLOADS[name][0]
     aq, a_s = oracle.quant_token_group(c.x(), c.group, c.ue8m0)
     wq, ws = weights(c.N, c.K, c.blk_n, c.blk_k, c.ue8m0, c.seed)
