@@ -248,6 +248,16 @@ def roofline_frac(flops: float, nbytes: float, us: float):
     return ("fp8" if t_fp8 > t_hbm else "hbm"), max(t_fp8, t_hbm) / (us * 1e-6)
 
 
+# [1,32] GEMMs from this M on, with a wave of 256 x 224 tiles, run on UE8M0
+# scale bytes: the two-accumulator tiles read them directly (other plans would
+# widen them to fp32 first, an extra step).
+E8_MIN_M = 2048
+
+
+def sm_count() -> int:
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
 def gemm_cases(sgq, timer, device, reps, names):
     """The metric's GEMM configurations: the M = 1..8192 sweep (two weight
     shapes, both recipes) and the two prefill shapes; each timed as the GEMM
@@ -263,34 +273,61 @@ def gemm_cases(sgq, timer, device, reps, names):
         del w
         wbytes = N * K + 4 * math.ceil(N / bn) * (K // bk)
         wrot = [(wq0, ws0)] + [(wq0.clone(), ws0.clone()) for _ in range(n_rotations(wbytes) - 1)]
+        # UE8M0 bytes of the weight scales, converted once (the load-time step)
+        werot = None
         for c in cs:
             x = c.x().to(device)
+            # The [1,32] recipe at prefill sizes reads UE8M0 scale bytes: the
+            # quantiser writes them, the GEMM reads them as they are (a quarter
+            # of the fp32 scale bytes per stage).  Elsewhere fp32 scales.
+            e8 = (c.ue8m0 and c.blk_k == 32 and c.M >= E8_MIN_M
+                  and math.ceil(c.M / 256) * math.ceil(c.N / 224) >= sm_count())
+            if e8 and werot is None:
+                werot = [sgq.scales_to_ue8m0(ws) for _, ws in wrot]
             xq = torch.empty((c.M, c.K), dtype=torch.uint8, device=device)
-            xs = torch.empty((c.M, c.K // c.group), dtype=torch.float32, device=device)
+            xs = torch.empty((c.M, c.K // c.group), dtype=torch.uint8 if e8 else torch.float32, device=device)
             d = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
-            sgq.sgq_quant_token_group(x, c.M, c.K, c.group, int(c.ue8m0), xq, xs, timer.stream.cuda_stream)
+            sp0 = timer.stream.cuda_stream
+            if e8:
+                sgq.sgq_quant_token_group_ue8m0(x, c.M, c.K, c.group, xq, xs, sp0)
+            else:
+                sgq.sgq_quant_token_group(x, c.M, c.K, c.group, int(c.ue8m0), xq, xs, sp0)
 
             # the configurations' scales are UE8M0: the caller may promise powers of two
             fl = sgq.SGQ_GEMM_SCALES_POW2 if c.ue8m0 else sgq.SGQ_GEMM_DEFAULT
 
-            def gemm(sp, r, c=c, xq=xq, xs=xs, d=d, fl=fl):
-                sgq.sgq_fp8_block_gemm_ex(xq, xs, wrot[r][0], wrot[r][1], d, c.M, c.N, c.K, c.blk_n, c.blk_k, fl, sp)
+            def gemm(sp, r, c=c, xq=xq, xs=xs, d=d, fl=fl, e8=e8):
+                if e8:
+                    sgq.sgq_fp8_block_gemm_ue8m0(xq, xs, wrot[r][0], werot[r], d, c.M, c.N, c.K, c.blk_n, c.blk_k,
+                                                 0, sp)
+                else:
+                    sgq.sgq_fp8_block_gemm_ex(xq, xs, wrot[r][0], wrot[r][1], d, c.M, c.N, c.K, c.blk_n, c.blk_k,
+                                              fl, sp)
 
-            def pair(sp, r, c=c, x=x, xq=xq, xs=xs, d=d):
-                sgq.sgq_quant_token_group(x, c.M, c.K, c.group, int(c.ue8m0), xq, xs, sp)
+            def pair(sp, r, c=c, x=x, xq=xq, xs=xs, d=d, e8=e8):
+                if e8:
+                    sgq.sgq_quant_token_group_ue8m0(x, c.M, c.K, c.group, xq, xs, sp)
+                else:
+                    sgq.sgq_quant_token_group(x, c.M, c.K, c.group, int(c.ue8m0), xq, xs, sp)
                 gemm(sp, r)
+            sb = 1 if e8 else 4
+            with torch.cuda.stream(timer.stream):
+                gemm(sp0, 0)   # outside the capture: any first-use set-up happens here
+            timer.stream.synchronize()
             for path, fn in (("gemm", gemm), ("pair", pair)):
                 calls = [lambda sp, r=r, fn=fn: fn(sp, r) for r in range(len(wrot))]
                 ms = timer.time(calls, reps)
                 us = ms * 1e3
-                nbytes = c.gemm_bytes() + (c.quant_bytes() if path == "pair" else 0.0)
+                nbytes = c.gemm_bytes(sb) + (c.quant_bytes(sb) if path == "pair" else 0.0)
                 bound, frac = roofline_frac(c.flops(), nbytes, us)
                 rows.append({"case": c.name, "path": path, "M": c.M, "N": c.N, "K": c.K,
-                             "recipe": [1, c.blk_n, c.blk_k], "flags": "scales_pow2" if fl else "default",
+                             "recipe": [1, c.blk_n, c.blk_k],
+                             "flags": ("scales_pow2" if fl else "default") + (" ue8m0_bytes" if e8 else ""),
                              "us": round(us, 3),
                              "tflops": round(c.flops() / us / 1e6, 2), "gbs": round(nbytes / us / 1e3, 1),
                              "bound": bound, "frac": round(frac, 4)})
             del x, xq, xs, d
+        del werot
         del wrot, wq0, ws0
         torch.cuda.empty_cache()
     return rows
@@ -318,7 +355,16 @@ def quant_cases(sgq, timer, device, reps):
                          "group": g, "us": round(us, 3), "gbs": round(nbytes / us / 1e3, 1), "bound": "hbm",
                          "frac": round(nbytes / us / 1e3 / peaks()["hbm_gbs"], 4)})
             del xq, xs
-        del xr, x0
+        # the byte-output quantiser (UE8M0 scale bytes), group 32
+        xq = torch.empty((M, K), dtype=torch.uint8, device=device)
+        xe = torch.empty((M, K // 32), dtype=torch.uint8, device=device)
+        calls = [lambda sp, x=x: sgq.sgq_quant_token_group_ue8m0(x, M, K, 32, xq, xe, sp) for x in xr]
+        us = timer.time(calls, reps) * 1e3
+        nbytes = 2 * M * K + M * K + M * K / 32
+        rows.append({"case": f"quant_token_group_ue8m0_M{M}_K{K}_g32", "path": "quant", "M": M, "K": K,
+                     "group": 32, "us": round(us, 3), "gbs": round(nbytes / us / 1e3, 1), "bound": "hbm",
+                     "frac": round(nbytes / us / 1e3 / peaks()["hbm_gbs"], 4)})
+        del xq, xe, xr, x0
         torch.cuda.empty_cache()
     return rows
 

@@ -13,7 +13,7 @@ from .binding import (  # noqa: F401
     load_library, sgq_device_status,
     sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_fp8_block_linear, sgq_fp8_scaled_mm,
     sgq_quant_per_tensor, sgq_quant_per_token, sgq_quant_token_group_v2, sgq_launch_count, sgq_quant_token_group,
-    sgq_allocated_bytes,
+    sgq_allocated_bytes, sgq_fp8_block_gemm_ue8m0, sgq_quant_token_group_ue8m0, sgq_scales_to_ue8m0,
     sgq_gemm_plan,
     sgq_quant_weight_block, sgq_version, status_string)
 
@@ -46,6 +46,36 @@ def fp8_block_gemm(aq, a_s, wq, ws, blk_n: int, blk_k: int, out=None, flags: int
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
     sgq_fp8_block_gemm_ex(aq, a_s, wq, ws, out, M, N, K, blk_n, blk_k, flags, stream)
+    return out
+
+
+def quant_token_group_ue8m0(x, group: int, stream=None):
+    """bf16 [M, K] CUDA tensor -> (uint8 E4M3 codes [M, K], UE8M0 scale bytes [M, K/group])."""
+    import torch
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    xe = torch.empty((M, K // group), dtype=torch.uint8, device=x.device)
+    sgq_quant_token_group_ue8m0(x, M, K, group, xq, xe, stream)
+    return xq, xe
+
+
+def scales_to_ue8m0(s, stream=None):
+    """fp32 power-of-two scales (CUDA tensor) -> UE8M0 bytes of the same shape."""
+    import torch
+    s = s.contiguous()
+    e = torch.empty(s.shape, dtype=torch.uint8, device=s.device)
+    sgq_scales_to_ue8m0(s, s.numel(), e, stream)
+    return e
+
+
+def fp8_block_gemm_ue8m0(aq, ae, wq, we, blk_n: int, blk_k: int, out=None, flags: int = 0, stream=None):
+    """D = (Aq*2^(Ae-127))(Wq*2^(We-127))^T as a bf16 [M, N] CUDA tensor."""
+    import torch
+    M, K = aq.shape
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    sgq_fp8_block_gemm_ue8m0(aq, ae, wq, we, out, M, N, K, blk_n, blk_k, flags, stream)
     return out
 
 

@@ -37,6 +37,9 @@ EXPORTS = (
     "sgq_fp8_block_gemm",
     "sgq_fp8_block_gemm_ex",
     "sgq_fp8_block_gemm_noalloc",
+    "sgq_fp8_block_gemm_ue8m0",
+    "sgq_quant_token_group_ue8m0",
+    "sgq_scales_to_ue8m0",
     "sgq_fp8_block_linear",
     "sgq_quant_token_group_v2",
     "sgq_quant_per_token",
@@ -77,6 +80,9 @@ def load_library(path: str = LIB_PATH):
         lib.sgq_fp8_block_gemm.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, P]
         lib.sgq_fp8_block_gemm_ex.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, u32, P]
         lib.sgq_fp8_block_gemm_noalloc.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, P]
+        lib.sgq_fp8_block_gemm_ue8m0.argtypes = [P, P, P, P, P, i64, i64, i64, ci, ci, u32, P]
+        lib.sgq_quant_token_group_ue8m0.argtypes = [P, i64, i64, ci, P, P, P]
+        lib.sgq_scales_to_ue8m0.argtypes = [P, i64, P, P]
         lib.sgq_fp8_block_linear.argtypes = [P, ci, P, P, P, i64, i64, i64, ci, ci, P, P, P]
         lib.sgq_quant_token_group_v2.argtypes = [P, i64, i64, i64, ci, ci, ci, P, P, P, P]
         lib.sgq_quant_per_token.argtypes = [P, i64, i64, P, P, P]
@@ -84,6 +90,7 @@ def load_library(path: str = LIB_PATH):
         lib.sgq_fp8_scaled_mm.argtypes = [P, P, i64, P, P, i64, P, P, i64, i64, i64, P]
         for f in ("sgq_quant_token_group", "sgq_quant_weight_block", "sgq_fp8_block_gemm",
                   "sgq_fp8_block_gemm_ex", "sgq_fp8_block_gemm_noalloc", "sgq_fp8_block_linear",
+                  "sgq_fp8_block_gemm_ue8m0", "sgq_quant_token_group_ue8m0", "sgq_scales_to_ue8m0",
                   "sgq_quant_per_token", "sgq_quant_per_tensor", "sgq_fp8_scaled_mm", "sgq_quant_token_group_v2"):
             getattr(lib, f).restype = ci
         lib.sgq_status_string.argtypes = [ci]
@@ -157,6 +164,22 @@ def sgq_fp8_block_gemm_noalloc(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, stream=
     _check(load_library().sgq_fp8_block_gemm_noalloc(_ptr(Aq), _ptr(As), _ptr(Wq), _ptr(Ws), _ptr(D), M, N,
                                                      K, blk_n, blk_k, _stream(stream)),
            "sgq_fp8_block_gemm_noalloc")
+
+
+def sgq_fp8_block_gemm_ue8m0(Aq, Ae, Wq, We, D, M, N, K, blk_n, blk_k, flags=0, stream=None):
+    """The GEMM with UE8M0 scale bytes (uint8 tensors) in place of fp32 scales."""
+    _check(load_library().sgq_fp8_block_gemm_ue8m0(_ptr(Aq), _ptr(Ae), _ptr(Wq), _ptr(We), _ptr(D), M, N, K,
+                                                   blk_n, blk_k, flags, _stream(stream)),
+           "sgq_fp8_block_gemm_ue8m0")
+
+
+def sgq_quant_token_group_ue8m0(x, M, K, group, xq, xe, stream=None):
+    _check(load_library().sgq_quant_token_group_ue8m0(_ptr(x), M, K, group, _ptr(xq), _ptr(xe), _stream(stream)),
+           "sgq_quant_token_group_ue8m0")
+
+
+def sgq_scales_to_ue8m0(s, n, e, stream=None):
+    _check(load_library().sgq_scales_to_ue8m0(_ptr(s), n, _ptr(e), _stream(stream)), "sgq_scales_to_ue8m0")
 
 
 def sgq_fp8_block_linear(x, ue8m0, Wq, Ws, D, M, N, K, blk_n, blk_k, xq=None, xs=None, stream=None):

@@ -60,6 +60,23 @@ sgq_status sgq_quant_token_group(const void* x, int64_t M, int64_t K, int group,
                                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+sgq_status sgq_quant_token_group_ue8m0(const void* x, int64_t M, int64_t K, int group, void* xq, uint8_t* xe,
+                                       sgq_stream_t stream) {
+    if (M < 0 || K <= 0 || (group != 32 && group != 128) || K % group != 0) return SGQ_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) / 1 || M * K > (int64_t(1) << 40)) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!x || !xq || !xe) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned16(xe)) return SGQ_ERR_MISALIGNED;
+    return sgq::launch_quant_token_group_e8(x, M, K, group, xq, xe, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgq_status sgq_scales_to_ue8m0(const float* s, int64_t n, uint8_t* e, sgq_stream_t stream) {
+    if (n < 0 || n > (int64_t(1) << 40)) return SGQ_ERR_INVALID_ARG;
+    if (n == 0) return SGQ_OK;
+    if (!s || !e) return SGQ_ERR_INVALID_ARG;
+    return sgq::launch_scales_to_ue8m0(s, n, e, reinterpret_cast<cudaStream_t>(stream));
+}
+
 sgq_status sgq_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n, int blk_k, int ue8m0,
                                   void* wq, float* ws, sgq_stream_t stream) {
     if (N < 0 || K <= 0 || (blk_n != 32 && blk_n != 128) || (blk_k != 32 && blk_k != 128) ||
@@ -96,6 +113,25 @@ sgq_status sgq_fp8_block_gemm_ex(const void* Aq, const float* As, const void* Wq
 sgq_status sgq_fp8_block_gemm(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D,
                               int64_t M, int64_t N, int64_t K, int blk_n, int blk_k, sgq_stream_t stream) {
     return sgq_fp8_block_gemm_ex(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, SGQ_GEMM_DEFAULT, stream);
+}
+
+sgq_status sgq_fp8_block_gemm_ue8m0(const void* Aq, const uint8_t* Ae, const void* Wq, const uint8_t* We, void* D,
+                                    int64_t M, int64_t N, int64_t K, int blk_n, int blk_k, uint32_t flags,
+                                    sgq_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || (blk_n != 32 && blk_n != 128) || (blk_k != 32 && blk_k != 128) ||
+        K % blk_k != 0 || N % 8 != 0 ||
+        (flags & ~uint32_t(SGQ_GEMM_FORCE_PROMOTE | SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE |
+                           SGQ_GEMM_SCALES_POW2)) != 0 ||
+        (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) == (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE))
+        return SGQ_ERR_INVALID_ARG;
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!Aq || !Ae || !Wq || !We || !D) return SGQ_ERR_INVALID_ARG;
+    if (!aligned16(Aq) || !aligned16(Ae) || !aligned16(Wq) || !aligned16(We) || !aligned16(D))
+        return SGQ_ERR_MISALIGNED;
+    return sgq::launch_fp8_block_gemm_ue8m0(Aq, Ae, Wq, We, D, M, N, K, blk_n, blk_k, flags,
+                                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq, const float* Ws,
@@ -207,6 +243,6 @@ sgq_status sgq_gemm_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_coun
     return sgq::gemm_plan_query(M, N, K, blk_k, sm_count, out);
 }
 
-int sgq_version(void) { return 102; }
+int sgq_version(void) { return 103; }
 
 }  // extern "C"

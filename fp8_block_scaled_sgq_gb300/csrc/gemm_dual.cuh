@@ -32,6 +32,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "sgq_internal.h"
@@ -55,6 +56,8 @@ constexpr uint32_t kStatusBadScale = 2u;
 struct DualArgs {
     const float* As;        // fp32 [M, K / blk_k]
     const float* Ws;        // fp32 [ceil(N / blk_n), K / blk_k]
+    const uint8_t* Ae;      // kE8: UE8M0 bytes [M, K / blk_k] (in place of As)
+    const uint8_t* We;      // kE8: UE8M0 bytes [ceil(N / blk_n), K / blk_k] (in place of Ws)
     __nv_bfloat16* D;       // bf16 [M, N]
     uint32_t* status;       // device status word
     float* partial;         // splits > 1: one fp32 partial tile per item (splits * per * 128 floats)
@@ -237,7 +240,9 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n
 // kSplit: K split over several CTAs per tile (splits > 1), with the partial
 // exchange in the epilogue; a separate instantiation, so that the plain
 // kernel's registers are allocated without it.
-template <int BN, int kBlkN, int kBlkK, bool kSplit, bool kPair>
+// kE8: the scales arrive as UE8M0 bytes (a 128-wide stage's four bytes of a
+// row are its scale word as they are), not as fp32 values to convert.
+template <int BN, int kBlkN, int kBlkK, bool kSplit, bool kPair, bool kE8>
 __global__ void __launch_bounds__(kThreads, 1)
     dual_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const DualArgs a) {
@@ -362,8 +367,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::grid_dependency_wait();   // As may be the preceding kernel's output
         // Raw scales of the next two stages are in flight while a stage is
         // converted (registers p0 for stage n + 1, p1 for stage n + 2).
-        struct Raw {
+        struct RawF {
             float4 a[4], b[4];
+        };
+        struct RawE {
+            uint32_t a[4], b[4];
+        };
+        using Raw = std::conditional_t<kE8, RawE, RawF>;
+        // UE8M0 word of one row's stage from its bytes (one per scale column)
+        auto load_word = [&](const uint8_t* p) -> uint32_t {
+            if constexpr (kSps == 4) return __ldg(reinterpret_cast<const uint32_t*>(p));
+            else return static_cast<uint32_t>(__ldg(p)) * 0x01010101u;
         };
         auto load = [&](Raw& v, int i, int kb) {
             if (i >= a.items) return;
@@ -372,13 +386,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int row = tr * kTileRows + static_cast<int>(rank) * kRowsA + h * kHalf + lane + 32 * j;
-                v.a[j] = row < a.M ? load_scales<kSps>(a.As + static_cast<int64_t>(row) * a.ks + kb * kSps)
-                                   : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
                 const int i = lane + 32 * j;
                 const int n = tc * BN + h * kBRowsPerWarp + i;
-                v.b[j] = (i < kBRowsPerWarp && n < a.N)
-                             ? load_scales<kSps>(a.Ws + static_cast<int64_t>(n / kBlkN) * a.ks + kb * kSps)
-                             : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                if constexpr (kE8) {
+                    v.a[j] = row < a.M ? load_word(a.Ae + static_cast<int64_t>(row) * a.ks + kb * kSps) : 0x7F7F7F7Fu;
+                    v.b[j] = (i < kBRowsPerWarp && n < a.N)
+                                 ? load_word(a.We + static_cast<int64_t>(n / kBlkN) * a.ks + kb * kSps)
+                                 : 0x7F7F7F7Fu;
+                } else {
+                    v.a[j] = row < a.M ? load_scales<kSps>(a.As + static_cast<int64_t>(row) * a.ks + kb * kSps)
+                                       : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                    v.b[j] = (i < kBRowsPerWarp && n < a.N)
+                                 ? load_scales<kSps>(a.Ws + static_cast<int64_t>(n / kBlkN) * a.ks + kb * kSps)
+                                 : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                }
+            }
+        };
+        // scale word of a loaded row (UE8M0 bytes: as loaded; 255 = NaN is refused)
+        auto word_of = [&](const auto& r, uint32_t& bad) -> uint32_t {
+            if constexpr (kE8) {
+                bad |= zero_byte(~r);
+                return r;
+            } else {
+                return sf_word<kSps>(r, bad);
             }
         };
         auto advance = [&](int& i, int& kb) {
@@ -405,14 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t bad = 0;
             uint32_t w4[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) w4[j] = sf_word<kSps>(cur.a[j], bad);
+            for (int j = 0; j < 4; ++j) w4[j] = word_of(cur.a[j], bad);
             *reinterpret_cast<uint4*>(&sl.sfa[h][lane * 4]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int i = lane + 32 * j;
                 if (i < kBRowsPerWarp) {
                     const int row = h * kBRowsPerWarp + i;   // weight row inside the tile
-                    sl.sfb[(row >> 7) * 128 + (row & 31) * 4 + ((row & 127) >> 5)] = sf_word<kSps>(cur.b[j], bad);
+                    sl.sfb[(row >> 7) * 128 + (row & 31) * 4 + ((row & 127) >> 5)] = word_of(cur.b[j], bad);
                 }
             }
             bad_all |= bad;
@@ -759,11 +789,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, int kBlkN, int kBlkK, bool kSplit, bool kPair>
+template <int BN, int kBlkN, int kBlkK, bool kSplit, bool kPair, bool kE8>
 sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a, int grid, cudaStream_t st) {
     using C = Cfg<BN, kSplit, kPair>;
     constexpr size_t kSmem = C::kSmem;
-    auto kern = dual_gemm_kernel<BN, kBlkN, kBlkK, kSplit, kPair>;
+    auto kern = dual_gemm_kernel<BN, kBlkN, kBlkK, kSplit, kPair, kE8>;
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
@@ -798,28 +828,45 @@ sgq_status run(const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a
 constexpr int kBNWide = 224;
 constexpr int kBNNarrow = 192;
 
-template <int BN, bool kSplit, bool kPair = false>
+template <int BN, bool kSplit, bool kPair, bool kE8>
 sgq_status dispatch_bn(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
                        int grid, cudaStream_t st) {
     if (blk_n == 32)
-        return blk_k == 32 ? run<BN, 32, 32, kSplit, kPair>(tmA, tmB, a, grid, st)
-                           : run<BN, 32, 128, kSplit, kPair>(tmA, tmB, a, grid, st);
-    return blk_k == 32 ? run<BN, 128, 32, kSplit, kPair>(tmA, tmB, a, grid, st)
-                       : run<BN, 128, 128, kSplit, kPair>(tmA, tmB, a, grid, st);
+        return blk_k == 32 ? run<BN, 32, 32, kSplit, kPair, kE8>(tmA, tmB, a, grid, st)
+                           : run<BN, 32, 128, kSplit, kPair, kE8>(tmA, tmB, a, grid, st);
+    return blk_k == 32 ? run<BN, 128, 32, kSplit, kPair, kE8>(tmA, tmB, a, grid, st)
+                       : run<BN, 128, 128, kSplit, kPair, kE8>(tmA, tmB, a, grid, st);
 }
-// One translation unit per width and kind (gemm_dual_{224,192}{,s,p}.cu).
-sgq_status dispatch_224(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
-                        int grid, cudaStream_t st);
-sgq_status dispatch_192(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
-                        int grid, cudaStream_t st);
-sgq_status dispatch_224_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const DualArgs& a, int grid, cudaStream_t st);
-sgq_status dispatch_192_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const DualArgs& a, int grid, cudaStream_t st);
-sgq_status dispatch_224_pair(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const DualArgs& a, int grid, cudaStream_t st);
-sgq_status dispatch_192_pair(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const DualArgs& a, int grid, cudaStream_t st);
+// Kinds of launch: one CTA per tile, K split over CTAs, CTA pairs.
+enum Kind : int { kPlain = 0, kSplitK = 1, kPairs = 2 };
+// One translation unit per width, kind and scale format
+// (gemm_dual_{224,192}{,s,p}{,e}.cu); `dispatch` picks among them.
+#define SGQ_DUAL_DISPATCH_DECL(NAME)                                                                            \
+    sgq_status NAME(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a, \
+                    int grid, cudaStream_t st);
+SGQ_DUAL_DISPATCH_DECL(dispatch_224)
+SGQ_DUAL_DISPATCH_DECL(dispatch_192)
+SGQ_DUAL_DISPATCH_DECL(dispatch_224_split)
+SGQ_DUAL_DISPATCH_DECL(dispatch_192_split)
+SGQ_DUAL_DISPATCH_DECL(dispatch_224_pair)
+SGQ_DUAL_DISPATCH_DECL(dispatch_192_pair)
+SGQ_DUAL_DISPATCH_DECL(dispatch_224_e8)
+SGQ_DUAL_DISPATCH_DECL(dispatch_192_e8)
+SGQ_DUAL_DISPATCH_DECL(dispatch_224_split_e8)
+SGQ_DUAL_DISPATCH_DECL(dispatch_192_split_e8)
+SGQ_DUAL_DISPATCH_DECL(dispatch_224_pair_e8)
+SGQ_DUAL_DISPATCH_DECL(dispatch_192_pair_e8)
+#undef SGQ_DUAL_DISPATCH_DECL
+inline sgq_status dispatch(int bn, Kind kind, bool e8, int blk_n, int blk_k, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, const DualArgs& a, int grid, cudaStream_t st) {
+    using Fn = sgq_status (*)(int, int, const CUtensorMap&, const CUtensorMap&, const DualArgs&, int, cudaStream_t);
+    static constexpr Fn table[2][3][2] = {
+        {{dispatch_224, dispatch_224_e8}, {dispatch_224_split, dispatch_224_split_e8},
+         {dispatch_224_pair, dispatch_224_pair_e8}},
+        {{dispatch_192, dispatch_192_e8}, {dispatch_192_split, dispatch_192_split_e8},
+         {dispatch_192_pair, dispatch_192_pair_e8}}};
+    return table[bn == 224 ? 0 : 1][kind][e8 ? 1 : 0](blk_n, blk_k, tmA, tmB, a, grid, st);
+}
 
 }  // namespace dual
 }  // namespace sgq

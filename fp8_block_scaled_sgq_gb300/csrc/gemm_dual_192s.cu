@@ -1,13 +1,13 @@
 // Instantiates the two-accumulator prefill GEMM (power-of-two scales) with
-// tiles of 192 weight rows and K split over several CTAs per tile, for the
-// four weight-block recipes.
+// tiles of 192 weight rows, K split over several CTAs per tile, fp32 scales, for the four weight-block
+// recipes.
 #include "gemm_dual.cuh"
 
 namespace sgq {
 namespace dual {
-sgq_status dispatch_192_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const DualArgs& a, int grid, cudaStream_t st) {
-    return dispatch_bn<192, true>(blk_n, blk_k, tmA, tmB, a, grid, st);
+sgq_status dispatch_192_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
+                  int grid, cudaStream_t st) {
+    return dispatch_bn<192, true, false, false>(blk_n, blk_k, tmA, tmB, a, grid, st);
 }
 }  // namespace dual
 }  // namespace sgq

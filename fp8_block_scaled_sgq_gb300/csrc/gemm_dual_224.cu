@@ -1,12 +1,13 @@
 // Instantiates the two-accumulator prefill GEMM (power-of-two scales) with
-// tiles of 224 weight rows, for the four weight-block recipes.
+// tiles of 224 weight rows, one CTA per tile, fp32 scales, for the four weight-block
+// recipes.
 #include "gemm_dual.cuh"
 
 namespace sgq {
 namespace dual {
 sgq_status dispatch_224(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
-                        int grid, cudaStream_t st) {
-    return dispatch_bn<224, false>(blk_n, blk_k, tmA, tmB, a, grid, st);
+                  int grid, cudaStream_t st) {
+    return dispatch_bn<224, false, false, false>(blk_n, blk_k, tmA, tmB, a, grid, st);
 }
 }  // namespace dual
 }  // namespace sgq

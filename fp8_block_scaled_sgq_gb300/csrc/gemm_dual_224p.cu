@@ -1,13 +1,13 @@
-// Instantiates the two-accumulator prefill GEMM (power-of-two scales) for
-// CTA pairs: tiles of 512 activation rows x 224 weight rows over a cluster of
-// two, for the four weight-block recipes.
+// Instantiates the two-accumulator prefill GEMM (power-of-two scales) with
+// tiles of 224 weight rows, CTA pairs (512-row tiles over a cluster of two), fp32 scales, for the four weight-block
+// recipes.
 #include "gemm_dual.cuh"
 
 namespace sgq {
 namespace dual {
-sgq_status dispatch_224_pair(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const DualArgs& a, int grid, cudaStream_t st) {
-    return dispatch_bn<224, false, true>(blk_n, blk_k, tmA, tmB, a, grid, st);
+sgq_status dispatch_224_pair(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
+                  int grid, cudaStream_t st) {
+    return dispatch_bn<224, false, true, false>(blk_n, blk_k, tmA, tmB, a, grid, st);
 }
 }  // namespace dual
 }  // namespace sgq

@@ -1,13 +1,13 @@
 // Instantiates the two-accumulator prefill GEMM (power-of-two scales) with
-// tiles of 224 weight rows and K split over several CTAs per tile, for the
-// four weight-block recipes.
+// tiles of 224 weight rows, K split over several CTAs per tile, fp32 scales, for the four weight-block
+// recipes.
 #include "gemm_dual.cuh"
 
 namespace sgq {
 namespace dual {
-sgq_status dispatch_224_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const DualArgs& a, int grid, cudaStream_t st) {
-    return dispatch_bn<224, true>(blk_n, blk_k, tmA, tmB, a, grid, st);
+sgq_status dispatch_224_split(int blk_n, int blk_k, const CUtensorMap& tmA, const CUtensorMap& tmB, const DualArgs& a,
+                  int grid, cudaStream_t st) {
+    return dispatch_bn<224, true, false, false>(blk_n, blk_k, tmA, tmB, a, grid, st);
 }
 }  // namespace dual
 }  // namespace sgq

@@ -359,14 +359,18 @@ int dual_splits(int64_t tiles, int kst, int sm_count, int bn, ScratchLimit lim) 
 // 256 activation rows x BN weight rows over a persistent grid of at most one
 // CTA per SM, with K split over several CTAs where the tiles are fewer than
 // the SMs.
+// Ae/We: UE8M0 scale bytes in place of As/Ws (both given or both null).
 sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D, int64_t M,
                        int64_t N, int64_t K, int blk_n, int blk_k, int sm_count, bool allow_split, bool pair,
-                       ScratchLimit lim, cudaStream_t st) {
+                       ScratchLimit lim, cudaStream_t st, const uint8_t* Ae = nullptr, const uint8_t* We = nullptr) {
     const int bn = dual_width(M, N, sm_count, pair);
     const int rows = pair ? 2 * dual::kRowsA : dual::kRowsA;   // activation rows per tile
     dual::DualArgs a{};
     a.As = As;
     a.Ws = Ws;
+    a.Ae = Ae;
+    a.We = We;
+    const bool e8 = Ae != nullptr;
     a.D = static_cast<__nv_bfloat16*>(D);
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
@@ -396,15 +400,11 @@ sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const fl
         return SGQ_ERR_CUDA;
     if (pair) {
         const int pairs = a.items < sm_count / 2 ? a.items : sm_count / 2;
-        return bn == dual::kBNNarrow ? dual::dispatch_192_pair(blk_n, blk_k, maps[0], maps[1], a, 2 * pairs, st)
-                                     : dual::dispatch_224_pair(blk_n, blk_k, maps[0], maps[1], a, 2 * pairs, st);
+        return dual::dispatch(bn, dual::kPairs, e8, blk_n, blk_k, maps[0], maps[1], a, 2 * pairs, st);
     }
     const int grid = a.items < sm_count ? a.items : sm_count;
-    if (a.splits > 1)
-        return bn == dual::kBNNarrow ? dual::dispatch_192_split(blk_n, blk_k, maps[0], maps[1], a, grid, st)
-                                     : dual::dispatch_224_split(blk_n, blk_k, maps[0], maps[1], a, grid, st);
-    return bn == dual::kBNNarrow ? dual::dispatch_192(blk_n, blk_k, maps[0], maps[1], a, grid, st)
-                                 : dual::dispatch_224(blk_n, blk_k, maps[0], maps[1], a, grid, st);
+    return dual::dispatch(bn, a.splits > 1 ? dual::kSplitK : dual::kPlain, e8, blk_n, blk_k, maps[0], maps[1], a,
+                          grid, st);
 }
 
 // Whether a GEMM with the power-of-two promise runs on the two-accumulator
@@ -421,7 +421,7 @@ sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const fl
 //   x (0.5 us per K stage + 3 us) (1024 x 1536 x 7168: 25.3 vs 36.7 us; at
 //   2048 x 1536 x 7168 and at M <= 512 the split plans measured no faster).
 int dual_mode(int64_t M, int64_t N, int64_t K, int blk_k, uint32_t flags, const Plan& p, int sm_count,
-              ScratchLimit lim) {
+              ScratchLimit lim, bool e8 = false) {
     static const int dual_env = env_int("SGQ_DUAL", -1);
     if (!(flags & SGQ_GEMM_SCALES_POW2) || K % kBK != 0 || M <= 64 ||
         (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0)
@@ -431,12 +431,16 @@ int dual_mode(int64_t M, int64_t N, int64_t K, int blk_k, uint32_t flags, const 
     if (dual_env >= 0) return dual_env == 0 ? 0 : (pair_env > 0 ? 3 : 2);
     const int64_t tr = (M + dual::kRowsA - 1) / dual::kRowsA;
     const int64_t dual_tiles = tr * ((N + dual::kBNWide - 1) / dual::kBNWide);
-    // A wave of tiles: CTA pairs for the [*,128] recipe with long K (4096 x
-    // 7168 x 7168: 161.6 vs 169.2 us; the pair's longer per-stage handshake
-    // loses on short K and on [*,32], whose scale work per stage is larger:
-    // 8192 x 24576 x 1536 333 vs 308 us, 4096 x 4096 x 7168 [*,32] 105 vs 100 us).
-    if (!p.swap && dual_tiles >= sm_count)
-        return pair_env > 0 || (pair_env < 0 && blk_k == 128 && K >= 4096) ? 3 : 1;
+    // A wave of tiles: CTA pairs with long K where a stage's scale work is
+    // light -- fp32 scales with the [*,128] recipe (4096 x 7168 x 7168: 161.6
+    // vs 169.2 us), UE8M0 bytes with [*,32] (4096 x 4096 x 7168: 85.2 vs 89.5
+    // us).  The pair's longer per-stage handshake loses on short K (8192 x
+    // 24576 x 1536: 333 vs 308 us), with fp32 [*,32] scales (4096 x 4096 x
+    // 7168: 105 vs 100 us) and with UE8M0 [*,128] bytes (218 vs 166 us).
+    if (!p.swap && dual_tiles >= sm_count) {
+        const bool pair_auto = K >= 4096 && blk_k == (e8 ? 32 : 128);
+        return pair_env > 0 || (pair_env < 0 && pair_auto) ? 3 : 1;
+    }
     if (M >= 128 && dual_tiles * 5 >= int64_t(sm_count) * 3) return 1;
     if (M < 768) return 0;
     const int bn = dual_width(M, N, sm_count);
@@ -590,6 +594,71 @@ sgq_status launch(const void* Aq, const float* As, const void* Wq, const float* 
     return dispatch_128_128(v, maps, a, fz, p.grid, st);
 }
 
+// Widened fp32 copies of UE8M0 scale bytes, for the plans that read fp32
+// scales (one buffer per device, grown on demand outside stream capture).
+struct WideScales {
+    float* p = nullptr;
+    size_t bytes = 0;
+};
+WideScales g_wide[64];
+std::mutex g_wide_mu;
+
+sgq_status wide_scales(size_t bytes, cudaStream_t st, float** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_wide_mu);
+    WideScales& w = g_wide[dev];
+    if (w.bytes < bytes) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return SGQ_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return SGQ_ERR_UNSUPPORTED;
+        size_t cap = size_t(1) << 20;
+        while (cap < bytes) cap <<= 1;
+        if (w.p) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return SGQ_ERR_CUDA;   // no launch still reads it
+            cudaFree(w.p);
+            w.p = nullptr;
+            w.bytes = 0;
+        }
+        void* p = nullptr;
+        if (cudaMalloc(&p, cap) != cudaSuccess) return SGQ_ERR_CUDA;
+        w.p = static_cast<float*>(p);
+        w.bytes = cap;
+    }
+    *out = w.p;
+    return SGQ_OK;
+}
+
+// UE8M0 scale bytes: the two-accumulator tiles read them as they are where
+// their rules take the shape; other plans get fp32 copies (2^(e - 127)) in a
+// library buffer first, then run as sgq_fp8_block_gemm_ex with the
+// power-of-two promise.
+sgq_status launch_ue8m0(const void* Aq, const uint8_t* Ae, const void* Wq, const uint8_t* We,
+                                       void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                       uint32_t flags, cudaStream_t st) {
+    if (M == 0) return SGQ_OK;
+    if (get_encoder() != SGQ_OK) return SGQ_ERR_CUDA;
+    DeviceInfo di;
+    sgq_status rc = device_info(&di);
+    if (rc != SGQ_OK) return rc;
+    if (di.cc_major != 10 || di.cc_minor != 3) return SGQ_ERR_UNSUPPORTED;
+    flags |= SGQ_GEMM_SCALES_POW2;
+    const Plan p = make_plan(M, N, K, blk_k, di.sm_count, (flags & (SGQ_GEMM_ISSUE_ALT | SGQ_GEMM_ISSUE_SINGLE)) != 0);
+    const int mode = dual_mode(M, N, K, blk_k, flags, p, di.sm_count, kWsLimit, true);
+    if (mode != 0 && (flags & SGQ_GEMM_FORCE_PROMOTE) == 0)
+        return launch_dual(Aq, nullptr, Wq, nullptr, D, M, N, K, blk_n, blk_k, di.sm_count, mode == 2, mode == 3,
+                           kWsLimit, st, Ae, We);
+    const int64_t ks = K / blk_k, nb = (N + blk_n - 1) / blk_n;
+    const size_t na = size_t(M) * size_t(ks), nw = size_t(nb) * size_t(ks);
+    float* wide = nullptr;
+    rc = wide_scales((na + nw) * sizeof(float), st, &wide);
+    if (rc != SGQ_OK) return rc;
+    rc = launch_ue8m0_to_scales(Ae, int64_t(na), wide, st);
+    if (rc == SGQ_OK) rc = launch_ue8m0_to_scales(We, int64_t(nw), wide + na, st);
+    if (rc != SGQ_OK) return rc;
+    return launch(Aq, wide, Wq, wide + na, D, M, N, K, blk_n, blk_k, flags, false, nullptr, st);
+}
+
 }  // namespace
 }  // namespace gemm
 
@@ -597,6 +666,12 @@ sgq_status launch_fp8_block_gemm(const void* Aq, const float* As, const void* Wq
                                  void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
                                  uint32_t flags, cudaStream_t st) {
     return gemm::launch(Aq, As, Wq, Ws, D, M, N, K, blk_n, blk_k, flags, false, nullptr, st);
+}
+
+sgq_status launch_fp8_block_gemm_ue8m0(const void* Aq, const uint8_t* Ae, const void* Wq, const uint8_t* We,
+                                       void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                       uint32_t flags, cudaStream_t st) {
+    return gemm::launch_ue8m0(Aq, Ae, Wq, We, D, M, N, K, blk_n, blk_k, flags, st);
 }
 
 // The launch plan of launch_fp8_block_gemm, except where that plan's split-K
@@ -651,8 +726,13 @@ sgq_status launch_fp8_block_linear(const void* x, int ue8m0, const void* Wq, con
 uint64_t allocated_bytes() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    std::lock_guard<std::mutex> lk(gemm::g_ws_mu);
-    return gemm::g_ws[dev].partial ? uint64_t(gemm::kWsBytes) + gemm::kMaxCounters * sizeof(uint32_t) : 0;
+    uint64_t b = 0;
+    {
+        std::lock_guard<std::mutex> lk(gemm::g_ws_mu);
+        if (gemm::g_ws[dev].partial) b += uint64_t(gemm::kWsBytes) + gemm::kMaxCounters * sizeof(uint32_t);
+    }
+    std::lock_guard<std::mutex> lk(gemm::g_wide_mu);
+    return b + gemm::g_wide[dev].bytes;
 }
 
 sgq_status read_and_clear_device_status(cudaStream_t st) {

@@ -23,11 +23,14 @@ using qm::unpack8;
 
 // One thread per 8 consecutive elements; kTpg = group/8 consecutive lanes own
 // one group.  Loop trip counts are warp-uniform so the shuffles see full warps.
-template <int kGroup, bool kUe8m0>
+// kE8: the group scales (powers of two) are stored as UE8M0 bytes (their
+// biased exponent field) in xs, uint8 [M, K / group], instead of fp32.
+template <int kGroup, bool kUe8m0, bool kE8 = false>
 __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __restrict__ x,
                                                                 uint2* __restrict__ xq,
-                                                                float* __restrict__ xs,
+                                                                void* __restrict__ xs_out,
                                                                 int64_t nvec) {
+    static_assert(!kE8 || kUe8m0, "UE8M0 bytes need power-of-two scales");
     // Let a programmatically-dependent GEMM launch now, so that its weight
     // prefetch overlaps this kernel; it still waits for this grid to finish
     // before it reads xq / xs.
@@ -67,7 +70,12 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
             const float s = group_scale(amax, kUe8m0);
             if (active) {
                 xq[v] = quantize8(f, s, kUe8m0);
-                if ((lane % kTpg) == 0) xs[v / kTpg] = s;
+                if ((lane % kTpg) == 0) {
+                    if constexpr (kE8)
+                        static_cast<uint8_t*>(xs_out)[v / kTpg] = static_cast<uint8_t>(__float_as_uint(s) >> 23);
+                    else
+                        static_cast<float*>(xs_out)[v / kTpg] = s;
+                }
             }
         }
     }
@@ -345,8 +353,8 @@ __global__ void __launch_bounds__(kRowThreads) quant_per_tensor_kernel(const uin
     }
 }
 
-template <int G, bool U>
-sgq_status launch_tg(const void* x, int64_t M, int64_t K, void* xq, float* xs, cudaStream_t st) {
+template <int G, bool U, bool E8 = false>
+sgq_status launch_tg(const void* x, int64_t M, int64_t K, void* xq, void* xs, cudaStream_t st) {
     const int64_t nvec = M * K / 8;
     DeviceInfo di;
     sgq_status rc = device_info(&di);
@@ -357,7 +365,7 @@ sgq_status launch_tg(const void* x, int64_t M, int64_t K, void* xq, float* xs, c
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGQ_ERR_CUDA;
     if (resident[dev] == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_token_group_kernel<G, U>, 256, 0) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_token_group_kernel<G, U, E8>, 256, 0) != cudaSuccess ||
             n < 1)
             return SGQ_ERR_CUDA;
         resident[dev] = n;
@@ -375,7 +383,7 @@ sgq_status launch_tg(const void* x, int64_t M, int64_t K, void* xq, float* xs, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, quant_token_group_kernel<G, U>, static_cast<const uint4*>(x),
+    if (cudaLaunchKernelEx(&cfg, quant_token_group_kernel<G, U, E8>, static_cast<const uint4*>(x),
                            static_cast<uint2*>(xq), xs, nvec) != cudaSuccess)
         return SGQ_ERR_CUDA;
     note_launch();
@@ -412,6 +420,62 @@ sgq_status launch_quant_token_group(const void* x, int64_t M, int64_t K, int gro
                                   : launch_tg<32, false>(x, M, K, xq, xs, st);
     return ue8m0 ? launch_tg<128, true>(x, M, K, xq, xs, st)
                  : launch_tg<128, false>(x, M, K, xq, xs, st);
+}
+
+sgq_status launch_quant_token_group_e8(const void* x, int64_t M, int64_t K, int group, void* xq, uint8_t* xe,
+                                       cudaStream_t st) {
+    return group == 32 ? launch_tg<32, true, true>(x, M, K, xq, xe, st) : launch_tg<128, true, true>(x, M, K, xq, xe, st);
+}
+
+namespace {
+// UE8M0 byte of a positive normal power of two: its biased exponent field;
+// anything else -> 255 (the format's NaN) and a status bit.
+__global__ void __launch_bounds__(256) scales_to_ue8m0_kernel(const float* __restrict__ s, int64_t n,
+                                                              uint8_t* __restrict__ e, uint32_t* status) {
+    uint32_t bad = 0;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const uint32_t b = __float_as_uint(__ldg(s + i));
+        const uint32_t x = (b >> 23) & 0xFFu;
+        const bool ok = (b & 0x807FFFFFu) == 0u && x >= 1u && x <= 254u;
+        e[i] = static_cast<uint8_t>(ok ? x : 255u);
+        bad |= ok ? 0u : 1u;
+    }
+    if (__any_sync(0xFFFFFFFFu, bad != 0u) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusBadValue);
+}
+// fp32 value 2^(e - 127) of a UE8M0 byte (255 -> NaN), by its bits.
+__global__ void __launch_bounds__(256) ue8m0_to_scales_kernel(const uint8_t* __restrict__ e, int64_t n,
+                                                              float* __restrict__ s) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const uint32_t x = __ldg(e + i);
+        s[i] = __uint_as_float(x == 255u ? 0x7FC00000u : (x == 0u ? 0x00400000u : x << 23));
+    }
+}
+int elementwise_blocks(int64_t n) {
+    DeviceInfo di;
+    if (device_info(&di) != SGQ_OK) return 1;
+    const int64_t want = (n + 255) / 256;
+    const int64_t cap = int64_t(di.sm_count) * 8;
+    return static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+}
+}  // namespace
+
+sgq_status launch_scales_to_ue8m0(const float* s, int64_t n, uint8_t* e, cudaStream_t st) {
+    if (n == 0) return SGQ_OK;
+    uint32_t* status = nullptr;
+    const sgq_status rc = gemm::status_word(&status);
+    if (rc != SGQ_OK) return rc;
+    scales_to_ue8m0_kernel<<<elementwise_blocks(n), 256, 0, st>>>(s, n, e, status);
+    if (cudaGetLastError() != cudaSuccess) return SGQ_ERR_CUDA;
+    note_launch();
+    return SGQ_OK;
+}
+
+sgq_status launch_ue8m0_to_scales(const uint8_t* e, int64_t n, float* s, cudaStream_t st) {
+    if (n == 0) return SGQ_OK;
+    ue8m0_to_scales_kernel<<<elementwise_blocks(n), 256, 0, st>>>(e, n, s);
+    if (cudaGetLastError() != cudaSuccess) return SGQ_ERR_CUDA;
+    note_launch();
+    return SGQ_OK;
 }
 
 sgq_status launch_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n, int blk_k,

@@ -19,6 +19,15 @@ void note_launch(int n = 1);
 
 sgq_status launch_quant_token_group(const void* x, int64_t M, int64_t K, int group,
                                     int ue8m0, void* xq, float* xs, cudaStream_t stream);
+sgq_status launch_quant_token_group_e8(const void* x, int64_t M, int64_t K, int group, void* xq, uint8_t* xe,
+                                       cudaStream_t stream);
+// fp32 power-of-two scales -> UE8M0 bytes (255 and a device status for others).
+sgq_status launch_scales_to_ue8m0(const float* s, int64_t n, uint8_t* e, cudaStream_t stream);
+// UE8M0 bytes -> fp32 scales 2^(e - 127).
+sgq_status launch_ue8m0_to_scales(const uint8_t* e, int64_t n, float* s, cudaStream_t stream);
+sgq_status launch_fp8_block_gemm_ue8m0(const void* Aq, const uint8_t* Ae, const void* Wq, const uint8_t* We,
+                                       void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                       uint32_t flags, cudaStream_t stream);
 sgq_status launch_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n,
                                      int blk_k, int ue8m0, void* wq, float* ws,
                                      cudaStream_t stream);
@@ -47,6 +56,13 @@ sgq_status launch_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, c
 sgq_status gemm_plan_query(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out);
 // Bytes of device memory the library has allocated on the current device.
 uint64_t allocated_bytes();
+// The device status word of the current device (kernels atomicOr bits into
+// it: 1 a bounded wait ran out, 2 a scale broke its power-of-two promise or
+// could not be expressed as UE8M0).
+namespace gemm {
+sgq_status status_word(uint32_t** out);
+}
+constexpr uint32_t kStatusBadValue = 2u;
 // Reads and clears the device status word of the current device (after a sync).
 sgq_status read_and_clear_device_status(cudaStream_t stream);
 

@@ -76,16 +76,17 @@ class Case:
     def flops(self) -> float:
         return 2.0 * self.M * self.N * self.K
 
-    def gemm_bytes(self) -> float:
-        """Algorithmic GEMM bytes: Aq + As + Wq + Ws + D."""
+    def gemm_bytes(self, scale_bytes: int = 4) -> float:
+        """Algorithmic GEMM bytes: Aq + As + Wq + Ws + D (scale_bytes per
+        scale: 4 for fp32, 1 for UE8M0 bytes)."""
         M, N, K = self.M, self.N, self.K
-        return (M * K + 4 * M * K / self.blk_k + N * K
-                + 4 * math.ceil(N / self.blk_n) * K / self.blk_k + 2 * M * N)
+        return (M * K + scale_bytes * M * K / self.blk_k + N * K
+                + scale_bytes * math.ceil(N / self.blk_n) * K / self.blk_k + 2 * M * N)
 
-    def quant_bytes(self) -> float:
-        """Algorithmic quant bytes: bf16 read + codes + fp32 scales written."""
+    def quant_bytes(self, scale_bytes: int = 4) -> float:
+        """Algorithmic quant bytes: bf16 read + codes + scales written."""
         M, K = self.M, self.K
-        return 2 * M * K + M * K + 4 * M * K / self.group
+        return 2 * M * K + M * K + scale_bytes * M * K / self.group
 
 
 def _cases() -> dict:

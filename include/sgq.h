@@ -128,6 +128,28 @@ sgq_status sgq_quant_weight_block(const void* w, int64_t N, int64_t K, int blk_n
                                   sgq_stream_t stream);
 
 /*
+ * UE8M0 scale bytes.  A power-of-two scale 2^(e - 127) is held as the one
+ * byte e (its biased exponent; 255 is NaN): the format of the block-scaled
+ * MMA's scale factors, and of the scale buffers that sglang PR #42604
+ * prepares (Modifications: "prepares block32 scale buffers", keeping "UE8M0
+ * activation rounding").  Bytes carry the scales in a quarter of the fp32
+ * bytes, and the GEMM reads them without conversion.
+ *
+ * sgq_quant_token_group_ue8m0: sgq_quant_token_group with ue8m0 = 1 (the
+ * same codes, bit for bit), each group's scale written as its UE8M0 byte.
+ * xe: uint8 [M, K/group], 16-byte aligned.
+ *
+ * sgq_scales_to_ue8m0: e[i] = UE8M0 byte of s[i], i < n, for fp32 scales
+ * that are positive normal powers of two (the weight scales of
+ * sgq_quant_weight_block with ue8m0 = 1, converted once at load time).  Any
+ * other value gives 255 and sets the device status (sgq_device_status ->
+ * SGQ_ERR_INVALID_ARG).
+ */
+sgq_status sgq_quant_token_group_ue8m0(const void* x, int64_t M, int64_t K, int group, void* xq,
+                                       uint8_t* xe, sgq_stream_t stream);
+sgq_status sgq_scales_to_ue8m0(const float* s, int64_t n, uint8_t* e, sgq_stream_t stream);
+
+/*
  * Block-scaled FP8 GEMM, "NT" form.
  *
  * Defined by the vLLM "scaled_mm" API page, AiterInt8ScaledMMLinearKernel.
@@ -208,6 +230,24 @@ sgq_status sgq_fp8_block_gemm_ex(const void* Aq, const float* As, const void* Wq
 sgq_status sgq_fp8_block_gemm_noalloc(const void* Aq, const float* As, const void* Wq,
                                       const float* Ws, void* D, int64_t M, int64_t N, int64_t K,
                                       int blk_n, int blk_k, sgq_stream_t stream);
+
+/*
+ * sgq_fp8_block_gemm_ex with UE8M0 scale bytes: Ae uint8 [M, K/blk_k] and
+ * We uint8 [ceil(N/blk_n), K/blk_k] in place of As and Ws (16-byte aligned;
+ * byte e is the scale 2^(e - 127)).  D is bit-identical to
+ * sgq_fp8_block_gemm_ex with the fp32 scales 2^(e - 127) and
+ * SGQ_GEMM_SCALES_POW2 (which this call implies).  Flags: as for
+ * sgq_fp8_block_gemm_ex, without SGQ_GEMM_TEST_TIMEOUT.  Where the
+ * two-accumulator tiles take the shape they read the bytes directly; other
+ * plans (e.g. decode sizes) first widen them to fp32 in a library buffer,
+ * allocated on the first call that needs it (not inside a stream capture;
+ * grown, with a device synchronisation, when a larger shape needs more).  A
+ * byte of 255 is reported as SGQ_ERR_INVALID_ARG by sgq_device_status where
+ * the bytes are read directly.
+ */
+sgq_status sgq_fp8_block_gemm_ue8m0(const void* Aq, const uint8_t* Ae, const void* Wq, const uint8_t* We,
+                                    void* D, int64_t M, int64_t N, int64_t K, int blk_n, int blk_k,
+                                    uint32_t flags, sgq_stream_t stream);
 
 /*
  * Quantise-and-multiply: the whole W8A8 linear layer in one call.

@@ -18,6 +18,10 @@ builds it with gcc on first use and wraps it with numpy arrays:
 * ``quant_token_group_v2`` (with ``exp_tc`` / ``silu_mul``) -- the V2
   per-token-group quantiser: fused SiLU-and-mul and masked M (same page,
   Quantization Routines and Signature).
+* ``ue8m0_bytes`` / ``ue8m0_values`` -- power-of-two scales as UE8M0 bytes
+  (8-bit biased exponent, value 2^(e - 127), 255 = NaN), the format of the
+  scale buffers the sglang PR #42604 path prepares (Modifications: "prepares
+  block32 scale buffers", with UE8M0 activation rounding).
 * ``quant_per_token`` / ``quant_per_tensor`` / ``scaled_mm`` -- the
   per-token and per-tensor quantisers and fp8_scaled_mm (per-tensor or per-row
   A scales, per-tensor or per-column B scales, optional bias) of "Sgl project
@@ -138,6 +142,25 @@ def ue8m0_ceil(s) -> np.ndarray:
     s = np.asarray(s, dtype=np.float32)
     return np.array([lib.sgqo_ue8m0_ceil(float(x)) for x in s.reshape(-1)],
                     dtype=np.float32).reshape(s.shape)
+
+
+def ue8m0_bytes(s) -> np.ndarray:
+    """fp32 scales -> UE8M0 bytes, elementwise: the biased exponent field of a
+    positive normal power of two (value 2^(e - 127), e in 1 .. 254); any other
+    value (not a power of two, zero, negative, subnormal, inf, NaN) -> 255,
+    the format's NaN."""
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    bits = s.view(np.uint32)
+    e = (bits >> np.uint32(23)) & np.uint32(0xFF)
+    exact = ((bits & np.uint32(0x807FFFFF)) == 0) & (e >= 1) & (e <= 254)
+    return np.where(exact, e, 255).astype(np.uint8)
+
+
+def ue8m0_values(e) -> np.ndarray:
+    """UE8M0 bytes -> fp32 values 2^(e - 127); 255 -> NaN."""
+    e = np.asarray(e, dtype=np.uint8).astype(np.int64)
+    v = np.ldexp(np.float64(1.0), (e - 127).astype(np.int32))
+    return np.where(e == 255, np.nan, v).astype(np.float32)
 
 
 def group_scale(amax: float, ue8m0: bool, eps: float = EPS) -> np.float32:

@@ -126,6 +126,29 @@ def test_ue8m0_is_minimal_power_of_two():
             assert float(s) == float(s32)
 
 
+def test_ue8m0_bytes_closed_forms_and_round_trip():
+    """UE8M0 byte of a power-of-two scale: the 8-bit biased exponent (value
+    2^(e - 127)).  Closed forms, every byte 1 .. 254 through ldexp and back,
+    the NaN byte (255) for everything that is not a positive normal power of
+    two, and log2 of the power-of-two rounding (ue8m0_ceil) for random scales."""
+    f32 = np.float32
+    known = {1.0: 127, 0.5: 126, 2.0: 128, 2.0 ** -126: 1, 2.0 ** 127: 254, 2.0 ** -7: 120, 448.0 / 448.0: 127}
+    for v, e in known.items():
+        assert int(oracle.ue8m0_bytes(np.array([v], f32))[0]) == e
+    e = np.arange(1, 255, dtype=np.uint8)
+    v = np.ldexp(np.float32(1.0), e.astype(np.int32) - 127).astype(f32)
+    assert np.array_equal(oracle.ue8m0_bytes(v), e)
+    assert np.array_equal(oracle.ue8m0_values(e), v)
+    bad = np.array([3.0, -1.0, 0.0, -0.0, 2.0 ** -130, np.inf, np.nan, 1.5, 448.0], f32)
+    assert np.all(oracle.ue8m0_bytes(bad) == 255)
+    assert np.isnan(oracle.ue8m0_values(np.array([255], np.uint8))[0])
+    rng = np.random.default_rng(7)
+    s = (rng.random(2000) * 10.0 ** rng.integers(-30, 30, 2000)).astype(f32)
+    s = s[(s > np.finfo(f32).tiny) & (s < 2.0 ** 126)]
+    p = oracle.ue8m0_ceil(s)
+    assert np.array_equal(oracle.ue8m0_bytes(p).astype(np.int64), np.ceil(np.log2(s.astype(np.float64))).astype(np.int64) + 127)
+
+
 def test_fp32_scale_is_correctly_rounded_division():
     rng = np.random.default_rng(3)
     a = rng.uniform(1e-3, 1e3, 5000).astype(np.float32)
