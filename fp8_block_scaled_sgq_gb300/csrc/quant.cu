@@ -68,14 +68,33 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
             for (int off = kTpg / 2; off > 0; off >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
             const float s = group_scale(amax, kUe8m0);
-            if (active) {
-                xq[v] = quantize8(f, s, kUe8m0);
-                if ((lane % kTpg) == 0) {
-                    if constexpr (kE8)
-                        static_cast<uint8_t*>(xs_out)[v / kTpg] = static_cast<uint8_t>(__float_as_uint(s) >> 23);
-                    else
-                        static_cast<float*>(xs_out)[v / kTpg] = s;
+            if constexpr (kE8) {
+                // The warp's 32 / kTpg group bytes are consecutive in xe: lane 0
+                // gathers them and stores them at once (8 or 2 bytes) when the
+                // whole chunk is in range; a ragged last chunk stores per group.
+                constexpr int kGroupsPerWarp = 32 / kTpg;
+                const uint32_t e = __float_as_uint(s) >> 23;
+                uint8_t* xe = static_cast<uint8_t*>(xs_out);
+                const int64_t v0 = base + u * stride;
+                if (v0 + 31 < nvec) {
+                    uint64_t packed = 0;
+#pragma unroll
+                    for (int j = 0; j < kGroupsPerWarp; ++j)
+                        packed |= static_cast<uint64_t>(__shfl_sync(0xFFFFFFFFu, e, j * kTpg) & 0xFFu) << (8 * j);
+                    if (active) xq[v] = quantize8(f, s, kUe8m0);
+                    if (lane == 0) {
+                        if constexpr (kGroupsPerWarp == 8)
+                            *reinterpret_cast<uint64_t*>(xe + v0 / kTpg) = packed;
+                        else
+                            *reinterpret_cast<uint16_t*>(xe + v0 / kTpg) = static_cast<uint16_t>(packed);
+                    }
+                } else if (active) {
+                    xq[v] = quantize8(f, s, kUe8m0);
+                    if ((lane % kTpg) == 0) xe[v / kTpg] = static_cast<uint8_t>(e);
                 }
+            } else if (active) {
+                xq[v] = quantize8(f, s, kUe8m0);
+                if ((lane % kTpg) == 0) static_cast<float*>(xs_out)[v / kTpg] = s;
             }
         }
     }

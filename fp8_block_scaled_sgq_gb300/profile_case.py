@@ -1,7 +1,8 @@
 """Runs one quantise + GEMM case of a workload a few times, for profilers.
 
-    python -m fp8_block_scaled_sgq_gb300.profile_case WORKLOAD [INDEX] [--iters N] [--fused | --quant-only] [--pow2]
-    python -m fp8_block_scaled_sgq_gb300.profile_case --shape M N K BLK [--iters N] [--fused | --quant-only] [--pow2]
+    python -m fp8_block_scaled_sgq_gb300.profile_case WORKLOAD [INDEX] [--iters N] [--fused | --quant-only]
+                                                      [--pow2 | --ue8m0-bytes]
+    python -m fp8_block_scaled_sgq_gb300.profile_case --shape M N K BLK [...]
 
 WORKLOAD/INDEX pick a case from ``synth.WORKLOADS`` (e.g. ``decode_block32 2``
 is M=16, N=7168, K=2048 with [32,32] blocks); --shape takes any shape with
@@ -9,8 +10,10 @@ is M=16, N=7168, K=2048 with [32,32] blocks); --shape takes any shape with
 activation quantisation kernel, then the block-scaled GEMM, on one stream.
 With --fused each iteration is one sgq_fp8_block_linear call instead (one
 kernel at decode-sized M); with --quant-only only the quantisation kernel;
---pow2 passes SGQ_GEMM_SCALES_POW2 to the GEMM.  The weight is quantised once up front (one extra
-launch).  The run ends with
+--pow2 passes SGQ_GEMM_SCALES_POW2 to the GEMM; --ue8m0-bytes runs the
+byte-output quantiser and sgq_fp8_block_gemm_ue8m0 (the weight scales
+converted to bytes once up front).  The weight is quantised once up front
+(one extra launch; two with --ue8m0-bytes).  The run ends with
 the device status word checked and one line of wall-clock timing, which is
 not a benchmark number (use bench.py for those).
 """
@@ -34,6 +37,7 @@ def main() -> None:
     ap.add_argument("--fused", action="store_true")
     ap.add_argument("--quant-only", action="store_true", help="launch only the activation quantiser")
     ap.add_argument("--pow2", action="store_true", help="GEMM with SGQ_GEMM_SCALES_POW2 (UE8M0 scales)")
+    ap.add_argument("--ue8m0-bytes", action="store_true", help="UE8M0 scale bytes (quantiser and GEMM)")
     args = ap.parse_args()
     if args.shape:
         M, N, K, blk = args.shape
@@ -56,10 +60,18 @@ def main() -> None:
     d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     torch.cuda.synchronize()
     binding.sgq_quant_weight_block(w, N, K, c.blk_n, c.blk_k, int(c.ue8m0), wq, ws, s)
+    if args.ue8m0_bytes:
+        we = torch.empty((nb, kb), dtype=torch.uint8, device=dev)
+        binding.sgq_scales_to_ue8m0(ws, nb * kb, we, s)
+        xe = torch.empty((M, -(-K // c.group)), dtype=torch.uint8, device=dev)
     t0 = time.perf_counter()
     for _ in range(args.iters):
         if args.fused:
             binding.sgq_fp8_block_linear(x, int(c.ue8m0), wq, ws, d, M, N, K, c.blk_n, c.blk_k, None, None, s)
+        elif args.ue8m0_bytes:
+            binding.sgq_quant_token_group_ue8m0(x, M, K, c.group, xq, xe, s)
+            if not args.quant_only:
+                binding.sgq_fp8_block_gemm_ue8m0(xq, xe, wq, we, d, M, N, K, c.blk_n, c.blk_k, 0, s)
         else:
             binding.sgq_quant_token_group(x, M, K, c.group, int(c.ue8m0), xq, xs, s)
             if not args.quant_only:
@@ -71,6 +83,7 @@ def main() -> None:
     if status != 0:
         raise RuntimeError(f"device status {binding.status_string(status)}")
     print(json.dumps({"case": c.name, "fused": args.fused, "quant_only": args.quant_only, "pow2": args.pow2,
+                      "ue8m0_bytes": args.ue8m0_bytes,
                       "M": M, "N": N, "K": K, "blk": [c.blk_n, c.blk_k],
                       "iters": args.iters, "wall_ms": round(wall * 1e3, 3)}))
 
