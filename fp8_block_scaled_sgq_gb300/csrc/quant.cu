@@ -77,16 +77,18 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
                 uint8_t* xe = static_cast<uint8_t*>(xs_out);
                 const int64_t v0 = base + u * stride;
                 if (v0 + 31 < nvec) {
-                    uint64_t packed = 0;
+                    // pack by halving: the leader of group j ends up with groups j, j+1, ...
+                    uint32_t w = e & 0xFFu;
 #pragma unroll
-                    for (int j = 0; j < kGroupsPerWarp; ++j)
-                        packed |= static_cast<uint64_t>(__shfl_sync(0xFFFFFFFFu, e, j * kTpg) & 0xFFu) << (8 * j);
+                    for (int d = kTpg, sh = 8; d < 32 && sh < 32; d *= 2, sh *= 2)
+                        w |= __shfl_down_sync(0xFFFFFFFFu, w, d) << sh;
                     if (active) xq[v] = quantize8(f, s, kUe8m0);
-                    if (lane == 0) {
-                        if constexpr (kGroupsPerWarp == 8)
-                            *reinterpret_cast<uint64_t*>(xe + v0 / kTpg) = packed;
-                        else
-                            *reinterpret_cast<uint16_t*>(xe + v0 / kTpg) = static_cast<uint16_t>(packed);
+                    if constexpr (kGroupsPerWarp == 8) {
+                        const uint32_t hi = __shfl_sync(0xFFFFFFFFu, w, 16);   // groups 4 .. 7
+                        if (lane == 0)
+                            *reinterpret_cast<uint2*>(xe + v0 / kTpg) = make_uint2(w, hi);
+                    } else {
+                        if (lane == 0) *reinterpret_cast<uint16_t*>(xe + v0 / kTpg) = static_cast<uint16_t>(w);
                     }
                 } else if (active) {
                     xq[v] = quantize8(f, s, kUe8m0);
