@@ -550,29 +550,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const int grow = it.tr * kTileRows + static_cast<int>(rank) * kRowsA + h * kHalf + quad * 32 + lane;
                     __nv_bfloat16* drow = a.D + static_cast<int64_t>(grow) * a.N;
+                    // The warp's share of the accumulator goes to registers as
+                    // packed bf16 first, and the accumulator is released before
+                    // the stores: the next tile's MMAs for this half start
+                    // while D is written.
+                    constexpr int kChunks = C::kColsPerWarp / 16;
+                    uint32_t w[kChunks][8];
 #pragma unroll
-                    for (int c0 = 0; c0 < C::kColsPerWarp; c0 += 16) {
-                        const int cl = chalf * C::kColsPerWarp + c0;   // column inside the tile
+                    for (int q = 0; q < kChunks; ++q) {
                         uint32_t rr[16];
-                        ptx::tmem_ld<16>(t_lane + static_cast<uint32_t>(h * BN + cl), rr);
+                        ptx::tmem_ld<16>(t_lane + static_cast<uint32_t>(h * BN + chalf * C::kColsPerWarp + 16 * q), rr);
                         ptx::tmem_wait_ld();
-                        uint32_t w[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const __nv_bfloat162 p =
                                 __floats2bfloat162_rn(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
-                            w[j] = *reinterpret_cast<const uint32_t*>(&p);
-                        }
-                        const int gcol = it.tc * BN + cl;
-                        if (grow < a.M) {
-                            if (v8 && gcol + 16 <= a.N) {
-                                ptx::st_global_v8(drow + gcol, w);
-                            } else {
-                                if (gcol < a.N)
-                                    *reinterpret_cast<uint4*>(drow + gcol) = make_uint4(w[0], w[1], w[2], w[3]);
-                                if (gcol + 8 < a.N)
-                                    *reinterpret_cast<uint4*>(drow + gcol + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-                            }
+                            w[q][j] = *reinterpret_cast<const uint32_t*>(&p);
                         }
                     }
                     ptx::tc_fence_before();
@@ -585,6 +578,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
                         if (lane == 0) ptx::mbar_arrive(acce_bar(h));
+                    }
+                    if (grow < a.M) {
+#pragma unroll
+                        for (int q = 0; q < kChunks; ++q) {
+                            const int gcol = it.tc * BN + chalf * C::kColsPerWarp + 16 * q;
+                            if (v8 && gcol + 16 <= a.N) {
+                                ptx::st_global_v8(drow + gcol, w[q]);
+                            } else {
+                                if (gcol < a.N)
+                                    *reinterpret_cast<uint4*>(drow + gcol) =
+                                        make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
+                                if (gcol + 8 < a.N)
+                                    *reinterpret_cast<uint4*>(drow + gcol + 8) =
+                                        make_uint4(w[q][4], w[q][5], w[q][6], w[q][7]);
+                            }
+                        }
                     }
                 }
                 if (failed) break;
