@@ -94,6 +94,21 @@ __global__ void __launch_bounds__(256) quant_token_group_kernel(const uint4* __r
                     xq[v] = quantize8(f, s, kUe8m0);
                     if ((lane % kTpg) == 0) xe[v / kTpg] = static_cast<uint8_t>(e);
                 }
+            } else if constexpr (kGroup == 128) {
+                // fp32 scales, group 128: the warp's two group scales go out as
+                // one 8-byte store when the chunk is whole (measured 32.0 ->
+                // 29.3 us at 8192 x 7168; for group 32 the eight shuffles cost
+                // more than the per-group stores they replace).
+                float* xs = static_cast<float*>(xs_out);
+                const int64_t v0 = base + u * stride;
+                if (v0 + 31 < nvec) {
+                    const float s1 = __shfl_sync(0xFFFFFFFFu, s, kTpg);
+                    if (active) xq[v] = quantize8(f, s, kUe8m0);
+                    if (lane == 0) *reinterpret_cast<float2*>(xs + v0 / kTpg) = make_float2(s, s1);
+                } else if (active) {
+                    xq[v] = quantize8(f, s, kUe8m0);
+                    if ((lane % kTpg) == 0) xs[v / kTpg] = s;
+                }
             } else if (active) {
                 xq[v] = quantize8(f, s, kUe8m0);
                 if ((lane % kTpg) == 0) static_cast<float*>(xs_out)[v / kTpg] = s;
