@@ -42,9 +42,11 @@ def test_scales_to_ue8m0_matches_oracle_and_flags_bad_values():
     assert sgq.sgq_device_status() == binding.SGQ_OK
 
 
-# the two-accumulator tiles (one CTA per tile, CTA pairs, K split over CTAs),
-# mid-M one split, and plans that widen the bytes first (decode, tiny, short K)
+# the two-accumulator tiles (one CTA per tile; CTA pairs for [*,32] with K >=
+# 4096; K split over CTAs), mid-M one split, and plans that widen the bytes
+# first (decode, tiny, short K)
 SHAPES = [(4096, 7168, 512, 128, 128), (4100, 7000, 4096, 128, 128), (4200, 7000, 384, 32, 32),
+          (4100, 7000, 4096, 32, 32), (2100, 14000, 4096, 128, 32),
           (1024, 1536, 7168, 128, 128), (700, 7168, 2048, 32, 32), (16, 7168, 2048, 32, 32),
           (3, 520, 1024, 128, 32), (300, 1032, 640, 32, 128)]
 
@@ -81,3 +83,42 @@ def test_gemm_ue8m0_reports_a_nan_byte():
     sgq.fp8_block_gemm_ue8m0(t(aq), t(ae), t(wq), t(we), bk, bk)
     assert sgq.sgq_device_status() == binding.SGQ_ERR_INVALID_ARG
     assert sgq.sgq_device_status() == binding.SGQ_OK
+
+
+_PAIR_CHILD = r"""
+import sys, numpy as np, torch
+import fp8_block_scaled_sgq_gb300 as sgq
+from fp8_block_scaled_sgq_gb300 import synth
+import oracle
+M, N, K, bn, bk = (int(v) for v in sys.argv[1:6])
+aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=47), bk, True)
+wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=47), bn, bk, True)
+t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()
+d8 = sgq.fp8_block_gemm_ue8m0(t(aq), t(oracle.ue8m0_bytes(a_s)), t(wq), t(oracle.ue8m0_bytes(ws)), bn, bk)
+assert sgq.sgq_device_status() == 0
+d32 = sgq.fp8_block_gemm(t(aq), t(a_s), t(wq), t(ws), bn, bk, flags=sgq.SGQ_GEMM_SCALES_POW2)
+assert sgq.sgq_device_status() == 0
+assert torch.equal(d8, d32)
+np.save(sys.argv[6], d8.view(torch.int16).cpu().numpy())
+"""
+
+
+@pytest.mark.parametrize("M,N,K,bn,bk", [(4100, 7000, 1280, 128, 128), (4096, 7168, 4096, 128, 32)])
+def test_gemm_ue8m0_on_forced_cta_pairs(tmp_path, M, N, K, bn, bk):
+    """Byte scales on CTA pairs where the default plan keeps single CTAs
+    ([*,128], short K), forced with SGQ_DUAL_PAIR=1 in a child process: bit
+    for bit the fp32 path on pairs, and the oracle on every 64-row block."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.path.join(root, "tests"), SGQ_DUAL_PAIR="1")
+    out = str(tmp_path / "d.npy")
+    subprocess.run([sys.executable, "-c", _PAIR_CHILD, str(M), str(N), str(K), str(bn), str(bk), out], env=env,
+                   check=True, timeout=600, cwd=root)
+    d = torch.from_numpy(np.load(out)).view(torch.bfloat16)
+    aq, a_s = oracle.quant_token_group(synth.activation(M, K, seed=47), bk, True)
+    wq, ws = oracle.quant_weight_block(synth.weight(N, K, seed=47), bn, bk, True)
+    r = tile_rows(M, seed=M)
+    dref, bound = oracle.gemm(aq[r], a_s[r], wq, ws, bn, bk)
+    check_gemm(d[torch.from_numpy(r)], dref, bound, f"ue8m0 pairs M={M} N={N} K={K} [{bn},{bk}]")
