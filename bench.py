@@ -55,15 +55,27 @@ def peaks():
             "source": "fallback"}
 
 
-def kernel_source_digest() -> str:
-    """sha256 over the CUDA sources, to tie ncu counters to the build they came from."""
+# The sources each workload's dominant kernel is compiled and planned from:
+# its translation unit, the headers that reach it, and the host code that picks
+# its tiles, splits and grid.  A workload not listed here hashes every source.
+KERNEL_SOURCES = {
+    "decode_block32": ["gemm_b32_32.cu", "gemm_kernel.cuh", "ptx.cuh", "quant_math.cuh", "sgq_internal.h",
+                       "gemm_host.cu"],
+}
+
+
+def kernel_source_digest(workload: str | None = None) -> str:
+    """sha256 over the CUDA sources of `workload`'s dominant kernel (all
+    sources when it has no list), to tie ncu counters to the build they came from."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "fp8_block_scaled_sgq_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(d, name), "rb").read())
+    names = KERNEL_SOURCES.get(workload) or [n for n in os.listdir(d) if n.endswith((".cu", ".cuh", ".h"))]
+    for name in sorted(names):
+        h.update(name.encode())
+        h.update(open(os.path.join(d, name), "rb").read())
+    inc = os.path.join(ROOT, "include", "sgq.h")
+    h.update(open(inc, "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -77,7 +89,7 @@ def measured_traffic(workload: str):
     """Bytes per launch for `workload` from the traffic record, or None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    digest = kernel_source_digest()
+    digest = kernel_source_digest(workload)
     for line in open(TRAFFIC_FILE):
         f = line.split()
         if len(f) >= 3 and not line.startswith("#") and f[0] == workload and f[1] == digest:
