@@ -260,7 +260,7 @@ def roofline_frac(flops: float, nbytes: float, us: float):
     return ("fp8" if t_fp8 > t_hbm else "hbm"), max(t_fp8, t_hbm) / (us * 1e-6)
 
 
-# [1,32] GEMMs from this M on, with a wave of 256 x 224 tiles, run on UE8M0
+# UE8M0 GEMMs from this M on, with a wave of 256 x 224 tiles, run on UE8M0
 # scale bytes: the two-accumulator tiles read them directly (other plans would
 # widen them to fp32 first, an extra step).
 E8_MIN_M = 2048
@@ -289,10 +289,10 @@ def gemm_cases(sgq, timer, device, reps, names):
         werot = None
         for c in cs:
             x = c.x().to(device)
-            # The [1,32] recipe at prefill sizes reads UE8M0 scale bytes: the
-            # quantiser writes them, the GEMM reads them as they are (a quarter
-            # of the fp32 scale bytes per stage).  Elsewhere fp32 scales.
-            e8 = (c.ue8m0 and c.blk_k == 32 and c.M >= E8_MIN_M
+            # UE8M0 scales at prefill sizes travel as bytes: the quantiser
+            # writes them, the GEMM reads them as they are (a quarter of the
+            # fp32 scale bytes per stage, no conversion).  Elsewhere fp32 scales.
+            e8 = (c.ue8m0 and c.M >= E8_MIN_M
                   and math.ceil(c.M / 256) * math.ceil(c.N / 224) >= sm_count())
             if e8 and werot is None:
                 werot = [sgq.scales_to_ue8m0(ws) for _, ws in wrot]

@@ -374,10 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t a[4], b[4];
         };
         using Raw = std::conditional_t<kE8, RawE, RawF>;
-        // UE8M0 word of one row's stage from its bytes (one per scale column)
+        // A row's bytes for one stage as loaded (four scale columns, or one
+        // [*,128] byte); the word is formed only where it is used, so that
+        // nothing waits on a load that is still in flight.
         auto load_word = [&](const uint8_t* p) -> uint32_t {
             if constexpr (kSps == 4) return __ldg(reinterpret_cast<const uint32_t*>(p));
-            else return static_cast<uint32_t>(__ldg(p)) * 0x01010101u;
+            else return static_cast<uint32_t>(__ldg(p));
         };
         auto load = [&](Raw& v, int i, int kb) {
             if (i >= a.items) return;
@@ -389,10 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int i = lane + 32 * j;
                 const int n = tc * BN + h * kBRowsPerWarp + i;
                 if constexpr (kE8) {
-                    v.a[j] = row < a.M ? load_word(a.Ae + static_cast<int64_t>(row) * a.ks + kb * kSps) : 0x7F7F7F7Fu;
+                    constexpr uint32_t kOne = kSps == 4 ? 0x7F7F7F7Fu : 0x7Fu;   // 1.0 for padding rows
+                    v.a[j] = row < a.M ? load_word(a.Ae + static_cast<int64_t>(row) * a.ks + kb * kSps) : kOne;
                     v.b[j] = (i < kBRowsPerWarp && n < a.N)
                                  ? load_word(a.We + static_cast<int64_t>(n / kBlkN) * a.ks + kb * kSps)
-                                 : 0x7F7F7F7Fu;
+                                 : kOne;
                 } else {
                     v.a[j] = row < a.M ? load_scales<kSps>(a.As + static_cast<int64_t>(row) * a.ks + kb * kSps)
                                        : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
@@ -402,11 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
-        // scale word of a loaded row (UE8M0 bytes: as loaded; 255 = NaN is refused)
+        // scale word of a loaded row (UE8M0 bytes: the four as loaded, or the
+        // one [*,128] byte in every lane; 255 = NaN is refused)
         auto word_of = [&](const auto& r, uint32_t& bad) -> uint32_t {
             if constexpr (kE8) {
-                bad |= zero_byte(~r);
-                return r;
+                const uint32_t w = kSps == 4 ? r : r * 0x01010101u;
+                bad |= zero_byte(~w);
+                return w;
             } else {
                 return sf_word<kSps>(r, bad);
             }

@@ -432,13 +432,14 @@ int dual_mode(int64_t M, int64_t N, int64_t K, int blk_k, uint32_t flags, const 
     const int64_t tr = (M + dual::kRowsA - 1) / dual::kRowsA;
     const int64_t dual_tiles = tr * ((N + dual::kBNWide - 1) / dual::kBNWide);
     // A wave of tiles: CTA pairs with long K where a stage's scale work is
-    // light -- fp32 scales with the [*,128] recipe (4096 x 7168 x 7168: 161.6
-    // vs 169.2 us), UE8M0 bytes with [*,32] (4096 x 4096 x 7168: 85.2 vs 89.5
-    // us).  The pair's longer per-stage handshake loses on short K (8192 x
-    // 24576 x 1536: 333 vs 308 us), with fp32 [*,32] scales (4096 x 4096 x
-    // 7168: 105 vs 100 us) and with UE8M0 [*,128] bytes (218 vs 166 us).
+    // light -- fp32 scales with the [*,128] recipe (4096 x 7168 x 7168: 159.3
+    // vs 167.9 us) and UE8M0 bytes with either recipe (4096 x 4096 x 7168
+    // [*,32]: 85.0 vs 89.5 us; 4096 x 7168 x 7168 [*,128]: 155.0 vs 160.8 us).
+    // The pair's longer per-stage handshake loses on short K (8192 x 24576 x
+    // 1536 [*,32]: 333 vs 308 us) and with fp32 [*,32] scales (4096 x 4096 x
+    // 7168: 105 vs 100 us).
     if (!p.swap && dual_tiles >= sm_count) {
-        const bool pair_auto = K >= 4096 && blk_k == (e8 ? 32 : 128);
+        const bool pair_auto = K >= 4096 && (e8 || blk_k == 128);
         return pair_env > 0 || (pair_env < 0 && pair_auto) ? 3 : 1;
     }
     if (M >= 128 && dual_tiles * 5 >= int64_t(sm_count) * 3) return 1;

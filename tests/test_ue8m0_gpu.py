@@ -42,9 +42,9 @@ def test_scales_to_ue8m0_matches_oracle_and_flags_bad_values():
     assert sgq.sgq_device_status() == binding.SGQ_OK
 
 
-# the two-accumulator tiles (one CTA per tile; CTA pairs for [*,32] with K >=
-# 4096; K split over CTAs), mid-M one split, and plans that widen the bytes
-# first (decode, tiny, short K)
+# the two-accumulator tiles (one CTA per tile; CTA pairs with K >= 4096; K
+# split over CTAs), mid-M one split, and plans that widen the bytes first
+# (decode, tiny, short K)
 SHAPES = [(4096, 7168, 512, 128, 128), (4100, 7000, 4096, 128, 128), (4200, 7000, 384, 32, 32),
           (4100, 7000, 4096, 32, 32), (2100, 14000, 4096, 128, 32),
           (1024, 1536, 7168, 128, 128), (700, 7168, 2048, 32, 32), (16, 7168, 2048, 32, 32),
@@ -103,11 +103,12 @@ np.save(sys.argv[6], d8.view(torch.int16).cpu().numpy())
 """
 
 
-@pytest.mark.parametrize("M,N,K,bn,bk", [(4100, 7000, 1280, 128, 128), (4096, 7168, 4096, 128, 32)])
+@pytest.mark.parametrize("M,N,K,bn,bk", [(4100, 7000, 1280, 128, 128), (4200, 7000, 2048, 32, 32),
+                                         (4096, 7168, 4096, 128, 32)])
 def test_gemm_ue8m0_on_forced_cta_pairs(tmp_path, M, N, K, bn, bk):
-    """Byte scales on CTA pairs where the default plan keeps single CTAs
-    ([*,128], short K), forced with SGQ_DUAL_PAIR=1 in a child process: bit
-    for bit the fp32 path on pairs, and the oracle on every 64-row block."""
+    """Byte scales on CTA pairs, forced with SGQ_DUAL_PAIR=1 in a child process
+    (the default plan keeps K < 4096 on single CTAs): bit for bit the fp32
+    path on pairs, and the oracle on every 64-row block."""
     import os
     import subprocess
     import sys
