@@ -14,7 +14,7 @@ from .binding import (  # noqa: F401
     sgq_fp8_block_gemm, sgq_fp8_block_gemm_ex, sgq_fp8_block_linear, sgq_fp8_scaled_mm,
     sgq_quant_per_tensor, sgq_quant_per_token, sgq_quant_token_group_v2, sgq_launch_count, sgq_quant_token_group,
     sgq_allocated_bytes, sgq_fp8_block_gemm_ue8m0, sgq_quant_token_group_ue8m0, sgq_scales_to_ue8m0,
-    sgq_gemm_plan,
+    sgq_gemm_plan, sgq_gemm_plan_pow2,
     sgq_quant_weight_block, sgq_version, status_string)
 
 

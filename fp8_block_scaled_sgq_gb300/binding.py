@@ -50,6 +50,7 @@ EXPORTS = (
     "sgq_launch_count",
     "sgq_allocated_bytes",
     "sgq_gemm_plan",
+    "sgq_gemm_plan_pow2",
     "sgq_version",
 )
 
@@ -103,6 +104,8 @@ def load_library(path: str = LIB_PATH):
         lib.sgq_allocated_bytes.restype = ctypes.c_uint64
         lib.sgq_gemm_plan.argtypes = [i64, i64, i64, ci, ci, P]
         lib.sgq_gemm_plan.restype = ci
+        lib.sgq_gemm_plan_pow2.argtypes = [i64, i64, i64, ci, ci, ci, P]
+        lib.sgq_gemm_plan_pow2.restype = ci
         lib.sgq_version.argtypes = []
         lib.sgq_version.restype = ci
         _lib = lib
@@ -237,3 +240,14 @@ def sgq_gemm_plan(M, N, K, blk_k, sm_count=152) -> dict:
     _check(load_library().sgq_gemm_plan(M, N, K, blk_k, sm_count, ctypes.cast(out, ctypes.c_void_p)),
            "sgq_gemm_plan")
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+PLAN_POW2_FIELDS = ("mode", "bn", "splits", "items", "grid", "tiles", "kps")
+
+
+def sgq_gemm_plan_pow2(M, N, K, blk_k, sm_count=152, e8=False) -> dict:
+    """The two-accumulator plan under the power-of-two promise (host only; see include/sgq.h)."""
+    out = (ctypes.c_int32 * 8)()
+    _check(load_library().sgq_gemm_plan_pow2(M, N, K, blk_k, sm_count, int(bool(e8)), ctypes.cast(out, ctypes.c_void_p)),
+           "sgq_gemm_plan_pow2")
+    return dict(zip(PLAN_POW2_FIELDS, (int(v) for v in out)))

@@ -243,6 +243,13 @@ sgq_status sgq_gemm_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_coun
     return sgq::gemm_plan_query(M, N, K, blk_k, sm_count, out);
 }
 
-int sgq_version(void) { return 103; }
+sgq_status sgq_gemm_plan_pow2(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int e8, int32_t* out) {
+    if (out == nullptr || M < 1 || N < 1 || K < 1 || (blk_k != 32 && blk_k != 128) || sm_count < 2 ||
+        (e8 != 0 && e8 != 1))
+        return SGQ_ERR_INVALID_ARG;
+    return sgq::gemm_plan_pow2_query(M, N, K, blk_k, sm_count, e8, out);
+}
+
+int sgq_version(void) { return 104; }
 
 }  // extern "C"

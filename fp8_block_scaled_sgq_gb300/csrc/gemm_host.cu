@@ -309,6 +309,9 @@ struct Chan {
 // us), 8192 x 24576 takes 224 (24 rounds against 27; 280 vs 294 us).
 // pair: tiles of 512 rows over the SM pairs, each CTA holding 256 rows and BN / 2.
 int dual_width(int64_t M, int64_t N, int sm_count, bool pair = false) {
+    // SGQ_DUAL_BN=192/224 forces a width
+    static const int forced = env_int("SGQ_DUAL_BN", 0);
+    if (forced == dual::kBNNarrow || forced == dual::kBNWide) return forced;
     const int rows = pair ? 2 * dual::kRowsA : dual::kRowsA;
     const int units = pair ? sm_count / 2 : sm_count;
     const int64_t tr = (M + rows - 1) / rows;
@@ -355,16 +358,38 @@ int dual_splits(int64_t tiles, int kst, int sm_count, int bn, ScratchLimit lim) 
     return best;
 }
 
-// Launches the two-accumulator prefill GEMM (power-of-two scales): tiles of
-// 256 activation rows x BN weight rows over a persistent grid of at most one
-// CTA per SM, with K split over several CTAs where the tiles are fewer than
-// the SMs.
+// Launch plan of the two-accumulator prefill GEMM (power-of-two scales):
+// tiles of 256 activation rows (512 on CTA pairs) x BN weight rows over a
+// persistent grid of at most one CTA per SM (pair), with K split over several
+// CTAs where the tiles are fewer than the SMs (allow_split: the split-K
+// workspace may be used; single CTAs only).
+struct DualPlan {
+    int bn, rows, tiles_r, tiles_c, kst, tiles, splits, kps, items, per, grid;
+};
+DualPlan plan_dual(int64_t M, int64_t N, int64_t K, int sm_count, bool allow_split, bool pair, ScratchLimit lim) {
+    DualPlan q{};
+    q.bn = dual_width(M, N, sm_count, pair);
+    q.rows = pair ? 2 * dual::kRowsA : dual::kRowsA;
+    q.tiles_r = static_cast<int>((M + q.rows - 1) / q.rows);
+    q.tiles_c = static_cast<int>((N + q.bn - 1) / q.bn);
+    q.kst = static_cast<int>(K / kBK);
+    q.tiles = q.tiles_r * q.tiles_c;
+    const int units = pair ? sm_count / 2 : sm_count;
+    q.splits = allow_split && !pair ? dual_splits(q.tiles, q.kst, sm_count, q.bn, lim) : 1;
+    q.kps = (q.kst + q.splits - 1) / q.splits;
+    q.items = q.tiles * q.splits;
+    q.per = 8 * ((q.bn / 4 + q.splits - 1) / q.splits);
+    q.grid = (q.items < units ? q.items : units) * (pair ? 2 : 1);
+    return q;
+}
+
+// Launches the two-accumulator prefill GEMM on plan_dual's plan.
 // Ae/We: UE8M0 scale bytes in place of As/Ws (both given or both null).
 sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const float* Ws, void* D, int64_t M,
                        int64_t N, int64_t K, int blk_n, int blk_k, int sm_count, bool allow_split, bool pair,
                        ScratchLimit lim, cudaStream_t st, const uint8_t* Ae = nullptr, const uint8_t* We = nullptr) {
-    const int bn = dual_width(M, N, sm_count, pair);
-    const int rows = pair ? 2 * dual::kRowsA : dual::kRowsA;   // activation rows per tile
+    const DualPlan q = plan_dual(M, N, K, sm_count, allow_split, pair, lim);
+    const int bn = q.bn;
     dual::DualArgs a{};
     a.As = As;
     a.Ws = Ws;
@@ -376,15 +401,15 @@ sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const fl
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.ks = static_cast<int>(K / blk_k);
-    a.tiles_r = static_cast<int>((M + rows - 1) / rows);
-    a.tiles_c = static_cast<int>((N + bn - 1) / bn);
-    a.kst = static_cast<int>(K / kBK);
-    a.tiles = a.tiles_r * a.tiles_c;
+    a.tiles_r = q.tiles_r;
+    a.tiles_c = q.tiles_c;
+    a.kst = q.kst;
+    a.tiles = q.tiles;
     a.group_r = a.tiles_r < 16 ? a.tiles_r : 16;
-    a.splits = allow_split && !pair ? dual_splits(a.tiles, a.kst, sm_count, bn, lim) : 1;
-    a.kps = (a.kst + a.splits - 1) / a.splits;
-    a.items = a.tiles * a.splits;
-    a.per = 8 * ((bn / 4 + a.splits - 1) / a.splits);
+    a.splits = q.splits;
+    a.kps = q.kps;
+    a.items = q.items;
+    a.per = q.per;
     sgq_status rc = status_word(&a.status);
     if (rc != SGQ_OK) return rc;
     if (a.splits > 1) {
@@ -398,13 +423,9 @@ sgq_status launch_dual(const void* Aq, const float* As, const void* Wq, const fl
     if (make_tmap(&maps[0], Aq, M, K, dual::kRowsA) != SGQ_OK ||
         make_tmap(&maps[1], Wq, N, K, pair ? bn / 2 : bn) != SGQ_OK)
         return SGQ_ERR_CUDA;
-    if (pair) {
-        const int pairs = a.items < sm_count / 2 ? a.items : sm_count / 2;
-        return dual::dispatch(bn, dual::kPairs, e8, blk_n, blk_k, maps[0], maps[1], a, 2 * pairs, st);
-    }
-    const int grid = a.items < sm_count ? a.items : sm_count;
+    if (pair) return dual::dispatch(bn, dual::kPairs, e8, blk_n, blk_k, maps[0], maps[1], a, q.grid, st);
     return dual::dispatch(bn, a.splits > 1 ? dual::kSplitK : dual::kPlain, e8, blk_n, blk_k, maps[0], maps[1], a,
-                          grid, st);
+                          q.grid, st);
 }
 
 // Whether a GEMM with the power-of-two promise runs on the two-accumulator
@@ -692,6 +713,18 @@ sgq_status gemm_plan_query(int64_t M, int64_t N, int64_t K, int blk_k, int sm_co
     const int32_t v[8] = {p.swap ? 1 : 0, p.bn, p.splits, p.items, p.grid, p.alt ? 1 : 0, p.ck ? 1 : 0,
                           p.pair ? 1 : 0};
     for (int i = 0; i < 8; ++i) out[i] = v[i];
+    return SGQ_OK;
+}
+
+sgq_status gemm_plan_pow2_query(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int e8, int32_t* out) {
+    const gemm::Plan p = gemm::make_plan(M, N, K, blk_k, sm_count);
+    const int mode = gemm::dual_mode(M, N, K, blk_k, SGQ_GEMM_SCALES_POW2, p, sm_count, gemm::kWsLimit, e8 != 0);
+    for (int i = 0; i < 8; ++i) out[i] = 0;
+    out[0] = mode;
+    if (mode == 0) return SGQ_OK;
+    const gemm::DualPlan q = gemm::plan_dual(M, N, K, sm_count, mode == 2, mode == 3, gemm::kWsLimit);
+    const int32_t v[6] = {q.bn, q.splits, q.items, q.grid, q.tiles, q.kps};
+    for (int i = 0; i < 6; ++i) out[i + 1] = v[i];
     return SGQ_OK;
 }
 

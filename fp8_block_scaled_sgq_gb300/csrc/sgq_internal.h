@@ -54,6 +54,7 @@ sgq_status launch_fp8_scaled_mm(const void* Aq, const float* sa, int64_t sa_n, c
 // out[0..7] = swap-AB, BN, K splits, work items, grid, alternating issuers,
 // cluster split-K, CTA pairs.
 sgq_status gemm_plan_query(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out);
+sgq_status gemm_plan_pow2_query(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int e8, int32_t* out);
 // Bytes of device memory the library has allocated on the current device.
 uint64_t allocated_bytes();
 // The device status word of the current device (kernels atomicOr bits into

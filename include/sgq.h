@@ -361,6 +361,23 @@ uint64_t sgq_allocated_bytes(void);
  */
 sgq_status sgq_gemm_plan(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int32_t* out);
 
+/*
+ * The plan of the two-accumulator tiles that sgq_fp8_block_gemm_ex with
+ * SGQ_GEMM_SCALES_POW2 (e8 = 0), or sgq_fp8_block_gemm_ue8m0 (e8 = 1), would
+ * use on a device with `sm_count` SMs; host only (no device is touched), for
+ * tests and tools.  The kernel computes the same D = (Aq * As)(Wq * Ws)^T as
+ * sgq_fp8_block_gemm (sglang PR #42604, Modifications: fp8_gemm_nt with a
+ * (1, blk_n, blk_k) recipe).  out (host, 8 entries, caller-owned):
+ * [0] mode: 0 = these tiles are not used (sgq_gemm_plan's plan applies; byte
+ * scales are widened to fp32 first), 1 = one CTA per 256-row tile, 2 = K split
+ * over CTAs, 3 = CTA pairs on 512-row tiles; then, for modes 1-3: [1] tile
+ * width in weight rows (192 or 224), [2] K splits, [3] work items (tiles x
+ * splits), [4] grid in CTAs, [5] tiles, [6] K stages (of 128) per split,
+ * [7] 0.  SGQ_ERR_INVALID_ARG for out == NULL, M, N or K < 1, blk_k not 32 or
+ * 128, sm_count < 2, or e8 not 0 or 1.
+ */
+sgq_status sgq_gemm_plan_pow2(int64_t M, int64_t N, int64_t K, int blk_k, int sm_count, int e8, int32_t* out);
+
 /* Library ABI version (major * 100 + minor). */
 int sgq_version(void);
 

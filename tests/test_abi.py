@@ -36,7 +36,7 @@ def test_status_strings(lib):
                        (3, "SGQ_ERR_MISALIGNED"), (4, "SGQ_ERR_CUDA"), (5, "SGQ_ERR_TIMEOUT")]:
         assert sgq.status_string(code) == name
     assert sgq.status_string(99) == "SGQ_ERR_UNKNOWN"
-    assert sgq.sgq_version() == 103
+    assert sgq.sgq_version() == 104
 
 
 A = 0x10000      # fake, 16-byte aligned device addresses: never dereferenced

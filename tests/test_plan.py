@@ -107,3 +107,69 @@ def test_plan_rejects_bad_arguments():
     assert lib.sgq_gemm_plan(16, 7168, 2048, 64, 152, ptr) == binding.SGQ_ERR_INVALID_ARG
     assert lib.sgq_gemm_plan(16, 7168, 2048, 32, 0, ptr) == binding.SGQ_ERR_INVALID_ARG
     assert lib.sgq_gemm_plan(16, 7168, 2048, 32, 152, ptr) == 0
+
+
+# ------------------------------------------- two-accumulator tiles (power-of-two scales)
+
+def plan2(M, N, K, bk, e8=False, sms=SMS):
+    return sgq.sgq_gemm_plan_pow2(M, N, K, bk, sms, e8)
+
+
+def test_pow2_plan_widths_and_pairs():
+    """Tile widths by rounds over the grid: 4096 x 7168 x 7168 on CTA pairs
+    takes 192-wide tiles (304 tiles, exactly four rounds of 76 pairs, where
+    224 would make 256 tiles in 3.4 rounds); 4096 x 4096 x 7168 on bytes 224
+    (152 tiles, two rounds); 8192 x 24576 x 1536 single CTAs 224 wide."""
+    p = plan2(4096, 7168, 7168, 128, e8=True)
+    assert p == {"mode": 3, "bn": 192, "splits": 1, "items": 304, "grid": 152, "tiles": 304, "kps": 56}
+    assert plan2(4096, 7168, 7168, 128) == p                       # fp32 [*,128] scales: the same plan
+    p = plan2(4096, 4096, 7168, 32, e8=True)
+    assert (p["mode"], p["bn"], p["items"], p["grid"]) == (3, 224, 152, 152)
+    p = plan2(8192, 24576, 1536, 32, e8=True)
+    assert (p["mode"], p["bn"], p["items"], p["grid"]) == (1, 224, 3520, 152)
+
+
+def test_pow2_plan_modes():
+    """Single CTAs for fp32 [*,32] scales and for short K, K split over CTAs
+    at mid M with few tiles, and the 128-row kernel for decode-sized M."""
+    assert plan2(4096, 4096, 7168, 32)["mode"] == 1              # fp32 [*,32]: no pairs
+    assert plan2(8192, 24576, 1536, 128, e8=True)["mode"] == 1   # K < 4096
+    p = plan2(1024, 1536, 7168, 128)
+    assert p["mode"] == 2 and p["splits"] == 4 and p["items"] == p["tiles"] * 4
+    assert plan2(16, 7168, 2048, 32, e8=True)["mode"] == 0
+    assert plan2(64, 24576, 7168, 128)["mode"] == 0
+
+
+POW2_SHAPES = list(itertools.product([65, 700, 1024, 2100, 4096, 6000, 8192, 16384], [448, 1536, 3000, 7168, 24576],
+                                     [512, 1536, 4096, 5120, 7168], [32, 128], [False, True]))
+
+
+@pytest.mark.parametrize("M,N,K,bk,e8", POW2_SHAPES)
+def test_pow2_plan_invariants(M, N, K, bk, e8):
+    p = plan2(M, N, K, bk, e8)
+    if p["mode"] == 0:
+        return
+    rows = 512 if p["mode"] == 3 else 256
+    units = SMS // 2 if p["mode"] == 3 else SMS
+    kst = K // 128
+    assert p["bn"] in (192, 224)
+    assert p["tiles"] == math.ceil(M / rows) * math.ceil(N / p["bn"])
+    s, kps = p["splits"], p["kps"]
+    assert 1 <= s <= 16 and kps == math.ceil(kst / s) and (s - 1) * kps < kst   # every split non-empty
+    if p["mode"] == 2:
+        assert p["items"] == p["tiles"] * s <= units   # one item per CTA
+    else:
+        assert s == 1 and p["items"] == p["tiles"]
+    assert p["grid"] == min(p["items"], units) * (2 if p["mode"] == 3 else 1)
+
+
+def test_pow2_plan_rejects_bad_arguments():
+    lib = binding.load_library()
+    import ctypes
+    out = (ctypes.c_int32 * 8)()
+    ptr = ctypes.cast(out, ctypes.c_void_p)
+    assert lib.sgq_gemm_plan_pow2(4096, 7168, 7168, 128, 152, 0, None) == binding.SGQ_ERR_INVALID_ARG
+    assert lib.sgq_gemm_plan_pow2(4096, 7168, 7168, 64, 152, 0, ptr) == binding.SGQ_ERR_INVALID_ARG
+    assert lib.sgq_gemm_plan_pow2(4096, 7168, 7168, 128, 1, 0, ptr) == binding.SGQ_ERR_INVALID_ARG
+    assert lib.sgq_gemm_plan_pow2(4096, 7168, 7168, 128, 152, 2, ptr) == binding.SGQ_ERR_INVALID_ARG
+    assert lib.sgq_gemm_plan_pow2(4096, 7168, 7168, 128, 152, 1, ptr) == 0 and out[0] == 3
