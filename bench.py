@@ -15,8 +15,9 @@ the same steps through the public API with the activation copied in from
 pinned host memory and D read back to the host inside the timed region: each
 step replays one CUDA graph holding the host-to-device copy of the step's
 activations (one pinned buffer), the quantisation and GEMM calls of every linear
-and the device-to-host copy of the outputs, then waits for it on the host (the
-way a decode loop runs).  `e2e.eager_ms_per_step` is the
+(largest M first) and each linear's device-to-host copy, issued on a copy stream
+as soon as its GEMM is done, then waits for it on the host (the way a decode
+loop runs).  `e2e.eager_ms_per_step` is the
 same step issued call by call from Python.
 
 `--impl reference` times the CPU oracle (test infrastructure) on a bounded
@@ -494,20 +495,28 @@ def run_ours(args, ws_, rank, local):
     del graph, fused_graph, case_graphs
 
     # end to end through the public API: H2D of x, quant + GEMM, D2H of D, every
-    # step; the step's activations (and outputs) sit in one buffer each, so one
-    # copy per direction moves them
+    # step.  The step's activations sit in one buffer (one H2D copy); each
+    # linear's output goes back on a copy stream as soon as its GEMM is done,
+    # largest first, so that the copies overlap the remaining linears.
+    order = sorted(range(len(per)), key=lambda j: -per[j][0].M)
     x_sizes = [x.numel() for _, x, _, _, _ in per]
     d_sizes = [d.numel() for *_, d in per]
     hx = torch.cat([x.reshape(-1).cpu() for _, x, _, _, _ in per]).pin_memory()
     hd = torch.empty(sum(d_sizes), dtype=torch.bfloat16).pin_memory()
     dx = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=device)
     dd = torch.empty(sum(d_sizes), dtype=torch.bfloat16, device=device)
-    per_e2e, ox, od = [], 0, 0
+    per_e2e, hd_parts, ox, od = [], [], 0, 0
     for (c, x, xq, xs, d), nx, nd in zip(per, x_sizes, d_sizes):
         per_e2e.append((c, dx[ox:ox + nx].view(x.shape), xq, xs, dd[od:od + nd].view(d.shape)))
+        hd_parts.append(hd[od:od + nd].view(d.shape))
         ox, od = ox + nx, od + nd
-    per = per_e2e
-    hx, hd = (hx, dx), (hd, dd)
+    per = [per_e2e[j] for j in order]
+    hd_parts = [hd_parts[j] for j in order]
+    e2e_wsets = wsets
+    wsets = lambda i: [e2e_wsets(i)[j] for j in order]   # noqa: E731
+    copy_stream = torch.cuda.Stream()
+    events = [torch.cuda.Event() for _ in range(len(per) + 1)]
+    hx, hd = (hx, dx), (hd_parts, copy_stream, events)
     for i in range(args.warmup):
         _e2e_step(sgq, per, wsets(i), hx, hd, stream)   # e2e warm-up
         stream.synchronize()
@@ -629,18 +638,26 @@ def run_ours(args, ws_, rank, local):
 
 
 def _e2e_step(sgq, per, wsets, hx, hd, stream):
-    """One host-to-device copy of the step's activations, quantisation + GEMM
-    for every linear, one device-to-host copy of the outputs, on `stream` (the
-    caller waits).  hx / hd: (pinned host buffer, device buffer) pairs; the
-    device views of `per` lie in them."""
+    """One host-to-device copy of the step's activations, then quantisation +
+    GEMM for every linear on `stream`, each linear's output copied to the host
+    on a copy stream once its GEMM is done; the copy stream joins `stream` at
+    the end (the caller waits on `stream`).  hx: (pinned host buffer, device
+    buffer), the device views of `per` lie in it; hd: (pinned host views of
+    each linear's output, in `per`'s order, copy stream, one event per linear
+    and one for the join)."""
+    hd_parts, copy_stream, events = hd
     with torch.cuda.stream(stream):
-        hd_host, hd_dev = hd
         hx_host, hx_dev = hx
         hx_dev.copy_(hx_host, non_blocking=True)
-        for (c, x, xq, xs, d), (wq, ws) in zip(per, wsets):
+        for (c, x, xq, xs, d), (wq, ws), h, done in zip(per, wsets, hd_parts, events):
             sgq.sgq_quant_token_group(x, c.M, c.K, c.group, c.ue8m0, xq, xs, stream.cuda_stream)
             sgq.sgq_fp8_block_gemm(xq, xs, wq, ws, d, c.M, c.N, c.K, c.blk_n, c.blk_k, stream.cuda_stream)
-        hd_host.copy_(hd_dev, non_blocking=True)
+            done.record(stream)
+            copy_stream.wait_event(done)
+            with torch.cuda.stream(copy_stream):
+                h.copy_(d, non_blocking=True)
+        events[-1].record(copy_stream)
+        stream.wait_event(events[-1])
 
 
 # ----------------------------------------------------------------- oracle timing
