@@ -22,8 +22,8 @@
  *    Arguments are checked on the host before anything is launched.
  *  - E4M3 is the OCP FP8 "E4M3FN" format (largest finite 448, no infinities).
  *    Scales are fp32.  A "UE8M0" scale is an fp32 value that is an exact
- *    power of two; it is converted to its 8-bit exponent byte only inside the
- *    GEMM.
+ *    power of two; the *_ue8m0 entry points below take or produce it as its
+ *    8-bit biased exponent byte instead (2^(byte - 127); 255 is NaN).
  *  - The library allocates device memory only once per device, on first use
  *    of a GEMM shape that needs a split-K workspace (and a 4-byte status
  *    word).  That first use must not happen inside a CUDA stream capture;
@@ -32,8 +32,9 @@
  *    per device and shared by every GEMM call on it.  GEMMs that use split-K
  *    must therefore not overlap on the GPU: calls on one stream are safe;
  *    calls on different streams, or from several host threads, must be
- *    ordered (events, or one stream per device).  sgq_gemm_plan tells which
- *    shapes split K (out[2] > 1).
+ *    ordered (events, or one stream per device).  sgq_gemm_plan (and, for
+ *    the power-of-two promise and UE8M0 bytes, sgq_gemm_plan_pow2) tells
+ *    which shapes split K (out[2] > 1).
  */
 #ifndef SGQ_H_
 #define SGQ_H_
