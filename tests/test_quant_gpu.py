@@ -97,3 +97,29 @@ def test_quant_weight_block(N, K, bn, bk, ue):
     torch.cuda.synchronize()
     rq, rs = oracle.quant_weight_block(w, bn, bk, ue)
     assert_same(wq.cpu().numpy(), ws.cpu().numpy(), rq, rs, f"weights N={N} K={K} [{bn},{bk}] ue={ue}")
+
+
+@pytest.mark.parametrize("M,K", [(147, 7168), (1639, 640), (2049, 1536), (3, 384)])
+@pytest.mark.parametrize("ue8m0", [False, True])
+@pytest.mark.parametrize("group", [32, 128])
+def test_both_access_widths(M, K, ue8m0, group):
+    """The quantiser runs with 32-byte accesses when x has at least 2^20
+    elements and starts on a 32-byte boundary, and with 16-byte ones otherwise
+    (smaller x, or another alignment): both give the oracle's codes and scale
+    bits (ragged last warp chunk included: M x K / 16 not a multiple of 32),
+    fp32 scales and UE8M0 bytes."""
+    x = synth.activation(M, K, seed=M + K)
+    rq, rs = oracle.quant_token_group(x, group, ue8m0)
+    buf = torch.empty(M * K + 16, dtype=torch.bfloat16, device="cuda")
+    for off in (0, 8):   # elements: byte offsets 0 (32-byte aligned) and 16
+        xd = buf[off:off + M * K].view(M, K)
+        xd.copy_(x.cuda())
+        assert (xd.data_ptr() % 32 == 0) == (off == 0)
+        xq, xs = sgq.quant_token_group(xd, group, ue8m0)
+        torch.cuda.synchronize()
+        assert sgq.sgq_device_status() == 0
+        assert_same(xq.cpu().numpy(), xs.cpu().numpy(), rq, rs, f"M={M} K={K} group={group} offset={off}")
+        if ue8m0:
+            xq8, xe = sgq.quant_token_group_ue8m0(xd, group)
+            assert np.array_equal(xq8.cpu().numpy(), rq)
+            assert np.array_equal(xe.cpu().numpy(), oracle.ue8m0_bytes(rs))
