@@ -27,8 +27,7 @@ def test_reference_arm_json_line():
                        cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     d = _last_json(r.stdout)
-    base = json.load(open(os.path.join(ROOT, "BASELINE.json")))
-    assert d["impl"] == "reference" and d["metric"] == base["metric"]
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
     assert d["value"] > 0 and d["unit"] in ("GB/s", "TFLOP/s") and d["higher_is_better"] is True
     assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] >= 3
     assert d["config"]["workload"] == "decode_block32" and d["dtype"] == "f64"
