@@ -179,3 +179,38 @@ def test_product_path_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "sgq_oracle" not in src and "sgqo_" not in src, f
+
+
+def test_ue8m0_entry_validation(lib):
+    """The UE8M0-byte entry points check their arguments on the host before
+    anything is launched (fake, never dereferenced addresses)."""
+    INV, MIS, OK = binding.SGQ_ERR_INVALID_ARG, binding.SGQ_ERR_MISALIGNED, binding.SGQ_OK
+    lib = binding.load_library()
+    qe = lib.sgq_quant_token_group_ue8m0
+    assert qe(A, 4, 256, 64, B, C, S) == INV            # group not 32/128
+    assert qe(A, 4, 96, 128, B, C, S) == INV            # K % group
+    assert qe(A, -1, 256, 128, B, C, S) == INV          # M < 0
+    assert qe(None, 4, 256, 128, B, C, S) == INV        # null
+    assert qe(A, 4, 256, 128, B, None, S) == INV
+    assert qe(A, 4, 256, 32, B, C + 4, S) == MIS        # byte scales 16-byte aligned too
+    assert qe(A + 8, 4, 256, 32, B, C, S) == MIS
+    assert qe(A, 0, 256, 128, None, None, S) == OK      # M == 0: no-op
+    se = lib.sgq_scales_to_ue8m0
+    assert se(A, -1, B, S) == INV
+    assert se(None, 16, B, S) == INV
+    assert se(A, 16, None, S) == INV
+    assert se(None, 0, None, S) == OK                   # n == 0: no-op
+    ge = lib.sgq_fp8_block_gemm_ue8m0
+    args = lambda **k: [k.get("Aq", A), k.get("Ae", B), k.get("Wq", C), k.get("We", D), k.get("D", E),
+                        k.get("M", 16), k.get("N", 256), k.get("K", 512), k.get("bn", 128),
+                        k.get("bk", 128), k.get("flags", 0), S]
+    assert ge(*args(bn=64)) == INV
+    assert ge(*args(K=96)) == INV                # K % blk_k
+    assert ge(*args(N=260)) == INV               # N % 8
+    assert ge(*args(flags=32)) == INV            # unknown flag
+    assert ge(*args(flags=6)) == INV             # both issue modes at once
+    assert ge(*args(M=1 << 31)) == INV
+    assert ge(*args(We=None)) == INV
+    assert ge(*args(Ae=B + 4)) == MIS
+    assert ge(*args(D=E + 8)) == MIS
+    assert ge(*args(M=0, Aq=None, Ae=None, D=None)) == OK
